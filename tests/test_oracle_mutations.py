@@ -1,0 +1,115 @@
+"""The pins must reject plausible mistakes in the oracle.
+
+Each case copies the oracle's C source, plants one mistake by a textual
+substitution (a wrong table entry, swapped nibble order, wrong block size, a
+sign error, a dropped term, a transposed operand, a slot mix-up, ...),
+compiles the broken copy on the CPU and runs the pin checks against it
+through ``oracle.using_library``.  At least one pin has to fail for every
+mutation; the unmodified source has to pass them all.
+"""
+import os
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
+
+MUTATIONS = {
+    "e2m1_table_entry": ("{0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0}", "{0.0, 0.5, 1.0, 1.5, 2.0, 2.5, 4.0, 6.0}"),
+    "e2m1_sign_bit": ("return (code & 8u) ? -v : v;", "return (code & 4u) ? -v : v;"),
+    "nibble_order": ("unsigned code = (k & 1) ? (byte >> 4) : (byte & 0xF);\n    double s = moe_oracle_scale",
+                     "unsigned code = (k & 1) ? (byte & 0xF) : (byte >> 4);\n    double s = moe_oracle_scale"),
+    "nv_block_size": ("return fmt == ORACLE_MXFP4 ? 32 : 16;", "return fmt == ORACLE_MXFP4 ? 32 : 32;"),
+    "ue8m0_bias": ("return ldexp(1.0, (int)b - 127);", "return ldexp(1.0, (int)b - 128);"),
+    "e4m3_bias": ("else v = ldexp(1.0 + (double)m / 8.0, e - 7);", "else v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    "e4m3_subnormal": ("if (e == 0) v = ldexp((double)m / 8.0, -6);", "if (e == 0) v = ldexp((double)m / 8.0, -7);"),
+    "silu_sign": ("return v / (1.0 + exp(-v));", "return v / (1.0 + exp(v));"),
+    "dropped_up": ("h[n] = silu(gate) * up;", "h[n] = silu(gate);"),
+    "gate_up_swapped": ("h[n] = silu(gate) * up;", "h[n] = silu(up) * gate;"),
+    "up_rows_offset": ("up += x[k] * weight_at(nib, sc, H, fmt, gu, I + n, k);",
+                       "up += x[k] * weight_at(nib, sc, H, fmt, gu, n, k);"),
+    "nv_global_swapped": ("double gg = fmt == ORACLE_NVFP4 ? (double)g13[2 * e + 0] : 1.0;\n    double gu = fmt == ORACLE_NVFP4 ? (double)g13[2 * e + 1] : 1.0;\n    for (int n = 0; n < I; ++n) {\n        double gate = 0.0",
+                          "double gg = fmt == ORACLE_NVFP4 ? (double)g13[2 * e + 1] : 1.0;\n    double gu = fmt == ORACLE_NVFP4 ? (double)g13[2 * e + 0] : 1.0;\n    for (int n = 0; n < I; ++n) {\n        double gate = 0.0"),
+    "down_global_dropped": ("double gd = fmt == ORACLE_NVFP4 ? (double)g2[e] : 1.0;\n    for (int m = 0; m < H; ++m) {",
+                            "double gd = 1.0;\n    for (int m = 0; m < H; ++m) {"),
+    "router_weight_ignored": ("double w = (double)tw[j];", "double w = 1.0;"),
+    "router_weight_wrong_slot": ("double w = (double)tw[j];", "double w = (double)tw[0];"),
+    "invalid_upper_bound": ("if (e < 0 || e >= E) continue; /* invalid route", "if (e < 0 || e > E) continue; /* invalid route"),
+    "accumulate_instead_of_overwrite": ("for (int m = 0; m < H; ++m) out[m] = 0.0;", ";"),
+    "fc2_index_transposed": ("for (int n = 0; n < I; ++n) acc += weight_at(nib, sc, I, fmt, gd, m, n) * h[n];",
+                             "for (int n = 0; n < I; ++n) acc += weight_at(nib, sc, I, fmt, gd, m, (n + 1) % I) * h[n];"),
+    "quant_global_rule": ("volatile float six448 = 6.0f * 448.0f;", "volatile float six448 = 6.0f * 256.0f;"),
+    "quant_tie_rule": ("if (d < bestd || (d == bestd && (c & 1) == 0)) {\n            bestd = d;\n            best = c;\n        }\n    }\n    if (best != 0",
+                       "if (d <= bestd) {\n            bestd = d;\n            best = c;\n        }\n    }\n    if (best != 0"),
+    "route_order": ("for (int t = 0; t < M; ++t)\n            for (int j = 0; j < top_k; ++j)\n                if (topk_ids[(size_t)t * top_k + j] == e) perm[r++] = t * top_k + j;",
+                    "for (int j = 0; j < top_k; ++j)\n            for (int t = 0; t < M; ++t)\n                if (topk_ids[(size_t)t * top_k + j] == e) perm[r++] = t * top_k + j;"),
+}
+
+
+def _run_pins():
+    """Run the pin checks; return the names of those that fail."""
+    failures = []
+    checks = [
+        ("e2m1", pins.test_e2m1_all_codes_closed_form),
+        ("ue8m0", pins.test_ue8m0_all_codes),
+        ("e4m3", pins.test_e4m3_all_codes_match_library),
+        ("e4m3_round", pins.test_e4m3_rounding_matches_library),
+        ("e2m1_round", pins.test_e2m1_rounding_golden),
+        ("dequant_mx", lambda: pins.test_dequant_structure(0)),
+        ("dequant_nv", lambda: pins.test_dequant_structure(1)),
+        ("quant_rules", pins.test_quant_row_global_and_scale_rules),
+        ("quant_nearest", pins.test_quant_row_codes_are_nearest),
+        ("route", pins.test_route_is_stable_counting_sort),
+        ("top1_mx", lambda: pins.test_top1_is_gated_mlp(0)),
+        ("top1_nv", lambda: pins.test_top1_is_gated_mlp(1)),
+    ]
+    for case in pins._golden_cases():
+        checks.append(("golden_" + case["name"], lambda c=case: pins.test_hand_worked_layers(c)))
+    checks.append(("brute_mx", lambda: _brute_once(0)))
+    checks.append(("brute_nv", lambda: _brute_once(1)))
+    for name, fn in checks:
+        try:
+            fn()
+        except (AssertionError, ValueError):
+            failures.append(name)
+    return failures
+
+
+def _brute_once(fmt):
+    E, H, I, M, k = 3, 32, 32, 2, 3
+    w = pins._tiny_weights(E, H, I, fmt, seed=99)
+    x = pins.gen.draw_activations(M, H, seed=98)
+    ids = np.array([[0, 2, -1], [1, 1, 3]], np.int32)
+    tw = np.array([[0.3, 0.6, 0.1], [0.2, 0.5, 0.3]], np.float32)
+    got = oracle.forward(x, w, ids, tw, E, H, I, k, fmt)
+    want = pins._np_layer(x.to(torch.float64).numpy(), w, ids, tw, E, H, I, fmt)
+    np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-12 * np.abs(want).max())
+
+
+def _build_variant(tmp_path, name, src_text):
+    c = tmp_path / f"{name}.c"
+    so = tmp_path / f"lib{name}.so"
+    c.write_text(src_text)
+    subprocess.run(["gcc", "-std=c99", "-O1", "-fPIC", "-shared", "-fno-fast-math", "-ffp-contract=off",
+                    "-o", str(so), str(c), "-lm"], check=True)
+    return str(so)
+
+
+def test_unmodified_oracle_passes_all_pins():
+    assert _run_pins() == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_reject_mutation(tmp_path, name):
+    src = open(SRC).read()
+    old, new = MUTATIONS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique/present"
+    so = _build_variant(tmp_path, name, src.replace(old, new))
+    with oracle.using_library(so):
+        failed = _run_pins()
+    assert failed, f"no pin caught mutation {name}"

@@ -1,0 +1,408 @@
+"""Pins that tie the FP64 oracle to things fixed independently of it.
+
+Each test checks the oracle against something other than itself: closed
+forms from the formats' bit definitions, a library routine (torch's
+float8_e4m3fn conversion), hand-worked examples (tests/golden), a NumPy
+brute force written separately below, and invariants of the layer's
+definition.  A plausible mistake in the oracle (wrong table entry, nibble
+order, block size, sign, dropped term, transposed operand, slot mix-up) makes
+at least one of them fail; ``test_oracle_mutations.py`` checks exactly that by
+building deliberately broken copies of the oracle.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workload import gen
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- formats
+def _e2m1_from_bits(c: int) -> float:
+    """E2M1 from its bit definition: sign | 2-bit exponent (bias 1) | 1-bit mantissa."""
+    s = -1.0 if c & 8 else 1.0
+    e = (c >> 1) & 3
+    m = c & 1
+    if e == 0:
+        return s * m * 0.5  # subnormal: 0.m * 2^(1-bias)
+    return s * (1.0 + m / 2.0) * 2.0 ** (e - 1)
+
+
+def test_e2m1_all_codes_closed_form():
+    vals = [oracle.e2m1(c) for c in range(16)]
+    for c in range(16):
+        assert vals[c] == _e2m1_from_bits(c)
+    assert sorted({abs(v) for v in vals}) == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_ue8m0_all_codes():
+    for b in range(255):
+        assert oracle.ue8m0(b) == math.ldexp(1.0, b - 127)
+    assert math.isnan(oracle.ue8m0(255))
+
+
+def test_e4m3_all_codes_match_library():
+    lib = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    for b in range(256):
+        o = oracle.e4m3(b)
+        ref = float(lib[b])
+        if math.isnan(ref):
+            assert math.isnan(o), b
+        else:
+            assert o == ref and math.copysign(1.0, o) == math.copysign(1.0, ref), b
+
+
+def test_e4m3_rounding_matches_library():
+    rng = np.random.default_rng(0)
+    vals = np.concatenate([
+        rng.uniform(0, 448, 4000), np.exp(rng.uniform(math.log(2.0 ** -12), math.log(448), 4000)),
+        [0.0, 2.0 ** -10, 2.0 ** -9, 1.5 * 2.0 ** -9, 2.5 * 2.0 ** -9, 0.5 * 2.0 ** -9, 0.9 * 2.0 ** -9,
+         448.0, 447.0, 440.0, 416.0, 432.0, 1.0625, 1.1875],
+    ]).astype(np.float32)
+    ref = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    for v, r in zip(vals, ref):
+        assert oracle.e4m3_round(float(v)) == int(r), float(v)
+    # saturation above the largest finite value
+    assert oracle.e4m3_round(460.0) == 0x7E and oracle.e4m3_round(1e30) == 0x7E
+
+
+def test_e2m1_rounding_golden():
+    with open(os.path.join(GOLDEN, "e2m1_rounding_ties.json")) as f:
+        cases = json.load(f)["cases"]
+    for v, code in cases:
+        assert oracle.e2m1_round(float(np.float32(v))) == code, v
+
+
+def test_e2m1_rounding_is_nearest():
+    """Brute force: the chosen code is a nearest grid point for many values."""
+    grid = np.array([_e2m1_from_bits(c) for c in range(8)])
+    for v in np.linspace(-7, 7, 2801, dtype=np.float32):
+        c = oracle.e2m1_round(float(v))
+        val = _e2m1_from_bits(c)
+        d = abs(val - float(v))
+        assert d <= np.min(np.abs(grid - abs(float(v)))) + 1e-12
+
+
+# ---------------------------------------------------------------- dequantisation
+@pytest.mark.parametrize("fmt", [gen.MXFP4, gen.NVFP4])
+def test_dequant_structure(fmt):
+    B = gen.BLOCK[fmt]
+    K = 4 * B
+    # row 0: codes 0..15 repeating, unit scale -> the E2M1 table, low nibble = even k
+    codes = np.arange(K) % 16
+    nib = (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)[None, :]
+    unit = 127 if fmt == gen.MXFP4 else 0x38
+    sc = np.full((1, K // B), unit, np.uint8)
+    d = oracle.dequant(nib, sc, K, fmt)[0]
+    assert [d[k] for k in range(K)] == [_e2m1_from_bits(int(c)) for c in codes]
+    # a scale change applies to exactly its own block of B elements
+    sc2 = sc.copy()
+    sc2[0, 1] = 128 if fmt == gen.MXFP4 else 0x40  # 2.0 in both encodings
+    d2 = oracle.dequant(nib, sc2, K, fmt)[0]
+    ratio = np.where(d != 0, d2 / np.where(d != 0, d, 1), 1.0)
+    assert np.all(ratio[:B] == 1.0) and np.all(ratio[B:2 * B][d[B:2 * B] != 0] == 2.0) and np.all(ratio[2 * B:] == 1.0)
+    # NVFP4 multiplier scales everything
+    if fmt == gen.NVFP4:
+        d3 = oracle.dequant(nib, sc, K, fmt, g=0.375)[0]
+        assert np.array_equal(d3, d * 0.375)
+
+
+def test_dequant_rows_are_independent():
+    rng = np.random.default_rng(1)
+    nib = rng.integers(0, 256, (3, 32), dtype=np.uint8)
+    sc = rng.integers(110, 140, (3, 2), dtype=np.uint8)
+    full = oracle.dequant(nib, sc, 64, gen.MXFP4)
+    for r in range(3):
+        assert np.array_equal(full[r], oracle.dequant(nib[r:r + 1], sc[r:r + 1], 64, gen.MXFP4)[0])
+
+
+# ---------------------------------------------------------------- hand-worked layers
+def _golden_weights(case):
+    fmt, E, H, I = case["fmt"], case["E"], case["H"], case["I"]
+    B = 32 if fmt == 0 else 16
+
+    def fill_nib(n):
+        return np.uint8(n | (n << 4))
+
+    w13 = np.zeros((E, 2 * I, H // 2), np.uint8)
+    w13[:, :I] = fill_nib(case["gate_nibble"])
+    w13[:, I:] = fill_nib(case["up_nibble"])
+    s13 = np.zeros((E, 2 * I, H // B), np.uint8)
+    s13[:, :I] = case["gate_scale_byte"]
+    s13[:, I:] = case["up_scale_byte"]
+    w2 = np.full((E, H, I // 2), fill_nib(case["down_nibble"]), np.uint8)
+    s2 = np.full((E, H, I // B), case["down_scale_byte"], np.uint8)
+    if "expert_down_scale_bytes" in case:
+        for e, b in enumerate(case["expert_down_scale_bytes"]):
+            s2[e] = b
+    w = dict(w13=w13, s13=s13, w2=w2, s2=s2)
+    if fmt == 1:
+        w["g13"] = np.array(case.get("g13", [[1.0, 1.0]] * E), np.float32)
+        w["g2"] = np.array(case.get("g2", [1.0] * E), np.float32)
+    return w
+
+
+def _golden_cases():
+    with open(os.path.join(GOLDEN, "hand_worked_layers.json")) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _golden_cases(), ids=lambda c: c["name"])
+def test_hand_worked_layers(case):
+    E, H, I, k, M, fmt = case["E"], case["H"], case["I"], case["top_k"], case["M"], case["fmt"]
+    x = torch.full((M, H), case["x_fill"], dtype=torch.bfloat16)
+    ids = np.array(case["ids"], np.int32)
+    tw = np.array(case["weights"], np.float32)
+    out = oracle.forward(x, _golden_weights(case), ids, tw, E, H, I, k, fmt)
+    if "expected_closed_form" in case:
+        exp_t = [eval(case["expected_closed_form"], {"exp": math.exp})]
+    else:
+        exp_t = [eval(s, {"exp": math.exp}) for s in case["expected_closed_form_per_token"]]
+    for t in range(M):
+        np.testing.assert_allclose(out[t], np.full(H, exp_t[t]), rtol=1e-12, atol=0)
+
+
+# ---------------------------------------------------------------- NumPy brute force
+_TABLE = np.array([_e2m1_from_bits(c) for c in range(16)])
+
+
+def _np_dequant(nib, sc, K, fmt, g=1.0):
+    """Independent NumPy dequantisation: [..., K/2] bytes -> [..., K]."""
+    B = 32 if fmt == 0 else 16
+    codes = np.stack([nib & 15, nib >> 4], axis=-1).reshape(*nib.shape[:-1], K)
+    if fmt == 0:
+        sv = np.where(sc == 255, np.nan, np.ldexp(1.0, sc.astype(np.int64) - 127))
+    else:
+        sv = torch.from_numpy(np.ascontiguousarray(sc)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return _TABLE[codes] * np.repeat(sv, B, axis=-1) * g
+
+
+def _np_layer(x, w, ids, tw, E, H, I, fmt):
+    """Gated-MLP mixture: einsum over every token and slot."""
+    M, k = ids.shape
+    out = np.zeros((M, H))
+    for e in range(E):
+        g13 = w["g13"][e] if fmt == 1 else (1.0, 1.0)
+        g2 = w["g2"][e] if fmt == 1 else 1.0
+        Wg = _np_dequant(w["w13"][e, :I], w["s13"][e, :I], H, fmt, float(g13[0]))
+        Wu = _np_dequant(w["w13"][e, I:], w["s13"][e, I:], H, fmt, float(g13[1]))
+        Wd = _np_dequant(w["w2"][e], w["s2"][e], I, fmt, float(g2))
+        G = np.einsum("mk,nk->mn", x, Wg)
+        U = np.einsum("mk,nk->mn", x, Wu)
+        Hh = G / (1.0 + np.exp(-G)) * U
+        Y = np.einsum("mn,hn->mh", Hh, Wd)
+        coef = np.where(ids == e, tw.astype(np.float64), 0.0).sum(-1)
+        out += coef[:, None] * Y
+    return out
+
+
+def _tiny_weights(E, H, I, fmt, seed):
+    w = gen.make_expert_weights(E, H, I, fmt, seed)
+    return {k: v.numpy() for k, v in w.items()}
+
+
+@pytest.mark.parametrize("fmt", [gen.MXFP4, gen.NVFP4])
+@pytest.mark.parametrize("H", [32, 64])
+def test_brute_force_all_routings(fmt, H):
+    E, I, M, k = 3, 32, 2, 2
+    w = _tiny_weights(E, H, I, fmt, seed=7 + H + fmt)
+    x = gen.draw_activations(M, H, seed=3)
+    xf = x.to(torch.float64).numpy()
+    ids_all = list(itertools.product(list(range(-1, E + 1)), repeat=k))
+    rng = np.random.default_rng(5)
+    for combo_t0 in ids_all:
+        combo_t1 = ids_all[rng.integers(len(ids_all))]
+        ids = np.array([combo_t0, combo_t1], np.int32)
+        tw = rng.uniform(0.1, 1.0, (M, k)).astype(np.float32)
+        got = oracle.forward(x, w, ids, tw, E, H, I, k, fmt)
+        want = _np_layer(xf, w, ids, tw, E, H, I, fmt)
+        np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-12 * (np.abs(want).max() + 1e-300))
+
+
+@pytest.mark.parametrize("fmt", [gen.MXFP4, gen.NVFP4])
+def test_top1_is_gated_mlp(fmt):
+    """top_k = 1 with weight 1 equals a plain gated MLP (NumPy float64 matmuls)."""
+    E, H, I, M = 4, 64, 64, 3
+    w = _tiny_weights(E, H, I, fmt, seed=11)
+    x = gen.draw_activations(M, H, seed=12)
+    xf = x.to(torch.float64).numpy()
+    for e in range(E):
+        ids = np.full((M, 1), e, np.int32)
+        tw = np.ones((M, 1), np.float32)
+        got = oracle.forward(x, w, ids, tw, E, H, I, 1, fmt)
+        g13 = w["g13"][e] if fmt == 1 else (1.0, 1.0)
+        g2 = w["g2"][e] if fmt == 1 else 1.0
+        Wg = oracle.dequant(w["w13"][e, :I], w["s13"][e, :I], H, fmt, float(g13[0]))
+        Wu = oracle.dequant(w["w13"][e, I:], w["s13"][e, I:], H, fmt, float(g13[1]))
+        Wd = oracle.dequant(w["w2"][e], w["s2"][e], I, fmt, float(g2))
+        a = xf @ Wg.T
+        b = xf @ Wu.T
+        want = (a / (1 + np.exp(-a)) * b) @ Wd.T
+        np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-13)
+
+
+# ---------------------------------------------------------------- invariants
+@pytest.fixture(scope="module")
+def small_case():
+    E, H, I, M, k = 6, 64, 32, 3, 4
+    w = _tiny_weights(E, H, I, gen.MXFP4, seed=21)
+    x = gen.draw_activations(M, H, seed=22)
+    ids = np.array([[0, 3, 5, 1], [2, 2, 4, 0], [5, 1, 3, 2]], np.int32)
+    tw = np.random.default_rng(23).uniform(0.05, 1.0, (M, k)).astype(np.float32)
+    return E, H, I, M, k, w, x, ids, tw
+
+
+def test_linear_in_router_weights(small_case):
+    E, H, I, M, k, w, x, ids, tw = small_case
+    a = oracle.forward(x, w, ids, tw, E, H, I, k, 0)
+    b = oracle.forward(x, w, ids, tw * 0.5, E, H, I, k, 0)
+    np.testing.assert_allclose(b, 0.5 * a, rtol=1e-13, atol=1e-15)
+
+
+def test_slot_permutation_invariant(small_case):
+    E, H, I, M, k, w, x, ids, tw = small_case
+    a = oracle.forward(x, w, ids, tw, E, H, I, k, 0)
+    p = [2, 0, 3, 1]
+    b = oracle.forward(x, w, ids[:, p].copy(), tw[:, p].copy(), E, H, I, k, 0)
+    np.testing.assert_allclose(b, a, rtol=1e-12, atol=1e-14)
+
+
+def test_invalid_slot_equals_removed(small_case):
+    E, H, I, M, k, w, x, ids, tw = small_case
+    ids_bad = ids.copy()
+    ids_bad[:, 1] = [-1, E, -7]
+    tw_bad = tw.copy()
+    tw_bad[:, 1] = [5.0, np.nan, 3.0]
+    a = oracle.forward(x, w, ids_bad, tw_bad, E, H, I, k, 0)
+    keep = [0, 2, 3]
+    b = oracle.forward(x, w, ids[:, keep].copy(), tw[:, keep].copy(), E, H, I, 3, 0)
+    np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-15)
+
+
+def test_all_invalid_is_zero(small_case):
+    E, H, I, M, k, w, x, ids, tw = small_case
+    out = oracle.forward(x, w, np.full_like(ids, -1), tw, E, H, I, k, 0)
+    assert np.all(out == 0.0)
+
+
+def test_duplicate_slots_sum(small_case):
+    E, H, I, M, k, w, x, ids, tw = small_case
+    one = oracle.forward(x, w, ids[:, :1].copy(), tw[:, :1].copy(), E, H, I, 1, 0)
+    dup = oracle.forward(x, w, np.repeat(ids[:, :1], 2, 1), np.repeat(tw[:, :1], 2, 1), E, H, I, 2, 0)
+    np.testing.assert_allclose(dup, 2 * one, rtol=1e-13, atol=1e-15)
+
+
+def test_token_subset_matches_full(small_case):
+    E, H, I, M, k, w, x, ids, tw = small_case
+    full = oracle.forward(x, w, ids, tw, E, H, I, k, 0)
+    sub = oracle.forward(x, w, ids, tw, E, H, I, k, 0, tokens=[2, 0])
+    assert np.array_equal(sub, full[[2, 0]])
+
+
+def test_fc1_stage_matches_layer_definition(small_case):
+    E, H, I, M, k, w, x, ids, tw = small_case
+    gate, up = oracle.fc1(x[0], w, 3, H, I, 0)
+    Wg = _np_dequant(w["w13"][3, :I], w["s13"][3, :I], H, 0)
+    Wu = _np_dequant(w["w13"][3, I:], w["s13"][3, I:], H, 0)
+    xf = x[0].to(torch.float64).numpy()
+    np.testing.assert_allclose(gate, Wg @ xf, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(up, Wu @ xf, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- prefill quantiser
+def _nv_grid_value(q, s, G, K):
+    codes = np.stack([q & 15, q >> 4], -1).reshape(K)
+    sv = torch.from_numpy(s.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return _TABLE[codes] * np.repeat(sv, 16) * G
+
+
+def test_quant_row_zero():
+    q, s, G = oracle.quant_nvfp4_row(np.zeros(64, np.float32))
+    assert G == 1.0 and not q.any() and not s.any()
+
+
+def test_quant_row_global_and_scale_rules():
+    rng = np.random.default_rng(31)
+    a = rng.standard_normal(256).astype(np.float32) * 3
+    q, s, G = oracle.quant_nvfp4_row(a)
+    amax = np.float32(np.abs(a).max())
+    assert np.float32(G) == np.float32(amax / np.float32(2688.0))
+    six_g = np.float32(6.0) * np.float32(G)
+    for b in range(16):
+        bmax = np.float32(np.abs(a[b * 16:(b + 1) * 16]).max())
+        want = torch.tensor([float(np.float32(bmax / six_g))], dtype=torch.float32).clamp(max=448)
+        assert int(want.to(torch.float8_e4m3fn).view(torch.uint8)) == int(s[b])
+
+
+def test_quant_row_codes_are_nearest():
+    """Every element's code is a nearest grid point of a/(s*G) (FP32 quotient), ties to even."""
+    rng = np.random.default_rng(32)
+    for trial in range(20):
+        a = (rng.standard_normal(128) * rng.uniform(1e-3, 1e3)).astype(np.float32)
+        if trial % 5 == 0:
+            a[rng.integers(0, 128, 20)] = 0.0
+        q, s, G = oracle.quant_nvfp4_row(a)
+        codes = np.stack([q & 15, q >> 4], -1).reshape(128)
+        sv = torch.from_numpy(s.copy()).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+        for k in range(128):
+            sg = np.float32(sv[k // 16] * np.float32(G))
+            if sg == 0:
+                assert codes[k] == 0
+                continue
+            r = float(np.float32(a[k] / sg))
+            mags = np.abs(_TABLE[:8] - min(abs(r), 1e30))
+            c = int(codes[k])
+            assert mags[c & 7] == mags.min()
+            if (c & 7) and mags[(c & 7) - 1] == mags.min():
+                assert (c & 1) == 0  # tie -> even code
+            if c & 8:
+                assert r < 0
+
+
+def test_quant_row_round_trip_on_grid():
+    """A row already on the grid (codes * 2^j block scales, G chosen by the rule) is reproduced exactly."""
+    rng = np.random.default_rng(33)
+    K = 64
+    codes = rng.integers(0, 16, K)
+    codes[::16] = 7  # every block holds a +6 so its amax is 6 * scale
+    bscale = 2.0 ** rng.integers(-3, 4, K // 16).astype(np.float64)
+    bscale[0] = 8.0  # row amax = 6 * 8 * 1, so G = 48/2688 and block scales are 8/... exactly?
+    a = (_TABLE[codes] * np.repeat(bscale, 16)).astype(np.float32)
+    q, s, G = oracle.quant_nvfp4_row(a)
+    back = _nv_grid_value(q, s, G, K)
+    # values recovered to within one FP32 rounding of the products involved
+    np.testing.assert_allclose(back, a.astype(np.float64), rtol=2e-7, atol=0)
+
+
+def test_quant_row_error_bound():
+    """|dequant - a| <= half a grid step (relative 1/4 of the block scale) plus saturation of the block max."""
+    rng = np.random.default_rng(34)
+    a = rng.standard_normal(512).astype(np.float32)
+    q, s, G = oracle.quant_nvfp4_row(a)
+    back = _nv_grid_value(q, s, G, 512)
+    sv = torch.from_numpy(s.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    step = np.repeat(sv, 16) * G  # grid spacing is at most 2 * (s*G) (between 4 and 6)
+    err = np.abs(back - a)
+    bmax = np.repeat(np.abs(a.reshape(-1, 16)).max(-1), 16)
+    assert np.all(err <= step + 0.07 * bmax)
+
+
+# ---------------------------------------------------------------- routing / compaction
+def test_route_is_stable_counting_sort():
+    rng = np.random.default_rng(41)
+    for M, E, k in [(1, 8, 2), (5, 6, 3), (64, 16, 4), (33, 128, 8)]:
+        ids = rng.integers(-2, E + 2, (M, k)).astype(np.int32)
+        perm, off = oracle.route(ids, E)
+        flat = ids.reshape(-1)
+        valid = np.nonzero((flat >= 0) & (flat < E))[0]
+        order = valid[np.lexsort((valid, flat[valid]))]  # expert, then flat index (= token, slot)
+        assert np.array_equal(perm, order)
+        counts = np.bincount(flat[valid], minlength=E)
+        assert np.array_equal(off, np.concatenate([[0], np.cumsum(counts)]))
