@@ -1,0 +1,340 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused FP4-weight MoE layer on GB300.
+
+Workload: the decode layer E=512, H=2560, I=320, top_k=10, M=1 token, NVFP4
+weights (an E4M3 scale per 16 K-elements plus FP32 per-tensor multipliers),
+BF16 activations, softmax top-k routing with distinct experts per token.  A
+step is one whole layer (routing inside the kernels, FC1, SiLU*up, FC2,
+router-weighted sum) on one routing draw.  Metric: routed-weight HBM GB/s
+(the routed experts' weight + scale bytes, plus activations, ids and output,
+divided by the layer time), with microseconds per layer alongside.
+
+Cold L2: the K timed layers cycle through K routing draws in which no expert
+repeats within 20 consecutive layers (20 x 13.8 MB = 276 MB > 2 x L2), so
+every layer streams its experts from HBM.  The K layers are captured in one
+CUDA graph and replayed once between two device syncs.
+
+--impl reference runs the FP64 CPU oracle (the only other implementation of
+this layer here) on the host cores on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused FP4 MoE µs/layer & routed-weight HBM GB/s at M=1..8; prefill TFLOP/s"
+WORKLOAD = "decode_e512"
+WINDOW = 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def layer_bytes(ids, E, H, I, M, top_k, fmt):
+    from workload import gen
+    uniq = len(gen.routed_unique_experts(ids, E))
+    return uniq * gen.expert_bytes(H, I, fmt) + M * H * 2 * 2 + M * top_k * 8, uniq
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_layers(c, seed, ids_pool, w_pool, x_host, seconds, max_layers):
+    """Time the FP64 oracle on successive routing draws (bounded sample)."""
+    import oracle
+    from workload import gen
+    E, H, I, k, M, fmt = c["E"], c["H"], c["I"], c["top_k"], c["M"], c["fmt"]
+    done, total_s, total_bytes = 0, 0.0, 0
+    for i in range(min(max_layers, len(ids_pool))):
+        ids = ids_pool[i]
+        used = gen.routed_unique_experts(ids, E)
+        sub = gen.make_expert_weights(E, H, I, fmt, seed, device="cpu", experts=used)
+        remap = {e: j for j, e in enumerate(used)}
+        ids_c = [[remap.get(e, -1) for e in row] for row in ids.tolist()]
+        t0 = time.perf_counter()
+        oracle.forward(x_host, sub, ids_c, w_pool[i], len(used), H, I, k, fmt)
+        total_s += time.perf_counter() - t0
+        total_bytes += layer_bytes(ids, E, H, I, M, k, fmt)[0]
+        done += 1
+        if total_s >= seconds:
+            break
+    threads = min(oracle.num_threads(), M)  # the oracle parallelises over tokens
+    return done, total_s, total_bytes, threads
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from workload import gen
+    c = gen.CONFIGS[WORKLOAD]
+    seed = gen.CONFIG_SEED[WORKLOAD]
+    n = args.warmup + args.steps
+    ids_pool, w_pool = gen.draw_routing_pool(max(n, WINDOW), c["M"], c["E"], c["top_k"], seed + 29, WINDOW)
+    x = gen.draw_activations(c["M"], c["H"], seed + 17)
+    # warm-up layers, then the timed layers (each step = one oracle layer)
+    oracle_layers(c, seed, ids_pool[:args.warmup], w_pool[:args.warmup], x, 1e9, args.warmup)
+    done, secs, nbytes, threads = oracle_layers(c, seed, ids_pool[args.warmup:n], w_pool[args.warmup:n], x, 1e9,
+                                                args.steps)
+    gbs = nbytes / secs / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": done, "warmup": args.warmup, "ms_per_step": secs / done * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "E": c["E"], "H": c["H"], "I": c["I"], "top_k": c["top_k"], "M": c["M"],
+                   "fmt": "nvfp4"},
+        "us_per_layer": secs / done * 1e6,
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{done} layers of {WORKLOAD}, one routing draw each"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import fp4_weight_moe_gb300 as m
+    from fp4_weight_moe_gb300 import build as b
+    from workload import gen
+    b.build()
+
+    c = gen.CONFIGS[WORKLOAD]
+    E, H, I, k, M, fmt = c["E"], c["H"], c["I"], c["top_k"], c["M"], c["fmt"]
+    seed = gen.CONFIG_SEED[WORKLOAD]
+    K, W = args.steps, args.warmup
+    weights = gen.make_expert_weights(E, H, I, fmt, seed, device=dev)
+    pw = m.prepare_weights(weights, E, H, I, fmt)
+    del weights
+    x = gen.draw_activations(M, H, seed + 17, device=dev)
+    ids_pool, w_pool = gen.draw_routing_pool(max(K, WINDOW), M, E, k, seed + 29 + 1000 * rank, WINDOW)
+    ids_d = [t.to(dev) for t in ids_pool]
+    w_d = [t.to(dev) for t in w_pool]
+    m.reserve_workspace(M, E, H, I, k, fmt)
+    out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+
+    # eager warm-up, then capture the K timed layers in one graph
+    for i in range(W):
+        m.forward(x, pw, ids_d[i % K], w_d[i % K], out=out)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(K):
+            m.forward(x, pw, ids_d[i], w_d[i], out=out)
+    torch.cuda.synchronize()
+    g.replay()  # untimed: graph upload and one more warm pass
+    torch.cuda.synchronize()
+
+    per_layer_bytes = [layer_bytes(ids_pool[i], E, H, I, M, k, fmt)[0] for i in range(K)]
+    step_bytes = sum(per_layer_bytes)
+
+    sampler = ClockSampler(local)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    ev0.record(cur)
+    g.replay()
+    ev1.record(cur)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if ws > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    t = torch.tensor([ms], device=dev)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    ms_per_step = ms_max / K
+    value = step_bytes * ws / (ms_max * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers (pinned), per step:
+    # H2D of x, ids and router weights, the layer, D2H of the output.
+    xh = x.cpu().pin_memory()
+    idh = [t.pin_memory() for t in ids_pool[:K]]
+    wh = [t.pin_memory() for t in w_pool[:K]]
+    outh = torch.empty((M, H), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(x)
+    idd = torch.empty((M, k), dtype=torch.int32, device=dev)
+    wd = torch.empty((M, k), dtype=torch.float32, device=dev)
+
+    def e2e_step(i):
+        xd.copy_(xh, non_blocking=True)
+        idd.copy_(idh[i], non_blocking=True)
+        wd.copy_(wh[i], non_blocking=True)
+        m.forward(xd, pw, idd, wd, out=out)
+        outh.copy_(out, non_blocking=True)
+
+    for i in range(W):
+        e2e_step(i % K)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for i in range(K):
+        e2e_step(i)
+    e1.record(cur)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    t = torch.tensor([e2e_ms], device=dev)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    e2e_value = step_bytes * ws / (float(t.item()) * 1e-3) / 1e9
+
+    peak, peak_kind = load_peaks()
+    achieved = (step_bytes / K) / (ms_per_step * 1e-3) / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "decode_e512_traffic.json")
+    if os.path.exists(prof):
+        try:
+            with open(prof) as f:
+                pd = json.load(f)
+            import hashlib
+            src = open(os.path.join(ROOT, "fp4_weight_moe_gb300", "csrc", "decode.cu"), "rb").read()
+            if pd.get("decode_cu_sha256") == hashlib.sha256(src).hexdigest():
+                traffic = pd.get("dram_bytes_per_layer")
+        except Exception:
+            traffic = None
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K, "warmup": W,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp32-accum e2m1 x bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "E": E, "H": H, "I": I, "top_k": k, "M": M, "fmt": "nvfp4",
+                   "l2": f"routing draws rotate; no expert repeats within {WINDOW} layers "
+                         f"({WINDOW} x {per_layer_bytes[0] / 1e6:.1f} MB > 2 x L2)",
+                   "timing": "K layers in one CUDA graph, one replay, CUDA events"},
+        "us_per_layer": ms_per_step * 1e3,
+        "routed_bytes_per_layer": step_bytes / K,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"hbm_gbs of {peak_kind}", "traffic": traffic,
+                     "kernel": "decode FC1+FC2 pair (PDL-overlapped), per layer"},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": M * H * 2 + M * k * 8,
+                "d2h_bytes_per_step": M * H * 2, "us_per_layer": float(t.item()) * 1e3 / K},
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+    }
+
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        done, secs, nbytes, threads = oracle_layers(c, seed, ids_pool, w_pool, x.cpu(), args.cpu_seconds, K)
+        line["cpu_baseline"] = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{done} layers of {WORKLOAD} (one routing draw each), "
+                                          f"{secs:.1f} s; us/layer {secs / done * 1e6:.0f}"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

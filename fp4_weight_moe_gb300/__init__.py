@@ -1,0 +1,143 @@
+"""GB300-native fused FP4-weight mixture-of-experts layer.
+
+The compute path is ``libmoe_fp4.so`` (hand-written CUDA for sm_103a behind a
+C ABI, see ``include/moe_fp4.h``).  This package is its thin Python binding:
+``_capi`` mirrors the C entry points one to one, and the helpers below only
+allocate torch device tensors and pass their pointers.  PyTorch provides device
+memory and streams; no step of the layer runs in PyTorch.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import torch
+
+from . import _capi
+from ._capi import (  # noqa: F401
+    MOE_FP4_DECODE_MAX_M,
+    MOE_FP4_MXFP4,
+    MOE_FP4_NVFP4,
+    MoeFp4Error,
+)
+
+MXFP4 = MOE_FP4_MXFP4
+NVFP4 = MOE_FP4_NVFP4
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("libmoe_fp4 takes CUDA tensors only (there is no CPU path)")
+
+
+@dataclasses.dataclass
+class PreparedWeights:
+    """Resident (repacked) expert weights on one device."""
+    w13: torch.Tensor
+    s13: torch.Tensor
+    w2: torch.Tensor
+    s2: torch.Tensor
+    E: int
+    H: int
+    I: int
+    fmt: int
+
+    def ptrs(self):
+        return _ptr(self.w13), _ptr(self.s13), _ptr(self.w2), _ptr(self.s2)
+
+
+def prepared_sizes(E: int, H: int, I: int, fmt: int):
+    return _capi.moe_fp4_prepared_sizes(E, H, I, fmt)
+
+
+def prepare_weights(weights: dict, E: int, H: int, I: int, fmt: int, stream=None) -> PreparedWeights:
+    """Repack logical checkpoint tensors (dict with w13, s13, w2, s2 and, for
+    NVFP4, g13, g2; CUDA tensors) into the resident layout."""
+    w13_l, s13_l, w2_l, s2_l = (weights[k].contiguous() for k in ("w13", "s13", "w2", "s2"))
+    g13 = weights.get("g13") if fmt == NVFP4 else None
+    g2 = weights.get("g2") if fmt == NVFP4 else None
+    if g13 is not None:
+        g13 = g13.contiguous().float()
+        g2 = g2.contiguous().float()
+    _require_cuda(w13_l, s13_l, w2_l, s2_l, g13, g2)
+    dev = w13_l.device
+    n13, ns13, n2, ns2 = prepared_sizes(E, H, I, fmt)
+    out = [torch.empty(n, dtype=torch.uint8, device=dev) for n in (n13, ns13, n2, ns2)]
+    _capi.moe_fp4_prepare_weights(_ptr(w13_l), _ptr(s13_l), _ptr(g13), _ptr(w2_l), _ptr(s2_l), _ptr(g2), E, H, I,
+                                  fmt, *[_ptr(t) for t in out], _stream(stream))
+    return PreparedWeights(*out, E=E, H=H, I=I, fmt=fmt)
+
+
+def unprepare_weights(pw: PreparedWeights, stream=None) -> dict:
+    """Resident -> logical tensors (test support)."""
+    E, H, I, fmt = pw.E, pw.H, pw.I, pw.fmt
+    B = 32 if fmt == MXFP4 else 16
+    dev = pw.w13.device
+    w13 = torch.empty((E, 2 * I, H // 2), dtype=torch.uint8, device=dev)
+    s13 = torch.empty((E, 2 * I, H // B), dtype=torch.uint8, device=dev)
+    w2 = torch.empty((E, H, I // 2), dtype=torch.uint8, device=dev)
+    s2 = torch.empty((E, H, I // B), dtype=torch.uint8, device=dev)
+    g13 = torch.empty((E, 2), dtype=torch.float32, device=dev) if fmt == NVFP4 else None
+    g2 = torch.empty((E,), dtype=torch.float32, device=dev) if fmt == NVFP4 else None
+    _capi.moe_fp4_unprepare_weights(*pw.ptrs(), E, H, I, fmt, _ptr(w13), _ptr(s13), _ptr(g13), _ptr(w2), _ptr(s2),
+                                    _ptr(g2), _stream(stream))
+    out = dict(w13=w13, s13=s13, w2=w2, s2=s2)
+    if fmt == NVFP4:
+        out.update(g13=g13, g2=g2)
+    return out
+
+
+def workspace_bytes(M_max: int, E: int, H: int, I: int, top_k: int, fmt: int) -> int:
+    return _capi.moe_fp4_workspace_bytes(M_max, E, H, I, top_k, fmt)
+
+
+def alloc_workspace(M_max: int, E: int, H: int, I: int, top_k: int, fmt: int, device=None) -> torch.Tensor:
+    """A zero-filled caller-owned workspace for ``forward(..., workspace=...)``."""
+    n = workspace_bytes(M_max, E, H, I, top_k, fmt)
+    if n == 0:
+        raise MoeFp4Error("moe_fp4_workspace_bytes", _capi.MOE_FP4_EUNSUPPORTED)
+    return torch.zeros(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+
+
+def reserve_workspace(M_max: int, E: int, H: int, I: int, top_k: int, fmt: int, stream=None):
+    _capi.moe_fp4_reserve_workspace(M_max, E, H, I, top_k, fmt, _stream(stream))
+
+
+def forward(x: torch.Tensor, pw: PreparedWeights, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+            out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The fused MoE layer: bf16 ``x [M, H]`` -> bf16 ``out [M, H]``."""
+    if x.dtype != torch.bfloat16 or topk_ids.dtype != torch.int32 or topk_weights.dtype != torch.float32:
+        raise TypeError("x must be bfloat16, topk_ids int32, topk_weights float32")
+    _require_cuda(x, topk_ids, topk_weights, out, workspace)
+    M, H = x.shape
+    top_k = topk_ids.shape[1]
+    if out is None:
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    args = (_ptr(x), *pw.ptrs(), _ptr(topk_ids), _ptr(topk_weights), _ptr(out), M, pw.E, pw.H, pw.I, top_k, pw.fmt)
+    if workspace is None:
+        _capi.moe_fp4_forward(*args, _stream(stream))
+    else:
+        _capi.moe_fp4_forward_ws(*args, _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    return out
+
+
+def debug_dequant(pw: PreparedWeights, which: int, expert: int, stream=None) -> torch.Tensor:
+    rows, K = (2 * pw.I, pw.H) if which == 0 else (pw.H, pw.I)
+    out = torch.empty((rows, K), dtype=torch.float32, device=pw.w13.device)
+    w, s = (pw.w13, pw.s13) if which == 0 else (pw.w2, pw.s2)
+    _capi.moe_fp4_debug_dequant(_ptr(w), _ptr(s), which, expert, pw.E, pw.H, pw.I, pw.fmt, _ptr(out),
+                                _stream(stream))
+    return out

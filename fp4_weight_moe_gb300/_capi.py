@@ -1,0 +1,150 @@
+"""ctypes binding of libmoe_fp4.so: one Python function per C entry point,
+same names, arguments marshalled as integers (device pointers, sizes,
+stream handles).  No arithmetic of the layer happens here.
+
+The library is loaded from this package directory (built in-tree by
+``fp4_weight_moe_gb300.build``).  If it is missing, every call raises: there
+is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_fp4.so")
+
+MOE_FP4_OK = 0
+MOE_FP4_EINVAL = 1
+MOE_FP4_EUNSUPPORTED = 2
+MOE_FP4_ECUDA = 3
+MOE_FP4_EWORKSPACE = 4
+MOE_FP4_MXFP4 = 0
+MOE_FP4_NVFP4 = 1
+MOE_FP4_DECODE_MAX_M = 8
+
+# (name, restype, argtypes) for every symbol declared in include/moe_fp4.h
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_Z = ctypes.c_size_t
+_PZ = ctypes.POINTER(ctypes.c_size_t)
+SIGNATURES = {
+    "moe_fp4_status_string": (ctypes.c_char_p, [_I]),
+    "moe_fp4_last_cuda_error": (_I, []),
+    "moe_fp4_version": (_I, []),
+    "moe_fp4_prepared_sizes": (_I, [_I, _I, _I, _I, _PZ, _PZ, _PZ, _PZ]),
+    "moe_fp4_prepare_weights": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "moe_fp4_unprepare_weights": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_fp4_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
+    "moe_fp4_reserve_workspace": (_I, [_I, _I, _I, _I, _I, _I, _P]),
+    "moe_fp4_release_workspace": (_I, []),
+    "moe_fp4_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "moe_fp4_forward_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "moe_fp4_debug_dequant": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "moe_fp4_debug_route": (_I, [_P, _I, _I, _I, _P, _P, _P, _Z, _P]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MoeFp4Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        lib = _load()
+        msg = lib.moe_fp4_status_string(status).decode()
+        if status == MOE_FP4_ECUDA:
+            msg += f" (cudaError {lib.moe_fp4_last_cuda_error()})"
+        super().__init__(f"{fn} failed: status {status} ({msg})")
+        self.status = status
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libmoe_fp4.so is not built ({LIB_PATH}); run fp4_weight_moe_gb300.build.build()")
+            lib = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(lib, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = lib
+        return _lib
+
+
+def lib():
+    return _load()
+
+
+def _check(fn: str, status: int) -> int:
+    if status != MOE_FP4_OK:
+        raise MoeFp4Error(fn, status)
+    return status
+
+
+# ------------------------------------------------------------- entry points
+def moe_fp4_status_string(status: int) -> str:
+    return _load().moe_fp4_status_string(status).decode()
+
+
+def moe_fp4_version() -> int:
+    return _load().moe_fp4_version()
+
+
+def moe_fp4_prepared_sizes(E, H, I, fmt):
+    sizes = [ctypes.c_size_t() for _ in range(4)]
+    _check("moe_fp4_prepared_sizes",
+           _load().moe_fp4_prepared_sizes(E, H, I, fmt, *[ctypes.byref(s) for s in sizes]))
+    return tuple(int(s.value) for s in sizes)
+
+
+def moe_fp4_prepare_weights(w13_l, s13_l, g13, w2_l, s2_l, g2, E, H, I, fmt, w13, s13, w2, s2, stream):
+    return _check("moe_fp4_prepare_weights",
+                  _load().moe_fp4_prepare_weights(w13_l, s13_l, g13, w2_l, s2_l, g2, E, H, I, fmt, w13, s13, w2, s2,
+                                                  stream))
+
+
+def moe_fp4_unprepare_weights(w13, s13, w2, s2, E, H, I, fmt, w13_l, s13_l, g13, w2_l, s2_l, g2, stream):
+    return _check("moe_fp4_unprepare_weights",
+                  _load().moe_fp4_unprepare_weights(w13, s13, w2, s2, E, H, I, fmt, w13_l, s13_l, g13, w2_l, s2_l,
+                                                    g2, stream))
+
+
+def moe_fp4_workspace_bytes(M_max, E, H, I, top_k, fmt) -> int:
+    return int(_load().moe_fp4_workspace_bytes(M_max, E, H, I, top_k, fmt))
+
+
+def moe_fp4_reserve_workspace(M_max, E, H, I, top_k, fmt, stream):
+    return _check("moe_fp4_reserve_workspace", _load().moe_fp4_reserve_workspace(M_max, E, H, I, top_k, fmt, stream))
+
+
+def moe_fp4_release_workspace():
+    return _check("moe_fp4_release_workspace", _load().moe_fp4_release_workspace())
+
+
+def moe_fp4_forward(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt, stream):
+    return _check("moe_fp4_forward",
+                  _load().moe_fp4_forward(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt, stream))
+
+
+def moe_fp4_forward_ws(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt, ws, ws_bytes, stream):
+    return _check("moe_fp4_forward_ws",
+                  _load().moe_fp4_forward_ws(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt, ws, ws_bytes,
+                                             stream))
+
+
+def moe_fp4_debug_dequant(w, s, which, expert, E, H, I, fmt, out, stream):
+    return _check("moe_fp4_debug_dequant",
+                  _load().moe_fp4_debug_dequant(w, s, which, expert, E, H, I, fmt, out, stream))
+
+
+def moe_fp4_debug_route(ids, M, E, top_k, perm, offset, ws, ws_bytes, stream):
+    return _check("moe_fp4_debug_route", _load().moe_fp4_debug_route(ids, M, E, top_k, perm, offset, ws, ws_bytes,
+                                                                       stream))
+
+
+def raw_status(name: str, *args) -> int:
+    """Call an entry point and return its status without raising (tests of the error contract)."""
+    return getattr(_load(), name)(*args)

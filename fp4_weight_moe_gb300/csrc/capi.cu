@@ -1,0 +1,243 @@
+// extern "C" entry points of libmoe_fp4.so: argument validation, workspace
+// management and band dispatch.  The declarations and the contract of each
+// function are in include/moe_fp4.h.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe_fp4 {
+cudaError_t launch_prepare(const void* w13_l, const void* s13_l, const float* g13, const void* w2_l,
+                           const void* s2_l, const float* g2, int E, int H, int I, int fmt, void* w13, void* s13,
+                           void* w2, void* s2, cudaStream_t st, bool inverse);
+cudaError_t launch_debug_dequant(const void* w, const void* s, int which, int e, int E, int H, int I, int fmt,
+                                 float* out, cudaStream_t st);
+size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int num_sms);
+cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
+                          const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
+                          int fmt, void* ws, int num_sms, cudaStream_t st);
+}  // namespace moe_fp4
+
+using namespace moe_fp4;
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+constexpr size_t kMaxWorkspace = (size_t)1 << 31;  // workspaces past 2^31 bytes are rejected
+
+int fail_cuda(cudaError_t e) {
+  g_last_cuda_error = (int)e;
+  return MOE_FP4_ECUDA;
+}
+
+int device_sms(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  static int cache[64] = {0};
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+    *sms = cache[dev];
+    return MOE_FP4_OK;
+  }
+  int v = 0;
+  e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (dev >= 0 && dev < 64) cache[dev] = v;
+  *sms = v;
+  return MOE_FP4_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int check_shape(int E, int H, int I, int top_k, int fmt) {
+  if (fmt != MOE_FP4_MXFP4 && fmt != MOE_FP4_NVFP4) return MOE_FP4_EINVAL;
+  if (E <= 0 || H <= 0 || I <= 0 || top_k <= 0) return MOE_FP4_EINVAL;
+  if (E > 65536 || top_k > 16) return MOE_FP4_EUNSUPPORTED;
+  if (H % 256 != 0 || I % 64 != 0) return MOE_FP4_EUNSUPPORTED;
+  if ((long long)H * 2 * I > (1LL << 31)) return MOE_FP4_EUNSUPPORTED;
+  return MOE_FP4_OK;
+}
+
+struct LibWorkspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::mutex g_ws_mutex;
+LibWorkspace g_ws[64];
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_fp4_status_string(int status) {
+  switch (status) {
+    case MOE_FP4_OK: return "ok";
+    case MOE_FP4_EINVAL: return "invalid argument";
+    case MOE_FP4_EUNSUPPORTED: return "unsupported shape";
+    case MOE_FP4_ECUDA: return "CUDA error";
+    case MOE_FP4_EWORKSPACE: return "workspace missing, too small or too large";
+    default: return "unknown status";
+  }
+}
+
+int moe_fp4_last_cuda_error(void) { return g_last_cuda_error; }
+
+int moe_fp4_version(void) { return 100; }
+
+int moe_fp4_prepared_sizes(int E, int H, int I, int fmt, size_t* w13_bytes, size_t* s13_bytes, size_t* w2_bytes,
+                           size_t* s2_bytes) {
+  int st = check_shape(E, H, I, 1, fmt);
+  if (st != MOE_FP4_OK) return st;
+  const size_t g13 = fmt == MOE_FP4_NVFP4 ? sizeof(float) * 2 * (size_t)E : 0;
+  const size_t g2 = fmt == MOE_FP4_NVFP4 ? sizeof(float) * (size_t)E : 0;
+  auto pad16 = [](size_t v) { return (v + 15) & ~(size_t)15; };
+  if (w13_bytes) *w13_bytes = (size_t)E * 2 * I * (H / 2);
+  if (s13_bytes) *s13_bytes = pad16((size_t)E * scale_chunk_bytes(2 * I, H, fmt) + g13);
+  if (w2_bytes) *w2_bytes = (size_t)E * H * (I / 2);
+  if (s2_bytes) *s2_bytes = pad16((size_t)E * scale_chunk_bytes(H, I, fmt) + g2);
+  return MOE_FP4_OK;
+}
+
+int moe_fp4_prepare_weights(const void* w13_logical, const void* s13_logical, const float* g13,
+                            const void* w2_logical, const void* s2_logical, const float* g2, int E, int H, int I,
+                            int fmt, void* w13, void* s13, void* w2, void* s2, void* stream) {
+  int st = check_shape(E, H, I, 1, fmt);
+  if (st != MOE_FP4_OK) return st;
+  if (!w13_logical || !s13_logical || !w2_logical || !s2_logical || !w13 || !s13 || !w2 || !s2)
+    return MOE_FP4_EINVAL;
+  if (fmt == MOE_FP4_NVFP4 && (!g13 || !g2)) return MOE_FP4_EINVAL;
+  if (!aligned16(w13_logical) || !aligned16(w13) || !aligned16(s13) || !aligned16(s2)) return MOE_FP4_EINVAL;
+  cudaError_t e = launch_prepare(w13_logical, s13_logical, g13, w2_logical, s2_logical, g2, E, H, I, fmt, w13, s13,
+                                 w2, s2, static_cast<cudaStream_t>(stream), false);
+  return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
+}
+
+int moe_fp4_unprepare_weights(const void* w13, const void* s13, const void* w2, const void* s2, int E, int H, int I,
+                              int fmt, void* w13_logical, void* s13_logical, float* g13, void* w2_logical,
+                              void* s2_logical, float* g2, void* stream) {
+  int st = check_shape(E, H, I, 1, fmt);
+  if (st != MOE_FP4_OK) return st;
+  if (!w13_logical || !s13_logical || !w2_logical || !s2_logical || !w13 || !s13 || !w2 || !s2)
+    return MOE_FP4_EINVAL;
+  if (fmt == MOE_FP4_NVFP4 && (!g13 || !g2)) return MOE_FP4_EINVAL;
+  if (!aligned16(w13_logical) || !aligned16(w13)) return MOE_FP4_EINVAL;
+  cudaError_t e = launch_prepare(w13_logical, s13_logical, g13, w2_logical, s2_logical, g2, E, H, I, fmt,
+                                 const_cast<void*>(w13), const_cast<void*>(s13), const_cast<void*>(w2),
+                                 const_cast<void*>(s2), static_cast<cudaStream_t>(stream), true);
+  return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
+}
+
+size_t moe_fp4_workspace_bytes(int M_max, int E, int H, int I, int top_k, int fmt) {
+  if (M_max < 0 || check_shape(E, H, I, top_k, fmt) != MOE_FP4_OK) return 0;
+  if (M_max > MOE_FP4_DECODE_MAX_M) return 0;  // prefill band: not available in this build
+  int sms = 0;
+  if (device_sms(&sms) != MOE_FP4_OK) return 0;
+  return decode_workspace_bytes(M_max < 1 ? 1 : M_max, H, I, top_k, sms);
+}
+
+int moe_fp4_reserve_workspace(int M_max, int E, int H, int I, int top_k, int fmt, void* stream) {
+  size_t need = moe_fp4_workspace_bytes(M_max, E, H, I, top_k, fmt);
+  if (need == 0) return check_shape(E, H, I, top_k, fmt) != MOE_FP4_OK ? check_shape(E, H, I, top_k, fmt)
+                                                                        : MOE_FP4_EUNSUPPORTED;
+  if (need >= kMaxWorkspace) return MOE_FP4_EWORKSPACE;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (dev < 0 || dev >= 64) return MOE_FP4_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_ws_mutex);
+  LibWorkspace& w = g_ws[dev];
+  if (w.bytes >= need) return MOE_FP4_OK;
+  if (w.ptr) {
+    e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e);
+    cudaFree(w.ptr);
+    w.ptr = nullptr;
+    w.bytes = 0;
+  }
+  void* p = nullptr;
+  e = cudaMalloc(&p, need);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = cudaMemsetAsync(p, 0, need, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaFree(p);
+    return fail_cuda(e);
+  }
+  w.ptr = p;
+  w.bytes = need;
+  return MOE_FP4_OK;
+}
+
+int moe_fp4_release_workspace(void) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (dev < 0 || dev >= 64) return MOE_FP4_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_ws_mutex);
+  LibWorkspace& w = g_ws[dev];
+  if (w.ptr) {
+    e = cudaDeviceSynchronize();
+    cudaFree(w.ptr);
+    w.ptr = nullptr;
+    w.bytes = 0;
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  return MOE_FP4_OK;
+}
+
+int moe_fp4_forward_ws(const void* x_bf16, const void* w13, const void* s13, const void* w2, const void* s2,
+                       const int32_t* topk_ids, const float* topk_weights, void* out_bf16, int M, int E, int H,
+                       int I, int top_k, int fmt, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_shape(E, H, I, top_k, fmt);
+  if (st != MOE_FP4_OK) return st;
+  if (M < 0) return MOE_FP4_EINVAL;
+  if (M == 0) return MOE_FP4_OK;
+  if (!x_bf16 || !w13 || !s13 || !w2 || !s2 || !topk_ids || !topk_weights || !out_bf16) return MOE_FP4_EINVAL;
+  if (!aligned16(x_bf16) || !aligned16(w13) || !aligned16(w2) || !aligned16(s13) || !aligned16(s2))
+    return MOE_FP4_EINVAL;
+  if (M > MOE_FP4_DECODE_MAX_M) return MOE_FP4_EUNSUPPORTED;
+  if (!workspace || ((uintptr_t)workspace & 255u)) return MOE_FP4_EWORKSPACE;
+  int sms = 0;
+  st = device_sms(&sms);
+  if (st != MOE_FP4_OK) return st;
+  const size_t need = decode_workspace_bytes(M, H, I, top_k, sms);
+  if (need >= kMaxWorkspace || workspace_bytes < need) return MOE_FP4_EWORKSPACE;
+  cudaError_t e = launch_decode(x_bf16, w13, s13, w2, s2, topk_ids, topk_weights, out_bf16, M, E, H, I, top_k, fmt,
+                                workspace, sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
+}
+
+int moe_fp4_forward(const void* x_bf16, const void* w13, const void* s13, const void* w2, const void* s2,
+                    const int32_t* topk_ids, const float* topk_weights, void* out_bf16, int M, int E, int H, int I,
+                    int top_k, int fmt, void* stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (dev < 0 || dev >= 64) return MOE_FP4_EUNSUPPORTED;
+  void* ptr;
+  size_t bytes;
+  {
+    std::lock_guard<std::mutex> lk(g_ws_mutex);
+    ptr = g_ws[dev].ptr;
+    bytes = g_ws[dev].bytes;
+  }
+  if (M > 0 && !ptr) return MOE_FP4_EWORKSPACE;
+  return moe_fp4_forward_ws(x_bf16, w13, s13, w2, s2, topk_ids, topk_weights, out_bf16, M, E, H, I, top_k, fmt, ptr,
+                            bytes, stream);
+}
+
+int moe_fp4_debug_dequant(const void* w, const void* s, int which, int expert, int E, int H, int I, int fmt,
+                          float* out_f32, void* stream) {
+  int st = check_shape(E, H, I, 1, fmt);
+  if (st != MOE_FP4_OK) return st;
+  if (!w || !s || !out_f32 || (which != 0 && which != 1) || expert < 0 || expert >= E) return MOE_FP4_EINVAL;
+  cudaError_t e = launch_debug_dequant(w, s, which, expert, E, H, I, fmt, out_f32, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
+}
+
+int moe_fp4_debug_route(const int32_t* topk_ids, int M, int E, int top_k, int32_t* perm, int32_t* expert_offset,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  (void)topk_ids; (void)M; (void)E; (void)top_k; (void)perm; (void)expert_offset; (void)workspace;
+  (void)workspace_bytes; (void)stream;
+  return MOE_FP4_EUNSUPPORTED;  // the prefill band is not part of this build yet
+}
+
+}  // extern "C"

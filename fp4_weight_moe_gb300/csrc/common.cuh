@@ -1,0 +1,107 @@
+// Shared device helpers of libmoe_fp4: resident-layout index math, E2M1 /
+// scale decode, and the inline PTX the kernels use (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/moe_fp4.h"
+
+namespace moe_fp4 {
+
+constexpr int kRowTile = 128;     // rows per resident tile (scale chunk height)
+constexpr int kChunkBytes = 512;  // one scale chunk: 128 rows x 4 K-blocks
+constexpr int kInterleave = 64;   // gate/up interleave granularity in w13
+
+__host__ __device__ constexpr int block_size(int fmt) { return fmt == MOE_FP4_MXFP4 ? 32 : 16; }
+__host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Number of 4-block groups along K.
+__host__ __device__ inline int k_groups(int K, int fmt) { return ceil_div(K / block_size(fmt), 4); }
+
+// Bytes of one expert-projection's scale chunks (rows x K).
+__host__ __device__ inline size_t scale_chunk_bytes(int rows, int K, int fmt) {
+  return (size_t)(rows / kRowTile) * k_groups(K, fmt) * kChunkBytes;
+}
+
+// Offset of (row, kblock) inside one expert-projection's chunk array.
+__host__ __device__ inline size_t scale_offset(int row, int kb, int KG) {
+  int rt = row / kRowTile, r = row % kRowTile;
+  return ((size_t)rt * KG + kb / 4) * kChunkBytes + (r % 32) * 16 + (r / 32) * 4 + (kb % 4);
+}
+
+// Resident w13 row -> logical row (gate rows 0..I-1, up rows I..2I-1).
+__host__ __device__ inline int w13_logical_row(int R, int I) {
+  int j = R / (2 * kInterleave), r = R % (2 * kInterleave);
+  return r < kInterleave ? j * kInterleave + r : I + j * kInterleave + (r - kInterleave);
+}
+// Logical w13 row -> resident row.
+__host__ __device__ inline int w13_resident_row(int L, int I) {
+  bool up = L >= I;
+  int n = up ? L - I : L;
+  return (n / kInterleave) * (2 * kInterleave) + (up ? kInterleave : 0) + n % kInterleave;
+}
+
+// ---------------------------------------------------------------- decode helpers
+__device__ __forceinline__ float ue8m0_to_float(uint32_t b) {
+  // 2^(b-127); byte 0 -> 2^-127 (subnormal), byte 255 -> NaN.
+  if (b == 0u) return __int_as_float(0x00400000);
+  if (b == 255u) return __int_as_float(0x7fc00000);
+  return __int_as_float((int)(b << 23));
+}
+
+__device__ __forceinline__ float e4m3_to_float(uint32_t b) {
+  uint32_t h2;
+  uint16_t in = (uint16_t)(b & 0xffu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
+}
+
+__device__ __forceinline__ float scale_to_float(uint32_t b, int fmt) {
+  return fmt == MOE_FP4_MXFP4 ? ue8m0_to_float(b) : e4m3_to_float(b);
+}
+
+// Eight E2M1 values (a 32-bit word, element 2i in the low nibble of byte i)
+// -> four half2 {element 2i, element 2i+1}; exact (hardware cvt).
+__device__ __forceinline__ void e2m1x8_to_half2x4(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t h) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// Streaming 16-byte load that bypasses L1 (weights are read exactly once).
+__device__ __forceinline__ uint4 ld_stream_16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue, and (in that kernel) wait until this grid's writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ float silu(float v) { return v / (1.0f + __expf(-v)); }
+
+}  // namespace moe_fp4

@@ -1,0 +1,194 @@
+/*
+ * moe_fp4.h — C ABI of libmoe_fp4.so, a fused mixture-of-experts layer over
+ * 4-bit E2M1 expert weights with block scales, for one NVIDIA GB300 GPU
+ * (sm_103a).
+ *
+ * The layer (b12x PR #22, "rp-native tiny-decode kernel for w4a8_mx (M=1)",
+ * section What): for every token t and each of its top-k slots j with a valid
+ * expert id e,
+ *     gate_n = x_t . W13[e][n],  up_n = x_t . W13[e][I+n]      (FC1, FP32)
+ *     h_n    = SiLU(gate_n) * up_n
+ *     y_m    = W2[e][m] . h                                     (FC2)
+ *     out_t  = sum_j topk_weights[t][j] * y                     (BF16 output)
+ * Activations are BF16 and are not quantised in the decode band (same
+ * section: "Activations stay BF16").  A slot whose id is < 0 or >= E
+ * contributes exactly zero (b12x PR #311, conversation: invalid routes get an
+ * exact-zero effective weight and caller tensors are never mutated).
+ *
+ * Formats (fmt):
+ *   MOE_FP4_MXFP4 — E2M1 elements, one UE8M0 scale byte per 32 K-elements
+ *                   (flashinfer PR #4285, scale_format_e8m0_k32).
+ *   MOE_FP4_NVFP4 — E2M1 elements, one E4M3 scale byte per 16 K-elements,
+ *                   times an FP32 per-tensor multiplier (b12x PR #459,
+ *                   "Reduce NVFP4-CSF scale reconstruction overhead":
+ *                   FP32 calibration kept with the scale bytes).
+ *
+ * Conventions for every function:
+ *   - All array arguments are DEVICE pointers on the current CUDA device,
+ *     unless stated as host.  They are owned by the caller; the library never
+ *     frees or retains them past the call (except the library workspace of
+ *     moe_fp4_reserve_workspace, which the library owns).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls enqueue work and return without synchronising.
+ *   - Every function returns a moe_fp4_status; nothing throws.  Argument
+ *     errors are reported before any work is enqueued.  MOE_FP4_ECUDA means a
+ *     CUDA launch or API call failed; moe_fp4_last_cuda_error() gives the
+ *     cudaError_t value.
+ *   - Shape limits: H % 256 == 0, I % 64 == 0, 1 <= top_k <= 16,
+ *     1 <= E <= 65536; violating shapes return MOE_FP4_EUNSUPPORTED.
+ */
+#ifndef MOE_FP4_H
+#define MOE_FP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_FP4_API __attribute__((visibility("default")))
+#else
+#define MOE_FP4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { MOE_FP4_MXFP4 = 0, MOE_FP4_NVFP4 = 1 } moe_fp4_fmt;
+
+typedef enum {
+    MOE_FP4_OK = 0,
+    MOE_FP4_EINVAL = 1,       /* null pointer, negative size, unknown fmt */
+    MOE_FP4_EUNSUPPORTED = 2, /* shape outside the supported limits */
+    MOE_FP4_ECUDA = 3,        /* a CUDA call failed */
+    MOE_FP4_EWORKSPACE = 4    /* workspace missing or too small, or >= 2^31 bytes */
+} moe_fp4_status;
+
+/* Largest token count handled by the decode band (HBM-bound GEMV kernels);
+ * larger M uses the prefill band (grouped block-scaled GEMM). */
+#define MOE_FP4_DECODE_MAX_M 8
+
+/* Human-readable name of a status code (static string, never NULL). */
+MOE_FP4_API const char *moe_fp4_status_string(int status);
+
+/* cudaError_t of the most recent MOE_FP4_ECUDA on the calling host thread. */
+MOE_FP4_API int moe_fp4_last_cuda_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+MOE_FP4_API int moe_fp4_version(void);
+
+/*
+ * Sizes in bytes of the four resident (prepared) weight buffers for E
+ * experts of shape (H, I) in format fmt.  Host pointers out; any may be NULL.
+ *
+ * Resident layout (written by moe_fp4_prepare_weights):
+ *   w13: [E][2I][H/2] bytes.  Rows are the logical gate/up rows interleaved
+ *        in groups of 64: resident rows 128j..128j+63 are gate rows
+ *        64j..64j+63 and resident rows 128j+64..128j+127 are up rows
+ *        64j..64j+63, so each 128-row tile holds matching gate and up rows.
+ *        Byte order within a row is the logical one (low nibble = even K).
+ *   w2:  [E][H][I/2] bytes, the logical layout.
+ *   s13, s2: scale bytes in 512-byte chunks, one per (expert, 128-row tile,
+ *        group of 4 consecutive K-blocks); inside a chunk the byte of row r
+ *        (0..127 within the tile) and K-block b (0..3 within the group) is at
+ *        (r % 32) * 16 + (r / 32) * 4 + b.  Chunks are ordered expert, row
+ *        tile, K-block group.  Missing K-blocks of a ragged last group are 0.
+ *        NVFP4 appends the FP32 multipliers after the chunks: s13 gets
+ *        [E][2] (gate, up), s2 gets [E].
+ */
+MOE_FP4_API int moe_fp4_prepared_sizes(int E, int H, int I, int fmt, size_t *w13_bytes, size_t *s13_bytes, size_t *w2_bytes,
+                           size_t *s2_bytes);
+
+/*
+ * Repack logical checkpoint tensors into the resident layout (one-time,
+ * outside the hot path).  Inputs (device):
+ *   w13_logical [E][2I][H/2] u8 — rows 0..I-1 gate, I..2I-1 up; low nibble =
+ *                                 even K index
+ *   s13_logical [E][2I][H/B] u8 — one scale byte per (row, K-block of B)
+ *   g13         [E][2] f32      — NVFP4 gate/up multipliers (NULL for MXFP4)
+ *   w2_logical  [E][H][I/2] u8, s2_logical [E][H][I/B] u8, g2 [E] f32 (NVFP4)
+ * Outputs (device, sizes from moe_fp4_prepared_sizes): w13, s13, w2, s2.
+ * Inputs and outputs must not overlap.
+ */
+MOE_FP4_API int moe_fp4_prepare_weights(const void *w13_logical, const void *s13_logical, const float *g13,
+                            const void *w2_logical, const void *s2_logical, const float *g2, int E, int H, int I,
+                            int fmt, void *w13, void *s13, void *w2, void *s2, void *stream);
+
+/* Inverse of moe_fp4_prepare_weights (test support): resident -> logical. */
+MOE_FP4_API int moe_fp4_unprepare_weights(const void *w13, const void *s13, const void *w2, const void *s2, int E, int H, int I,
+                              int fmt, void *w13_logical, void *s13_logical, float *g13, void *w2_logical,
+                              void *s2_logical, float *g2, void *stream);
+
+/*
+ * Workspace bytes needed by moe_fp4_forward_ws for up to M_max tokens.
+ * Returns 0 for invalid arguments.  Workspaces of 2^31 bytes or more are
+ * rejected by the forward calls (MOE_FP4_EWORKSPACE).
+ */
+MOE_FP4_API size_t moe_fp4_workspace_bytes(int M_max, int E, int H, int I, int top_k, int fmt);
+
+/*
+ * Allocate (cudaMalloc) and zero a library-owned workspace on the current
+ * device, sized for moe_fp4_workspace_bytes(M_max, ...).  A later call with
+ * larger sizes grows it; smaller calls keep it.  Call it before capturing
+ * moe_fp4_forward in a CUDA graph: moe_fp4_forward itself never allocates.
+ * moe_fp4_release_workspace frees it.
+ */
+MOE_FP4_API int moe_fp4_reserve_workspace(int M_max, int E, int H, int I, int top_k, int fmt, void *stream);
+MOE_FP4_API int moe_fp4_release_workspace(void);
+
+/*
+ * The fused MoE layer, using the reserved library workspace
+ * (MOE_FP4_EWORKSPACE if none is reserved or it is too small).
+ *   x_bf16       [M][H] bf16 activations
+ *   w13, s13, w2, s2  resident weights from moe_fp4_prepare_weights
+ *   topk_ids     [M][top_k] int32 expert ids (ids < 0 or >= E are ignored)
+ *   topk_weights [M][top_k] f32 router weights
+ *   out_bf16     [M][H] bf16, fully overwritten (tokens with no valid slot
+ *                get +0.0); must not overlap any input.
+ * M = 0 is a no-op.  Inputs are never written.  Decode (M <= 8) results are
+ * bitwise deterministic; the prefill band sums routed rows into an FP32
+ * token accumulator with atomic adds, so its low-order bits may vary run to
+ * run.
+ */
+MOE_FP4_API int moe_fp4_forward(const void *x_bf16, const void *w13, const void *s13, const void *w2, const void *s2,
+                    const int32_t *topk_ids, const float *topk_weights, void *out_bf16, int M, int E, int H, int I,
+                    int top_k, int fmt, void *stream);
+
+/*
+ * Same as moe_fp4_forward with an explicit caller-owned workspace of at
+ * least moe_fp4_workspace_bytes(M, E, H, I, top_k, fmt) bytes (256-byte
+ * aligned).  Before its first use a workspace must be zero-filled
+ * (cudaMemset); every call leaves its synchronisation counters at zero
+ * again, so later calls need no re-zeroing.  Calls sharing one workspace must
+ * be ordered (same stream or explicit dependencies).
+ */
+MOE_FP4_API int moe_fp4_forward_ws(const void *x_bf16, const void *w13, const void *s13, const void *w2, const void *s2,
+                       const int32_t *topk_ids, const float *topk_weights, void *out_bf16, int M, int E, int H,
+                       int I, int top_k, int fmt, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Test support: dequantise one expert's projection from the resident layout
+ * into out_f32 [rows][K] in LOGICAL row order, each element computed as the
+ * decode kernels do: e2m1 * scale (MXFP4, exact) or RN_fp32((e2m1 * e4m3) *
+ * g) (NVFP4, one rounding).  which = 0: w13 (rows 2I, K = H, gate rows
+ * first), which = 1: w2 (rows H, K = I).
+ */
+MOE_FP4_API int moe_fp4_debug_dequant(const void *w, const void *s, int which, int expert, int E, int H, int I, int fmt,
+                          float *out_f32, void *stream);
+
+/*
+ * Test support: the prefill band's routing compaction.  Routed rows (t, j)
+ * with a valid id are grouped by expert (ascending), then token, then slot:
+ * perm[r] = t*top_k + j for grouped row r, and expert_offset[e] ..
+ * expert_offset[e+1] delimit expert e's rows (expert_offset has E+1
+ * entries).  perm has M*top_k entries; those past expert_offset[E] are -1.
+ * Uses `workspace` (moe_fp4_workspace_bytes(M, ...) bytes, zero-filled before
+ * first use).
+ */
+MOE_FP4_API int moe_fp4_debug_route(const int32_t *topk_ids, int M, int E, int top_k, int32_t *perm, int32_t *expert_offset,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FP4_H */

@@ -1,0 +1,91 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and
+loads, exports every symbol that include/moe_fp4.h declares, and rejects bad
+arguments with the documented status codes before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from fp4_weight_moe_gb300 import _capi
+from fp4_weight_moe_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_fp4.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return _capi.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MOE_FP4_API\s+[\w\s\*]*?\b(moe_fp4_\w+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = _declared()
+    for must in ("moe_fp4_prepare_weights", "moe_fp4_forward", "moe_fp4_forward_ws", "moe_fp4_workspace_bytes",
+                 "moe_fp4_prepared_sizes", "moe_fp4_debug_dequant", "moe_fp4_debug_route"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert name in _capi.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert _capi.moe_fp4_status_string(s)
+    assert _capi.moe_fp4_status_string(99) == "unknown status"
+    assert _capi.moe_fp4_version() >= 100
+
+
+@pytest.mark.parametrize("fmt,B", [(0, 32), (1, 16)])
+def test_prepared_sizes_closed_form(lib, fmt, B):
+    E, H, I = 5, 512, 192
+    w13, s13, w2, s2 = _capi.moe_fp4_prepared_sizes(E, H, I, fmt)
+    assert w13 == E * 2 * I * H // 2
+    assert w2 == E * H * I // 2
+    kg13 = -(-(H // B) // 4)
+    kg2 = -(-(I // B) // 4)
+    pad = lambda v: (v + 15) // 16 * 16  # noqa: E731
+    assert s13 == pad(E * (2 * I // 128) * kg13 * 512 + (8 * E if fmt == 1 else 0))
+    assert s2 == pad(E * (H // 128) * kg2 * 512 + (4 * E if fmt == 1 else 0))
+
+
+def _fwd_status(M=1, E=8, H=256, I=128, k=2, fmt=0, ptr=0x1000, ws=0x10000, ws_bytes=1 << 20, out=None):
+    p = ptr
+    return _capi.raw_status("moe_fp4_forward_ws", p, p, p, p, p, p, p, out if out is not None else p, M, E, H, I, k,
+                            fmt, ws, ws_bytes, None)
+
+
+def test_forward_argument_errors(lib):
+    assert _fwd_status(M=-1) == _capi.MOE_FP4_EINVAL
+    assert _fwd_status(fmt=7) == _capi.MOE_FP4_EINVAL
+    assert _fwd_status(E=0) == _capi.MOE_FP4_EINVAL
+    assert _fwd_status(H=384) == _capi.MOE_FP4_EUNSUPPORTED  # H % 256
+    assert _fwd_status(I=96) == _capi.MOE_FP4_EUNSUPPORTED  # I % 64
+    assert _fwd_status(k=17) == _capi.MOE_FP4_EUNSUPPORTED
+    assert _fwd_status(ptr=0) == _capi.MOE_FP4_EINVAL  # null pointers
+    assert _fwd_status(ptr=0x1008) == _capi.MOE_FP4_EINVAL  # x / weights not 16-byte aligned
+    assert _fwd_status(M=0) == _capi.MOE_FP4_OK  # empty batch is a no-op
+    assert _fwd_status(ws=0) == _capi.MOE_FP4_EWORKSPACE
+    assert _fwd_status(ws=0x10010) == _capi.MOE_FP4_EWORKSPACE  # not 256-byte aligned
+
+
+def test_prepare_argument_errors(lib):
+    st = _capi.raw_status("moe_fp4_prepare_weights", 0x1000, 0x1000, None, 0x1000, 0x1000, None, 4, 256, 128, 1,
+                          0x1000, 0x1000, 0x1000, 0x1000, None)
+    assert st == _capi.MOE_FP4_EINVAL  # NVFP4 needs the FP32 multipliers
+    st = _capi.raw_status("moe_fp4_prepare_weights", 0x1000, 0x1000, None, 0x1000, 0x1000, None, 4, 200, 128, 0,
+                          0x1000, 0x1000, 0x1000, 0x1000, None)
+    assert st == _capi.MOE_FP4_EUNSUPPORTED
+    st = _capi.raw_status("moe_fp4_debug_dequant", 0x1000, 0x1000, 2, 0, 4, 256, 128, 0, 0x1000, None)
+    assert st == _capi.MOE_FP4_EINVAL
+    st = _capi.raw_status("moe_fp4_debug_dequant", 0x1000, 0x1000, 0, 4, 4, 256, 128, 0, 0x1000, None)
+    assert st == _capi.MOE_FP4_EINVAL  # expert out of range

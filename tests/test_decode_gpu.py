@@ -1,0 +1,182 @@
+"""Parity of the decode band (M <= 8) with the FP64 oracle, through the C ABI.
+
+Covers: the resident-layout round trip (bitwise), dequantised weights
+(bit-exact), every decode workload shape at oracle-friendly sizes spanning
+several tiles and ragged K-block groups, the full-size workloads, invalid and
+duplicate routes, all-invalid tokens, NaN-poisoned outputs, determinism,
+untouched inputs, CUDA-graph replay and the workspace contract.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.gpu_util import assert_layer_close, compact_for_oracle, ensure_built, oracle_layer
+from workload import gen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    ensure_built()
+
+
+def fm():
+    import fp4_weight_moe_gb300 as m
+    return m
+
+
+def _prepare(wl):
+    return fm().prepare_weights(wl.weights, wl.E, wl.H, wl.I, wl.fmt)
+
+
+def _run(wl, pw=None, out=None, ws=None):
+    m = fm()
+    pw = pw or _prepare(wl)
+    ws = ws if ws is not None else m.alloc_workspace(wl.M, wl.E, wl.H, wl.I, wl.top_k, wl.fmt)
+    return m.forward(wl.x, pw, wl.topk_ids, wl.topk_weights, out=out, workspace=ws)
+
+
+# ------------------------------------------------------------------ resident layout
+@pytest.mark.parametrize("fmt", [gen.MXFP4, gen.NVFP4])
+@pytest.mark.parametrize("H,I", [(256, 128), (512, 320)])
+def test_prepare_round_trip(fmt, H, I):
+    wl = gen.make_workload("tiny_decode", device="cuda", fmt=fmt, E=3, H=H, I=I)
+    pw = _prepare(wl)
+    back = fm().unprepare_weights(pw)
+    torch.cuda.synchronize()
+    for k in ("w13", "s13", "w2", "s2") + (("g13", "g2") if fmt == gen.NVFP4 else ()):
+        assert torch.equal(back[k], wl.weights[k]), k
+
+
+@pytest.mark.parametrize("fmt", [gen.MXFP4, gen.NVFP4])
+def test_dequant_bit_exact(fmt):
+    wl = gen.make_workload("tiny_decode", device="cuda", fmt=fmt, E=3, H=512, I=320)
+    pw = _prepare(wl)
+    B = gen.BLOCK[fmt]
+    w = {k: v.cpu().numpy() for k, v in wl.weights.items()}
+    for e in range(wl.E):
+        for which in (0, 1):
+            got = fm().debug_dequant(pw, which, e).cpu().numpy()
+            if which == 0:
+                rows = []
+                for proj, sl in ((0, slice(0, wl.I)), (1, slice(wl.I, 2 * wl.I))):
+                    g = float(w["g13"][e, proj]) if fmt == gen.NVFP4 else 1.0
+                    rows.append(oracle.dequant(w["w13"][e, sl], w["s13"][e, sl], wl.H, fmt, g))
+                want = np.concatenate(rows)
+            else:
+                g = float(w["g2"][e]) if fmt == gen.NVFP4 else 1.0
+                want = oracle.dequant(w["w2"][e], w["s2"][e], wl.I, fmt, g)
+            # FP64 product rounded once to FP32 must equal the kernel's bits
+            assert np.array_equal(got.view(np.uint32), want.astype(np.float32).view(np.uint32)), (e, which, B)
+
+
+# ------------------------------------------------------------------ layer parity
+DECODE_CASES = [
+    # name, overrides
+    ("tiny_decode", {}),
+    ("tiny_decode", dict(fmt=gen.NVFP4)),
+    ("tiny_decode", dict(M=3, E=16, top_k=4)),
+    ("decode_e512", dict(E=24)),                      # NVFP4, H=2560 (split K), I=320
+    ("decode_e512", dict(E=24, fmt=gen.MXFP4)),       # MX with a ragged K-block group in FC2
+    ("decode_e512", dict(E=40, M=8)),
+    ("decode_e288_m4", dict(E=24)),                   # 2 invalid slots (-1 and E)
+    ("decode_e288_m4", dict(E=24, M=8, fmt=gen.NVFP4)),
+    ("decode_e256", dict(E=12, H=1792, I=512, M=2)),  # Zipf routing
+    ("decode_e256", dict(E=12, H=1792, I=512, M=5, fmt=gen.NVFP4)),
+]
+
+
+@pytest.mark.parametrize("name,ov", DECODE_CASES, ids=[f"{n}-{i}" for i, (n, _) in enumerate(DECODE_CASES)])
+def test_decode_parity(name, ov):
+    wl = gen.make_workload(name, device="cuda", **ov)
+    out = torch.full((wl.M, wl.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    got = _run(wl, out=out)
+    torch.cuda.synchronize()
+    assert_layer_close(got, oracle_layer(wl), f"{name} {ov}")
+
+
+def test_duplicate_and_invalid_routes():
+    wl = gen.make_workload("tiny_decode", device="cuda", M=4, E=6, top_k=4)
+    ids = torch.tensor([[0, 0, 3, -1], [5, 6, 2, 2], [1, 1, 1, 1], [-5, 100, 6, 4]], dtype=torch.int32)
+    wl.topk_ids = ids.cuda()
+    wl.topk_weights = torch.rand((4, 4), generator=torch.Generator().manual_seed(0)).cuda()
+    got = _run(wl)
+    torch.cuda.synchronize()
+    assert_layer_close(got, oracle_layer(wl), "duplicates/invalid")
+
+
+def test_all_invalid_gives_exact_zero():
+    wl = gen.make_workload("tiny_decode", device="cuda", M=3, E=8, top_k=2)
+    wl.topk_ids = torch.tensor([[-1, 8], [9, -3], [-1, -1]], dtype=torch.int32, device="cuda")
+    out = torch.full((3, wl.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    got = _run(wl, out=out)
+    torch.cuda.synchronize()
+    assert torch.all(got.float() == 0) and not torch.any(torch.signbit(got.float()))
+
+
+def test_deterministic_and_inputs_untouched():
+    m = fm()
+    wl = gen.make_workload("decode_e512", device="cuda", E=32, M=4)
+    pw = _prepare(wl)
+    snap = [t.clone() for t in (wl.x, wl.topk_ids, wl.topk_weights, pw.w13, pw.s13, pw.w2, pw.s2)]
+    ws = m.alloc_workspace(wl.M, wl.E, wl.H, wl.I, wl.top_k, wl.fmt)
+    a = m.forward(wl.x, pw, wl.topk_ids, wl.topk_weights, workspace=ws).clone()
+    b = m.forward(wl.x, pw, wl.topk_ids, wl.topk_weights, workspace=ws).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for s, t in zip(snap, (wl.x, wl.topk_ids, wl.topk_weights, pw.w13, pw.s13, pw.w2, pw.s2)):
+        assert torch.equal(s, t)
+
+
+def test_library_workspace_and_graph_replay():
+    m = fm()
+    wl = gen.make_workload("decode_e512", device="cuda", E=32, M=2)
+    pw = _prepare(wl)
+    m.reserve_workspace(8, wl.E, wl.H, wl.I, wl.top_k, wl.fmt)
+    eager = m.forward(wl.x, pw, wl.topk_ids, wl.topk_weights).clone()
+    out = torch.empty_like(eager)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        m.forward(wl.x, pw, wl.topk_ids, wl.topk_weights, out=out, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        m.forward(wl.x, pw, wl.topk_ids, wl.topk_weights, out=out)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+
+
+def test_workspace_too_small_is_rejected():
+    m = fm()
+    wl = gen.make_workload("tiny_decode", device="cuda")
+    pw = _prepare(wl)
+    n = m.workspace_bytes(wl.M, wl.E, wl.H, wl.I, wl.top_k, wl.fmt)
+    small = torch.zeros(n - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(m.MoeFp4Error) as ei:
+        m.forward(wl.x, pw, wl.topk_ids, wl.topk_weights, workspace=small)
+    assert ei.value.status == 4
+
+
+# ------------------------------------------------------------------ full-size workloads
+FULL = [
+    ("decode_e512", {}),
+    ("decode_e288_m4", {}),
+    ("decode_e256", dict(M=1)),
+    ("decode_e256", dict(M=8, fmt=gen.NVFP4)),
+]
+
+
+@pytest.mark.parametrize("name,ov", FULL, ids=[f"{n}-{i}" for i, (n, _) in enumerate(FULL)])
+def test_decode_full_size(name, ov):
+    wl = gen.make_workload(name, device="cuda", **ov)
+    got = _run(wl)
+    torch.cuda.synchronize()
+    assert_layer_close(got, oracle_layer(wl), f"{name} {ov}")
+    del wl
+    torch.cuda.empty_cache()

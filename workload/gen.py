@@ -134,22 +134,27 @@ def _expert_generator(seed: int, expert: int, proj: int, device) -> torch.Genera
     return gen
 
 
-def make_expert_weights(E: int, H: int, I: int, fmt: int, seed: int, device="cpu", std: float = 0.02):
+def make_expert_weights(E: int, H: int, I: int, fmt: int, seed: int, device="cpu", std: float = 0.02,
+                        experts=None):
     """Draw and encode all experts' weights. Returns a dict of logical tensors on
     ``device``: w13, s13, w2, s2 and (NVFP4) g13, g2.
 
     Each expert's floats come from its own counter-seeded generator, so a
-    subset of experts can be regenerated alone."""
+    subset of experts can be generated alone: with ``experts`` (a list of ids)
+    only those are drawn, in that order, and the leading dimension is
+    ``len(experts)``."""
     B = BLOCK[fmt]
+    expert_ids = list(range(E)) if experts is None else list(experts)
+    E = len(expert_ids)
     w13 = torch.empty((E, 2 * I, H // 2), dtype=torch.uint8, device=device)
     s13 = torch.empty((E, 2 * I, H // B), dtype=torch.uint8, device=device)
     w2 = torch.empty((E, H, I // 2), dtype=torch.uint8, device=device)
     s2 = torch.empty((E, H, I // B), dtype=torch.uint8, device=device)
     g13 = torch.ones((E, 2), dtype=torch.float32, device=device) if fmt == NVFP4 else None
     g2 = torch.ones((E,), dtype=torch.float32, device=device) if fmt == NVFP4 else None
-    for e in range(E):
+    for e, eid in enumerate(expert_ids):
         for proj, rows, K in ((0, I, H), (1, I, H), (2, H, I)):
-            gen = _expert_generator(seed, e, proj, device)
+            gen = _expert_generator(seed, eid, proj, device)
             wf = torch.randn((rows, K), generator=gen, device=device, dtype=torch.float32) * std
             if fmt == MXFP4:
                 nib, sc = encode_mxfp4(wf)
@@ -221,26 +226,30 @@ def draw_routing(M: int, E: int, top_k: int, seed: int, mode: str = "softmax", n
 
 def draw_routing_pool(n_draws: int, M: int, E: int, top_k: int, seed: int, window: int):
     """``n_draws`` routings for a timing loop, drawn like ``draw_routing`` in
-    softmax mode except that an expert used in one of the previous
-    ``window - 1`` draws is excluded from the next draw (its logit is set to
-    -inf before the top-k).  The bytes touched by ``window`` consecutive draws
-    then exceed the L2 cache, so every timed layer streams its experts from
-    HBM."""
+    softmax mode except that no expert appears in two draws closer than
+    ``window`` positions apart, cyclically (draw i and draw (i + d) mod n for
+    0 < d < window share no expert; the excluded experts get logit -inf
+    before the top-k).  Replaying the sequence in a loop, the bytes touched by
+    any ``window`` consecutive layers then exceed the L2 cache, so every timed
+    layer streams its experts from HBM."""
     assert window * top_k * M <= E, "window too large for E"
+    assert n_draws >= 1
     rng = np.random.Generator(np.random.PCG64(seed))
-    ids_all, w_all = [], []
-    recent: list = []
-    for _ in range(n_draws):
+    sets = [None] * n_draws
+    ids_all, w_all = [None] * n_draws, [None] * n_draws
+    for i in range(n_draws):
         logits = rng.standard_normal((M, E))
         banned = set()
-        for r in recent[-(window - 1):] if window > 1 else []:
-            banned.update(r)
+        for d in range(1, min(window, n_draws)):
+            for j in ((i - d) % n_draws, (i + d) % n_draws):
+                if sets[j] is not None and j != i:
+                    banned.update(sets[j])
         if banned:
             logits[:, sorted(banned)] = -np.inf
         ids, w = _softmax_topk(logits, top_k)
-        recent.append(set(ids.reshape(-1).tolist()))
-        ids_all.append(torch.from_numpy(ids))
-        w_all.append(torch.from_numpy(w))
+        sets[i] = set(ids.reshape(-1).tolist())
+        ids_all[i] = torch.from_numpy(ids)
+        w_all[i] = torch.from_numpy(w)
     return ids_all, w_all
 
 
