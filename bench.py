@@ -43,8 +43,25 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--workload", default=WORKLOAD, help="workload name (default: the decode_e512 headline)")
+    ap.add_argument("--M", type=int, default=None, help="override the token count")
+    ap.add_argument("--E", type=int, default=None, help="override the expert count (profiling on smaller memory)")
+    ap.add_argument("--fmt", choices=["mxfp4", "nvfp4"], default=None)
     return ap.parse_args()
+
+
+def workload_config(args):
+    from workload import gen
+    c = dict(gen.CONFIGS[args.workload])
+    if args.M is not None:
+        c["M"] = args.M
+    if args.E is not None:
+        c["E"] = args.E
+    if args.fmt is not None:
+        c["fmt"] = gen.MXFP4 if args.fmt == "mxfp4" else gen.NVFP4
+    return c
 
 
 def load_peaks():
@@ -152,10 +169,11 @@ def run_reference(args):
     if rank != 0:
         return
     from workload import gen
-    c = gen.CONFIGS[WORKLOAD]
-    seed = gen.CONFIG_SEED[WORKLOAD]
+    c = workload_config(args)
+    seed = gen.CONFIG_SEED[args.workload]
     n = args.warmup + args.steps
-    ids_pool, w_pool = gen.draw_routing_pool(max(n, WINDOW), c["M"], c["E"], c["top_k"], seed + 29, WINDOW)
+    window = max(1, min(WINDOW, c["E"] // (c["top_k"] * c["M"])))
+    ids_pool, w_pool = gen.draw_routing_pool(max(n, window), c["M"], c["E"], c["top_k"], seed + 29, window)
     x = gen.draw_activations(c["M"], c["H"], seed + 17)
     # warm-up layers, then the timed layers (each step = one oracle layer)
     oracle_layers(c, seed, ids_pool[:args.warmup], w_pool[:args.warmup], x, 1e9, args.warmup)
@@ -166,11 +184,11 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": done, "warmup": args.warmup, "ms_per_step": secs / done * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "E": c["E"], "H": c["H"], "I": c["I"], "top_k": c["top_k"], "M": c["M"],
-                   "fmt": "nvfp4"},
+        "config": {"workload": args.workload, "E": c["E"], "H": c["H"], "I": c["I"], "top_k": c["top_k"],
+                   "M": c["M"], "fmt": gen.FMT_NAMES[c["fmt"]]},
         "us_per_layer": secs / done * 1e6,
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{done} layers of {WORKLOAD}, one routing draw each"},
+                         "sample": f"{done} layers of {args.workload}, one routing draw each"},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -192,15 +210,16 @@ def run_ours(args):
     from workload import gen
     b.build()
 
-    c = gen.CONFIGS[WORKLOAD]
+    c = workload_config(args)
     E, H, I, k, M, fmt = c["E"], c["H"], c["I"], c["top_k"], c["M"], c["fmt"]
-    seed = gen.CONFIG_SEED[WORKLOAD]
+    seed = gen.CONFIG_SEED[args.workload]
     K, W = args.steps, args.warmup
+    window = max(1, min(WINDOW, E // (k * M)))
     weights = gen.make_expert_weights(E, H, I, fmt, seed, device=dev)
     pw = m.prepare_weights(weights, E, H, I, fmt)
     del weights
     x = gen.draw_activations(M, H, seed + 17, device=dev)
-    ids_pool, w_pool = gen.draw_routing_pool(max(K, WINDOW), M, E, k, seed + 29 + 1000 * rank, WINDOW)
+    ids_pool, w_pool = gen.draw_routing_pool(max(K, window), M, E, k, seed + 29 + 1000 * rank, window)
     ids_d = [t.to(dev) for t in ids_pool]
     w_d = [t.to(dev) for t in w_pool]
     m.reserve_workspace(M, E, H, I, k, fmt)
@@ -248,6 +267,7 @@ def run_ours(args):
     ms_per_step = ms_max / K
     value = step_bytes * ws / (ms_max * 1e-3) / 1e9
 
+    e2e_value = None
     # end to end through the public API with host buffers (pinned), per step:
     # H2D of x, ids and router weights, the layer, D2H of the output.
     xh = x.cpu().pin_memory()
@@ -265,23 +285,25 @@ def run_ours(args):
         m.forward(xd, pw, idd, wd, out=out)
         outh.copy_(out, non_blocking=True)
 
-    for i in range(W):
-        e2e_step(i % K)
-    torch.cuda.synchronize()
-    if ws > 1:
-        dist.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(cur)
-    for i in range(K):
-        e2e_step(i)
-    e1.record(cur)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    t = torch.tensor([e2e_ms], device=dev)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    e2e_value = step_bytes * ws / (float(t.item()) * 1e-3) / 1e9
+    e2e_ms = float("nan")
+    if not args.no_e2e:
+        for i in range(W):
+            e2e_step(i % K)
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(cur)
+        for i in range(K):
+            e2e_step(i)
+        e1.record(cur)
+        torch.cuda.synchronize()
+        t = torch.tensor([e0.elapsed_time(e1)], device=dev)
+        if ws > 1:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+        e2e_value = step_bytes * ws / (e2e_ms * 1e-3) / 1e9
 
     peak, peak_kind = load_peaks()
     achieved = (step_bytes / K) / (ms_per_step * 1e-3) / 1e9
@@ -302,9 +324,10 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K, "warmup": W,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp32-accum e2m1 x bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "E": E, "H": H, "I": I, "top_k": k, "M": M, "fmt": "nvfp4",
-                   "l2": f"routing draws rotate; no expert repeats within {WINDOW} layers "
-                         f"({WINDOW} x {per_layer_bytes[0] / 1e6:.1f} MB > 2 x L2)",
+        "config": {"workload": args.workload, "E": E, "H": H, "I": I, "top_k": k, "M": M,
+                   "fmt": gen.FMT_NAMES[fmt],
+                   "l2": f"routing draws rotate; no expert repeats within {window} layers "
+                         f"({window} x {per_layer_bytes[0] / 1e6:.1f} MB)",
                    "timing": "K layers in one CUDA graph, one replay, CUDA events"},
         "us_per_layer": ms_per_step * 1e3,
         "routed_bytes_per_layer": step_bytes / K,
@@ -312,7 +335,7 @@ def run_ours(args):
                      "peak_source": f"hbm_gbs of {peak_kind}", "traffic": traffic,
                      "kernel": "decode FC1+FC2 pair (PDL-overlapped), per layer"},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": M * H * 2 + M * k * 8,
-                "d2h_bytes_per_step": M * H * 2, "us_per_layer": float(t.item()) * 1e3 / K},
+                "d2h_bytes_per_step": M * H * 2, "us_per_layer": e2e_ms * 1e3 / K},
         "gpu_launches": 2 * K,
         "clocks": clocks,
     }
@@ -320,7 +343,7 @@ def run_ours(args):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         done, secs, nbytes, threads = oracle_layers(c, seed, ids_pool, w_pool, x.cpu(), args.cpu_seconds, K)
         line["cpu_baseline"] = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                                "sample": f"{done} layers of {WORKLOAD} (one routing draw each), "
+                                "sample": f"{done} layers of {args.workload} (one routing draw each), "
                                           f"{secs:.1f} s; us/layer {secs / done * 1e6:.0f}"}
     if rank == 0:
         print(json.dumps(line), flush=True)

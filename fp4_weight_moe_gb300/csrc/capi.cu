@@ -87,8 +87,8 @@ int moe_fp4_prepared_sizes(int E, int H, int I, int fmt, size_t* w13_bytes, size
                            size_t* s2_bytes) {
   int st = check_shape(E, H, I, 1, fmt);
   if (st != MOE_FP4_OK) return st;
-  const size_t g13 = fmt == MOE_FP4_NVFP4 ? sizeof(float) * 2 * (size_t)E : 0;
-  const size_t g2 = fmt == MOE_FP4_NVFP4 ? sizeof(float) * (size_t)E : 0;
+  const size_t g13 = sizeof(float) * 2 * (size_t)E;
+  const size_t g2 = sizeof(float) * (size_t)E;
   auto pad16 = [](size_t v) { return (v + 15) & ~(size_t)15; };
   if (w13_bytes) *w13_bytes = (size_t)E * 2 * I * (H / 2);
   if (s13_bytes) *s13_bytes = pad16((size_t)E * scale_chunk_bytes(2 * I, H, fmt) + g13);

@@ -7,7 +7,7 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
-#include "../../include/moe_fp4.h"
+#include "moe_fp4.h"
 
 namespace moe_fp4 {
 
@@ -87,6 +87,37 @@ __device__ __forceinline__ uint4 ld_stream_16(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
+}
+
+// L2 policy: lines loaded with it are the first candidates for eviction.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Streaming 16-byte load, no L1 allocation, L2 evict-first.
+__device__ __forceinline__ uint4 ld_stream_16_ef(const void* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+
+// Bring [p, p + bytes) into L2 without a destination (bytes % 16 == 0).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// d = a * b + c on two FP32 lanes at once.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2,%3};\n\tmov.b64 rb, {%4,%5};\n\t"
+      "mov.b64 rc, {%6,%7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0,%1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {

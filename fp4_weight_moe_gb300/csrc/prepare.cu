@@ -64,6 +64,33 @@ __global__ void repack_scales_kernel(const uint8_t* __restrict__ in, uint8_t* __
   }
 }
 
+// MXFP4: per (expert, projection) multiplier g = 2^(max scale exponent - 12),
+// so the decode band can carry each block scale divided by g as an exact f16
+// (2^-24 .. 2^12) and apply g after the K sum, like the NVFP4 multiplier.
+// One CTA per (expert, projection); scale byte 255 (NaN) is ignored.
+__global__ void mx_multiplier_kernel(const uint8_t* __restrict__ s_logical, int rows_per_proj, int KB, int nproj,
+                                     float* __restrict__ g_out) {
+  const int e = blockIdx.x / nproj, proj = blockIdx.x % nproj;
+  const uint8_t* base = s_logical + ((size_t)e * nproj + proj) * rows_per_proj * KB;
+  const size_t n = (size_t)rows_per_proj * KB;
+  uint32_t mx = 0;
+  for (size_t i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint32_t b = base[i];
+    if (b != 255u && b > mx) mx = b;
+  }
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  __shared__ uint32_t s_mx[32];
+  if ((threadIdx.x & 31) == 0) s_mx[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t m = 0;
+    for (int w = 0; w < (int)(blockDim.x + 31) / 32; ++w) m = max(m, s_mx[w]);
+    int k = (int)m - 127 - 12;
+    if (k < -126) k = -126;
+    g_out[blockIdx.x] = __int_as_float((k + 127) << 23);
+  }
+}
+
 // Dequantise one expert's projection (logical row order) for tests.
 __global__ void debug_dequant_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ s, int which, int e,
                                      int E, int H, int I, int fmt, float* __restrict__ out) {
@@ -123,6 +150,13 @@ cudaError_t launch_prepare(const void* w13_l, const void* s13_l, const float* g1
   else
     err = cudaMemcpyAsync(const_cast<void*>(w2_l), w2, w2_bytes, cudaMemcpyDeviceToDevice, st);
   if (err != cudaSuccess) return err;
+  if (fmt == MOE_FP4_MXFP4 && !inverse) {
+    float* s13g = reinterpret_cast<float*>(static_cast<uint8_t*>(s13) + s13_bytes);
+    float* s2g = reinterpret_cast<float*>(static_cast<uint8_t*>(s2) + s2_bytes);
+    mx_multiplier_kernel<<<E * 2, 256, 0, st>>>(static_cast<const uint8_t*>(s13_l), I, H / 32, 2, s13g);
+    mx_multiplier_kernel<<<E, 256, 0, st>>>(static_cast<const uint8_t*>(s2_l), H, I / 32, 1, s2g);
+    err = cudaGetLastError();
+  }
   if (fmt == MOE_FP4_NVFP4) {
     uint8_t* s13g = static_cast<uint8_t*>(s13) + s13_bytes;
     uint8_t* s2g = static_cast<uint8_t*>(s2) + s2_bytes;

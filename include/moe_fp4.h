@@ -92,8 +92,12 @@ MOE_FP4_API int moe_fp4_version(void);
  *        (0..127 within the tile) and K-block b (0..3 within the group) is at
  *        (r % 32) * 16 + (r / 32) * 4 + b.  Chunks are ordered expert, row
  *        tile, K-block group.  Missing K-blocks of a ragged last group are 0.
- *        NVFP4 appends the FP32 multipliers after the chunks: s13 gets
- *        [E][2] (gate, up), s2 gets [E].
+ *        After the chunks, s13 holds FP32 multipliers [E][2] (gate, up) and
+ *        s2 holds [E]: for NVFP4 the per-tensor multipliers, for MXFP4
+ *        2^(largest scale exponent of that expert's projection - 12), which
+ *        lets the decode kernels carry each block scale divided by it as an
+ *        exact f16 (block scales more than 2^35 below the largest of their
+ *        projection are flushed to zero in the decode band).
  */
 MOE_FP4_API int moe_fp4_prepared_sizes(int E, int H, int I, int fmt, size_t *w13_bytes, size_t *s13_bytes, size_t *w2_bytes,
                            size_t *s2_bytes);

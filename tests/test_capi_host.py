@@ -54,8 +54,8 @@ def test_prepared_sizes_closed_form(lib, fmt, B):
     kg13 = -(-(H // B) // 4)
     kg2 = -(-(I // B) // 4)
     pad = lambda v: (v + 15) // 16 * 16  # noqa: E731
-    assert s13 == pad(E * (2 * I // 128) * kg13 * 512 + (8 * E if fmt == 1 else 0))
-    assert s2 == pad(E * (H // 128) * kg2 * 512 + (4 * E if fmt == 1 else 0))
+    assert s13 == pad(E * (2 * I // 128) * kg13 * 512 + 8 * E)
+    assert s2 == pad(E * (H // 128) * kg2 * 512 + 4 * E)
 
 
 def _fwd_status(M=1, E=8, H=256, I=128, k=2, fmt=0, ptr=0x1000, ws=0x10000, ws_bytes=1 << 20, out=None):
