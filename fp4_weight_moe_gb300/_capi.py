@@ -23,6 +23,7 @@ MOE_FP4_EWORKSPACE = 4
 MOE_FP4_MXFP4 = 0
 MOE_FP4_NVFP4 = 1
 MOE_FP4_DECODE_MAX_M = 8
+MOE_FP4_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 # (name, restype, argtypes) for every symbol declared in include/moe_fp4.h
 _P = ctypes.c_void_p
@@ -41,6 +42,7 @@ SIGNATURES = {
     "moe_fp4_release_workspace": (_I, []),
     "moe_fp4_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "moe_fp4_forward_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "moe_fp4_forward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "moe_fp4_debug_dequant": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "moe_fp4_debug_route": (_I, [_P, _I, _I, _I, _P, _P, _P, _Z, _P]),
 }
@@ -133,6 +135,11 @@ def moe_fp4_forward_ws(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt
     return _check("moe_fp4_forward_ws",
                   _load().moe_fp4_forward_ws(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt, ws, ws_bytes,
                                              stream))
+
+
+def moe_fp4_forward_noalloc(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt, stream):
+    return _check("moe_fp4_forward_noalloc",
+                  _load().moe_fp4_forward_noalloc(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt, stream))
 
 
 def moe_fp4_debug_dequant(w, s, which, expert, E, H, I, fmt, out, stream):

@@ -170,6 +170,33 @@ MOE_FP4_API int moe_fp4_forward_ws(const void *x_bf16, const void *w13, const vo
                        int I, int top_k, int fmt, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * The decode-band layer (M <= MOE_FP4_DECODE_MAX_M) without any device
+ * allocation, for callers that cannot call cudaMalloc where they run the
+ * layer: inside a stream capture, under a runtime that owns all device memory
+ * through its own pool, or on a latency-critical path that cannot afford an
+ * allocation's implicit synchronisation.  The pages have no counterpart of
+ * this entry point; it is an addition of this library.
+ *
+ * Arguments, layouts and results are those of moe_fp4_forward (same
+ * kernels, bitwise the same output).  Instead of a workspace it uses one
+ * fixed scratch array of MOE_FP4_NOALLOC_SCRATCH_BYTES in the library's
+ * device image, which every GPU that loads the library's device code keeps
+ * until the process exits.  Shapes whose scratch need
+ * (moe_fp4_workspace_bytes(M, ...)) exceeds that size return
+ * MOE_FP4_EWORKSPACE; M > MOE_FP4_DECODE_MAX_M returns MOE_FP4_EUNSUPPORTED.
+ * The first call on each device looks up the array's device address while
+ * that device is current; make that first call outside any stream capture.
+ * All calls on a device share the one array: calls that may overlap on the
+ * GPU (different streams without ordering between them) race and corrupt
+ * each other's results, so order them.  Nothing in the array needs to start
+ * at zero.
+ */
+#define MOE_FP4_NOALLOC_SCRATCH_BYTES (4u << 20)
+MOE_FP4_API int moe_fp4_forward_noalloc(const void *x_bf16, const void *w13, const void *s13, const void *w2,
+                                        const void *s2, const int32_t *topk_ids, const float *topk_weights,
+                                        void *out_bf16, int M, int E, int H, int I, int top_k, int fmt, void *stream);
+
+/*
  * Test support: dequantise one expert's projection from the resident layout
  * into out_f32 [rows][K] in LOGICAL row order, each element computed as the
  * decode kernels do: e2m1 * scale (MXFP4, exact) or RN_fp32((e2m1 * e4m3) *
