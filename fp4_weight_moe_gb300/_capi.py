@@ -44,6 +44,7 @@ SIGNATURES = {
     "moe_fp4_forward_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "moe_fp4_forward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "moe_fp4_debug_dequant": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "moe_fp4_debug_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_fp4_debug_route": (_I, [_P, _I, _I, _I, _P, _P, _P, _Z, _P]),
 }
 
@@ -145,6 +146,11 @@ def moe_fp4_forward_noalloc(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k
 def moe_fp4_debug_dequant(w, s, which, expert, E, H, I, fmt, out, stream):
     return _check("moe_fp4_debug_dequant",
                   _load().moe_fp4_debug_dequant(w, s, which, expert, E, H, I, fmt, out, stream))
+
+
+def moe_fp4_debug_gemm(a_q, a_sf, b_q, b_sf, d, M_rows, N_rows, K, fmt, status, stream):
+    return _check("moe_fp4_debug_gemm",
+                  _load().moe_fp4_debug_gemm(a_q, a_sf, b_q, b_sf, d, M_rows, N_rows, K, fmt, status, stream))
 
 
 def moe_fp4_debug_route(ids, M, E, top_k, perm, offset, ws, ws_bytes, stream):

@@ -12,6 +12,8 @@ cudaError_t launch_prepare(const void* w13_l, const void* s13_l, const float* g1
 cudaError_t launch_debug_dequant(const void* w, const void* s, int which, int e, int E, int H, int I, int fmt,
                                  float* out, cudaStream_t st);
 size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int num_sms);
+cudaError_t launch_debug_gemm(const void* a_q, const void* a_sf, const void* b_q, const void* b_sf, float* d,
+                              int M_rows, int N_rows, int K, uint32_t* status, cudaStream_t st, int* cu_err);
 cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                           const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
                           int fmt, void* ws, int num_sms, cudaStream_t st);
@@ -230,6 +232,21 @@ int moe_fp4_debug_dequant(const void* w, const void* s, int which, int expert, i
   if (st != MOE_FP4_OK) return st;
   if (!w || !s || !out_f32 || (which != 0 && which != 1) || expert < 0 || expert >= E) return MOE_FP4_EINVAL;
   cudaError_t e = launch_debug_dequant(w, s, which, expert, E, H, I, fmt, out_f32, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
+}
+
+int moe_fp4_debug_gemm(const void* a_q, const void* a_sf, const void* b_q, const void* b_sf, float* d, int M_rows,
+                       int N_rows, int K, int fmt, uint32_t* status, void* stream) {
+  if (fmt != MOE_FP4_NVFP4 && fmt != MOE_FP4_MXFP4) return MOE_FP4_EINVAL;
+  if (fmt != MOE_FP4_NVFP4) return MOE_FP4_EUNSUPPORTED;
+  if (!a_q || !a_sf || !b_q || !b_sf || !d || !status) return MOE_FP4_EINVAL;
+  if (M_rows <= 0 || N_rows <= 0 || K <= 0) return MOE_FP4_EINVAL;
+  if (M_rows % 128 || N_rows % 256 || K % 256) return MOE_FP4_EUNSUPPORTED;
+  if (!aligned16(a_q) || !aligned16(b_q) || !aligned16(a_sf) || !aligned16(b_sf) || !aligned16(d))
+    return MOE_FP4_EINVAL;
+  int cu = 0;
+  cudaError_t e = launch_debug_gemm(a_q, a_sf, b_q, b_sf, d, M_rows, N_rows, K, status,
+                                    static_cast<cudaStream_t>(stream), &cu);
   return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
 }
 

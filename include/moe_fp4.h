@@ -207,6 +207,19 @@ MOE_FP4_API int moe_fp4_debug_dequant(const void *w, const void *s, int which, i
                           float *out_f32, void *stream);
 
 /*
+ * Test support: the prefill band's block-scaled FP4 GEMM on one pair of
+ * matrices, D[m][n] = sum_k A[m][k] * B[n][k] in FP32 (no per-tensor
+ * multipliers).  a_q [M_rows][K/2] and b_q [N_rows][K/2] packed E2M1 (low
+ * nibble = even k); a_sf, b_sf their E4M3 scales (one per 16 K-elements) in
+ * the resident 512-byte chunk layout of moe_fp4_prepared_sizes (rows in
+ * 128-row tiles); d [M_rows][N_rows] FP32.  status: one device word, zeroed
+ * by the caller; nonzero afterwards means an internal wait timed out.
+ * M_rows % 128 == 0, N_rows % 256 == 0, K % 256 == 0; NVFP4 only.
+ */
+MOE_FP4_API int moe_fp4_debug_gemm(const void *a_q, const void *a_sf, const void *b_q, const void *b_sf, float *d,
+                                   int M_rows, int N_rows, int K, int fmt, uint32_t *status, void *stream);
+
+/*
  * Test support: the prefill band's routing compaction.  Routed rows (t, j)
  * with a valid id are grouped by expert (ascending), then token, then slot:
  * perm[r] = t*top_k + j for grouped row r, and expert_offset[e] ..
