@@ -14,6 +14,14 @@ cudaError_t launch_debug_dequant(const void* w, const void* s, int which, int e,
 size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int num_sms);
 cudaError_t launch_debug_gemm(const void* a_q, const void* a_sf, const void* b_q, const void* b_sf, float* d,
                               int M_rows, int N_rows, int K, uint32_t* status, cudaStream_t st, int* cu_err);
+size_t prefill_workspace_bytes(int M, int E, int H, int I, int top_k);
+size_t debug_route_workspace_bytes(int M, int E, int top_k);
+cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
+                           const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
+                           void* ws, cudaStream_t st, int* cu_err);
+cudaError_t launch_debug_route(const int32_t* ids, int M, int E, int top_k, int32_t* perm, int32_t* expert_offset,
+                               void* ws, cudaStream_t st);
+cudaError_t launch_debug_quant(const float* in, int rows, int K, uint8_t* q, uint8_t* s, float* G, cudaStream_t st);
 cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                           const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
                           int fmt, void* ws, int num_sms, cudaStream_t st);
@@ -57,6 +65,23 @@ int check_shape(int E, int H, int I, int top_k, int fmt) {
   if (H % 256 != 0 || I % 64 != 0) return MOE_FP4_EUNSUPPORTED;
   if ((long long)H * 2 * I > (1LL << 31)) return MOE_FP4_EUNSUPPORTED;
   return MOE_FP4_OK;
+}
+
+// Extra limits of the prefill band (M > MOE_FP4_DECODE_MAX_M).
+int check_prefill(int M, int E, int I, int top_k, int fmt) {
+  if (fmt != MOE_FP4_NVFP4) return MOE_FP4_EUNSUPPORTED;
+  if (I % 256 != 0 || E > 4096) return MOE_FP4_EUNSUPPORTED;
+  if ((long long)M * top_k >= (1LL << 30)) return MOE_FP4_EUNSUPPORTED;
+  return MOE_FP4_OK;
+}
+
+size_t workspace_need(int M, int E, int H, int I, int top_k, int sms) {
+  size_t d = decode_workspace_bytes(M < MOE_FP4_DECODE_MAX_M ? M : MOE_FP4_DECODE_MAX_M, H, I, top_k, sms);
+  if (M > MOE_FP4_DECODE_MAX_M) {
+    const size_t p = prefill_workspace_bytes(M, E, H, I, top_k);
+    if (p > d) d = p;
+  }
+  return d;
 }
 
 struct LibWorkspace {
@@ -130,10 +155,10 @@ int moe_fp4_unprepare_weights(const void* w13, const void* s13, const void* w2, 
 
 size_t moe_fp4_workspace_bytes(int M_max, int E, int H, int I, int top_k, int fmt) {
   if (M_max < 0 || check_shape(E, H, I, top_k, fmt) != MOE_FP4_OK) return 0;
-  if (M_max > MOE_FP4_DECODE_MAX_M) return 0;  // prefill band: not available in this build
+  if (M_max > MOE_FP4_DECODE_MAX_M && check_prefill(M_max, E, I, top_k, fmt) != MOE_FP4_OK) return 0;
   int sms = 0;
   if (device_sms(&sms) != MOE_FP4_OK) return 0;
-  return decode_workspace_bytes(M_max < 1 ? 1 : M_max, H, I, top_k, sms);
+  return workspace_need(M_max < 1 ? 1 : M_max, E, H, I, top_k, sms);
 }
 
 int moe_fp4_reserve_workspace(int M_max, int E, int H, int I, int top_k, int fmt, void* stream) {
@@ -195,15 +220,26 @@ int moe_fp4_forward_ws(const void* x_bf16, const void* w13, const void* s13, con
   if (!x_bf16 || !w13 || !s13 || !w2 || !s2 || !topk_ids || !topk_weights || !out_bf16) return MOE_FP4_EINVAL;
   if (!aligned16(x_bf16) || !aligned16(w13) || !aligned16(w2) || !aligned16(s13) || !aligned16(s2))
     return MOE_FP4_EINVAL;
-  if (M > MOE_FP4_DECODE_MAX_M) return MOE_FP4_EUNSUPPORTED;
+  if (M > MOE_FP4_DECODE_MAX_M) {
+    st = check_prefill(M, E, I, top_k, fmt);
+    if (st != MOE_FP4_OK) return st;
+  }
   if (!workspace || ((uintptr_t)workspace & 255u)) return MOE_FP4_EWORKSPACE;
   int sms = 0;
   st = device_sms(&sms);
   if (st != MOE_FP4_OK) return st;
-  const size_t need = decode_workspace_bytes(M, H, I, top_k, sms);
+  if (M <= MOE_FP4_DECODE_MAX_M) {
+    const size_t need = decode_workspace_bytes(M, H, I, top_k, sms);
+    if (need >= kMaxWorkspace || workspace_bytes < need) return MOE_FP4_EWORKSPACE;
+    cudaError_t e = launch_decode(x_bf16, w13, s13, w2, s2, topk_ids, topk_weights, out_bf16, M, E, H, I, top_k,
+                                  fmt, workspace, sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
+  }
+  const size_t need = prefill_workspace_bytes(M, E, H, I, top_k);
   if (need >= kMaxWorkspace || workspace_bytes < need) return MOE_FP4_EWORKSPACE;
-  cudaError_t e = launch_decode(x_bf16, w13, s13, w2, s2, topk_ids, topk_weights, out_bf16, M, E, H, I, top_k, fmt,
-                                workspace, sms, static_cast<cudaStream_t>(stream));
+  int cu = 0;
+  cudaError_t e = launch_prefill(x_bf16, w13, s13, w2, s2, topk_ids, topk_weights, out_bf16, M, E, H, I, top_k,
+                                 workspace, static_cast<cudaStream_t>(stream), &cu);
   return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
 }
 
@@ -252,9 +288,26 @@ int moe_fp4_debug_gemm(const void* a_q, const void* a_sf, const void* b_q, const
 
 int moe_fp4_debug_route(const int32_t* topk_ids, int M, int E, int top_k, int32_t* perm, int32_t* expert_offset,
                         void* workspace, size_t workspace_bytes, void* stream) {
-  (void)topk_ids; (void)M; (void)E; (void)top_k; (void)perm; (void)expert_offset; (void)workspace;
-  (void)workspace_bytes; (void)stream;
-  return MOE_FP4_EUNSUPPORTED;  // the prefill band is not part of this build yet
+  if (!topk_ids || !perm || !expert_offset || M <= 0 || E <= 0 || top_k <= 0) return MOE_FP4_EINVAL;
+  if (E > 4096 || top_k > 16) return MOE_FP4_EUNSUPPORTED;
+  if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < debug_route_workspace_bytes(M, E, top_k))
+    return MOE_FP4_EWORKSPACE;
+  cudaError_t e = launch_debug_route(topk_ids, M, E, top_k, perm, expert_offset, workspace,
+                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
+}
+
+size_t moe_fp4_debug_route_workspace_bytes(int M, int E, int top_k) {
+  if (M <= 0 || E <= 0 || top_k <= 0 || E > 4096 || top_k > 16) return 0;
+  return debug_route_workspace_bytes(M, E, top_k);
+}
+
+int moe_fp4_debug_quant_rows(const float* in, int rows, int K, uint8_t* q, uint8_t* s, float* G, void* stream) {
+  if (!in || !q || !s || !G || rows <= 0 || K <= 0) return MOE_FP4_EINVAL;
+  if (K % 16 != 0) return MOE_FP4_EUNSUPPORTED;
+  if (((uintptr_t)q & 7u) || ((uintptr_t)in & 3u)) return MOE_FP4_EINVAL;
+  cudaError_t e = launch_debug_quant(in, rows, K, q, s, G, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
 }
 
 }  // extern "C"

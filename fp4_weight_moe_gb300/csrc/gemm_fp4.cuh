@@ -51,9 +51,10 @@ struct GemmTile {
   bool valid;
 };
 
-// Generic tile loop body.  Tile source: functor `tile_of(blockIdx) -> GemmTile`;
-// epilogue: functor `epi(row_in_tile, col0, const float* v32, tile)` called
-// per thread for 8 consecutive 32-column groups of its row.
+// Generic tile body.  Tile source: functor `tile_of() -> GemmTile`;
+// epilogue: functor `epi(tmem_row, row_in_tile, tile)` called once per
+// thread after the accumulator is complete; tmem_row addresses this thread's
+// accumulator row (add a column offset and read it with tmem_ld32).
 template <class TileOf, class Epi>
 __device__ __forceinline__ void gemm_fp4_tile(const CUtensorMap* map_a, const CUtensorMap* map_b, int K,
                                               uint32_t* err, const TileOf& tile_of, const Epi& epi) {
@@ -138,12 +139,7 @@ __device__ __forceinline__ void gemm_fp4_tile(const CUtensorMap* map_a, const CU
   tc_fence_after();
   const int row = (warp & 3) * 32 + lane;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-#pragma unroll 1
-  for (int c = 0; c < kGemmBN / 32; ++c) {
-    uint32_t r[32];
-    tmem_ld32(tmem + lane_base + 32 * c, r);
-    epi(row, 32 * c, reinterpret_cast<const float*>(r), t);
-  }
+  epi(tmem + lane_base, row, t);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);

@@ -50,10 +50,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     t.valid = true;
     return t;
   };
-  auto epi = [&](int row, int col0, const float* v, const GemmTile& t) {
-    float4* dst = reinterpret_cast<float4*>(d + (size_t)(t.a_row0 + row) * N + t.b_row0 + col0);
+  auto epi = [&](uint32_t tmem_row, int row, const GemmTile& t) {
+#pragma unroll 1
+    for (int c = 0; c < kGemmBN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tmem_row + 32 * c, r);
+      float4* dst = reinterpret_cast<float4*>(d + (size_t)(t.a_row0 + row) * N + t.b_row0 + 32 * c);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      for (int i = 0; i < 8; ++i)
+        dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]), __uint_as_float(r[4 * i + 2]),
+                             __uint_as_float(r[4 * i + 3]));
+    }
   };
   gemm_fp4_tile(&map_a, &map_b, K, err, tile_of, epi);
 }
@@ -72,6 +79,569 @@ cudaError_t launch_debug_gemm(const void* a_q, const void* a_sf, const void* b_q
   dim3 grid(M_rows / kGemmBM, N_rows / kGemmBN);
   debug_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, st>>>(ma, mb, static_cast<const uint8_t*>(a_sf),
                                                            static_cast<const uint8_t*>(b_sf), d, K, N_rows, status);
+  return cudaGetLastError();
+}
+
+
+// ============================================================================
+// Prefill band (M > 8): route -> quantise x -> FC1 GEMM (SiLU*up) ->
+// quantise h -> FC2 GEMM (router-weighted FP32 accumulation) -> cast.
+//
+// Prior art: the SM12x sync PR's dynamic prefill backend (flashinfer PR
+// #4285): routed rows grouped per expert and processed as MMA tiles, W4A4
+// NVFP4 with a fast FP4 activation quantiser for gated activations; and the
+// W4A16 route PR's prefill epilogue (b12x PR #311, conversation): routed
+// outputs reduced with relaxed FP32 global reductions into a caller-owned
+// FP32 token accumulator and cast to BF16 once.
+//
+// Activations: x per token and h per routed row are quantised to NVFP4 (E2M1,
+// one E4M3 scale per 16 elements, one FP32 multiplier per row):
+//   G = amax/(6*448) (1 if the row is zero), s = e4m3_rn_satfinite(bmax/(6G)),
+//   q = e2m1_rn_satfinite(a/(s*G)) (0 where s*G == 0),
+// every step an IEEE FP32 operation; h is staged in BF16 between FC1 and its
+// quantiser.  Each expert's routed rows are padded to a multiple of 128 so an
+// MMA tile never straddles two experts.
+// ============================================================================
+
+namespace {
+
+constexpr int kRouteBlock = 256;  // routing entries per count/scatter block
+constexpr int kMaxPrefillE = 4096;
+
+struct PrefillArgs {
+  const __nv_bfloat16* x;
+  const int32_t* ids;
+  const float* tw;
+  const uint8_t* s13;  // resident scale chunks (+ multipliers)
+  const uint8_t* s2;
+  __nv_bfloat16* out;
+  int M, E, H, I, top_k, n_entries, n_route_blocks, max_tiles;
+  int* counts;      // [n_route_blocks][E]
+  int* block_base;  // [n_route_blocks][E]
+  int* expert_off;  // [E+1]
+  int* expert_poff; // [E+1]
+  int* tile_expert; // [max_tiles]
+  int* num_tiles;   // [1]
+  int* pos;         // [n_entries]
+  int* row_src;     // [128 * max_tiles]
+  uint8_t* xq;      // [rows][H/2]
+  uint8_t* xsf;     // chunks [rows/128][H/64][512]
+  float* xG;        // [rows]
+  __nv_bfloat16* hbuf;  // [rows][I]
+  uint8_t* hq;      // [rows][I/2]
+  uint8_t* hsf;     // chunks [rows/128][I/64][512]
+  float* hG;        // [rows]
+  float* acc;       // [M][H]
+  uint32_t* status;
+};
+
+// Byte offset of (row, 16-element block kb) in a chunk array of K = 64*KG.
+__device__ __forceinline__ size_t sf_chunk_offset(int row, int kb, int KG) {
+  return ((size_t)(row >> 7) * KG + (kb >> 2)) * kChunkBytes + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (kb & 3);
+}
+
+__device__ __forceinline__ uint32_t e4m3_rn_sat(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+  return r & 0xffu;
+}
+// Two E2M1 codes, element `lo` in the low nibble.
+__device__ __forceinline__ uint32_t e2m1x2_rn_sat(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}" : "=h"(r) : "f"(hi), "f"(lo));
+  return r & 0xffu;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// One warp quantises a row of K elements given by load16(block, float[16]).
+// For each 16-element block calls emit(block, scale_byte, code words w0, w1
+// (8 bytes of codes)).  Returns G.
+template <class Load16, class Emit>
+__device__ __forceinline__ float quant_row_nvfp4(int K, const Load16& load16, const Emit& emit) {
+  const int lane = threadIdx.x & 31;
+  const int nb = K / 16;
+  float amax = 0.f;
+  for (int b = lane; b < nb; b += 32) {
+    float v[16];
+    load16(b, v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  }
+  amax = warp_max(amax);
+  const float G = amax == 0.f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+  const float six_g = __fmul_rn(6.0f, G);
+  for (int b = lane; b < nb; b += 32) {
+    float v[16];
+    load16(b, v);
+    float bmax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+    const uint32_t sb = e4m3_rn_sat(__fdiv_rn(bmax, six_g));
+    const float sdec = e4m3_to_float(sb);
+    const float sg = __fmul_rn(sdec, G);
+    uint32_t w0 = 0, w1 = 0;
+    if (sg != 0.f) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w0 |= e2m1x2_rn_sat(__fdiv_rn(v[2 * i], sg), __fdiv_rn(v[2 * i + 1], sg)) << (8 * i);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        w1 |= e2m1x2_rn_sat(__fdiv_rn(v[8 + 2 * i], sg), __fdiv_rn(v[8 + 2 * i + 1], sg)) << (8 * i);
+    }
+    emit(b, sb, w0, w1);
+  }
+  return G;
+}
+
+__device__ __forceinline__ void bf16x16_to_f32(const __nv_bfloat16* p, float (&v)[16]) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+  const uint4 u0 = __ldg(q), u1 = __ldg(q + 1);
+  const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// ---------------------------------------------------------------- routing
+__global__ void route_count_kernel(PrefillArgs a) {
+  extern __shared__ int s_hist[];
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) s_hist[e] = 0;
+  __syncthreads();
+  const int i = blockIdx.x * kRouteBlock + threadIdx.x;
+  if (i < a.n_entries) {
+    const int e = a.ids[i];
+    if (e >= 0 && e < a.E) atomicAdd(&s_hist[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) a.counts[(size_t)blockIdx.x * a.E + e] = s_hist[e];
+}
+
+// One CTA: per-expert totals, unpadded and 128-padded exclusive offsets, the
+// per-block bases of the stable scatter, the tile list and the padding rows.
+__global__ void route_scan_kernel(PrefillArgs a) {
+  __shared__ int s_tot[kMaxPrefillE];
+  __shared__ int s_part[2][1024];
+  const int E = a.E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int t = 0;
+    for (int b = 0; b < a.n_route_blocks; ++b) t += a.counts[(size_t)b * E + e];
+    s_tot[e] = t;
+  }
+  __syncthreads();
+  // exclusive scans over experts: each thread owns a contiguous run
+  const int per = (E + blockDim.x - 1) / blockDim.x;
+  const int e0 = min(E, (int)threadIdx.x * per), e1 = min(E, e0 + per);
+  int su = 0, sp = 0;
+  for (int e = e0; e < e1; ++e) {
+    su += s_tot[e];
+    sp += (s_tot[e] + 127) & ~127;
+  }
+  s_part[0][threadIdx.x] = su;
+  s_part[1][threadIdx.x] = sp;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ru = 0, rp = 0;
+    for (int t = 0; t < (int)blockDim.x; ++t) {
+      const int u = s_part[0][t], pp = s_part[1][t];
+      s_part[0][t] = ru;
+      s_part[1][t] = rp;
+      ru += u;
+      rp += pp;
+    }
+    a.expert_off[E] = ru;
+    a.expert_poff[E] = rp;
+    *a.num_tiles = rp / 128;
+  }
+  __syncthreads();
+  int ru = s_part[0][threadIdx.x], rp = s_part[1][threadIdx.x];
+  for (int e = e0; e < e1; ++e) {
+    const int tot = s_tot[e], padded = (tot + 127) & ~127;
+    a.expert_off[e] = ru;
+    a.expert_poff[e] = rp;
+    int run = rp;
+    for (int b = 0; b < a.n_route_blocks; ++b) {
+      a.block_base[(size_t)b * E + e] = run;
+      run += a.counts[(size_t)b * E + e];
+    }
+    for (int t = 0; t < padded / 128; ++t) a.tile_expert[rp / 128 + t] = e;
+    for (int r = rp + tot; r < rp + padded; ++r) a.row_src[r] = -1;
+    ru += tot;
+    rp += padded;
+  }
+}
+
+// One warp per block of entries: stable ranks by expert in index order.
+__global__ void route_scatter_kernel(PrefillArgs a) {
+  extern __shared__ int s_base[];
+  const int lane = threadIdx.x;
+  for (int e = lane; e < a.E; e += 32) s_base[e] = a.block_base[(size_t)blockIdx.x * a.E + e];
+  __syncwarp();
+  for (int r0 = 0; r0 < kRouteBlock; r0 += 32) {
+    const int i = blockIdx.x * kRouteBlock + r0 + lane;
+    const int e = i < a.n_entries ? a.ids[i] : -1;
+    const bool valid = e >= 0 && e < a.E;
+    const int key = valid ? e : -1 - lane;  // invalid entries stay alone
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    const uint32_t below = peers & ((1u << lane) - 1u);
+    if (valid) {
+      const int row = s_base[e] + __popc(below);
+      a.pos[i] = row;
+      a.row_src[row] = i;
+    } else if (i < a.n_entries) {
+      a.pos[i] = -1;
+    }
+    __syncwarp();
+    if (valid && below == 0) s_base[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------- quantisers
+// One warp per token: NVFP4 row of x into every routed row of the token;
+// also zeroes the token's FP32 accumulator row.
+__global__ void quant_x_kernel(PrefillArgs a) {
+  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (t >= a.M) return;
+  const int lane = threadIdx.x & 31;
+  const int H = a.H, KG = H / 64, k = a.top_k;
+  const __nv_bfloat16* xr = a.x + (size_t)t * H;
+  const int* prow = a.pos + (size_t)t * k;
+  const float G = quant_row_nvfp4(
+      H, [&](int b, float (&v)[16]) { bf16x16_to_f32(xr + 16 * b, v); },
+      [&](int b, uint32_t sb, uint32_t w0, uint32_t w1) {
+        for (int j = 0; j < k; ++j) {
+          const int r = prow[j];
+          if (r < 0) continue;
+          *reinterpret_cast<uint2*>(a.xq + (size_t)r * (H / 2) + 8 * b) = make_uint2(w0, w1);
+          a.xsf[sf_chunk_offset(r, b, KG)] = (uint8_t)sb;
+        }
+      });
+  if (lane == 0)
+    for (int j = 0; j < k; ++j)
+      if (prow[j] >= 0) a.xG[prow[j]] = G;
+  float4* accr = reinterpret_cast<float4*>(a.acc + (size_t)t * H);
+  for (int v = lane; v < H / 4; v += 32) accr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// One warp per routed row: NVFP4 row of h (BF16) for FC2; padding rows get
+// zero codes, zero scales and G = 0.
+__global__ void quant_h_kernel(PrefillArgs a) {
+  const int r = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (r >= 128 * *a.num_tiles) return;
+  const int lane = threadIdx.x & 31;
+  const int I = a.I, KG = I / 64;
+  if (a.row_src[r] < 0) {
+    for (int b = lane; b < I / 16; b += 32) {
+      *reinterpret_cast<uint2*>(a.hq + (size_t)r * (I / 2) + 8 * b) = make_uint2(0u, 0u);
+      a.hsf[sf_chunk_offset(r, b, KG)] = 0;
+    }
+    if (lane == 0) a.hG[r] = 0.f;
+    return;
+  }
+  const __nv_bfloat16* hr = a.hbuf + (size_t)r * I;
+  const float G = quant_row_nvfp4(
+      I, [&](int b, float (&v)[16]) { bf16x16_to_f32(hr + 16 * b, v); },
+      [&](int b, uint32_t sb, uint32_t w0, uint32_t w1) {
+        *reinterpret_cast<uint2*>(a.hq + (size_t)r * (I / 2) + 8 * b) = make_uint2(w0, w1);
+        a.hsf[sf_chunk_offset(r, b, KG)] = (uint8_t)sb;
+      });
+  if (lane == 0) a.hG[r] = G;
+}
+
+// ---------------------------------------------------------------- GEMMs
+// Tile (m, n) with n fastest: CTAs sharing an activation tile run together,
+// and the M-tiles of one expert (sharing weight tiles) follow each other.
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    fc1_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                    PrefillArgs a) {
+  const int NT = 2 * a.I / kGemmBN;
+  const int mt = blockIdx.x / NT, nt = blockIdx.x % NT;
+  const int KG = a.H / 64;
+  const size_t scb = scale_chunk_bytes(2 * a.I, a.H, MOE_FP4_NVFP4);
+  const float* g13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * scb);
+  auto tile_of = [&]() {
+    GemmTile t;
+    t.valid = mt < *a.num_tiles;
+    if (!t.valid) return t;
+    const int e = a.tile_expert[mt];
+    t.a_row0 = kGemmBM * mt;
+    t.b_row0 = e * 2 * a.I + kGemmBN * nt;
+    t.a_sf = a.xsf + (size_t)mt * KG * kChunkBytes;
+    t.b_sf0 = a.s13 + (size_t)e * scb + (size_t)(2 * nt) * KG * kChunkBytes;
+    t.b_sf1 = t.b_sf0 + (size_t)KG * kChunkBytes;
+    return t;
+  };
+  auto epi = [&](uint32_t tmem_row, int row, const GemmTile& t) {
+    const int r = t.a_row0 + row;
+    const int e = a.tile_expert[mt];
+    const bool live = a.row_src[r] >= 0;
+    const float xg = live ? a.xG[r] : 0.f;
+    const float sgate = xg * g13[2 * e], sup = xg * g13[2 * e + 1];
+    __nv_bfloat16* hrow = a.hbuf + (size_t)r * a.I;
+#pragma unroll 1
+    for (int q = 0; q < 2; ++q) {    // the two 128-row resident tiles of this N tile
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {  // 32-pair chunks of the tile's 64 pairs
+        uint32_t g[32], u[32];
+        tmem_ld32(tmem_row + 128 * q + 32 * c, g);
+        tmem_ld32(tmem_row + 128 * q + 64 + 32 * c, u);
+        if (live) {
+          const int n0 = 64 * (2 * nt + q) + 32 * c;
+          uint32_t packed[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float h0 = silu(__uint_as_float(g[2 * j]) * sgate) * (__uint_as_float(u[2 * j]) * sup);
+            const float h1 = silu(__uint_as_float(g[2 * j + 1]) * sgate) * (__uint_as_float(u[2 * j + 1]) * sup);
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
+            packed[j] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(hrow + n0);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+        }
+      }
+    }
+  };
+  gemm_fp4_tile(&map_x, &map_w, a.H, a.status, tile_of, epi);
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    fc2_gemm_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
+                    PrefillArgs a) {
+  const int NT = a.H / kGemmBN;
+  const int mt = blockIdx.x / NT, nt = blockIdx.x % NT;
+  const int KG = a.I / 64;
+  const size_t scb = scale_chunk_bytes(a.H, a.I, MOE_FP4_NVFP4);
+  const float* g2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * scb);
+  auto tile_of = [&]() {
+    GemmTile t;
+    t.valid = mt < *a.num_tiles;
+    if (!t.valid) return t;
+    const int e = a.tile_expert[mt];
+    t.a_row0 = kGemmBM * mt;
+    t.b_row0 = e * a.H + kGemmBN * nt;
+    t.a_sf = a.hsf + (size_t)mt * KG * kChunkBytes;
+    t.b_sf0 = a.s2 + (size_t)e * scb + (size_t)(2 * nt) * KG * kChunkBytes;
+    t.b_sf1 = t.b_sf0 + (size_t)KG * kChunkBytes;
+    return t;
+  };
+  auto epi = [&](uint32_t tmem_row, int row, const GemmTile& t) {
+    const int r = t.a_row0 + row;
+    const int e = a.tile_expert[mt];
+    const int src = a.row_src[r];
+    const float f = src >= 0 ? a.hG[r] * g2[e] * a.tw[src] : 0.f;
+    float* dst = a.acc + (size_t)(src >= 0 ? src / a.top_k : 0) * a.H + kGemmBN * nt;
+#pragma unroll 1
+    for (int c = 0; c < kGemmBN / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld32(tmem_row + 32 * c, v);
+      if (src >= 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float* p = dst + 32 * c + 4 * i;
+          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p),
+                       "f"(__uint_as_float(v[4 * i]) * f), "f"(__uint_as_float(v[4 * i + 1]) * f),
+                       "f"(__uint_as_float(v[4 * i + 2]) * f), "f"(__uint_as_float(v[4 * i + 3]) * f)
+                       : "memory");
+        }
+      }
+    }
+  };
+  gemm_fp4_tile(&map_h, &map_w, a.I, a.status, tile_of, epi);
+}
+
+__global__ void cast_out_kernel(PrefillArgs a) {
+  const size_t n8 = (size_t)a.M * a.H / 8;
+  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n8; v += (size_t)gridDim.x * blockDim.x) {
+    const float4 p = reinterpret_cast<const float4*>(a.acc)[2 * v];
+    const float4 q = reinterpret_cast<const float4*>(a.acc)[2 * v + 1];
+    const __nv_bfloat162 b0 = __floats2bfloat162_rn(p.x, p.y), b1 = __floats2bfloat162_rn(p.z, p.w);
+    const __nv_bfloat162 b2 = __floats2bfloat162_rn(q.x, q.y), b3 = __floats2bfloat162_rn(q.z, q.w);
+    reinterpret_cast<uint4*>(a.out)[v] =
+        make_uint4(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1),
+                   *reinterpret_cast<const uint32_t*>(&b2), *reinterpret_cast<const uint32_t*>(&b3));
+  }
+}
+
+// Grouped routed rows -> unpadded permutation (test support).
+__global__ void route_perm_kernel(PrefillArgs a, int32_t* perm) {
+  const int e = blockIdx.x;
+  const int n = a.expert_off[e + 1] - a.expert_off[e];
+  for (int i = threadIdx.x; i < n; i += blockDim.x) perm[a.expert_off[e] + i] = a.row_src[a.expert_poff[e] + i];
+}
+__global__ void fill_i32_kernel(int32_t* p, int n, int v) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = v;
+}
+
+// One warp per row: the quantiser alone (test support), logical outputs.
+__global__ void debug_quant_kernel(const float* in, int rows, int K, uint8_t* q, uint8_t* s, float* G) {
+  const int r = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const float* row = in + (size_t)r * K;
+  const float g = quant_row_nvfp4(
+      K, [&](int b, float (&v)[16]) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = row[16 * b + i];
+      },
+      [&](int b, uint32_t sb, uint32_t w0, uint32_t w1) {
+        *reinterpret_cast<uint2*>(q + (size_t)r * (K / 2) + 8 * b) = make_uint2(w0, w1);
+        s[(size_t)r * (K / 16) + b] = (uint8_t)sb;
+      });
+  if ((threadIdx.x & 31) == 0) G[r] = g;
+}
+
+size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
+
+struct PrefillCarve {
+  size_t counts, block_base, expert_off, expert_poff, tile_expert, num_tiles, pos, row_src, xq, xsf, xG, hbuf, hq,
+      hsf, hG, acc, status, total;
+  int n_route_blocks, max_tiles;
+};
+
+PrefillCarve prefill_carve(int M, int E, int H, int I, int top_k) {
+  PrefillCarve c;
+  const size_t n = (size_t)M * top_k;
+  c.n_route_blocks = (int)((n + kRouteBlock - 1) / kRouteBlock);
+  c.max_tiles = (int)((n + 127) / 128) + E;
+  const size_t rows = (size_t)128 * c.max_tiles;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align_up(bytes);
+    return at;
+  };
+  c.status = take(256);
+  c.counts = take(sizeof(int) * c.n_route_blocks * E);
+  c.block_base = take(sizeof(int) * c.n_route_blocks * E);
+  c.expert_off = take(sizeof(int) * (E + 1));
+  c.expert_poff = take(sizeof(int) * (E + 1));
+  c.tile_expert = take(sizeof(int) * c.max_tiles);
+  c.num_tiles = take(sizeof(int));
+  c.pos = take(sizeof(int) * n);
+  c.row_src = take(sizeof(int) * rows);
+  c.xq = take(rows * H / 2);
+  c.xsf = take(rows * H / 16);
+  c.xG = take(sizeof(float) * rows);
+  c.hbuf = take(rows * I * 2);
+  c.hq = take(rows * I / 2);
+  c.hsf = take(rows * I / 16);
+  c.hG = take(sizeof(float) * rows);
+  c.acc = take(sizeof(float) * M * H);
+  c.total = o;
+  return c;
+}
+
+PrefillArgs prefill_args(const PrefillCarve& c, void* ws, int M, int E, int H, int I, int top_k) {
+  char* b = static_cast<char*>(ws);
+  PrefillArgs a;
+  a.x = nullptr;
+  a.ids = nullptr;
+  a.tw = nullptr;
+  a.s13 = a.s2 = nullptr;
+  a.out = nullptr;
+  a.M = M;
+  a.E = E;
+  a.H = H;
+  a.I = I;
+  a.top_k = top_k;
+  a.n_entries = M * top_k;
+  a.n_route_blocks = c.n_route_blocks;
+  a.max_tiles = c.max_tiles;
+  a.status = reinterpret_cast<uint32_t*>(b + c.status);
+  a.counts = reinterpret_cast<int*>(b + c.counts);
+  a.block_base = reinterpret_cast<int*>(b + c.block_base);
+  a.expert_off = reinterpret_cast<int*>(b + c.expert_off);
+  a.expert_poff = reinterpret_cast<int*>(b + c.expert_poff);
+  a.tile_expert = reinterpret_cast<int*>(b + c.tile_expert);
+  a.num_tiles = reinterpret_cast<int*>(b + c.num_tiles);
+  a.pos = reinterpret_cast<int*>(b + c.pos);
+  a.row_src = reinterpret_cast<int*>(b + c.row_src);
+  a.xq = reinterpret_cast<uint8_t*>(b + c.xq);
+  a.xsf = reinterpret_cast<uint8_t*>(b + c.xsf);
+  a.xG = reinterpret_cast<float*>(b + c.xG);
+  a.hbuf = reinterpret_cast<__nv_bfloat16*>(b + c.hbuf);
+  a.hq = reinterpret_cast<uint8_t*>(b + c.hq);
+  a.hsf = reinterpret_cast<uint8_t*>(b + c.hsf);
+  a.hG = reinterpret_cast<float*>(b + c.hG);
+  a.acc = reinterpret_cast<float*>(b + c.acc);
+  return a;
+}
+
+cudaError_t launch_route(PrefillArgs& a, cudaStream_t st) {
+  route_count_kernel<<<a.n_route_blocks, kRouteBlock, sizeof(int) * a.E, st>>>(a);
+  route_scan_kernel<<<1, 1024, 0, st>>>(a);
+  route_scatter_kernel<<<a.n_route_blocks, 32, sizeof(int) * a.E, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- host side
+size_t prefill_workspace_bytes(int M, int E, int H, int I, int top_k) {
+  return prefill_carve(M, E, H, I, top_k).total;
+}
+
+cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
+                           const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
+                           void* ws, cudaStream_t st, int* cu_err) {
+  const PrefillCarve c = prefill_carve(M, E, H, I, top_k);
+  PrefillArgs a = prefill_args(c, ws, M, E, H, I, top_k);
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.ids = ids;
+  a.tw = tw;
+  a.s13 = static_cast<const uint8_t*>(s13);
+  a.s2 = static_cast<const uint8_t*>(s2);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  const size_t rows = (size_t)128 * c.max_tiles;
+  CUtensorMap mx, mw13, mh, mw2;
+  CUresult r = make_fp4_map(&mx, a.xq, (uint64_t)H / 2, rows, kGemmBM);
+  if (r == CUDA_SUCCESS) r = make_fp4_map(&mw13, w13, (uint64_t)H / 2, (uint64_t)E * 2 * I, kGemmBN);
+  if (r == CUDA_SUCCESS) r = make_fp4_map(&mh, a.hq, (uint64_t)I / 2, rows, kGemmBM);
+  if (r == CUDA_SUCCESS) r = make_fp4_map(&mw2, w2, (uint64_t)I / 2, (uint64_t)E * H, kGemmBN);
+  if (r != CUDA_SUCCESS) {
+    *cu_err = (int)r;
+    return cudaErrorInvalidValue;
+  }
+  static bool attrs = false;
+  if (!attrs) {
+    cudaError_t e = cudaFuncSetAttribute(fc1_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fc2_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    if (e != cudaSuccess) return e;
+    attrs = true;
+  }
+  cudaError_t e = launch_route(a, st);
+  if (e != cudaSuccess) return e;
+  quant_x_kernel<<<(M + 7) / 8, 256, 0, st>>>(a);
+  fc1_gemm_kernel<<<c.max_tiles * (2 * I / kGemmBN), kGemmThreads, kGemmSmem, st>>>(mx, mw13, a);
+  quant_h_kernel<<<(int)((rows + 7) / 8), 256, 0, st>>>(a);
+  fc2_gemm_kernel<<<c.max_tiles * (H / kGemmBN), kGemmThreads, kGemmSmem, st>>>(mh, mw2, a);
+  cast_out_kernel<<<4 * 152, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+size_t debug_route_workspace_bytes(int M, int E, int top_k) { return prefill_carve(M, E, 256, 256, top_k).total; }
+
+cudaError_t launch_debug_route(const int32_t* ids, int M, int E, int top_k, int32_t* perm, int32_t* expert_offset,
+                               void* ws, cudaStream_t st) {
+  const PrefillCarve c = prefill_carve(M, E, 256, 256, top_k);
+  PrefillArgs a = prefill_args(c, ws, M, E, 256, 256, top_k);
+  a.ids = ids;
+  cudaError_t e = launch_route(a, st);
+  if (e != cudaSuccess) return e;
+  fill_i32_kernel<<<64, 256, 0, st>>>(perm, M * top_k, -1);
+  route_perm_kernel<<<E, 256, 0, st>>>(a, perm);
+  return cudaMemcpyAsync(expert_offset, a.expert_off, sizeof(int) * (E + 1), cudaMemcpyDeviceToDevice, st);
+}
+
+cudaError_t launch_debug_quant(const float* in, int rows, int K, uint8_t* q, uint8_t* s, float* G, cudaStream_t st) {
+  debug_quant_kernel<<<(rows + 7) / 8, 256, 0, st>>>(in, rows, K, q, s, G);
   return cudaGetLastError();
 }
 

@@ -152,6 +152,11 @@ MOE_FP4_API int moe_fp4_release_workspace(void);
  * bitwise deterministic; the prefill band sums routed rows into an FP32
  * token accumulator with atomic adds, so its low-order bits may vary run to
  * run.
+ *
+ * Prefill band (M > 8): NVFP4 only, I % 256 == 0, E <= 4096 (else
+ * MOE_FP4_EUNSUPPORTED).  Activations are quantised to NVFP4 per row (x per
+ * token, h = SiLU(gate)*up per routed row after BF16 staging) so both GEMMs
+ * run on the FP4 tensor cores.
  */
 MOE_FP4_API int moe_fp4_forward(const void *x_bf16, const void *w13, const void *s13, const void *w2, const void *s2,
                     const int32_t *topk_ids, const float *topk_weights, void *out_bf16, int M, int E, int H, int I,
@@ -225,11 +230,23 @@ MOE_FP4_API int moe_fp4_debug_gemm(const void *a_q, const void *a_sf, const void
  * perm[r] = t*top_k + j for grouped row r, and expert_offset[e] ..
  * expert_offset[e+1] delimit expert e's rows (expert_offset has E+1
  * entries).  perm has M*top_k entries; those past expert_offset[E] are -1.
- * Uses `workspace` (moe_fp4_workspace_bytes(M, ...) bytes, zero-filled before
- * first use).
+ * Uses `workspace` of moe_fp4_debug_route_workspace_bytes(M, E, top_k)
+ * bytes.  E <= 4096.
  */
-MOE_FP4_API int moe_fp4_debug_route(const int32_t *topk_ids, int M, int E, int top_k, int32_t *perm, int32_t *expert_offset,
-                        void *workspace, size_t workspace_bytes, void *stream);
+MOE_FP4_API int moe_fp4_debug_route(const int32_t *topk_ids, int M, int E, int top_k, int32_t *perm,
+                                    int32_t *expert_offset, void *workspace, size_t workspace_bytes, void *stream);
+MOE_FP4_API size_t moe_fp4_debug_route_workspace_bytes(int M, int E, int top_k);
+
+/*
+ * Test support: the prefill band's NVFP4 activation quantiser on FP32 rows
+ * in[rows][K] (K % 16 == 0): q [rows][K/2] packed E2M1 (low nibble = even
+ * element), s [rows][K/16] E4M3 scale bytes, G [rows] FP32 multipliers, by
+ *   G = amax/(6*448) (1 for an all-zero row), s = e4m3_rn_satfinite(bmax/(6G)),
+ *   q = e2m1_rn_satfinite(a/(s*G)) (0 where s*G == 0),
+ * each step an IEEE FP32 operation.
+ */
+MOE_FP4_API int moe_fp4_debug_quant_rows(const float *in, int rows, int K, uint8_t *q, uint8_t *s, float *G,
+                                         void *stream);
 
 #ifdef __cplusplus
 }

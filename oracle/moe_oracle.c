@@ -308,6 +308,20 @@ void moe_oracle_quant_nvfp4_row(const float *a, int K, uint8_t *q, uint8_t *s, f
     }
 }
 
+/* Round an FP32 value to the nearest BF16 (ties to even), returned as FP32.
+ * The prefill band stages h = SiLU(gate)*up in BF16 between FC1 and the h
+ * quantiser; the mirror takes the same rounding from an FP32 value. */
+static float bf16_round(float v)
+{
+    uint32_t u;
+    memcpy(&u, &v, 4);
+    if ((u & 0x7f800000u) == 0x7f800000u) return v; /* inf / nan unchanged */
+    uint32_t lsb = (u >> 16) & 1u;
+    u = (u + 0x7fffu + lsb) & 0xffff0000u;
+    memcpy(&v, &u, 4);
+    return v;
+}
+
 /* Dequantise a quantised row back to FP64: q * s * G. */
 static void dequant_nvfp4_row(const uint8_t *q, const uint8_t *s, float G, int K, double *out)
 {
@@ -320,7 +334,8 @@ static void dequant_nvfp4_row(const uint8_t *q, const uint8_t *s, float G, int K
 
 /* Prefill band (mirrored quantisation), for the tokens listed (NULL = all):
  *   x_q = quant(x_t); for each valid slot: g,u = FC1(dequant(x_q)) in FP64;
- *   h = SiLU(g)*u rounded to FP32; h_q = quant(h); y = FC2(dequant(h_q));
+ *   h = SiLU(g)*u rounded to FP32, then to BF16; h_q = quant(h);
+ *   y = FC2(dequant(h_q));
  *   out_t = sum_j w_j y.
  * Also returns (optionally) the quantised x rows of the listed tokens. */
 int moe_oracle_forward_prefill(const uint16_t *x_bf16, const uint8_t *w13, const uint8_t *s13, const float *g13,
@@ -364,7 +379,7 @@ int moe_oracle_forward_prefill(const uint16_t *x_bf16, const uint8_t *w13, const
                 int e = topk_ids[(size_t)t * top_k + j];
                 if (e < 0 || e >= E) continue;
                 expert_fc1(xd, w13, s13, g13, e, H, I, fmt, h);
-                for (int n = 0; n < I; ++n) hf[n] = (float)h[n];
+                for (int n = 0; n < I; ++n) hf[n] = bf16_round((float)h[n]);
                 float hG;
                 moe_oracle_quant_nvfp4_row(hf, I, hq, hs, &hG);
                 dequant_nvfp4_row(hq, hs, hG, I, hd);
