@@ -250,7 +250,8 @@ static uint8_t e4m3_from_float_pos(float v)
 }
 
 /* Round to the E2M1 grid, nearest-even on the code, saturating at +-6.
- * Returns the 4-bit code. */
+ * Like IEEE rounding it keeps the input's sign, so a negative value that
+ * rounds to zero gives -0 (code 8).  Returns the 4-bit code. */
 static uint8_t e2m1_from_float(float v)
 {
     double dv = fabs((double)v);
@@ -263,7 +264,7 @@ static uint8_t e2m1_from_float(float v)
             best = c;
         }
     }
-    if (best != 0 && v < 0.0f) best |= 8;
+    if (signbit(v)) best |= 8; /* the sign survives rounding: small negatives give -0 */
     return (uint8_t)best;
 }
 

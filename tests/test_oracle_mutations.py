@@ -44,8 +44,9 @@ MUTATIONS = {
     "fc2_index_transposed": ("for (int n = 0; n < I; ++n) acc += weight_at(nib, sc, I, fmt, gd, m, n) * h[n];",
                              "for (int n = 0; n < I; ++n) acc += weight_at(nib, sc, I, fmt, gd, m, (n + 1) % I) * h[n];"),
     "quant_global_rule": ("volatile float six448 = 6.0f * 448.0f;", "volatile float six448 = 6.0f * 256.0f;"),
-    "quant_tie_rule": ("if (d < bestd || (d == bestd && (c & 1) == 0)) {\n            bestd = d;\n            best = c;\n        }\n    }\n    if (best != 0",
-                       "if (d <= bestd) {\n            bestd = d;\n            best = c;\n        }\n    }\n    if (best != 0"),
+    "quant_tie_rule": ("if (d < bestd || (d == bestd && (c & 1) == 0)) {\n            bestd = d;\n            best = c;\n        }\n    }\n    if (signbit(v))",
+                       "if (d <= bestd) {\n            bestd = d;\n            best = c;\n        }\n    }\n    if (signbit(v))"),
+    "quant_negative_zero": ("if (signbit(v)) best |= 8;", "if (best != 0 && v < 0.0f) best |= 8;"),
     "route_order": ("for (int t = 0; t < M; ++t)\n            for (int j = 0; j < top_k; ++j)\n                if (topk_ids[(size_t)t * top_k + j] == e) perm[r++] = t * top_k + j;",
                     "for (int j = 0; j < top_k; ++j)\n            for (int t = 0; t < M; ++t)\n                if (topk_ids[(size_t)t * top_k + j] == e) perm[r++] = t * top_k + j;"),
 }
