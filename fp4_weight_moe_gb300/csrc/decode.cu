@@ -1,4 +1,6 @@
-// Decode band (M <= 8 tokens): the layer as the HBM-bound GEMV it is.
+// Decode band (M <= 8 tokens) for MXFP4 weights: the layer as the HBM-bound
+// GEMV it is, on the warp-level tensor-core MMA.  (NVFP4 weights take the
+// tcgen05 path in decode_tc.cu; launch_decode below dispatches.)
 //
 // Prior art: the pages' tiny-decode kernel pair (b12x PR #22, "rp-native
 // tiny-decode kernel for w4a8_mx (M=1)", section What) -- FC1 streams the
@@ -481,18 +483,33 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fc2_kernel(DecodeParams p)
 }
 
 // ---------------------------------------------------------------- host side
-// Scratch: h, [M*top_k][M][I] FP32.
+bool decode_tc_supported(int fmt);
+cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
+                             const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
+                             float* h, uint32_t* status, int num_sms, cudaStream_t st, int* cu_err);
+
+static size_t decode_h_bytes(int M_max, int I, int top_k) {
+  const size_t n = (size_t)M_max * top_k;
+  return (sizeof(float) * n * M_max * I + 255) & ~(size_t)255;
+}
+
+// Scratch: h, [M*top_k][M][I] FP32, then a 256-byte status block (bit flags
+// of bounded waits that gave up; sticky).
 size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int num_sms) {
   (void)H;
   (void)num_sms;
-  const size_t n = (size_t)M_max * top_k;
-  return (sizeof(float) * n * M_max * I + 255) & ~(size_t)255;
+  return decode_h_bytes(M_max, I, top_k) + 256;
 }
 
 cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                           const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
                           int fmt, void* ws, int num_sms, cudaStream_t st) {
-  (void)num_sms;
+  if (decode_tc_supported(fmt)) {
+    int cu = 0;
+    uint32_t* status = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + decode_h_bytes(M, I, top_k));
+    return launch_decode_tc(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, static_cast<float*>(ws), status,
+                            num_sms, st, &cu);
+  }
   DecodeParams p;
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.w13 = static_cast<const uint8_t*>(w13);

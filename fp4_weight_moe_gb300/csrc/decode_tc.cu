@@ -1,0 +1,754 @@
+// Decode band (M <= 8 tokens) for NVFP4 weights on the 5th-generation tensor
+// cores: the expert weights are streamed by TMA straight into shared memory
+// and consumed by tcgen05.mma kind::mxf4nvf4 with their own E4M3 block scales,
+// so no instruction is spent decoding a weight nibble.
+//
+// Prior art: the pages' tiny-decode kernel pair (b12x PR #22, "rp-native
+// tiny-decode kernel for w4a8_mx (M=1)", section What): FC1 streams the
+// routed experts' packed weights and writes an FP32 gate/up intermediate,
+// FC2 applies the activation and performs the router-weighted sum; two plain
+// launches rather than one cooperative launch (section Notes).  The routing is
+// read directly by the GEMM kernels (the small-batch "direct" path of
+// flashinfer PR #4285, "sync SM12x NVFP4 fused-MoE kernels"), ids outside
+// [0, E) contribute exactly zero (b12x PR #311, conversation).
+//
+// The tensor-core MMA wants both operands in FP4.  The activations (BF16 x
+// for FC1, FP32 h for FC2) enter as a sum of kTerms NVFP4 terms:
+//   r_1 = a;  for t = 1..T:  term_t = NVFP4(r_t; G_t),  r_{t+1} = r_t - term_t
+// where NVFP4(r; G) is the per-16-element quantisation with block scale
+// s = e4m3_rn_satfinite(bmax / (6 G)) and codes e2m1_rn_satfinite(r / (s G)),
+// and G_1 is the smallest power of two >= amax / (6 * 448) over the 256
+// values of one (token, K stage), G_{t+1} = G_t / 4.  Every term is exact in
+// FP32 and the dropped remainder r_{T+1} is about 10^-T of the block maximum
+// (four terms: ~1e-4 relative error of the dot products, below the BF16
+// rounding of the inputs).  Each (token, term) is one B row of the MMA
+// (N = kTerms * M rounded up to 16), so for M <= 4 the terms ride in columns
+// the N = 16 minimum would leave empty.  Each K stage ("item") accumulates
+// into its own group of tensor-memory columns; the accumulator warps fold
+// the group with its multipliers into FP32 registers, in item order, and
+// release it for the item four stages later.
+//
+// FC1: a CTA owns one (route slot, 128-row w13 tile = 64 gate/up pairs, K
+//      range); the K ranges of one tile form a thread-block cluster.  Each
+//      CTA sends its partial rows to the CTA that owns them with asynchronous
+//      distributed-shared-memory stores counted on the owner's mbarrier (no
+//      cluster-wide barrier at the end); the owner sums them in rank order and
+//      writes h = SiLU(gate) * up * (router weight) * (down multiplier) in
+//      FP32 (FC2 is linear in h, so it only sums).
+// FC2: a CTA owns one (128-row w2 tile, share of the (route slot, K stage)
+//      items); the CTAs of one tile form a cluster and reduce the same way;
+//      each output element is written once, in BF16.  Both kernels use
+//      programmatic dependent launch: FC1's prologue overlaps the previous
+//      kernel, FC2's weight stream overlaps FC1 (at most one CTA of each per
+//      SM, so they fit side by side); only the warps that read h wait for FC1.
+//
+// The tensor cores issue an MMA about every hundred cycles however small N
+// is, so with N = 16 the issue, not the arithmetic, sets the pace: the MMAs
+// are issued by two converged warps (alternate items), and the scale factors
+// reach tensor memory through tcgen05.st from the warps that produce or
+// receive them instead of through tcgen05.cp from the issuing thread.
+//
+// Roles in a 352-thread CTA: warp 0 lane 0 issues the TMA weight tiles and
+// scale chunks into a 4-deep ring; warps 1-2 issue the MMAs (alternate
+// items; warp 1 also owns the tensor-memory allocation); warps 3-6 build the
+// activation terms (B operand, one warp per (stage, token)) and write their
+// scales into tensor memory; warps 7-10 write the weight scales into tensor
+// memory and drain the accumulator groups.  At most two CTAs share an SM
+// (shared memory), so their 2 x 256 tensor-memory columns always fit and no
+// allocation waits on another grid.
+#include "common.cuh"
+#include "tcgen05.cuh"
+
+namespace moe_fp4 {
+
+CUresult make_fp4_map(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint32_t box_rows);
+
+namespace {
+
+constexpr int kTerms = 4;
+constexpr int kRing = 4;                               // ring slots = accumulator groups
+constexpr int kGSlots = 2 * kRing;                     // term-multiplier sets in flight
+constexpr int kMmaWarp0 = 1, kMmaWarps = 2;            // warps 1..2 issue the MMAs
+constexpr int kQuantWarp0 = 3, kQuantWarps = 4;        // warps 3..6 build B
+constexpr int kEpiWarp0 = 7;                           // warps 7..10 drain the accumulator
+constexpr int kTcThreads = 32 * (kEpiWarp0 + 4);
+constexpr int kMaxN = 32;                              // kTerms * 8 tokens
+constexpr uint32_t kSlotA = 128 * 128;                 // 128 rows x 256 K (FP4)
+constexpr uint32_t kSlotB = kMaxN * 128;               // N rows x 256 K
+constexpr uint32_t kSlotSF = 4 * kChunkBytes;          // 4 K-groups
+constexpr uint32_t kSlotBytes = kSlotA + kSlotB + 2 * kSlotSF;  // 24 KB, 1024-aligned
+constexpr int kMaxSlotsTc = 128;
+constexpr uint32_t kTmemColsTc = 256;
+constexpr uint32_t kTmemSFBase = 32 * kRing;           // accumulator groups in [0, 128)
+
+constexpr int kPartFloats = 1280;  // split * M * 2 * ceil(64 / split) <= 1120 (FC1); M * 128 (FC2)
+
+struct SmemTc {
+  float part[kPartFloats];         // partial sums received from the cluster
+  float G[kGSlots][8][kTerms];     // term multipliers per (item, token)
+  int ids[kMaxSlotsTc];
+  float tw[kMaxSlotsTc];
+  int own[kMaxSlotsTc];            // FC2: first slot naming each valid expert, in slot order
+  int own_cnt[4];                  // FC2: owners per 32-slot chunk
+  int expert;                      // FC1: this CTA's expert (-1: nothing to do)
+  float wtok[8];                   // FC1: router weight of the expert per token
+  uint32_t routed;                 // FC1: tokens routed to the expert (bit mask)
+  uint64_t fullA[kRing];           // weight tile + its scale chunks landed (TMA)
+  uint64_t fullB[kRing];           // activation terms + their scales in place (builders)
+  uint64_t sfa[kRing];             // weight scales copied to tensor memory
+  uint64_t done[kRing];            // MMAs of the slot complete (slot and group reusable)
+  uint64_t acce[kRing];            // accumulator group drained
+  uint64_t gready[kGSlots];        // term multipliers written
+  uint64_t bsf;                    // a wave's B scales are staged (all builder warps)
+  uint64_t red;                    // every partial row this CTA reduces has landed
+  uint32_t tmem;
+};
+constexpr uint32_t kTcSmem = kRing * kSlotBytes + sizeof(SmemTc) + 1024;
+
+struct TcArgs {
+  const __nv_bfloat16* x;
+  const int32_t* ids;
+  const float* tw;
+  const uint8_t* s13;
+  const uint8_t* s2;
+  float* h;  // [n_slots][M][I]
+  __nv_bfloat16* out;
+  uint32_t* status;
+  int M, E, H, I, top_k, n_slots;
+  int split;  // cluster size: FC1 K ranges per w13 tile, FC2 CTAs per w2 tile
+  int N;      // B rows per item (accumulator columns)
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// Asynchronous FP32 store to the same shared-memory offset in another CTA of
+// the cluster; its completion is counted (4 bytes) on that CTA's mbarrier.
+__device__ __forceinline__ void st_async_peer_f32(float* local, uint64_t* local_bar, uint32_t rank, float v) {
+  uint32_t ra, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(local_bar)), "r"(rank));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(ra),
+               "r"(__float_as_uint(v)), "r"(rb)
+               : "memory");
+}
+
+
+__device__ __forceinline__ uint32_t e4m3_rn_satf(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+  return r & 0xffu;
+}
+// Two E2M1 codes, `lo` in the low nibble.
+__device__ __forceinline__ uint32_t e2m1x2_rn_satf(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}" : "=h"(r) : "f"(hi), "f"(lo));
+  return r & 0xffu;
+}
+
+// Smallest power of two >= amax / 2688 (0 for amax == 0).
+__device__ __forceinline__ float term_g1(float amax) {
+  if (!(amax > 0.f)) return 0.f;
+  const float q = amax * (1.0f / 2688.0f) * 1.0000002f;
+  uint32_t b = __float_as_uint(q);
+  uint32_t e = b >> 23;
+  if (b & 0x7fffffu) ++e;
+  if (e < 1u) e = 1u;
+  if (e > 254u) e = 254u;
+  return __uint_as_float(e << 23);
+}
+
+// Byte offset of 16-element block b of B row n in a 128-byte-swizzled tile.
+__device__ __forceinline__ uint32_t b_tile_offset(int n, int b) {
+  return (uint32_t)(n * 128 + ((((b >> 1) ^ (n & 7)) & 7) << 4) + ((b & 1) << 3));
+}
+// Byte offset of the scale of (B row n < 32, block b of the 256-K stage) in
+// the item's B scale staging: row n's 16 scale bytes, 64-K group g in bytes
+// 4g .. 4g+3 (the 32-bit word tensor memory holds per row and group).
+__device__ __forceinline__ uint32_t sf_offset(int n, int b) { return (uint32_t)((n & 31) * 16 + b); }
+
+// 1/g for a power of two g in [2^-126, 2^126] (exact).
+__device__ __forceinline__ float pow2_inv(float g) { return __uint_as_float((254u << 23) - __float_as_uint(g)); }
+
+__device__ __forceinline__ float rcp_approx(float v) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// The kTerms NVFP4 terms of one token's 256-value K stage, built by one warp:
+// lane l holds values 8l .. 8l+7 (half l%2 of 16-element block l/2).  The
+// term multipliers are G1 * 4^-t.  Lane l writes its 4 code bytes of each
+// term's B row token*kTerms + t, the even lane of a block its scale byte.
+// Any quotient rounding is corrected by the next term (the residual is
+// formed from the exact term values), so the reciprocals are approximate.
+__device__ __forceinline__ void emit_stage_terms(float (&v)[8], float G1, uint8_t* btile, uint8_t* sfb, int token,
+                                                 int lane, bool store) {
+  const int b = lane >> 1, half = lane & 1;
+  float g = G1;
+#pragma unroll
+  for (int t = 0; t < kTerms; ++t, g *= 0.25f) {
+    const int n = token * kTerms + t;
+    float m01 = fmaxf(fabsf(v[0]), fabsf(v[1])), m23 = fmaxf(fabsf(v[2]), fabsf(v[3]));
+    float m45 = fmaxf(fabsf(v[4]), fabsf(v[5])), m67 = fmaxf(fabsf(v[6]), fabsf(v[7]));
+    float bm = fmaxf(fmaxf(m01, m23), fmaxf(m45, m67));
+    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+    uint32_t sc = 0, w = 0;
+    if (g > 0.f) {
+      const float inv_g = pow2_inv(g);
+      sc = e4m3_rn_satf(bm * (inv_g * (1.0f / 6.0f)));
+      const float s = e4m3_to_float(sc);
+      if (s > 0.f) {
+        const float sg = s * g, inv = rcp_approx(s) * inv_g;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w |= e2m1x2_rn_satf(v[2 * j] * inv, v[2 * j + 1] * inv) << (8 * j);
+        uint32_t hv[4];
+        e2m1x8_to_half2x4(w, hv);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 d = half2_bits_to_float2(hv[j]);
+          v[2 * j] = fmaf(-d.x, sg, v[2 * j]);
+          v[2 * j + 1] = fmaf(-d.y, sg, v[2 * j + 1]);
+        }
+      } else {
+        sc = 0;
+      }
+    }
+    if (store) {
+      *reinterpret_cast<uint32_t*>(btile + b_tile_offset(n, b) + 4 * half) = w;
+      if (!half) sfb[sf_offset(n, b)] = (uint8_t)sc;
+    }
+  }
+}
+
+// Loads issued where they stand (volatile): the activation prefetch must not
+// be moved below the barriers that follow it.
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ float ld_nc_f32(const void* p) {
+  float r;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(r) : "l"(p));
+  return r;
+}
+// 8 consecutive BF16 / FP32 activations as FP32.
+__device__ __forceinline__ void load_bf16x8(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 u = ld_nc_v4(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void load_f32x8(const float* p, float (&v)[8]) {
+  const uint4 u0 = ld_cg_v4(p), u1 = ld_cg_v4(p + 4);
+  v[0] = __uint_as_float(u0.x);
+  v[1] = __uint_as_float(u0.y);
+  v[2] = __uint_as_float(u0.z);
+  v[3] = __uint_as_float(u0.w);
+  v[4] = __uint_as_float(u1.x);
+  v[5] = __uint_as_float(u1.y);
+  v[6] = __uint_as_float(u1.z);
+  v[7] = __uint_as_float(u1.w);
+}
+
+// FC1 (kFc2 = false) and FC2 (kFc2 = true).
+template <bool kFc2>
+__global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_constant__ CUtensorMap map_w, TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  SmemTc& S = *reinterpret_cast<SmemTc*>(ring + kRing * kSlotBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int M = a.M, H = a.H, I = a.I, n = a.n_slots, N = a.N;
+  const int split = a.split;
+  const uint32_t rank = cluster_rank();
+  const int unit = blockIdx.x / split;  // FC1: slot * tiles1 + tile; FC2: w2 row tile
+  const int tiles1 = I / 64, ns2 = (I + 255) / 256;
+  const bool is_quant = warp >= kQuantWarp0 && warp < kQuantWarp0 + kQuantWarps;
+  const bool is_epi = warp >= kEpiWarp0;
+
+  // ---- prologue: touches no input
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&S.fullA[s], 1);
+      mbar_init(&S.fullB[s], kQuantWarps);
+      mbar_init(&S.sfa[s], 4);
+      mbar_init(&S.done[s], 1);
+      mbar_init(&S.acce[s], 4);
+    }
+    for (int s = 0; s < kGSlots; ++s) mbar_init(&S.gready[s], kQuantWarps);
+    mbar_init(&S.bsf, kQuantWarps);
+    mbar_init(&S.red, 1);
+    // the partial rows this CTA will receive: FC1 owns pairs p = rank mod
+    // split (gate and up rows), FC2 rows r = rank mod split; every CTA of
+    // the cluster sends its share of them
+    const int own = kFc2 ? (128 - (int)rank + split - 1) / split : 2 * ((64 - (int)rank + split - 1) / split);
+    mbar_arrive_expect_tx(&S.red, (uint32_t)(split * own * M * 4));
+    fence_mbar_init();
+    tma_prefetch_desc(&map_w);
+  }
+  // cluster phase 1: this CTA runs and its barriers are initialised
+  // (awaited before any remote store)
+  cluster_arrive_release();
+  if (warp == kMmaWarp0) tmem_alloc(&S.tmem, kTmemColsTc);
+  // FC1 waits for whatever produced x and the routing; FC2 is launched by FC1
+  // only after that point, so both may read the routing from here on.
+  if (!kFc2) pdl_wait();
+  pdl_launch_dependents();
+
+  int slot1 = 0, tile = 0, k0 = 0, n_items = 0, n_own = 0;
+  auto item_slot = [&](int i) { return kFc2 ? S.own[((int)rank + split * i) % n_own] : slot1; };
+  auto item_stage = [&](int i) { return kFc2 ? ((int)rank + split * i) / n_own : k0 + i; };
+  auto item_groups = [&](int i) {
+    if (!kFc2) return 4;
+    const int rem = I / 64 - 4 * item_stage(i);
+    return rem < 4 ? rem : 4;
+  };
+  const uint64_t KG = kFc2 ? (uint64_t)(I / 64) : (uint64_t)(H / 64);
+  auto issue = [&](int i, int e) {  // TMA of item i's weight tile and scale chunks
+    const int sl = i % kRing, st = item_stage(i), ng = item_groups(i);
+    uint8_t* slotp = ring + sl * kSlotBytes;
+    mbar_arrive_expect_tx(&S.fullA[sl], kSlotA + (uint32_t)ng * kChunkBytes);
+    int row0;
+    const uint8_t* sfa;
+    if (!kFc2) {
+      row0 = e * 2 * I + tile * 128;
+      sfa = a.s13 + (((uint64_t)e * tiles1 + tile) * KG + 4 * (uint64_t)st) * kChunkBytes;
+    } else {
+      row0 = e * H + unit * 128;
+      sfa = a.s2 + (((uint64_t)e * (H / 128) + unit) * KG + 4 * (uint64_t)st) * kChunkBytes;
+    }
+    tma_load_2d(slotp, &map_w, st * 128, row0, &S.fullA[sl]);
+    bulk_load(slotp + kSlotA + kSlotB, sfa, (uint32_t)ng * kChunkBytes, &S.fullA[sl]);
+  };
+
+  float pre[8];
+  bool pre_ok = false;
+  const int qw = warp - kQuantWarp0;  // quantiser warp: one (item, token) per round
+  if (!kFc2) {
+    slot1 = unit / tiles1;
+    tile = unit % tiles1;
+    const int nk = H / 256;
+    k0 = (int)rank * nk / split;
+    n_items = ((int)rank + 1) * nk / split - k0;
+    // the first activation blocks need nothing else: start their loads
+    if (is_quant && qw < (n_items < kRing ? n_items : kRing) * M) {
+      load_bf16x8(a.x + (size_t)(qw % M) * H + (k0 + qw / M) * 256 + lane * 8, pre);
+      pre_ok = true;
+    }
+  }
+  if (warp == 0) {
+    for (int j = lane; j < n; j += 32) {
+      S.ids[j] = __ldg(a.ids + j);
+      S.tw[j] = __ldg(a.tw + j);
+    }
+    __syncwarp();
+    if (!kFc2) {
+      // does an earlier slot name the same expert?  If not, stream the first
+      // ring wave of weight tiles right away.
+      const int e = S.ids[slot1];
+      bool ok = e >= 0 && e < a.E;
+      for (int base = 0; ok && base < slot1; base += 32) {
+        const int j = base + lane;
+        ok = !__any_sync(0xffffffffu, j < slot1 && S.ids[j] == e);
+      }
+      if (lane == 0) {
+        S.expert = ok ? e : -1;
+        if (ok)
+          for (int i = 0; i < n_items && i < kRing; ++i) issue(i, e);
+      }
+      // router weight of this expert per token
+      float wt = 0.f;
+      bool rt = false;
+      if (lane < M)
+        for (int k = 0; k < a.top_k; ++k)
+          if (S.ids[lane * a.top_k + k] == e) {
+            wt += S.tw[lane * a.top_k + k];
+            rt = true;
+          }
+      const uint32_t rm = __ballot_sync(0xffffffffu, rt);
+      if (lane < M) S.wtok[lane] = wt;
+      if (lane == 0) S.routed = rm;
+    }
+  }
+  tc_fence_before();
+  __syncwarp();  // converge every warp before the CTA barrier (it counts whole warps)
+  __syncthreads();
+  tc_fence_after();
+
+  int e1 = -1;
+  float g_gate = 0.f, g_up = 0.f, g_down = 0.f;
+  if (!kFc2) {
+    e1 = S.expert;
+    if (e1 < 0) {  // every CTA of the cluster shares the slot: all leave
+      if (warp == kMmaWarp0) tmem_dealloc(S.tmem, kTmemColsTc);
+      return;
+    }
+    const float* gl13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * tiles1 * (H / 64) * kChunkBytes);
+    const float* gl2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * (H / 128) * (I / 64) * kChunkBytes);
+    g_gate = ld_nc_f32(gl13 + 2 * e1);
+    g_up = ld_nc_f32(gl13 + 2 * e1 + 1);
+    g_down = ld_nc_f32(gl2 + e1);
+  } else {
+    // owners: the first slot naming each valid expert, in slot order
+    bool own_j = false;
+    uint32_t bal = 0;
+    const int j = 32 * warp + lane;
+    if (warp < 4) {
+      const int id = j < n ? S.ids[j] : -1;
+      const bool valid = j < n && id >= 0 && id < a.E;
+      const uint32_t mm = __match_any_sync(0xffffffffu, valid ? id : -1 - lane);
+      bool dup = (mm & ((1u << lane) - 1u)) != 0;
+      for (int c = 0; valid && !dup && c < warp; ++c)
+        for (int k = 0; k < 32; ++k) dup = dup || S.ids[32 * c + k] == id;
+      own_j = valid && !dup;
+      bal = __ballot_sync(0xffffffffu, own_j);
+      if (lane == 0) S.own_cnt[warp] = __popc(bal);
+    }
+    __syncwarp();
+    __syncthreads();
+    if (own_j) {
+      int base = 0;
+      for (int c = 0; c < warp; ++c) base += S.own_cnt[c];
+      S.own[base + __popc(bal & ((1u << lane) - 1u))] = j;
+    }
+    n_own = S.own_cnt[0] + S.own_cnt[1] + S.own_cnt[2] + S.own_cnt[3];
+    __syncwarp();
+    __syncthreads();
+    // items (owner, K stage) stage-major, dealt round-robin to the cluster
+    const int total = n_own * ns2;
+    n_items = total > (int)rank ? (total - (int)rank + split - 1) / split : 0;
+  }
+
+  float vout[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) vout[t] = 0.f;
+
+  if (warp == 0) {
+    // ---------------- TMA producer (the weights need nothing from FC1)
+    if (lane == 0) {
+      for (int i = kFc2 ? 0 : kRing; i < n_items; ++i) {
+        const int sl = i % kRing, round = i / kRing;
+        if (round > 0 && !mbar_wait(&S.done[sl], (round - 1) & 1, a.status, 1u)) break;
+        issue(i, kFc2 ? S.ids[item_slot(i)] : e1);
+      }
+    }
+  } else if (warp < kMmaWarp0 + kMmaWarps) {
+    // ---------------- MMA issuers: items alternate between two warps (the
+    // issue cost of an MMA, not its execution, bounds these tiny-N tiles);
+    // each warp runs converged and one elected lane issues
+    const int mw = warp - kMmaWarp0;
+    const uint32_t tmem = S.tmem;
+    const uint32_t idesc = idesc_mxf4nvf4(128, N, false);
+    for (int i = mw; i < n_items; i += kMmaWarps) {
+      const int sl = i % kRing, round = i / kRing;
+      bool ok = mbar_wait(&S.fullA[sl], round & 1, a.status, 2u);
+      ok = ok && mbar_wait(&S.sfa[sl], round & 1, a.status, 2u);
+      ok = ok && mbar_wait(&S.fullB[sl], round & 1, a.status, 2u);
+      ok = ok && (round == 0 || mbar_wait(&S.acce[sl], (round - 1) & 1, a.status, 2u));
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int ng = item_groups(i);
+      uint8_t* slotp = ring + sl * kSlotBytes;
+      const uint32_t sfa_t = tmem + kTmemSFBase + sl * 32, sfb_t = sfa_t + 16;
+      const uint64_t da = smem_desc(smem_u32(slotp), 16, 1024, kLayoutSW128);
+      const uint64_t db = smem_desc(smem_u32(slotp + kSlotA), 16, 1024, kLayoutSW128);
+      for (int k = 0; k < ng; ++k)  // K step of 64 = 32 bytes = 2 descriptor units
+        mma_nvf4_warp(tmem + 32 * sl, da + 2 * k, db + 2 * k, idesc, sfa_t + 4 * k, sfb_t + 4 * k, k > 0);
+      mma_commit_warp(&S.done[sl]);
+    }
+  } else if (is_quant) {
+    // ---------------- activation terms (B operand), one wave of ring slots at a time
+    if (kFc2) pdl_wait();  // h is complete and visible
+    const int waves = (n_items + kRing - 1) / kRing;
+    for (int w = 0; w < waves; ++w) {
+      const int i0 = w * kRing, wi = n_items - i0 < kRing ? n_items - i0 : kRing;
+      if (w > 0) {
+        bool ok = true;
+        for (int k = 0; k < wi; ++k) ok = ok && mbar_wait(&S.done[(i0 + k) % kRing], (w - 1) & 1, a.status, 8u);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      const int pairs = wi * M;
+      for (int r = 0; r * kQuantWarps < pairs; ++r) {
+        const int p = r * kQuantWarps + qw;
+        if (p >= pairs) break;  // warp-uniform
+        const int item = i0 + p / M, token = p % M;
+        const bool act = lane < 8 * item_groups(item);  // lanes beyond the stage's valid K
+        float v[8];
+        if (!kFc2 && w == 0 && r == 0) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = pre_ok ? pre[j] : 0.f;
+        } else if (act) {
+          const int st = item_stage(item);
+          if (!kFc2)
+            load_bf16x8(a.x + (size_t)token * H + st * 256 + lane * 8, v);
+          else
+            load_f32x8(a.h + ((size_t)item_slot(item) * M + token) * I + st * 256 + lane * 8, v);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = 0.f;
+        }
+        // G1 of this (item, token): the maximum over the whole stage
+        float m = fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
+                        fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float G1 = term_g1(m);
+        if (lane < kTerms) S.G[item % kGSlots][token][lane] = G1 * __uint_as_float((127u - 2u * lane) << 23);
+        uint8_t* slotp = ring + (item % kRing) * kSlotBytes;
+        emit_stage_terms(v, G1, slotp + kSlotA, slotp + kSlotA + kSlotB + kSlotSF, token, lane, act);
+      }
+      fence_proxy_async_smem();
+      // the wave's B scales -> tensor memory: each warp fills its lane quarter
+      // (the scales of B rows 0..31 are replicated in all four)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.bsf);
+      if (!__all_sync(0xffffffffu, mbar_wait(&S.bsf, w & 1, a.status, 64u))) break;
+      for (int k = 0; k < wi; ++k) {
+        const int sl = (i0 + k) % kRing;
+        const uint4 u = *reinterpret_cast<const uint4*>(ring + sl * kSlotBytes + kSlotA + kSlotB + kSlotSF + lane * 16);
+        const uint32_t r[16] = {u.x, 0u, 0u, 0u, u.y, 0u, 0u, 0u, u.z, 0u, 0u, 0u, u.w, 0u, 0u, 0u};
+        tmem_st16(S.tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kTmemSFBase + sl * 32 + 16, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0)
+        for (int k = 0; k < wi; ++k) {
+          mbar_arrive(&S.gready[(i0 + k) % kGSlots]);
+          mbar_arrive(&S.fullB[(i0 + k) % kRing]);
+        }
+    }
+  } else {
+    // ---------------- weight scales -> tensor memory, accumulator drain.
+    // Warps 6..9 own lanes 32*(warp%4) ..; each copies an item's scale chunks
+    // into its quarter (replicated) as soon as the item's TMA lands.
+    const int q = warp & 3;
+    const uint32_t tq = S.tmem + ((uint32_t)(32 * q) << 16);
+    bool ok = true;
+    auto store_sfa = [&](int i) {
+      const int sl = i % kRing;
+      ok = ok && mbar_wait(&S.fullA[sl], (i / kRing) & 1, a.status, 32u);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) return;
+      const uint8_t* src = ring + sl * kSlotBytes + kSlotA + kSlotB;
+      uint32_t r[16];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const uint4 u = *reinterpret_cast<const uint4*>(src + g * kChunkBytes + lane * 16);
+        r[4 * g] = u.x;
+        r[4 * g + 1] = u.y;
+        r[4 * g + 2] = u.z;
+        r[4 * g + 3] = u.w;
+      }
+      tmem_st16(tq + kTmemSFBase + sl * 32, r);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.sfa[sl]);
+    };
+    for (int i = 0; i < n_items && i < kRing; ++i) store_sfa(i);
+    for (int i = 0; ok && i < n_items; ++i) {
+      const int sl = i % kRing, gs = i % kGSlots;
+      ok = mbar_wait(&S.gready[gs], (i / kGSlots) & 1, a.status, 16u);
+      ok = ok && mbar_wait(&S.done[sl], (i / kRing) & 1, a.status, 4u);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      float acc[kMaxN];
+      uint32_t r[16];
+      tmem_ld16(tq + 32 * sl, r);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) acc[c] = __uint_as_float(r[c]);
+      if (N > 16) {
+        tmem_ld16(tq + 32 * sl + 16, r);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) acc[16 + c] = __uint_as_float(r[c]);
+      } else {
+#pragma unroll
+        for (int c = 16; c < kMaxN; ++c) acc[c] = 0.f;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.acce[sl]);
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+        if (t < M) {
+#pragma unroll
+          for (int u = 0; u < kTerms; ++u) vout[t] = fmaf(acc[t * kTerms + u], S.G[gs][t][u], vout[t]);
+        }
+      if (i + kRing < n_items) store_sfa(i + kRing);
+    }
+  }
+
+  // ---- cluster reduction: partial rows go to their owner CTA (asynchronous
+  // stores counted on its barrier), summed there in rank order
+  tc_fence_before();
+  __syncwarp();
+  cluster_wait();  // phase 1: every CTA of the cluster runs
+  // FC1: pair p is owned by rank p % split (cpo pairs each); FC2: row r by rank r % split
+  const int cpo = (64 + split - 1) / split;
+  const int rpo = kFc2 ? (128 + split - 1) / split : 2 * cpo;
+  if (is_epi) {
+    const int row = 32 * (warp & 3) + lane;
+    int owner, j;
+    if (!kFc2) {
+      const int pr = row & 63;
+      owner = pr % split;
+      j = (row >> 6) * cpo + pr / split;
+    } else {
+      owner = row % split;
+      j = row / split;
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      if (t < M) st_async_peer_f32(&S.part[((int)rank * M + t) * rpo + j], &S.red, (uint32_t)owner, vout[t]);
+  }
+  __syncwarp();
+  __syncthreads();  // tensor memory is no longer read
+  if (warp == kMmaWarp0) tmem_dealloc(S.tmem, kTmemColsTc);
+  if (!__all_sync(0xffffffffu, mbar_wait(&S.red, 0, a.status, 128u))) return;
+  if (!kFc2) {
+    for (int idx = threadIdx.x; idx < M * cpo; idx += kTcThreads) {
+      const int token = idx / cpo, jj = idx % cpo, pair = (int)rank + split * jj;
+      if (pair >= 64) continue;
+      float gate = 0.f, up = 0.f;
+      for (int src = 0; src < split; ++src) {
+        gate += S.part[(src * M + token) * rpo + jj];
+        up += S.part[(src * M + token) * rpo + cpo + jj];
+      }
+      const float hv = (S.routed >> token) & 1u ? silu(gate * g_gate) * (up * g_up) * (S.wtok[token] * g_down) : 0.f;
+      a.h[((size_t)slot1 * M + token) * I + tile * 64 + pair] = hv;
+    }
+  } else {
+    for (int idx = threadIdx.x; idx < M * rpo; idx += kTcThreads) {
+      const int token = idx / rpo, j = idx % rpo, row = (int)rank + split * j;
+      if (row >= 128) continue;
+      float v = 0.f;
+      for (int src = 0; src < split; ++src) v += S.part[(src * M + token) * rpo + j];
+      a.out[(size_t)token * H + unit * 128 + row] = __float2bfloat16_rn(v);
+    }
+  }
+}
+
+// K ranges per w13 tile: as many as keep FC1 at one CTA per SM (so that the
+// FC2 CTAs can start streaming their weights beside it), at most 8.
+int fc1_split(int n_slots, int H, int I, int sms) {
+  const int units = n_slots * (I / 64), nk = H / 256;
+  int s = sms / units;
+  s = s > 8 ? 8 : s;
+  s = s > nk ? nk : s;
+  return s < 1 ? 1 : s;
+}
+
+// CTAs per w2 row tile: FC2 also at one CTA per SM, at most 8 and at most
+// the number of (slot, K stage) items.
+int fc2_split(int n_slots, int H, int I, int sms) {
+  const int tiles = H / 128, items = n_slots * ((I + 255) / 256);
+  int q = sms / tiles;
+  q = q > 8 ? 8 : q;
+  q = q > items ? items : q;
+  return q < 1 ? 1 : q;
+}
+
+}  // namespace
+
+bool decode_tc_supported(int fmt) { return fmt == MOE_FP4_NVFP4; }
+
+cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
+                             const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
+                             float* h, uint32_t* status, int num_sms, cudaStream_t st, int* cu_err) {
+  CUtensorMap m13, m2;
+  CUresult r = make_fp4_map(&m13, w13, (uint64_t)H / 2, (uint64_t)E * 2 * I, 128);
+  if (r == CUDA_SUCCESS) r = make_fp4_map(&m2, w2, (uint64_t)I / 2, (uint64_t)E * H, 128);
+  if (r != CUDA_SUCCESS) {
+    *cu_err = (int)r;
+    return cudaErrorInvalidValue;
+  }
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    err = cudaFuncSetAttribute(decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(decode_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    if (err != cudaSuccess) return err;
+    attr_done[dev] = true;
+  }
+  TcArgs a;
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.ids = ids;
+  a.tw = tw;
+  a.s13 = static_cast<const uint8_t*>(s13);
+  a.s2 = static_cast<const uint8_t*>(s2);
+  a.h = h;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.status = status;
+  a.M = M;
+  a.E = E;
+  a.H = H;
+  a.I = I;
+  a.top_k = top_k;
+  a.n_slots = M * top_k;
+  a.N = (kTerms * M + 15) / 16 * 16;
+  const int sms = num_sms > 0 ? num_sms : 152;
+
+  // FC1: clusters of K ranges per w13 tile; programmatic dependent launch so
+  // that its prologue overlaps whatever runs before it
+  const int units1 = a.n_slots * (I / 64);
+  const int s1 = fc1_split(a.n_slots, H, I, sms);
+  a.split = s1;
+  cudaLaunchAttribute at1[2];
+  at1[0].id = cudaLaunchAttributeClusterDimension;
+  at1[0].val.clusterDim.x = (unsigned)s1;
+  at1[0].val.clusterDim.y = 1;
+  at1[0].val.clusterDim.z = 1;
+  at1[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at1[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t c1 = {};
+  c1.gridDim = dim3((unsigned)(units1 * s1));
+  c1.blockDim = dim3(kTcThreads);
+  c1.dynamicSmemBytes = kTcSmem;
+  c1.stream = st;
+  c1.attrs = at1;
+  c1.numAttrs = 2;
+  err = cudaLaunchKernelEx(&c1, decode_tc_kernel<false>, m13, a);
+  if (err != cudaSuccess) return err;
+
+  // FC2: clusters of CTAs per w2 row tile, dependent launch on FC1
+  const int tiles2 = H / 128;
+  const int q = fc2_split(a.n_slots, H, I, sms);
+  a.split = q;
+  cudaLaunchAttribute at2[2];
+  at2[0].id = cudaLaunchAttributeClusterDimension;
+  at2[0].val.clusterDim.x = (unsigned)q;
+  at2[0].val.clusterDim.y = 1;
+  at2[0].val.clusterDim.z = 1;
+  at2[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at2[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t c2 = {};
+  c2.gridDim = dim3((unsigned)(tiles2 * q));
+  c2.blockDim = dim3(kTcThreads);
+  c2.dynamicSmemBytes = kTcSmem;
+  c2.stream = st;
+  c2.attrs = at2;
+  c2.numAttrs = 2;
+  return cudaLaunchKernelEx(&c2, decode_tc_kernel<true>, m2, a);
+}
+
+}  // namespace moe_fp4
