@@ -211,6 +211,16 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ GPU arm
+def decode_src_sha256():
+    """Hash of the decode kernels' sources: a stored ncu traffic figure is used
+    only while the kernels it was measured on are unchanged."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("common.cuh", "tcgen05.cuh", "decode_tc.cu", "decode.cu"):
+        h.update(open(os.path.join(ROOT, "fp4_weight_moe_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -335,9 +345,7 @@ def run_ours(args):
         try:
             with open(prof) as f:
                 pd = json.load(f)
-            import hashlib
-            src = open(os.path.join(ROOT, "fp4_weight_moe_gb300", "csrc", "decode.cu"), "rb").read()
-            if pd.get("decode_cu_sha256") == hashlib.sha256(src).hexdigest():
+            if pd.get("decode_src_sha256") == decode_src_sha256():
                 traffic = pd.get("dram_bytes_per_layer")
         except Exception:
             traffic = None
