@@ -29,8 +29,11 @@ cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const
 
 namespace {
 
-// Scratch of moe_fp4_forward_noalloc, shared by all its calls on a device.
-static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_FP4_NOALLOC_SCRATCH_BYTES];
+// Scratch of moe_fp4_forward_noalloc, shared by all its calls on a device:
+// the intermediate (MOE_FP4_NOALLOC_SCRATCH_BYTES) and the decode kernels'
+// 256-byte status block after it.
+constexpr size_t kNoallocStatusBytes = 256;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_FP4_NOALLOC_SCRATCH_BYTES + kNoallocStatusBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
@@ -81,7 +84,8 @@ extern "C" int moe_fp4_forward_noalloc(const void* x_bf16, const void* w13, cons
   int sms = 0;
   int st = scratch_for_current_device(&scratch, &sms);
   if (st != MOE_FP4_OK) return st;
-  if (decode_workspace_bytes(M, H, I, top_k, sms) > (size_t)MOE_FP4_NOALLOC_SCRATCH_BYTES) return MOE_FP4_EWORKSPACE;
+  if (decode_workspace_bytes(M, H, I, top_k, sms) > (size_t)MOE_FP4_NOALLOC_SCRATCH_BYTES + kNoallocStatusBytes)
+    return MOE_FP4_EWORKSPACE;
   // Nothing in the scratch needs to start at zero: FC1 writes every
   // intermediate element that FC2 reads in the same call.
   cudaError_t e = launch_decode(x_bf16, w13, s13, w2, s2, topk_ids, topk_weights, out_bf16, M, E, H, I, top_k, fmt,

@@ -184,10 +184,11 @@ MOE_FP4_API int moe_fp4_forward_ws(const void *x_bf16, const void *w13, const vo
  *
  * Arguments, layouts and results are those of moe_fp4_forward (same
  * kernels, bitwise the same output).  Instead of a workspace it uses one
- * fixed scratch array of MOE_FP4_NOALLOC_SCRATCH_BYTES in the library's
- * device image, which every GPU that loads the library's device code keeps
- * until the process exits.  Shapes whose scratch need
- * (moe_fp4_workspace_bytes(M, ...)) exceeds that size return
+ * fixed scratch array in the library's device image (an intermediate of
+ * MOE_FP4_NOALLOC_SCRATCH_BYTES plus a 256-byte status block), which every
+ * GPU that loads the library's device code keeps until the process exits.
+ * Shapes whose scratch need (moe_fp4_workspace_bytes(M, ...)) exceeds
+ * MOE_FP4_NOALLOC_SCRATCH_BYTES + 256 return
  * MOE_FP4_EWORKSPACE; M > MOE_FP4_DECODE_MAX_M returns MOE_FP4_EUNSUPPORTED.
  * The first call on each device looks up the array's device address while
  * that device is current; make that first call outside any stream capture.
