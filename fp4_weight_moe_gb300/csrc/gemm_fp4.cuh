@@ -3,18 +3,25 @@
 // one E4M3 scale per 16 K-elements on both sides, FP32 accumulation in
 // tensor memory.
 //
-// One CTA computes a 128 x 256 tile:
+// One CTA computes a 128 x 256 tile with six warps:
 //   warp 0 lane 0  TMA producer: A box 128 rows x 128 B and B box 256 rows x
 //                  128 B (SWIZZLE_128B) plus the 512 B scale chunks of the
 //                  stage, into a 4-deep shared-memory ring (mbarrier
 //                  full/empty pairs);
-//   warp 1         allocates 512 tensor-memory columns; lane 0 issues per
-//                  stage the scale-factor copies (tcgen05.cp 32x128b.warpx4)
-//                  and four tcgen05.mma kind::mxf4nvf4 (K = 64 each), then a
-//                  commit that frees the stage;
-//   warps 0-3      epilogue: each reads its 32 accumulator lanes
+//   warp 1         allocates 512 tensor-memory columns and, converged (one
+//                  elected lane), issues four tcgen05.mma kind::mxf4nvf4
+//                  (K = 64 each) per stage and a commit that frees the stage;
+//   warps 2-5      copy each stage's scale chunks from shared memory into
+//                  tensor memory with tcgen05.st (each warp its own lane
+//                  quarter: the 32-row chunks are replicated in all four),
+//                  then run the epilogue: each reads its 32 accumulator lanes
 //                  (tcgen05.ld 32x32b) and hands rows of FP32 to the
 //                  epilogue functor.
+// The tensor cores accept an MMA about every hundred cycles and a scale copy
+// (tcgen05.cp) every seventy to a hundred from one issuing thread, so keeping
+// the copies off the MMA warp and issuing from a converged warp lets the
+// four MMAs of a stage (about 390 cycles of FP4 work at 128 x 256 x 256)
+// keep the tensor pipe busy.
 // Tensor memory: columns [0, 256) accumulator; from 256, per ring slot, 16
 // columns of A scales (4 K-groups x 4) and 32 of B scales (4 K-groups x 2
 // row tiles x 4).  A 512-byte scale chunk (128 rows x 4 K-blocks, byte
@@ -31,7 +38,7 @@ constexpr int kGemmBM = 128;
 constexpr int kGemmBN = 256;
 constexpr int kGemmBK = 256;  // K elements per stage (128 bytes per row)
 constexpr int kGemmStages = 4;
-constexpr int kGemmThreads = 128;
+constexpr int kGemmThreads = 192;
 constexpr uint32_t kStageA = kGemmBM * kGemmBK / 2;              // 16 KB
 constexpr uint32_t kStageB = kGemmBN * kGemmBK / 2;              // 32 KB
 constexpr uint32_t kStageSFA = (kGemmBM / 128) * 4 * kChunkBytes;  // 2 KB
@@ -63,18 +70,19 @@ __device__ __forceinline__ void gemm_fp4_tile(const CUtensorMap* map_a, const CU
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kGemmStages * kStageBytes);
   uint64_t* empty = full + kGemmStages;
   uint64_t* done = empty + kGemmStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* sfready = done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfready + kGemmStages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const GemmTile t = tile_of();
   if (!t.valid) return;
   const int nk = K / kGemmBK;
-  const int KG = K / 64;  // 4-block groups per row (NVFP4: 16-element blocks)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGemmStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&sfready[s], 4);
     }
     mbar_init(done, 1);
     fence_mbar_init();
@@ -83,6 +91,7 @@ __device__ __forceinline__ void gemm_fp4_tile(const CUtensorMap* map_a, const CU
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
+  __syncwarp();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -92,58 +101,92 @@ __device__ __forceinline__ void gemm_fp4_tile(const CUtensorMap* map_a, const CU
   auto stage_sfa = [&](int s) { return smem + s * kStageBytes + kStageA + kStageB; };
   auto stage_sfb = [&](int s) { return smem + s * kStageBytes + kStageA + kStageB + kStageSFA; };
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // producer
-    for (int s = 0; s < nk; ++s) {
-      const int slot = s % kGemmStages, round = s / kGemmStages;
-      if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, err, 1u)) break;
-      mbar_arrive_expect_tx(&full[slot], kStageBytes);
-      tma_load_2d(stage_a(slot), map_a, s * (kGemmBK / 2), t.a_row0, &full[slot]);
-      tma_load_2d(stage_b(slot), map_b, s * (kGemmBK / 2), t.b_row0, &full[slot]);
-      bulk_load(stage_sfa(slot), t.a_sf + (size_t)(4 * s) * kChunkBytes, kStageSFA, &full[slot]);
-      bulk_load(stage_sfb(slot), t.b_sf0 + (size_t)(4 * s) * kChunkBytes, kStageSFB / 2, &full[slot]);
-      bulk_load(stage_sfb(slot) + kStageSFB / 2, t.b_sf1 + (size_t)(4 * s) * kChunkBytes, kStageSFB / 2,
-                &full[slot]);
+    if (lane == 0) {
+      for (int s = 0; s < nk; ++s) {
+        const int slot = s % kGemmStages, round = s / kGemmStages;
+        if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, err, 1u)) break;
+        mbar_arrive_expect_tx(&full[slot], kStageBytes);
+        tma_load_2d(stage_a(slot), map_a, s * (kGemmBK / 2), t.a_row0, &full[slot]);
+        tma_load_2d(stage_b(slot), map_b, s * (kGemmBK / 2), t.b_row0, &full[slot]);
+        bulk_load(stage_sfa(slot), t.a_sf + (size_t)(4 * s) * kChunkBytes, kStageSFA, &full[slot]);
+        bulk_load(stage_sfb(slot), t.b_sf0 + (size_t)(4 * s) * kChunkBytes, kStageSFB / 2, &full[slot]);
+        bulk_load(stage_sfb(slot) + kStageSFB / 2, t.b_sf1 + (size_t)(4 * s) * kChunkBytes, kStageSFB / 2,
+                  &full[slot]);
+      }
     }
-  } else if (warp == 1 && lane == 0) {
-    // MMA issuer
+  } else if (warp == 1) {
+    // MMA issuer, converged
     const uint32_t idesc = idesc_mxf4nvf4(kGemmBM, kGemmBN, false);
     for (int s = 0; s < nk; ++s) {
       const int slot = s % kGemmStages, round = s / kGemmStages;
-      if (!mbar_wait(&full[slot], round & 1, err, 2u)) break;
+      bool ok = mbar_wait(&full[slot], round & 1, err, 2u);
+      ok = ok && mbar_wait(&sfready[slot], round & 1, err, 2u);
+      if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t sf_a = tmem + kTmemSF + slot * kTmemSFPerSlot;
       const uint32_t sf_b = sf_a + 16;
-      const uint32_t sa = smem_u32(stage_sfa(slot)), sb = smem_u32(stage_sfb(slot));
+      const uint64_t da = smem_desc(smem_u32(stage_a(slot)), 16, 1024, kLayoutSW128);
+      const uint64_t db = smem_desc(smem_u32(stage_b(slot)), 16, 1024, kLayoutSW128);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        sf_copy(sf_a + 4 * k, smem_desc(sa + k * kChunkBytes, 128, 128, kLayoutNone));
-        sf_copy(sf_b + 8 * k, smem_desc(sb + k * kChunkBytes, 128, 128, kLayoutNone));
-        sf_copy(sf_b + 8 * k + 4, smem_desc(sb + kStageSFB / 2 + k * kChunkBytes, 128, 128, kLayoutNone));
-      }
-      const uint32_t a0 = smem_u32(stage_a(slot)), b0 = smem_u32(stage_b(slot));
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        mma_nvf4(tmem, smem_desc(a0 + 32 * k, 16, 1024, kLayoutSW128), smem_desc(b0 + 32 * k, 16, 1024, kLayoutSW128),
-                 idesc, sf_a + 4 * k, sf_b + 8 * k, s > 0 || k > 0);
-      }
-      mma_commit(&empty[slot]);
+      for (int k = 0; k < 4; ++k)  // K step of 64 = 32 bytes = 2 descriptor units
+        mma_nvf4_warp(tmem, da + 2 * k, db + 2 * k, idesc, sf_a + 4 * k, sf_b + 8 * k, s > 0 || k > 0);
+      mma_commit_warp(&empty[slot]);
     }
-    mma_commit(done);
+    mma_commit_warp(done);
+  } else {
+    // scale chunks -> tensor memory (this warp's lane quarter), stage by stage
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    for (int s = 0; s < nk; ++s) {
+      const int slot = s % kGemmStages, round = s / kGemmStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], round & 1, err, 8u))) break;
+      uint32_t r[16];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 u = *reinterpret_cast<const uint4*>(stage_sfa(slot) + k * kChunkBytes + lane * 16);
+        r[4 * k] = u.x;
+        r[4 * k + 1] = u.y;
+        r[4 * k + 2] = u.z;
+        r[4 * k + 3] = u.w;
+      }
+      const uint32_t col = tmem + lane_base + kTmemSF + slot * kTmemSFPerSlot;
+      tmem_st16(col, r);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // B: K-groups 2h, 2h+1, each both row tiles
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const int k = 2 * h + kk;
+          const uint4 u0 = *reinterpret_cast<const uint4*>(stage_sfb(slot) + k * kChunkBytes + lane * 16);
+          const uint4 u1 =
+              *reinterpret_cast<const uint4*>(stage_sfb(slot) + kStageSFB / 2 + k * kChunkBytes + lane * 16);
+          r[8 * kk] = u0.x;
+          r[8 * kk + 1] = u0.y;
+          r[8 * kk + 2] = u0.z;
+          r[8 * kk + 3] = u0.w;
+          r[8 * kk + 4] = u1.x;
+          r[8 * kk + 5] = u1.y;
+          r[8 * kk + 6] = u1.z;
+          r[8 * kk + 7] = u1.w;
+        }
+        tmem_st16(col + 16 + 16 * h, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sfready[slot]);
+    }
+    // epilogue: every warp reads its 32 lanes (rows) of the accumulator
+    mbar_wait(done, 0, err, 4u);
+    __syncwarp();
+    tc_fence_after();
+    const int row = (warp & 3) * 32 + lane;
+    epi(tmem + lane_base, row, t);
   }
-  __syncwarp();
-
-  // epilogue: every warp reads its 32 lanes (rows) of the accumulator
-  mbar_wait(done, 0, err, 4u);
-  __syncwarp();
-  tc_fence_after();
-  const int row = (warp & 3) * 32 + lane;
-  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-  epi(tmem + lane_base, row, t);
   tc_fence_before();
+  __syncwarp();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
-  (void)KG;
 }
 
 }  // namespace moe_fp4
