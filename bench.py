@@ -363,10 +363,10 @@ def run_ours(args):
         "routed_bytes_per_layer": step_bytes / K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"hbm_gbs of {peak_kind}", "traffic": traffic,
-                     "kernel": "decode FC1+FC2 pair (PDL-overlapped), per layer"},
+                     "kernel": "decode layer: activation pre-pass + FC1 + FC2 (PDL-overlapped)" if fmt == gen.NVFP4 else "decode layer: FC1 + FC2 (PDL-overlapped)"},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": M * H * 2 + M * k * 8,
                 "d2h_bytes_per_step": M * H * 2, "us_per_layer": e2e_ms * 1e3 / K},
-        "gpu_launches": 2 * K,
+        "gpu_launches": (3 if fmt == gen.NVFP4 else 2) * K,
         "clocks": clocks,
     }
 

@@ -11,7 +11,7 @@ cudaError_t launch_prepare(const void* w13_l, const void* s13_l, const float* g1
                            void* w2, void* s2, cudaStream_t st, bool inverse);
 cudaError_t launch_debug_dequant(const void* w, const void* s, int which, int e, int E, int H, int I, int fmt,
                                  float* out, cudaStream_t st);
-size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int num_sms);
+size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int fmt, int num_sms);
 cudaError_t launch_debug_gemm(const void* a_q, const void* a_sf, const void* b_q, const void* b_sf, float* d,
                               int M_rows, int N_rows, int K, uint32_t* status, cudaStream_t st, int* cu_err);
 size_t prefill_workspace_bytes(int M, int E, int H, int I, int top_k);
@@ -75,8 +75,14 @@ int check_prefill(int M, int E, int I, int top_k, int fmt) {
   return MOE_FP4_OK;
 }
 
-size_t workspace_need(int M, int E, int H, int I, int top_k, int sms) {
-  size_t d = decode_workspace_bytes(M < MOE_FP4_DECODE_MAX_M ? M : MOE_FP4_DECODE_MAX_M, H, I, top_k, sms);
+// Scratch for every batch size up to M (a workspace reserved for M_max serves
+// all smaller batches).
+size_t workspace_need(int M, int E, int H, int I, int top_k, int fmt, int sms) {
+  size_t d = 0;
+  for (int m = 1; m <= M && m <= MOE_FP4_DECODE_MAX_M; ++m) {
+    const size_t b = decode_workspace_bytes(m, H, I, top_k, fmt, sms);
+    if (b > d) d = b;
+  }
   if (M > MOE_FP4_DECODE_MAX_M) {
     const size_t p = prefill_workspace_bytes(M, E, H, I, top_k);
     if (p > d) d = p;
@@ -158,7 +164,7 @@ size_t moe_fp4_workspace_bytes(int M_max, int E, int H, int I, int top_k, int fm
   if (M_max > MOE_FP4_DECODE_MAX_M && check_prefill(M_max, E, I, top_k, fmt) != MOE_FP4_OK) return 0;
   int sms = 0;
   if (device_sms(&sms) != MOE_FP4_OK) return 0;
-  return workspace_need(M_max < 1 ? 1 : M_max, E, H, I, top_k, sms);
+  return workspace_need(M_max < 1 ? 1 : M_max, E, H, I, top_k, fmt, sms);
 }
 
 int moe_fp4_reserve_workspace(int M_max, int E, int H, int I, int top_k, int fmt, void* stream) {
@@ -229,7 +235,7 @@ int moe_fp4_forward_ws(const void* x_bf16, const void* w13, const void* s13, con
   st = device_sms(&sms);
   if (st != MOE_FP4_OK) return st;
   if (M <= MOE_FP4_DECODE_MAX_M) {
-    const size_t need = decode_workspace_bytes(M, H, I, top_k, sms);
+    const size_t need = decode_workspace_bytes(M, H, I, top_k, fmt, sms);
     if (need >= kMaxWorkspace || workspace_bytes < need) return MOE_FP4_EWORKSPACE;
     cudaError_t e = launch_decode(x_bf16, w13, s13, w2, s2, topk_ids, topk_weights, out_bf16, M, E, H, I, top_k,
                                   fmt, workspace, sms, static_cast<cudaStream_t>(stream));

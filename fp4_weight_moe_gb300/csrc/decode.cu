@@ -484,21 +484,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fc2_kernel(DecodeParams p)
 
 // ---------------------------------------------------------------- host side
 bool decode_tc_supported(int fmt);
+size_t decode_tc_scratch_bytes(int M, int H, int I, int top_k, int num_sms);
 cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                              const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
-                             float* h, uint32_t* status, int num_sms, cudaStream_t st, int* cu_err);
+                             float* part1, uint32_t* status, int num_sms, cudaStream_t st, int* cu_err);
 
-static size_t decode_h_bytes(int M_max, int I, int top_k) {
-  const size_t n = (size_t)M_max * top_k;
-  return (sizeof(float) * n * M_max * I + 255) & ~(size_t)255;
+// Scratch before the 256-byte status block: MXFP4, h [M*top_k][M][I] FP32;
+// NVFP4, FC1's partial sums (decode_tc_scratch_bytes).
+static size_t decode_scratch_bytes(int M_max, int H, int I, int top_k, int fmt, int num_sms) {
+  const size_t b = decode_tc_supported(fmt) ? decode_tc_scratch_bytes(M_max, H, I, top_k, num_sms)
+                                            : sizeof(float) * (size_t)M_max * top_k * M_max * I;
+  return (b + 255) & ~(size_t)255;
 }
 
-// Scratch: h, [M*top_k][M][I] FP32, then a 256-byte status block (bit flags
-// of bounded waits that gave up; sticky).
-size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int num_sms) {
-  (void)H;
-  (void)num_sms;
-  return decode_h_bytes(M_max, I, top_k) + 256;
+// Scratch, then a 256-byte status block (bit flags of bounded waits that
+// gave up; sticky).
+size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int fmt, int num_sms) {
+  return decode_scratch_bytes(M_max, H, I, top_k, fmt, num_sms) + 256;
 }
 
 cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
@@ -506,7 +508,8 @@ cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const
                           int fmt, void* ws, int num_sms, cudaStream_t st) {
   if (decode_tc_supported(fmt)) {
     int cu = 0;
-    uint32_t* status = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + decode_h_bytes(M, I, top_k));
+    uint32_t* status =
+        reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + decode_scratch_bytes(M, H, I, top_k, fmt, num_sms));
     return launch_decode_tc(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, static_cast<float*>(ws), status,
                             num_sms, st, &cu);
   }

@@ -81,7 +81,9 @@ constexpr int kMaxSlotsTc = 128;
 constexpr uint32_t kTmemColsTc = 256;
 constexpr uint32_t kTmemSFBase = 32 * kRing;           // accumulator groups in [0, 128)
 
-constexpr int kPartFloats = 1280;  // split * M * 2 * ceil(64 / split) <= 1120 (FC1); M * 128 (FC2)
+// FC2: split * M * ceil(128 / split) floats; split <= 8 gives at most
+// 7 * 19 = 133 per token (split 7), so 8 tokens fit in 8 * 136.
+constexpr int kPartFloats = 8 * 136;
 
 struct SmemTc {
   float part[kPartFloats];         // partial sums received from the cluster
@@ -91,8 +93,7 @@ struct SmemTc {
   int own[kMaxSlotsTc];            // FC2: first slot naming each valid expert, in slot order
   int own_cnt[4];                  // FC2: owners per 32-slot chunk
   int expert;                      // FC1: this CTA's expert (-1: nothing to do)
-  float wtok[8];                   // FC1: router weight of the expert per token
-  uint32_t routed;                 // FC1: tokens routed to the expert (bit mask)
+  float gmul[kMaxSlotsTc][3];      // FC2: gate, up, down multipliers per owner slot
   uint64_t fullA[kRing];           // weight tile + its scale chunks landed (TMA)
   uint64_t fullB[kRing];           // activation terms + their scales in place (builders)
   uint64_t sfa[kRing];             // weight scales copied to tensor memory
@@ -111,11 +112,14 @@ struct TcArgs {
   const float* tw;
   const uint8_t* s13;
   const uint8_t* s2;
-  float* h;  // [n_slots][M][I]
+  float* part1;  // [n_slots][split1][M][2I]: FC1 partial sums (resident row order), per K range
+  uint8_t* ximg;  // per K stage of x: B tile (N rows x 128 B, swizzled), 512 B of scales, G [M][kTerms]
+  int ximg_stride;
   __nv_bfloat16* out;
   uint32_t* status;
   int M, E, H, I, top_k, n_slots;
-  int split;  // cluster size: FC1 K ranges per w13 tile, FC2 CTAs per w2 tile
+  int split;   // FC1: K ranges per w13 tile; FC2: CTAs (cluster size) per w2 tile
+  int split1;  // FC1's K ranges (read by FC2)
   int N;      // B rows per item (accumulator columns)
 };
 
@@ -254,16 +258,88 @@ __device__ __forceinline__ void load_bf16x8(const __nv_bfloat16* p, float (&v)[8
     v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
   }
 }
-__device__ __forceinline__ void load_f32x8(const float* p, float (&v)[8]) {
-  const uint4 u0 = ld_cg_v4(p), u1 = ld_cg_v4(p + 4);
-  v[0] = __uint_as_float(u0.x);
-  v[1] = __uint_as_float(u0.y);
-  v[2] = __uint_as_float(u0.z);
-  v[3] = __uint_as_float(u0.w);
-  v[4] = __uint_as_float(u1.x);
-  v[5] = __uint_as_float(u1.y);
-  v[6] = __uint_as_float(u1.z);
-  v[7] = __uint_as_float(u1.w);
+
+// FC2's activations for route slot j (owner index o) and `token`, pairs
+// p0 .. p0+7 of the intermediate: FC1's partial gate/up sums of every K range,
+// added in range order, times the projection multipliers, SiLU(gate) * up,
+// times the router weight (summed over the token's slots naming the expert)
+// and the down multiplier -- exactly 0 for a token not routed to the expert.
+__device__ __forceinline__ void fc2_activation(const TcArgs& a, const SmemTc& S, int j, int o, int token, int p0,
+                                               float (&v)[8]) {
+  const int e = S.ids[j];
+  float w = 0.f;
+  bool routed = false;
+  for (int k = 0; k < a.top_k; ++k)
+    if (S.ids[token * a.top_k + k] == e) {
+      w += S.tw[token * a.top_k + k];
+      routed = true;
+    }
+  if (!routed) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    return;
+  }
+  const size_t row_len = 2 * (size_t)a.I, kstride = (size_t)a.M * row_len;
+  const float* base = a.part1 + ((size_t)j * a.split1 * a.M + token) * row_len + (p0 >> 6) * 128 + (p0 & 63);
+  float g[8], u[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) g[i] = u[i] = 0.f;
+  for (int k0 = 0; k0 < a.split1; k0 += 2) {
+    uint4 q[2][4];
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      if (k0 + kk < a.split1) {
+        const float* pk = base + (size_t)(k0 + kk) * kstride;
+        q[kk][0] = ld_cg_v4(pk);
+        q[kk][1] = ld_cg_v4(pk + 4);
+        q[kk][2] = ld_cg_v4(pk + 64);
+        q[kk][3] = ld_cg_v4(pk + 68);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) q[kk][c] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const uint32_t gw[8] = {q[kk][0].x, q[kk][0].y, q[kk][0].z, q[kk][0].w,
+                              q[kk][1].x, q[kk][1].y, q[kk][1].z, q[kk][1].w};
+      const uint32_t uw[8] = {q[kk][2].x, q[kk][2].y, q[kk][2].z, q[kk][2].w,
+                              q[kk][3].x, q[kk][3].y, q[kk][3].z, q[kk][3].w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        g[i] += __uint_as_float(gw[i]);
+        u[i] += __uint_as_float(uw[i]);
+      }
+    }
+  }
+  const float gg = S.gmul[o][0], gu = S.gmul[o][1], wd = w * S.gmul[o][2];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = silu(g[i] * gg) * (u[i] * gu) * wd;
+}
+
+// Activation pre-pass of FC1: the four NVFP4 terms of x for every (K stage,
+// token), built once per layer call and stored as the images FC1 copies
+// into its ring: the B tile (rows token*kTerms + t, 128-byte swizzle), the
+// scales (row n's 16 bytes at 16n) and the term multipliers G [M][kTerms].
+// One CTA per K stage, one warp per token.
+__global__ void __launch_bounds__(256) decode_quant_x_kernel(TcArgs a) {
+  pdl_wait();               // x comes from the previous kernel
+  pdl_launch_dependents();  // FC1 may start: the routing is final as well
+  const int st = blockIdx.x, token = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (token >= a.M) return;
+  uint8_t* img = a.ximg + (size_t)st * a.ximg_stride;
+  float v[8];
+  load_bf16x8(a.x + (size_t)token * a.H + st * 256 + lane * 8, v);
+  float m = fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
+                  fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float G1 = term_g1(m);
+  const uint32_t tb = (uint32_t)a.N * 128;
+  if (lane < kTerms)
+    reinterpret_cast<float*>(img + tb + kChunkBytes)[token * kTerms + lane] =
+        G1 * __uint_as_float((127u - 2u * lane) << 23);
+  emit_stage_terms(v, G1, img, img + tb, token, lane, true);
 }
 
 // FC1 (kFc2 = false) and FC2 (kFc2 = true).
@@ -276,7 +352,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M = a.M, H = a.H, I = a.I, n = a.n_slots, N = a.N;
   const int split = a.split;
-  const uint32_t rank = cluster_rank();
+  // FC1: independent CTAs, blockIdx = (slot, tile, K range); FC2: clusters
+  // of `split` CTAs per w2 row tile
+  const uint32_t rank = kFc2 ? cluster_rank() : (uint32_t)(blockIdx.x % split);
   const int unit = blockIdx.x / split;  // FC1: slot * tiles1 + tile; FC2: w2 row tile
   const int tiles1 = I / 64, ns2 = (I + 255) / 256;
   const bool is_quant = warp >= kQuantWarp0 && warp < kQuantWarp0 + kQuantWarps;
@@ -286,29 +364,30 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&S.fullA[s], 1);
-      mbar_init(&S.fullB[s], kQuantWarps);
+      mbar_init(&S.fullB[s], kFc2 ? kQuantWarps : 1);
       mbar_init(&S.sfa[s], 4);
       mbar_init(&S.done[s], 1);
       mbar_init(&S.acce[s], 4);
     }
     for (int s = 0; s < kGSlots; ++s) mbar_init(&S.gready[s], kQuantWarps);
     mbar_init(&S.bsf, kQuantWarps);
-    mbar_init(&S.red, 1);
-    // the partial rows this CTA will receive: FC1 owns pairs p = rank mod
-    // split (gate and up rows), FC2 rows r = rank mod split; every CTA of
-    // the cluster sends its share of them
-    const int own = kFc2 ? (128 - (int)rank + split - 1) / split : 2 * ((64 - (int)rank + split - 1) / split);
-    mbar_arrive_expect_tx(&S.red, (uint32_t)(split * own * M * 4));
+    if (kFc2) {
+      // the output rows this CTA reduces (r = rank mod split), one partial
+      // from every CTA of the cluster
+      mbar_init(&S.red, 1);
+      mbar_arrive_expect_tx(&S.red, (uint32_t)(split * ((128 - (int)rank + split - 1) / split) * M * 4));
+    }
     fence_mbar_init();
     tma_prefetch_desc(&map_w);
   }
-  // cluster phase 1: this CTA runs and its barriers are initialised
+  // FC2 cluster phase 1: this CTA runs and its barriers are initialised
   // (awaited before any remote store)
-  cluster_arrive_release();
+  if (kFc2) cluster_arrive_release();
   if (warp == kMmaWarp0) tmem_alloc(&S.tmem, kTmemColsTc);
-  // FC1 waits for whatever produced x and the routing; FC2 is launched by FC1
-  // only after that point, so both may read the routing from here on.
-  if (!kFc2) pdl_wait();
+  // Both kernels are launched only after the activation pre-pass has passed
+  // its wait on whatever produced x and the routing, so they may read the
+  // routing right away; FC1 waits (griddepcontrol.wait) before it reads the
+  // pre-pass's activation terms, FC2 before it reads FC1's partial sums.
   pdl_launch_dependents();
 
   int slot1 = 0, tile = 0, k0 = 0, n_items = 0, n_own = 0;
@@ -336,21 +415,25 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     tma_load_2d(slotp, &map_w, st * 128, row0, &S.fullA[sl]);
     bulk_load(slotp + kSlotA + kSlotB, sfa, (uint32_t)ng * kChunkBytes, &S.fullA[sl]);
   };
+  // FC1: bulk copy of item i's activation terms (B tile, scales, G) from the
+  // pre-pass's image into the ring slot
+  auto issue_b = [&](int i) {
+    const int sl = i % kRing;
+    uint8_t* slotp = ring + sl * kSlotBytes;
+    const uint8_t* img = a.ximg + (size_t)item_stage(i) * a.ximg_stride;
+    const uint32_t tb = (uint32_t)N * 128, sb = kChunkBytes + 16u * (uint32_t)M;
+    mbar_arrive_expect_tx(&S.fullB[sl], tb + sb);
+    bulk_load(slotp + kSlotA, img, tb, &S.fullB[sl]);
+    bulk_load(slotp + kSlotA + kSlotB + kSlotSF, img + tb, sb, &S.fullB[sl]);
+  };
 
-  float pre[8];
-  bool pre_ok = false;
-  const int qw = warp - kQuantWarp0;  // quantiser warp: one (item, token) per round
+  const int qw = warp - kQuantWarp0;  // FC2 quantiser warp: one (item, token) per round
   if (!kFc2) {
     slot1 = unit / tiles1;
     tile = unit % tiles1;
     const int nk = H / 256;
     k0 = (int)rank * nk / split;
     n_items = ((int)rank + 1) * nk / split - k0;
-    // the first activation blocks need nothing else: start their loads
-    if (is_quant && qw < (n_items < kRing ? n_items : kRing) * M) {
-      load_bf16x8(a.x + (size_t)(qw % M) * H + (k0 + qw / M) * 256 + lane * 8, pre);
-      pre_ok = true;
-    }
   }
   if (warp == 0) {
     for (int j = lane; j < n; j += 32) {
@@ -372,18 +455,6 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
         if (ok)
           for (int i = 0; i < n_items && i < kRing; ++i) issue(i, e);
       }
-      // router weight of this expert per token
-      float wt = 0.f;
-      bool rt = false;
-      if (lane < M)
-        for (int k = 0; k < a.top_k; ++k)
-          if (S.ids[lane * a.top_k + k] == e) {
-            wt += S.tw[lane * a.top_k + k];
-            rt = true;
-          }
-      const uint32_t rm = __ballot_sync(0xffffffffu, rt);
-      if (lane < M) S.wtok[lane] = wt;
-      if (lane == 0) S.routed = rm;
     }
   }
   tc_fence_before();
@@ -392,18 +463,12 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   tc_fence_after();
 
   int e1 = -1;
-  float g_gate = 0.f, g_up = 0.f, g_down = 0.f;
   if (!kFc2) {
     e1 = S.expert;
-    if (e1 < 0) {  // every CTA of the cluster shares the slot: all leave
+    if (e1 < 0) {  // an earlier slot names this expert and does the work
       if (warp == kMmaWarp0) tmem_dealloc(S.tmem, kTmemColsTc);
       return;
     }
-    const float* gl13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * tiles1 * (H / 64) * kChunkBytes);
-    const float* gl2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * (H / 128) * (I / 64) * kChunkBytes);
-    g_gate = ld_nc_f32(gl13 + 2 * e1);
-    g_up = ld_nc_f32(gl13 + 2 * e1 + 1);
-    g_down = ld_nc_f32(gl2 + e1);
   } else {
     // owners: the first slot naming each valid expert, in slot order
     bool own_j = false;
@@ -425,7 +490,14 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     if (own_j) {
       int base = 0;
       for (int c = 0; c < warp; ++c) base += S.own_cnt[c];
-      S.own[base + __popc(bal & ((1u << lane) - 1u))] = j;
+      const int o = base + __popc(bal & ((1u << lane) - 1u));
+      S.own[o] = j;
+      const int e = S.ids[j];
+      const float* gl13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * tiles1 * (H / 64) * kChunkBytes);
+      const float* gl2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * (H / 128) * (I / 64) * kChunkBytes);
+      S.gmul[o][0] = ld_nc_f32(gl13 + 2 * e);
+      S.gmul[o][1] = ld_nc_f32(gl13 + 2 * e + 1);
+      S.gmul[o][2] = ld_nc_f32(gl2 + e);
     }
     n_own = S.own_cnt[0] + S.own_cnt[1] + S.own_cnt[2] + S.own_cnt[3];
     __syncwarp();
@@ -442,10 +514,15 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   if (warp == 0) {
     // ---------------- TMA producer (the weights need nothing from FC1)
     if (lane == 0) {
+      if (!kFc2) {
+        pdl_wait();  // the activation pre-pass is complete
+        for (int i = 0; i < n_items && i < kRing; ++i) issue_b(i);
+      }
       for (int i = kFc2 ? 0 : kRing; i < n_items; ++i) {
         const int sl = i % kRing, round = i / kRing;
         if (round > 0 && !mbar_wait(&S.done[sl], (round - 1) & 1, a.status, 1u)) break;
         issue(i, kFc2 ? S.ids[item_slot(i)] : e1);
+        if (!kFc2) issue_b(i);
       }
     }
   } else if (warp < kMmaWarp0 + kMmaWarps) {
@@ -473,8 +550,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
       mma_commit_warp(&S.done[sl]);
     }
   } else if (is_quant) {
-    // ---------------- activation terms (B operand), one wave of ring slots at a time
-    if (kFc2) pdl_wait();  // h is complete and visible
+    // ---------------- FC2: activation terms (B operand), one wave of ring slots at a time
+    if (kFc2) {  // (FC1's terms come from the pre-pass)
+    pdl_wait();  // FC1's partial sums are complete and visible
     const int waves = (n_items + kRing - 1) / kRing;
     for (int w = 0; w < waves; ++w) {
       const int i0 = w * kRing, wi = n_items - i0 < kRing ? n_items - i0 : kRing;
@@ -490,15 +568,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
         const int item = i0 + p / M, token = p % M;
         const bool act = lane < 8 * item_groups(item);  // lanes beyond the stage's valid K
         float v[8];
-        if (!kFc2 && w == 0 && r == 0) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = pre_ok ? pre[j] : 0.f;
-        } else if (act) {
-          const int st = item_stage(item);
-          if (!kFc2)
-            load_bf16x8(a.x + (size_t)token * H + st * 256 + lane * 8, v);
-          else
-            load_f32x8(a.h + ((size_t)item_slot(item) * M + token) * I + st * 256 + lane * 8, v);
+        if (act) {
+          fc2_activation(a, S, item_slot(item), ((int)rank + split * item) % n_own, token, item_stage(item) * 256 + lane * 8,
+                         v);
         } else {
 #pragma unroll
           for (int j = 0; j < 8; ++j) v[j] = 0.f;
@@ -534,6 +606,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
           mbar_arrive(&S.fullB[(i0 + k) % kRing]);
         }
     }
+    }
   } else {
     // ---------------- weight scales -> tensor memory, accumulator drain.
     // Warps 6..9 own lanes 32*(warp%4) ..; each copies an item's scale chunks
@@ -544,6 +617,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     auto store_sfa = [&](int i) {
       const int sl = i % kRing;
       ok = ok && mbar_wait(&S.fullA[sl], (i / kRing) & 1, a.status, 32u);
+      if (!kFc2) ok = ok && mbar_wait(&S.fullB[sl], (i / kRing) & 1, a.status, 32u);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) return;
       const uint8_t* src = ring + sl * kSlotBytes + kSlotA + kSlotB;
@@ -557,6 +631,17 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
         r[4 * g + 3] = u.w;
       }
       tmem_st16(tq + kTmemSFBase + sl * 32, r);
+      if (!kFc2) {
+        // FC1: the item's activation scales (B rows 0..31, 64-K group g in
+        // column 4g) and its term multipliers, copied by the pre-pass image
+        const uint8_t* bsf = src + kSlotSF;
+        const uint4 u = *reinterpret_cast<const uint4*>(bsf + lane * 16);
+        const uint32_t rb[16] = {u.x, 0u, 0u, 0u, u.y, 0u, 0u, 0u, u.z, 0u, 0u, 0u, u.w, 0u, 0u, 0u};
+        tmem_st16(tq + kTmemSFBase + sl * 32 + 16, rb);
+        const float* gi = reinterpret_cast<const float*>(bsf + kChunkBytes);
+        if (lane < M * kTerms) S.G[i % kGSlots][lane / kTerms][lane % kTerms] = gi[lane];
+        __syncwarp();
+      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -565,7 +650,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     for (int i = 0; i < n_items && i < kRing; ++i) store_sfa(i);
     for (int i = 0; ok && i < n_items; ++i) {
       const int sl = i % kRing, gs = i % kGSlots;
-      ok = mbar_wait(&S.gready[gs], (i / kGSlots) & 1, a.status, 16u);
+      ok = !kFc2 || mbar_wait(&S.gready[gs], (i / kGSlots) & 1, a.status, 16u);
       ok = ok && mbar_wait(&S.done[sl], (i / kRing) & 1, a.status, 4u);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
@@ -595,25 +680,29 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     }
   }
 
-  // ---- cluster reduction: partial rows go to their owner CTA (asynchronous
-  // stores counted on its barrier), summed there in rank order
   tc_fence_before();
   __syncwarp();
+  if (!kFc2) {
+    // FC1: this CTA's partial gate/up rows, for FC2 to combine
+    if (is_epi) {
+      const int row = 32 * (warp & 3) + lane;
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+        if (t < M)
+          a.part1[(((size_t)slot1 * split + rank) * M + t) * (2 * I) + tile * 128 + row] = vout[t];
+    }
+    __syncwarp();
+    __syncthreads();  // tensor memory is no longer read
+    if (warp == kMmaWarp0) tmem_dealloc(S.tmem, kTmemColsTc);
+    return;
+  }
+  // ---- FC2 cluster reduction: partial rows go to their owner CTA
+  // (asynchronous stores counted on its barrier), summed there in rank order
   cluster_wait();  // phase 1: every CTA of the cluster runs
-  // FC1: pair p is owned by rank p % split (cpo pairs each); FC2: row r by rank r % split
-  const int cpo = (64 + split - 1) / split;
-  const int rpo = kFc2 ? (128 + split - 1) / split : 2 * cpo;
+  const int rpo = (128 + split - 1) / split;  // row r is owned by rank r % split
   if (is_epi) {
     const int row = 32 * (warp & 3) + lane;
-    int owner, j;
-    if (!kFc2) {
-      const int pr = row & 63;
-      owner = pr % split;
-      j = (row >> 6) * cpo + pr / split;
-    } else {
-      owner = row % split;
-      j = row / split;
-    }
+    const int owner = row % split, j = row / split;
 #pragma unroll
     for (int t = 0; t < 8; ++t)
       if (t < M) st_async_peer_f32(&S.part[((int)rank * M + t) * rpo + j], &S.red, (uint32_t)owner, vout[t]);
@@ -622,26 +711,12 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   __syncthreads();  // tensor memory is no longer read
   if (warp == kMmaWarp0) tmem_dealloc(S.tmem, kTmemColsTc);
   if (!__all_sync(0xffffffffu, mbar_wait(&S.red, 0, a.status, 128u))) return;
-  if (!kFc2) {
-    for (int idx = threadIdx.x; idx < M * cpo; idx += kTcThreads) {
-      const int token = idx / cpo, jj = idx % cpo, pair = (int)rank + split * jj;
-      if (pair >= 64) continue;
-      float gate = 0.f, up = 0.f;
-      for (int src = 0; src < split; ++src) {
-        gate += S.part[(src * M + token) * rpo + jj];
-        up += S.part[(src * M + token) * rpo + cpo + jj];
-      }
-      const float hv = (S.routed >> token) & 1u ? silu(gate * g_gate) * (up * g_up) * (S.wtok[token] * g_down) : 0.f;
-      a.h[((size_t)slot1 * M + token) * I + tile * 64 + pair] = hv;
-    }
-  } else {
-    for (int idx = threadIdx.x; idx < M * rpo; idx += kTcThreads) {
-      const int token = idx / rpo, j = idx % rpo, row = (int)rank + split * j;
-      if (row >= 128) continue;
-      float v = 0.f;
-      for (int src = 0; src < split; ++src) v += S.part[(src * M + token) * rpo + j];
-      a.out[(size_t)token * H + unit * 128 + row] = __float2bfloat16_rn(v);
-    }
+  for (int idx = threadIdx.x; idx < M * rpo; idx += kTcThreads) {
+    const int token = idx / rpo, j = idx % rpo, row = (int)rank + split * j;
+    if (row >= 128) continue;
+    float v = 0.f;
+    for (int src = 0; src < split; ++src) v += S.part[(src * M + token) * rpo + j];
+    a.out[(size_t)token * H + unit * 128 + row] = __float2bfloat16_rn(v);
   }
 }
 
@@ -669,9 +744,26 @@ int fc2_split(int n_slots, int H, int I, int sms) {
 
 bool decode_tc_supported(int fmt) { return fmt == MOE_FP4_NVFP4; }
 
+// Bytes of one K stage's activation image: B tile, scales, multipliers.
+static int ximg_stride(int M) {
+  const int N = (kTerms * M + 15) / 16 * 16;
+  return (N * 128 + kChunkBytes + 16 * M + 127) / 128 * 128;
+}
+static size_t part1_bytes(int M, int H, int I, int top_k, int num_sms) {
+  const int n = M * top_k;
+  const size_t b = (size_t)n * fc1_split(n, H, I, num_sms > 0 ? num_sms : 152) * M * 2 * (size_t)I * sizeof(float);
+  return (b + 255) & ~(size_t)255;
+}
+
+// FC1's partial sums [M*top_k slots][K ranges][M][2I] FP32, then the
+// activation images of the H/256 K stages.
+size_t decode_tc_scratch_bytes(int M, int H, int I, int top_k, int num_sms) {
+  return part1_bytes(M, H, I, top_k, num_sms) + (size_t)(H / 256) * ximg_stride(M);
+}
+
 cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                              const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
-                             float* h, uint32_t* status, int num_sms, cudaStream_t st, int* cu_err) {
+                             float* part1, uint32_t* status, int num_sms, cudaStream_t st, int* cu_err) {
   CUtensorMap m13, m2;
   CUresult r = make_fp4_map(&m13, w13, (uint64_t)H / 2, (uint64_t)E * 2 * I, 128);
   if (r == CUDA_SUCCESS) r = make_fp4_map(&m2, w2, (uint64_t)I / 2, (uint64_t)E * H, 128);
@@ -696,7 +788,9 @@ cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, co
   a.tw = tw;
   a.s13 = static_cast<const uint8_t*>(s13);
   a.s2 = static_cast<const uint8_t*>(s2);
-  a.h = h;
+  a.part1 = part1;
+  a.ximg = reinterpret_cast<uint8_t*>(part1) + part1_bytes(M, H, I, top_k, num_sms);
+  a.ximg_stride = ximg_stride(M);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.status = status;
   a.M = M;
@@ -708,25 +802,35 @@ cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, co
   a.N = (kTerms * M + 15) / 16 * 16;
   const int sms = num_sms > 0 ? num_sms : 152;
 
-  // FC1: clusters of K ranges per w13 tile; programmatic dependent launch so
-  // that its prologue overlaps whatever runs before it
+  // activation pre-pass: one CTA per K stage, one warp per token
+  cudaLaunchAttribute at0[1];
+  at0[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at0[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t c0 = {};
+  c0.gridDim = dim3((unsigned)(H / 256));
+  c0.blockDim = dim3((unsigned)(32 * M));
+  c0.stream = st;
+  c0.attrs = at0;
+  c0.numAttrs = 1;
+  err = cudaLaunchKernelEx(&c0, decode_quant_x_kernel, a);
+  if (err != cudaSuccess) return err;
+
+  // FC1: K ranges per w13 tile (independent CTAs); programmatic dependent
+  // launch so that its prologue overlaps the pre-pass
   const int units1 = a.n_slots * (I / 64);
   const int s1 = fc1_split(a.n_slots, H, I, sms);
   a.split = s1;
-  cudaLaunchAttribute at1[2];
-  at1[0].id = cudaLaunchAttributeClusterDimension;
-  at1[0].val.clusterDim.x = (unsigned)s1;
-  at1[0].val.clusterDim.y = 1;
-  at1[0].val.clusterDim.z = 1;
-  at1[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at1[1].val.programmaticStreamSerializationAllowed = 1;
+  a.split1 = s1;
+  cudaLaunchAttribute at1[1];
+  at1[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at1[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t c1 = {};
   c1.gridDim = dim3((unsigned)(units1 * s1));
   c1.blockDim = dim3(kTcThreads);
   c1.dynamicSmemBytes = kTcSmem;
   c1.stream = st;
   c1.attrs = at1;
-  c1.numAttrs = 2;
+  c1.numAttrs = 1;
   err = cudaLaunchKernelEx(&c1, decode_tc_kernel<false>, m13, a);
   if (err != cudaSuccess) return err;
 

@@ -21,7 +21,7 @@
 #include "common.cuh"
 
 namespace moe_fp4 {
-size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int num_sms);
+size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int fmt, int num_sms);
 cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                           const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
                           int fmt, void* ws, int num_sms, cudaStream_t st);
@@ -84,7 +84,7 @@ extern "C" int moe_fp4_forward_noalloc(const void* x_bf16, const void* w13, cons
   int sms = 0;
   int st = scratch_for_current_device(&scratch, &sms);
   if (st != MOE_FP4_OK) return st;
-  if (decode_workspace_bytes(M, H, I, top_k, sms) > (size_t)MOE_FP4_NOALLOC_SCRATCH_BYTES + kNoallocStatusBytes)
+  if (decode_workspace_bytes(M, H, I, top_k, fmt, sms) > (size_t)MOE_FP4_NOALLOC_SCRATCH_BYTES + kNoallocStatusBytes)
     return MOE_FP4_EWORKSPACE;
   // Nothing in the scratch needs to start at zero: FC1 writes every
   // intermediate element that FC2 reads in the same call.
