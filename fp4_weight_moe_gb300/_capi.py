@@ -23,7 +23,7 @@ MOE_FP4_EWORKSPACE = 4
 MOE_FP4_MXFP4 = 0
 MOE_FP4_NVFP4 = 1
 MOE_FP4_DECODE_MAX_M = 8
-MOE_FP4_NOALLOC_SCRATCH_BYTES = 8 << 20
+MOE_FP4_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 # (name, restype, argtypes) for every symbol declared in include/moe_fp4.h
 _P = ctypes.c_void_p

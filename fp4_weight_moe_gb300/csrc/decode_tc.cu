@@ -115,6 +115,7 @@ struct TcArgs {
   float* part1;  // [n_slots][split1][M][2I]: FC1 partial sums (resident row order), per K range
   uint8_t* ximg;  // per K stage of x: B tile (N rows x 128 B, swizzled), 512 B of scales, G [M][kTerms]
   int ximg_stride;
+  uint8_t* himg;  // per (route slot, K stage of h): the same images for FC2, or null (FC2 builds its own)
   __nv_bfloat16* out;
   uint32_t* status;
   int M, E, H, I, top_k, n_slots;
@@ -264,14 +265,14 @@ __device__ __forceinline__ void load_bf16x8(const __nv_bfloat16* p, float (&v)[8
 // added in range order, times the projection multipliers, SiLU(gate) * up,
 // times the router weight (summed over the token's slots naming the expert)
 // and the down multiplier -- exactly 0 for a token not routed to the expert.
-__device__ __forceinline__ void fc2_activation(const TcArgs& a, const SmemTc& S, int j, int o, int token, int p0,
-                                               float (&v)[8]) {
-  const int e = S.ids[j];
+__device__ __forceinline__ void fc2_activation(const TcArgs& a, const int* ids, const float* tw, const float* gmul,
+                                               int j, int token, int p0, float (&v)[8]) {
+  const int e = ids[j];
   float w = 0.f;
   bool routed = false;
   for (int k = 0; k < a.top_k; ++k)
-    if (S.ids[token * a.top_k + k] == e) {
-      w += S.tw[token * a.top_k + k];
+    if (ids[token * a.top_k + k] == e) {
+      w += tw[token * a.top_k + k];
       routed = true;
     }
   if (!routed) {
@@ -312,7 +313,7 @@ __device__ __forceinline__ void fc2_activation(const TcArgs& a, const SmemTc& S,
       }
     }
   }
-  const float gg = S.gmul[o][0], gu = S.gmul[o][1], wd = w * S.gmul[o][2];
+  const float gg = gmul[0], gu = gmul[1], wd = w * gmul[2];
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = silu(g[i] * gg) * (u[i] * gu) * wd;
 }
@@ -342,6 +343,53 @@ __global__ void __launch_bounds__(256) decode_quant_x_kernel(TcArgs a) {
   emit_stage_terms(v, G1, img, img + tb, token, lane, true);
 }
 
+// Activation pre-pass of FC2 (larger M): the four NVFP4 terms of h for every
+// (route slot that owns its expert, K stage of the intermediate, token),
+// from FC1's partial sums, stored as FC2's images.  One CTA per (slot,
+// stage), one warp per token.
+__global__ void __launch_bounds__(256) decode_quant_h_kernel(TcArgs a) {
+  __shared__ int s_ids[kMaxSlotsTc];
+  __shared__ float s_tw[kMaxSlotsTc];
+  pdl_launch_dependents();  // FC2 may start streaming its weights
+  const int ns2 = (a.I + 255) / 256;
+  const int j = blockIdx.x / ns2, st = blockIdx.x % ns2;
+  const int token = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int k = threadIdx.x; k < a.n_slots; k += blockDim.x) {
+    s_ids[k] = __ldg(a.ids + k);
+    s_tw[k] = __ldg(a.tw + k);
+  }
+  __syncthreads();
+  const int e = s_ids[j];
+  if (e < 0 || e >= a.E) return;
+  for (int k = 0; k < j; ++k)
+    if (s_ids[k] == e) return;  // an earlier slot owns this expert
+  const float* gl13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * (a.I / 64) * (a.H / 64) * kChunkBytes);
+  const float* gl2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * (a.H / 128) * (a.I / 64) * kChunkBytes);
+  const float gmul[3] = {ld_nc_f32(gl13 + 2 * e), ld_nc_f32(gl13 + 2 * e + 1), ld_nc_f32(gl2 + e)};
+  pdl_wait();  // FC1's partial sums are complete
+  if (token >= a.M) return;
+  const int rem = a.I / 64 - 4 * st;
+  const bool act = lane < 8 * (rem < 4 ? rem : 4);
+  float v[8];
+  if (act) {
+    fc2_activation(a, s_ids, s_tw, gmul, j, token, st * 256 + lane * 8, v);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+  }
+  float m = fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
+                  fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float G1 = term_g1(m);
+  uint8_t* img = a.himg + ((size_t)j * ns2 + st) * a.ximg_stride;
+  const uint32_t tb = (uint32_t)a.N * 128;
+  if (lane < kTerms)
+    reinterpret_cast<float*>(img + tb + kChunkBytes)[token * kTerms + lane] =
+        G1 * __uint_as_float((127u - 2u * lane) << 23);
+  emit_stage_terms(v, G1, img, img + tb, token, lane, act);
+}
+
 // FC1 (kFc2 = false) and FC2 (kFc2 = true).
 template <bool kFc2>
 __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_constant__ CUtensorMap map_w, TcArgs a) {
@@ -358,13 +406,16 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   const int unit = blockIdx.x / split;  // FC1: slot * tiles1 + tile; FC2: w2 row tile
   const int tiles1 = I / 64, ns2 = (I + 255) / 256;
   const bool is_quant = warp >= kQuantWarp0 && warp < kQuantWarp0 + kQuantWarps;
+  // activation terms from a pre-pass image (FC1 always, FC2 for larger M)
+  // or built in this CTA (FC2 for small M)
+  const bool use_img = !kFc2 || a.himg != nullptr;
   const bool is_epi = warp >= kEpiWarp0;
 
   // ---- prologue: touches no input
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&S.fullA[s], 1);
-      mbar_init(&S.fullB[s], kFc2 ? kQuantWarps : 1);
+      mbar_init(&S.fullB[s], use_img ? 1 : kQuantWarps);
       mbar_init(&S.sfa[s], 4);
       mbar_init(&S.done[s], 1);
       mbar_init(&S.acce[s], 4);
@@ -420,7 +471,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   auto issue_b = [&](int i) {
     const int sl = i % kRing;
     uint8_t* slotp = ring + sl * kSlotBytes;
-    const uint8_t* img = a.ximg + (size_t)item_stage(i) * a.ximg_stride;
+    const uint8_t* img = kFc2 ? a.himg + ((size_t)item_slot(i) * ns2 + item_stage(i)) * a.ximg_stride
+                              : a.ximg + (size_t)item_stage(i) * a.ximg_stride;
     const uint32_t tb = (uint32_t)N * 128, sb = kChunkBytes + 16u * (uint32_t)M;
     mbar_arrive_expect_tx(&S.fullB[sl], tb + sb);
     bulk_load(slotp + kSlotA, img, tb, &S.fullB[sl]);
@@ -514,15 +566,18 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   if (warp == 0) {
     // ---------------- TMA producer (the weights need nothing from FC1)
     if (lane == 0) {
-      if (!kFc2) {
-        pdl_wait();  // the activation pre-pass is complete
-        for (int i = 0; i < n_items && i < kRing; ++i) issue_b(i);
+      const int wave0 = n_items < kRing ? n_items : kRing;
+      if (kFc2)  // (FC1 issued its first wave of weight tiles already)
+        for (int i = 0; i < wave0; ++i) issue(i, S.ids[item_slot(i)]);
+      if (use_img) {
+        pdl_wait();  // the pre-pass images are complete
+        for (int i = 0; i < wave0; ++i) issue_b(i);
       }
-      for (int i = kFc2 ? 0 : kRing; i < n_items; ++i) {
+      for (int i = wave0; i < n_items; ++i) {
         const int sl = i % kRing, round = i / kRing;
-        if (round > 0 && !mbar_wait(&S.done[sl], (round - 1) & 1, a.status, 1u)) break;
+        if (!mbar_wait(&S.done[sl], (round - 1) & 1, a.status, 1u)) break;
         issue(i, kFc2 ? S.ids[item_slot(i)] : e1);
-        if (!kFc2) issue_b(i);
+        if (use_img) issue_b(i);
       }
     }
   } else if (warp < kMmaWarp0 + kMmaWarps) {
@@ -551,7 +606,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     }
   } else if (is_quant) {
     // ---------------- FC2: activation terms (B operand), one wave of ring slots at a time
-    if (kFc2) {  // (FC1's terms come from the pre-pass)
+    if (!use_img) {  // (otherwise the terms come from a pre-pass)
     pdl_wait();  // FC1's partial sums are complete and visible
     const int waves = (n_items + kRing - 1) / kRing;
     for (int w = 0; w < waves; ++w) {
@@ -569,8 +624,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
         const bool act = lane < 8 * item_groups(item);  // lanes beyond the stage's valid K
         float v[8];
         if (act) {
-          fc2_activation(a, S, item_slot(item), ((int)rank + split * item) % n_own, token, item_stage(item) * 256 + lane * 8,
-                         v);
+          fc2_activation(a, S.ids, S.tw, S.gmul[((int)rank + split * item) % n_own], item_slot(item), token,
+                         item_stage(item) * 256 + lane * 8, v);
         } else {
 #pragma unroll
           for (int j = 0; j < 8; ++j) v[j] = 0.f;
@@ -617,7 +672,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     auto store_sfa = [&](int i) {
       const int sl = i % kRing;
       ok = ok && mbar_wait(&S.fullA[sl], (i / kRing) & 1, a.status, 32u);
-      if (!kFc2) ok = ok && mbar_wait(&S.fullB[sl], (i / kRing) & 1, a.status, 32u);
+      if (use_img) ok = ok && mbar_wait(&S.fullB[sl], (i / kRing) & 1, a.status, 32u);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) return;
       const uint8_t* src = ring + sl * kSlotBytes + kSlotA + kSlotB;
@@ -631,9 +686,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
         r[4 * g + 3] = u.w;
       }
       tmem_st16(tq + kTmemSFBase + sl * 32, r);
-      if (!kFc2) {
-        // FC1: the item's activation scales (B rows 0..31, 64-K group g in
-        // column 4g) and its term multipliers, copied by the pre-pass image
+      if (use_img) {
+        // the item's activation scales (B rows 0..31, 64-K group g in column
+        // 4g) and its term multipliers, copied from the pre-pass image
         const uint8_t* bsf = src + kSlotSF;
         const uint4 u = *reinterpret_cast<const uint4*>(bsf + lane * 16);
         const uint32_t rb[16] = {u.x, 0u, 0u, 0u, u.y, 0u, 0u, 0u, u.z, 0u, 0u, 0u, u.w, 0u, 0u, 0u};
@@ -650,7 +705,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     for (int i = 0; i < n_items && i < kRing; ++i) store_sfa(i);
     for (int i = 0; ok && i < n_items; ++i) {
       const int sl = i % kRing, gs = i % kGSlots;
-      ok = !kFc2 || mbar_wait(&S.gready[gs], (i / kGSlots) & 1, a.status, 16u);
+      ok = use_img || mbar_wait(&S.gready[gs], (i / kGSlots) & 1, a.status, 16u);
       ok = ok && mbar_wait(&S.done[sl], (i / kRing) & 1, a.status, 4u);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
@@ -720,24 +775,24 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   }
 }
 
-// K ranges per w13 tile: as many as keep FC1 at one CTA per SM (so that the
-// FC2 CTAs can start streaming their weights beside it), at most 8.
+// K ranges per w13 tile: about 1.5 CTAs per SM in total (measured best on
+// GB300 for 1..8 tokens: more ranges shorten each CTA's weight stream, fewer
+// leave room for FC2's CTAs beside them), at most 8.
 int fc1_split(int n_slots, int H, int I, int sms) {
   const int units = n_slots * (I / 64), nk = H / 256;
-  int s = sms / units;
+  int s = 3 * sms / (2 * units);
   s = s > 8 ? 8 : s;
   s = s > nk ? nk : s;
   return s < 1 ? 1 : s;
 }
 
-// CTAs per w2 row tile: FC2 also at one CTA per SM, at most 8 and at most
-// the number of (slot, K stage) items.
+// CTAs per w2 row tile (the cluster): 8, or the number of (slot, K stage)
+// items if smaller (measured best: the items of a tile spread over more SMs).
 int fc2_split(int n_slots, int H, int I, int sms) {
-  const int tiles = H / 128, items = n_slots * ((I + 255) / 256);
-  int q = sms / tiles;
-  q = q > 8 ? 8 : q;
-  q = q > items ? items : q;
-  return q < 1 ? 1 : q;
+  (void)H;
+  (void)sms;
+  const int items = n_slots * ((I + 255) / 256);
+  return items < 8 ? (items < 1 ? 1 : items) : 8;
 }
 
 }  // namespace
@@ -755,10 +810,18 @@ static size_t part1_bytes(int M, int H, int I, int top_k, int num_sms) {
   return (b + 255) & ~(size_t)255;
 }
 
-// FC1's partial sums [M*top_k slots][K ranges][M][2I] FP32, then the
-// activation images of the H/256 K stages.
+// From this batch size on, FC2's activation terms come from a pre-pass (built
+// once per slot instead of once per CTA of the slot's row tiles); below it
+// FC2 builds them itself and the layer saves a launch on its critical path.
+constexpr int kHPrepassMinM = 2;
+
+// FC1's partial sums [M*top_k slots][K ranges][M][2I] FP32, the activation
+// images of x's H/256 K stages, and (M >= kHPrepassMinM) those of h's
+// (slot, K stage) pairs.
 size_t decode_tc_scratch_bytes(int M, int H, int I, int top_k, int num_sms) {
-  return part1_bytes(M, H, I, top_k, num_sms) + (size_t)(H / 256) * ximg_stride(M);
+  size_t b = part1_bytes(M, H, I, top_k, num_sms) + (size_t)(H / 256) * ximg_stride(M);
+  if (M >= kHPrepassMinM) b += (size_t)M * top_k * ((I + 255) / 256) * ximg_stride(M);
+  return b;
 }
 
 cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
@@ -791,6 +854,7 @@ cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, co
   a.part1 = part1;
   a.ximg = reinterpret_cast<uint8_t*>(part1) + part1_bytes(M, H, I, top_k, num_sms);
   a.ximg_stride = ximg_stride(M);
+  a.himg = M >= kHPrepassMinM ? a.ximg + (size_t)(H / 256) * a.ximg_stride : nullptr;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.status = status;
   a.M = M;
@@ -834,7 +898,19 @@ cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, co
   err = cudaLaunchKernelEx(&c1, decode_tc_kernel<false>, m13, a);
   if (err != cudaSuccess) return err;
 
-  // FC2: clusters of CTAs per w2 row tile, dependent launch on FC1
+  if (a.himg) {
+    // h's activation pre-pass: one CTA per (route slot, K stage), a warp per token
+    cudaLaunchConfig_t ch = {};
+    ch.gridDim = dim3((unsigned)(a.n_slots * ((I + 255) / 256)));
+    ch.blockDim = dim3((unsigned)(32 * M));
+    ch.stream = st;
+    ch.attrs = at0;
+    ch.numAttrs = 1;
+    err = cudaLaunchKernelEx(&ch, decode_quant_h_kernel, a);
+    if (err != cudaSuccess) return err;
+  }
+
+  // FC2: clusters of CTAs per w2 row tile, dependent launch on the kernel before
   const int tiles2 = H / 128;
   const int q = fc2_split(a.n_slots, H, I, sms);
   a.split = q;

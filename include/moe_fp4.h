@@ -197,7 +197,7 @@ MOE_FP4_API int moe_fp4_forward_ws(const void *x_bf16, const void *w13, const vo
  * each other's results, so order them.  Nothing in the array needs to start
  * at zero.
  */
-#define MOE_FP4_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define MOE_FP4_NOALLOC_SCRATCH_BYTES (16u << 20)
 MOE_FP4_API int moe_fp4_forward_noalloc(const void *x_bf16, const void *w13, const void *s13, const void *w2,
                                         const void *s2, const int32_t *topk_ids, const float *topk_weights,
                                         void *out_bf16, int M, int E, int H, int I, int top_k, int fmt, void *stream);

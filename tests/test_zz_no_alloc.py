@@ -60,10 +60,10 @@ def test_noalloc_rejects_oversized_scratch():
     lib = _capi.lib()
     buf = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
     p = buf.data_ptr()
-    # M=8, top_k=16, I=4096 (MXFP4): needs 8*16*8*4096*4 bytes = 16 MiB > 8 MiB
-    need = lib.moe_fp4_workspace_bytes(8, 4, 256, 4096, 16, 0)
+    # M=8, top_k=16, I=8192 (MXFP4): needs 8*16*8*8192*4 bytes = 32 MiB > 16 MiB
+    need = lib.moe_fp4_workspace_bytes(8, 4, 256, 8192, 16, 0)
     assert need > _capi.MOE_FP4_NOALLOC_SCRATCH_BYTES
-    st = lib.moe_fp4_forward_noalloc(p, p, p, p, p, p, p, p, 8, 4, 256, 4096, 16, 0, ctypes.c_void_p(0))
+    st = lib.moe_fp4_forward_noalloc(p, p, p, p, p, p, p, p, 8, 4, 256, 8192, 16, 0, ctypes.c_void_p(0))
     assert st == _capi.MOE_FP4_EWORKSPACE
     # the prefill band is not served by this entry point
     st = lib.moe_fp4_forward_noalloc(p, p, p, p, p, p, p, p, 9, 4, 256, 128, 2, 0, ctypes.c_void_p(0))
