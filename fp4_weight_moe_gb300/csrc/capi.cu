@@ -69,7 +69,7 @@ int check_shape(int E, int H, int I, int top_k, int fmt) {
 
 // Extra limits of the prefill band (M > MOE_FP4_DECODE_MAX_M).
 int check_prefill(int M, int E, int I, int top_k, int fmt) {
-  if (fmt != MOE_FP4_NVFP4) return MOE_FP4_EUNSUPPORTED;
+  (void)fmt;  // both formats share the resident layout and the kernels
   if (I % 256 != 0 || E > 4096) return MOE_FP4_EUNSUPPORTED;
   if ((long long)M * top_k >= (1LL << 30)) return MOE_FP4_EUNSUPPORTED;
   return MOE_FP4_OK;
@@ -124,9 +124,9 @@ int moe_fp4_prepared_sizes(int E, int H, int I, int fmt, size_t* w13_bytes, size
   const size_t g2 = sizeof(float) * (size_t)E;
   auto pad16 = [](size_t v) { return (v + 15) & ~(size_t)15; };
   if (w13_bytes) *w13_bytes = (size_t)E * 2 * I * (H / 2);
-  if (s13_bytes) *s13_bytes = pad16((size_t)E * scale_chunk_bytes(2 * I, H, fmt) + g13);
+  if (s13_bytes) *s13_bytes = pad16((size_t)E * scale_chunk_bytes(2 * I, H) + g13);
   if (w2_bytes) *w2_bytes = (size_t)E * H * (I / 2);
-  if (s2_bytes) *s2_bytes = pad16((size_t)E * scale_chunk_bytes(H, I, fmt) + g2);
+  if (s2_bytes) *s2_bytes = pad16((size_t)E * scale_chunk_bytes(H, I) + g2);
   return MOE_FP4_OK;
 }
 

@@ -15,15 +15,22 @@ constexpr int kRowTile = 128;     // rows per resident tile (scale chunk height)
 constexpr int kChunkBytes = 512;  // one scale chunk: 128 rows x 4 K-blocks
 constexpr int kInterleave = 64;   // gate/up interleave granularity in w13
 
+// Scale block of the LOGICAL (checkpoint) layout: 32 elements for MXFP4
+// (UE8M0 bytes), 16 for NVFP4 (E4M3 bytes).
 __host__ __device__ constexpr int block_size(int fmt) { return fmt == MOE_FP4_MXFP4 ? 32 : 16; }
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Number of 4-block groups along K.
-__host__ __device__ inline int k_groups(int K, int fmt) { return ceil_div(K / block_size(fmt), 4); }
+// The RESIDENT layout has one E4M3 scale byte per 16 elements for both
+// formats (MXFP4 block scales are re-expressed at prepare time, see
+// prepare.cu), so both run on the same block-scaled MMA.
+constexpr int kResBlock = 16;
 
-// Bytes of one expert-projection's scale chunks (rows x K).
-__host__ __device__ inline size_t scale_chunk_bytes(int rows, int K, int fmt) {
-  return (size_t)(rows / kRowTile) * k_groups(K, fmt) * kChunkBytes;
+// Number of 4-block groups along K (resident).
+__host__ __device__ inline int k_groups(int K) { return ceil_div(K / kResBlock, 4); }
+
+// Bytes of one expert-projection's scale chunks (rows x K), resident.
+__host__ __device__ inline size_t scale_chunk_bytes(int rows, int K) {
+  return (size_t)(rows / kRowTile) * k_groups(K) * kChunkBytes;
 }
 
 // Offset of (row, kblock) inside one expert-projection's chunk array.
@@ -45,22 +52,11 @@ __host__ __device__ inline int w13_resident_row(int L, int I) {
 }
 
 // ---------------------------------------------------------------- decode helpers
-__device__ __forceinline__ float ue8m0_to_float(uint32_t b) {
-  // 2^(b-127); byte 0 -> 2^-127 (subnormal), byte 255 -> NaN.
-  if (b == 0u) return __int_as_float(0x00400000);
-  if (b == 255u) return __int_as_float(0x7fc00000);
-  return __int_as_float((int)(b << 23));
-}
-
 __device__ __forceinline__ float e4m3_to_float(uint32_t b) {
   uint32_t h2;
   uint16_t in = (uint16_t)(b & 0xffu);
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
   return __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
-}
-
-__device__ __forceinline__ float scale_to_float(uint32_t b, int fmt) {
-  return fmt == MOE_FP4_MXFP4 ? ue8m0_to_float(b) : e4m3_to_float(b);
 }
 
 // Eight E2M1 values (a 32-bit word, element 2i in the low nibble of byte i)

@@ -1,7 +1,8 @@
-// Decode band (M <= 8 tokens) for NVFP4 weights on the 5th-generation tensor
-// cores: the expert weights are streamed by TMA straight into shared memory
-// and consumed by tcgen05.mma kind::mxf4nvf4 with their own E4M3 block scales,
-// so no instruction is spent decoding a weight nibble.
+// Decode band (M <= 8 tokens) on the 5th-generation tensor cores: the expert
+// weights (NVFP4, or MXFP4 re-expressed at prepare time with E4M3 block
+// scales) are streamed by TMA straight into shared memory and consumed by
+// tcgen05.mma kind::mxf4nvf4 with their own block scales, so no instruction
+// is spent decoding a weight nibble.
 //
 // Prior art: the pages' tiny-decode kernel pair (b12x PR #22, "rp-native
 // tiny-decode kernel for w4a8_mx (M=1)", section What): FC1 streams the
@@ -796,8 +797,6 @@ int fc2_split(int n_slots, int H, int I, int sms) {
 }
 
 }  // namespace
-
-bool decode_tc_supported(int fmt) { return fmt == MOE_FP4_NVFP4; }
 
 // Bytes of one K stage's activation image: B tile, scales, multipliers.
 static int ximg_stride(int M) {

@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int NT = 2 * a.I / kGemmBN;
   const int mt = blockIdx.x / NT, nt = blockIdx.x % NT;
   const int KG = a.H / 64;
-  const size_t scb = scale_chunk_bytes(2 * a.I, a.H, MOE_FP4_NVFP4);
+  const size_t scb = scale_chunk_bytes(2 * a.I, a.H);
   const float* g13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * scb);
   auto tile_of = [&]() {
     GemmTile t;
@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int NT = a.H / kGemmBN;
   const int mt = blockIdx.x / NT, nt = blockIdx.x % NT;
   const int KG = a.I / 64;
-  const size_t scb = scale_chunk_bytes(a.H, a.I, MOE_FP4_NVFP4);
+  const size_t scb = scale_chunk_bytes(a.H, a.I);
   const float* g2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * scb);
   auto tile_of = [&]() {
     GemmTile t;

@@ -87,17 +87,19 @@ MOE_FP4_API int moe_fp4_version(void);
  *        64j..64j+63, so each 128-row tile holds matching gate and up rows.
  *        Byte order within a row is the logical one (low nibble = even K).
  *   w2:  [E][H][I/2] bytes, the logical layout.
- *   s13, s2: scale bytes in 512-byte chunks, one per (expert, 128-row tile,
- *        group of 4 consecutive K-blocks); inside a chunk the byte of row r
+ *   s13, s2: E4M3 scale bytes, one per 16 K-elements for both formats, in
+ *        512-byte chunks, one per (expert, 128-row tile, group of 4
+ *        consecutive 16-element K-blocks); inside a chunk the byte of row r
  *        (0..127 within the tile) and K-block b (0..3 within the group) is at
  *        (r % 32) * 16 + (r / 32) * 4 + b.  Chunks are ordered expert, row
- *        tile, K-block group.  Missing K-blocks of a ragged last group are 0.
- *        After the chunks, s13 holds FP32 multipliers [E][2] (gate, up) and
- *        s2 holds [E]: for NVFP4 the per-tensor multipliers, for MXFP4
- *        2^(largest scale exponent of that expert's projection - 12), which
- *        lets the decode kernels carry each block scale divided by it as an
- *        exact f16 (block scales more than 2^35 below the largest of their
- *        projection are flushed to zero in the decode band).
+ *        tile, K-block group.  After the chunks, s13 holds FP32 multipliers
+ *        [E][2] (gate, up) and s2 holds [E].  NVFP4: the checkpoint's scale
+ *        bytes and per-tensor multipliers.  MXFP4: each UE8M0 block scale
+ *        2^(e-127) becomes the E4M3 power of two 2^(e-127-b) for both of its
+ *        16-element halves, with the projection multiplier 2^b, b = (largest
+ *        block exponent of that expert's projection) - 127 - 8; block scales
+ *        more than 2^17 below the projection's largest are stored as 0 (their
+ *        weights read as zero), all others exactly.
  */
 MOE_FP4_API int moe_fp4_prepared_sizes(int E, int H, int I, int fmt, size_t *w13_bytes, size_t *s13_bytes, size_t *w2_bytes,
                            size_t *s2_bytes);
@@ -153,7 +155,7 @@ MOE_FP4_API int moe_fp4_release_workspace(void);
  * token accumulator with atomic adds, so its low-order bits may vary run to
  * run.
  *
- * Prefill band (M > 8): NVFP4 only, I % 256 == 0, E <= 4096 (else
+ * Prefill band (M > 8): I % 256 == 0, E <= 4096 (else
  * MOE_FP4_EUNSUPPORTED).  Activations are quantised to NVFP4 per row (x per
  * token, h = SiLU(gate)*up per routed row after BF16 staging) so both GEMMs
  * run on the FP4 tensor cores.
@@ -205,9 +207,9 @@ MOE_FP4_API int moe_fp4_forward_noalloc(const void *x_bf16, const void *w13, con
 /*
  * Test support: dequantise one expert's projection from the resident layout
  * into out_f32 [rows][K] in LOGICAL row order, each element computed as the
- * decode kernels do: e2m1 * scale (MXFP4, exact) or RN_fp32((e2m1 * e4m3) *
- * g) (NVFP4, one rounding).  which = 0: w13 (rows 2I, K = H, gate rows
- * first), which = 1: w2 (rows H, K = I).
+ * kernels use it: RN_fp32((e2m1 * e4m3) * g) (one rounding; exact for MXFP4,
+ * whose e4m3 and g are powers of two).  which = 0: w13 (rows 2I, K = H, gate
+ * rows first), which = 1: w2 (rows H, K = I).
  */
 MOE_FP4_API int moe_fp4_debug_dequant(const void *w, const void *s, int which, int expert, int E, int H, int I, int fmt,
                           float *out_f32, void *stream);

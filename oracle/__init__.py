@@ -180,12 +180,13 @@ def forward(x_bf16, weights: dict, topk_ids, topk_weights, E: int, H: int, I: in
 
 
 def forward_prefill(x_bf16, weights: dict, topk_ids, topk_weights, E: int, H: int, I: int, top_k: int,
-                    tokens: Optional[Sequence[int]] = None, nthreads: int = 0):
-    """Prefill-band definition (NVFP4 activations, mirrored): returns
-    (out ``[n_tok][H]`` FP64, x_q ``[n_tok][H/2]``, x_s ``[n_tok][H/16]``, x_G ``[n_tok]``)."""
+                    tokens: Optional[Sequence[int]] = None, nthreads: int = 0, fmt: int = NVFP4):
+    """Prefill-band definition (NVFP4 activations, mirrored; weights in either
+    format): returns (out ``[n_tok][H]`` FP64, x_q ``[n_tok][H/2]``,
+    x_s ``[n_tok][H/16]``, x_G ``[n_tok]``)."""
     x = _np(x_bf16, np.uint16)
     M = x.shape[0]
-    w13, s13, g13, w2, s2, g2 = _weights_np(weights, NVFP4)
+    w13, s13, g13, w2, s2, g2 = _weights_np(weights, fmt)
     ids = _np(topk_ids, np.int32)
     tw = _np(topk_weights, np.float32)
     tok = None if tokens is None else np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
@@ -195,7 +196,7 @@ def forward_prefill(x_bf16, weights: dict, topk_ids, topk_weights, E: int, H: in
     xs = np.zeros((n_tok, H // 16), dtype=np.uint8)
     xg = np.zeros((n_tok,), dtype=np.float32)
     rc = _load().moe_oracle_forward_prefill(_ptr(x), _ptr(w13), _ptr(s13), _ptr(g13), _ptr(w2), _ptr(s2), _ptr(g2),
-                                            _ptr(ids), _ptr(tw), M, E, H, I, top_k, NVFP4, _ptr(tok), n_tok,
+                                            _ptr(ids), _ptr(tw), M, E, H, I, top_k, fmt, _ptr(tok), n_tok,
                                             _ptr(out), _ptr(xq), _ptr(xs), _ptr(xg), nthreads)
     if rc != 0:
         raise ValueError("oracle rejected the shapes")

@@ -345,7 +345,8 @@ int moe_oracle_forward_prefill(const uint16_t *x_bf16, const uint8_t *w13, const
                                const int32_t *tokens, int n_tok, double *out, uint8_t *xq_out, uint8_t *xs_out,
                                float *xg_out, int nthreads)
 {
-    if (fmt != ORACLE_NVFP4 || H % 16 || I % 16) return 1;
+    if (fmt != ORACLE_NVFP4 && fmt != ORACLE_MXFP4) return 1;
+    if (H % block_of(fmt) || I % block_of(fmt) || H % 16 || I % 16) return 1;
     if (!tokens) n_tok = M;
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);

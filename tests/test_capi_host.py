@@ -51,8 +51,9 @@ def test_prepared_sizes_closed_form(lib, fmt, B):
     w13, s13, w2, s2 = _capi.moe_fp4_prepared_sizes(E, H, I, fmt)
     assert w13 == E * 2 * I * H // 2
     assert w2 == E * H * I // 2
-    kg13 = -(-(H // B) // 4)
-    kg2 = -(-(I // B) // 4)
+    # resident scales: one E4M3 byte per 16 elements for both formats
+    kg13 = -(-(H // 16) // 4)
+    kg2 = -(-(I // 16) // 4)
     pad = lambda v: (v + 15) // 16 * 16  # noqa: E731
     assert s13 == pad(E * (2 * I // 128) * kg13 * 512 + 8 * E)
     assert s2 == pad(E * (H // 128) * kg2 * 512 + 4 * E)

@@ -72,6 +72,31 @@ def test_dequant_bit_exact(fmt):
             assert np.array_equal(got.view(np.uint32), want.astype(np.float32).view(np.uint32)), (e, which, B)
 
 
+def test_mx_scale_range_in_resident_layout():
+    """MXFP4 block scales are carried as E4M3 powers of two relative to a
+    per-projection power-of-two multiplier: exactly within 2^17 of the
+    projection's largest block scale, as zero below (the resident layout's
+    documented limit)."""
+    E, H, I = 1, 256, 128
+    w = gen.make_expert_weights(E, H, I, gen.MXFP4, 11, device="cuda")
+    for key, rows, kb in (("s13", 2 * I, H // 32), ("s2", H, I // 32)):
+        exps = 140 - (torch.arange(rows * kb, device="cuda") % 30)  # 140 .. 111 in every projection
+        w[key] = exps.reshape(1, rows, kb).to(torch.uint8)
+    pw = fm().prepare_weights(w, E, H, I, gen.MXFP4)
+    wn = {k: v.cpu().numpy() for k, v in w.items() if v is not None}
+    for which, (wk, sk, K) in enumerate((("w13", "s13", H), ("w2", "s2", I))):
+        got = fm().debug_dequant(pw, which, 0).cpu().numpy()
+        want = oracle.dequant(wn[wk][0], wn[sk][0], K, gen.MXFP4, 1.0)
+        blk_exp = np.repeat(wn[sk][0].astype(np.int64), 32, axis=1)
+        keep = blk_exp >= 140 - 17
+        assert np.array_equal(got[keep], want[keep].astype(np.float32)), which
+        assert not np.any(got[~keep]), which
+    back = fm().unprepare_weights(pw)
+    s_back = back["s13"].cpu().numpy()[0]
+    kept = wn["s13"][0] >= 123
+    assert np.array_equal(s_back[kept], wn["s13"][0][kept])
+
+
 # ------------------------------------------------------------------ layer parity
 DECODE_CASES = [
     # name, overrides

@@ -88,8 +88,8 @@ def test_quant_rows_bit_exact():
         assert np.array_equal(qg[r], wq), r
 
 
-def _prefill_case(M, E, H, I, k, seed, invalid=0.0):
-    w = gen.make_expert_weights(E, H, I, gen.NVFP4, seed, device="cuda")
+def _prefill_case(M, E, H, I, k, seed, invalid=0.0, fmt=gen.NVFP4):
+    w = gen.make_expert_weights(E, H, I, fmt, seed, device="cuda")
     x = gen.draw_activations(M, H, seed + 1, device="cuda")
     ids, tw = gen.draw_routing(M, E, k, seed + 2)
     if invalid:
@@ -100,18 +100,20 @@ def _prefill_case(M, E, H, I, k, seed, invalid=0.0):
     return w, x, ids.cuda(), tw.cuda()
 
 
-@pytest.mark.parametrize("M,E,H,I,k,invalid", [(16, 4, 256, 256, 2, 0.0), (200, 8, 512, 256, 4, 0.05),
-                                               (600, 6, 768, 512, 3, 0.0)])
-def test_prefill_parity(M, E, H, I, k, invalid):
+@pytest.mark.parametrize("M,E,H,I,k,invalid,fmt", [(16, 4, 256, 256, 2, 0.0, gen.NVFP4),
+                                                   (200, 8, 512, 256, 4, 0.05, gen.NVFP4),
+                                                   (600, 6, 768, 512, 3, 0.0, gen.NVFP4),
+                                                   (300, 8, 512, 512, 4, 0.05, gen.MXFP4)])
+def test_prefill_parity(M, E, H, I, k, invalid, fmt):
     m = fm()
-    w, x, ids, tw = _prefill_case(M, E, H, I, k, seed=M + E, invalid=invalid)
-    pw = m.prepare_weights(w, E, H, I, gen.NVFP4)
-    ws = m.alloc_workspace(M, E, H, I, k, gen.NVFP4)
+    w, x, ids, tw = _prefill_case(M, E, H, I, k, seed=M + E, invalid=invalid, fmt=fmt)
+    pw = m.prepare_weights(w, E, H, I, fmt)
+    ws = m.alloc_workspace(M, E, H, I, k, fmt)
     out = torch.full((M, H), float("nan"), dtype=torch.bfloat16, device="cuda")
     got = m.forward(x, pw, ids, tw, out=out, workspace=ws)
     torch.cuda.synchronize()
-    want, _, _, _ = oracle.forward_prefill(x, w, ids, tw, E, H, I, k)
-    assert_layer_close(got, want, f"prefill M={M} E={E} H={H} I={I} k={k}")
+    want, _, _, _ = oracle.forward_prefill(x, w, ids, tw, E, H, I, k, fmt=fmt)
+    assert_layer_close(got, want, f"prefill M={M} E={E} H={H} I={I} k={k} fmt={fmt}")
 
 
 def test_prefill_repeat_and_library_workspace():
