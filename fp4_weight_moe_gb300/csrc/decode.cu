@@ -9,13 +9,13 @@ namespace moe_fp4 {
 size_t decode_tc_scratch_bytes(int M, int H, int I, int top_k, int num_sms);
 cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                              const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
-                             float* part1, uint32_t* status, int num_sms, cudaStream_t st, int* cu_err);
+                             float* scratch, uint32_t* status, int num_sms, cudaStream_t st, int* cu_err);
 
 static size_t decode_scratch_bytes(int M_max, int H, int I, int top_k, int num_sms) {
   return (decode_tc_scratch_bytes(M_max, H, I, top_k, num_sms) + 255) & ~(size_t)255;
 }
 
-// Scratch (FC1 partial sums, activation-term images), then a 256-byte status
+// Scratch (h, activation-term images), then a 256-byte status
 // block (bit flags of bounded waits that gave up; sticky).
 size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int fmt, int num_sms) {
   (void)fmt;

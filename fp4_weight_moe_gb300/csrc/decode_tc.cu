@@ -84,7 +84,10 @@ constexpr uint32_t kTmemSFBase = 32 * kRing;           // accumulator groups in 
 
 // FC2: split * M * ceil(128 / split) floats; split <= 8 gives at most
 // 7 * 19 = 133 per token (split 7), so 8 tokens fit in 8 * 136.
-constexpr int kPartFloats = 8 * 136;
+// FC1 (cluster of K ranges): split * M * 2 * ceil(64 / split) floats, at
+// most 7 * 2 * 10 = 140 per token (split 7); FC2: split * M * ceil(128 /
+// split), at most 133 per token.  8 tokens: 8 * 140.
+constexpr int kPartFloats = 8 * 140;
 
 struct SmemTc {
   float part[kPartFloats];         // partial sums received from the cluster
@@ -94,7 +97,9 @@ struct SmemTc {
   int own[kMaxSlotsTc];            // FC2: first slot naming each valid expert, in slot order
   int own_cnt[4];                  // FC2: owners per 32-slot chunk
   int expert;                      // FC1: this CTA's expert (-1: nothing to do)
-  float gmul[kMaxSlotsTc][3];      // FC2: gate, up, down multipliers per owner slot
+  float wtok[8];                   // FC1: router weight of the expert per token
+  float g3[3];                     // FC1: gate, up, down multipliers of the expert
+  uint32_t routed;                 // FC1: tokens routed to the expert (bit mask)
   uint64_t fullA[kRing];           // weight tile + its scale chunks landed (TMA)
   uint64_t fullB[kRing];           // activation terms + their scales in place (builders)
   uint64_t sfa[kRing];             // weight scales copied to tensor memory
@@ -113,7 +118,7 @@ struct TcArgs {
   const float* tw;
   const uint8_t* s13;
   const uint8_t* s2;
-  float* part1;  // [n_slots][split1][M][2I]: FC1 partial sums (resident row order), per K range
+  float* h;      // [n_slots][M][I]: FC1's output, SiLU(gate)*up*(router weight)*(down multiplier)
   uint8_t* ximg;  // per K stage of x: B tile (N rows x 128 B, swizzled), 512 B of scales, G [M][kTerms]
   int ximg_stride;
   uint8_t* himg;  // per (route slot, K stage of h): the same images for FC2, or null (FC2 builds its own)
@@ -121,7 +126,6 @@ struct TcArgs {
   uint32_t* status;
   int M, E, H, I, top_k, n_slots;
   int split;   // FC1: K ranges per w13 tile; FC2: CTAs (cluster size) per w2 tile
-  int split1;  // FC1's K ranges (read by FC2)
   int N;      // B rows per item (accumulator columns)
 };
 
@@ -245,6 +249,11 @@ __device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
   asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
   return r;
 }
+__device__ __forceinline__ int ld_nc_s32(const void* p) {
+  int r;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
 __device__ __forceinline__ float ld_nc_f32(const void* p) {
   float r;
   asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(r) : "l"(p));
@@ -261,62 +270,18 @@ __device__ __forceinline__ void load_bf16x8(const __nv_bfloat16* p, float (&v)[8
   }
 }
 
-// FC2's activations for route slot j (owner index o) and `token`, pairs
-// p0 .. p0+7 of the intermediate: FC1's partial gate/up sums of every K range,
-// added in range order, times the projection multipliers, SiLU(gate) * up,
-// times the router weight (summed over the token's slots naming the expert)
-// and the down multiplier -- exactly 0 for a token not routed to the expert.
-__device__ __forceinline__ void fc2_activation(const TcArgs& a, const int* ids, const float* tw, const float* gmul,
-                                               int j, int token, int p0, float (&v)[8]) {
-  const int e = ids[j];
-  float w = 0.f;
-  bool routed = false;
-  for (int k = 0; k < a.top_k; ++k)
-    if (ids[token * a.top_k + k] == e) {
-      w += tw[token * a.top_k + k];
-      routed = true;
-    }
-  if (!routed) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = 0.f;
-    return;
-  }
-  const size_t row_len = 2 * (size_t)a.I, kstride = (size_t)a.M * row_len;
-  const float* base = a.part1 + ((size_t)j * a.split1 * a.M + token) * row_len + (p0 >> 6) * 128 + (p0 & 63);
-  float g[8], u[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) g[i] = u[i] = 0.f;
-  for (int k0 = 0; k0 < a.split1; k0 += 2) {
-    uint4 q[2][4];
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      if (k0 + kk < a.split1) {
-        const float* pk = base + (size_t)(k0 + kk) * kstride;
-        q[kk][0] = ld_cg_v4(pk);
-        q[kk][1] = ld_cg_v4(pk + 4);
-        q[kk][2] = ld_cg_v4(pk + 64);
-        q[kk][3] = ld_cg_v4(pk + 68);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) q[kk][c] = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      const uint32_t gw[8] = {q[kk][0].x, q[kk][0].y, q[kk][0].z, q[kk][0].w,
-                              q[kk][1].x, q[kk][1].y, q[kk][1].z, q[kk][1].w};
-      const uint32_t uw[8] = {q[kk][2].x, q[kk][2].y, q[kk][2].z, q[kk][2].w,
-                              q[kk][3].x, q[kk][3].y, q[kk][3].z, q[kk][3].w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        g[i] += __uint_as_float(gw[i]);
-        u[i] += __uint_as_float(uw[i]);
-      }
-    }
-  }
-  const float gg = gmul[0], gu = gmul[1], wd = w * gmul[2];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = silu(g[i] * gg) * (u[i] * gu) * wd;
+// FC2's activations for route slot j and `token`: h at pairs p0 .. p0+7.
+__device__ __forceinline__ void fc2_activation(const TcArgs& a, int j, int token, int p0, float (&v)[8]) {
+  const float* p = a.h + ((size_t)j * a.M + token) * a.I + p0;
+  const uint4 u0 = ld_cg_v4(p), u1 = ld_cg_v4(p + 4);
+  v[0] = __uint_as_float(u0.x);
+  v[1] = __uint_as_float(u0.y);
+  v[2] = __uint_as_float(u0.z);
+  v[3] = __uint_as_float(u0.w);
+  v[4] = __uint_as_float(u1.x);
+  v[5] = __uint_as_float(u1.y);
+  v[6] = __uint_as_float(u1.z);
+  v[7] = __uint_as_float(u1.w);
 }
 
 // Activation pre-pass of FC1: the four NVFP4 terms of x for every (K stage,
@@ -346,34 +311,27 @@ __global__ void __launch_bounds__(256) decode_quant_x_kernel(TcArgs a) {
 
 // Activation pre-pass of FC2 (larger M): the four NVFP4 terms of h for every
 // (route slot that owns its expert, K stage of the intermediate, token),
-// from FC1's partial sums, stored as FC2's images.  One CTA per (slot,
+// stored as FC2's images.  One CTA per (slot,
 // stage), one warp per token.
 __global__ void __launch_bounds__(256) decode_quant_h_kernel(TcArgs a) {
   __shared__ int s_ids[kMaxSlotsTc];
-  __shared__ float s_tw[kMaxSlotsTc];
   pdl_launch_dependents();  // FC2 may start streaming its weights
   const int ns2 = (a.I + 255) / 256;
   const int j = blockIdx.x / ns2, st = blockIdx.x % ns2;
   const int token = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int k = threadIdx.x; k < a.n_slots; k += blockDim.x) {
-    s_ids[k] = __ldg(a.ids + k);
-    s_tw[k] = __ldg(a.tw + k);
-  }
+  for (int k = threadIdx.x; k < a.n_slots; k += blockDim.x) s_ids[k] = __ldg(a.ids + k);
   __syncthreads();
   const int e = s_ids[j];
   if (e < 0 || e >= a.E) return;
   for (int k = 0; k < j; ++k)
     if (s_ids[k] == e) return;  // an earlier slot owns this expert
-  const float* gl13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * (a.I / 64) * (a.H / 64) * kChunkBytes);
-  const float* gl2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * (a.H / 128) * (a.I / 64) * kChunkBytes);
-  const float gmul[3] = {ld_nc_f32(gl13 + 2 * e), ld_nc_f32(gl13 + 2 * e + 1), ld_nc_f32(gl2 + e)};
-  pdl_wait();  // FC1's partial sums are complete
+  pdl_wait();  // FC1's h is complete
   if (token >= a.M) return;
   const int rem = a.I / 64 - 4 * st;
   const bool act = lane < 8 * (rem < 4 ? rem : 4);
   float v[8];
   if (act) {
-    fc2_activation(a, s_ids, s_tw, gmul, j, token, st * 256 + lane * 8, v);
+    fc2_activation(a, j, token, st * 256 + lane * 8, v);
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = 0.f;
@@ -401,9 +359,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M = a.M, H = a.H, I = a.I, n = a.n_slots, N = a.N;
   const int split = a.split;
-  // FC1: independent CTAs, blockIdx = (slot, tile, K range); FC2: clusters
-  // of `split` CTAs per w2 row tile
-  const uint32_t rank = kFc2 ? cluster_rank() : (uint32_t)(blockIdx.x % split);
+  // FC1: clusters of `split` K ranges per (slot, w13 tile); FC2: clusters of
+  // `split` CTAs per w2 row tile
+  const uint32_t rank = cluster_rank();
   const int unit = blockIdx.x / split;  // FC1: slot * tiles1 + tile; FC2: w2 row tile
   const int tiles1 = I / 64, ns2 = (I + 255) / 256;
   const bool is_quant = warp >= kQuantWarp0 && warp < kQuantWarp0 + kQuantWarps;
@@ -412,7 +370,20 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   const bool use_img = !kFc2 || a.himg != nullptr;
   const bool is_epi = warp >= kEpiWarp0;
 
-  // ---- prologue: touches no input
+  // the routing first: its latency overlaps the barrier setup below (the
+  // kernels are launched only after whatever produced it is complete)
+  int idr[4];
+  float twr[4];
+  if (warp == 0) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int j = lane + 32 * k;
+      idr[k] = j < n ? ld_nc_s32(a.ids + j) : -1;
+      twr[k] = j < n ? ld_nc_f32(a.tw + j) : 0.f;
+    }
+  }
+
+  // ---- setup
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&S.fullA[s], 1);
@@ -423,18 +394,18 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     }
     for (int s = 0; s < kGSlots; ++s) mbar_init(&S.gready[s], kQuantWarps);
     mbar_init(&S.bsf, kQuantWarps);
-    if (kFc2) {
-      // the output rows this CTA reduces (r = rank mod split), one partial
-      // from every CTA of the cluster
-      mbar_init(&S.red, 1);
-      mbar_arrive_expect_tx(&S.red, (uint32_t)(split * ((128 - (int)rank + split - 1) / split) * M * 4));
-    }
+    // the partial rows this CTA reduces, one from every CTA of the cluster:
+    // FC1 the gate and up rows of pairs p = rank mod split, FC2 the rows
+    // r = rank mod split
+    mbar_init(&S.red, 1);
+    const int own = kFc2 ? (128 - (int)rank + split - 1) / split : 2 * ((64 - (int)rank + split - 1) / split);
+    mbar_arrive_expect_tx(&S.red, (uint32_t)(split * own * M * 4));
     fence_mbar_init();
     tma_prefetch_desc(&map_w);
   }
-  // FC2 cluster phase 1: this CTA runs and its barriers are initialised
+  // cluster phase 1: this CTA runs and its barriers are initialised
   // (awaited before any remote store)
-  if (kFc2) cluster_arrive_release();
+  cluster_arrive_release();
   if (warp == kMmaWarp0) tmem_alloc(&S.tmem, kTmemColsTc);
   // Both kernels are launched only after the activation pre-pass has passed
   // its wait on whatever produced x and the routing, so they may read the
@@ -489,10 +460,12 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     n_items = ((int)rank + 1) * nk / split - k0;
   }
   if (warp == 0) {
-    for (int j = lane; j < n; j += 32) {
-      S.ids[j] = __ldg(a.ids + j);
-      S.tw[j] = __ldg(a.tw + j);
-    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (lane + 32 * k < n) {
+        S.ids[lane + 32 * k] = idr[k];
+        S.tw[lane + 32 * k] = twr[k];
+      }
     __syncwarp();
     if (!kFc2) {
       // does an earlier slot name the same expert?  If not, stream the first
@@ -508,6 +481,18 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
         if (ok)
           for (int i = 0; i < n_items && i < kRing; ++i) issue(i, e);
       }
+      // router weight of this expert per token
+      float wt = 0.f;
+      bool rt = false;
+      if (lane < M)
+        for (int k = 0; k < a.top_k; ++k)
+          if (S.ids[lane * a.top_k + k] == e) {
+            wt += S.tw[lane * a.top_k + k];
+            rt = true;
+          }
+      const uint32_t rm = __ballot_sync(0xffffffffu, rt);
+      if (lane < M) S.wtok[lane] = wt;
+      if (lane == 0) S.routed = rm;
     }
   }
   tc_fence_before();
@@ -518,9 +503,14 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   int e1 = -1;
   if (!kFc2) {
     e1 = S.expert;
-    if (e1 < 0) {  // an earlier slot names this expert and does the work
+    if (e1 < 0) {  // an earlier slot names this expert: the whole cluster leaves
       if (warp == kMmaWarp0) tmem_dealloc(S.tmem, kTmemColsTc);
       return;
+    }
+    if (warp == kQuantWarp0 && lane < 3) {  // (FC1's builder warps are free)
+      const float* gl13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * tiles1 * (H / 64) * kChunkBytes);
+      const float* gl2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * (H / 128) * (I / 64) * kChunkBytes);
+      S.g3[lane] = ld_nc_f32(lane < 2 ? gl13 + 2 * e1 + lane : gl2 + e1);
     }
   } else {
     // owners: the first slot naming each valid expert, in slot order
@@ -543,14 +533,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     if (own_j) {
       int base = 0;
       for (int c = 0; c < warp; ++c) base += S.own_cnt[c];
-      const int o = base + __popc(bal & ((1u << lane) - 1u));
-      S.own[o] = j;
-      const int e = S.ids[j];
-      const float* gl13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * tiles1 * (H / 64) * kChunkBytes);
-      const float* gl2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * (H / 128) * (I / 64) * kChunkBytes);
-      S.gmul[o][0] = ld_nc_f32(gl13 + 2 * e);
-      S.gmul[o][1] = ld_nc_f32(gl13 + 2 * e + 1);
-      S.gmul[o][2] = ld_nc_f32(gl2 + e);
+      S.own[base + __popc(bal & ((1u << lane) - 1u))] = j;
     }
     n_own = S.own_cnt[0] + S.own_cnt[1] + S.own_cnt[2] + S.own_cnt[3];
     __syncwarp();
@@ -608,7 +591,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   } else if (is_quant) {
     // ---------------- FC2: activation terms (B operand), one wave of ring slots at a time
     if (!use_img) {  // (otherwise the terms come from a pre-pass)
-    pdl_wait();  // FC1's partial sums are complete and visible
+    pdl_wait();  // FC1's h is complete and visible
     const int waves = (n_items + kRing - 1) / kRing;
     for (int w = 0; w < waves; ++w) {
       const int i0 = w * kRing, wi = n_items - i0 < kRing ? n_items - i0 : kRing;
@@ -625,8 +608,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
         const bool act = lane < 8 * item_groups(item);  // lanes beyond the stage's valid K
         float v[8];
         if (act) {
-          fc2_activation(a, S.ids, S.tw, S.gmul[((int)rank + split * item) % n_own], item_slot(item), token,
-                         item_stage(item) * 256 + lane * 8, v);
+          fc2_activation(a, item_slot(item), token, item_stage(item) * 256 + lane * 8, v);
         } else {
 #pragma unroll
           for (int j = 0; j < 8; ++j) v[j] = 0.f;
@@ -736,29 +718,26 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     }
   }
 
+  // ---- cluster reduction: partial rows go to their owner CTA (asynchronous
+  // stores counted on its barrier), summed there in rank order
   tc_fence_before();
   __syncwarp();
-  if (!kFc2) {
-    // FC1: this CTA's partial gate/up rows, for FC2 to combine
-    if (is_epi) {
-      const int row = 32 * (warp & 3) + lane;
-#pragma unroll
-      for (int t = 0; t < 8; ++t)
-        if (t < M)
-          a.part1[(((size_t)slot1 * split + rank) * M + t) * (2 * I) + tile * 128 + row] = vout[t];
-    }
-    __syncwarp();
-    __syncthreads();  // tensor memory is no longer read
-    if (warp == kMmaWarp0) tmem_dealloc(S.tmem, kTmemColsTc);
-    return;
-  }
-  // ---- FC2 cluster reduction: partial rows go to their owner CTA
-  // (asynchronous stores counted on its barrier), summed there in rank order
   cluster_wait();  // phase 1: every CTA of the cluster runs
-  const int rpo = (128 + split - 1) / split;  // row r is owned by rank r % split
+  // FC1: pair p is owned by rank p % split (cpo pairs each, gate and up rows);
+  // FC2: row r by rank r % split
+  const int cpo = (64 + split - 1) / split;
+  const int rpo = kFc2 ? (128 + split - 1) / split : 2 * cpo;
   if (is_epi) {
     const int row = 32 * (warp & 3) + lane;
-    const int owner = row % split, j = row / split;
+    int owner, j;
+    if (!kFc2) {
+      const int pr = row & 63;
+      owner = pr % split;
+      j = (row >> 6) * cpo + pr / split;
+    } else {
+      owner = row % split;
+      j = row / split;
+    }
 #pragma unroll
     for (int t = 0; t < 8; ++t)
       if (t < M) st_async_peer_f32(&S.part[((int)rank * M + t) * rpo + j], &S.red, (uint32_t)owner, vout[t]);
@@ -767,12 +746,27 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   __syncthreads();  // tensor memory is no longer read
   if (warp == kMmaWarp0) tmem_dealloc(S.tmem, kTmemColsTc);
   if (!__all_sync(0xffffffffu, mbar_wait(&S.red, 0, a.status, 128u))) return;
-  for (int idx = threadIdx.x; idx < M * rpo; idx += kTcThreads) {
-    const int token = idx / rpo, j = idx % rpo, row = (int)rank + split * j;
-    if (row >= 128) continue;
-    float v = 0.f;
-    for (int src = 0; src < split; ++src) v += S.part[(src * M + token) * rpo + j];
-    a.out[(size_t)token * H + unit * 128 + row] = __float2bfloat16_rn(v);
+  if (!kFc2) {
+    for (int idx = threadIdx.x; idx < M * cpo; idx += kTcThreads) {
+      const int token = idx / cpo, jj = idx % cpo, pair = (int)rank + split * jj;
+      if (pair >= 64) continue;
+      float gate = 0.f, up = 0.f;
+      for (int src = 0; src < split; ++src) {
+        gate += S.part[(src * M + token) * rpo + jj];
+        up += S.part[(src * M + token) * rpo + cpo + jj];
+      }
+      const float hv =
+          (S.routed >> token) & 1u ? silu(gate * S.g3[0]) * (up * S.g3[1]) * (S.wtok[token] * S.g3[2]) : 0.f;
+      a.h[((size_t)slot1 * M + token) * I + tile * 64 + pair] = hv;
+    }
+  } else {
+    for (int idx = threadIdx.x; idx < M * rpo; idx += kTcThreads) {
+      const int token = idx / rpo, j = idx % rpo, row = (int)rank + split * j;
+      if (row >= 128) continue;
+      float v = 0.f;
+      for (int src = 0; src < split; ++src) v += S.part[(src * M + token) * rpo + j];
+      a.out[(size_t)token * H + unit * 128 + row] = __float2bfloat16_rn(v);
+    }
   }
 }
 
@@ -788,12 +782,15 @@ int fc1_split(int n_slots, int H, int I, int sms) {
 }
 
 // CTAs per w2 row tile (the cluster): 8, or the number of (slot, K stage)
-// items if smaller (measured best: the items of a tile spread over more SMs).
+// items if smaller (measured best: the items of a tile spread over more SMs);
+// fewer when that lets all of FC2 start at once beside FC1 (one CTA per SM)
+// without giving up more than a sixth of the CTAs.
 int fc2_split(int n_slots, int H, int I, int sms) {
-  (void)H;
-  (void)sms;
-  const int items = n_slots * ((I + 255) / 256);
-  return items < 8 ? (items < 1 ? 1 : items) : 8;
+  const int tiles = H / 128, items = n_slots * ((I + 255) / 256);
+  int q = items < 8 ? (items < 1 ? 1 : items) : 8;
+  const int fit = sms / tiles;
+  if (q * tiles > sms && fit >= 1 && fit < q && 6 * fit * tiles >= 5 * sms) q = fit;
+  return q;
 }
 
 }  // namespace
@@ -803,9 +800,8 @@ static int ximg_stride(int M) {
   const int N = (kTerms * M + 15) / 16 * 16;
   return (N * 128 + kChunkBytes + 16 * M + 127) / 128 * 128;
 }
-static size_t part1_bytes(int M, int H, int I, int top_k, int num_sms) {
-  const int n = M * top_k;
-  const size_t b = (size_t)n * fc1_split(n, H, I, num_sms > 0 ? num_sms : 152) * M * 2 * (size_t)I * sizeof(float);
+static size_t h_bytes(int M, int I, int top_k) {
+  const size_t b = (size_t)M * top_k * M * (size_t)I * sizeof(float);
   return (b + 255) & ~(size_t)255;
 }
 
@@ -814,18 +810,18 @@ static size_t part1_bytes(int M, int H, int I, int top_k, int num_sms) {
 // FC2 builds them itself and the layer saves a launch on its critical path.
 constexpr int kHPrepassMinM = 2;
 
-// FC1's partial sums [M*top_k slots][K ranges][M][2I] FP32, the activation
-// images of x's H/256 K stages, and (M >= kHPrepassMinM) those of h's
-// (slot, K stage) pairs.
+// h [M*top_k slots][M][I] FP32, the activation images of x's H/256 K
+// stages, and (M >= kHPrepassMinM) those of h's (slot, K stage) pairs.
 size_t decode_tc_scratch_bytes(int M, int H, int I, int top_k, int num_sms) {
-  size_t b = part1_bytes(M, H, I, top_k, num_sms) + (size_t)(H / 256) * ximg_stride(M);
+  (void)num_sms;
+  size_t b = h_bytes(M, I, top_k) + (size_t)(H / 256) * ximg_stride(M);
   if (M >= kHPrepassMinM) b += (size_t)M * top_k * ((I + 255) / 256) * ximg_stride(M);
   return b;
 }
 
 cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                              const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
-                             float* part1, uint32_t* status, int num_sms, cudaStream_t st, int* cu_err) {
+                             float* scratch, uint32_t* status, int num_sms, cudaStream_t st, int* cu_err) {
   CUtensorMap m13, m2;
   CUresult r = make_fp4_map(&m13, w13, (uint64_t)H / 2, (uint64_t)E * 2 * I, 128);
   if (r == CUDA_SUCCESS) r = make_fp4_map(&m2, w2, (uint64_t)I / 2, (uint64_t)E * H, 128);
@@ -850,8 +846,8 @@ cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, co
   a.tw = tw;
   a.s13 = static_cast<const uint8_t*>(s13);
   a.s2 = static_cast<const uint8_t*>(s2);
-  a.part1 = part1;
-  a.ximg = reinterpret_cast<uint8_t*>(part1) + part1_bytes(M, H, I, top_k, num_sms);
+  a.h = scratch;
+  a.ximg = reinterpret_cast<uint8_t*>(scratch) + h_bytes(M, I, top_k);
   a.ximg_stride = ximg_stride(M);
   a.himg = M >= kHPrepassMinM ? a.ximg + (size_t)(H / 256) * a.ximg_stride : nullptr;
   a.out = static_cast<__nv_bfloat16*>(out);
@@ -883,17 +879,20 @@ cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, co
   const int units1 = a.n_slots * (I / 64);
   const int s1 = fc1_split(a.n_slots, H, I, sms);
   a.split = s1;
-  a.split1 = s1;
-  cudaLaunchAttribute at1[1];
-  at1[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at1[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute at1[2];
+  at1[0].id = cudaLaunchAttributeClusterDimension;
+  at1[0].val.clusterDim.x = (unsigned)s1;
+  at1[0].val.clusterDim.y = 1;
+  at1[0].val.clusterDim.z = 1;
+  at1[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at1[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t c1 = {};
   c1.gridDim = dim3((unsigned)(units1 * s1));
   c1.blockDim = dim3(kTcThreads);
   c1.dynamicSmemBytes = kTcSmem;
   c1.stream = st;
   c1.attrs = at1;
-  c1.numAttrs = 1;
+  c1.numAttrs = 2;
   err = cudaLaunchKernelEx(&c1, decode_tc_kernel<false>, m13, a);
   if (err != cudaSuccess) return err;
 
