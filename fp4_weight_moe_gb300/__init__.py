@@ -134,6 +134,38 @@ def forward(x: torch.Tensor, pw: PreparedWeights, topk_ids: torch.Tensor, topk_w
     return out
 
 
+def host_workspace_bytes(M_max: int, E: int, H: int, I: int, top_k: int, fmt: int) -> int:
+    return _capi.moe_fp4_host_workspace_bytes(M_max, E, H, I, top_k, fmt)
+
+
+def alloc_host_workspace(M_max: int, E: int, H: int, I: int, top_k: int, fmt: int, device=None) -> torch.Tensor:
+    """A zero-filled device workspace for ``forward_host``."""
+    n = host_workspace_bytes(M_max, E, H, I, top_k, fmt)
+    if n == 0:
+        raise MoeFp4Error("moe_fp4_host_workspace_bytes", _capi.MOE_FP4_EUNSUPPORTED)
+    return torch.zeros(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+
+
+def forward_host(x: torch.Tensor, pw: PreparedWeights, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                 out: torch.Tensor, workspace: torch.Tensor, stream=None) -> torch.Tensor:
+    """The layer on HOST tensors (pinned for asynchronous copies): enqueues the
+    input copies, the layer and the output copy on ``stream``; ``out`` holds
+    the result once the stream has been synchronised."""
+    if x.dtype != torch.bfloat16 or topk_ids.dtype != torch.int32 or topk_weights.dtype != torch.float32:
+        raise TypeError("x must be bfloat16, topk_ids int32, topk_weights float32")
+    if out.dtype != torch.bfloat16 or out.shape != x.shape:
+        raise TypeError("out must be bfloat16 of x's shape")
+    for t in (x, topk_ids, topk_weights, out):
+        if not t.is_contiguous():
+            raise ValueError("host tensors must be contiguous")
+    _require_cuda(workspace)
+    M, H = x.shape
+    _capi.moe_fp4_forward_host(_ptr(x), *pw.ptrs(), _ptr(topk_ids), _ptr(topk_weights), _ptr(out), M, pw.E, pw.H,
+                               pw.I, topk_ids.shape[1], pw.fmt, _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    return out
+
+
 def debug_dequant(pw: PreparedWeights, which: int, expert: int, stream=None) -> torch.Tensor:
     rows, K = (2 * pw.I, pw.H) if which == 0 else (pw.H, pw.I)
     out = torch.empty((rows, K), dtype=torch.float32, device=pw.w13.device)

@@ -43,6 +43,8 @@ SIGNATURES = {
     "moe_fp4_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "moe_fp4_forward_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "moe_fp4_forward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "moe_fp4_host_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
+    "moe_fp4_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "moe_fp4_debug_dequant": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "moe_fp4_debug_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_fp4_debug_route": (_I, [_P, _I, _I, _I, _P, _P, _P, _Z, _P]),
@@ -143,6 +145,16 @@ def moe_fp4_forward_ws(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt
 def moe_fp4_forward_noalloc(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt, stream):
     return _check("moe_fp4_forward_noalloc",
                   _load().moe_fp4_forward_noalloc(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt, stream))
+
+
+def moe_fp4_host_workspace_bytes(M_max, E, H, I, top_k, fmt) -> int:
+    return int(_load().moe_fp4_host_workspace_bytes(M_max, E, H, I, top_k, fmt))
+
+
+def moe_fp4_forward_host(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt, ws, ws_bytes, stream):
+    return _check("moe_fp4_forward_host",
+                  _load().moe_fp4_forward_host(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt, ws,
+                                               ws_bytes, stream))
 
 
 def moe_fp4_debug_dequant(w, s, which, expert, E, H, I, fmt, out, stream):

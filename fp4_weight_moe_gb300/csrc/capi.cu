@@ -90,6 +90,24 @@ size_t workspace_need(int M, int E, int H, int I, int top_k, int fmt, int sms) {
   return d;
 }
 
+size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// Host-buffer staging area of moe_fp4_forward_host: x, ids, router weights and
+// the output, each 256-byte aligned, placed right after the layer's own
+// workspace for M tokens.
+struct HostStage {
+  size_t x, ids, tw, out, total;
+};
+HostStage host_stage(int M, int H, int top_k) {
+  HostStage h;
+  h.x = 0;
+  h.ids = h.x + align256((size_t)M * H * 2);
+  h.tw = h.ids + align256((size_t)M * top_k * 4);
+  h.out = h.tw + align256((size_t)M * top_k * 4);
+  h.total = h.out + align256((size_t)M * H * 2);
+  return h;
+}
+
 struct LibWorkspace {
   void* ptr = nullptr;
   size_t bytes = 0;
@@ -266,6 +284,49 @@ int moe_fp4_forward(const void* x_bf16, const void* w13, const void* s13, const 
   if (M > 0 && !ptr) return MOE_FP4_EWORKSPACE;
   return moe_fp4_forward_ws(x_bf16, w13, s13, w2, s2, topk_ids, topk_weights, out_bf16, M, E, H, I, top_k, fmt, ptr,
                             bytes, stream);
+}
+
+size_t moe_fp4_host_workspace_bytes(int M_max, int E, int H, int I, int top_k, int fmt) {
+  if (check_shape(E, H, I, top_k, fmt) != MOE_FP4_OK || M_max <= 0) return 0;
+  if (M_max > MOE_FP4_DECODE_MAX_M && check_prefill(M_max, E, I, top_k, fmt) != MOE_FP4_OK) return 0;
+  int sms = 0;
+  if (device_sms(&sms) != MOE_FP4_OK) return 0;
+  // both parts grow with M, so the M_max layout covers every smaller batch
+  return align256(workspace_need(M_max, E, H, I, top_k, fmt, sms)) + host_stage(M_max, H, top_k).total;
+}
+
+int moe_fp4_forward_host(const void* x_bf16, const void* w13, const void* s13, const void* w2, const void* s2,
+                         const int32_t* topk_ids, const float* topk_weights, void* out_bf16, int M, int E, int H,
+                         int I, int top_k, int fmt, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_shape(E, H, I, top_k, fmt);
+  if (st != MOE_FP4_OK) return st;
+  if (M < 0) return MOE_FP4_EINVAL;
+  if (M == 0) return MOE_FP4_OK;
+  if (!x_bf16 || !topk_ids || !topk_weights || !out_bf16) return MOE_FP4_EINVAL;
+  if (M > MOE_FP4_DECODE_MAX_M) {
+    st = check_prefill(M, E, I, top_k, fmt);
+    if (st != MOE_FP4_OK) return st;
+  }
+  if (!workspace || ((uintptr_t)workspace & 255u)) return MOE_FP4_EWORKSPACE;
+  int sms = 0;
+  st = device_sms(&sms);
+  if (st != MOE_FP4_OK) return st;
+  const size_t base = align256(workspace_need(M, E, H, I, top_k, fmt, sms));
+  const HostStage hs = host_stage(M, H, top_k);
+  if (base + hs.total >= kMaxWorkspace || workspace_bytes < base + hs.total) return MOE_FP4_EWORKSPACE;
+  char* stage = static_cast<char*>(workspace) + base;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t xb = (size_t)M * H * 2, rb = (size_t)M * top_k * 4;
+  cudaError_t e = cudaMemcpyAsync(stage + hs.x, x_bf16, xb, cudaMemcpyDefault, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(stage + hs.ids, topk_ids, rb, cudaMemcpyDefault, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(stage + hs.tw, topk_weights, rb, cudaMemcpyDefault, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  st = moe_fp4_forward_ws(stage + hs.x, w13, s13, w2, s2, reinterpret_cast<const int32_t*>(stage + hs.ids),
+                          reinterpret_cast<const float*>(stage + hs.tw), stage + hs.out, M, E, H, I, top_k, fmt,
+                          workspace, base, stream);
+  if (st != MOE_FP4_OK) return st;
+  e = cudaMemcpyAsync(out_bf16, stage + hs.out, xb, cudaMemcpyDefault, s);
+  return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
 }
 
 int moe_fp4_debug_dequant(const void* w, const void* s, int which, int expert, int E, int H, int I, int fmt,

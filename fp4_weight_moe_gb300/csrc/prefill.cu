@@ -1,5 +1,7 @@
 // Prefill band building blocks: the tcgen05 block-scaled FP4 GEMM and its
 // test-support entry point.
+#include <mutex>
+
 #include "gemm_fp4.cuh"
 
 namespace moe_fp4 {
@@ -24,16 +26,47 @@ static EncodeTiledFn encode_tiled() {
 
 // 2-D tensor map over a row-major byte matrix [rows][inner_bytes], box of
 // box_rows x 128 bytes, 128-byte swizzle (the K-major SW128 operand layout).
+// Encoded maps are kept in a small cache keyed by all four arguments (a map
+// depends on nothing else), so repeated layer calls skip the encoding.
 CUresult make_fp4_map(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint32_t box_rows) {
+  struct Entry {
+    const void* base;
+    uint64_t inner, rows;
+    uint32_t box;
+    CUtensorMap map;
+  };
+  static Entry cache[64];
+  static int n_used = 0, next = 0;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < n_used; ++i)
+      if (cache[i].base == base && cache[i].inner == inner_bytes && cache[i].rows == rows && cache[i].box == box_rows) {
+        *m = cache[i].map;
+        return CUDA_SUCCESS;
+      }
+  }
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return CUDA_ERROR_NOT_FOUND;
   cuuint64_t dims[2] = {inner_bytes, rows};
   cuuint64_t strides[1] = {inner_bytes};
   cuuint32_t box[2] = {128, box_rows};
   cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS) {
+    std::lock_guard<std::mutex> lk(mu);
+    Entry& e = cache[next];
+    e.base = base;
+    e.inner = inner_bytes;
+    e.rows = rows;
+    e.box = box_rows;
+    e.map = *m;
+    next = (next + 1) % 64;
+    if (n_used < 64) ++n_used;
+  }
+  return r;
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1)

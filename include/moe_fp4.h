@@ -177,6 +177,42 @@ MOE_FP4_API int moe_fp4_forward_ws(const void *x_bf16, const void *w13, const vo
                        int I, int top_k, int fmt, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Workspace bytes needed by moe_fp4_forward_host for up to M_max tokens: the
+ * layer's own workspace plus a staging area for the inputs and the output.
+ * Returns 0 for invalid or unsupported arguments.  Queries the current
+ * device's SM count.
+ */
+MOE_FP4_API size_t moe_fp4_host_workspace_bytes(int M_max, int E, int H, int I, int top_k, int fmt);
+
+/*
+ * The fused MoE layer with its per-call tensors in HOST memory:
+ *   x_bf16       [M][H] bf16, host
+ *   topk_ids     [M][top_k] int32, host
+ *   topk_weights [M][top_k] f32, host
+ *   out_bf16     [M][H] bf16, host, fully overwritten
+ *   w13, s13, w2, s2  resident weights on the device (moe_fp4_prepare_weights)
+ *   workspace    device memory of moe_fp4_host_workspace_bytes(M, ...) bytes
+ *                or more, 256-byte aligned, zero-filled before its first use
+ * Enqueues on `stream`, in order: one host-to-device copy per input into the
+ * workspace's staging area, the layer (the kernels of moe_fp4_forward_ws),
+ * and one device-to-host copy of the output.  Returns once everything is
+ * enqueued: out_bf16 holds the result when the stream has reached that point
+ * (cudaStreamSynchronize or an event), and the host buffers must stay valid
+ * until then.  Page-locked host buffers (cudaHostAlloc / cudaHostRegister)
+ * make the copies asynchronous; pageable ones work but the copies may block
+ * the calling thread.  Device pointers are accepted in place of host ones
+ * (the copies become device-to-device).  Results, M = 0 and the error codes
+ * are those of moe_fp4_forward_ws; a workspace that is too small gives
+ * MOE_FP4_EWORKSPACE before anything is enqueued.  Calls sharing a workspace
+ * must be ordered.  The pages have no counterpart of this entry point: it is
+ * the library's end-to-end call for callers whose tensors live on the host.
+ */
+MOE_FP4_API int moe_fp4_forward_host(const void *x_bf16, const void *w13, const void *s13, const void *w2,
+                                     const void *s2, const int32_t *topk_ids, const float *topk_weights,
+                                     void *out_bf16, int M, int E, int H, int I, int top_k, int fmt, void *workspace,
+                                     size_t workspace_bytes, void *stream);
+
+/*
  * The decode-band layer (M <= MOE_FP4_DECODE_MAX_M) without any device
  * allocation, for callers that cannot call cudaMalloc where they run the
  * layer: inside a stream capture, under a runtime that owns all device memory
