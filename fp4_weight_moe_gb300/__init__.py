@@ -29,8 +29,16 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
-def _stream(stream) -> Optional[int]:
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, device: Optional[torch.device] = None) -> Optional[int]:
+    """Raw cudaStream_t of ``stream`` (None: the current stream of ``device``,
+    else of the current device)."""
     if stream is None:
+        if _raw_stream is not None:
+            idx = device.index if device is not None and device.index is not None else torch.cuda.current_device()
+            return _raw_stream(idx)
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream
@@ -55,8 +63,11 @@ class PreparedWeights:
     I: int
     fmt: int
 
+    def __post_init__(self):
+        self._ptrs = (_ptr(self.w13), _ptr(self.s13), _ptr(self.w2), _ptr(self.s2))
+
     def ptrs(self):
-        return _ptr(self.w13), _ptr(self.s13), _ptr(self.w2), _ptr(self.s2)
+        return self._ptrs
 
 
 def prepared_sizes(E: int, H: int, I: int, fmt: int):
@@ -128,9 +139,10 @@ def forward(x: torch.Tensor, pw: PreparedWeights, topk_ids: torch.Tensor, topk_w
         out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
     args = (_ptr(x), *pw.ptrs(), _ptr(topk_ids), _ptr(topk_weights), _ptr(out), M, pw.E, pw.H, pw.I, top_k, pw.fmt)
     if workspace is None:
-        _capi.moe_fp4_forward(*args, _stream(stream))
+        _capi.moe_fp4_forward(*args, _stream(stream, x.device))
     else:
-        _capi.moe_fp4_forward_ws(*args, _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+        _capi.moe_fp4_forward_ws(*args, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream(stream, x.device))
     return out
 
 
@@ -155,14 +167,14 @@ def forward_host(x: torch.Tensor, pw: PreparedWeights, topk_ids: torch.Tensor, t
         raise TypeError("x must be bfloat16, topk_ids int32, topk_weights float32")
     if out.dtype != torch.bfloat16 or out.shape != x.shape:
         raise TypeError("out must be bfloat16 of x's shape")
-    for t in (x, topk_ids, topk_weights, out):
-        if not t.is_contiguous():
-            raise ValueError("host tensors must be contiguous")
-    _require_cuda(workspace)
+    if not (x.is_contiguous() and topk_ids.is_contiguous() and topk_weights.is_contiguous() and out.is_contiguous()):
+        raise ValueError("host tensors must be contiguous")
+    if not workspace.is_cuda:
+        raise ValueError("the workspace must be a CUDA tensor")
     M, H = x.shape
-    _capi.moe_fp4_forward_host(_ptr(x), *pw.ptrs(), _ptr(topk_ids), _ptr(topk_weights), _ptr(out), M, pw.E, pw.H,
-                               pw.I, topk_ids.shape[1], pw.fmt, _ptr(workspace),
-                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _capi.moe_fp4_forward_host(x.data_ptr(), *pw.ptrs(), topk_ids.data_ptr(), topk_weights.data_ptr(), out.data_ptr(),
+                               M, pw.E, pw.H, pw.I, topk_ids.shape[1], pw.fmt, workspace.data_ptr(),
+                               workspace.nbytes, _stream(stream, workspace.device))
     return out
 
 

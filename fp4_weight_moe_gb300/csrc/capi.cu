@@ -108,6 +108,24 @@ HostStage host_stage(int M, int H, int top_k) {
   return h;
 }
 
+// The address under which the current device reaches `p`, or null if it
+// cannot (pageable host memory, another device's memory) or `p` is not
+// 16-byte aligned.  Page-locked host memory is mapped for every device on a
+// unified-address system, so its device view is usable by the kernels.
+void* device_view(const void* p) {
+  if (!aligned16(p)) return nullptr;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+  if (a.type == cudaMemoryTypeDevice && a.device == dev) return a.devicePointer;
+  return nullptr;
+}
+
 struct LibWorkspace {
   void* ptr = nullptr;
   size_t bytes = 0;
@@ -317,15 +335,36 @@ int moe_fp4_forward_host(const void* x_bf16, const void* w13, const void* s13, c
   char* stage = static_cast<char*>(workspace) + base;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t xb = (size_t)M * H * 2, rb = (size_t)M * top_k * 4;
-  cudaError_t e = cudaMemcpyAsync(stage + hs.x, x_bf16, xb, cudaMemcpyDefault, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(stage + hs.ids, topk_ids, rb, cudaMemcpyDefault, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(stage + hs.tw, topk_weights, rb, cudaMemcpyDefault, s);
+  // In the decode band, buffers the GPU can address (page-locked host
+  // memory, mapped into the device's address space over the CPU-GPU link) are
+  // read and written in place by the kernels: a few KB each, where a copy's
+  // fixed cost would exceed the layer's.  Everything else, and the prefill
+  // band's large tensors, go through the staging area.
+  const bool decode = M <= MOE_FP4_DECODE_MAX_M;
+  void* xd = decode ? device_view(x_bf16) : nullptr;
+  void* idd = decode ? device_view(topk_ids) : nullptr;
+  void* twd = decode ? device_view(topk_weights) : nullptr;
+  void* od = decode ? device_view(out_bf16) : nullptr;
+  cudaError_t e = cudaSuccess;
+  if (!xd) {
+    xd = stage + hs.x;
+    e = cudaMemcpyAsync(xd, x_bf16, xb, cudaMemcpyDefault, s);
+  }
+  if (!idd && e == cudaSuccess) {
+    idd = stage + hs.ids;
+    e = cudaMemcpyAsync(idd, topk_ids, rb, cudaMemcpyDefault, s);
+  }
+  if (!twd && e == cudaSuccess) {
+    twd = stage + hs.tw;
+    e = cudaMemcpyAsync(twd, topk_weights, rb, cudaMemcpyDefault, s);
+  }
   if (e != cudaSuccess) return fail_cuda(e);
-  st = moe_fp4_forward_ws(stage + hs.x, w13, s13, w2, s2, reinterpret_cast<const int32_t*>(stage + hs.ids),
-                          reinterpret_cast<const float*>(stage + hs.tw), stage + hs.out, M, E, H, I, top_k, fmt,
-                          workspace, base, stream);
-  if (st != MOE_FP4_OK) return st;
-  e = cudaMemcpyAsync(out_bf16, stage + hs.out, xb, cudaMemcpyDefault, s);
+  const bool out_direct = od != nullptr;
+  if (!out_direct) od = stage + hs.out;
+  st = moe_fp4_forward_ws(xd, w13, s13, w2, s2, static_cast<const int32_t*>(idd), static_cast<const float*>(twd), od,
+                          M, E, H, I, top_k, fmt, workspace, base, stream);
+  if (st != MOE_FP4_OK || out_direct) return st;
+  e = cudaMemcpyAsync(out_bf16, od, xb, cudaMemcpyDefault, s);
   return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
 }
 

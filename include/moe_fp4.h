@@ -193,15 +193,19 @@ MOE_FP4_API size_t moe_fp4_host_workspace_bytes(int M_max, int E, int H, int I, 
  *   w13, s13, w2, s2  resident weights on the device (moe_fp4_prepare_weights)
  *   workspace    device memory of moe_fp4_host_workspace_bytes(M, ...) bytes
  *                or more, 256-byte aligned, zero-filled before its first use
- * Enqueues on `stream`, in order: one host-to-device copy per input into the
- * workspace's staging area, the layer (the kernels of moe_fp4_forward_ws),
- * and one device-to-host copy of the output.  Returns once everything is
+ * Enqueues on `stream` the layer (the kernels of moe_fp4_forward_ws) and
+ * the transfers of its per-call tensors.  In the decode band
+ * (M <= MOE_FP4_DECODE_MAX_M) a 16-byte-aligned buffer that the current
+ * device can address (page-locked host memory from cudaHostAlloc or
+ * cudaHostRegister, mapped over the CPU-GPU link; or memory of the current
+ * device) is read or written in place by the kernels.  Any other buffer, and
+ * every buffer in the prefill band, goes through the workspace's staging
+ * area: one host-to-device copy per input before the layer, one
+ * device-to-host copy of the output after it.  Returns once everything is
  * enqueued: out_bf16 holds the result when the stream has reached that point
  * (cudaStreamSynchronize or an event), and the host buffers must stay valid
- * until then.  Page-locked host buffers (cudaHostAlloc / cudaHostRegister)
- * make the copies asynchronous; pageable ones work but the copies may block
- * the calling thread.  Device pointers are accepted in place of host ones
- * (the copies become device-to-device).  Results, M = 0 and the error codes
+ * and unmodified until then.  Pageable buffers work, but their copies may
+ * block the calling thread.  Results, M = 0 and the error codes
  * are those of moe_fp4_forward_ws; a workspace that is too small gives
  * MOE_FP4_EWORKSPACE before anything is enqueued.  Calls sharing a workspace
  * must be ordered.  The pages have no counterpart of this entry point: it is

@@ -1,12 +1,13 @@
 """moe_fp4_forward_host: the layer on host buffers.
 
-The entry point copies x, the expert ids and the router weights from host
-memory into its workspace, runs the same kernels as moe_fp4_forward_ws and
-copies the output back, all on one stream.  These tests check that its result
-equals moe_fp4_forward_ws on device copies of the same inputs (bitwise in the
+In the decode band the kernels read page-locked host inputs and write a
+page-locked host output in place; other buffers (and all of them in the
+prefill band) are copied through the workspace.  Either way the layer runs
+the same kernels as moe_fp4_forward_ws, on one stream.  These tests check
+that its result equals moe_fp4_forward_ws on device copies of the same inputs (bitwise in the
 decode band, whose kernels are deterministic; within the parity bound in the
-prefill band, whose FP32 token accumulator takes atomic adds), with pinned
-and with pageable host tensors, across batch sizes sharing one workspace, and
+prefill band, whose FP32 token accumulator takes atomic adds), with pinned,
+pageable and mixed host tensors, across batch sizes sharing one workspace, and
 that a short workspace is refused before anything runs.
 """
 import ctypes
@@ -25,9 +26,12 @@ def _host(t, pinned):
     return h.pin_memory() if pinned else h
 
 
-@pytest.mark.parametrize("name,ov,pinned", [("decode_e512", dict(E=32, M=1), True),
-                                            ("decode_e288_m4", dict(E=24), False),
-                                            ("tiny_decode", dict(M=8, fmt=gen.NVFP4), True)])
+# pinned: (x, ids, router weights, out) page-locked (read or written in place
+# by the kernels) or pageable (staged through the workspace)
+@pytest.mark.parametrize("name,ov,pinned", [("decode_e512", dict(E=32, M=1), (True,) * 4),
+                                            ("decode_e288_m4", dict(E=24), (False,) * 4),
+                                            ("decode_e288_m4", dict(E=24, M=3), (True, False, True, False)),
+                                            ("tiny_decode", dict(M=8, fmt=gen.NVFP4), (False, True, False, True))])
 def test_host_entry_matches_device_entry(name, ov, pinned):
     ensure_built()
     import fp4_weight_moe_gb300 as m
@@ -36,9 +40,9 @@ def test_host_entry_matches_device_entry(name, ov, pinned):
     ws = m.alloc_workspace(wl.M, wl.E, wl.H, wl.I, wl.top_k, wl.fmt)
     ref = m.forward(wl.x, pw, wl.topk_ids, wl.topk_weights, workspace=ws).clone()
     hws = m.alloc_host_workspace(wl.M, wl.E, wl.H, wl.I, wl.top_k, wl.fmt)
-    xh, idh, twh = (_host(t, pinned) for t in (wl.x, wl.topk_ids, wl.topk_weights))
+    xh, idh, twh = (_host(t, p) for t, p in zip((wl.x, wl.topk_ids, wl.topk_weights), pinned))
     for call in range(2):
-        outh = _host(torch.full_like(ref, float("nan")), pinned)
+        outh = _host(torch.full_like(ref, float("nan")), pinned[3])
         m.forward_host(xh, pw, idh, twh, outh, hws)
         torch.cuda.current_stream().synchronize()
         assert torch.equal(outh.view(torch.int16), ref.cpu().view(torch.int16)), call
