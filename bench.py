@@ -341,8 +341,10 @@ def run_ours(args):
         try:
             with open(prof) as f:
                 pd = json.load(f)
-            if pd.get("decode_src_sha256") == decode_src_sha256():
-                traffic = pd.get("dram_bytes_per_layer")
+            key = f"{args.workload}/M={M}/{gen.FMT_NAMES[fmt]}"
+            if (args.E is None and pd.get("decode_src_sha256") == decode_src_sha256()
+                    and key in pd.get("configs", {})):
+                traffic = pd["configs"][key]["dram_bytes_per_layer"]
         except Exception:
             traffic = None
 
