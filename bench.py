@@ -361,10 +361,13 @@ def run_ours(args):
         "routed_bytes_per_layer": step_bytes / K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"hbm_gbs of {peak_kind}", "traffic": traffic,
-                     "kernel": "decode layer: x pre-pass + FC1 + " + ("" if M < 2 else "h pre-pass + ") + "FC2 (PDL-chained)"},
+                     "kernel": ("decode layer: streaming-GEMV FC1 + FC2 (PDL-chained)"
+                              if m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) == 2 else
+                              "decode layer: x pre-pass + FC1 + " + ("" if M < 2 else "h pre-pass + ")
+                              + "FC2 (tcgen05, PDL-chained)")},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": M * H * 2 + M * k * 8,
                 "d2h_bytes_per_step": M * H * 2, "us_per_layer": e2e_ms * 1e3 / K},
-        "gpu_launches": (3 if M < 2 else 4) * K,
+        "gpu_launches": m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) * K,
         "clocks": clocks,
     }
 

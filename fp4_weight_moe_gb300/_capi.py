@@ -45,6 +45,9 @@ SIGNATURES = {
     "moe_fp4_forward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "moe_fp4_host_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
     "moe_fp4_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "moe_fp4_debug_set_decode_family": (_I, [_I, ctypes.POINTER(ctypes.c_int)]),
+    "moe_fp4_debug_decode_gemv_fits": (_I, [_I, _I, _I, _I, _I]),
+    "moe_fp4_debug_decode_launches": (_I, [_I, _I, _I, _I, _I]),
     "moe_fp4_debug_dequant": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "moe_fp4_debug_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_fp4_debug_route": (_I, [_P, _I, _I, _I, _P, _P, _P, _Z, _P]),
@@ -155,6 +158,20 @@ def moe_fp4_forward_host(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, f
     return _check("moe_fp4_forward_host",
                   _load().moe_fp4_forward_host(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt, ws,
                                                ws_bytes, stream))
+
+
+def moe_fp4_debug_set_decode_family(family: int) -> int:
+    prev = ctypes.c_int()
+    _check("moe_fp4_debug_set_decode_family", _load().moe_fp4_debug_set_decode_family(family, ctypes.byref(prev)))
+    return prev.value
+
+
+def moe_fp4_debug_decode_gemv_fits(M, E, H, I, top_k) -> bool:
+    return bool(_load().moe_fp4_debug_decode_gemv_fits(M, E, H, I, top_k))
+
+
+def moe_fp4_debug_decode_launches(M, E, H, I, top_k) -> int:
+    return int(_load().moe_fp4_debug_decode_launches(M, E, H, I, top_k))
 
 
 def moe_fp4_debug_dequant(w, s, which, expert, E, H, I, fmt, out, stream):

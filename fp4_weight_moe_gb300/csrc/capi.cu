@@ -1,6 +1,7 @@
 // extern "C" entry points of libmoe_fp4.so: argument validation, workspace
 // management and band dispatch.  The declarations and the contract of each
 // function are in include/moe_fp4.h.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -22,6 +23,9 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
 cudaError_t launch_debug_route(const int32_t* ids, int M, int E, int top_k, int32_t* perm, int32_t* expert_offset,
                                void* ws, cudaStream_t st);
 cudaError_t launch_debug_quant(const float* in, int rows, int K, uint8_t* q, uint8_t* s, float* G, cudaStream_t st);
+extern std::atomic<int> g_decode_family;
+bool decode_gemv_fits(int M, int E, int H, int I, int top_k);
+int decode_launches(int M, int E, int H, int I, int top_k);
 cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                           const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
                           int fmt, void* ws, int num_sms, cudaStream_t st);
@@ -366,6 +370,22 @@ int moe_fp4_forward_host(const void* x_bf16, const void* w13, const void* s13, c
   if (st != MOE_FP4_OK || out_direct) return st;
   e = cudaMemcpyAsync(out_bf16, od, xb, cudaMemcpyDefault, s);
   return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
+}
+
+int moe_fp4_debug_set_decode_family(int family, int* previous) {
+  if (family < 0 || family > 2) return MOE_FP4_EINVAL;
+  const int old = g_decode_family.exchange(family);
+  if (previous) *previous = old;
+  return MOE_FP4_OK;
+}
+
+int moe_fp4_debug_decode_gemv_fits(int M, int E, int H, int I, int top_k) {
+  return decode_gemv_fits(M, E, H, I, top_k) ? 1 : 0;
+}
+
+int moe_fp4_debug_decode_launches(int M, int E, int H, int I, int top_k) {
+  if (M < 1 || M > MOE_FP4_DECODE_MAX_M || check_shape(E, H, I, top_k, MOE_FP4_NVFP4) != MOE_FP4_OK) return 0;
+  return decode_launches(M, E, H, I, top_k);
 }
 
 int moe_fp4_debug_dequant(const void* w, const void* s, int which, int expert, int E, int H, int I, int fmt,

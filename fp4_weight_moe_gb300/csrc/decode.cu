@@ -1,25 +1,62 @@
 // Decode band (M <= 8 tokens): host-side entry of the layer for both weight
 // formats.  MXFP4 and NVFP4 weights share the resident layout (E4M3 scale
 // bytes per 16 elements and FP32 projection multipliers, see prepare.cu), so
-// both run the tcgen05 kernels of decode_tc.cu.
+// both run the same kernels.  Two kernel families serve the band:
+//   decode_gemv.cu  TMA-staged streaming GEMV on the CUDA cores, one pass
+//                   over each routed expert's weights for all of its tokens;
+//   decode_tc.cu    tcgen05 block-scaled MMA with the activations split into
+//                   four NVFP4 terms.
+// By default the shape decides (gemv_preferred below).
+#include <atomic>
+
 #include "common.cuh"
 
 namespace moe_fp4 {
+
+// Which family serves the band: 0 chooses by shape (gemv_preferred), 1 the
+// streaming GEMV where it fits, 2 the tcgen05 kernels.  Set
+// only by moe_fp4_debug_set_decode_family (test support).
+std::atomic<int> g_decode_family{0};
 
 size_t decode_tc_scratch_bytes(int M, int H, int I, int top_k, int num_sms);
 cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                              const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
                              float* scratch, uint32_t* status, int num_sms, cudaStream_t st, int* cu_err);
+bool decode_gemv_fits(int M, int E, int H, int I, int top_k);
+size_t decode_gemv_scratch_bytes(int M, int I, int top_k);
+cudaError_t launch_decode_gemv(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
+                               const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I,
+                               int top_k, float* scratch, uint32_t* status, cudaStream_t st, int* cu_err);
 
 static size_t decode_scratch_bytes(int M_max, int H, int I, int top_k, int num_sms) {
-  return (decode_tc_scratch_bytes(M_max, H, I, top_k, num_sms) + 255) & ~(size_t)255;
+  const size_t tc = decode_tc_scratch_bytes(M_max, H, I, top_k, num_sms);
+  const size_t gv = decode_gemv_scratch_bytes(M_max, I, top_k);
+  return ((tc > gv ? tc : gv) + 255) & ~(size_t)255;
 }
 
-// Scratch (h, activation-term images), then a 256-byte status
-// block (bit flags of bounded waits that gave up; sticky).
+// The streaming GEMV wins where the layer is mostly fixed latency: one token
+// and at most 4 MB of routed weights (measured on GB300: 5.2 vs 9.4 us at
+// 0.1 MB, 7.4 vs 9.2 us at 1.8 MB, even at 7 MB, and the tcgen05 kernels
+// ahead at every M >= 2).  Past that the CUDA cores' FP4 decode rate, not
+// HBM, bounds it, while the tensor cores take FP4 operands directly.
+static bool gemv_preferred(int M, int H, int I, int top_k) {
+  const double expert = 3.0 * I * H / 2 + 3.0 * I * H / 16 + 12;
+  return M == 1 && (double)M * top_k * expert <= 4.0 * (1 << 20);
+}
+
+// Scratch (the larger of the two families' intermediates), then a 256-byte
+// status block (bit flags of bounded waits that gave up; sticky).
 size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int fmt, int num_sms) {
   (void)fmt;
   return decode_scratch_bytes(M_max, H, I, top_k, num_sms) + 256;
+}
+
+// Kernel launches of one decode-band layer under the current family setting.
+int decode_launches(int M, int E, int H, int I, int top_k) {
+  const int family = g_decode_family.load(std::memory_order_relaxed);
+  const bool fits = decode_gemv_fits(M, E, H, I, top_k);
+  if (family == 1 ? fits : family == 0 && fits && gemv_preferred(M, H, I, top_k)) return 2;
+  return M >= 2 ? 4 : 3;  // x pre-pass, FC1, (h pre-pass,) FC2
 }
 
 cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
@@ -29,6 +66,11 @@ cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const
   int cu = 0;
   uint32_t* status =
       reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + decode_scratch_bytes(M, H, I, top_k, num_sms));
+  const int family = g_decode_family.load(std::memory_order_relaxed);
+  const bool fits = decode_gemv_fits(M, E, H, I, top_k);
+  if (family == 1 ? fits : family == 0 && fits && gemv_preferred(M, H, I, top_k))
+    return launch_decode_gemv(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, static_cast<float*>(ws),
+                              status, st, &cu);
   return launch_decode_tc(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, static_cast<float*>(ws), status,
                           num_sms, st, &cu);
 }

@@ -24,49 +24,78 @@ static EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// 2-D tensor map over a row-major byte matrix [rows][inner_bytes], box of
-// box_rows x 128 bytes, 128-byte swizzle (the K-major SW128 operand layout).
-// Encoded maps are kept in a small cache keyed by all four arguments (a map
-// depends on nothing else), so repeated layer calls skip the encoding.
-CUresult make_fp4_map(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint32_t box_rows) {
+// Tensor map over a byte array of up to three dimensions (d[0] innermost,
+// stride[i] the byte distance between consecutive indices of dimension i+1),
+// boxes of box[0..rank) bytes x rows, optional 128-byte swizzle.  Encoded
+// maps are kept in a small cache keyed by every argument (a map depends on
+// nothing else), so repeated layer calls skip the encoding.
+CUresult make_u8_map(CUtensorMap* m, const void* base, int rank, const uint64_t* d, const uint64_t* stride,
+                     const uint32_t* box, bool swizzle128) {
   struct Entry {
     const void* base;
-    uint64_t inner, rows;
-    uint32_t box;
+    int rank;
+    uint64_t d[3], stride[2];
+    uint32_t box[3];
+    bool sw;
     CUtensorMap map;
   };
   static Entry cache[64];
   static int n_used = 0, next = 0;
   static std::mutex mu;
+  if (rank < 1 || rank > 3) return CUDA_ERROR_INVALID_VALUE;
+  auto same = [&](const Entry& e) {
+    if (e.base != base || e.rank != rank || e.sw != swizzle128) return false;
+    for (int i = 0; i < rank; ++i)
+      if (e.d[i] != d[i] || e.box[i] != box[i] || (i + 1 < rank && e.stride[i] != stride[i])) return false;
+    return true;
+  };
   {
     std::lock_guard<std::mutex> lk(mu);
     for (int i = 0; i < n_used; ++i)
-      if (cache[i].base == base && cache[i].inner == inner_bytes && cache[i].rows == rows && cache[i].box == box_rows) {
+      if (same(cache[i])) {
         *m = cache[i].map;
         return CUDA_SUCCESS;
       }
   }
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return CUDA_ERROR_NOT_FOUND;
-  cuuint64_t dims[2] = {inner_bytes, rows};
-  cuuint64_t strides[1] = {inner_bytes};
-  cuuint32_t box[2] = {128, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  cuuint64_t dims[3], strides[2];
+  cuuint32_t bx[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    dims[i] = d[i];
+    bx[i] = box[i];
+    if (i + 1 < rank) strides[i] = stride[i];
+  }
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), dims, strides,
+                         bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r == CUDA_SUCCESS) {
     std::lock_guard<std::mutex> lk(mu);
     Entry& e = cache[next];
+    e = Entry{};
     e.base = base;
-    e.inner = inner_bytes;
-    e.rows = rows;
-    e.box = box_rows;
+    e.rank = rank;
+    e.sw = swizzle128;
+    for (int i = 0; i < rank; ++i) {
+      e.d[i] = d[i];
+      e.box[i] = box[i];
+      if (i + 1 < rank) e.stride[i] = stride[i];
+    }
     e.map = *m;
     next = (next + 1) % 64;
     if (n_used < 64) ++n_used;
   }
   return r;
+}
+
+// 2-D tensor map over a row-major byte matrix [rows][inner_bytes], box of
+// box_rows x 128 bytes, 128-byte swizzle (the K-major SW128 operand layout).
+CUresult make_fp4_map(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint32_t box_rows) {
+  const uint64_t d[2] = {inner_bytes, rows};
+  const uint64_t stride[1] = {inner_bytes};
+  const uint32_t box[2] = {128, box_rows};
+  return make_u8_map(m, base, 2, d, stride, box, true);
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1)

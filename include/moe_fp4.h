@@ -245,6 +245,27 @@ MOE_FP4_API int moe_fp4_forward_noalloc(const void *x_bf16, const void *w13, con
                                         void *out_bf16, int M, int E, int H, int I, int top_k, int fmt, void *stream);
 
 /*
+ * Test support: choose the kernel family of the decode band (M <=
+ * MOE_FP4_DECODE_MAX_M) for every later call in the process.
+ *   family 0  by shape (default): the streaming GEMV kernels for one token
+ *             with at most 4 MB of routed weights, else the tcgen05 kernels
+ *   family 1  the streaming GEMV kernels where the shape fits them
+ *   family 2  the tcgen05 kernels
+ * Both families compute the same layer; the GEMV family sums in a different
+ * order, so results agree within the parity bound, not bitwise.  *previous
+ * (if non-null) receives the old setting.  MOE_FP4_EINVAL for other values.
+ * moe_fp4_debug_decode_gemv_fits returns 1 if the GEMV kernels take the
+ * shape (their shared memory holds all tokens' activations and every routed
+ * pair's h), else 0.
+ */
+MOE_FP4_API int moe_fp4_debug_set_decode_family(int family, int *previous);
+MOE_FP4_API int moe_fp4_debug_decode_gemv_fits(int M, int E, int H, int I, int top_k);
+/* Kernel launches one decode-band layer of this shape makes under the
+ * current family setting (2 streaming GEMV; 3, or 4 from M = 2, tcgen05);
+ * 0 for shapes outside the band or invalid arguments. */
+MOE_FP4_API int moe_fp4_debug_decode_launches(int M, int E, int H, int I, int top_k);
+
+/*
  * Test support: dequantise one expert's projection from the resident layout
  * into out_f32 [rows][K] in LOGICAL row order, each element computed as the
  * kernels use it: RN_fp32((e2m1 * e4m3) * g) (one rounding; exact for MXFP4,
