@@ -98,16 +98,35 @@ CUresult make_fp4_map(CUtensorMap* m, const void* base, uint64_t inner_bytes, ui
   return make_u8_map(m, base, 2, d, stride, box, true);
 }
 
+// SM count of the current device (cached): the persistent GEMMs launch one
+// CTA per SM.
+static cudaError_t gemm_sms(int* sms) {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+    *sms = cache[dev];
+    return cudaSuccess;
+  }
+  e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) cache[dev] = *sms;
+  return e;
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1)
     debug_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                      const uint8_t* a_sf, const uint8_t* b_sf, float* d, int K, int N, uint32_t* err) {
+                      const uint8_t* a_sf, const uint8_t* b_sf, float* d, int K, int N, int n_tiles, uint32_t* err) {
   const int KG = K / 64;
-  auto tile_of = [&]() {
+  const int NT = N / kGemmBN;
+  auto tile_of = [&](int idx) {
     GemmTile t;
-    t.a_row0 = blockIdx.x * kGemmBM;
-    t.b_row0 = blockIdx.y * kGemmBN;
-    t.a_sf = a_sf + (size_t)blockIdx.x * KG * kChunkBytes;
-    t.b_sf0 = b_sf + (size_t)(2 * blockIdx.y) * KG * kChunkBytes;
+    t.m_tile = idx / NT;
+    t.n_tile = idx % NT;
+    t.a_row0 = t.m_tile * kGemmBM;
+    t.b_row0 = t.n_tile * kGemmBN;
+    t.a_sf = a_sf + (size_t)t.m_tile * KG * kChunkBytes;
+    t.b_sf0 = b_sf + (size_t)(2 * t.n_tile) * KG * kChunkBytes;
     t.b_sf1 = t.b_sf0 + (size_t)KG * kChunkBytes;
     t.valid = true;
     return t;
@@ -124,7 +143,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                              __uint_as_float(r[4 * i + 3]));
     }
   };
-  gemm_fp4_tile(&map_a, &map_b, K, err, tile_of, epi);
+  gemm_fp4_persistent(&map_a, &map_b, K, err, n_tiles, tile_of, epi);
 }
 
 cudaError_t launch_debug_gemm(const void* a_q, const void* a_sf, const void* b_q, const void* b_sf, float* d,
@@ -138,9 +157,12 @@ cudaError_t launch_debug_gemm(const void* a_q, const void* a_sf, const void* b_q
   }
   cudaError_t e = cudaFuncSetAttribute(debug_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid(M_rows / kGemmBM, N_rows / kGemmBN);
-  debug_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, st>>>(ma, mb, static_cast<const uint8_t*>(a_sf),
-                                                           static_cast<const uint8_t*>(b_sf), d, K, N_rows, status);
+  const int n_tiles = (M_rows / kGemmBM) * (N_rows / kGemmBN);
+  int sms = 0;
+  e = gemm_sms(&sms);
+  if (e != cudaSuccess) return e;
+  debug_gemm_kernel<<<n_tiles < sms ? n_tiles : sms, kGemmThreads, kGemmSmem, st>>>(
+      ma, mb, static_cast<const uint8_t*>(a_sf), static_cast<const uint8_t*>(b_sf), d, K, N_rows, n_tiles, status);
   return cudaGetLastError();
 }
 
@@ -416,19 +438,23 @@ __global__ void quant_h_kernel(PrefillArgs a) {
 }
 
 // ---------------------------------------------------------------- GEMMs
-// Tile (m, n) with n fastest: CTAs sharing an activation tile run together,
-// and the M-tiles of one expert (sharing weight tiles) follow each other.
+// Tile (m, n) with n fastest, dealt round-robin to one persistent CTA per
+// SM: CTAs sharing an activation tile run together, and the M-tiles of one
+// expert (sharing weight tiles) follow each other.
 __global__ void __launch_bounds__(kGemmThreads, 1)
     fc1_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                     PrefillArgs a) {
   const int NT = 2 * a.I / kGemmBN;
-  const int mt = blockIdx.x / NT, nt = blockIdx.x % NT;
   const int KG = a.H / 64;
   const size_t scb = scale_chunk_bytes(2 * a.I, a.H);
   const float* g13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * scb);
-  auto tile_of = [&]() {
+  const int n_mt = *a.num_tiles;
+  auto tile_of = [&](int idx) {
     GemmTile t;
-    t.valid = mt < *a.num_tiles;
+    const int mt = idx / NT, nt = idx % NT;
+    t.m_tile = mt;
+    t.n_tile = nt;
+    t.valid = mt < n_mt;
     if (!t.valid) return t;
     const int e = a.tile_expert[mt];
     t.a_row0 = kGemmBM * mt;
@@ -440,7 +466,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   };
   auto epi = [&](uint32_t tmem_row, int row, const GemmTile& t) {
     const int r = t.a_row0 + row;
-    const int e = a.tile_expert[mt];
+    const int e = a.tile_expert[t.m_tile];
     const bool live = a.row_src[r] >= 0;
     const float xg = live ? a.xG[r] : 0.f;
     const float sgate = xg * g13[2 * e], sup = xg * g13[2 * e + 1];
@@ -453,7 +479,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tmem_ld32(tmem_row + 128 * q + 32 * c, g);
         tmem_ld32(tmem_row + 128 * q + 64 + 32 * c, u);
         if (live) {
-          const int n0 = 64 * (2 * nt + q) + 32 * c;
+          const int n0 = 64 * (2 * t.n_tile + q) + 32 * c;
           uint32_t packed[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -470,20 +496,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   };
-  gemm_fp4_tile(&map_x, &map_w, a.H, a.status, tile_of, epi);
+  gemm_fp4_persistent(&map_x, &map_w, a.H, a.status, n_mt * NT, tile_of, epi);
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
     fc2_gemm_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
                     PrefillArgs a) {
   const int NT = a.H / kGemmBN;
-  const int mt = blockIdx.x / NT, nt = blockIdx.x % NT;
   const int KG = a.I / 64;
   const size_t scb = scale_chunk_bytes(a.H, a.I);
   const float* g2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * scb);
-  auto tile_of = [&]() {
+  const int n_mt = *a.num_tiles;
+  auto tile_of = [&](int idx) {
     GemmTile t;
-    t.valid = mt < *a.num_tiles;
+    const int mt = idx / NT, nt = idx % NT;
+    t.m_tile = mt;
+    t.n_tile = nt;
+    t.valid = mt < n_mt;
     if (!t.valid) return t;
     const int e = a.tile_expert[mt];
     t.a_row0 = kGemmBM * mt;
@@ -495,10 +524,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   };
   auto epi = [&](uint32_t tmem_row, int row, const GemmTile& t) {
     const int r = t.a_row0 + row;
-    const int e = a.tile_expert[mt];
+    const int e = a.tile_expert[t.m_tile];
     const int src = a.row_src[r];
     const float f = src >= 0 ? a.hG[r] * g2[e] * a.tw[src] : 0.f;
-    float* dst = a.acc + (size_t)(src >= 0 ? src / a.top_k : 0) * a.H + kGemmBN * nt;
+    float* dst = a.acc + (size_t)(src >= 0 ? src / a.top_k : 0) * a.H + kGemmBN * t.n_tile;
 #pragma unroll 1
     for (int c = 0; c < kGemmBN / 32; ++c) {
       uint32_t v[32];
@@ -515,7 +544,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   };
-  gemm_fp4_tile(&map_h, &map_w, a.I, a.status, tile_of, epi);
+  gemm_fp4_persistent(&map_h, &map_w, a.I, a.status, n_mt * NT, tile_of, epi);
 }
 
 __global__ void cast_out_kernel(PrefillArgs a) {
@@ -681,9 +710,14 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
   cudaError_t e = launch_route(a, st);
   if (e != cudaSuccess) return e;
   quant_x_kernel<<<(M + 7) / 8, 256, 0, st>>>(a);
-  fc1_gemm_kernel<<<c.max_tiles * (2 * I / kGemmBN), kGemmThreads, kGemmSmem, st>>>(mx, mw13, a);
+  int sms = 0;
+  cudaError_t es = gemm_sms(&sms);
+  if (es != cudaSuccess) return es;
+  // persistent: one CTA per SM (the valid tile count is known on the device)
+  const int g1 = c.max_tiles * (2 * I / kGemmBN), g2 = c.max_tiles * (H / kGemmBN);
+  fc1_gemm_kernel<<<g1 < sms ? g1 : sms, kGemmThreads, kGemmSmem, st>>>(mx, mw13, a);
   quant_h_kernel<<<(int)((rows + 7) / 8), 256, 0, st>>>(a);
-  fc2_gemm_kernel<<<c.max_tiles * (H / kGemmBN), kGemmThreads, kGemmSmem, st>>>(mh, mw2, a);
+  fc2_gemm_kernel<<<g2 < sms ? g2 : sms, kGemmThreads, kGemmSmem, st>>>(mh, mw2, a);
   cast_out_kernel<<<4 * 152, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
