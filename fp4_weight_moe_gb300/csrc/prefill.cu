@@ -310,11 +310,21 @@ __global__ void route_count_kernel(PrefillArgs a) {
 __global__ void route_scan_kernel(PrefillArgs a) {
   __shared__ int s_tot[kMaxPrefillE];
   __shared__ int s_part[2][1024];
-  const int E = a.E;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+  __shared__ int s_poff[kMaxPrefillE];
+  const int E = a.E, nb = a.n_route_blocks;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  // lanes per expert column (a power of two <= 32 that divides the warp):
+  // the column's count blocks are split in contiguous segments
+  int tpe = 1;
+  while (tpe < 32 && tpe * 2 * E <= (int)blockDim.x) tpe *= 2;
+  const int seg = (nb + tpe - 1) / tpe;
+  for (int base = 0; base < E * tpe; base += blockDim.x) {
+    const int v = base + threadIdx.x, e = v / tpe, part = v % tpe;
     int t = 0;
-    for (int b = 0; b < a.n_route_blocks; ++b) t += a.counts[(size_t)b * E + e];
-    s_tot[e] = t;
+    if (e < E)
+      for (int b = part * seg; b < min(nb, part * seg + seg); ++b) t += a.counts[(size_t)b * E + e];
+    for (int d = 1; d < tpe; d <<= 1) t += __shfl_xor_sync(0xffffffffu, t, d);
+    if (e < E && part == 0) s_tot[e] = t;
   }
   __syncthreads();
   // exclusive scans over experts: each thread owns a contiguous run
@@ -325,37 +335,75 @@ __global__ void route_scan_kernel(PrefillArgs a) {
     su += s_tot[e];
     sp += (s_tot[e] + 127) & ~127;
   }
-  s_part[0][threadIdx.x] = su;
-  s_part[1][threadIdx.x] = sp;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int ru = 0, rp = 0;
-    for (int t = 0; t < (int)blockDim.x; ++t) {
-      const int u = s_part[0][t], pp = s_part[1][t];
-      s_part[0][t] = ru;
-      s_part[1][t] = rp;
-      ru += u;
-      rp += pp;
+  // exclusive block scan of (su, sp): within warps by shuffles, then over
+  // the warp totals
+  int iu = su, ip = sp;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int ou = __shfl_up_sync(0xffffffffu, iu, d), op = __shfl_up_sync(0xffffffffu, ip, d);
+    if (lane >= d) {
+      iu += ou;
+      ip += op;
     }
-    a.expert_off[E] = ru;
-    a.expert_poff[E] = rp;
-    *a.num_tiles = rp / 128;
+  }
+  if (lane == 31) {
+    s_part[0][warp] = iu;
+    s_part[1][warp] = ip;
   }
   __syncthreads();
-  int ru = s_part[0][threadIdx.x], rp = s_part[1][threadIdx.x];
+  if (warp == 0) {
+    int wu = lane < nw ? s_part[0][lane] : 0, wp = lane < nw ? s_part[1][lane] : 0;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int ou = __shfl_up_sync(0xffffffffu, wu, d), op = __shfl_up_sync(0xffffffffu, wp, d);
+      if (lane >= d) {
+        wu += ou;
+        wp += op;
+      }
+    }
+    if (lane < nw) {
+      s_part[0][32 + lane] = wu;  // inclusive warp prefixes
+      s_part[1][32 + lane] = wp;
+    }
+    if (lane == nw - 1) {
+      a.expert_off[E] = wu;
+      a.expert_poff[E] = wp;
+      *a.num_tiles = wp / 128;
+    }
+  }
+  __syncthreads();
+  int ru = iu - su + (warp > 0 ? s_part[0][32 + warp - 1] : 0);
+  int rp = ip - sp + (warp > 0 ? s_part[1][32 + warp - 1] : 0);
   for (int e = e0; e < e1; ++e) {
     const int tot = s_tot[e], padded = (tot + 127) & ~127;
     a.expert_off[e] = ru;
     a.expert_poff[e] = rp;
-    int run = rp;
-    for (int b = 0; b < a.n_route_blocks; ++b) {
-      a.block_base[(size_t)b * E + e] = run;
-      run += a.counts[(size_t)b * E + e];
-    }
+    s_poff[e] = rp;
     for (int t = 0; t < padded / 128; ++t) a.tile_expert[rp / 128 + t] = e;
     for (int r = rp + tot; r < rp + padded; ++r) a.row_src[r] = -1;
     ru += tot;
     rp += padded;
+  }
+  __syncthreads();
+  // per-block bases of the stable scatter: the expert's padded offset plus
+  // the counts of the earlier blocks (segment sums, then a scan in order)
+  for (int base = 0; base < E * tpe; base += blockDim.x) {
+    const int v = base + threadIdx.x, e = v / tpe, part = v % tpe;
+    const int b0 = part * seg, b1 = e < E ? min(nb, b0 + seg) : b0;
+    int t = 0;
+    for (int b = b0; b < b1; ++b) t += a.counts[(size_t)b * E + e];
+    int incl = t;  // inclusive scan over the parts of this expert
+    for (int d = 1; d < tpe; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (part >= d) incl += o;
+    }
+    if (e < E) {
+      int run = s_poff[e] + incl - t;
+      for (int b = b0; b < b1; ++b) {
+        a.block_base[(size_t)b * E + e] = run;
+        run += a.counts[(size_t)b * E + e];
+      }
+    }
   }
 }
 
