@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                              __uint_as_float(r[4 * i + 3]));
     }
   };
-  gemm_fp4_persistent(&map_a, &map_b, K, err, n_tiles, tile_of, epi);
+  gemm_fp4_persistent<kGemmBN>(&map_a, &map_b, K, err, n_tiles, tile_of, epi);
 }
 
 cudaError_t launch_debug_gemm(const void* a_q, const void* a_sf, const void* b_q, const void* b_sf, float* d,
@@ -486,6 +486,10 @@ __global__ void quant_h_kernel(PrefillArgs a) {
 }
 
 // ---------------------------------------------------------------- GEMMs
+// FC2's tile width.  128 (two accumulators, the reduction epilogue beside
+// the next tile's MMAs) measured slower on GB300 than 256 (FC2 327 vs 300 us
+// on prefill_e128): the narrower tiles stage a third more bytes per FLOP.
+constexpr int kFc2BN = 256;
 // Tile (m, n) with n fastest, dealt round-robin to one persistent CTA per
 // SM: CTAs sharing an activation tile run together, and the M-tiles of one
 // expert (sharing weight tiles) follow each other.
@@ -544,13 +548,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   };
-  gemm_fp4_persistent(&map_x, &map_w, a.H, a.status, n_mt * NT, tile_of, epi);
+  gemm_fp4_persistent<kGemmBN>(&map_x, &map_w, a.H, a.status, n_mt * NT, tile_of, epi);
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
     fc2_gemm_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
                     PrefillArgs a) {
-  const int NT = a.H / kGemmBN;
+  const int NT = a.H / kFc2BN;
   const int KG = a.I / 64;
   const size_t scb = scale_chunk_bytes(a.H, a.I);
   const float* g2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * scb);
@@ -564,9 +568,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (!t.valid) return t;
     const int e = a.tile_expert[mt];
     t.a_row0 = kGemmBM * mt;
-    t.b_row0 = e * a.H + kGemmBN * nt;
+    t.b_row0 = e * a.H + kFc2BN * nt;
     t.a_sf = a.hsf + (size_t)mt * KG * kChunkBytes;
-    t.b_sf0 = a.s2 + (size_t)e * scb + (size_t)(2 * nt) * KG * kChunkBytes;
+    t.b_sf0 = a.s2 + (size_t)e * scb + (size_t)(kFc2BN / 128) * nt * KG * kChunkBytes;
     t.b_sf1 = t.b_sf0 + (size_t)KG * kChunkBytes;
     return t;
   };
@@ -575,9 +579,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int e = a.tile_expert[t.m_tile];
     const int src = a.row_src[r];
     const float f = src >= 0 ? a.hG[r] * g2[e] * a.tw[src] : 0.f;
-    float* dst = a.acc + (size_t)(src >= 0 ? src / a.top_k : 0) * a.H + kGemmBN * t.n_tile;
+    float* dst = a.acc + (size_t)(src >= 0 ? src / a.top_k : 0) * a.H + kFc2BN * t.n_tile;
 #pragma unroll 1
-    for (int c = 0; c < kGemmBN / 32; ++c) {
+    for (int c = 0; c < kFc2BN / 32; ++c) {
       uint32_t v[32];
       tmem_ld32(tmem_row + 32 * c, v);
       if (src >= 0) {
@@ -592,7 +596,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   };
-  gemm_fp4_persistent(&map_h, &map_w, a.I, a.status, n_mt * NT, tile_of, epi);
+  gemm_fp4_persistent<kFc2BN>(&map_h, &map_w, a.I, a.status, n_mt * NT, tile_of, epi);
 }
 
 __global__ void cast_out_kernel(PrefillArgs a) {
@@ -742,7 +746,7 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
   CUresult r = make_fp4_map(&mx, a.xq, (uint64_t)H / 2, rows, kGemmBM);
   if (r == CUDA_SUCCESS) r = make_fp4_map(&mw13, w13, (uint64_t)H / 2, (uint64_t)E * 2 * I, kGemmBN);
   if (r == CUDA_SUCCESS) r = make_fp4_map(&mh, a.hq, (uint64_t)I / 2, rows, kGemmBM);
-  if (r == CUDA_SUCCESS) r = make_fp4_map(&mw2, w2, (uint64_t)I / 2, (uint64_t)E * H, kGemmBN);
+  if (r == CUDA_SUCCESS) r = make_fp4_map(&mw2, w2, (uint64_t)I / 2, (uint64_t)E * H, kFc2BN);
   if (r != CUDA_SUCCESS) {
     *cu_err = (int)r;
     return cudaErrorInvalidValue;
@@ -751,7 +755,8 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
   if (!attrs) {
     cudaError_t e = cudaFuncSetAttribute(fc1_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(fc2_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+      e = cudaFuncSetAttribute(fc2_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               GemmCfg<kFc2BN>::kSmem);
     if (e != cudaSuccess) return e;
     attrs = true;
   }
@@ -762,10 +767,10 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
   cudaError_t es = gemm_sms(&sms);
   if (es != cudaSuccess) return es;
   // persistent: one CTA per SM (the valid tile count is known on the device)
-  const int g1 = c.max_tiles * (2 * I / kGemmBN), g2 = c.max_tiles * (H / kGemmBN);
+  const int g1 = c.max_tiles * (2 * I / kGemmBN), g2 = c.max_tiles * (H / kFc2BN);
   fc1_gemm_kernel<<<g1 < sms ? g1 : sms, kGemmThreads, kGemmSmem, st>>>(mx, mw13, a);
   quant_h_kernel<<<(int)((rows + 7) / 8), 256, 0, st>>>(a);
-  fc2_gemm_kernel<<<g2 < sms ? g2 : sms, kGemmThreads, kGemmSmem, st>>>(mh, mw2, a);
+  fc2_gemm_kernel<<<g2 < sms ? g2 : sms, kGemmThreads, GemmCfg<kFc2BN>::kSmem, st>>>(mh, mw2, a);
   cast_out_kernel<<<4 * 152, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
