@@ -74,7 +74,7 @@ int check_shape(int E, int H, int I, int top_k, int fmt) {
 // Extra limits of the prefill band (M > MOE_FP4_DECODE_MAX_M).
 int check_prefill(int M, int E, int I, int top_k, int fmt) {
   (void)fmt;  // both formats share the resident layout and the kernels
-  if (I % 256 != 0 || E > 4096) return MOE_FP4_EUNSUPPORTED;
+  if (E > 4096) return MOE_FP4_EUNSUPPORTED;
   if ((long long)M * top_k >= (1LL << 30)) return MOE_FP4_EUNSUPPORTED;
   return MOE_FP4_OK;
 }

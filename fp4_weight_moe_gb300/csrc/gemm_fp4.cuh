@@ -80,8 +80,11 @@ struct GemmTile {
 // GemmTile`; epilogue: functor `epi(tmem_row, row_in_tile, tile)`, called
 // once per epilogue thread and tile, after the tile's accumulator is
 // complete; tmem_row addresses this thread's accumulator row (add a column
-// offset below BN and read it with tmem_ld32).  Launch with kGemmThreads
-// threads and GemmCfg<BN>::kSmem bytes of dynamic shared memory.
+// offset below BN and read it with tmem_ld32).  K is a multiple of 64; a
+// last stage shorter than 256 loads (zero-filled by the tensor maps) and
+// multiplies only its valid 64-K groups, and copies only their scale
+// chunks.  Launch with kGemmThreads threads and GemmCfg<BN>::kSmem bytes of
+// dynamic shared memory.
 template <int BN, class TileOf, class Epi>
 __device__ __forceinline__ void gemm_fp4_persistent(const CUtensorMap* map_a, const CUtensorMap* map_b, int K,
                                                     uint32_t* err, int n_tiles, const TileOf& tile_of,
@@ -99,7 +102,9 @@ __device__ __forceinline__ void gemm_fp4_persistent(const CUtensorMap* map_a, co
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if ((int)blockIdx.x >= n_tiles || !tile_of((int)blockIdx.x).valid) return;
-  const int nk = K / kGemmBK;
+  const int nk = (K + kGemmBK - 1) / kGemmBK;
+  // 64-K groups of stage s (4, fewer in a ragged last stage)
+  auto groups = [&](int s) { return s + 1 < nk ? 4 : K / 64 - 4 * (nk - 1); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -143,14 +148,14 @@ __device__ __forceinline__ void gemm_fp4_persistent(const CUtensorMap* map_a, co
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[slot], Cfg::kStageBytes);
+          const uint32_t sfb = (uint32_t)groups(s) * kChunkBytes;  // scale bytes of one 128-row tile
+          mbar_arrive_expect_tx(&full[slot], Cfg::kStageA + Cfg::kStageB + (1 + BN / 128) * sfb);
           tma_load_2d(stage_a(slot), map_a, s * (kGemmBK / 2), t.a_row0, &full[slot]);
           tma_load_2d(stage_b(slot), map_b, s * (kGemmBK / 2), t.b_row0, &full[slot]);
-          bulk_load(stage_sfa(slot), t.a_sf + (size_t)(4 * s) * kChunkBytes, Cfg::kStageSFA, &full[slot]);
-          bulk_load(stage_sfb(slot), t.b_sf0 + (size_t)(4 * s) * kChunkBytes, 4 * kChunkBytes, &full[slot]);
+          bulk_load(stage_sfa(slot), t.a_sf + (size_t)(4 * s) * kChunkBytes, sfb, &full[slot]);
+          bulk_load(stage_sfb(slot), t.b_sf0 + (size_t)(4 * s) * kChunkBytes, sfb, &full[slot]);
           if (BN == 256)
-            bulk_load(stage_sfb(slot) + 4 * kChunkBytes, t.b_sf1 + (size_t)(4 * s) * kChunkBytes, 4 * kChunkBytes,
-                      &full[slot]);
+            bulk_load(stage_sfb(slot) + 4 * kChunkBytes, t.b_sf1 + (size_t)(4 * s) * kChunkBytes, sfb, &full[slot]);
         }
       }
     }
@@ -179,8 +184,8 @@ __device__ __forceinline__ void gemm_fp4_persistent(const CUtensorMap* map_a, co
         const uint32_t sf_b = sf_a + 16;
         const uint64_t da = smem_desc(smem_u32(stage_a(slot)), 16, 1024, kLayoutSW128);
         const uint64_t db = smem_desc(smem_u32(stage_b(slot)), 16, 1024, kLayoutSW128);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)  // K step of 64 = 32 bytes = 2 descriptor units
+        const int ng = groups(s);
+        for (int k = 0; k < ng; ++k)  // K step of 64 = 32 bytes = 2 descriptor units
           mma_nvf4_warp(acc, da + 2 * k, db + 2 * k, idesc, sf_a + 4 * k, sf_b + 4 * (BN / 128) * k,
                         s > 0 || k > 0);
         mma_commit_warp(&empty[slot]);

@@ -493,10 +493,13 @@ constexpr int kFc2BN = 256;
 // Tile (m, n) with n fastest, dealt round-robin to one persistent CTA per
 // SM: CTAs sharing an activation tile run together, and the M-tiles of one
 // expert (sharing weight tiles) follow each other.
+// FC1 N tiles span BN / 128 resident w13 tiles (64 gate/up pairs each):
+// 256 wide when 2I is a multiple of 256, else 128.
+template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     fc1_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                     PrefillArgs a) {
-  const int NT = 2 * a.I / kGemmBN;
+  const int NT = 2 * a.I / BN;
   const int KG = a.H / 64;
   const size_t scb = scale_chunk_bytes(2 * a.I, a.H);
   const float* g13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * scb);
@@ -510,9 +513,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (!t.valid) return t;
     const int e = a.tile_expert[mt];
     t.a_row0 = kGemmBM * mt;
-    t.b_row0 = e * 2 * a.I + kGemmBN * nt;
+    t.b_row0 = e * 2 * a.I + BN * nt;
     t.a_sf = a.xsf + (size_t)mt * KG * kChunkBytes;
-    t.b_sf0 = a.s13 + (size_t)e * scb + (size_t)(2 * nt) * KG * kChunkBytes;
+    t.b_sf0 = a.s13 + (size_t)e * scb + (size_t)(BN / 128) * nt * KG * kChunkBytes;
     t.b_sf1 = t.b_sf0 + (size_t)KG * kChunkBytes;
     return t;
   };
@@ -524,14 +527,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const float sgate = xg * g13[2 * e], sup = xg * g13[2 * e + 1];
     __nv_bfloat16* hrow = a.hbuf + (size_t)r * a.I;
 #pragma unroll 1
-    for (int q = 0; q < 2; ++q) {    // the two 128-row resident tiles of this N tile
+    for (int q = 0; q < BN / 128; ++q) {  // the 128-row resident tiles of this N tile
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {  // 32-pair chunks of the tile's 64 pairs
         uint32_t g[32], u[32];
         tmem_ld32(tmem_row + 128 * q + 32 * c, g);
         tmem_ld32(tmem_row + 128 * q + 64 + 32 * c, u);
         if (live) {
-          const int n0 = 64 * (2 * t.n_tile + q) + 32 * c;
+          const int n0 = 64 * ((BN / 128) * t.n_tile + q) + 32 * c;
           uint32_t packed[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -548,7 +551,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   };
-  gemm_fp4_persistent<kGemmBN>(&map_x, &map_w, a.H, a.status, n_mt * NT, tile_of, epi);
+  gemm_fp4_persistent<BN>(&map_x, &map_w, a.H, a.status, n_mt * NT, tile_of, epi);
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -744,7 +747,8 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
   const size_t rows = (size_t)128 * c.max_tiles;
   CUtensorMap mx, mw13, mh, mw2;
   CUresult r = make_fp4_map(&mx, a.xq, (uint64_t)H / 2, rows, kGemmBM);
-  if (r == CUDA_SUCCESS) r = make_fp4_map(&mw13, w13, (uint64_t)H / 2, (uint64_t)E * 2 * I, kGemmBN);
+  const int bn1 = (2 * I) % 256 == 0 ? 256 : 128;  // FC1 tile width
+  if (r == CUDA_SUCCESS) r = make_fp4_map(&mw13, w13, (uint64_t)H / 2, (uint64_t)E * 2 * I, (uint32_t)bn1);
   if (r == CUDA_SUCCESS) r = make_fp4_map(&mh, a.hq, (uint64_t)I / 2, rows, kGemmBM);
   if (r == CUDA_SUCCESS) r = make_fp4_map(&mw2, w2, (uint64_t)I / 2, (uint64_t)E * H, kFc2BN);
   if (r != CUDA_SUCCESS) {
@@ -753,7 +757,11 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
   }
   static bool attrs = false;
   if (!attrs) {
-    cudaError_t e = cudaFuncSetAttribute(fc1_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(fc1_gemm_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg<256>::kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fc1_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               GemmCfg<128>::kSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(fc2_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                GemmCfg<kFc2BN>::kSmem);
@@ -767,8 +775,11 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
   cudaError_t es = gemm_sms(&sms);
   if (es != cudaSuccess) return es;
   // persistent: one CTA per SM (the valid tile count is known on the device)
-  const int g1 = c.max_tiles * (2 * I / kGemmBN), g2 = c.max_tiles * (H / kFc2BN);
-  fc1_gemm_kernel<<<g1 < sms ? g1 : sms, kGemmThreads, kGemmSmem, st>>>(mx, mw13, a);
+  const int g1 = c.max_tiles * (2 * I / bn1), g2 = c.max_tiles * (H / kFc2BN);
+  if (bn1 == 256)
+    fc1_gemm_kernel<256><<<g1 < sms ? g1 : sms, kGemmThreads, GemmCfg<256>::kSmem, st>>>(mx, mw13, a);
+  else
+    fc1_gemm_kernel<128><<<g1 < sms ? g1 : sms, kGemmThreads, GemmCfg<128>::kSmem, st>>>(mx, mw13, a);
   quant_h_kernel<<<(int)((rows + 7) / 8), 256, 0, st>>>(a);
   fc2_gemm_kernel<<<g2 < sms ? g2 : sms, kGemmThreads, GemmCfg<kFc2BN>::kSmem, st>>>(mh, mw2, a);
   cast_out_kernel<<<4 * 152, 256, 0, st>>>(a);

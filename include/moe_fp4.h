@@ -155,7 +155,7 @@ MOE_FP4_API int moe_fp4_release_workspace(void);
  * token accumulator with atomic adds, so its low-order bits may vary run to
  * run.
  *
- * Prefill band (M > 8): I % 256 == 0, E <= 4096 (else
+ * Prefill band (M > 8): E <= 4096 (else
  * MOE_FP4_EUNSUPPORTED).  Activations are quantised to NVFP4 per row (x per
  * token, h = SiLU(gate)*up per routed row after BF16 staging) so both GEMMs
  * run on the FP4 tensor cores.

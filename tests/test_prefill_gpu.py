@@ -100,10 +100,17 @@ def _prefill_case(M, E, H, I, k, seed, invalid=0.0, fmt=gen.NVFP4):
     return w, x, ids.cuda(), tw.cuda()
 
 
+# The last cases have I % 256 != 0: FC1 runs 128-wide tiles (2I % 256 != 0)
+# and FC2's last K stage holds 1 or 2 of 4 groups (I = 320, 128), the
+# shapes of the decode workloads above 8 tokens (the mid band).
 @pytest.mark.parametrize("M,E,H,I,k,invalid,fmt", [(16, 4, 256, 256, 2, 0.0, gen.NVFP4),
                                                    (200, 8, 512, 256, 4, 0.05, gen.NVFP4),
                                                    (600, 6, 768, 512, 3, 0.0, gen.NVFP4),
-                                                   (300, 8, 512, 512, 4, 0.05, gen.MXFP4)])
+                                                   (300, 8, 512, 512, 4, 0.05, gen.MXFP4),
+                                                   (16, 12, 512, 320, 4, 0.0, gen.NVFP4),
+                                                   (40, 8, 256, 128, 2, 0.05, gen.MXFP4),
+                                                   (64, 24, 2560, 320, 10, 0.0, gen.NVFP4),
+                                                   (9, 6, 512, 192, 3, 0.0, gen.NVFP4)])
 def test_prefill_parity(M, E, H, I, k, invalid, fmt):
     m = fm()
     w, x, ids, tw = _prefill_case(M, E, H, I, k, seed=M + E, invalid=invalid, fmt=fmt)
