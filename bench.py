@@ -134,6 +134,22 @@ def dist_env():
     return ws, rank, local
 
 
+def job_time_and_units(ms, units, ws, device):
+    """Whole-job timing of the replicas: the slowest rank's time (every rank
+    times its own K layers with CUDA events) and the units all ranks
+    processed (each rank draws its own routing, so their bytes differ)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms, units], dtype=torch.float64, device=device)
+    if ws > 1:
+        tmax = t[:1].clone()
+        tsum = t[1:].clone()
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+        dist.all_reduce(tsum, op=dist.ReduceOp.SUM)
+        return float(tmax.item()), float(tsum.item())
+    return float(t[0].item()), float(t[1].item())
+
+
 def layer_flops(ids, E, H, I):
     """2 * (gate + up + down) multiply-adds per valid routed row."""
     n = int(((ids >= 0) & (ids < E)).sum())
@@ -288,14 +304,9 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     ms = ev0.elapsed_time(ev1)
-    t = torch.tensor([ms], device=dev)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max, job_units = job_time_and_units(ms, step_flops if prefill else step_bytes, ws, dev)
     ms_per_step = ms_max / K
-    value = step_bytes * ws / (ms_max * 1e-3) / 1e9
-    if prefill:
-        value = step_flops * ws / (ms_max * 1e-3) / 1e12
+    value = job_units / (ms_max * 1e-3) / (1e12 if prefill else 1e9)
 
     e2e_value = None
     # end to end through the C ABI's host-buffer entry point, one eager call
@@ -325,13 +336,8 @@ def run_ours(args):
             e2e_step(i)
         e1.record(cur)
         torch.cuda.synchronize()
-        t = torch.tensor([e0.elapsed_time(e1)], device=dev)
-        if ws > 1:
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-        e2e_value = step_bytes * ws / (e2e_ms * 1e-3) / 1e9
-        if prefill:
-            e2e_value = step_flops * ws / (e2e_ms * 1e-3) / 1e12
+        e2e_ms, job_units = job_time_and_units(e0.elapsed_time(e1), step_flops if prefill else step_bytes, ws, dev)
+        e2e_value = job_units / (e2e_ms * 1e-3) / (1e12 if prefill else 1e9)
 
     peak, peak_kind = load_peaks()
     achieved = (step_bytes / K) / (ms_per_step * 1e-3) / 1e9
