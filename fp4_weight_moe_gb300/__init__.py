@@ -146,6 +146,28 @@ def forward(x: torch.Tensor, pw: PreparedWeights, topk_ids: torch.Tensor, topk_w
     return out
 
 
+ACT_SILU, ACT_GELU_TANH, ACT_SWIGLUOAI = (_capi.MOE_FP4_ACT_SILU, _capi.MOE_FP4_ACT_GELU_TANH,
+                                        _capi.MOE_FP4_ACT_SWIGLUOAI)
+
+
+def forward_act(x: torch.Tensor, pw: PreparedWeights, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                workspace: torch.Tensor, kind: int = ACT_SILU, alpha: float = 0.0, beta: float = 1.0,
+                limit: float = 0.0, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The layer with a chosen gated activation (ACT_SILU, ACT_GELU_TANH, or
+    ACT_SWIGLUOAI with alpha, beta, limit), on a caller-owned workspace."""
+    if x.dtype != torch.bfloat16 or topk_ids.dtype != torch.int32 or topk_weights.dtype != torch.float32:
+        raise TypeError("x must be bfloat16, topk_ids int32, topk_weights float32")
+    _require_cuda(x, topk_ids, topk_weights, out, workspace)
+    M, H = x.shape
+    if out is None:
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    act = _capi.MoeFp4Activation(kind, alpha, beta, limit)
+    _capi.moe_fp4_forward_ex(_ptr(x), *pw.ptrs(), _ptr(topk_ids), _ptr(topk_weights), _ptr(out), M, pw.E, pw.H, pw.I,
+                             topk_ids.shape[1], pw.fmt, act, _ptr(workspace), workspace.nbytes,
+                             _stream(stream, x.device))
+    return out
+
+
 def host_workspace_bytes(M_max: int, E: int, H: int, I: int, top_k: int, fmt: int) -> int:
     return _capi.moe_fp4_host_workspace_bytes(M_max, E, H, I, top_k, fmt)
 

@@ -24,6 +24,16 @@ MOE_FP4_MXFP4 = 0
 MOE_FP4_NVFP4 = 1
 MOE_FP4_DECODE_MAX_M = 8
 MOE_FP4_NOALLOC_SCRATCH_BYTES = 16 << 20
+MOE_FP4_ACT_SILU = 0
+MOE_FP4_ACT_GELU_TANH = 1
+MOE_FP4_ACT_SWIGLUOAI = 2
+
+
+class MoeFp4Activation(ctypes.Structure):
+    """struct moe_fp4_activation."""
+    _fields_ = [("kind", ctypes.c_int), ("alpha", ctypes.c_float), ("beta", ctypes.c_float),
+                ("limit", ctypes.c_float)]
+
 
 # (name, restype, argtypes) for every symbol declared in include/moe_fp4.h
 _P = ctypes.c_void_p
@@ -42,6 +52,8 @@ SIGNATURES = {
     "moe_fp4_release_workspace": (_I, []),
     "moe_fp4_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "moe_fp4_forward_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "moe_fp4_forward_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                ctypes.POINTER(MoeFp4Activation), _P, _Z, _P]),
     "moe_fp4_forward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "moe_fp4_host_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
     "moe_fp4_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
@@ -143,6 +155,13 @@ def moe_fp4_forward_ws(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt
     return _check("moe_fp4_forward_ws",
                   _load().moe_fp4_forward_ws(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt, ws, ws_bytes,
                                              stream))
+
+
+def moe_fp4_forward_ex(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt, act, ws, ws_bytes, stream):
+    """``act``: None (SiLU) or a MoeFp4Activation."""
+    return _check("moe_fp4_forward_ex",
+                  _load().moe_fp4_forward_ex(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt,
+                                             None if act is None else ctypes.byref(act), ws, ws_bytes, stream))
 
 
 def moe_fp4_forward_noalloc(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt, stream):

@@ -2,6 +2,7 @@
 // management and band dispatch.  The declarations and the contract of each
 // function are in include/moe_fp4.h.
 #include <atomic>
+#include <cmath>
 #include <mutex>
 
 #include "common.cuh"
@@ -19,7 +20,7 @@ size_t prefill_workspace_bytes(int M, int E, int H, int I, int top_k);
 size_t debug_route_workspace_bytes(int M, int E, int top_k);
 cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                            const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
-                           void* ws, cudaStream_t st, int* cu_err);
+                           const ActParams& act, void* ws, cudaStream_t st, int* cu_err);
 cudaError_t launch_debug_route(const int32_t* ids, int M, int E, int top_k, int32_t* perm, int32_t* expert_offset,
                                void* ws, cudaStream_t st);
 cudaError_t launch_debug_quant(const float* in, int rows, int K, uint8_t* q, uint8_t* s, float* G, cudaStream_t st);
@@ -28,7 +29,7 @@ bool decode_gemv_fits(int M, int E, int H, int I, int top_k);
 int decode_launches(int M, int E, int H, int I, int top_k);
 cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                           const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
-                          int fmt, void* ws, int num_sms, cudaStream_t st);
+                          int fmt, const ActParams& act, void* ws, int num_sms, cudaStream_t st);
 }  // namespace moe_fp4
 
 using namespace moe_fp4;
@@ -256,9 +257,19 @@ int moe_fp4_release_workspace(void) {
   return MOE_FP4_OK;
 }
 
-int moe_fp4_forward_ws(const void* x_bf16, const void* w13, const void* s13, const void* w2, const void* s2,
+int moe_fp4_forward_ex(const void* x_bf16, const void* w13, const void* s13, const void* w2, const void* s2,
                        const int32_t* topk_ids, const float* topk_weights, void* out_bf16, int M, int E, int H,
-                       int I, int top_k, int fmt, void* workspace, size_t workspace_bytes, void* stream) {
+                       int I, int top_k, int fmt, const moe_fp4_activation* act, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  ActParams ap = {MOE_FP4_ACT_SILU, 0.f, 0.f, 0.f};
+  if (act) {
+    if (act->kind != MOE_FP4_ACT_SILU && act->kind != MOE_FP4_ACT_GELU_TANH && act->kind != MOE_FP4_ACT_SWIGLUOAI)
+      return MOE_FP4_EINVAL;
+    if (act->kind == MOE_FP4_ACT_SWIGLUOAI &&
+        (!std::isfinite(act->alpha) || !std::isfinite(act->beta) || !(act->limit > 0.f)))
+      return MOE_FP4_EINVAL;
+    ap = {act->kind, act->alpha, act->beta, act->limit};
+  }
   int st = check_shape(E, H, I, top_k, fmt);
   if (st != MOE_FP4_OK) return st;
   if (M < 0) return MOE_FP4_EINVAL;
@@ -278,15 +289,22 @@ int moe_fp4_forward_ws(const void* x_bf16, const void* w13, const void* s13, con
     const size_t need = decode_workspace_bytes(M, H, I, top_k, fmt, sms);
     if (need >= kMaxWorkspace || workspace_bytes < need) return MOE_FP4_EWORKSPACE;
     cudaError_t e = launch_decode(x_bf16, w13, s13, w2, s2, topk_ids, topk_weights, out_bf16, M, E, H, I, top_k,
-                                  fmt, workspace, sms, static_cast<cudaStream_t>(stream));
+                                  fmt, ap, workspace, sms, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
   }
   const size_t need = prefill_workspace_bytes(M, E, H, I, top_k);
   if (need >= kMaxWorkspace || workspace_bytes < need) return MOE_FP4_EWORKSPACE;
   int cu = 0;
-  cudaError_t e = launch_prefill(x_bf16, w13, s13, w2, s2, topk_ids, topk_weights, out_bf16, M, E, H, I, top_k,
+  cudaError_t e = launch_prefill(x_bf16, w13, s13, w2, s2, topk_ids, topk_weights, out_bf16, M, E, H, I, top_k, ap,
                                  workspace, static_cast<cudaStream_t>(stream), &cu);
   return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
+}
+
+int moe_fp4_forward_ws(const void* x_bf16, const void* w13, const void* s13, const void* w2, const void* s2,
+                       const int32_t* topk_ids, const float* topk_weights, void* out_bf16, int M, int E, int H,
+                       int I, int top_k, int fmt, void* workspace, size_t workspace_bytes, void* stream) {
+  return moe_fp4_forward_ex(x_bf16, w13, s13, w2, s2, topk_ids, topk_weights, out_bf16, M, E, H, I, top_k, fmt,
+                            nullptr, workspace, workspace_bytes, stream);
 }
 
 int moe_fp4_forward(const void* x_bf16, const void* w13, const void* s13, const void* w2, const void* s2,

@@ -131,4 +131,25 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 __device__ __forceinline__ float silu(float v) { return v / (1.0f + __expf(-v)); }
 
+// The gated activation of FC1's (gate, up) pair (MOE_FP4_ACT_*): SiLU(gate) *
+// up; GELU in its tanh form; SwiGLU-OAI with gate' = min(gate, limit), up' =
+// clamp(up, -limit, limit), (up' + beta) * gate' * sigmoid(alpha * gate').
+struct ActParams {
+  int kind;
+  float alpha, beta, limit;
+};
+
+__device__ __forceinline__ float gated_act(float gate, float up, const ActParams& p) {
+  if (p.kind == MOE_FP4_ACT_GELU_TANH) {
+    const float c = 0.7978845608028654f;  // sqrt(2 / pi)
+    return 0.5f * gate * (1.0f + tanhf(c * fmaf(0.044715f * gate, gate * gate, gate))) * up;
+  }
+  if (p.kind == MOE_FP4_ACT_SWIGLUOAI) {
+    const float g = fminf(gate, p.limit);
+    const float u = fminf(fmaxf(up, -p.limit), p.limit);
+    return (u + p.beta) * g / (1.0f + __expf(-p.alpha * g));
+  }
+  return silu(gate) * up;
+}
+
 }  // namespace moe_fp4

@@ -76,6 +76,7 @@ struct GvArgs {
   __nv_bfloat16* out;      // [M][H]
   uint32_t* status;
   int M, E, H, I, top_k, n_slots, ring;
+  ActParams act;           // FC1's gated activation
 };
 
 struct GvCtl {
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(kGvThreads, 4)
     const float gate = red[rg * 8 + i] + red[(kGvRows + rg) * 8 + i];
     const float up = red[ru * 8 + i] + red[(kGvRows + ru) * 8 + i];
     const int ni = 64 * t + qs * kGvQ + q + 32 * p;
-    const float hv = silu(gate * C.g3[0]) * (up * C.g3[1]) * (C.wtok[i] * C.g3[2]);
+    const float hv = gated_act(gate * C.g3[0], up * C.g3[1], a.act) * (C.wtok[i] * C.g3[2]);
     a.h[(((size_t)slot * M + C.tok[i]) * (I / 64) + ni / 64) * kGvGroup + ni % 64] = hv;
   }
 }
@@ -584,7 +585,8 @@ size_t decode_gemv_scratch_bytes(int M, int I, int top_k) {
 
 cudaError_t launch_decode_gemv(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                                const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I,
-                               int top_k, float* scratch, uint32_t* status, cudaStream_t st, int* cu_err) {
+                               int top_k, const ActParams& act, float* scratch, uint32_t* status, cudaStream_t st,
+                               int* cu_err) {
   CUtensorMap w13m, s13m, w2m, s2m;
   {
     const uint64_t d[3] = {(uint64_t)H / 2, 32, (uint64_t)E * 2 * I / 32};
@@ -633,6 +635,7 @@ cudaError_t launch_decode_gemv(const void* x, const void* w13, const void* s13, 
   a.top_k = top_k;
   a.n_slots = M * top_k;
   a.ring = 1;
+  a.act = act;
   switch (gv_mt(M)) {
     case 1: return gv_launch<1>(w13m, s13m, w2m, s2m, a, st);
     case 2: return gv_launch<2>(w13m, s13m, w2m, s2m, a, st);

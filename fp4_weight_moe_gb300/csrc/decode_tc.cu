@@ -127,6 +127,7 @@ struct TcArgs {
   int M, E, H, I, top_k, n_slots;
   int split;   // FC1: K ranges per w13 tile; FC2: CTAs (cluster size) per w2 tile
   int N;      // B rows per item (accumulator columns)
+  ActParams act;  // FC1's gated activation
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -756,7 +757,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
         up += S.part[(src * M + token) * rpo + cpo + jj];
       }
       const float hv =
-          (S.routed >> token) & 1u ? silu(gate * S.g3[0]) * (up * S.g3[1]) * (S.wtok[token] * S.g3[2]) : 0.f;
+          (S.routed >> token) & 1u ? gated_act(gate * S.g3[0], up * S.g3[1], a.act) * (S.wtok[token] * S.g3[2]) : 0.f;
       a.h[((size_t)slot1 * M + token) * I + tile * 64 + pair] = hv;
     }
   } else {
@@ -821,7 +822,8 @@ size_t decode_tc_scratch_bytes(int M, int H, int I, int top_k, int num_sms) {
 
 cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                              const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
-                             float* scratch, uint32_t* status, int num_sms, cudaStream_t st, int* cu_err) {
+                             const ActParams& act, float* scratch, uint32_t* status, int num_sms, cudaStream_t st,
+                             int* cu_err) {
   CUtensorMap m13, m2;
   CUresult r = make_fp4_map(&m13, w13, (uint64_t)H / 2, (uint64_t)E * 2 * I, 128);
   if (r == CUDA_SUCCESS) r = make_fp4_map(&m2, w2, (uint64_t)I / 2, (uint64_t)E * H, 128);
@@ -859,6 +861,7 @@ cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, co
   a.top_k = top_k;
   a.n_slots = M * top_k;
   a.N = (kTerms * M + 15) / 16 * 16;
+  a.act = act;
   const int sms = num_sms > 0 ? num_sms : 152;
 
   // activation pre-pass: one CTA per K stage, one warp per token

@@ -24,7 +24,7 @@ namespace moe_fp4 {
 size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int fmt, int num_sms);
 cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                           const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
-                          int fmt, void* ws, int num_sms, cudaStream_t st);
+                          int fmt, const ActParams& act, void* ws, int num_sms, cudaStream_t st);
 }  // namespace moe_fp4
 
 namespace {
@@ -88,7 +88,8 @@ extern "C" int moe_fp4_forward_noalloc(const void* x_bf16, const void* w13, cons
     return MOE_FP4_EWORKSPACE;
   // Nothing in the scratch needs to start at zero: FC1 writes every
   // intermediate element that FC2 reads in the same call.
+  const ActParams silu_act = {MOE_FP4_ACT_SILU, 0.f, 0.f, 0.f};
   cudaError_t e = launch_decode(x_bf16, w13, s13, w2, s2, topk_ids, topk_weights, out_bf16, M, E, H, I, top_k, fmt,
-                                scratch, sms, static_cast<cudaStream_t>(stream));
+                                silu_act, scratch, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_FP4_OK : MOE_FP4_ECUDA;
 }

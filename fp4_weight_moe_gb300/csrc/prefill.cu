@@ -200,6 +200,7 @@ struct PrefillArgs {
   const uint8_t* s2;
   __nv_bfloat16* out;
   int M, E, H, I, top_k, n_entries, n_route_blocks, max_tiles;
+  ActParams act;  // FC1's gated activation
   int* counts;      // [n_route_blocks][E]
   int* block_base;  // [n_route_blocks][E]
   int* expert_off;  // [E+1]
@@ -538,8 +539,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint32_t packed[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float h0 = silu(__uint_as_float(g[2 * j]) * sgate) * (__uint_as_float(u[2 * j]) * sup);
-            const float h1 = silu(__uint_as_float(g[2 * j + 1]) * sgate) * (__uint_as_float(u[2 * j + 1]) * sup);
+            const float h0 = gated_act(__uint_as_float(g[2 * j]) * sgate, __uint_as_float(u[2 * j]) * sup, a.act);
+            const float h1 =
+                gated_act(__uint_as_float(g[2 * j + 1]) * sgate, __uint_as_float(u[2 * j + 1]) * sup, a.act);
             const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
             packed[j] = *reinterpret_cast<const uint32_t*>(&hv);
           }
@@ -735,9 +737,10 @@ size_t prefill_workspace_bytes(int M, int E, int H, int I, int top_k) {
 
 cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                            const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
-                           void* ws, cudaStream_t st, int* cu_err) {
+                           const ActParams& act, void* ws, cudaStream_t st, int* cu_err) {
   const PrefillCarve c = prefill_carve(M, E, H, I, top_k);
   PrefillArgs a = prefill_args(c, ws, M, E, H, I, top_k);
+  a.act = act;
   a.x = static_cast<const __nv_bfloat16*>(x);
   a.ids = ids;
   a.tw = tw;

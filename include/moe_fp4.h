@@ -217,6 +217,36 @@ MOE_FP4_API int moe_fp4_forward_host(const void *x_bf16, const void *w13, const 
                                      size_t workspace_bytes, void *stream);
 
 /*
+ * Gated activations of FC1's (gate, up) pair.  MOE_FP4_ACT_SILU,
+ * SiLU(gate) * up, is the layer's own (and the default of every other
+ * entry point).  The SM12x sync PR's kernels also take "gelu_tanh" and
+ * "swigluoai_uninterleave":
+ *   MOE_FP4_ACT_GELU_TANH  0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))) u
+ *   MOE_FP4_ACT_SWIGLUOAI  g' = min(g, limit), u' = min(max(u, -limit), limit),
+ *                          (u' + beta) g' sigmoid(alpha g')
+ * with g and u the dequantised FC1 outputs (per-tensor multipliers applied).
+ * alpha, beta and limit are read for MOE_FP4_ACT_SWIGLUOAI only.
+ */
+#define MOE_FP4_ACT_SILU 0
+#define MOE_FP4_ACT_GELU_TANH 1
+#define MOE_FP4_ACT_SWIGLUOAI 2
+typedef struct moe_fp4_activation {
+  int kind;
+  float alpha, beta, limit;
+} moe_fp4_activation;
+
+/*
+ * moe_fp4_forward_ws with a chosen activation (act == NULL: SiLU).  Same
+ * arguments, workspace, results and errors otherwise; MOE_FP4_EINVAL for an
+ * unknown kind, or for SwiGLU-OAI with a non-finite alpha or beta or a
+ * limit that is not a positive number.
+ */
+MOE_FP4_API int moe_fp4_forward_ex(const void *x_bf16, const void *w13, const void *s13, const void *w2,
+                                   const void *s2, const int32_t *topk_ids, const float *topk_weights, void *out_bf16,
+                                   int M, int E, int H, int I, int top_k, int fmt, const moe_fp4_activation *act,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * The decode-band layer (M <= MOE_FP4_DECODE_MAX_M) without any device
  * allocation, for callers that cannot call cudaMalloc where they run the
  * layer: inside a stream capture, under a runtime that owns all device memory

@@ -91,6 +91,12 @@ def _bind(lib):
     lib.moe_oracle_forward.argtypes = [P, P, P, P, P, P, P, P, P, i, i, i, i, i, i, P, i, P, i]
     lib.moe_oracle_forward_prefill.restype = i
     lib.moe_oracle_forward_prefill.argtypes = [P, P, P, P, P, P, P, P, P, i, i, i, i, i, i, P, i, P, P, P, P, i]
+    d = ctypes.c_double
+    lib.moe_oracle_forward_act.restype = i
+    lib.moe_oracle_forward_act.argtypes = [P, P, P, P, P, P, P, P, P, i, i, i, i, i, i, P, i, P, i, i, d, d, d]
+    lib.moe_oracle_forward_prefill_act.restype = i
+    lib.moe_oracle_forward_prefill_act.argtypes = [P, P, P, P, P, P, P, P, P, i, i, i, i, i, i, P, i, P, P, P, P, i,
+                                                   i, d, d, d]
     lib.moe_oracle_fc1.restype = i
     lib.moe_oracle_fc1.argtypes = [P, P, P, P, i, i, i, i, P, P]
     lib.moe_oracle_quant_nvfp4_row.restype = None
@@ -161,8 +167,21 @@ def _weights_np(weights: dict, fmt: int):
     return w13, s13, g13, w2, s2, g2
 
 
+# Gated activations: SiLU (the layer's own), GELU (tanh form), SwiGLU-OAI
+# (parameters alpha, beta, limit).  ``act`` arguments take None (SiLU) or a
+# tuple (kind, alpha, beta, limit).
+ACT_SILU, ACT_GELU_TANH, ACT_SWIGLUOAI = 0, 1, 2
+
+
+def _act_args(act):
+    if act is None:
+        return None
+    kind, alpha, beta, limit = act
+    return int(kind), float(alpha), float(beta), float(limit)
+
+
 def forward(x_bf16, weights: dict, topk_ids, topk_weights, E: int, H: int, I: int, top_k: int, fmt: int,
-            tokens: Optional[Sequence[int]] = None, nthreads: int = 0) -> np.ndarray:
+            tokens: Optional[Sequence[int]] = None, nthreads: int = 0, act=None) -> np.ndarray:
     """Decode-band definition of the layer in FP64: returns ``[n_tok][H]`` (all tokens if ``tokens`` is None)."""
     x = _np(x_bf16, np.uint16)
     M = x.shape[0]
@@ -172,15 +191,17 @@ def forward(x_bf16, weights: dict, topk_ids, topk_weights, E: int, H: int, I: in
     tok = None if tokens is None else np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
     n_tok = M if tok is None else len(tok)
     out = np.full((n_tok, H), np.nan, dtype=np.float64)  # poisoned: the oracle must overwrite
-    rc = _load().moe_oracle_forward(_ptr(x), _ptr(w13), _ptr(s13), _ptr(g13), _ptr(w2), _ptr(s2), _ptr(g2), _ptr(ids),
-                                    _ptr(tw), M, E, H, I, top_k, fmt, _ptr(tok), n_tok, _ptr(out), nthreads)
+    args = (_ptr(x), _ptr(w13), _ptr(s13), _ptr(g13), _ptr(w2), _ptr(s2), _ptr(g2), _ptr(ids), _ptr(tw), M, E, H, I,
+            top_k, fmt, _ptr(tok), n_tok, _ptr(out), nthreads)
+    a = _act_args(act)
+    rc = _load().moe_oracle_forward(*args) if a is None else _load().moe_oracle_forward_act(*args, *a)
     if rc != 0:
         raise ValueError("oracle rejected the shapes")
     return out
 
 
 def forward_prefill(x_bf16, weights: dict, topk_ids, topk_weights, E: int, H: int, I: int, top_k: int,
-                    tokens: Optional[Sequence[int]] = None, nthreads: int = 0, fmt: int = NVFP4):
+                    tokens: Optional[Sequence[int]] = None, nthreads: int = 0, fmt: int = NVFP4, act=None):
     """Prefill-band definition (NVFP4 activations, mirrored; weights in either
     format): returns (out ``[n_tok][H]`` FP64, x_q ``[n_tok][H/2]``,
     x_s ``[n_tok][H/16]``, x_G ``[n_tok]``)."""
@@ -195,9 +216,11 @@ def forward_prefill(x_bf16, weights: dict, topk_ids, topk_weights, E: int, H: in
     xq = np.zeros((n_tok, H // 2), dtype=np.uint8)
     xs = np.zeros((n_tok, H // 16), dtype=np.uint8)
     xg = np.zeros((n_tok,), dtype=np.float32)
-    rc = _load().moe_oracle_forward_prefill(_ptr(x), _ptr(w13), _ptr(s13), _ptr(g13), _ptr(w2), _ptr(s2), _ptr(g2),
-                                            _ptr(ids), _ptr(tw), M, E, H, I, top_k, fmt, _ptr(tok), n_tok,
-                                            _ptr(out), _ptr(xq), _ptr(xs), _ptr(xg), nthreads)
+    args = (_ptr(x), _ptr(w13), _ptr(s13), _ptr(g13), _ptr(w2), _ptr(s2), _ptr(g2), _ptr(ids), _ptr(tw), M, E, H, I,
+            top_k, fmt, _ptr(tok), n_tok, _ptr(out), _ptr(xq), _ptr(xs), _ptr(xg), nthreads)
+    a = _act_args(act)
+    rc = (_load().moe_oracle_forward_prefill(*args) if a is None
+          else _load().moe_oracle_forward_prefill_act(*args, *a))
     if rc != 0:
         raise ValueError("oracle rejected the shapes")
     return out, xq, xs, xg

@@ -111,9 +111,36 @@ void moe_oracle_dequant(const uint8_t *nib, const uint8_t *sc, int rows, int K, 
 
 static double silu(double v) { return v / (1.0 + exp(-v)); }
 
-/* h[n] = SiLU(x . W13[e][n]) * (x . W13[e][I+n]) for n < I. */
+/* The gated activation applied to FC1's (gate, up) pair.  SiLU is the
+ * layer's own (tiny-decode PR, What); the SM12x sync PR's kernels also take
+ * "gelu_tanh" and "swigluoai_uninterleave" with parameters alpha, beta
+ * (default 1.0) and limit:
+ *   GELU, tanh form:  h = 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))) u
+ *   SwiGLU-OAI:       g' = min(g, limit), u' = min(max(u, -limit), limit),
+ *                     h = (u' + beta) g' sigmoid(alpha g')                 */
+#define ORACLE_ACT_SILU 0
+#define ORACLE_ACT_GELU_TANH 1
+#define ORACLE_ACT_SWIGLUOAI 2
+typedef struct {
+    int kind;
+    double alpha, beta, limit;
+} oracle_act;
+
+static double gated_other(double gate, double up, const oracle_act *a)
+{
+    if (a->kind == ORACLE_ACT_GELU_TANH) {
+        double c = sqrt(2.0 / acos(-1.0));
+        return 0.5 * gate * (1.0 + tanh(c * (gate + 0.044715 * gate * gate * gate))) * up;
+    }
+    double g = gate < a->limit ? gate : a->limit;
+    double u = up < -a->limit ? -a->limit : (up > a->limit ? a->limit : up);
+    return (u + a->beta) * g / (1.0 + exp(-a->alpha * g));
+}
+
+/* h[n] = act(x . W13[e][n], x . W13[e][I+n]) for n < I (SiLU(gate) * up by
+ * default). */
 static void expert_fc1(const double *x, const uint8_t *w13, const uint8_t *s13, const float *g13, int e, int H,
-                       int I, int fmt, double *h)
+                       int I, int fmt, const oracle_act *act, double *h)
 {
     int B = block_of(fmt);
     const uint8_t *nib = w13 + (size_t)e * 2 * I * (H / 2);
@@ -126,7 +153,10 @@ static void expert_fc1(const double *x, const uint8_t *w13, const uint8_t *s13, 
             gate += x[k] * weight_at(nib, sc, H, fmt, gg, n, k);
             up += x[k] * weight_at(nib, sc, H, fmt, gu, I + n, k);
         }
-        h[n] = silu(gate) * up;
+        if (act->kind == ORACLE_ACT_SILU)
+            h[n] = silu(gate) * up;
+        else
+            h[n] = gated_other(gate, up, act);
     }
 }
 
@@ -148,14 +178,14 @@ static void expert_fc2(const double *h, const uint8_t *w2, const uint8_t *s2, co
 /* One token: out[m] = sum over valid slots j of w[j] * FC2(SiLU(FC1 gate) * FC1 up). */
 static void token_forward(const double *x, const uint8_t *w13, const uint8_t *s13, const float *g13,
                           const uint8_t *w2, const uint8_t *s2, const float *g2, const int32_t *ids,
-                          const float *tw, int E, int H, int I, int top_k, int fmt, double *out, double *h,
-                          double *y)
+                          const float *tw, int E, int H, int I, int top_k, int fmt, const oracle_act *act,
+                          double *out, double *h, double *y)
 {
     for (int m = 0; m < H; ++m) out[m] = 0.0;
     for (int j = 0; j < top_k; ++j) {
         int e = ids[j];
         if (e < 0 || e >= E) continue; /* invalid route: exact-zero contribution */
-        expert_fc1(x, w13, s13, g13, e, H, I, fmt, h);
+        expert_fc1(x, w13, s13, g13, e, H, I, fmt, act, h);
         expert_fc2(h, w2, s2, g2, e, H, I, fmt, y);
         double w = (double)tw[j];
         for (int m = 0; m < H; ++m) out[m] += w * y[m];
@@ -163,12 +193,16 @@ static void token_forward(const double *x, const uint8_t *w13, const uint8_t *s1
 }
 
 /* Full layer for the tokens listed in `tokens` (n_tok entries; NULL = all M
- * tokens in order).  out is [n_tok][H] FP64.  Returns 0 on success. */
-int moe_oracle_forward(const uint16_t *x_bf16, const uint8_t *w13, const uint8_t *s13, const float *g13,
-                       const uint8_t *w2, const uint8_t *s2, const float *g2, const int32_t *topk_ids,
-                       const float *topk_w, int M, int E, int H, int I, int top_k, int fmt, const int32_t *tokens,
-                       int n_tok, double *out, int nthreads)
+ * tokens in order), activation `act_kind` with parameters alpha, beta, limit
+ * (SwiGLU-OAI only).  out is [n_tok][H] FP64.  Returns 0 on success. */
+int moe_oracle_forward_act(const uint16_t *x_bf16, const uint8_t *w13, const uint8_t *s13, const float *g13,
+                           const uint8_t *w2, const uint8_t *s2, const float *g2, const int32_t *topk_ids,
+                           const float *topk_w, int M, int E, int H, int I, int top_k, int fmt, const int32_t *tokens,
+                           int n_tok, double *out, int nthreads, int act_kind, double alpha, double beta,
+                           double limit)
 {
+    oracle_act act = {act_kind, alpha, beta, limit};
+    if (act_kind < ORACLE_ACT_SILU || act_kind > ORACLE_ACT_SWIGLUOAI) return 1;
     if (M < 0 || E <= 0 || H <= 0 || I <= 0 || top_k <= 0) return 1;
     if (fmt != ORACLE_MXFP4 && fmt != ORACLE_NVFP4) return 1;
     if (H % block_of(fmt) || I % block_of(fmt)) return 1;
@@ -188,7 +222,7 @@ int moe_oracle_forward(const uint16_t *x_bf16, const uint8_t *w13, const uint8_t
             int t = tokens ? tokens[i] : i;
             for (int k = 0; k < H; ++k) x[k] = bf16_to_double(x_bf16[(size_t)t * H + k]);
             token_forward(x, w13, s13, g13, w2, s2, g2, topk_ids + (size_t)t * top_k, topk_w + (size_t)t * top_k,
-                          E, H, I, top_k, fmt, out + (size_t)i * H, h, y);
+                          E, H, I, top_k, fmt, &act, out + (size_t)i * H, h, y);
         }
         free(x);
         free(h);
@@ -196,6 +230,16 @@ int moe_oracle_forward(const uint16_t *x_bf16, const uint8_t *w13, const uint8_t
     }
     (void)nthreads;
     return 0;
+}
+
+/* The layer with its own activation (SiLU). */
+int moe_oracle_forward(const uint16_t *x_bf16, const uint8_t *w13, const uint8_t *s13, const float *g13,
+                       const uint8_t *w2, const uint8_t *s2, const float *g2, const int32_t *topk_ids,
+                       const float *topk_w, int M, int E, int H, int I, int top_k, int fmt, const int32_t *tokens,
+                       int n_tok, double *out, int nthreads)
+{
+    return moe_oracle_forward_act(x_bf16, w13, s13, g13, w2, s2, g2, topk_ids, topk_w, M, E, H, I, top_k, fmt, tokens,
+                                  n_tok, out, nthreads, ORACLE_ACT_SILU, 0.0, 0.0, 0.0);
 }
 
 /* FC1 stage alone for one (token, expert): gate[n], up[n] for n < I. */
@@ -335,16 +379,20 @@ static void dequant_nvfp4_row(const uint8_t *q, const uint8_t *s, float G, int K
 
 /* Prefill band (mirrored quantisation), for the tokens listed (NULL = all):
  *   x_q = quant(x_t); for each valid slot: g,u = FC1(dequant(x_q)) in FP64;
- *   h = SiLU(g)*u rounded to FP32, then to BF16; h_q = quant(h);
+ *   h = act(g, u) (SiLU(g)*u by default) rounded to FP32, then to BF16;
+ *   h_q = quant(h);
  *   y = FC2(dequant(h_q));
  *   out_t = sum_j w_j y.
  * Also returns (optionally) the quantised x rows of the listed tokens. */
-int moe_oracle_forward_prefill(const uint16_t *x_bf16, const uint8_t *w13, const uint8_t *s13, const float *g13,
-                               const uint8_t *w2, const uint8_t *s2, const float *g2, const int32_t *topk_ids,
-                               const float *topk_w, int M, int E, int H, int I, int top_k, int fmt,
-                               const int32_t *tokens, int n_tok, double *out, uint8_t *xq_out, uint8_t *xs_out,
-                               float *xg_out, int nthreads)
+int moe_oracle_forward_prefill_act(const uint16_t *x_bf16, const uint8_t *w13, const uint8_t *s13,
+                                   const float *g13, const uint8_t *w2, const uint8_t *s2, const float *g2,
+                                   const int32_t *topk_ids, const float *topk_w, int M, int E, int H, int I,
+                                   int top_k, int fmt, const int32_t *tokens, int n_tok, double *out,
+                                   uint8_t *xq_out, uint8_t *xs_out, float *xg_out, int nthreads, int act_kind,
+                                   double alpha, double beta, double limit)
 {
+    oracle_act act = {act_kind, alpha, beta, limit};
+    if (act_kind < ORACLE_ACT_SILU || act_kind > ORACLE_ACT_SWIGLUOAI) return 1;
     if (fmt != ORACLE_NVFP4 && fmt != ORACLE_MXFP4) return 1;
     if (H % block_of(fmt) || I % block_of(fmt) || H % 16 || I % 16) return 1;
     if (!tokens) n_tok = M;
@@ -380,7 +428,7 @@ int moe_oracle_forward_prefill(const uint16_t *x_bf16, const uint8_t *w13, const
             for (int j = 0; j < top_k; ++j) {
                 int e = topk_ids[(size_t)t * top_k + j];
                 if (e < 0 || e >= E) continue;
-                expert_fc1(xd, w13, s13, g13, e, H, I, fmt, h);
+                expert_fc1(xd, w13, s13, g13, e, H, I, fmt, &act, h);
                 for (int n = 0; n < I; ++n) hf[n] = bf16_round((float)h[n]);
                 float hG;
                 moe_oracle_quant_nvfp4_row(hf, I, hq, hs, &hG);
@@ -394,6 +442,18 @@ int moe_oracle_forward_prefill(const uint16_t *x_bf16, const uint8_t *w13, const
     }
     (void)nthreads;
     return 0;
+}
+
+/* The prefill band with the layer's own activation (SiLU). */
+int moe_oracle_forward_prefill(const uint16_t *x_bf16, const uint8_t *w13, const uint8_t *s13, const float *g13,
+                               const uint8_t *w2, const uint8_t *s2, const float *g2, const int32_t *topk_ids,
+                               const float *topk_w, int M, int E, int H, int I, int top_k, int fmt,
+                               const int32_t *tokens, int n_tok, double *out, uint8_t *xq_out, uint8_t *xs_out,
+                               float *xg_out, int nthreads)
+{
+    return moe_oracle_forward_prefill_act(x_bf16, w13, s13, g13, w2, s2, g2, topk_ids, topk_w, M, E, H, I, top_k,
+                                          fmt, tokens, n_tok, out, xq_out, xs_out, xg_out, nthreads,
+                                          ORACLE_ACT_SILU, 0.0, 0.0, 0.0);
 }
 
 /* ------------------------------------------------- routing / compaction */

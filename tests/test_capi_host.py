@@ -90,3 +90,16 @@ def test_prepare_argument_errors(lib):
     assert st == _capi.MOE_FP4_EINVAL
     st = _capi.raw_status("moe_fp4_debug_dequant", 0x1000, 0x1000, 0, 4, 4, 256, 128, 0, 0x1000, None)
     assert st == _capi.MOE_FP4_EINVAL  # expert out of range
+
+
+def test_forward_ex_rejects_bad_activation(lib):
+    """The activation is validated before anything else touches the device."""
+    import ctypes
+    p = ctypes.c_void_p(16)
+    bad = [_capi.MoeFp4Activation(7, 0.0, 0.0, 0.0),
+           _capi.MoeFp4Activation(_capi.MOE_FP4_ACT_SWIGLUOAI, 1.702, 1.0, 0.0),
+           _capi.MoeFp4Activation(_capi.MOE_FP4_ACT_SWIGLUOAI, float("nan"), 1.0, 7.0),
+           _capi.MoeFp4Activation(_capi.MOE_FP4_ACT_SWIGLUOAI, 1.702, float("inf"), 7.0)]
+    for act in bad:
+        st = lib.moe_fp4_forward_ex(p, p, p, p, p, p, p, p, 1, 8, 256, 128, 2, 1, ctypes.byref(act), p, 1 << 20, None)
+        assert st == _capi.MOE_FP4_EINVAL

@@ -47,6 +47,15 @@ MUTATIONS = {
     "quant_tie_rule": ("if (d < bestd || (d == bestd && (c & 1) == 0)) {\n            bestd = d;\n            best = c;\n        }\n    }\n    if (signbit(v))",
                        "if (d <= bestd) {\n            bestd = d;\n            best = c;\n        }\n    }\n    if (signbit(v))"),
     "quant_negative_zero": ("if (signbit(v)) best |= 8;", "if (best != 0 && v < 0.0f) best |= 8;"),
+    "gelu_cubic_coefficient": ("(gate + 0.044715 * gate * gate * gate)", "(gate + 0.0447 * gate * gate * gate)"),
+    "gelu_half_dropped": ("return 0.5 * gate * (1.0 + tanh(", "return gate * (1.0 + tanh("),
+    "swiglu_beta_multiplied": ("return (u + a->beta) * g / (1.0 + exp(-a->alpha * g));",
+                               "return (u * a->beta) * g / (1.0 + exp(-a->alpha * g));"),
+    "swiglu_gate_unclamped": ("double g = gate < a->limit ? gate : a->limit;", "double g = gate;"),
+    "swiglu_up_clamp_dropped": ("double u = up < -a->limit ? -a->limit : (up > a->limit ? a->limit : up);",
+                                "double u = up;"),
+    "swiglu_alpha_outside": ("return (u + a->beta) * g / (1.0 + exp(-a->alpha * g));",
+                             "return a->alpha * (u + a->beta) * g / (1.0 + exp(-g));"),
     "route_order": ("for (int t = 0; t < M; ++t)\n            for (int j = 0; j < top_k; ++j)\n                if (topk_ids[(size_t)t * top_k + j] == e) perm[r++] = t * top_k + j;",
                     "for (int j = 0; j < top_k; ++j)\n            for (int t = 0; t < M; ++t)\n                if (topk_ids[(size_t)t * top_k + j] == e) perm[r++] = t * top_k + j;"),
 }
@@ -68,6 +77,11 @@ def _run_pins():
         ("route", pins.test_route_is_stable_counting_sort),
         ("top1_mx", lambda: pins.test_top1_is_gated_mlp(0)),
         ("top1_nv", lambda: pins.test_top1_is_gated_mlp(1)),
+        ("gelu_mx", lambda: pins.test_top1_gelu_tanh_is_gated_mlp(0)),
+        ("gelu_nv", lambda: pins.test_top1_gelu_tanh_is_gated_mlp(1)),
+        ("swiglu_reductions", lambda: pins.test_swigluoai_reductions(_small_case())),
+        ("swiglu_relu", lambda: pins.test_swigluoai_large_alpha_is_relu_gated(0)),
+        ("swiglu_clamps", pins.test_swigluoai_hand_worked_clamps),
     ]
     for case in pins._golden_cases():
         checks.append(("golden_" + case["name"], lambda c=case: pins.test_hand_worked_layers(c)))
@@ -79,6 +93,15 @@ def _run_pins():
         except (AssertionError, ValueError):
             failures.append(name)
     return failures
+
+
+def _small_case():
+    E, H, I, M, k = 6, 64, 32, 3, 4
+    w = pins._tiny_weights(E, H, I, pins.gen.MXFP4, seed=21)
+    x = pins.gen.draw_activations(M, H, seed=22)
+    ids = np.array([[0, 3, 5, 1], [2, 2, 4, 0], [5, 1, 3, 2]], np.int32)
+    tw = np.random.default_rng(23).uniform(0.05, 1.0, (M, k)).astype(np.float32)
+    return E, H, I, M, k, w, x, ids, tw
 
 
 def _brute_once(fmt):

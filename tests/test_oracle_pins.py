@@ -406,3 +406,78 @@ def test_route_is_stable_counting_sort():
         assert np.array_equal(perm, order)
         counts = np.bincount(flat[valid], minlength=E)
         assert np.array_equal(off, np.concatenate([[0], np.cumsum(counts)]))
+
+
+# ---------------------------------------------------------------- other gated activations
+# GELU (tanh form) and SwiGLU-OAI (alpha, beta, limit) of the SM12x sync PR's
+# activation list.  Pins: torch's tanh-approximate GELU (a library routine) in
+# a top-1 gated MLP; SwiGLU-OAI reducing to the SiLU layer and, with a large
+# alpha, to a ReLU-gated MLP (np.maximum); affine in beta; a hand-worked
+# layer where both clamps bind.
+def _top1_gated(x, w, e, H, I, fmt, act_fn):
+    g13 = w["g13"][e] if fmt == 1 else (1.0, 1.0)
+    g2 = w["g2"][e] if fmt == 1 else 1.0
+    Wg = oracle.dequant(w["w13"][e, :I], w["s13"][e, :I], H, fmt, float(g13[0]))
+    Wu = oracle.dequant(w["w13"][e, I:], w["s13"][e, I:], H, fmt, float(g13[1]))
+    Wd = oracle.dequant(w["w2"][e], w["s2"][e], I, fmt, float(g2))
+    xf = x.to(torch.float64).numpy()
+    return act_fn(xf @ Wg.T, xf @ Wu.T) @ Wd.T
+
+
+@pytest.mark.parametrize("fmt", [gen.MXFP4, gen.NVFP4])
+def test_top1_gelu_tanh_is_gated_mlp(fmt):
+    E, H, I, M = 3, 64, 64, 3
+    w = _tiny_weights(E, H, I, fmt, seed=31)
+    x = gen.draw_activations(M, H, seed=32)
+
+    def gelu_up(a, b):
+        return torch.nn.functional.gelu(torch.from_numpy(a), approximate="tanh").numpy() * b
+
+    for e in range(E):
+        ids = np.full((M, 1), e, np.int32)
+        got = oracle.forward(x, w, ids, np.ones((M, 1), np.float32), E, H, I, 1, fmt,
+                             act=(oracle.ACT_GELU_TANH, 0, 0, 0))
+        np.testing.assert_allclose(got, _top1_gated(x, w, e, H, I, fmt, gelu_up), rtol=1e-11, atol=1e-13)
+
+
+def test_swigluoai_reductions(small_case):
+    E, H, I, M, k, w, x, ids, tw = small_case
+    silu = oracle.forward(x, w, ids, tw, E, H, I, k, gen.MXFP4)
+    # alpha = 1, beta = 0, no clamping: (u) * g * sigmoid(g) = SiLU(g) * u
+    same = oracle.forward(x, w, ids, tw, E, H, I, k, gen.MXFP4, act=(oracle.ACT_SWIGLUOAI, 1.0, 0.0, 1e300))
+    np.testing.assert_allclose(same, silu, rtol=1e-13, atol=1e-15)
+    # affine in beta: out(2) - out(0) = 2 (out(1) - out(0))
+    o = [oracle.forward(x, w, ids, tw, E, H, I, k, gen.MXFP4, act=(oracle.ACT_SWIGLUOAI, 1.702, b, 7.0))
+         for b in (0.0, 1.0, 2.0)]
+    np.testing.assert_allclose(o[2] - o[0], 2 * (o[1] - o[0]), rtol=1e-9, atol=1e-12 * np.abs(o[1]).max())
+    assert np.abs(o[1] - o[0]).max() > 0
+
+
+@pytest.mark.parametrize("fmt", [gen.MXFP4, gen.NVFP4])
+def test_swigluoai_large_alpha_is_relu_gated(fmt):
+    E, H, I, M = 3, 64, 64, 3
+    w = _tiny_weights(E, H, I, fmt, seed=33)
+    x = gen.draw_activations(M, H, seed=34)
+    for e in range(E):
+        ids = np.full((M, 1), e, np.int32)
+        got = oracle.forward(x, w, ids, np.ones((M, 1), np.float32), E, H, I, 1, fmt,
+                             act=(oracle.ACT_SWIGLUOAI, 1e9, 0.0, 1e300))
+        want = _top1_gated(x, w, e, H, I, fmt, lambda a, b: np.maximum(a, 0.0) * b)
+        np.testing.assert_allclose(got, want, rtol=1e-9, atol=1e-12)
+
+
+def test_swigluoai_hand_worked_clamps():
+    # MX layer E = 1, H = I = 32: x = 1, gate nibbles 1.0 and up nibbles 0.5
+    # (scale 1) give gate = 32, up = 16; w2 nibbles 1.0 with scale 2^-5 make
+    # every FC2 row sum h.  With limit 2: gate' = 2, up' = 2, so
+    # h = (2 + beta) * 2 * sigmoid(2 alpha) for every n and out = 32 * 2^-5 * h.
+    E, H, I = 1, 32, 32
+    case = dict(fmt=0, E=E, H=H, I=I, gate_nibble=2, up_nibble=1, gate_scale_byte=127, up_scale_byte=127,
+                down_nibble=2, down_scale_byte=122)
+    w = _golden_weights(case)
+    x = torch.full((1, H), 1.0, dtype=torch.bfloat16)
+    for alpha, beta in ((1.0, 1.0), (1.702, 0.5)):
+        out = oracle.forward(x, w, np.zeros((1, 1), np.int32), np.ones((1, 1), np.float32), E, H, I, 1, 0,
+                             act=(oracle.ACT_SWIGLUOAI, alpha, beta, 2.0))
+        h = (2.0 + beta) * 2.0 / (1.0 + math.exp(-2.0 * alpha))
+        np.testing.assert_allclose(out, np.full((1, H), h), rtol=1e-13, atol=0)
