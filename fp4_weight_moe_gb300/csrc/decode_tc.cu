@@ -548,6 +548,45 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
 #pragma unroll
   for (int t = 0; t < 8; ++t) vout[t] = 0.f;
 
+  // An item's weight scales (and, with pre-pass images, its activation scales
+  // and term multipliers) into tensor memory, this warp's lane quarter
+  // (replicated), as soon as the item's TMA lands; returns false if a wait
+  // gave up.
+  auto store_sfa = [&](int i, uint32_t tq) -> bool {
+      const int sl = i % kRing;
+      bool ok = mbar_wait(&S.fullA[sl], (i / kRing) & 1, a.status, 32u);
+      if (use_img) ok = ok && mbar_wait(&S.fullB[sl], (i / kRing) & 1, a.status, 32u);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) return false;
+      const uint8_t* src = ring + sl * kSlotBytes + kSlotA + kSlotB;
+      uint32_t r[16];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const uint4 u = *reinterpret_cast<const uint4*>(src + g * kChunkBytes + lane * 16);
+        r[4 * g] = u.x;
+        r[4 * g + 1] = u.y;
+        r[4 * g + 2] = u.z;
+        r[4 * g + 3] = u.w;
+      }
+      tmem_st16(tq + kTmemSFBase + sl * 32, r);
+      if (use_img) {
+        // the item's activation scales (B rows 0..31, 64-K group g in column
+        // 4g) and its term multipliers, copied from the pre-pass image
+        const uint8_t* bsf = src + kSlotSF;
+        const uint4 u = *reinterpret_cast<const uint4*>(bsf + lane * 16);
+        const uint32_t rb[16] = {u.x, 0u, 0u, 0u, u.y, 0u, 0u, 0u, u.z, 0u, 0u, 0u, u.w, 0u, 0u, 0u};
+        tmem_st16(tq + kTmemSFBase + sl * 32 + 16, rb);
+        const float* gi = reinterpret_cast<const float*>(bsf + kChunkBytes);
+        if (lane < M * kTerms) S.G[i % kGSlots][lane / kTerms][lane % kTerms] = gi[lane];
+        __syncwarp();
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.sfa[sl]);
+      return true;
+  };
+
   if (warp == 0) {
     // ---------------- TMA producer (the weights need nothing from FC1)
     if (lane == 0) {
@@ -591,6 +630,13 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     }
   } else if (is_quant) {
     // ---------------- FC2: activation terms (B operand), one wave of ring slots at a time
+    if (use_img) {
+      // the terms come from a pre-pass image: these warps put every item's
+      // scales into tensor memory instead, running ahead of the drain
+      const uint32_t tq = S.tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+      for (int i = 0; i < n_items; ++i)
+        if (!store_sfa(i, tq)) break;
+    }
     if (!use_img) {  // (otherwise the terms come from a pre-pass)
     pdl_wait();  // FC1's h is complete and visible
     const int waves = (n_items + kRing - 1) / kRing;
@@ -647,46 +693,14 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     }
     }
   } else {
-    // ---------------- weight scales -> tensor memory, accumulator drain.
-    // Warps 6..9 own lanes 32*(warp%4) ..; each copies an item's scale chunks
-    // into its quarter (replicated) as soon as the item's TMA lands.
+    // ---------------- accumulator drain (and, when this CTA builds its own
+    // activation terms, the weight scales -> tensor memory).  Warps 7..10
+    // own lanes 32*(warp%4) ...
     const int q = warp & 3;
     const uint32_t tq = S.tmem + ((uint32_t)(32 * q) << 16);
     bool ok = true;
-    auto store_sfa = [&](int i) {
-      const int sl = i % kRing;
-      ok = ok && mbar_wait(&S.fullA[sl], (i / kRing) & 1, a.status, 32u);
-      if (use_img) ok = ok && mbar_wait(&S.fullB[sl], (i / kRing) & 1, a.status, 32u);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) return;
-      const uint8_t* src = ring + sl * kSlotBytes + kSlotA + kSlotB;
-      uint32_t r[16];
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const uint4 u = *reinterpret_cast<const uint4*>(src + g * kChunkBytes + lane * 16);
-        r[4 * g] = u.x;
-        r[4 * g + 1] = u.y;
-        r[4 * g + 2] = u.z;
-        r[4 * g + 3] = u.w;
-      }
-      tmem_st16(tq + kTmemSFBase + sl * 32, r);
-      if (use_img) {
-        // the item's activation scales (B rows 0..31, 64-K group g in column
-        // 4g) and its term multipliers, copied from the pre-pass image
-        const uint8_t* bsf = src + kSlotSF;
-        const uint4 u = *reinterpret_cast<const uint4*>(bsf + lane * 16);
-        const uint32_t rb[16] = {u.x, 0u, 0u, 0u, u.y, 0u, 0u, 0u, u.z, 0u, 0u, 0u, u.w, 0u, 0u, 0u};
-        tmem_st16(tq + kTmemSFBase + sl * 32 + 16, rb);
-        const float* gi = reinterpret_cast<const float*>(bsf + kChunkBytes);
-        if (lane < M * kTerms) S.G[i % kGSlots][lane / kTerms][lane % kTerms] = gi[lane];
-        __syncwarp();
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.sfa[sl]);
-    };
-    for (int i = 0; i < n_items && i < kRing; ++i) store_sfa(i);
+    if (!use_img)
+      for (int i = 0; ok && i < n_items && i < kRing; ++i) ok = store_sfa(i, tq);
     for (int i = 0; ok && i < n_items; ++i) {
       const int sl = i % kRing, gs = i % kGSlots;
       ok = use_img || mbar_wait(&S.gready[gs], (i / kGSlots) & 1, a.status, 16u);
@@ -706,16 +720,18 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
 #pragma unroll
         for (int c = 16; c < kMaxN; ++c) acc[c] = 0.f;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.acce[sl]);
 #pragma unroll
       for (int t = 0; t < 8; ++t)
         if (t < M) {
 #pragma unroll
           for (int u = 0; u < kTerms; ++u) vout[t] = fmaf(acc[t * kTerms + u], S.G[gs][t][u], vout[t]);
         }
-      if (i + kRing < n_items) store_sfa(i + kRing);
+      // (the multipliers are read before the slot is released: with images,
+      // the scale warps refill S.G for later items as soon as they may)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.acce[sl]);
+      if (!use_img && i + kRing < n_items) ok = ok && store_sfa(i + kRing, tq);
     }
   }
 
