@@ -127,16 +127,29 @@ def reserve_workspace(M_max: int, E: int, H: int, I: int, top_k: int, fmt: int, 
     _capi.moe_fp4_reserve_workspace(M_max, E, H, I, top_k, fmt, _stream(stream))
 
 
+def _check_dtypes(x, topk_ids, topk_weights):
+    if x.dtype != torch.bfloat16 or topk_ids.dtype not in (torch.int32, torch.int64) or \
+            topk_weights.dtype != torch.float32:
+        raise TypeError("x must be bfloat16, topk_ids int32 or int64, topk_weights float32")
+
+
 def forward(x: torch.Tensor, pw: PreparedWeights, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
             out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """The fused MoE layer: bf16 ``x [M, H]`` -> bf16 ``out [M, H]``."""
-    if x.dtype != torch.bfloat16 or topk_ids.dtype != torch.int32 or topk_weights.dtype != torch.float32:
-        raise TypeError("x must be bfloat16, topk_ids int32, topk_weights float32")
+    """The fused MoE layer: bf16 ``x [M, H]`` -> bf16 ``out [M, H]``.  int64
+    ``topk_ids`` need a caller ``workspace`` (moe_fp4_forward_ex_i64)."""
+    _check_dtypes(x, topk_ids, topk_weights)
     _require_cuda(x, topk_ids, topk_weights, out, workspace)
     M, H = x.shape
     top_k = topk_ids.shape[1]
     if out is None:
         out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    if topk_ids.dtype == torch.int64:
+        if workspace is None:
+            raise TypeError("int64 topk_ids need a caller workspace (alloc_workspace)")
+        _capi.moe_fp4_forward_ex_i64(_ptr(x), *pw.ptrs(), _ptr(topk_ids), _ptr(topk_weights), _ptr(out), M, pw.E,
+                                     pw.H, pw.I, top_k, pw.fmt, None, _ptr(workspace), workspace.nbytes,
+                                     _stream(stream, x.device))
+        return out
     args = (_ptr(x), *pw.ptrs(), _ptr(topk_ids), _ptr(topk_weights), _ptr(out), M, pw.E, pw.H, pw.I, top_k, pw.fmt)
     if workspace is None:
         _capi.moe_fp4_forward(*args, _stream(stream, x.device))
@@ -155,16 +168,15 @@ def forward_act(x: torch.Tensor, pw: PreparedWeights, topk_ids: torch.Tensor, to
                 limit: float = 0.0, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """The layer with a chosen gated activation (ACT_SILU, ACT_GELU_TANH, or
     ACT_SWIGLUOAI with alpha, beta, limit), on a caller-owned workspace."""
-    if x.dtype != torch.bfloat16 or topk_ids.dtype != torch.int32 or topk_weights.dtype != torch.float32:
-        raise TypeError("x must be bfloat16, topk_ids int32, topk_weights float32")
+    _check_dtypes(x, topk_ids, topk_weights)
     _require_cuda(x, topk_ids, topk_weights, out, workspace)
     M, H = x.shape
     if out is None:
         out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
     act = _capi.MoeFp4Activation(kind, alpha, beta, limit)
-    _capi.moe_fp4_forward_ex(_ptr(x), *pw.ptrs(), _ptr(topk_ids), _ptr(topk_weights), _ptr(out), M, pw.E, pw.H, pw.I,
-                             topk_ids.shape[1], pw.fmt, act, _ptr(workspace), workspace.nbytes,
-                             _stream(stream, x.device))
+    call = _capi.moe_fp4_forward_ex_i64 if topk_ids.dtype == torch.int64 else _capi.moe_fp4_forward_ex
+    call(_ptr(x), *pw.ptrs(), _ptr(topk_ids), _ptr(topk_weights), _ptr(out), M, pw.E, pw.H, pw.I, topk_ids.shape[1],
+         pw.fmt, act, _ptr(workspace), workspace.nbytes, _stream(stream, x.device))
     return out
 
 

@@ -54,6 +54,8 @@ SIGNATURES = {
     "moe_fp4_forward_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "moe_fp4_forward_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                 ctypes.POINTER(MoeFp4Activation), _P, _Z, _P]),
+    "moe_fp4_forward_ex_i64": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                    ctypes.POINTER(MoeFp4Activation), _P, _Z, _P]),
     "moe_fp4_forward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "moe_fp4_host_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
     "moe_fp4_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
@@ -162,6 +164,13 @@ def moe_fp4_forward_ex(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt
     return _check("moe_fp4_forward_ex",
                   _load().moe_fp4_forward_ex(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt,
                                              None if act is None else ctypes.byref(act), ws, ws_bytes, stream))
+
+
+def moe_fp4_forward_ex_i64(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt, act, ws, ws_bytes, stream):
+    """moe_fp4_forward_ex with int64 ``ids``."""
+    return _check("moe_fp4_forward_ex_i64",
+                  _load().moe_fp4_forward_ex_i64(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt,
+                                                 None if act is None else ctypes.byref(act), ws, ws_bytes, stream))
 
 
 def moe_fp4_forward_noalloc(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, fmt, stream):

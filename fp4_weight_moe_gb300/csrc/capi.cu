@@ -19,8 +19,8 @@ cudaError_t launch_debug_gemm(const void* a_q, const void* a_sf, const void* b_q
 size_t prefill_workspace_bytes(int M, int E, int H, int I, int top_k);
 size_t debug_route_workspace_bytes(int M, int E, int top_k);
 cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
-                           const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
-                           const ActParams& act, void* ws, cudaStream_t st, int* cu_err);
+                           const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
+                           int top_k, const ActParams& act, void* ws, cudaStream_t st, int* cu_err);
 cudaError_t launch_debug_route(const int32_t* ids, int M, int E, int top_k, int32_t* perm, int32_t* expert_offset,
                                void* ws, cudaStream_t st);
 cudaError_t launch_debug_quant(const float* in, int rows, int K, uint8_t* q, uint8_t* s, float* G, cudaStream_t st);
@@ -28,8 +28,8 @@ extern std::atomic<int> g_decode_family;
 bool decode_gemv_fits(int M, int E, int H, int I, int top_k);
 int decode_launches(int M, int E, int H, int I, int top_k);
 cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
-                          const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
-                          int fmt, const ActParams& act, void* ws, int num_sms, cudaStream_t st);
+                          const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
+                          int top_k, int fmt, const ActParams& act, void* ws, int num_sms, cudaStream_t st);
 }  // namespace moe_fp4
 
 using namespace moe_fp4;
@@ -257,10 +257,14 @@ int moe_fp4_release_workspace(void) {
   return MOE_FP4_OK;
 }
 
-int moe_fp4_forward_ex(const void* x_bf16, const void* w13, const void* s13, const void* w2, const void* s2,
-                       const int32_t* topk_ids, const float* topk_weights, void* out_bf16, int M, int E, int H,
-                       int I, int top_k, int fmt, const moe_fp4_activation* act, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+namespace {
+// moe_fp4_forward_ex and moe_fp4_forward_ex_i64: topk_ids int32 (ids64 = 0)
+// or int64 (ids64 = 1)
+int forward_any_ids(const void* x_bf16, const void* w13, const void* s13, const void* w2, const void* s2,
+                    const void* topk_ids, int ids64, const float* topk_weights, void* out_bf16, int M, int E, int H,
+                    int I, int top_k, int fmt, const moe_fp4_activation* act, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  const int32_t* ids = static_cast<const int32_t*>(topk_ids);
   ActParams ap = {MOE_FP4_ACT_SILU, 0.f, 0.f, 0.f};
   if (act) {
     if (act->kind != MOE_FP4_ACT_SILU && act->kind != MOE_FP4_ACT_GELU_TANH && act->kind != MOE_FP4_ACT_SWIGLUOAI)
@@ -288,16 +292,34 @@ int moe_fp4_forward_ex(const void* x_bf16, const void* w13, const void* s13, con
   if (M <= MOE_FP4_DECODE_MAX_M) {
     const size_t need = decode_workspace_bytes(M, H, I, top_k, fmt, sms);
     if (need >= kMaxWorkspace || workspace_bytes < need) return MOE_FP4_EWORKSPACE;
-    cudaError_t e = launch_decode(x_bf16, w13, s13, w2, s2, topk_ids, topk_weights, out_bf16, M, E, H, I, top_k,
+    cudaError_t e = launch_decode(x_bf16, w13, s13, w2, s2, ids, ids64, topk_weights, out_bf16, M, E, H, I, top_k,
                                   fmt, ap, workspace, sms, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
   }
   const size_t need = prefill_workspace_bytes(M, E, H, I, top_k);
   if (need >= kMaxWorkspace || workspace_bytes < need) return MOE_FP4_EWORKSPACE;
   int cu = 0;
-  cudaError_t e = launch_prefill(x_bf16, w13, s13, w2, s2, topk_ids, topk_weights, out_bf16, M, E, H, I, top_k, ap,
-                                 workspace, static_cast<cudaStream_t>(stream), &cu);
+  cudaError_t e = launch_prefill(x_bf16, w13, s13, w2, s2, ids, ids64, topk_weights, out_bf16, M, E, H, I, top_k,
+                                 ap, workspace, static_cast<cudaStream_t>(stream), &cu);
   return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
+}
+}  // namespace
+
+int moe_fp4_forward_ex(const void* x_bf16, const void* w13, const void* s13, const void* w2, const void* s2,
+                       const int32_t* topk_ids, const float* topk_weights, void* out_bf16, int M, int E, int H,
+                       int I, int top_k, int fmt, const moe_fp4_activation* act, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return forward_any_ids(x_bf16, w13, s13, w2, s2, topk_ids, 0, topk_weights, out_bf16, M, E, H, I, top_k, fmt, act,
+                         workspace, workspace_bytes, stream);
+}
+
+int moe_fp4_forward_ex_i64(const void* x_bf16, const void* w13, const void* s13, const void* w2, const void* s2,
+                           const int64_t* topk_ids, const float* topk_weights, void* out_bf16, int M, int E, int H,
+                           int I, int top_k, int fmt, const moe_fp4_activation* act, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (((uintptr_t)topk_ids & 7u) != 0) return MOE_FP4_EINVAL;
+  return forward_any_ids(x_bf16, w13, s13, w2, s2, topk_ids, 1, topk_weights, out_bf16, M, E, H, I, top_k, fmt, act,
+                         workspace, workspace_bytes, stream);
 }
 
 int moe_fp4_forward_ws(const void* x_bf16, const void* w13, const void* s13, const void* w2, const void* s2,

@@ -85,6 +85,21 @@ __device__ __forceinline__ uint4 ld_stream_16(const void* p) {
   return v;
 }
 
+// Routing id j of the caller's top-k ids: int32 as stored, or int64 (wide)
+// narrowed to int32 with every value outside [0, E) mapped to -1, so that the
+// narrowing never turns an invalid id into a valid one.  The ids are inputs
+// of the call and stay unchanged during it (non-coherent loads).
+__device__ __forceinline__ int route_id(const int32_t* ids, int j, int wide, int E) {
+  if (wide) {
+    long long v;
+    asm volatile("ld.global.nc.s64 %0, [%1];" : "=l"(v) : "l"(reinterpret_cast<const long long*>(ids) + j));
+    return v >= 0 && v < (long long)E ? (int)v : -1;
+  }
+  int r;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(r) : "l"(ids + j));
+  return r;
+}
+
 // L2 policy: lines loaded with it are the first candidates for eviction.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;

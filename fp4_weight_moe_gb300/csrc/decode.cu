@@ -20,15 +20,15 @@ std::atomic<int> g_decode_family{0};
 
 size_t decode_tc_scratch_bytes(int M, int H, int I, int top_k, int num_sms);
 cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
-                             const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
-                             const ActParams& act, float* scratch, uint32_t* status, int num_sms, cudaStream_t st,
-                             int* cu_err);
+                             const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
+                             int top_k, const ActParams& act, float* scratch, uint32_t* status, int num_sms,
+                             cudaStream_t st, int* cu_err);
 bool decode_gemv_fits(int M, int E, int H, int I, int top_k);
 size_t decode_gemv_scratch_bytes(int M, int I, int top_k);
 cudaError_t launch_decode_gemv(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
-                               const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I,
-                               int top_k, const ActParams& act, float* scratch, uint32_t* status, cudaStream_t st,
-                               int* cu_err);
+                               const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H,
+                               int I, int top_k, const ActParams& act, float* scratch, uint32_t* status,
+                               cudaStream_t st, int* cu_err);
 
 static size_t decode_scratch_bytes(int M_max, int H, int I, int top_k, int num_sms) {
   const size_t tc = decode_tc_scratch_bytes(M_max, H, I, top_k, num_sms);
@@ -62,8 +62,8 @@ int decode_launches(int M, int E, int H, int I, int top_k) {
 }
 
 cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
-                          const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
-                          int fmt, const ActParams& act, void* ws, int num_sms, cudaStream_t st) {
+                          const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
+                          int top_k, int fmt, const ActParams& act, void* ws, int num_sms, cudaStream_t st) {
   (void)fmt;
   int cu = 0;
   uint32_t* status =
@@ -71,9 +71,9 @@ cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const
   const int family = g_decode_family.load(std::memory_order_relaxed);
   const bool fits = decode_gemv_fits(M, E, H, I, top_k);
   if (family == 1 ? fits : family == 0 && fits && gemv_preferred(M, H, I, top_k))
-    return launch_decode_gemv(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, act, static_cast<float*>(ws),
+    return launch_decode_gemv(x, w13, s13, w2, s2, ids, ids64, tw, out, M, E, H, I, top_k, act, static_cast<float*>(ws),
                               status, st, &cu);
-  return launch_decode_tc(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, act, static_cast<float*>(ws),
+  return launch_decode_tc(x, w13, s13, w2, s2, ids, ids64, tw, out, M, E, H, I, top_k, act, static_cast<float*>(ws),
                           status, num_sms, st, &cu);
 }
 

@@ -68,7 +68,8 @@ constexpr uint32_t kErrGvFull = 256u, kErrGvEmpty = 512u, kErrGvH = 1024u;
 
 struct GvArgs {
   const __nv_bfloat16* x;  // [M][H]
-  const int32_t* ids;      // [M][top_k]
+  const int32_t* ids;      // [M][top_k], int32 or (ids64) int64
+  int ids64;
   const float* tw;         // [M][top_k]
   const uint8_t* s13;      // resident scales + multipliers (for the multipliers)
   const uint8_t* s2;
@@ -120,11 +121,6 @@ __device__ __forceinline__ uint8_t* gv_smem_base() {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gv_smem_raw) + 1023) & ~(uintptr_t)1023);
 }
 
-__device__ __forceinline__ int gv_ld_s32(const void* p) {
-  int r;
-  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(r) : "l"(p));
-  return r;
-}
 __device__ __forceinline__ float gv_ld_f32(const void* p) {
   float r;
   asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(r) : "l"(p));
@@ -212,7 +208,7 @@ __global__ void __launch_bounds__(kGvThreads, 4)
 
   if (warp == 0) {
     for (int j = lane; j < n; j += 32) {
-      C.ids[j] = gv_ld_s32(a.ids + j);
+      C.ids[j] = route_id(a.ids, j, a.ids64, a.E);
       C.tw[j] = gv_ld_f32(a.tw + j);
     }
     __syncwarp();
@@ -381,7 +377,7 @@ __global__ void __launch_bounds__(kGvThreads, 4)
     // The routing is stable for the whole call (FC1 waited for its
     // producer), so the weight stream starts before FC1 is done.
     for (int j = lane; j < kGvMaxSlots; j += 32) {
-      C.ids[j] = j < n ? gv_ld_s32(a.ids + j) : -1;
+      C.ids[j] = j < n ? route_id(a.ids, j, a.ids64, a.E) : -1;
       C.tmask[j] = 0u;
     }
     __syncwarp();
@@ -584,8 +580,8 @@ size_t decode_gemv_scratch_bytes(int M, int I, int top_k) {
 }
 
 cudaError_t launch_decode_gemv(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
-                               const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I,
-                               int top_k, const ActParams& act, float* scratch, uint32_t* status, cudaStream_t st,
+                               const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H,
+                               int I, int top_k, const ActParams& act, float* scratch, uint32_t* status, cudaStream_t st,
                                int* cu_err) {
   CUtensorMap w13m, s13m, w2m, s2m;
   {
@@ -622,6 +618,7 @@ cudaError_t launch_decode_gemv(const void* x, const void* w13, const void* s13, 
   GvArgs a;
   a.x = static_cast<const __nv_bfloat16*>(x);
   a.ids = ids;
+  a.ids64 = ids64;
   a.tw = tw;
   a.s13 = static_cast<const uint8_t*>(s13);
   a.s2 = static_cast<const uint8_t*>(s2);

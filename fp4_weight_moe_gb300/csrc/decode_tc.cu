@@ -114,7 +114,8 @@ constexpr uint32_t kTcSmem = kRing * kSlotBytes + sizeof(SmemTc) + 1024;
 
 struct TcArgs {
   const __nv_bfloat16* x;
-  const int32_t* ids;
+  const int32_t* ids;  // [M][top_k], int32 or (ids64) int64
+  int ids64;
   const float* tw;
   const uint8_t* s13;
   const uint8_t* s2;
@@ -250,11 +251,6 @@ __device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
   asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
   return r;
 }
-__device__ __forceinline__ int ld_nc_s32(const void* p) {
-  int r;
-  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(r) : "l"(p));
-  return r;
-}
 __device__ __forceinline__ float ld_nc_f32(const void* p) {
   float r;
   asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(r) : "l"(p));
@@ -320,7 +316,7 @@ __global__ void __launch_bounds__(256) decode_quant_h_kernel(TcArgs a) {
   const int ns2 = (a.I + 255) / 256;
   const int j = blockIdx.x / ns2, st = blockIdx.x % ns2;
   const int token = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int k = threadIdx.x; k < a.n_slots; k += blockDim.x) s_ids[k] = __ldg(a.ids + k);
+  for (int k = threadIdx.x; k < a.n_slots; k += blockDim.x) s_ids[k] = route_id(a.ids, k, a.ids64, a.E);
   __syncthreads();
   const int e = s_ids[j];
   if (e < 0 || e >= a.E) return;
@@ -379,7 +375,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int j = lane + 32 * k;
-      idr[k] = j < n ? ld_nc_s32(a.ids + j) : -1;
+      idr[k] = j < n ? route_id(a.ids, j, a.ids64, a.E) : -1;
       twr[k] = j < n ? ld_nc_f32(a.tw + j) : 0.f;
     }
   }
@@ -842,8 +838,8 @@ size_t decode_tc_scratch_bytes(int M, int H, int I, int top_k, int num_sms) {
 }
 
 cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
-                             const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
-                             const ActParams& act, float* scratch, uint32_t* status, int num_sms, cudaStream_t st,
+                             const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
+                             int top_k, const ActParams& act, float* scratch, uint32_t* status, int num_sms, cudaStream_t st,
                              int* cu_err) {
   CUtensorMap m13, m2;
   CUresult r = make_fp4_map(&m13, w13, (uint64_t)H / 2, (uint64_t)E * 2 * I, 128);
@@ -866,6 +862,7 @@ cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, co
   TcArgs a;
   a.x = static_cast<const __nv_bfloat16*>(x);
   a.ids = ids;
+  a.ids64 = ids64;
   a.tw = tw;
   a.s13 = static_cast<const uint8_t*>(s13);
   a.s2 = static_cast<const uint8_t*>(s2);

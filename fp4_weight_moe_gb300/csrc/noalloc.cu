@@ -23,8 +23,8 @@
 namespace moe_fp4 {
 size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int fmt, int num_sms);
 cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
-                          const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
-                          int fmt, const ActParams& act, void* ws, int num_sms, cudaStream_t st);
+                          const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
+                          int top_k, int fmt, const ActParams& act, void* ws, int num_sms, cudaStream_t st);
 }  // namespace moe_fp4
 
 namespace {
@@ -89,7 +89,7 @@ extern "C" int moe_fp4_forward_noalloc(const void* x_bf16, const void* w13, cons
   // Nothing in the scratch needs to start at zero: FC1 writes every
   // intermediate element that FC2 reads in the same call.
   const ActParams silu_act = {MOE_FP4_ACT_SILU, 0.f, 0.f, 0.f};
-  cudaError_t e = launch_decode(x_bf16, w13, s13, w2, s2, topk_ids, topk_weights, out_bf16, M, E, H, I, top_k, fmt,
+  cudaError_t e = launch_decode(x_bf16, w13, s13, w2, s2, topk_ids, 0, topk_weights, out_bf16, M, E, H, I, top_k, fmt,
                                 silu_act, scratch, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_FP4_OK : MOE_FP4_ECUDA;
 }

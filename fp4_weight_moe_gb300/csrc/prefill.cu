@@ -194,7 +194,8 @@ constexpr int kMaxPrefillE = 4096;
 
 struct PrefillArgs {
   const __nv_bfloat16* x;
-  const int32_t* ids;
+  const int32_t* ids;  // [M][top_k], int32 or (ids64) int64
+  int ids64;
   const float* tw;
   const uint8_t* s13;  // resident scale chunks (+ multipliers)
   const uint8_t* s2;
@@ -299,7 +300,7 @@ __global__ void route_count_kernel(PrefillArgs a) {
   __syncthreads();
   const int i = blockIdx.x * kRouteBlock + threadIdx.x;
   if (i < a.n_entries) {
-    const int e = a.ids[i];
+    const int e = route_id(a.ids, i, a.ids64, a.E);
     if (e >= 0 && e < a.E) atomicAdd(&s_hist[e], 1);
   }
   __syncthreads();
@@ -416,7 +417,7 @@ __global__ void route_scatter_kernel(PrefillArgs a) {
   __syncwarp();
   for (int r0 = 0; r0 < kRouteBlock; r0 += 32) {
     const int i = blockIdx.x * kRouteBlock + r0 + lane;
-    const int e = i < a.n_entries ? a.ids[i] : -1;
+    const int e = i < a.n_entries ? route_id(a.ids, i, a.ids64, a.E) : -1;
     const bool valid = e >= 0 && e < a.E;
     const int key = valid ? e : -1 - lane;  // invalid entries stay alone
     const uint32_t peers = __match_any_sync(0xffffffffu, key);
@@ -690,6 +691,7 @@ PrefillArgs prefill_args(const PrefillCarve& c, void* ws, int M, int E, int H, i
   PrefillArgs a;
   a.x = nullptr;
   a.ids = nullptr;
+  a.ids64 = 0;
   a.tw = nullptr;
   a.s13 = a.s2 = nullptr;
   a.out = nullptr;
@@ -736,13 +738,14 @@ size_t prefill_workspace_bytes(int M, int E, int H, int I, int top_k) {
 }
 
 cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
-                           const int32_t* ids, const float* tw, void* out, int M, int E, int H, int I, int top_k,
-                           const ActParams& act, void* ws, cudaStream_t st, int* cu_err) {
+                           const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
+                           int top_k, const ActParams& act, void* ws, cudaStream_t st, int* cu_err) {
   const PrefillCarve c = prefill_carve(M, E, H, I, top_k);
   PrefillArgs a = prefill_args(c, ws, M, E, H, I, top_k);
   a.act = act;
   a.x = static_cast<const __nv_bfloat16*>(x);
   a.ids = ids;
+  a.ids64 = ids64;
   a.tw = tw;
   a.s13 = static_cast<const uint8_t*>(s13);
   a.s2 = static_cast<const uint8_t*>(s2);

@@ -247,6 +247,25 @@ MOE_FP4_API int moe_fp4_forward_ex(const void *x_bf16, const void *w13, const vo
                                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * moe_fp4_forward_ex with int64 routing ids (topk_ids int64 [M][top_k],
+ * row-major, device memory, 8-byte aligned).  The b12x PR #459 page (Reduce
+ * NVFP4-CSF scale reconstruction overhead, its commit list) keeps kernels
+ * for both integer types of the routing ids; here the same kernels read
+ * either width.  Every id outside [0, E) is invalid and contributes exactly
+ * zero, including values that do not fit in 32 bits (they are never
+ * truncated into a valid expert).  Same arguments, workspace, results and
+ * errors as moe_fp4_forward_ex otherwise, plus MOE_FP4_EINVAL for a
+ * topk_ids pointer that is not 8-byte aligned.  For ids that are all in
+ * [-2^31, 2^31) the output is bitwise that of moe_fp4_forward_ex on the same
+ * ids as int32.
+ */
+MOE_FP4_API int moe_fp4_forward_ex_i64(const void *x_bf16, const void *w13, const void *s13, const void *w2,
+                                       const void *s2, const int64_t *topk_ids, const float *topk_weights,
+                                       void *out_bf16, int M, int E, int H, int I, int top_k, int fmt,
+                                       const moe_fp4_activation *act, void *workspace, size_t workspace_bytes,
+                                       void *stream);
+
+/*
  * The decode-band layer (M <= MOE_FP4_DECODE_MAX_M) without any device
  * allocation, for callers that cannot call cudaMalloc where they run the
  * layer: inside a stream capture, under a runtime that owns all device memory

@@ -103,3 +103,21 @@ def test_forward_ex_rejects_bad_activation(lib):
     for act in bad:
         st = lib.moe_fp4_forward_ex(p, p, p, p, p, p, p, p, 1, 8, 256, 128, 2, 1, ctypes.byref(act), p, 1 << 20, None)
         assert st == _capi.MOE_FP4_EINVAL
+
+
+def test_forward_ex_i64_argument_errors(lib):
+    """int64 routing ids: an ids pointer that is not 8-byte aligned, null
+    pointers and bad shapes are rejected on the host; an empty batch is a
+    no-op."""
+    import ctypes
+    p = ctypes.c_void_p(0x1000)
+
+    def st(ids=0x1000, x=0x1000, M=1, H=256):
+        return lib.moe_fp4_forward_ex_i64(ctypes.c_void_p(x), p, p, p, p, ctypes.c_void_p(ids), p, p, M, 8, H, 128, 2,
+                                          1, None, p, 1 << 20, None)
+
+    assert st(ids=0x1004) == _capi.MOE_FP4_EINVAL  # 4-byte aligned only
+    assert st(x=0) == _capi.MOE_FP4_EINVAL
+    assert st(ids=0) == _capi.MOE_FP4_EINVAL
+    assert st(H=384) == _capi.MOE_FP4_EUNSUPPORTED
+    assert st(M=0) == _capi.MOE_FP4_OK
