@@ -795,18 +795,15 @@ int fc1_split(int n_slots, int H, int I, int sms) {
 }
 
 // CTAs per w2 row tile (the cluster): 8, or the number of (slot, K stage)
-// items if smaller (measured best: the items of a tile spread over more SMs);
-// fewer when that lets all of FC2 start at once beside FC1 (one CTA per SM)
-// without giving up more than a sixth of the CTAs; and for wide layers (many
-// row tiles) never more than about 1.5 CTAs per SM, so that FC2 runs in one
-// wave after FC1 leaves the SMs instead of a wave and a tail (measured on
-// H = 7168: 4 CTAs per tile, 224 CTAs, beat 8 by 9% at one token and 1-2% at
-// 4 and 8).
+// items if smaller (the items of a tile spread over more SMs), but never
+// more than about 1.5 CTAs per SM, so that FC2 runs in one wave once FC1
+// leaves the SMs instead of a wave and a tail.  Measured on GB300: H = 4096
+// at 4 tokens 33.7-34.1 us with 6-8 CTAs per tile against 35.7 with 4;
+// H = 2560, 4 and 8 tokens, 8 beats 7 by 2-4%; H = 7168 (56 tiles), 4 CTAs
+// (224) beat 8 (448) by 9% at one token and 5 (280) by 15% at two.
 int fc2_split(int n_slots, int H, int I, int sms) {
   const int tiles = H / 128, items = n_slots * ((I + 255) / 256);
   int q = items < 8 ? (items < 1 ? 1 : items) : 8;
-  const int fit = sms / tiles;
-  if (q * tiles > sms && fit >= 1 && fit < q && 6 * fit * tiles >= 5 * sms) q = fit;
   if (2 * q * tiles > 3 * sms) q = 3 * sms / (2 * tiles);
   return q < 1 ? 1 : q;
 }
