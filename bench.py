@@ -284,7 +284,8 @@ def run_ours(args):
 
     per_layer_bytes = [layer_bytes(ids_pool[i], E, H, I, M, k, fmt)[0] for i in range(K)]
     step_bytes = sum(per_layer_bytes)
-    prefill = M > m.MOE_FP4_DECODE_MAX_M
+    # batches past the decode band that run as decode-band chunks report like the decode band
+    prefill = M > m.MOE_FP4_DECODE_MAX_M and m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) == 0
     step_flops = sum(layer_flops(ids_pool[i], E, H, I) for i in range(K))
 
     sampler = ClockSampler(local)
@@ -369,7 +370,9 @@ def run_ours(args):
                      "peak_source": f"hbm_gbs of {peak_kind}", "traffic": traffic,
                      "kernel": ("decode layer: streaming-GEMV FC1 + FC2 (PDL-chained)"
                               if m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) == 2 else
-                              "decode layer: x pre-pass + FC1 + " + ("" if M < 2 else "h pre-pass + ")
+                              ("decode layer" if M <= m.MOE_FP4_DECODE_MAX_M else
+                               f"decode layer in {-(-M // m.MOE_FP4_DECODE_MAX_M)} chunks")
+                              + ": x pre-pass + FC1 + " + ("" if M < 2 else "h pre-pass + ")
                               + "FC2 (tcgen05, PDL-chained)")},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": M * H * 2 + M * k * 8,
                 "d2h_bytes_per_step": M * H * 2, "us_per_layer": e2e_ms * 1e3 / K},

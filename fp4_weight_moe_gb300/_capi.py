@@ -60,6 +60,7 @@ SIGNATURES = {
     "moe_fp4_host_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
     "moe_fp4_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "moe_fp4_debug_set_decode_family": (_I, [_I, ctypes.POINTER(ctypes.c_int)]),
+    "moe_fp4_debug_set_mid_band": (_I, [_I, ctypes.POINTER(ctypes.c_int)]),
     "moe_fp4_debug_decode_gemv_fits": (_I, [_I, _I, _I, _I, _I]),
     "moe_fp4_debug_decode_launches": (_I, [_I, _I, _I, _I, _I]),
     "moe_fp4_debug_dequant": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
@@ -191,6 +192,12 @@ def moe_fp4_forward_host(x, w13, s13, w2, s2, ids, tw, out, M, E, H, I, top_k, f
 def moe_fp4_debug_set_decode_family(family: int) -> int:
     prev = ctypes.c_int()
     _check("moe_fp4_debug_set_decode_family", _load().moe_fp4_debug_set_decode_family(family, ctypes.byref(prev)))
+    return prev.value
+
+
+def moe_fp4_debug_set_mid_band(mode: int) -> int:
+    prev = ctypes.c_int()
+    _check("moe_fp4_debug_set_mid_band", _load().moe_fp4_debug_set_mid_band(mode, ctypes.byref(prev)))
     return prev.value
 
 

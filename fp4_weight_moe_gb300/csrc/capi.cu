@@ -258,6 +258,28 @@ int moe_fp4_release_workspace(void) {
 }
 
 namespace {
+// Batches past the decode band: 0 by shape, 1 the prefill band, 2 the decode
+// kernels in chunks (test support: moe_fp4_debug_set_mid_band).
+std::atomic<int> g_mid_band{0};
+constexpr int kMidBandMaxM = 3 * MOE_FP4_DECODE_MAX_M;
+
+// Does a batch of M > MOE_FP4_DECODE_MAX_M tokens run as decode-band chunks?
+// By shape: up to 2 * MOE_FP4_DECODE_MAX_M tokens when one expert's weights
+// (3IH/2 nibble bytes) are at most 8 MiB.  Chunks stream an expert once per
+// chunk that routes to it instead of once per layer, but skip the prefill
+// band's routing, quantisation and cast launches; with small experts the
+// launches cost more.  Measured on GB300 (us per layer, prefill / chunks):
+// E=512 H=2560 I=320 k=10: M=9 78.8 / 49.0, 12 89.8 / 58.1, 16 103.6 / 82.8,
+// 24 124.2 / 124.1; E=288 H=4096 I=512 k=10: M=9 106.6 / 80.9, 16 150.0 /
+// 120.9, 24 181.4 / 181.0; E=256 H=7168 I=2048 k=8 (21 MiB experts, Zipf
+// routing): M=9 285.0 / 298.2, 16 412.5 / 482.6.
+bool mid_band_chunks(int M, int H, int I) {
+  const int mode = g_mid_band.load(std::memory_order_relaxed);
+  if (M > kMidBandMaxM) return false;
+  if (mode != 0) return mode == 2;
+  return M <= 2 * MOE_FP4_DECODE_MAX_M && 3 * (size_t)I * H / 2 <= ((size_t)8 << 20);
+}
+
 // moe_fp4_forward_ex and moe_fp4_forward_ex_i64: topk_ids int32 (ids64 = 0)
 // or int64 (ids64 = 1)
 int forward_any_ids(const void* x_bf16, const void* w13, const void* s13, const void* w2, const void* s2,
@@ -289,6 +311,34 @@ int forward_any_ids(const void* x_bf16, const void* w13, const void* s13, const 
   int sms = 0;
   st = device_sms(&sms);
   if (st != MOE_FP4_OK) return st;
+  if (M > MOE_FP4_DECODE_MAX_M && mid_band_chunks(M, H, I)) {
+    // balanced chunks of at most MOE_FP4_DECODE_MAX_M tokens, one after
+    // another on the stream (each overwrites only its own rows of out; a
+    // chunk's first kernel waits for the previous chunk before it touches
+    // the shared workspace)
+    const int n = (M + MOE_FP4_DECODE_MAX_M - 1) / MOE_FP4_DECODE_MAX_M;
+    size_t need = 0;
+    for (int c = 0, m0 = 0; c < n; ++c) {
+      const int mc = (M - m0) / (n - c);
+      const size_t b = decode_workspace_bytes(mc, H, I, top_k, fmt, sms);
+      need = b > need ? b : need;
+      m0 += mc;
+    }
+    if (need >= kMaxWorkspace || workspace_bytes < need) return MOE_FP4_EWORKSPACE;
+    const size_t id_bytes = ids64 ? 8 : 4;
+    for (int c = 0, m0 = 0; c < n; ++c) {
+      const int mc = (M - m0) / (n - c);
+      const size_t r0 = (size_t)m0 * top_k;
+      cudaError_t e = launch_decode(
+          static_cast<const uint16_t*>(x_bf16) + (size_t)m0 * H, w13, s13, w2, s2,
+          reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(topk_ids) + r0 * id_bytes), ids64,
+          topk_weights + r0, static_cast<uint16_t*>(out_bf16) + (size_t)m0 * H, mc, E, H, I, top_k, fmt, ap,
+          workspace, sms, static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return fail_cuda(e);
+      m0 += mc;
+    }
+    return MOE_FP4_OK;
+  }
   if (M <= MOE_FP4_DECODE_MAX_M) {
     const size_t need = decode_workspace_bytes(M, H, I, top_k, fmt, sms);
     if (need >= kMaxWorkspace || workspace_bytes < need) return MOE_FP4_EWORKSPACE;
@@ -379,12 +429,13 @@ int moe_fp4_forward_host(const void* x_bf16, const void* w13, const void* s13, c
   char* stage = static_cast<char*>(workspace) + base;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t xb = (size_t)M * H * 2, rb = (size_t)M * top_k * 4;
-  // In the decode band, buffers the GPU can address (page-locked host
-  // memory, mapped into the device's address space over the CPU-GPU link) are
-  // read and written in place by the kernels: a few KB each, where a copy's
-  // fixed cost would exceed the layer's.  Everything else, and the prefill
-  // band's large tensors, go through the staging area.
-  const bool decode = M <= MOE_FP4_DECODE_MAX_M;
+  // On the decode-band kernels (and their chunks), buffers the GPU can
+  // address (page-locked host memory, mapped into the device's address space
+  // over the CPU-GPU link) are read and written in place by the kernels: a
+  // few KB each, where a copy's fixed cost would exceed the layer's.
+  // Everything else, and the prefill band's large tensors, go through the
+  // staging area.
+  const bool decode = M <= MOE_FP4_DECODE_MAX_M || mid_band_chunks(M, H, I);
   void* xd = decode ? device_view(x_bf16) : nullptr;
   void* idd = decode ? device_view(topk_ids) : nullptr;
   void* twd = decode ? device_view(topk_weights) : nullptr;
@@ -419,13 +470,29 @@ int moe_fp4_debug_set_decode_family(int family, int* previous) {
   return MOE_FP4_OK;
 }
 
+int moe_fp4_debug_set_mid_band(int mode, int* previous) {
+  if (mode < 0 || mode > 2) return MOE_FP4_EINVAL;
+  const int old = g_mid_band.exchange(mode);
+  if (previous) *previous = old;
+  return MOE_FP4_OK;
+}
+
 int moe_fp4_debug_decode_gemv_fits(int M, int E, int H, int I, int top_k) {
   return decode_gemv_fits(M, E, H, I, top_k) ? 1 : 0;
 }
 
 int moe_fp4_debug_decode_launches(int M, int E, int H, int I, int top_k) {
-  if (M < 1 || M > MOE_FP4_DECODE_MAX_M || check_shape(E, H, I, top_k, MOE_FP4_NVFP4) != MOE_FP4_OK) return 0;
-  return decode_launches(M, E, H, I, top_k);
+  if (M < 1 || check_shape(E, H, I, top_k, MOE_FP4_NVFP4) != MOE_FP4_OK) return 0;
+  if (M <= MOE_FP4_DECODE_MAX_M) return decode_launches(M, E, H, I, top_k);
+  if (!mid_band_chunks(M, H, I)) return 0;
+  const int n = (M + MOE_FP4_DECODE_MAX_M - 1) / MOE_FP4_DECODE_MAX_M;
+  int total = 0;
+  for (int c = 0, m0 = 0; c < n; ++c) {
+    const int mc = (M - m0) / (n - c);
+    total += decode_launches(mc, E, H, I, top_k);
+    m0 += mc;
+  }
+  return total;
 }
 
 int moe_fp4_debug_dequant(const void* w, const void* s, int which, int expert, int E, int H, int I, int fmt,

@@ -63,8 +63,10 @@ typedef enum {
     MOE_FP4_EWORKSPACE = 4    /* workspace missing or too small, or >= 2^31 bytes */
 } moe_fp4_status;
 
-/* Largest token count handled by the decode band (HBM-bound GEMV kernels);
- * larger M uses the prefill band (grouped block-scaled GEMM). */
+/* Largest token count handled by one pass of the decode band (HBM-bound
+ * weight-streaming kernels).  Batches of up to twice this run as balanced
+ * chunks of the decode band when one expert's weights are at most 8 MiB;
+ * other larger batches use the prefill band (grouped block-scaled GEMM). */
 #define MOE_FP4_DECODE_MAX_M 8
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -150,12 +152,13 @@ MOE_FP4_API int moe_fp4_release_workspace(void);
  *   topk_weights [M][top_k] f32 router weights
  *   out_bf16     [M][H] bf16, fully overwritten (tokens with no valid slot
  *                get +0.0); must not overlap any input.
- * M = 0 is a no-op.  Inputs are never written.  Decode (M <= 8) results are
- * bitwise deterministic; the prefill band sums routed rows into an FP32
- * token accumulator with atomic adds, so its low-order bits may vary run to
- * run.
+ * M = 0 is a no-op.  Inputs are never written.  Decode-band results (M <=
+ * 8, and 9 <= M <= 16 with experts of at most 8 MiB of weights, which run
+ * as chunks of at most 8 tokens on the decode kernels) are bitwise
+ * deterministic; the prefill band sums routed rows into an FP32 token
+ * accumulator with atomic adds, so its low-order bits may vary run to run.
  *
- * Prefill band (M > 8): E <= 4096 (else
+ * Prefill band (M > 8, except the chunked batches above): E <= 4096 (else
  * MOE_FP4_EUNSUPPORTED).  Activations are quantised to NVFP4 per row (x per
  * token, h = SiLU(gate)*up per routed row after BF16 staging) so both GEMMs
  * run on the FP4 tensor cores.
@@ -308,10 +311,25 @@ MOE_FP4_API int moe_fp4_forward_noalloc(const void *x_bf16, const void *w13, con
  * pair's h), else 0.
  */
 MOE_FP4_API int moe_fp4_debug_set_decode_family(int family, int *previous);
+/*
+ * Test support: the kernels of batches just past the decode band
+ * (MOE_FP4_DECODE_MAX_M < M <= 3 * MOE_FP4_DECODE_MAX_M) for every later
+ * call in the process.
+ *   mode 0  by shape (default): the chunks up to 2 * MOE_FP4_DECODE_MAX_M
+ *           tokens when one expert's weights (3IH/2 nibble bytes) are at
+ *           most 8 MiB, else the prefill band
+ *   mode 1  the prefill band
+ *   mode 2  the decode-band kernels on balanced chunks of at most
+ *           MOE_FP4_DECODE_MAX_M tokens, one chunk after another
+ * Larger batches always take the prefill band.  *previous (if non-null)
+ * receives the old setting.  MOE_FP4_EINVAL for other values.
+ */
+MOE_FP4_API int moe_fp4_debug_set_mid_band(int mode, int *previous);
 MOE_FP4_API int moe_fp4_debug_decode_gemv_fits(int M, int E, int H, int I, int top_k);
 /* Kernel launches one decode-band layer of this shape makes under the
- * current family setting (2 streaming GEMV; 3, or 4 from M = 2, tcgen05);
- * 0 for shapes outside the band or invalid arguments. */
+ * current family and mid-band settings (2 streaming GEMV; 3, or 4 from
+ * M = 2, tcgen05; the sum over the chunks of a chunked batch); 0 for shapes
+ * that take the prefill band or invalid arguments. */
 MOE_FP4_API int moe_fp4_debug_decode_launches(int M, int E, int H, int I, int top_k);
 
 /*

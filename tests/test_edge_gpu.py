@@ -2,9 +2,9 @@
 
 The largest decode batch with the largest top_k, one expert taking every
 route (all of a layer's tokens in one expert: the GEMV family's 8-token path),
-the smallest H and I the boundary accepts, the first prefill batch (M = 9)
-beside the last decode one (M = 8), and routings whose slots all repeat one
-expert.  Each decode case runs on both kernel families.
+the smallest H and I the boundary accepts, the band boundaries (M = 8, the
+chunked M = 9 and 16, the first prefill batch M = 17), and routings whose
+slots all repeat one expert.  Each decode case runs on both kernel families.
 """
 import pytest
 import torch
@@ -61,12 +61,13 @@ def test_decode_edges(case, family):
     assert_layer_close(got, oracle_layer(wl), f"{case} family {family}")
 
 
-@pytest.mark.parametrize("M", [8, 9])
+@pytest.mark.parametrize("M", [8, 9, 16, 17])
 def test_band_boundary(M):
-    """The last decode batch and the first prefill batch of one geometry."""
+    """The last decode batch, the chunked batches past it (9..16 tokens: this
+    geometry's experts are small) and the first prefill batch (17)."""
     wl = gen.make_workload("decode_e512", device="cuda", E=32, M=M)
     got = _run(wl)
-    if M <= 8:
+    if M <= 16:
         want = oracle_layer(wl)
     else:  # the prefill band quantises the activations; the oracle mirrors it
         import oracle

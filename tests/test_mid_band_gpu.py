@@ -1,0 +1,76 @@
+"""Batches just past the decode band (MOE_FP4_DECODE_MAX_M < M <= 3x that).
+
+They run either on the prefill band or on the decode-band kernels over
+balanced chunks of at most MOE_FP4_DECODE_MAX_M tokens.  The chunked path
+keeps the decode band's numerics (BF16 activations, no activation
+quantisation), so it is held to the unquantised FP64 oracle, and it must be
+bitwise the concatenation of the chunks run as separate decode calls.  The
+prefill path is held to the oracle that mirrors its activation quantisation.
+"""
+import pytest
+import torch
+
+import oracle
+from tests.gpu_util import assert_layer_close, ensure_built, oracle_layer
+from workload import gen
+
+pytestmark = pytest.mark.gpu
+
+PREFILL, CHUNKS = 1, 2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    ensure_built()
+
+
+def _run(wl, mode, ids=None, tw=None, x=None):
+    import fp4_weight_moe_gb300 as m
+    from fp4_weight_moe_gb300 import _capi
+    pw = m.prepare_weights(wl.weights, wl.E, wl.H, wl.I, wl.fmt)
+    xx = wl.x if x is None else x
+    M = xx.shape[0]
+    ws = m.alloc_workspace(max(M, 1), wl.E, wl.H, wl.I, wl.top_k, wl.fmt)
+    out = torch.full((M, wl.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    prev = _capi.moe_fp4_debug_set_mid_band(mode)
+    try:
+        m.forward(xx, pw, wl.topk_ids if ids is None else ids, wl.topk_weights if tw is None else tw, out=out,
+                  workspace=ws)
+        torch.cuda.synchronize()
+    finally:
+        _capi.moe_fp4_debug_set_mid_band(prev)
+    return out
+
+
+@pytest.mark.parametrize("name,ov", [("decode_e512", dict(E=48, M=9)), ("decode_e512", dict(E=64, M=16)),
+                                     ("decode_e288_m4", dict(E=40, M=13)), ("tiny_decode", dict(M=24, E=10,
+                                                                                               top_k=3))])
+def test_chunked_mid_band_parity(name, ov):
+    wl = gen.make_workload(name, device="cuda", **ov)
+    got = _run(wl, CHUNKS)
+    assert_layer_close(got, oracle_layer(wl), f"{name} {ov} chunked")
+
+
+def test_chunks_equal_separate_decode_calls():
+    wl = gen.make_workload("decode_e512", device="cuda", E=40, M=11)
+    whole = _run(wl, CHUNKS)
+    # balanced chunks of 11 tokens: 5 + 6
+    parts = [_run(wl, CHUNKS, ids=wl.topk_ids[a:b].contiguous(), tw=wl.topk_weights[a:b].contiguous(),
+                  x=wl.x[a:b].contiguous()) for a, b in ((0, 5), (5, 11))]
+    assert torch.equal(whole.view(torch.int16), torch.cat(parts).view(torch.int16))
+
+
+@pytest.mark.parametrize("M", [9, 16])
+def test_mid_band_prefill_mode(M):
+    wl = gen.make_workload("decode_e512", device="cuda", E=32, M=M)
+    got = _run(wl, PREFILL)
+    want, _, _, _ = oracle.forward_prefill(wl.x, wl.weights, wl.topk_ids, wl.topk_weights, wl.E, wl.H, wl.I,
+                                           wl.top_k, fmt=wl.fmt)
+    assert_layer_close(got, want, f"decode_e512 M={M} prefill band")
+
+
+def test_int64_ids_through_chunks():
+    wl = gen.make_workload("decode_e512", device="cuda", E=48, M=12)
+    a = _run(wl, CHUNKS)
+    b = _run(wl, CHUNKS, ids=wl.topk_ids.long())
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))

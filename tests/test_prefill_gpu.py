@@ -23,7 +23,13 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(scope="module", autouse=True)
 def _build():
+    """Build, and send every batch past the decode band to the prefill band
+    (small ones would otherwise run as chunks of the decode band)."""
     ensure_built()
+    from fp4_weight_moe_gb300 import _capi as c
+    prev = c.moe_fp4_debug_set_mid_band(1)
+    yield
+    c.moe_fp4_debug_set_mid_band(prev)
 
 
 def fm():
