@@ -77,6 +77,17 @@ def test_quant_rows_bit_exact():
     a[5] = (np.float32(1e-30) * rng.standard_normal(K)).astype(np.float32)  # tiny row
     a[6, ::7] = np.float32(5.0)                           # exact ties after scaling
     a[7] = np.round(a[7] * 4) / 4
+    # G = 1 (row max 2688) and a block with block max 6 (scale 1): the
+    # quotients are the values themselves, placed on every E2M1 rounding
+    # midpoint and one unit in the last place to either side of it
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], dtype=np.float32)
+    a[8] = 0.0
+    a[8, 0] = 2688.0
+    a[8, 16:32] = np.concatenate([[6.0], mids, -mids, [-6.0]])
+    a[8, 32:48] = np.concatenate([[6.0], np.nextafter(mids, np.float32(np.inf)),
+                                  -np.nextafter(mids, np.float32(0)), [0.0]])
+    a[8, 48:64] = np.concatenate([[6.0], np.nextafter(mids, np.float32(0)),
+                                  -np.nextafter(mids, np.float32(np.inf)), [-0.0]])
     c = _capi()
     dev = torch.device("cuda")
     ta = torch.from_numpy(a).to(dev)
