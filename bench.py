@@ -228,12 +228,16 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ GPU arm
 def decode_src_sha256():
-    """Hash of the decode kernels' sources: a stored ncu traffic figure is used
-    only while the kernels it was measured on are unchanged."""
+    """Hash of the decode kernels' code: a stored ncu traffic figure is used
+    only while the kernels it was measured on are unchanged.  Line comments
+    and blank lines are left out (they do not change the kernels)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in ("common.cuh", "tcgen05.cuh", "decode_tc.cu", "decode.cu"):
-        h.update(open(os.path.join(ROOT, "fp4_weight_moe_gb300", "csrc", f), "rb").read())
+        text = open(os.path.join(ROOT, "fp4_weight_moe_gb300", "csrc", f)).read()
+        code = [re.sub(r"\s*//.*$", "", ln).rstrip() for ln in text.splitlines()]
+        h.update("\n".join(ln for ln in code if ln).encode())
     return h.hexdigest()
 
 

@@ -40,8 +40,9 @@
 //      items); the CTAs of one tile form a cluster and reduce the same way;
 //      each output element is written once, in BF16.  Both kernels use
 //      programmatic dependent launch: FC1's prologue overlaps the previous
-//      kernel, FC2's weight stream overlaps FC1 (at most one CTA of each per
-//      SM, so they fit side by side); only the warps that read h wait for FC1.
+//      kernel, and FC2's CTAs that find room beside FC1's (at most two CTAs
+//      per SM) start streaming their weights before FC1 is done; only the
+//      warps that read h wait for FC1.
 //
 // The tensor cores issue an MMA about every hundred cycles however small N
 // is, so with N = 16 the issue, not the arithmetic, sets the pace: the MMAs
