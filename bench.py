@@ -241,6 +241,16 @@ def decode_src_sha256():
     return h.hexdigest()
 
 
+def decode_kernel_label(m, M, E, H, I, k):
+    """What one decode layer of this shape launches (for the JSON line)."""
+    c = m._capi
+    if M <= m.MOE_FP4_DECODE_MAX_M and c.moe_fp4_debug_decode_family_of(M, E, H, I, k) == 1:
+        return "decode layer: streaming-GEMV FC1 + FC2 (PDL-chained)"
+    head = "decode layer" if M <= m.MOE_FP4_DECODE_MAX_M else \
+        f"decode layer in {-(-M // m.MOE_FP4_DECODE_MAX_M)} chunks"
+    return f"{head}: x pre-pass + FC1 + " + ("" if M < 2 else "h pre-pass + ") + "FC2 (tcgen05, PDL-chained)"
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -372,12 +382,7 @@ def run_ours(args):
         "routed_bytes_per_layer": step_bytes / K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"hbm_gbs of {peak_kind}", "traffic": traffic,
-                     "kernel": ("decode layer: streaming-GEMV FC1 + FC2 (PDL-chained)"
-                              if m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) == 2 else
-                              ("decode layer" if M <= m.MOE_FP4_DECODE_MAX_M else
-                               f"decode layer in {-(-M // m.MOE_FP4_DECODE_MAX_M)} chunks")
-                              + ": x pre-pass + FC1 + " + ("" if M < 2 else "h pre-pass + ")
-                              + "FC2 (tcgen05, PDL-chained)")},
+                     "kernel": decode_kernel_label(m, M, E, H, I, k)},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": M * H * 2 + M * k * 8,
                 "d2h_bytes_per_step": M * H * 2, "us_per_layer": e2e_ms * 1e3 / K},
         "gpu_launches": m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) * K,

@@ -63,6 +63,7 @@ SIGNATURES = {
     "moe_fp4_debug_set_mid_band": (_I, [_I, ctypes.POINTER(ctypes.c_int)]),
     "moe_fp4_debug_decode_gemv_fits": (_I, [_I, _I, _I, _I, _I]),
     "moe_fp4_debug_decode_launches": (_I, [_I, _I, _I, _I, _I]),
+    "moe_fp4_debug_decode_family_of": (_I, [_I, _I, _I, _I, _I]),
     "moe_fp4_debug_dequant": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "moe_fp4_debug_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_fp4_debug_route": (_I, [_P, _I, _I, _I, _P, _P, _P, _Z, _P]),
@@ -203,6 +204,10 @@ def moe_fp4_debug_set_mid_band(mode: int) -> int:
 
 def moe_fp4_debug_decode_gemv_fits(M, E, H, I, top_k) -> bool:
     return bool(_load().moe_fp4_debug_decode_gemv_fits(M, E, H, I, top_k))
+
+
+def moe_fp4_debug_decode_family_of(M, E, H, I, top_k) -> int:
+    return int(_load().moe_fp4_debug_decode_family_of(M, E, H, I, top_k))
 
 
 def moe_fp4_debug_decode_launches(M, E, H, I, top_k) -> int:

@@ -27,6 +27,7 @@ cudaError_t launch_debug_quant(const float* in, int rows, int K, uint8_t* q, uin
 extern std::atomic<int> g_decode_family;
 bool decode_gemv_fits(int M, int E, int H, int I, int top_k);
 int decode_launches(int M, int E, int H, int I, int top_k);
+int decode_family_of(int M, int E, int H, int I, int top_k);
 cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                           const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
                           int top_k, int fmt, const ActParams& act, void* ws, int num_sms, cudaStream_t st);
@@ -475,6 +476,11 @@ int moe_fp4_debug_set_mid_band(int mode, int* previous) {
   const int old = g_mid_band.exchange(mode);
   if (previous) *previous = old;
   return MOE_FP4_OK;
+}
+
+int moe_fp4_debug_decode_family_of(int M, int E, int H, int I, int top_k) {
+  if (M < 1 || M > MOE_FP4_DECODE_MAX_M || check_shape(E, H, I, top_k, MOE_FP4_NVFP4) != MOE_FP4_OK) return 0;
+  return decode_family_of(M, E, H, I, top_k);
 }
 
 int moe_fp4_debug_decode_gemv_fits(int M, int E, int H, int I, int top_k) {

@@ -54,10 +54,16 @@ size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int fmt, int n
 }
 
 // Kernel launches of one decode-band layer under the current family setting.
-int decode_launches(int M, int E, int H, int I, int top_k) {
+// The family the current setting picks for a decode-band shape: 1 streaming
+// GEMV, 2 tcgen05.
+int decode_family_of(int M, int E, int H, int I, int top_k) {
   const int family = g_decode_family.load(std::memory_order_relaxed);
   const bool fits = decode_gemv_fits(M, E, H, I, top_k);
-  if (family == 1 ? fits : family == 0 && fits && gemv_preferred(M, H, I, top_k)) return 2;
+  return (family == 1 ? fits : family == 0 && fits && gemv_preferred(M, H, I, top_k)) ? 1 : 2;
+}
+
+int decode_launches(int M, int E, int H, int I, int top_k) {
+  if (decode_family_of(M, E, H, I, top_k) == 1) return 2;
   return M >= 2 ? 4 : 3;  // x pre-pass, FC1, (h pre-pass,) FC2
 }
 

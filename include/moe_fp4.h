@@ -326,6 +326,10 @@ MOE_FP4_API int moe_fp4_debug_set_decode_family(int family, int *previous);
  */
 MOE_FP4_API int moe_fp4_debug_set_mid_band(int mode, int *previous);
 MOE_FP4_API int moe_fp4_debug_decode_gemv_fits(int M, int E, int H, int I, int top_k);
+/* The family the current setting picks for a decode-band shape (1 streaming
+ * GEMV, 2 tcgen05); 0 for M outside 1..MOE_FP4_DECODE_MAX_M or invalid
+ * arguments. */
+MOE_FP4_API int moe_fp4_debug_decode_family_of(int M, int E, int H, int I, int top_k);
 /* Kernel launches one decode-band layer of this shape makes under the
  * current family and mid-band settings (2 streaming GEMV; 3, or 4 from
  * M = 2, tcgen05; the sum over the chunks of a chunked batch); 0 for shapes
