@@ -320,10 +320,12 @@ __global__ void __launch_bounds__(256) decode_quant_h_kernel(TcArgs a) {
   for (int k = threadIdx.x; k < a.n_slots; k += blockDim.x) s_ids[k] = route_id(a.ids, k, a.ids64, a.E);
   __syncthreads();
   const int e = s_ids[j];
-  if (e < 0 || e >= a.E) return;
-  for (int k = 0; k < j; ++k)
-    if (s_ids[k] == e) return;  // an earlier slot owns this expert
+  bool skip = e < 0 || e >= a.E;
+  for (int k = 0; !skip && k < j; ++k) skip = s_ids[k] == e;  // an earlier slot owns this expert
+  // every CTA waits, the ones with nothing to do too: FC2 takes this grid's
+  // completion for FC1's
   pdl_wait();  // FC1's h is complete
+  if (skip) return;
   if (token >= a.M) return;
   const int rem = a.I / 64 - 4 * st;
   const bool act = lane < 8 * (rem < 4 ? rem : 4);
@@ -502,6 +504,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   if (!kFc2) {
     e1 = S.expert;
     if (e1 < 0) {  // an earlier slot names this expert: the whole cluster leaves
+      // (not before the x pre-pass is complete: FC2 and the next layer take
+      // FC1's completion for the pre-pass's, and a layer whose slots all
+      // leave here would otherwise let them run beside a pre-pass still
+      // writing its images)
+      pdl_wait();
       if (warp == kMmaWarp0) tmem_dealloc(S.tmem, kTmemColsTc);
       return;
     }
