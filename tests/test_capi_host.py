@@ -121,3 +121,31 @@ def test_forward_ex_i64_argument_errors(lib):
     assert st(ids=0) == _capi.MOE_FP4_EINVAL
     assert st(H=384) == _capi.MOE_FP4_EUNSUPPORTED
     assert st(M=0) == _capi.MOE_FP4_OK
+
+
+def test_band_policy_by_shape(lib):
+    """Which kernels a batch takes (host logic only): the decode band up to 8
+    tokens (streaming GEMV for one token with few routed bytes, else tcgen05
+    with 3 launches, 4 from two tokens), 9-16 tokens with experts of at most
+    8 MiB as balanced chunks of the decode kernels, everything else the
+    prefill band (0 decode launches); the test knobs force either path."""
+    c = _capi
+    e512 = (512, 2560, 320, 10)     # 1.38 MB experts
+    e256 = (256, 7168, 2048, 8)     # 22 MB experts
+    tiny = (8, 256, 128, 2)
+    assert c.moe_fp4_debug_decode_family_of(1, *tiny) == 1
+    assert c.moe_fp4_debug_decode_launches(1, *tiny) == 2
+    assert c.moe_fp4_debug_decode_family_of(1, *e512) == 2
+    assert [c.moe_fp4_debug_decode_launches(M, *e512) for M in (1, 2, 8)] == [3, 4, 4]
+    assert [c.moe_fp4_debug_decode_launches(M, *e512) for M in (9, 12, 16, 17, 24)] == [8, 8, 8, 0, 0]
+    assert [c.moe_fp4_debug_decode_launches(M, *e256) for M in (8, 9, 16)] == [4, 0, 0]
+    assert c.moe_fp4_debug_decode_family_of(9, *e512) == 0
+    prev = c.moe_fp4_debug_set_mid_band(2)
+    try:
+        assert [c.moe_fp4_debug_decode_launches(M, *e256) for M in (9, 17, 24, 25)] == [8, 12, 12, 0]
+        c.moe_fp4_debug_set_mid_band(1)
+        assert c.moe_fp4_debug_decode_launches(9, *e512) == 0
+    finally:
+        c.moe_fp4_debug_set_mid_band(prev)
+    with pytest.raises(c.MoeFp4Error):
+        c.moe_fp4_debug_set_mid_band(3)
