@@ -101,6 +101,10 @@ def _bind(lib):
     lib.moe_oracle_fc1.argtypes = [P, P, P, P, i, i, i, i, P, P]
     lib.moe_oracle_quant_nvfp4_row.restype = None
     lib.moe_oracle_quant_nvfp4_row.argtypes = [P, i, P, P, P]
+    lib.moe_oracle_quant_mxfp8_row.restype = None
+    lib.moe_oracle_quant_mxfp8_row.argtypes = [P, i, P, P]
+    lib.moe_oracle_forward_w4a8_act.restype = i
+    lib.moe_oracle_forward_w4a8_act.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, P, i, P, i, i, d, d, d]
     lib.moe_oracle_route.restype = i
     lib.moe_oracle_route.argtypes = [P, i, i, i, P, P]
     lib.moe_oracle_num_threads.restype = i
@@ -245,6 +249,36 @@ def quant_nvfp4_row(a) -> tuple:
     g = np.zeros(1, dtype=np.float32)
     _load().moe_oracle_quant_nvfp4_row(_ptr(a), K, _ptr(q), _ptr(s), _ptr(g))
     return q, s, float(g[0])
+
+
+def quant_mxfp8_row(a) -> tuple:
+    """FP32 row -> (E4M3 bytes [K], UE8M0 scale bytes [K/32])."""
+    a = _np(a, np.float32).reshape(-1)
+    K = a.shape[0]
+    q = np.zeros(K, dtype=np.uint8)
+    s = np.zeros(K // 32, dtype=np.uint8)
+    _load().moe_oracle_quant_mxfp8_row(_ptr(a), K, _ptr(q), _ptr(s))
+    return q, s
+
+
+def forward_w4a8(x_bf16, weights: dict, topk_ids, topk_weights, E: int, H: int, I: int, top_k: int,
+                 tokens: Optional[Sequence[int]] = None, nthreads: int = 0, act=None):
+    """W4A8-MX definition (MXFP4 weights, MXFP8 activations, mirrored):
+    returns out ``[n_tok][H]`` FP64."""
+    x = _np(x_bf16, np.uint16)
+    M = x.shape[0]
+    w13, s13, _, w2, s2, _ = _weights_np(weights, MXFP4)
+    ids = _np(topk_ids, np.int32)
+    tw = _np(topk_weights, np.float32)
+    tok = None if tokens is None else np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    n_tok = M if tok is None else len(tok)
+    out = np.full((n_tok, H), np.nan, dtype=np.float64)  # poisoned: the oracle must overwrite
+    a = _act_args(act) or (ACT_SILU, 0.0, 0.0, 0.0)
+    rc = _load().moe_oracle_forward_w4a8_act(_ptr(x), _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2), _ptr(ids), _ptr(tw),
+                                             M, E, H, I, top_k, _ptr(tok), n_tok, _ptr(out), nthreads, *a)
+    if rc != 0:
+        raise ValueError("oracle rejected the shapes")
+    return out
 
 
 def route(topk_ids, E: int):

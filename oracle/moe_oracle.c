@@ -29,6 +29,8 @@
  *     FP32 row multiplier, then the same FP64 layer from the dequantised
  *     values (flashinfer PR #4285: W4A4 NVFP4 prefill with a fast FP4
  *     quantiser restricted to gated activations).
+ *   - W4A8-MX mirror: MXFP4 weights with activations quantised to MXFP8
+ *     (E4M3 elements, a UE8M0 scale per 32), then the same FP64 layer.
  *
  * Build: plain C99, -O2 -fno-fast-math -ffp-contract=off, optional OpenMP.
  */
@@ -454,6 +456,118 @@ int moe_oracle_forward_prefill(const uint16_t *x_bf16, const uint8_t *w13, const
     return moe_oracle_forward_prefill_act(x_bf16, w13, s13, g13, w2, s2, g2, topk_ids, topk_w, M, E, H, I, top_k,
                                           fmt, tokens, n_tok, out, xq_out, xs_out, xg_out, nthreads,
                                           ORACLE_ACT_SILU, 0.0, 0.0, 0.0);
+}
+
+/* ------------------------------------------- W4A8-MX activations (MXFP8) */
+
+/*
+ * MXFP8 quantiser of one row a[K] (K % 32 == 0): E4M3 elements with one
+ * UE8M0 scale per 32 K-elements, the activation format of the W4A8-MX
+ * variant (b12x PR #22, "rp-native tiny-decode kernel for w4a8_mx (M=1)":
+ * MXFP8 activations on the prefill side; flashinfer PR #4285:
+ * scale_format_e8m0_k32).  The pages do not print the rule; the reading
+ * follows the MX weight recipe of the synthetic checkpoints with E4M3's
+ * largest finite value 448 in place of E2M1's 6:
+ *   per 32-block:  e = ceil(log2(amax_blk / 448))  (e = 0 if amax_blk == 0),
+ *                  clamped to [-127, 127]; scale byte e + 127
+ *   per element:   q = e4m3_rn(a / 2^e), |a / 2^e| <= 448 by construction
+ * The sign survives rounding (a small negative value gives -0, byte 0x80).
+ * q[K] E4M3 bytes, s[K/32] UE8M0 bytes.
+ */
+void moe_oracle_quant_mxfp8_row(const float *a, int K, uint8_t *q, uint8_t *s)
+{
+    for (int b = 0; b < K / 32; ++b) {
+        double amax = 0.0;
+        for (int k = 0; k < 32; ++k) {
+            double v = fabs((double)a[b * 32 + k]);
+            if (v > amax) amax = v;
+        }
+        int e = 0;
+        if (amax > 0.0) {
+            int ex;
+            double m = frexp(amax / 448.0, &ex); /* amax/448 = m * 2^ex, m in [0.5, 1) */
+            e = (m == 0.5) ? ex - 1 : ex;         /* ceil(log2(amax/448)) */
+        }
+        if (e < -127) e = -127;
+        if (e > 127) e = 127;
+        s[b] = (uint8_t)(e + 127);
+        double scale = ldexp(1.0, e);
+        for (int k = 0; k < 32; ++k) {
+            float v = a[b * 32 + k];
+            float r = (float)((double)v / scale); /* a power-of-two division: exact unless it underflows */
+            uint8_t c = e4m3_from_float_pos(fabsf(r));
+            if (signbit(v)) c |= 0x80;
+            q[b * 32 + k] = c;
+        }
+    }
+}
+
+/* Dequantise an MXFP8 row back to FP64: e4m3(q) * 2^(s - 127). */
+static void dequant_mxfp8_row(const uint8_t *q, const uint8_t *s, int K, double *out)
+{
+    for (int k = 0; k < K; ++k) {
+        double v = moe_oracle_e4m3(q[k] & 0x7F);
+        if (q[k] & 0x80) v = -v;
+        out[k] = v * ldexp(1.0, (int)s[k / 32] - 127);
+    }
+}
+
+/* W4A8-MX layer (MXFP4 weights, MXFP8 activations, mirrored), for the
+ * tokens listed (NULL = all):
+ *   x_q = mxfp8(x_t); for each valid slot: g,u = FC1(dequant(x_q)) in FP64;
+ *   h = act(g, u) rounded to FP32, then to BF16 (staged like the NVFP4
+ *   prefill band's h); h_q = mxfp8(h); y = FC2(dequant(h_q));
+ *   out_t = sum_j w_j y.                                                    */
+int moe_oracle_forward_w4a8_act(const uint16_t *x_bf16, const uint8_t *w13, const uint8_t *s13,
+                                const uint8_t *w2, const uint8_t *s2, const int32_t *topk_ids, const float *topk_w,
+                                int M, int E, int H, int I, int top_k, const int32_t *tokens, int n_tok,
+                                double *out, int nthreads, int act_kind, double alpha, double beta, double limit)
+{
+    oracle_act act = {act_kind, alpha, beta, limit};
+    if (act_kind < ORACLE_ACT_SILU || act_kind > ORACLE_ACT_SWIGLUOAI) return 1;
+    if (H % 32 || I % 32) return 1;
+    if (!tokens) n_tok = M;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel
+#endif
+    {
+        float *xf = (float *)malloc(sizeof(float) * (size_t)H);
+        uint8_t *xq = (uint8_t *)malloc((size_t)H);
+        uint8_t *xs = (uint8_t *)malloc((size_t)H / 32);
+        double *xd = (double *)malloc(sizeof(double) * (size_t)H);
+        double *h = (double *)malloc(sizeof(double) * (size_t)I);
+        float *hf = (float *)malloc(sizeof(float) * (size_t)I);
+        uint8_t *hq = (uint8_t *)malloc((size_t)I);
+        uint8_t *hs = (uint8_t *)malloc((size_t)I / 32);
+        double *hd = (double *)malloc(sizeof(double) * (size_t)I);
+        double *y = (double *)malloc(sizeof(double) * (size_t)H);
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int i = 0; i < n_tok; ++i) {
+            int t = tokens ? tokens[i] : i;
+            for (int k = 0; k < H; ++k) xf[k] = (float)bf16_to_double(x_bf16[(size_t)t * H + k]);
+            moe_oracle_quant_mxfp8_row(xf, H, xq, xs);
+            dequant_mxfp8_row(xq, xs, H, xd);
+            double *o = out + (size_t)i * H;
+            for (int m = 0; m < H; ++m) o[m] = 0.0;
+            for (int j = 0; j < top_k; ++j) {
+                int e = topk_ids[(size_t)t * top_k + j];
+                if (e < 0 || e >= E) continue;
+                expert_fc1(xd, w13, s13, NULL, e, H, I, ORACLE_MXFP4, &act, h);
+                for (int n = 0; n < I; ++n) hf[n] = bf16_round((float)h[n]);
+                moe_oracle_quant_mxfp8_row(hf, I, hq, hs);
+                dequant_mxfp8_row(hq, hs, I, hd);
+                expert_fc2(hd, w2, s2, NULL, e, H, I, ORACLE_MXFP4, y);
+                double w = (double)topk_w[(size_t)t * top_k + j];
+                for (int m = 0; m < H; ++m) o[m] += w * y[m];
+            }
+        }
+        free(xf); free(xq); free(xs); free(xd); free(h); free(hf); free(hq); free(hs); free(hd); free(y);
+    }
+    (void)nthreads;
+    return 0;
 }
 
 /* ------------------------------------------------- routing / compaction */

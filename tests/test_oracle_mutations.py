@@ -56,6 +56,13 @@ MUTATIONS = {
                                 "double u = up;"),
     "swiglu_alpha_outside": ("return (u + a->beta) * g / (1.0 + exp(-a->alpha * g));",
                              "return a->alpha * (u + a->beta) * g / (1.0 + exp(-g));"),
+    "mxfp8_scale_floor": ("e = (m == 0.5) ? ex - 1 : ex;         /* ceil(log2(amax/448)) */",
+                          "e = ex - 1;"),
+    "mxfp8_scale_bias": ("s[b] = (uint8_t)(e + 127);\n        double scale = ldexp(1.0, e);",
+                         "s[b] = (uint8_t)(e + 128);\n        double scale = ldexp(1.0, e);"),
+    "mxfp8_sign_dropped": ("if (signbit(v)) c |= 0x80;", "if (v < 0.0f && c != 0) c |= 0x80;"),
+    "mxfp8_h_unquantised": ("moe_oracle_quant_mxfp8_row(hf, I, hq, hs);\n                dequant_mxfp8_row(hq, hs, I, hd);",
+                            "moe_oracle_quant_mxfp8_row(hf, I, hq, hs);\n                for (int n = 0; n < I; ++n) hd[n] = h[n];"),
     "route_order": ("for (int t = 0; t < M; ++t)\n            for (int j = 0; j < top_k; ++j)\n                if (topk_ids[(size_t)t * top_k + j] == e) perm[r++] = t * top_k + j;",
                     "for (int j = 0; j < top_k; ++j)\n            for (int t = 0; t < M; ++t)\n                if (topk_ids[(size_t)t * top_k + j] == e) perm[r++] = t * top_k + j;"),
 }
@@ -82,6 +89,10 @@ def _run_pins():
         ("swiglu_reductions", lambda: pins.test_swigluoai_reductions(_small_case())),
         ("swiglu_relu", lambda: pins.test_swigluoai_large_alpha_is_relu_gated(0)),
         ("swiglu_clamps", pins.test_swigluoai_hand_worked_clamps),
+        ("mxfp8_library", pins.test_mxfp8_quantiser_matches_library),
+        ("mxfp8_grid", pins.test_mxfp8_exact_on_grid),
+        ("w4a8_golden", pins.test_w4a8_hand_worked_layer),
+        ("w4a8_invariants", pins.test_w4a8_invariants_and_accuracy),
     ]
     for case in pins._golden_cases():
         checks.append(("golden_" + case["name"], lambda c=case: pins.test_hand_worked_layers(c)))

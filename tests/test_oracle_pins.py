@@ -481,3 +481,94 @@ def test_swigluoai_hand_worked_clamps():
                              act=(oracle.ACT_SWIGLUOAI, alpha, beta, 2.0))
         h = (2.0 + beta) * 2.0 / (1.0 + math.exp(-2.0 * alpha))
         np.testing.assert_allclose(out, np.full((1, H), h), rtol=1e-13, atol=0)
+
+
+# ------------------------------------------------ W4A8-MX (MXFP8 activations)
+def _ceil_log2_ratio(amax: float, top: float) -> int:
+    m, ex = math.frexp(amax / top)
+    return ex - 1 if m == 0.5 else ex
+
+
+def test_mxfp8_quantiser_matches_library():
+    """Per 32-block: scale byte 127 + ceil(log2(amax/448)) (closed form with
+    Python's math), elements = torch's float8_e4m3fn conversion (a library
+    round-to-nearest-even) of a / scale; all-zero blocks: byte 127, zeros;
+    -0.0 keeps its sign."""
+    rng = np.random.default_rng(31)
+    a = (rng.standard_normal(512) * np.exp(rng.uniform(-20, 20, 512))).astype(np.float32)
+    a[64:96] = 0.0
+    a[96:128] = 0.0
+    a[100] = np.float32(-0.0)
+    a[128:160] = np.float32(448.0 * 2.0 ** -30) * np.linspace(-1, 1, 32, dtype=np.float32)
+    q, s = oracle.quant_mxfp8_row(a)
+    for b in range(len(a) // 32):
+        blk = a[32 * b:32 * (b + 1)].astype(np.float64)
+        amax = float(np.abs(blk).max())
+        e = 0 if amax == 0 else _ceil_log2_ratio(amax, 448.0)
+        assert s[b] == e + 127, b
+        want = torch.tensor((blk / 2.0 ** e).astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(q[32 * b:32 * (b + 1)], want), b
+    assert q[100] == 0x80 and q[101] == 0x00
+
+
+def test_mxfp8_exact_on_grid():
+    """Values on the E4M3 grid times 2^j, with 448 * 2^j in the block, come
+    back exactly; a block max one ulp above 448 * 2^j takes the next scale."""
+    codes = np.arange(0, 0x7F, dtype=np.uint8)
+    grid = np.array([oracle.e4m3(int(c)) for c in codes], np.float64)
+    for j in (-12, 0, 5):
+        blk = np.zeros(32, np.float64)
+        blk[:31] = grid[np.linspace(0, len(grid) - 1, 31).astype(int)] * 2.0 ** j
+        blk[31] = 448.0 * 2.0 ** j
+        blk[::3] *= -1
+        q, s = oracle.quant_mxfp8_row(blk.astype(np.float32))
+        assert s[0] == 127 + j
+        back = np.array([(-1 if c & 0x80 else 1) * oracle.e4m3(int(c) & 0x7F) for c in q]) * 2.0 ** (int(s[0]) - 127)
+        np.testing.assert_array_equal(back, blk)
+        up = blk.astype(np.float32)
+        up[31] = np.nextafter(np.float32(448.0 * 2.0 ** j), np.float32(np.inf))
+        assert oracle.quant_mxfp8_row(up)[1][0] == 128 + j
+
+
+def test_w4a8_hand_worked_layer():
+    """The MX hand-worked layer (x = 1, gate 1.0, up 0.5, down 2^-5): x, h = 512
+    (after FP32 and BF16 rounding) and y are all exact in MXFP8, so the
+    W4A8-MX layer returns 512 exactly."""
+    case = [c for c in _golden_cases() if c["fmt"] == 0][0]
+    E, H, I = case["E"], case["H"], case["I"]
+    x = torch.full((1, H), case["x_fill"], dtype=torch.bfloat16)
+    out = oracle.forward_w4a8(x, _golden_weights(case), np.array(case["ids"], np.int32),
+                              np.array(case["weights"], np.float32), E, H, I, case["top_k"])
+    np.testing.assert_array_equal(out, np.full((1, H), 512.0))
+
+
+def test_w4a8_invariants_and_accuracy():
+    """Invalid slots contribute zero, router weights scale linearly, and the
+    MXFP8 activations stay within their precision of the unquantised layer."""
+    E, H, I, M, k = 5, 64, 64, 3, 3
+    w = _tiny_weights(E, H, I, gen.MXFP4, seed=41)
+    x = gen.draw_activations(M, H, seed=42)
+    ids = np.array([[0, 3, 1], [2, 4, 4], [1, 0, 2]], np.int32)
+    tw = np.random.default_rng(43).uniform(0.1, 1.0, (M, k)).astype(np.float32)
+    base = oracle.forward_w4a8(x, w, ids, tw, E, H, I, k)
+    ids_bad = ids.copy()
+    ids_bad[0, 1] = -1
+    ids_bad[2, 2] = E
+    cut = oracle.forward_w4a8(x, w, ids_bad, tw, E, H, I, k)
+    tw_cut = tw.copy()
+    tw_cut[0, 1] = 0.0
+    tw_cut[2, 2] = 0.0
+    np.testing.assert_allclose(cut, oracle.forward_w4a8(x, w, ids, tw_cut, E, H, I, k), rtol=0, atol=0)
+    np.testing.assert_allclose(oracle.forward_w4a8(x, w, ids, 2 * tw, E, H, I, k), 2 * base, rtol=1e-13)
+    ref = oracle.forward(x, w, ids, tw, E, H, I, k, gen.MXFP4)
+
+    def cos(u):
+        return float(np.dot(u.ravel(), ref.ravel()) / (np.linalg.norm(u) * np.linalg.norm(ref)))
+
+    # the pages measure cosine 0.9990 for MXFP8 activations on a model layer
+    # (b12x PR #22, Measured); 8-bit activations must also beat the 4-bit
+    # NVFP4 activations of the prefill mirror on the same layer
+    nv4, _, _, _ = oracle.forward_prefill(x, w, ids, tw, E, H, I, k, fmt=gen.MXFP4)
+    assert cos(base) > 0.998 and not np.array_equal(base, ref)
+    assert cos(base) > cos(nv4)
+    assert np.abs(base - ref).max() < np.abs(nv4 - ref).max()
