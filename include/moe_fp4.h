@@ -259,8 +259,9 @@ MOE_FP4_API int moe_fp4_forward_ex(const void *x_bf16, const void *w13, const vo
  * truncated into a valid expert).  Same arguments, workspace, results and
  * errors as moe_fp4_forward_ex otherwise, plus MOE_FP4_EINVAL for a
  * topk_ids pointer that is not 8-byte aligned.  For ids that are all in
- * [-2^31, 2^31) the output is bitwise that of moe_fp4_forward_ex on the same
- * ids as int32.
+ * [-2^31, 2^31) the result is that of moe_fp4_forward_ex on the same ids as
+ * int32: bitwise on the decode kernels, which are deterministic, and up to
+ * the prefill band's run-to-run summation order there.
  */
 MOE_FP4_API int moe_fp4_forward_ex_i64(const void *x_bf16, const void *w13, const void *s13, const void *w2,
                                        const void *s2, const int64_t *topk_ids, const float *topk_weights,
