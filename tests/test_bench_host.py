@@ -1,0 +1,65 @@
+"""Host-side pieces of bench.py, on CPU.
+
+The reported metric's units (routed-weight bytes and FLOPs per layer), the
+key that ties a stored ncu traffic figure to the decode kernels' code (line
+comments do not count, code does), and the stored traffic file's shape.
+"""
+import json
+import os
+import shutil
+import sys
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from workload import gen  # noqa: E402
+
+
+def test_layer_bytes_count_unique_valid_experts_once():
+    ids = torch.tensor([[3, 7, -1], [7, 9, 12]], dtype=torch.int32)  # 12 is invalid for E = 12
+    E, H, I, M, k = 12, 512, 256, 2, 3
+    b, uniq = bench.layer_bytes(ids, E, H, I, M, k, gen.NVFP4)
+    assert uniq == 3  # experts 3, 7, 9
+    assert b == 3 * gen.expert_bytes(H, I, gen.NVFP4) + M * H * 2 * 2 + M * k * 8
+
+
+def test_layer_flops_count_valid_routed_rows():
+    ids = torch.tensor([[0, 1], [1, -1], [5, 2]], dtype=torch.int32)
+    assert bench.layer_flops(ids, 5, 256, 128) == 2 * 3 * 256 * 128 * 4
+
+
+def test_traffic_key_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    csrc = tmp_path / "fp4_weight_moe_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in ("common.cuh", "tcgen05.cuh", "decode_tc.cu", "decode.cu"):
+        shutil.copy(os.path.join(ROOT, "fp4_weight_moe_gb300", "csrc", f), csrc / f)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    base = bench.decode_src_sha256()
+    assert base == bench.decode_src_sha256()
+    p = csrc / "decode_tc.cu"
+    text = p.read_text()
+    p.write_text("// a new comment line\n\n" + text.replace("\n", "  // trailing note\n", 1))
+    assert bench.decode_src_sha256() == base
+    p.write_text(text.replace("constexpr int kRing = 4;", "constexpr int kRing = 3;"))
+    assert bench.decode_src_sha256() != base
+
+
+def test_stored_traffic_file_shape():
+    with open(os.path.join(ROOT, "profiles", "decode_e512_traffic.json")) as f:
+        d = json.load(f)
+    assert len(d["decode_src_sha256"]) == 64
+    for key, c in d["configs"].items():
+        workload, m, fmt = key.split("/")
+        assert workload in gen.CONFIGS and m.startswith("M=") and fmt in gen.FMT_NAMES.values()
+        assert c["dram_bytes_per_layer"] == sum(c["kernels_per_layer"].values())
+        assert c["algorithmic_bytes_per_layer"] > 0 and "ncu" in c["command"]
+        # each routed byte is read about once on the tcgen05 decode layers
+        if workload == "decode_e512":
+            assert 1.0 <= c["dram_bytes_per_layer"] / c["algorithmic_bytes_per_layer"] < 1.05
+    # ten distinct routed experts plus x, out, ids and router weights of one token
+    assert np.isclose(d["configs"]["decode_e512/M=1/nvfp4"]["algorithmic_bytes_per_layer"],
+                      10 * gen.expert_bytes(2560, 320, gen.NVFP4) + 2560 * 2 * 2 + 10 * 8)
