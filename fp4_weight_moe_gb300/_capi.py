@@ -68,6 +68,7 @@ SIGNATURES = {
     "moe_fp4_debug_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_fp4_debug_route": (_I, [_P, _I, _I, _I, _P, _P, _P, _Z, _P]),
     "moe_fp4_debug_route_workspace_bytes": (_Z, [_I, _I, _I]),
+    "moe_fp4_debug_quant_mxfp8_rows": (_I, [_P, _I, _I, _P, _P, _P]),
     "moe_fp4_debug_quant_rows": (_I, [_P, _I, _I, _P, _P, _P, _P]),
 }
 
@@ -231,6 +232,10 @@ def moe_fp4_debug_route(ids, M, E, top_k, perm, offset, ws, ws_bytes, stream):
 
 def moe_fp4_debug_route_workspace_bytes(M, E, top_k) -> int:
     return int(_load().moe_fp4_debug_route_workspace_bytes(M, E, top_k))
+
+
+def moe_fp4_debug_quant_mxfp8_rows(inp, rows, K, q, s, stream):
+    return _check("moe_fp4_debug_quant_mxfp8_rows", _load().moe_fp4_debug_quant_mxfp8_rows(inp, rows, K, q, s, stream))
 
 
 def moe_fp4_debug_quant_rows(inp, rows, K, q, s, G, stream):

@@ -24,6 +24,7 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
 cudaError_t launch_debug_route(const int32_t* ids, int M, int E, int top_k, int32_t* perm, int32_t* expert_offset,
                                void* ws, cudaStream_t st);
 cudaError_t launch_debug_quant(const float* in, int rows, int K, uint8_t* q, uint8_t* s, float* G, cudaStream_t st);
+cudaError_t launch_debug_quant_mxfp8(const float* in, int rows, int K, uint8_t* q, uint8_t* s, cudaStream_t st);
 extern std::atomic<int> g_decode_family;
 bool decode_gemv_fits(int M, int E, int H, int I, int top_k);
 int decode_launches(int M, int E, int H, int I, int top_k);
@@ -546,6 +547,14 @@ int moe_fp4_debug_quant_rows(const float* in, int rows, int K, uint8_t* q, uint8
   if (K % 16 != 0) return MOE_FP4_EUNSUPPORTED;
   if (((uintptr_t)q & 7u) || ((uintptr_t)in & 3u)) return MOE_FP4_EINVAL;
   cudaError_t e = launch_debug_quant(in, rows, K, q, s, G, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
+}
+
+int moe_fp4_debug_quant_mxfp8_rows(const float* in, int rows, int K, uint8_t* q, uint8_t* s, void* stream) {
+  if (!in || !q || !s || rows <= 0 || K <= 0) return MOE_FP4_EINVAL;
+  if (K % 32 != 0) return MOE_FP4_EUNSUPPORTED;
+  if (((uintptr_t)q & 15u) || ((uintptr_t)in & 3u)) return MOE_FP4_EINVAL;
+  cudaError_t e = launch_debug_quant_mxfp8(in, rows, K, q, s, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
 }
 

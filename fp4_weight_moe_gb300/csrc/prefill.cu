@@ -628,6 +628,65 @@ __global__ void fill_i32_kernel(int32_t* p, int n, int v) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = v;
 }
 
+// MXFP8 (W4A8-MX activations): E4M3 elements with one UE8M0 scale per 32
+// K-elements; block scale 2^e with e = ceil(log2(amax_blk / 448)) (0 for an
+// all-zero block), clamped to [-127, 127]; elements e4m3_rn(a / 2^e), never
+// above 448 by construction.  ceil(log2(amax / 448)) from amax's bits:
+// amax = m 2^E with m in [1, 2) and 448 = 1.75 2^8, so it is E - 8, plus one
+// when m > 1.75 (mantissa field above 0x600000); amaxes below the normal
+// range give less than -127.
+__device__ __forceinline__ int mxfp8_scale_exponent(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  if (b == 0u) return 0;
+  const int E = (int)(b >> 23) - 127;
+  if (E == -127) return -127;
+  const int e = E - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+// One warp quantises a row of K elements (K % 32 == 0): lane l takes the
+// 32-element blocks l, l + 32, ...; load32(block, float[32]) supplies a
+// block, emit(block, scale_byte, 32 code bytes as 8 words) takes the result.
+template <class Load32, class Emit>
+__device__ __forceinline__ void quant_row_mxfp8(int K, const Load32& load32, const Emit& emit) {
+  const int lane = threadIdx.x & 31;
+  for (int b = lane; b < K / 32; b += 32) {
+    float v[32];
+    load32(b, v);
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int e = mxfp8_scale_exponent(amax);
+    const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, exact (e <= 119 for finite FP32)
+    uint32_t w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // (the second source lands in the low byte)
+      uint16_t lo, hi;
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(v[4 * j + 1] * inv), "f"(v[4 * j] * inv));
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(v[4 * j + 3] * inv), "f"(v[4 * j + 2] * inv));
+      w[j] = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+    emit(b, (uint32_t)(e + 127), w);
+  }
+}
+
+// One warp per row: the MXFP8 quantiser alone (test support).
+__global__ void debug_quant_mxfp8_kernel(const float* in, int rows, int K, uint8_t* q, uint8_t* s) {
+  const int r = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const float* row = in + (size_t)r * K;
+  quant_row_mxfp8(
+      K, [&](int b, float (&v)[32]) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = row[32 * b + i];
+      },
+      [&](int b, uint32_t sb, const uint32_t (&w)[8]) {
+        uint4* dst = reinterpret_cast<uint4*>(q + (size_t)r * K + 32 * b);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        s[(size_t)r * (K / 32) + b] = (uint8_t)sb;
+      });
+}
+
 // One warp per row: the quantiser alone (test support), logical outputs.
 __global__ void debug_quant_kernel(const float* in, int rows, int K, uint8_t* q, uint8_t* s, float* G) {
   const int r = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
@@ -807,6 +866,11 @@ cudaError_t launch_debug_route(const int32_t* ids, int M, int E, int top_k, int3
 
 cudaError_t launch_debug_quant(const float* in, int rows, int K, uint8_t* q, uint8_t* s, float* G, cudaStream_t st) {
   debug_quant_kernel<<<(rows + 7) / 8, 256, 0, st>>>(in, rows, K, q, s, G);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_quant_mxfp8(const float* in, int rows, int K, uint8_t* q, uint8_t* s, cudaStream_t st) {
+  debug_quant_mxfp8_kernel<<<(rows + 7) / 8, 256, 0, st>>>(in, rows, K, q, s);
   return cudaGetLastError();
 }
 

@@ -384,6 +384,22 @@ MOE_FP4_API size_t moe_fp4_debug_route_workspace_bytes(int M, int E, int top_k);
 MOE_FP4_API int moe_fp4_debug_quant_rows(const float *in, int rows, int K, uint8_t *q, uint8_t *s, float *G,
                                          void *stream);
 
+/*
+ * Test support: the MXFP8 activation quantiser of the W4A8-MX variant on
+ * rows x K FP32 values in device memory (K % 32 == 0): q [rows][K] E4M3
+ * bytes (16-byte aligned), s [rows][K/32] UE8M0 bytes.  Per 32-block the
+ * scale is 2^ceil(log2(amax/448)) (2^0 for an all-zero block, exponent
+ * clamped to [-127, 127]) and each element e4m3_rn(a / scale); the sign of a
+ * value that rounds to zero is kept.  The pages name MXFP8 activations with
+ * UE8M0 scales per 32 (b12x PR #22, "rp-native tiny-decode kernel for
+ * w4a8_mx (M=1)"; flashinfer PR #4285, scale_format_e8m0_k32) without the
+ * scale rule; this is the MX weight rule with 448 in place of 6.
+ * MOE_FP4_EINVAL for null or misaligned pointers, MOE_FP4_EUNSUPPORTED for
+ * K % 32 != 0.
+ */
+MOE_FP4_API int moe_fp4_debug_quant_mxfp8_rows(const float *in, int rows, int K, uint8_t *q, uint8_t *s,
+                                               void *stream);
+
 #ifdef __cplusplus
 }
 #endif
