@@ -149,3 +149,35 @@ def test_band_policy_by_shape(lib):
         c.moe_fp4_debug_set_mid_band(prev)
     with pytest.raises(c.MoeFp4Error):
         c.moe_fp4_debug_set_mid_band(3)
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """include/moe_fp4.h compiles as C99 (-pedantic, no warnings) and a C
+    program links against libmoe_fp4.so and calls a host-only entry point."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "abi.c"
+    src.write_text("""
+#include <stddef.h>
+#include <stdint.h>
+#include "moe_fp4.h"
+int main(void) {
+  size_t w13, s13, w2, s2;
+  moe_fp4_activation act = {MOE_FP4_ACT_SWIGLUOAI, 1.702f, 1.0f, 7.0f};
+  int st = moe_fp4_prepared_sizes(8, 256, 128, MOE_FP4_MXFP4, &w13, &s13, &w2, &s2);
+  (void)act;
+  if (st != MOE_FP4_OK) return 1;
+  if (w13 != (size_t)8 * 256 * 128 || w2 != (size_t)8 * 256 * 64) return 2;
+  return moe_fp4_status_string(MOE_FP4_EWORKSPACE)[0] ? 0 : 3;
+}
+""")
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(_capi.LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-L", libdir, "-lmoe_fp4", f"-Wl,-rpath,{libdir}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    assert subprocess.run([str(exe)]).returncode == 0
