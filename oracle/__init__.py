@@ -105,6 +105,8 @@ def _bind(lib):
     lib.moe_oracle_quant_mxfp8_row.argtypes = [P, i, P, P]
     lib.moe_oracle_forward_w4a8_act.restype = i
     lib.moe_oracle_forward_w4a8_act.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, P, i, P, i, i, d, d, d]
+    lib.moe_oracle_forward_relu2.restype = i
+    lib.moe_oracle_forward_relu2.argtypes = [P, P, P, P, P, P, P, P, P, i, i, i, i, i, i, P, i, P, i]
     lib.moe_oracle_route.restype = i
     lib.moe_oracle_route.argtypes = [P, i, i, i, P, P]
     lib.moe_oracle_num_threads.restype = i
@@ -276,6 +278,30 @@ def forward_w4a8(x_bf16, weights: dict, topk_ids, topk_weights, E: int, H: int, 
     a = _act_args(act) or (ACT_SILU, 0.0, 0.0, 0.0)
     rc = _load().moe_oracle_forward_w4a8_act(_ptr(x), _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2), _ptr(ids), _ptr(tw),
                                              M, E, H, I, top_k, _ptr(tok), n_tok, _ptr(out), nthreads, *a)
+    if rc != 0:
+        raise ValueError("oracle rejected the shapes")
+    return out
+
+
+def forward_relu2(x_bf16, weights: dict, topk_ids, topk_weights, E: int, H: int, I: int, top_k: int, fmt: int,
+                  tokens: Optional[Sequence[int]] = None, nthreads: int = 0) -> np.ndarray:
+    """Non-gated experts with the squared ReLU in FP64: ``weights`` holds w1
+    ``[E][I][H/2]``, s1 ``[E][I][H/B]``, (NVFP4) g1 ``[E]``, and w2, s2, g2 as
+    for the gated layer.  Returns ``[n_tok][H]``."""
+    x = _np(x_bf16, np.uint16)
+    M = x.shape[0]
+    w1, s1 = _np(weights["w1"], np.uint8), _np(weights["s1"], np.uint8)
+    g1 = _np(weights.get("g1"), np.float32) if fmt == NVFP4 else None
+    w2, s2 = _np(weights["w2"], np.uint8), _np(weights["s2"], np.uint8)
+    g2 = _np(weights.get("g2"), np.float32) if fmt == NVFP4 else None
+    ids = _np(topk_ids, np.int32)
+    tw = _np(topk_weights, np.float32)
+    tok = None if tokens is None else np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    n_tok = M if tok is None else len(tok)
+    out = np.full((n_tok, H), np.nan, dtype=np.float64)  # poisoned: the oracle must overwrite
+    rc = _load().moe_oracle_forward_relu2(_ptr(x), _ptr(w1), _ptr(s1), _ptr(g1), _ptr(w2), _ptr(s2), _ptr(g2),
+                                          _ptr(ids), _ptr(tw), M, E, H, I, top_k, fmt, _ptr(tok), n_tok, _ptr(out),
+                                          nthreads)
     if rc != 0:
         raise ValueError("oracle rejected the shapes")
     return out

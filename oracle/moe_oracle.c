@@ -31,6 +31,7 @@
  *     quantiser restricted to gated activations).
  *   - W4A8-MX mirror: MXFP4 weights with activations quantised to MXFP8
  *     (E4M3 elements, a UE8M0 scale per 32), then the same FP64 layer.
+ *   - Non-gated experts with the squared ReLU: FC1 of I rows, h = max(u, 0)^2.
  *
  * Build: plain C99, -O2 -fno-fast-math -ffp-contract=off, optional OpenMP.
  */
@@ -456,6 +457,64 @@ int moe_oracle_forward_prefill(const uint16_t *x_bf16, const uint8_t *w13, const
     return moe_oracle_forward_prefill_act(x_bf16, w13, s13, g13, w2, s2, g2, topk_ids, topk_w, M, E, H, I, top_k,
                                           fmt, tokens, n_tok, out, xq_out, xs_out, xg_out, nthreads,
                                           ORACLE_ACT_SILU, 0.0, 0.0, 0.0);
+}
+
+/* --------------------------------------------- non-gated experts (ReLU^2) */
+
+/*
+ * Non-gated experts with the squared ReLU ("relu2" of the SM12x sync PR,
+ * flashinfer PR #4285, which keeps the exact activation quantiser for it
+ * because its squared outputs are not a gated product): FC1 has I rows,
+ * w1 [E][I][H/2] with s1 [E][I][H/B] (and for NVFP4 one multiplier g1[e]),
+ *   h[n] = max(x . W1[e][n], 0)^2
+ * then FC2 and the router-weighted sum as for the gated layer.  For the
+ * tokens listed (NULL = all M); out is [n_tok][H] FP64.                     */
+int moe_oracle_forward_relu2(const uint16_t *x_bf16, const uint8_t *w1, const uint8_t *s1, const float *g1,
+                             const uint8_t *w2, const uint8_t *s2, const float *g2, const int32_t *topk_ids,
+                             const float *topk_w, int M, int E, int H, int I, int top_k, int fmt,
+                             const int32_t *tokens, int n_tok, double *out, int nthreads)
+{
+    if (fmt != ORACLE_NVFP4 && fmt != ORACLE_MXFP4) return 1;
+    int B = block_of(fmt);
+    if (H % B || I % B) return 1;
+    if (!tokens) n_tok = M;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel
+#endif
+    {
+        double *x = (double *)malloc(sizeof(double) * (size_t)H);
+        double *h = (double *)malloc(sizeof(double) * (size_t)I);
+        double *y = (double *)malloc(sizeof(double) * (size_t)H);
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int i = 0; i < n_tok; ++i) {
+            int t = tokens ? tokens[i] : i;
+            for (int k = 0; k < H; ++k) x[k] = bf16_to_double(x_bf16[(size_t)t * H + k]);
+            double *o = out + (size_t)i * H;
+            for (int m = 0; m < H; ++m) o[m] = 0.0;
+            for (int j = 0; j < top_k; ++j) {
+                int e = topk_ids[(size_t)t * top_k + j];
+                if (e < 0 || e >= E) continue;
+                const uint8_t *nib = w1 + (size_t)e * I * (H / 2);
+                const uint8_t *sc = s1 + (size_t)e * I * (H / B);
+                double g = fmt == ORACLE_NVFP4 ? (double)g1[e] : 1.0;
+                for (int n = 0; n < I; ++n) {
+                    double u = 0.0;
+                    for (int k = 0; k < H; ++k) u += x[k] * weight_at(nib, sc, H, fmt, g, n, k);
+                    double r = u > 0.0 ? u : 0.0;
+                    h[n] = r * r;
+                }
+                expert_fc2(h, w2, s2, g2, e, H, I, fmt, y);
+                double w = (double)topk_w[(size_t)t * top_k + j];
+                for (int m = 0; m < H; ++m) o[m] += w * y[m];
+            }
+        }
+        free(x); free(h); free(y);
+    }
+    (void)nthreads;
+    return 0;
 }
 
 /* ------------------------------------------- W4A8-MX activations (MXFP8) */

@@ -63,6 +63,10 @@ MUTATIONS = {
     "mxfp8_sign_dropped": ("if (signbit(v)) c |= 0x80;", "if (v < 0.0f && c != 0) c |= 0x80;"),
     "mxfp8_h_unquantised": ("moe_oracle_quant_mxfp8_row(hf, I, hq, hs);\n                dequant_mxfp8_row(hq, hs, I, hd);",
                             "moe_oracle_quant_mxfp8_row(hf, I, hq, hs);\n                for (int n = 0; n < I; ++n) hd[n] = h[n];"),
+    "relu2_square_dropped": ("h[n] = r * r;", "h[n] = r;"),
+    "relu2_relu_dropped": ("double r = u > 0.0 ? u : 0.0;", "double r = u;"),
+    "relu2_rows_shifted": ("for (int k = 0; k < H; ++k) u += x[k] * weight_at(nib, sc, H, fmt, g, n, k);",
+                           "for (int k = 0; k < H; ++k) u += x[k] * weight_at(nib, sc, H, fmt, g, (n + 1) % I, k);"),
     "route_order": ("for (int t = 0; t < M; ++t)\n            for (int j = 0; j < top_k; ++j)\n                if (topk_ids[(size_t)t * top_k + j] == e) perm[r++] = t * top_k + j;",
                     "for (int j = 0; j < top_k; ++j)\n            for (int t = 0; t < M; ++t)\n                if (topk_ids[(size_t)t * top_k + j] == e) perm[r++] = t * top_k + j;"),
 }
@@ -93,6 +97,9 @@ def _run_pins():
         ("mxfp8_grid", pins.test_mxfp8_exact_on_grid),
         ("w4a8_golden", pins.test_w4a8_hand_worked_layer),
         ("w4a8_invariants", pins.test_w4a8_invariants_and_accuracy),
+        ("relu2_golden", pins.test_relu2_hand_worked_layer),
+        ("relu2_mlp_mx", lambda: pins.test_relu2_is_a_plain_mlp_mixture(0)),
+        ("relu2_mlp_nv", lambda: pins.test_relu2_is_a_plain_mlp_mixture(1)),
     ]
     for case in pins._golden_cases():
         checks.append(("golden_" + case["name"], lambda c=case: pins.test_hand_worked_layers(c)))

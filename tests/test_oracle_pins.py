@@ -572,3 +572,57 @@ def test_w4a8_invariants_and_accuracy():
     assert cos(base) > 0.998 and not np.array_equal(base, ref)
     assert cos(base) > cos(nv4)
     assert np.abs(base - ref).max() < np.abs(nv4 - ref).max()
+
+
+# ------------------------------------------------ non-gated experts (ReLU^2)
+def _relu2_weights(E, H, I, fmt, seed):
+    g = torch.Generator().manual_seed(seed)
+    enc = gen.encode_mxfp4 if fmt == gen.MXFP4 else gen.encode_nvfp4
+    out = {"w1": [], "s1": [], "g1": [], "w2": [], "s2": [], "g2": []}
+    for _ in range(E):
+        for name, rows, K in (("1", I, H), ("2", H, I)):
+            r = enc(torch.randn(rows, K, generator=g) * 0.05)
+            out["w" + name].append(r[0].numpy())
+            out["s" + name].append(r[1].numpy())
+            out["g" + name].append(float(r[2]) if fmt == gen.NVFP4 else 1.0)
+    return {k: np.array(v, np.float32 if k[0] == "g" else np.uint8) for k, v in out.items()}
+
+
+def test_relu2_hand_worked_layer():
+    """H = I = 32, x = 1: up nibbles 0.5 (scale 1) give u = 16, h = 16^2 =
+    256; down nibbles 1.0 with scale 2^-5 make every output 32 * 2^-5 * 256 =
+    256.  With the up nibbles -0.5 the ReLU clips u = -16 to zero."""
+    E, H, I = 1, 32, 32
+    x = torch.full((1, H), 1.0, dtype=torch.bfloat16)
+    ids, tw = np.zeros((1, 1), np.int32), np.ones((1, 1), np.float32)
+    for up_nibble, want in ((0x1, 256.0), (0x9, 0.0)):
+        w = {"w1": np.full((E, I, H // 2), up_nibble | (up_nibble << 4), np.uint8),
+             "s1": np.full((E, I, H // 32), 127, np.uint8),
+             "w2": np.full((E, H, I // 2), 0x22, np.uint8), "s2": np.full((E, H, I // 32), 122, np.uint8)}
+        out = oracle.forward_relu2(x, w, ids, tw, E, H, I, 1, gen.MXFP4)
+        np.testing.assert_array_equal(out, np.full((1, H), want))
+
+
+@pytest.mark.parametrize("fmt", [gen.MXFP4, gen.NVFP4])
+def test_relu2_is_a_plain_mlp_mixture(fmt):
+    """The layer equals the router-weighted sum of plain ReLU^2 MLPs,
+    computed with NumPy float64 matrix products on independently dequantised
+    weights; invalid slots contribute nothing."""
+    E, H, I, M, k = 4, 64, 32, 3, 2
+    w = _relu2_weights(E, H, I, fmt, seed=51 + fmt)
+    x = gen.draw_activations(M, H, seed=52)
+    ids = np.array([[0, 3], [2, -1], [1, 4]], np.int32)
+    tw = np.array([[0.7, 0.3], [0.9, 0.5], [0.4, 0.6]], np.float32)
+    got = oracle.forward_relu2(x, w, ids, tw, E, H, I, k, fmt)
+    xf = x.to(torch.float64).numpy()
+    want = np.zeros((M, H))
+    for t in range(M):
+        for j in range(k):
+            e = int(ids[t, j])
+            if not 0 <= e < E:
+                continue
+            W1 = _np_dequant(w["w1"][e], w["s1"][e], H, fmt, float(w["g1"][e]))
+            W2 = _np_dequant(w["w2"][e], w["s2"][e], I, fmt, float(w["g2"][e]))
+            h = np.maximum(W1 @ xf[t], 0.0) ** 2
+            want[t] += float(tw[t, j]) * (W2 @ h)
+    np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-12 * np.abs(want).max())
