@@ -97,6 +97,7 @@ def _run_pins():
         ("mxfp8_grid", pins.test_mxfp8_exact_on_grid),
         ("w4a8_golden", pins.test_w4a8_hand_worked_layer),
         ("w4a8_invariants", pins.test_w4a8_invariants_and_accuracy),
+        ("w4a8_brute", pins.test_w4a8_layer_brute_force),
         ("relu2_golden", pins.test_relu2_hand_worked_layer),
         ("relu2_mlp_mx", lambda: pins.test_relu2_is_a_plain_mlp_mixture(0)),
         ("relu2_mlp_nv", lambda: pins.test_relu2_is_a_plain_mlp_mixture(1)),

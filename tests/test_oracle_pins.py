@@ -626,3 +626,44 @@ def test_relu2_is_a_plain_mlp_mixture(fmt):
             h = np.maximum(W1 @ xf[t], 0.0) ** 2
             want[t] += float(tw[t, j]) * (W2 @ h)
     np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-12 * np.abs(want).max())
+
+
+def _torch_mxfp8(v: np.ndarray) -> np.ndarray:
+    """MXFP8 round trip of a float32 vector (K % 32 == 0) through torch's
+    float8_e4m3fn conversion, with the scales from Python's math."""
+    out = np.empty(v.shape, np.float64)
+    for b in range(0, v.size, 32):
+        blk = v[b:b + 32].astype(np.float64)
+        amax = float(np.abs(blk).max())
+        e = 0 if amax == 0 else max(-127, min(127, _ceil_log2_ratio(amax, 448.0)))
+        q = torch.tensor((blk / 2.0 ** e).astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+        out[b:b + 32] = q * 2.0 ** e
+    return out
+
+
+def test_w4a8_layer_brute_force():
+    """The W4A8-MX layer rebuilt from library pieces: x and h (FP64 -> FP32 ->
+    BF16 by torch) through torch's E4M3 conversion per 32-block, NumPy float64
+    matrix products on independently dequantised MXFP4 weights."""
+    E, H, I, M, k = 3, 64, 64, 2, 2
+    w = _tiny_weights(E, H, I, gen.MXFP4, seed=61)
+    x = gen.draw_activations(M, H, seed=62)
+    ids = np.array([[0, 2], [1, -1]], np.int32)
+    tw = np.array([[0.6, 0.4], [0.8, 0.2]], np.float32)
+    got = oracle.forward_w4a8(x, w, ids, tw, E, H, I, k)
+    xf = x.to(torch.float32).numpy()
+    want = np.zeros((M, H))
+    for t in range(M):
+        xq = _torch_mxfp8(xf[t])
+        for j in range(k):
+            e = int(ids[t, j])
+            if not 0 <= e < E:
+                continue
+            Wg = _np_dequant(w["w13"][e, :I], w["s13"][e, :I], H, 0)
+            Wu = _np_dequant(w["w13"][e, I:], w["s13"][e, I:], H, 0)
+            Wd = _np_dequant(w["w2"][e], w["s2"][e], I, 0)
+            g, u = Wg @ xq, Wu @ xq
+            h = g / (1.0 + np.exp(-g)) * u
+            hb = torch.tensor(h).to(torch.float32).to(torch.bfloat16).to(torch.float32).numpy()
+            want[t] += float(tw[t, j]) * (Wd @ _torch_mxfp8(hb))
+    np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-12 * np.abs(want).max())
