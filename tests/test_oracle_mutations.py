@@ -67,6 +67,15 @@ MUTATIONS = {
     "relu2_relu_dropped": ("double r = u > 0.0 ? u : 0.0;", "double r = u;"),
     "relu2_rows_shifted": ("for (int k = 0; k < H; ++k) u += x[k] * weight_at(nib, sc, H, fmt, g, n, k);",
                            "for (int k = 0; k < H; ++k) u += x[k] * weight_at(nib, sc, H, fmt, g, (n + 1) % I, k);"),
+    "prefill_bf16_staging_dropped": ("hf[n] = bf16_round((float)h[n]);\n                float hG;",
+                                     "hf[n] = (float)h[n];\n                float hG;"),
+    "prefill_h_takes_x_multiplier": ("moe_oracle_quant_nvfp4_row(hf, I, hq, hs, &hG);\n                dequant_nvfp4_row(hq, hs, hG, I, hd);",
+                                     "moe_oracle_quant_nvfp4_row(hf, I, hq, hs, &hG);\n                dequant_nvfp4_row(hq, hs, xG, I, hd);"),
+    "prefill_h_dequant_skipped": ("dequant_nvfp4_row(hq, hs, hG, I, hd);\n                expert_fc2(hd,",
+                                  "dequant_nvfp4_row(hq, hs, hG, I, hd);\n                expert_fc2(h,"),
+    "prefill_x_multiplier_dropped": ("dequant_nvfp4_row(xq, xs, xG, H, xd);", "dequant_nvfp4_row(xq, xs, 1.0f, H, xd);"),
+    "prefill_h_multiplier_per_token": ("float hG;\n                moe_oracle_quant_nvfp4_row(hf, I, hq, hs, &hG);",
+                                       "float hG;\n                static float shared_hG;\n                moe_oracle_quant_nvfp4_row(hf, I, hq, hs, &hG);\n                if (j > 0) hG = shared_hG; else shared_hG = hG;"),
     "route_order": ("for (int t = 0; t < M; ++t)\n            for (int j = 0; j < top_k; ++j)\n                if (topk_ids[(size_t)t * top_k + j] == e) perm[r++] = t * top_k + j;",
                     "for (int j = 0; j < top_k; ++j)\n            for (int t = 0; t < M; ++t)\n                if (topk_ids[(size_t)t * top_k + j] == e) perm[r++] = t * top_k + j;"),
 }
@@ -101,6 +110,9 @@ def _run_pins():
         ("relu2_golden", pins.test_relu2_hand_worked_layer),
         ("relu2_mlp_mx", lambda: pins.test_relu2_is_a_plain_mlp_mixture(0)),
         ("relu2_mlp_nv", lambda: pins.test_relu2_is_a_plain_mlp_mixture(1)),
+        ("prefill_brute_nv", lambda: pins.test_prefill_mirror_brute_force(1)),
+        ("prefill_brute_mx", lambda: pins.test_prefill_mirror_brute_force(0)),
+        ("prefill_per_row_h", pins.test_prefill_mirror_quantises_h_per_routed_row),
     ]
     for case in pins._golden_cases():
         checks.append(("golden_" + case["name"], lambda c=case: pins.test_hand_worked_layers(c)))

@@ -667,3 +667,99 @@ def test_w4a8_layer_brute_force():
             hb = torch.tensor(h).to(torch.float32).to(torch.bfloat16).to(torch.float32).numpy()
             want[t] += float(tw[t, j]) * (Wd @ _torch_mxfp8(hb))
     np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-12 * np.abs(want).max())
+
+
+# ------------------------------------------------------------------ prefill mirror (NVFP4 activations)
+_E2M1_MIDS = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+
+
+def _np_e2m1_nearest_even(r: np.ndarray) -> np.ndarray:
+    """E2M1 magnitudes of float32 quotients by decision thresholds: the
+    number of midpoints strictly below |r| gives the code, and a value exactly
+    on a midpoint goes to the even code of its two neighbours; beyond 6 the
+    code saturates at 7 (6.0).  Returns the grid values with r's sign."""
+    a = np.abs(r)
+    code = np.searchsorted(_E2M1_MIDS, a, side="left")
+    on_mid = np.zeros(a.shape, bool)
+    inside = code < _E2M1_MIDS.size
+    on_mid[inside] = a[inside] == _E2M1_MIDS[code[inside]]
+    code = code + (on_mid & (code % 2 == 1))
+    return np.copysign(_TABLE[np.minimum(code, 7)], r)
+
+
+def _np_nvfp4_row(v: np.ndarray) -> np.ndarray:
+    """NVFP4 round trip of one float32 row (K % 16 == 0) with the prefill
+    rules: G = amax / (6 * 448) (1 for a zero row), block scale E4M3 (torch's
+    float8_e4m3fn conversion) of bmax / (6 G), codes nearest-even of a / (s G),
+    each step one float32 operation; returns the dequantised values q s G."""
+    v = v.astype(np.float32)
+    amax = np.float32(np.abs(v).max())
+    G = np.float32(1.0) if amax == 0 else np.float32(amax / np.float32(2688.0))
+    six_g = np.float32(np.float32(6.0) * G)
+    out = np.empty(v.size, np.float64)
+    for b in range(0, v.size, 16):
+        blk = v[b:b + 16]
+        bmax = np.float32(np.abs(blk).max())
+        sf = np.float32(min(np.float32(bmax / six_g), np.float32(448.0)))
+        s = np.float32(torch.tensor([sf]).to(torch.float8_e4m3fn).to(torch.float32).item())
+        sg = np.float32(s * G)
+        if sg == 0:
+            out[b:b + 16] = 0.0
+            continue
+        q = _np_e2m1_nearest_even((blk / sg).astype(np.float32))
+        out[b:b + 16] = q * float(s) * float(G)
+    return out
+
+
+@pytest.mark.parametrize("fmt", [gen.NVFP4, gen.MXFP4])
+def test_prefill_mirror_brute_force(fmt):
+    """The prefill band's mirrored layer rebuilt from independent pieces: x
+    and h quantised per row by the NumPy float32 NVFP4 round trip above (h
+    taken FP64 -> FP32 -> BF16 by torch before it), NumPy float64 matrix
+    products on independently dequantised weights, one multiplier per
+    quantised row and h quantised per routed row (token, slot)."""
+    E, H, I, M, k = 3, 64, 64, 3, 2
+    w = _tiny_weights(E, H, I, fmt, seed=71)
+    x = gen.draw_activations(M, H, seed=72)
+    ids = np.array([[0, 2], [1, -1], [2, 0]], np.int32)
+    tw = np.array([[0.6, 0.4], [0.8, 0.2], [0.3, 0.7]], np.float32)
+    got = oracle.forward_prefill(x, w, ids, tw, E, H, I, k, fmt=fmt)[0]
+    xf = x.to(torch.float32).numpy()
+    want = np.zeros((M, H))
+    for t in range(M):
+        xq = _np_nvfp4_row(xf[t])
+        for j in range(k):
+            e = int(ids[t, j])
+            if not 0 <= e < E:
+                continue
+            g13 = w["g13"][e] if fmt == gen.NVFP4 else (1.0, 1.0)
+            g2 = w["g2"][e] if fmt == gen.NVFP4 else 1.0
+            Wg = _np_dequant(w["w13"][e, :I], w["s13"][e, :I], H, fmt, float(g13[0]))
+            Wu = _np_dequant(w["w13"][e, I:], w["s13"][e, I:], H, fmt, float(g13[1]))
+            Wd = _np_dequant(w["w2"][e], w["s2"][e], I, fmt, float(g2))
+            g, u = Wg @ xq, Wu @ xq
+            h = g / (1.0 + np.exp(-g)) * u
+            hb = torch.tensor(h).to(torch.float32).to(torch.bfloat16).to(torch.float32).numpy()
+            want[t] += float(tw[t, j]) * (Wd @ _np_nvfp4_row(hb))
+    np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-12 * np.abs(want).max())
+
+
+def test_prefill_mirror_quantises_h_per_routed_row():
+    """Two slots of one token on experts whose h differ by a factor of 2^10
+    get their own h multipliers: the mirrored output equals the sum of the two
+    one-slot layers (a multiplier shared across the token's slots would flush
+    the small slot's h to zero)."""
+    E, H, I = 2, 64, 64
+    w = _tiny_weights(E, H, I, gen.NVFP4, seed=73)
+    w["g2"] = w["g2"].copy()
+    w["g13"] = w["g13"].copy()
+    w["g13"][1] *= 2.0 ** -5  # expert 1's gate and up scaled by 2^-5: h by 2^-10
+    x = gen.draw_activations(1, H, seed=74)
+    both = oracle.forward_prefill(x, w, np.array([[0, 1]], np.int32), np.array([[1.0, 1.0]], np.float32),
+                                  E, H, I, 2)[0]
+    a = oracle.forward_prefill(x, w, np.array([[0, -1]], np.int32), np.array([[1.0, 1.0]], np.float32),
+                               E, H, I, 2)[0]
+    b = oracle.forward_prefill(x, w, np.array([[-1, 1]], np.int32), np.array([[1.0, 1.0]], np.float32),
+                               E, H, I, 2)[0]
+    assert np.abs(b).max() > 0
+    np.testing.assert_allclose(both, a + b, rtol=1e-12, atol=1e-14 * np.abs(both).max())
