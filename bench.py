@@ -34,6 +34,8 @@ sys.path.insert(0, ROOT)
 METRIC = "fused FP4 MoE µs/layer & routed-weight HBM GB/s at M=1..8; prefill TFLOP/s"
 WORKLOAD = "decode_e512"
 WINDOW = 20
+# decode-band kernel plans of moe_fp4_debug_set_decode_family
+DECODE_PLANS = {"auto": 0, "gemv": 1, "chain": 2, "single": 3}
 
 
 def parse():
@@ -45,10 +47,15 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-sweep", action="store_true", help="time the headline workload only")
+    ap.add_argument("--min-timed-s", type=float, default=0.6,
+                    help="device time of the headline's timed replays (at least 15 replays); sweep entries a quarter")
     ap.add_argument("--workload", default=WORKLOAD, help="workload name (default: the decode_e512 headline)")
     ap.add_argument("--M", type=int, default=None, help="override the token count")
     ap.add_argument("--E", type=int, default=None, help="override the expert count (profiling on smaller memory)")
     ap.add_argument("--fmt", choices=["mxfp4", "nvfp4"], default=None)
+    ap.add_argument("--decode-plan", choices=list(DECODE_PLANS), default="auto",
+                    help="decode-band kernel plan (auto: by shape)")
     return ap.parse_args()
 
 
@@ -75,7 +82,9 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling during the timed regions: start()
+    before a timed region, pause() after it; stop() summarises every sample
+    taken."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -85,30 +94,41 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.lines = []
+        self.available = True
 
     def start(self):
+        if self.proc is not None or not self.available:
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread = threading.Thread(target=self._read, args=(self.proc,), daemon=True)
             self.thread.start()
         except Exception:
             self.proc = None
+            self.available = False
 
-    def _read(self):
-        for line in self.proc.stdout:
+    def _read(self, proc):
+        for line in proc.stdout:
             self.lines.append(line.strip())
 
-    def stop(self):
+    def pause(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return
         time.sleep(0.25)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
+        self.thread.join(timeout=5)
+        self.proc = None
+
+    def stop(self):
+        self.pause()
+        if not self.available:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
@@ -173,8 +193,9 @@ def layer_bytes(ids, E, H, I, M, top_k, fmt):
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_layers(c, seed, ids_pool, w_pool, x_host, seconds, max_layers):
-    """Time the FP64 oracle on successive routing draws (bounded sample)."""
+def oracle_layers(c, seed, ids_pool, w_pool, x_host, seconds, max_layers, threads=0):
+    """Time the FP64 oracle on successive routing draws (bounded sample), on
+    `threads` OpenMP threads (0: the affinity cores)."""
     import oracle
     from workload import gen
     E, H, I, k, M, fmt = c["E"], c["H"], c["I"], c["top_k"], c["M"], c["fmt"]
@@ -186,14 +207,14 @@ def oracle_layers(c, seed, ids_pool, w_pool, x_host, seconds, max_layers):
         remap = {e: j for j, e in enumerate(used)}
         ids_c = [[remap.get(e, -1) for e in row] for row in ids.tolist()]
         t0 = time.perf_counter()
-        oracle.forward(x_host, sub, ids_c, w_pool[i], len(used), H, I, k, fmt)
+        oracle.forward(x_host, sub, ids_c, w_pool[i], len(used), H, I, k, fmt, nthreads=threads)
         total_s += time.perf_counter() - t0
         total_bytes += layer_bytes(ids, E, H, I, M, k, fmt)[0]
         done += 1
         if total_s >= seconds:
             break
-    threads = min(oracle.num_threads(), M)  # the oracle parallelises over tokens
-    return done, total_s, total_bytes, threads
+    # the oracle spreads each layer over (token, slot, row) and (token, output row)
+    return done, total_s, total_bytes, threads if threads > 0 else affinity_cores()
 
 
 def run_reference(args):
@@ -244,11 +265,249 @@ def decode_src_sha256():
 def decode_kernel_label(m, M, E, H, I, k):
     """What one decode layer of this shape launches (for the JSON line)."""
     c = m._capi
-    if M <= m.MOE_FP4_DECODE_MAX_M and c.moe_fp4_debug_decode_family_of(M, E, H, I, k) == 1:
+    fam = c.moe_fp4_debug_decode_family_of(M, E, H, I, k) if M <= m.MOE_FP4_DECODE_MAX_M else 0
+    if fam == 1:
         return "decode layer: streaming-GEMV FC1 + FC2 (PDL-chained)"
+    if fam == 3:
+        return "decode layer: one tcgen05 launch (FC1, h handed over by flags, FC2)"
     head = "decode layer" if M <= m.MOE_FP4_DECODE_MAX_M else \
         f"decode layer in {-(-M // m.MOE_FP4_DECODE_MAX_M)} chunks"
     return f"{head}: x pre-pass + FC1 + " + ("" if M < 2 else "h pre-pass + ") + "FC2 (tcgen05, PDL-chained)"
+
+
+COS_MIN, MAXABS_REL_RMS = 0.99995, 2e-2  # the parity bound of the layer output against the FP64 oracle
+
+# The sweep: every workload configuration beside the headline, each checked
+# against the oracle before it is timed.  (label, workload, overrides)
+SWEEP = [("C0", "tiny_decode", {}),
+         ("C1/M=8", "decode_e512", dict(M=8)),
+         ("C2", "decode_e288_m4", {})] + \
+    [(f"C3/M={M}/{f}", "decode_e256", dict(M=M, fmt=fmt)) for fmt, f in ((0, "mxfp4"), (1, "nvfp4"))
+     for M in (1, 2, 4, 8)] + \
+    [("C4", "prefill_e128", {})]
+
+
+def affinity_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def parity_metrics(got, want):
+    """(cosine, max |got - want| / RMS(want), zero rows exact) over the flattened output."""
+    import numpy as np
+    g = np.asarray(got, np.float64).reshape(-1)
+    w = np.asarray(want, np.float64).reshape(-1)
+    rms = float(np.sqrt(np.mean(w * w)))
+    ng, nw = float(np.linalg.norm(g)), float(np.linalg.norm(w))
+    cos = float(np.dot(g, w) / (ng * nw)) if ng > 0 and nw > 0 else (1.0 if ng == nw == 0 else 0.0)
+    err = float(np.max(np.abs(g - w))) / rms if rms > 0 else float(np.max(np.abs(g)))
+    rows_w = np.asarray(want).reshape(np.asarray(got).shape)
+    zero_rows = ~np.any(rows_w != 0, axis=-1)
+    zero_ok = not np.any(np.asarray(got)[zero_rows])
+    ok = bool(np.all(np.isfinite(g))) and zero_ok and (rms == 0 or (cos >= COS_MIN and err <= MAXABS_REL_RMS))
+    return {"cos": cos, "maxabs_over_rms": err, "zero_rows_exact": zero_ok, "ok": ok}
+
+
+def oracle_check(m, gen, weights, c, x, ids, tw, got, prefill, threads):
+    """The layer of one routing draw on the FP64 oracle (routed experts only;
+    the prefill band on a spread of 16 tokens, its activation quantisation
+    mirrored) against the GPU output of the same draw."""
+    import numpy as np
+    import oracle
+    import torch
+    E, H, I, k, M, fmt = c["E"], c["H"], c["I"], c["top_k"], c["M"], c["fmt"]
+    tokens = None
+    if prefill:
+        tokens = sorted(set(int(t) for t in np.linspace(0, M - 1, 16)))
+        ids_used = ids[tokens]
+    else:
+        ids_used = ids
+    used = gen.routed_unique_experts(ids_used, E)
+    remap = {e: j for j, e in enumerate(used)}
+    ids_c = np.array([[remap.get(e, -1) for e in row] for row in ids.tolist()], dtype=np.int32)
+    idx = torch.tensor(used if used else [0], dtype=torch.long, device=weights["w13"].device)
+    sub = {kk: v.index_select(0, idx).cpu() for kk, v in weights.items() if v is not None}
+    t0 = time.perf_counter()
+    if prefill:
+        want = oracle.forward_prefill(x.cpu(), sub, ids_c, tw.cpu(), max(1, len(used)), H, I, k, tokens=tokens,
+                                      nthreads=threads, fmt=fmt)[0]
+        got_rows = got.float().cpu().double().numpy()[tokens]
+    else:
+        want = oracle.forward(x.cpu(), sub, ids_c, tw.cpu(), max(1, len(used)), H, I, k, fmt, nthreads=threads)
+        got_rows = got.float().cpu().double().numpy()
+    secs = time.perf_counter() - t0
+    r = parity_metrics(got_rows, want)
+    r["oracle_s"] = secs
+    r["checked"] = f"{len(tokens)} sampled tokens (mirrored activation quantisation)" if prefill else \
+        f"all {M} tokens"
+    return r
+
+
+def measure(m, name, ov, K, W, dev, rank, ws_world, min_timed_s, threads, do_e2e, sampler):
+    """One workload: draw it, check it against the oracle, then time K layers
+    in a CUDA graph replayed R >= 15 times (and at least min_timed_s of device
+    time), each replay between CUDA events; and, end to end, K calls of the
+    host-buffer entry point.  Returns a dict (or the parity failure)."""
+    import statistics as st
+    import torch
+    from workload import gen
+    c = dict(gen.CONFIGS[name])
+    c.update({kk: v for kk, v in ov.items() if v is not None})
+    E, H, I, k, M, fmt = c["E"], c["H"], c["I"], c["top_k"], c["M"], c["fmt"]
+    seed = gen.CONFIG_SEED[name]
+    window = max(1, min(WINDOW, E // (k * M)))
+    weights = gen.make_expert_weights(E, H, I, fmt, seed, device=dev)
+    pw = m.prepare_weights(weights, E, H, I, fmt)
+    x = gen.draw_activations(M, H, seed + 17, device=dev)
+    ids_pool, w_pool = gen.draw_routing_pool(max(K, window), M, E, k, seed + 29 + 1000 * rank, window)
+    ids_d = [t.to(dev) for t in ids_pool]
+    w_d = [t.to(dev) for t in w_pool]
+    ws = m.alloc_workspace(M, E, H, I, k, fmt, device=dev)
+    out = torch.full((M, H), float("nan"), dtype=torch.bfloat16, device=dev)
+    decode = M <= m.MOE_FP4_DECODE_MAX_M or m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) > 0
+    prefill = not decode
+    res = {"workload": name, "E": E, "H": H, "I": I, "top_k": k, "M": M, "fmt": gen.FMT_NAMES[fmt]}
+    # correctness first: one layer against the oracle, and a clean status word
+    m.forward(x, pw, ids_d[0], w_d[0], out=out, workspace=ws)
+    torch.cuda.synchronize()
+    res["parity"] = oracle_check(m, gen, weights, c, x, ids_pool[0], w_pool[0], out, prefill, threads)
+    res["parity"]["status_word"] = m.workspace_status(ws)
+    del weights
+    if not res["parity"]["ok"] or res["parity"]["status_word"] != 0:
+        res["timed"] = False
+        return res
+    per_layer_bytes = [layer_bytes(ids_pool[i], E, H, I, M, k, fmt)[0] for i in range(K)]
+    step_flops = sum(layer_flops(ids_pool[i], E, H, I) for i in range(K))
+    for i in range(W):
+        m.forward(x, pw, ids_d[i % K], w_d[i % K], out=out, workspace=ws)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(K):
+            m.forward(x, pw, ids_d[i], w_d[i], out=out, workspace=ws)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    R = max(15, int(min_timed_s * 1e3 / max(e0.elapsed_time(e1), 1e-3)) + 1)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(R)]
+    if ws_world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler is not None:
+        sampler.start()
+        time.sleep(0.3)
+    for a, b in evs:
+        a.record(cur)
+        g.replay()
+        b.record(cur)
+    torch.cuda.synchronize()
+    if sampler is not None:
+        sampler.pause()
+    if ws_world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    times = [a.elapsed_time(b) for a, b in evs]
+    med = st.median(times)
+    ms_max, job_units = job_time_and_units(med, step_flops if prefill else sum(per_layer_bytes), ws_world, dev)
+    res.update({"timed": True, "replays": R, "layers_per_replay": K,
+                "us_per_layer": ms_max * 1e3 / K, "us_per_layer_min": min(times) * 1e3 / K,
+                "us_per_layer_max": max(times) * 1e3 / K, "routed_bytes_per_layer": sum(per_layer_bytes) / K,
+                "flops_per_layer": step_flops / K, "job_units": job_units, "ms_per_replay": ms_max,
+                "launches_per_layer": m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) if decode else 8,
+                "plan": decode_kernel_label(m, M, E, H, I, k) if decode else
+                "prefill layer: route, x quantiser, FC1 GEMM, h quantiser, FC2 GEMM, cast (8 launches)",
+                "window": window, "prefill": prefill})
+    if do_e2e:
+        # end to end through the host-buffer entry point, one eager call per
+        # layer: H2D of x, ids and router weights, the layer, D2H of the output
+        xh = x.cpu().pin_memory()
+        idh = [t.contiguous().pin_memory() for t in ids_pool[:K]]
+        wh = [t.contiguous().pin_memory() for t in w_pool[:K]]
+        outh = torch.empty((M, H), dtype=torch.bfloat16).pin_memory()
+        hws = m.alloc_host_workspace(M, E, H, I, k, fmt, device=dev)
+        torch.cuda.synchronize()
+        for i in range(W):
+            m.forward_host(xh, pw, idh[i % K], wh[i % K], outh, hws)
+        torch.cuda.synchronize()
+        if ws_world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        for i in range(K):
+            m.forward_host(xh, pw, idh[i], wh[i], outh, hws)
+        b.record(cur)
+        torch.cuda.synchronize()
+        e2e_ms, units = job_time_and_units(a.elapsed_time(b), step_flops if prefill else sum(per_layer_bytes),
+                                           ws_world, dev)
+        res["e2e"] = {"value": units / (e2e_ms * 1e-3) / (1e12 if prefill else 1e9),
+                      "unit": "TFLOP/s" if prefill else "GB/s", "h2d_bytes_per_step": M * H * 2 + M * k * 8,
+                      "d2h_bytes_per_step": M * H * 2, "us_per_layer": e2e_ms * 1e3 / K}
+        res["e2e_status_word"] = m.workspace_status(hws)
+        del hws
+    res["_state"] = (c, seed, ids_pool, w_pool, x)
+    del pw, ws, g
+    torch.cuda.empty_cache()
+    return res
+
+
+def roofline_of(res, peak, peak_kind, traffic):
+    """The roofline object of one measured workload (decode: HBM on routed
+    bytes; prefill: min(FP4 peak, intensity x HBM) with the tensor view)."""
+    us = res["us_per_layer"]
+    if not res["prefill"]:
+        ach = res["routed_bytes_per_layer"] / (us * 1e-6) / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                "peak_source": f"hbm_gbs of {peak_kind}", "traffic": traffic, "kernel": res["plan"]}
+    from workload import gen
+    bf16, bf16_kind = load_bf16_peak()
+    fp4_peak = 6.0 * bf16
+    c = res["_state"][0]
+    E, H, I, M, fmt = c["E"], c["H"], c["I"], c["M"], c["fmt"]
+    ids_pool = res["_state"][2]
+    K = res["layers_per_replay"]
+    n_exp = [len(gen.routed_unique_experts(ids_pool[i], E)) for i in range(K)]
+    alg_bytes = sum(n * gen.expert_bytes(H, I, fmt) + 2 * M * H * 2 for n in n_exp) / K
+    ach_tf = res["flops_per_layer"] / (us * 1e-6) / 1e12
+    ach_gbs = alg_bytes / (us * 1e-6) / 1e9
+    ai = res["flops_per_layer"] / alg_bytes
+    bound = "hbm" if ai * peak * 1e9 < fp4_peak * 1e12 else "tensor"
+    return {"bound": bound, "achieved": ach_gbs if bound == "hbm" else ach_tf,
+            "peak": peak if bound == "hbm" else fp4_peak, "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "frac": ach_gbs / peak if bound == "hbm" else ach_tf / fp4_peak,
+            "peak_source": f"hbm_gbs of {peak_kind}" if bound == "hbm"
+            else f"bf16_tflops of {bf16_kind} x 6 (nominal fp4/bf16)",
+            "traffic": traffic, "kernel": res["plan"], "algorithmic_bytes_per_layer": alg_bytes,
+            "arithmetic_intensity_flop_per_byte": ai, "ceiling_tflops": min(fp4_peak, ai * peak * 1e9 / 1e12),
+            "tflops": ach_tf,
+            "tensor_view": {"achieved": ach_tf, "peak": fp4_peak, "unit": "TFLOP/s", "frac": ach_tf / fp4_peak,
+                            "peak_source": f"bf16_tflops of {bf16_kind} x 6 (nominal fp4/bf16)"}}
+
+
+def stored_traffic(args_workload, M, fmt_name, E_override):
+    prof = os.path.join(ROOT, "profiles", "decode_e512_traffic.json")
+    if E_override is not None or not os.path.exists(prof):
+        return None
+    try:
+        with open(prof) as f:
+            pd = json.load(f)
+        key = f"{args_workload}/M={M}/{fmt_name}"
+        if pd.get("decode_src_sha256") == decode_src_sha256() and key in pd.get("configs", {}):
+            return pd["configs"][key]["dram_bytes_per_layer"]
+    except Exception:
+        return None
+    return None
 
 
 def run_ours(args):
@@ -265,186 +524,74 @@ def run_ours(args):
     from fp4_weight_moe_gb300 import build as b
     from workload import gen
     b.build()
-
-    c = workload_config(args)
-    E, H, I, k, M, fmt = c["E"], c["H"], c["I"], c["top_k"], c["M"], c["fmt"]
-    seed = gen.CONFIG_SEED[args.workload]
+    m._capi.moe_fp4_debug_set_decode_family(DECODE_PLANS[args.decode_plan])
+    threads = affinity_cores()
     K, W = args.steps, args.warmup
-    window = max(1, min(WINDOW, E // (k * M)))
-    weights = gen.make_expert_weights(E, H, I, fmt, seed, device=dev)
-    pw = m.prepare_weights(weights, E, H, I, fmt)
-    del weights
-    x = gen.draw_activations(M, H, seed + 17, device=dev)
-    ids_pool, w_pool = gen.draw_routing_pool(max(K, window), M, E, k, seed + 29 + 1000 * rank, window)
-    ids_d = [t.to(dev) for t in ids_pool]
-    w_d = [t.to(dev) for t in w_pool]
-    m.reserve_workspace(M, E, H, I, k, fmt)
-    out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
-    torch.cuda.synchronize()
-
-    # eager warm-up, then capture the K timed layers in one graph
-    for i in range(W):
-        m.forward(x, pw, ids_d[i % K], w_d[i % K], out=out)
-    torch.cuda.synchronize()
-    s = torch.cuda.Stream(device=dev)
-    s.wait_stream(torch.cuda.current_stream())
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        for i in range(K):
-            m.forward(x, pw, ids_d[i], w_d[i], out=out)
-    torch.cuda.synchronize()
-    g.replay()  # untimed: graph upload and one more warm pass
-    torch.cuda.synchronize()
-
-    per_layer_bytes = [layer_bytes(ids_pool[i], E, H, I, M, k, fmt)[0] for i in range(K)]
-    step_bytes = sum(per_layer_bytes)
-    # batches past the decode band that run as decode-band chunks report like the decode band
-    prefill = M > m.MOE_FP4_DECODE_MAX_M and m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) == 0
-    step_flops = sum(layer_flops(ids_pool[i], E, H, I) for i in range(K))
-
     sampler = ClockSampler(local)
-    if ws > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    sampler.start()
-    time.sleep(0.3)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    cur = torch.cuda.current_stream()
-    ev0.record(cur)
-    g.replay()
-    ev1.record(cur)
-    torch.cuda.synchronize()
-    clocks = sampler.stop()
-    if ws > 1:
-        dist.barrier()
-    ms = ev0.elapsed_time(ev1)
-    ms_max, job_units = job_time_and_units(ms, step_flops if prefill else step_bytes, ws, dev)
-    ms_per_step = ms_max / K
-    value = job_units / (ms_max * 1e-3) / (1e12 if prefill else 1e9)
-
-    e2e_value = None
-    # end to end through the C ABI's host-buffer entry point, one eager call
-    # per layer: H2D of x, ids and router weights, the layer, D2H of the
-    # output, all enqueued by moe_fp4_forward_host on the current stream.
-    xh = x.cpu().pin_memory()
-    idh = [t.contiguous().pin_memory() for t in ids_pool[:K]]
-    wh = [t.contiguous().pin_memory() for t in w_pool[:K]]
-    outh = torch.empty((M, H), dtype=torch.bfloat16).pin_memory()
-    hws = m.alloc_host_workspace(M, E, H, I, k, fmt, device=dev)
-    torch.cuda.synchronize()
-
-    def e2e_step(i):
-        m.forward_host(xh, pw, idh[i], wh[i], outh, hws)
-
-    e2e_ms = float("nan")
-    if not args.no_e2e:
-        for i in range(W):
-            e2e_step(i % K)
-        torch.cuda.synchronize()
-        if ws > 1:
-            dist.barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(cur)
-        for i in range(K):
-            e2e_step(i)
-        e1.record(cur)
-        torch.cuda.synchronize()
-        e2e_ms, job_units = job_time_and_units(e0.elapsed_time(e1), step_flops if prefill else step_bytes, ws, dev)
-        e2e_value = job_units / (e2e_ms * 1e-3) / (1e12 if prefill else 1e9)
-
+    ov = {"M": args.M, "E": args.E, "fmt": None if args.fmt is None else (0 if args.fmt == "mxfp4" else 1)}
+    head = measure(m, args.workload, ov, K, W, dev, rank, ws, args.min_timed_s, threads, not args.no_e2e, sampler)
+    c, seed, ids_pool, w_pool, x = head.pop("_state")
+    E, H, I, k, M, fmt = c["E"], c["H"], c["I"], c["top_k"], c["M"], c["fmt"]
     peak, peak_kind = load_peaks()
-    achieved = (step_bytes / K) / (ms_per_step * 1e-3) / 1e9
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "decode_e512_traffic.json")
-    if os.path.exists(prof):
-        try:
-            with open(prof) as f:
-                pd = json.load(f)
-            key = f"{args.workload}/M={M}/{gen.FMT_NAMES[fmt]}"
-            if (args.E is None and pd.get("decode_src_sha256") == decode_src_sha256()
-                    and key in pd.get("configs", {})):
-                traffic = pd["configs"][key]["dram_bytes_per_layer"]
-        except Exception:
-            traffic = None
-
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K, "warmup": W,
-        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp32-accum e2m1 x bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "E": E, "H": H, "I": I, "top_k": k, "M": M,
-                   "fmt": gen.FMT_NAMES[fmt],
-                   "l2": f"routing draws rotate; no expert repeats within {window} layers "
-                         f"({window} x {per_layer_bytes[0] / 1e6:.1f} MB)",
-                   "timing": "K layers in one CUDA graph, one replay, CUDA events"},
-        "us_per_layer": ms_per_step * 1e3,
-        "routed_bytes_per_layer": step_bytes / K,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": f"hbm_gbs of {peak_kind}", "traffic": traffic,
-                     "kernel": decode_kernel_label(m, M, E, H, I, k)},
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": M * H * 2 + M * k * 8,
-                "d2h_bytes_per_step": M * H * 2, "us_per_layer": e2e_ms * 1e3 / K},
-        "gpu_launches": m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) * K,
-        "clocks": clocks,
-    }
-
-    if prefill:
-        # Roofline = min(FP4 tensor peak, arithmetic intensity x HBM): the
-        # layer's algorithmic bytes are the routed experts' weights and
-        # scales plus x read and out written once (the intermediates could
-        # stay on chip).  At prefill_e128 the intensity (~870 flop/B) is below
-        # the ridge (FP4 peak / HBM), so HBM bounds it; the FP4-peak view is
-        # reported beside it.  FP4 peak: measured BF16 dense peak x the
-        # nominal FP4/BF16 ratio (13.5 / 2.25 = 6).
-        bf16, bf16_kind = load_bf16_peak()
-        fp4_peak = 6.0 * bf16
-        ach_tf = (step_flops / K) / (ms_per_step * 1e-3) / 1e12
-        n_exp = [len(gen.routed_unique_experts(ids_pool[i], E)) for i in range(K)]
-        alg_bytes = sum(n * gen.expert_bytes(H, I, fmt) + 2 * M * H * 2 for n in n_exp) / K
-        ach_gbs = alg_bytes / (ms_per_step * 1e-3) / 1e9
-        ai = (step_flops / K) / alg_bytes
-        line["unit"] = "TFLOP/s"
-        line["dtype"] = "e2m1 x e2m1 (nvfp4 activations), fp32 accumulate"
-        line["config"]["l2"] = f"inputs larger than L2 (expert weights {E * gen.expert_bytes(H, I, fmt) / 1e9:.2f} GB)"
-        line["flops_per_layer"] = step_flops / K
-        line["algorithmic_bytes_per_layer"] = alg_bytes
-        bound = "hbm" if ai * peak * 1e9 < fp4_peak * 1e12 else "tensor"
-        line["roofline"] = {"bound": bound, "achieved": ach_gbs if bound == "hbm" else ach_tf,
-                            "peak": peak if bound == "hbm" else fp4_peak,
-                            "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
-                            "frac": ach_gbs / peak if bound == "hbm" else ach_tf / fp4_peak,
-                            "peak_source": f"hbm_gbs of {peak_kind}" if bound == "hbm"
-                            else f"bf16_tflops of {bf16_kind} x 6 (nominal fp4/bf16)",
-                            "traffic": None, "kernel": "prefill layer (8 launches), per layer",
-                            "arithmetic_intensity_flop_per_byte": ai,
-                            "ceiling_tflops": min(fp4_peak, ai * peak * 1e9 / 1e12),
-                            "tensor_view": {"achieved": ach_tf, "peak": fp4_peak, "unit": "TFLOP/s",
-                                            "frac": ach_tf / fp4_peak,
-                                            "peak_source": f"bf16_tflops of {bf16_kind} x 6 (nominal fp4/bf16)"}}
-        line["e2e"]["unit"] = "TFLOP/s"
-        line["gpu_launches"] = 8 * K
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline and prefill:
-        # the oracle on a bounded sample: the first 4 tokens of the first draw
-        import oracle
-        tok = [0, 1, 2, 3]
-        ids_s = ids_pool[0][tok]
-        used = gen.routed_unique_experts(ids_s, E)
-        sub = gen.make_expert_weights(E, H, I, fmt, seed, device="cpu", experts=used)
-        remap = {e: j for j, e in enumerate(used)}
-        ids_c = [[remap.get(e, -1) for e in row] for row in ids_s.tolist()]
-        t1 = time.perf_counter()
-        oracle.forward_prefill(x.cpu()[tok], sub, ids_c, w_pool[0][tok], len(used), H, I, k)
-        secs = time.perf_counter() - t1
-        fl = layer_flops(ids_s, E, H, I)
-        line["cpu_baseline"] = {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": min(oracle.num_threads(), 4),
-                                "kind": "oracle", "sample": f"4 tokens of {args.workload} (mirrored activation "
-                                                            f"quantisation), {secs:.1f} s"}
-    elif rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        done, secs, nbytes, threads = oracle_layers(c, seed, ids_pool, w_pool, x.cpu(), args.cpu_seconds, K)
-        line["cpu_baseline"] = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                                "sample": f"{done} layers of {args.workload} (one routing draw each), "
-                                          f"{secs:.1f} s; us/layer {secs / done * 1e6:.0f}"}
+    line = {"metric": METRIC, "n_gpus": ws, "steps": K, "warmup": W, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp32-accum e2m1 x bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "E": E, "H": H, "I": I, "top_k": k, "M": M,
+                       "fmt": gen.FMT_NAMES[fmt],
+                       "l2": f"routing draws rotate; no expert repeats within {head.get('window')} layers "
+                             f"({head.get('window')} x {head.get('routed_bytes_per_layer', 0) / 1e6:.1f} MB)",
+                       "timing": "K layers in one CUDA graph, replayed R times between CUDA events; "
+                                 "median replay (min/max beside it)"},
+            "parity": head["parity"]}
+    if not head["timed"]:
+        line.update({"value": None, "unit": "GB/s", "ms_per_step": None,
+                     "error": "the oracle check failed: not timed"})
+    else:
+        prefill = head["prefill"]
+        head["_state"] = (c, seed, ids_pool, w_pool, x)
+        traffic = None if prefill else stored_traffic(args.workload, M, gen.FMT_NAMES[fmt], args.E)
+        rl = roofline_of(head, peak, peak_kind, traffic)
+        head.pop("_state")
+        line.update({"value": head["job_units"] / (head["ms_per_replay"] * 1e-3) / (1e12 if prefill else 1e9),
+                     "unit": "TFLOP/s" if prefill else "GB/s", "ms_per_step": head["ms_per_replay"] / K,
+                     "us_per_layer": head["us_per_layer"], "us_per_layer_min": head["us_per_layer_min"],
+                     "us_per_layer_max": head["us_per_layer_max"], "replays": head["replays"],
+                     "routed_bytes_per_layer": head["routed_bytes_per_layer"], "roofline": rl,
+                     "e2e": head.get("e2e"),
+                     "gpu_launches": head["launches_per_layer"] * K * head["replays"]})
+        if prefill:
+            line["dtype"] = "e2m1 x e2m1 (nvfp4 activations), fp32 accumulate"
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and head["timed"] and not head["prefill"]:
+        done, secs, nbytes, used_threads = oracle_layers(c, seed, ids_pool, w_pool, x.cpu(), args.cpu_seconds, K,
+                                                         threads)
+        d1, s1, b1, _ = oracle_layers(c, seed, ids_pool, w_pool, x.cpu(), 0.0, 1, 1)
+        line["cpu_baseline"] = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": used_threads,
+                                "kind": "oracle",
+                                "sample": f"{done} layers of {args.workload} (one routing draw each), {secs:.2f} s "
+                                          f"on {used_threads} threads; us/layer {secs / done * 1e6:.0f}",
+                                "single_thread": {"value": b1 / s1 / 1e9, "unit": "GB/s", "cores": 1,
+                                                  "us_per_layer": s1 / d1 * 1e6}}
+    if not args.no_sweep:
+        sweep = []
+        for label, name, sov in SWEEP:
+            if name == args.workload and all(sov.get(kk, c[kk]) == c[kk] for kk in ("M", "fmt")) \
+                    and args.E is None:
+                continue  # the headline itself
+            try:
+                r = measure(m, name, sov, K, W, dev, rank, ws, args.min_timed_s / 4, threads, not args.no_e2e,
+                            sampler)
+            except Exception as exc:  # report, keep going
+                sweep.append({"config": label, "workload": name, "error": repr(exc)[:300]})
+                torch.cuda.empty_cache()
+                continue
+            ent = {"config": label}
+            if r["timed"]:
+                r["roofline"] = roofline_of(r, peak, peak_kind, None)
+            r.pop("_state", None)
+            r.pop("job_units", None)
+            ent.update(r)
+            sweep.append(ent)
+        line["sweep"] = sweep
+    line["clocks"] = sampler.stop()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

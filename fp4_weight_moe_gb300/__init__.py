@@ -219,3 +219,16 @@ def debug_dequant(pw: PreparedWeights, which: int, expert: int, stream=None) -> 
     _capi.moe_fp4_debug_dequant(_ptr(w), _ptr(s), which, expert, pw.E, pw.H, pw.I, pw.fmt, _ptr(out),
                                 _stream(stream))
     return out
+
+
+def workspace_status(workspace: Optional[torch.Tensor] = None, clear: bool = False, stream=None) -> int:
+    """Status word of a workspace (None: the reserved library workspace): 0,
+    or bits of kernel waits that gave up (the outputs since the last clear
+    are not valid).  Synchronises ``stream``; ``clear`` resets the word."""
+    dev = workspace.device if workspace is not None else None
+    return _capi.moe_fp4_workspace_status(_ptr(workspace), clear, _stream(stream, dev))
+
+
+def noalloc_status(clear: bool = False, stream=None) -> int:
+    """Status word of moe_fp4_forward_noalloc's scratch array on the current device."""
+    return _capi.moe_fp4_noalloc_status(clear, _stream(stream))

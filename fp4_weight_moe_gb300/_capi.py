@@ -27,6 +27,8 @@ MOE_FP4_NOALLOC_SCRATCH_BYTES = 16 << 20
 MOE_FP4_ACT_SILU = 0
 MOE_FP4_ACT_GELU_TANH = 1
 MOE_FP4_ACT_SWIGLUOAI = 2
+MOE_FP4_STATUS_OK = 0
+MOE_FP4_STATUS_TEST_WAIT = 8192
 
 
 class MoeFp4Activation(ctypes.Structure):
@@ -48,6 +50,7 @@ SIGNATURES = {
     "moe_fp4_prepare_weights": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_fp4_unprepare_weights": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "moe_fp4_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
+    "moe_fp4_workspace_zero_bytes": (_Z, [_I, _I, _I, _I, _I]),
     "moe_fp4_reserve_workspace": (_I, [_I, _I, _I, _I, _I, _I, _P]),
     "moe_fp4_release_workspace": (_I, []),
     "moe_fp4_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
@@ -70,6 +73,10 @@ SIGNATURES = {
     "moe_fp4_debug_route_workspace_bytes": (_Z, [_I, _I, _I]),
     "moe_fp4_debug_quant_mxfp8_rows": (_I, [_P, _I, _I, _P, _P, _P]),
     "moe_fp4_debug_quant_rows": (_I, [_P, _I, _I, _P, _P, _P, _P]),
+    "moe_fp4_workspace_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint32), _I, _P]),
+    "moe_fp4_noalloc_status": (_I, [ctypes.POINTER(ctypes.c_uint32), _I, _P]),
+    "moe_fp4_debug_wait_timeout": (_I, [_P, ctypes.c_uint, _P]),
+    "moe_fp4_debug_decode_plan": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
 }
 
 _lock = threading.Lock()
@@ -141,6 +148,10 @@ def moe_fp4_unprepare_weights(w13, s13, w2, s2, E, H, I, fmt, w13_l, s13_l, g13,
 
 def moe_fp4_workspace_bytes(M_max, E, H, I, top_k, fmt) -> int:
     return int(_load().moe_fp4_workspace_bytes(M_max, E, H, I, top_k, fmt))
+
+
+def moe_fp4_workspace_zero_bytes(E, H, I, top_k, fmt) -> int:
+    return int(lib().moe_fp4_workspace_zero_bytes(E, H, I, top_k, fmt))
 
 
 def moe_fp4_reserve_workspace(M_max, E, H, I, top_k, fmt, stream):
@@ -240,6 +251,29 @@ def moe_fp4_debug_quant_mxfp8_rows(inp, rows, K, q, s, stream):
 
 def moe_fp4_debug_quant_rows(inp, rows, K, q, s, G, stream):
     return _check("moe_fp4_debug_quant_rows", _load().moe_fp4_debug_quant_rows(inp, rows, K, q, s, G, stream))
+
+
+def moe_fp4_workspace_status(ws, clear: bool, stream) -> int:
+    v = ctypes.c_uint32(0)
+    _check("moe_fp4_workspace_status", lib().moe_fp4_workspace_status(ws, ctypes.byref(v), int(bool(clear)), stream))
+    return v.value
+
+
+def moe_fp4_noalloc_status(clear: bool, stream) -> int:
+    v = ctypes.c_uint32(0)
+    _check("moe_fp4_noalloc_status", lib().moe_fp4_noalloc_status(ctypes.byref(v), int(bool(clear)), stream))
+    return v.value
+
+
+def moe_fp4_debug_wait_timeout(status_word, polls: int, stream):
+    _check("moe_fp4_debug_wait_timeout", lib().moe_fp4_debug_wait_timeout(status_word, polls, stream))
+
+
+def moe_fp4_debug_decode_plan(M, E, H, I, top_k):
+    """(C, s1, Q, cap) of the single-launch plan on the current device, zeros if none."""
+    v = (ctypes.c_int * 4)()
+    _check("moe_fp4_debug_decode_plan", lib().moe_fp4_debug_decode_plan(M, E, H, I, top_k, v))
+    return tuple(v)
 
 
 def raw_status(name: str, *args) -> int:

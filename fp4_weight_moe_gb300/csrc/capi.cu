@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace moe_fp4 {
 cudaError_t launch_prepare(const void* w13_l, const void* s13_l, const float* g13, const void* w2_l,
@@ -14,6 +15,7 @@ cudaError_t launch_prepare(const void* w13_l, const void* s13_l, const float* g1
 cudaError_t launch_debug_dequant(const void* w, const void* s, int which, int e, int E, int H, int I, int fmt,
                                  float* out, cudaStream_t st);
 size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int fmt, int num_sms);
+size_t decode_sync_bytes(int H, int I, int top_k);
 cudaError_t launch_debug_gemm(const void* a_q, const void* a_sf, const void* b_q, const void* b_sf, float* d,
                               int M_rows, int N_rows, int K, uint32_t* status, cudaStream_t st, int* cu_err);
 size_t prefill_workspace_bytes(int M, int E, int H, int I, int top_k);
@@ -29,12 +31,45 @@ extern std::atomic<int> g_decode_family;
 bool decode_gemv_fits(int M, int E, int H, int I, int top_k);
 int decode_launches(int M, int E, int H, int I, int top_k);
 int decode_family_of(int M, int E, int H, int I, int top_k);
+bool decode_fused_plan(int M, int H, int I, int top_k, int* C, int* s1, int* Q, int* cap);
 cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                           const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
                           int top_k, int fmt, const ActParams& act, void* ws, int num_sms, cudaStream_t st);
 }  // namespace moe_fp4
 
 using namespace moe_fp4;
+
+namespace {
+// Test support: one thread waits on an mbarrier that nothing arrives on,
+// polling it `polls` times, so that the bounded wait gives up and records
+// MOE_FP4_STATUS_TEST_WAIT in the status word.
+__global__ void wait_timeout_kernel(uint32_t* status, uint32_t polls) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  (void)mbar_wait_for(&bar, 0, status, MOE_FP4_STATUS_TEST_WAIT, polls);
+}
+
+// Copy the status word at `word` (device) to *flags and, if asked, clear it;
+// the stream is synchronised.
+int read_status_word(void* word, uint32_t* flags, int clear, cudaStream_t st);
+}  // namespace
+
+namespace moe_fp4 {
+// Shape limits shared by every entry point that runs the layer: a known
+// format, positive sizes, E <= 65536, top_k <= 16, H % 256 == 0, I % 64 == 0,
+// and one expert projection's elements (2I x H) within 2^31, so that the
+// kernels' 32-bit element offsets cannot overflow.
+int check_layer_shape(int E, int H, int I, int top_k, int fmt) {
+  if (fmt != MOE_FP4_MXFP4 && fmt != MOE_FP4_NVFP4) return MOE_FP4_EINVAL;
+  if (E <= 0 || H <= 0 || I <= 0 || top_k <= 0) return MOE_FP4_EINVAL;
+  if (E > 65536 || top_k > 16) return MOE_FP4_EUNSUPPORTED;
+  if (H % 256 != 0 || I % 64 != 0) return MOE_FP4_EUNSUPPORTED;
+  if ((long long)H * 2 * I > (1LL << 31)) return MOE_FP4_EUNSUPPORTED;
+  return MOE_FP4_OK;
+}
+}  // namespace moe_fp4
 
 namespace {
 
@@ -65,14 +100,18 @@ int device_sms(int* sms) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-int check_shape(int E, int H, int I, int top_k, int fmt) {
-  if (fmt != MOE_FP4_MXFP4 && fmt != MOE_FP4_NVFP4) return MOE_FP4_EINVAL;
-  if (E <= 0 || H <= 0 || I <= 0 || top_k <= 0) return MOE_FP4_EINVAL;
-  if (E > 65536 || top_k > 16) return MOE_FP4_EUNSUPPORTED;
-  if (H % 256 != 0 || I % 64 != 0) return MOE_FP4_EUNSUPPORTED;
-  if ((long long)H * 2 * I > (1LL << 31)) return MOE_FP4_EUNSUPPORTED;
+int read_status_word(void* word, uint32_t* flags, int clear, cudaStream_t st) {
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, word, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync(word, 0, sizeof(uint32_t), st);
+  if (e == cudaSuccess && clear) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail_cuda(e);
+  *flags = v;
   return MOE_FP4_OK;
 }
+
+int check_shape(int E, int H, int I, int top_k, int fmt) { return check_layer_shape(E, H, I, top_k, fmt); }
 
 // Extra limits of the prefill band (M > MOE_FP4_DECODE_MAX_M).
 int check_prefill(int M, int E, int I, int top_k, int fmt) {
@@ -200,6 +239,11 @@ int moe_fp4_unprepare_weights(const void* w13, const void* s13, const void* w2, 
                                  const_cast<void*>(w13), const_cast<void*>(s13), const_cast<void*>(w2),
                                  const_cast<void*>(s2), static_cast<cudaStream_t>(stream), true);
   return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
+}
+
+size_t moe_fp4_workspace_zero_bytes(int E, int H, int I, int top_k, int fmt) {
+  if (check_shape(E, H, I, top_k, fmt) != MOE_FP4_OK) return 0;
+  return 256 + decode_sync_bytes(H, I, top_k);
 }
 
 size_t moe_fp4_workspace_bytes(int M_max, int E, int H, int I, int top_k, int fmt) {
@@ -465,8 +509,32 @@ int moe_fp4_forward_host(const void* x_bf16, const void* w13, const void* s13, c
   return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
 }
 
+int moe_fp4_workspace_status(const void* workspace, uint32_t* flags, int clear, void* stream) {
+  if (!flags) return MOE_FP4_EINVAL;
+  void* ws = const_cast<void*>(workspace);
+  if (!ws) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev < 0 || dev >= 64) return MOE_FP4_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_ws_mutex);
+    ws = g_ws[dev].ptr;
+  }
+  if (!ws) return MOE_FP4_EWORKSPACE;
+  if ((uintptr_t)ws & 255u) return MOE_FP4_EWORKSPACE;
+  return read_status_word(ws, flags, clear, static_cast<cudaStream_t>(stream));
+}
+
+int moe_fp4_debug_wait_timeout(void* status_word, unsigned polls, void* stream) {
+  if (!status_word || ((uintptr_t)status_word & 3u)) return MOE_FP4_EINVAL;
+  if (polls == 0 || polls > (1u << 20)) return MOE_FP4_EINVAL;
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint32_t*>(status_word), polls);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
+}
+
 int moe_fp4_debug_set_decode_family(int family, int* previous) {
-  if (family < 0 || family > 2) return MOE_FP4_EINVAL;
+  if (family < 0 || family > 3) return MOE_FP4_EINVAL;
   const int old = g_decode_family.exchange(family);
   if (previous) *previous = old;
   return MOE_FP4_OK;
@@ -482,6 +550,22 @@ int moe_fp4_debug_set_mid_band(int mode, int* previous) {
 int moe_fp4_debug_decode_family_of(int M, int E, int H, int I, int top_k) {
   if (M < 1 || M > MOE_FP4_DECODE_MAX_M || check_shape(E, H, I, top_k, MOE_FP4_NVFP4) != MOE_FP4_OK) return 0;
   return decode_family_of(M, E, H, I, top_k);
+}
+
+int moe_fp4_debug_decode_plan(int M, int E, int H, int I, int top_k, int* plan) {
+  if (!plan) return MOE_FP4_EINVAL;
+  plan[0] = plan[1] = plan[2] = plan[3] = 0;
+  if (M < 1 || M > MOE_FP4_DECODE_MAX_M) return MOE_FP4_EINVAL;
+  const int st = check_shape(E, H, I, top_k, MOE_FP4_NVFP4);
+  if (st != MOE_FP4_OK) return st;
+  int C = 0, s1 = 0, Q = 0, cap = 0;
+  if (decode_fused_plan(M, H, I, top_k, &C, &s1, &Q, &cap)) {
+    plan[0] = C;
+    plan[1] = s1;
+    plan[2] = Q;
+    plan[3] = cap;
+  }
+  return MOE_FP4_OK;
 }
 
 int moe_fp4_debug_decode_gemv_fits(int M, int E, int H, int I, int top_k) {

@@ -130,6 +130,11 @@ struct TcArgs {
   int split;   // FC1: K ranges per w13 tile; FC2: CTAs (cluster size) per w2 tile
   int N;      // B rows per item (accumulator columns)
   ActParams act;  // FC1's gated activation
+  // single-launch layer only: h-ready counters and reader counts, both
+  // [owner][K stage of h], and the K ranges per w13 tile
+  uint32_t* hflag;
+  uint32_t* hused;
+  int s1;
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -791,6 +796,456 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   }
 }
 
+// ---------------------------------------------------------------- single launch
+// The whole decode layer in one launch, for shapes whose work fits one
+// resident grid with every CTA's weight tiles in flight at once (see
+// launch_decode_fused).  A CTA owns one FC1 share (a K range of one 128-row
+// w13 tile of one routed expert) and one FC2 share (some of the (expert, K
+// stage) items of one 128-row w2 tile); its shared-memory ring has a slot for
+// every item, so the producer issues all of its weight tiles as the CTA
+// starts and FC2's weights are in shared memory before h exists.  The
+// tiny-decode PR keeps FC1 and FC2 as two launches and found one cooperative
+// launch slower because of its grid synchronisation (b12x PR #22, section
+// Notes); here nothing waits for the whole grid: an FC2 item waits only for
+// the h values it reads, published per (expert, w13 tile, K range) by a flag
+// in global memory, and both reductions stay inside thread-block clusters.
+//
+// Cluster of C CTAs (rank r): FC1 sub-clusters of s1 CTAs (the K ranges of one
+// w13 tile; C / s1 tiles per cluster), FC2 the whole cluster (the items of
+// one w2 tile dealt round-robin).  Unit index of an FC1 share: cluster * (C /
+// s1) + r / s1 over the (owner, w13 tile) pairs; w2 tile: the cluster index.
+//
+// Roles (352 threads): warp 0 lane 0 issues every weight TMA at the start;
+// warps 1-2 issue the MMAs (alternate items, each into its own accumulator
+// group); warps 3-6 build the activation terms (x for FC1's items, h for
+// FC2's, items or (item, token) pairs spread over the four warps) and write
+// both scale sets of every item into tensor memory (each warp its lane
+// quarter); warps 7-10 drain the accumulators, then run the FC1 and FC2
+// reductions.
+//
+// h-ready protocol: the CTA that reduces pairs p = r1 mod s1 of an FC1 unit
+// writes their h and adds 1 (release, GPU scope) to the counter of the
+// (expert, 256-wide K stage of h) the unit belongs to; the stage is complete
+// when its counter reaches (its w13 tiles) x s1.  One lane of each FC2
+// builder polls that counter (acquire) before the warp loads h.  Every
+// (expert, K stage) item is read by exactly one CTA of each w2 tile; after
+// its items are published each reader counts itself in a second counter, and
+// the last reader sets both back to zero, so every call ends with them all at
+// zero (the workspace starts with them zero).
+
+// Ring geometry of the single launch for N activation-term rows (16 up to 4
+// tokens, 32 up to 8): slot = weight tile (128 rows x 256 K), the B tile (N
+// rows, 128-byte swizzle), the weight scale chunks (4 K-groups) and the B
+// scales (row n's 16 bytes at 16n), rounded to 1 KB; as many slots as fit
+// one CTA per SM, and tensor memory for one accumulator group of N columns
+// plus 32 scale columns per slot.
+template <int kN>
+struct FzCfg {
+  static constexpr uint32_t kB = kN * 128;
+  static constexpr uint32_t kSFA = kSlotA + kB;
+  static constexpr uint32_t kSFB = kSFA + 4 * kChunkBytes;
+  static constexpr uint32_t kSlot = (kSFB + 512 + 1023) / 1024 * 1024;
+  static constexpr int kRing = kN == 16 ? 10 : 8;
+  static constexpr uint32_t kTmemSF = kRing * kN;  // scale columns after the accumulator groups
+  static_assert(kTmemSF + 32 * kRing <= 512, "tensor memory");
+};
+
+struct SmemFz {
+  float part1[8 * 144];            // FC1 partials received from the sub-cluster
+  float part2[8 * 144];            // FC2 partials received from the cluster
+  float G[10][8][kTerms];          // term multipliers per (item, token)
+  int ids[kMaxSlotsTc];
+  float tw[kMaxSlotsTc];
+  int own[kMaxSlotsTc];            // first slot naming each valid expert, in slot order
+  int own_cnt[4];
+  float wtok[8];                   // FC1: router weight of the unit's expert per token
+  float g3[3];                     // FC1: gate, up, down multipliers of the expert
+  uint32_t routed;                 // FC1: tokens routed to the expert (bit mask)
+  uint64_t fullA[10];              // weight tile + its scale chunks landed (TMA)
+  uint64_t ready[10];              // activation terms, both scale sets and G in place (builders)
+  uint64_t done[10];               // MMAs of the item complete
+  uint64_t red1, red2;             // FC1 / FC2 partial rows this CTA reduces have landed
+  uint32_t tmem;
+};
+template <int kN>
+constexpr uint32_t fz_smem() {
+  return FzCfg<kN>::kRing * FzCfg<kN>::kSlot + sizeof(SmemFz) + 1024;
+}
+static_assert(fz_smem<16>() <= 227 * 1024 && fz_smem<32>() <= 227 * 1024, "shared memory");
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Polls of an h-ready counter before the builder gives up (each poll is an
+// L2 round trip of a few hundred nanoseconds: about two seconds in all).
+constexpr uint32_t kFlagPollLimit = 1u << 22;
+constexpr uint32_t kErrHFlag = 2048u, kErrFzRed = 4096u;
+
+// One (item, token) activation row: the kTerms NVFP4 terms of 256 values
+// (v, zero past `act` lanes) into the item's slot, its multipliers into G.
+__device__ __forceinline__ void fz_build_row(float (&v)[8], uint8_t* slotp, uint32_t sfa_off, float* G, int token,
+                                             int lane, bool act) {
+  float m = fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
+                  fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  const float G1 = term_g1(m);
+  if (lane < kTerms) G[lane] = G1 * __uint_as_float((127u - 2u * lane) << 23);
+  emit_stage_terms(v, G1, slotp + kSlotA, slotp + sfa_off + 4 * kChunkBytes, token, lane, act);
+}
+
+template <int kN>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_constant__ CUtensorMap map2, TcArgs a) {
+  using Cfg = FzCfg<kN>;
+  constexpr int R = Cfg::kRing;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  SmemFz& S = *reinterpret_cast<SmemFz*>(ring + R * Cfg::kSlot);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int M = a.M, H = a.H, I = a.I, n = a.n_slots;
+  const int C = a.split, s1 = a.s1;
+  const int rank = (int)cluster_rank();
+  const int q = blockIdx.x / C, sub = rank / s1, r1 = rank % s1;
+  const int tiles1 = I / 64, ns2 = (I + 255) / 256, tiles2 = H / 128, nk = H / 256;
+  const int cpo = (64 + s1 - 1) / s1, rpo1 = 2 * cpo;  // FC1 pairs per owner, partial rows per sender
+  const int rpo2 = (128 + C - 1) / C;                   // FC2 rows per owner
+  const bool is_epi = warp >= kEpiWarp0;
+  const bool is_quant = warp >= kQuantWarp0 && warp < kQuantWarp0 + kQuantWarps;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < R; ++s) {
+      mbar_init(&S.fullA[s], 1);
+      mbar_init(&S.ready[s], kQuantWarps);
+      mbar_init(&S.done[s], 1);
+    }
+    mbar_init(&S.red1, 1);
+    mbar_init(&S.red2, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&map13);
+    tma_prefetch_desc(&map2);
+  }
+  // cluster phase 1: this CTA runs and its barriers are initialised (awaited
+  // before any remote store)
+  cluster_arrive_release();
+  if (warp == kMmaWarp0) tmem_alloc(&S.tmem, 512);
+  // The next kernel may start its prologue; it waits (griddepcontrol.wait)
+  // for this whole grid before it reads anything this launch writes.
+  pdl_launch_dependents();
+  pdl_wait();  // x and the routing come from the previous kernel
+
+  // ---- routing: owners (the first slot naming each valid expert, in slot order)
+  bool own_j = false;
+  uint32_t bal = 0;
+  if (warp < 4) {
+    const int j = 32 * warp + lane;
+    const int id = j < n ? route_id(a.ids, j, a.ids64, a.E) : -1;
+    S.ids[j] = id;
+    S.tw[j] = j < n ? ld_nc_f32(a.tw + j) : 0.f;
+    const bool valid = j < n && id >= 0 && id < a.E;
+    const uint32_t mm = __match_any_sync(0xffffffffu, valid ? id : -1 - lane);
+    own_j = valid && (mm & ((1u << lane) - 1u)) == 0;  // earlier 32-slot chunks are checked below
+  }
+  __syncthreads();
+  if (warp < 4) {
+    const int j = 32 * warp + lane;
+    for (int c = 0; own_j && c < warp; ++c)
+      for (int k = 0; k < 32; ++k) own_j = own_j && S.ids[32 * c + k] != S.ids[j];
+    bal = __ballot_sync(0xffffffffu, own_j);
+    if (lane == 0) S.own_cnt[warp] = __popc(bal);
+  }
+  __syncthreads();
+  if (own_j) {
+    const int j = 32 * warp + lane;
+    int base = 0;
+    for (int c = 0; c < warp; ++c) base += S.own_cnt[c];
+    S.own[base + __popc(bal & ((1u << lane) - 1u))] = j;
+  }
+  const int n_own = S.own_cnt[0] + S.own_cnt[1] + S.own_cnt[2] + S.own_cnt[3];
+  __syncthreads();
+
+  // ---- this CTA's work: an FC1 share, then an FC2 share (at most R items)
+  const int u1 = q * (C / s1) + sub;
+  const bool valid1 = u1 < n_own * tiles1;
+  const int o1 = valid1 ? u1 / tiles1 : 0, tile1 = valid1 ? u1 % tiles1 : 0;
+  const int e1 = valid1 ? S.ids[S.own[o1]] : -1;
+  const int k0 = r1 * nk / s1;
+  const int n1 = valid1 ? (r1 + 1) * nk / s1 - k0 : 0;
+  const int t2 = q;
+  const bool valid2 = t2 < tiles2;
+  const int T2 = n_own * ns2;
+  const int n2 = valid2 && T2 > rank ? (T2 - rank + C - 1) / C : 0;
+  const int n_items = n1 + n2 < R ? n1 + n2 : R;  // (the plan keeps n1 + n2 <= R)
+  auto item_o = [&](int i) { return (rank + C * (i - n1)) % n_own; };
+  auto item_s2 = [&](int i) { return (rank + C * (i - n1)) / n_own; };
+  auto item_groups = [&](int i) {
+    if (i < n1) return 4;
+    const int rem = tiles1 - 4 * item_s2(i);
+    return rem < 4 ? rem : 4;
+  };
+  const uint64_t KG1 = (uint64_t)(H / 64), KG2 = (uint64_t)(I / 64);
+  if (threadIdx.x == 0) {
+    // every weight tile of the CTA, FC1's first
+    for (int i = 0; i < n_items; ++i) {
+      uint8_t* slotp = ring + i * Cfg::kSlot;
+      const int ng = item_groups(i);
+      mbar_arrive_expect_tx(&S.fullA[i], kSlotA + (uint32_t)ng * kChunkBytes);
+      if (i < n1) {
+        const int st = k0 + i;
+        const uint8_t* sfa = a.s13 + (((uint64_t)e1 * tiles1 + tile1) * KG1 + 4 * (uint64_t)st) * kChunkBytes;
+        tma_load_2d(slotp, &map13, st * 128, e1 * 2 * I + tile1 * 128, &S.fullA[i]);
+        bulk_load(slotp + Cfg::kSFA, sfa, (uint32_t)ng * kChunkBytes, &S.fullA[i]);
+      } else {
+        const int st = item_s2(i), e = S.ids[S.own[item_o(i)]];
+        const uint8_t* sfa = a.s2 + (((uint64_t)e * tiles2 + t2) * KG2 + 4 * (uint64_t)st) * kChunkBytes;
+        tma_load_2d(slotp, &map2, st * 128, e * H + t2 * 128, &S.fullA[i]);
+        bulk_load(slotp + Cfg::kSFA, sfa, (uint32_t)ng * kChunkBytes, &S.fullA[i]);
+      }
+    }
+    // the partial rows this CTA reduces: FC1 from the s1 CTAs of its
+    // sub-cluster (gate and up rows of its pairs), FC2 from the C CTAs of
+    // the cluster (its rows)
+    if (valid1)
+      mbar_arrive_expect_tx(&S.red1, (uint32_t)(s1 * 2 * ((64 - r1 + s1 - 1) / s1) * M * 4));
+    else
+      mbar_arrive(&S.red1);
+    if (valid2)
+      mbar_arrive_expect_tx(&S.red2, (uint32_t)(C * ((128 - rank + C - 1) / C) * M * 4));
+    else
+      mbar_arrive(&S.red2);
+  }
+  if (warp == 0 && valid1) {
+    // router weight of the unit's expert per token
+    float wt = 0.f;
+    bool rt = false;
+    if (lane < M)
+      for (int k = 0; k < a.top_k; ++k)
+        if (S.ids[lane * a.top_k + k] == e1) {
+          wt += S.tw[lane * a.top_k + k];
+          rt = true;
+        }
+    const uint32_t rm = __ballot_sync(0xffffffffu, rt);
+    if (lane < M) S.wtok[lane] = wt;
+    if (lane == 0) S.routed = rm;
+  }
+  if (warp == kQuantWarp0 && valid1 && lane < 3) {
+    const float* gl13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * tiles1 * (H / 64) * kChunkBytes);
+    const float* gl2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * tiles2 * (I / 64) * kChunkBytes);
+    S.g3[lane] = ld_nc_f32(lane < 2 ? gl13 + 2 * e1 + lane : gl2 + e1);
+  }
+  tc_fence_before();
+  __syncwarp();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp < kMmaWarp0) {
+    // (the producer issued everything above)
+  } else if (warp < kMmaWarp0 + kMmaWarps) {
+    // ---------------- MMA issuers (alternate items, one elected lane each)
+    const int mw = warp - kMmaWarp0;
+    const uint32_t tmem = S.tmem;
+    const uint32_t idesc = idesc_mxf4nvf4(128, kN, false);
+    for (int i = mw; i < n_items; i += kMmaWarps) {
+      bool ok = mbar_wait(&S.fullA[i], 0, a.status, 2u);
+      ok = ok && mbar_wait(&S.ready[i], 0, a.status, 2u);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int ng = item_groups(i);
+      uint8_t* slotp = ring + i * Cfg::kSlot;
+      const uint32_t sfa_t = tmem + Cfg::kTmemSF + i * 32, sfb_t = sfa_t + 16;
+      const uint64_t da = smem_desc(smem_u32(slotp), 16, 1024, kLayoutSW128);
+      const uint64_t db = smem_desc(smem_u32(slotp + kSlotA), 16, 1024, kLayoutSW128);
+      for (int k = 0; k < ng; ++k)
+        mma_nvf4_warp(tmem + kN * i, da + 2 * k, db + 2 * k, idesc, sfa_t + 4 * k, sfb_t + 4 * k, k > 0);
+      mma_commit_warp(&S.done[i]);
+    }
+  } else if (is_quant) {
+    // ---------------- activation terms and scales.  (No early exit: the four
+    // warps meet at named barriers; after a wait that gave up they go on
+    // without waiting.)
+    const int qw = warp - kQuantWarp0;
+    const uint32_t tq = S.tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    bool live = true;
+    // both scale sets of item i into this warp's lane quarter, then its
+    // arrival (the weight scales once the item's TMA has landed)
+    auto publish = [&](int i) {
+      uint8_t* slotp = ring + i * Cfg::kSlot;
+      {
+        const uint4 u = *reinterpret_cast<const uint4*>(slotp + Cfg::kSFB + lane * 16);
+        const uint32_t r[16] = {u.x, 0u, 0u, 0u, u.y, 0u, 0u, 0u, u.z, 0u, 0u, 0u, u.w, 0u, 0u, 0u};
+        tmem_st16(tq + Cfg::kTmemSF + i * 32 + 16, r);
+      }
+      if (live) live = __all_sync(0xffffffffu, mbar_wait(&S.fullA[i], 0, a.status, 32u));
+      uint32_t r[16];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const uint4 u = *reinterpret_cast<const uint4*>(slotp + Cfg::kSFA + g * kChunkBytes + lane * 16);
+        r[4 * g] = u.x;
+        r[4 * g + 1] = u.y;
+        r[4 * g + 2] = u.z;
+        r[4 * g + 3] = u.w;
+      }
+      tmem_st16(tq + Cfg::kTmemSF + i * 32, r);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.ready[i]);
+    };
+    // FC1: the (item, token) rows of x, dealt over the four warps
+    for (int p = qw; p < n1 * M; p += kQuantWarps) {
+      const int i = p / M, t = p % M;
+      float v[8];
+      load_bf16x8(a.x + (size_t)t * H + (k0 + i) * 256 + lane * 8, v);
+      fz_build_row(v, ring + i * Cfg::kSlot, Cfg::kSFA, S.G[i][t], t, lane, true);
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, 32 * kQuantWarps);  // FC1's terms and scales are staged
+    for (int i = 0; i < n1; ++i) publish(i);
+    // FC2: warp qw takes items n1 + qw, n1 + qw + 4, ...: waits for the flags
+    // of the w13 tiles its K stage of h comes from, loads h, builds the terms
+    for (int i = n1 + qw; i < n_items; i += kQuantWarps) {
+      const int o = item_o(i), s2 = item_s2(i);
+      const int ntl = tiles1 - 4 * s2 < 4 ? tiles1 - 4 * s2 : 4;
+      if (lane == 0) {
+        const uint32_t* f = a.hflag + (size_t)o * ns2 + s2;
+        const uint32_t want = (uint32_t)(ntl * s1);
+        for (uint32_t pl = 0; ld_acquire_gpu(f) != want;)
+          if (++pl > kFlagPollLimit) {
+            atomicOr(a.status, kErrHFlag);
+            break;
+          }
+      }
+      __syncwarp();  // (lane 0's acquire orders the warp's loads of h below)
+      const bool act = lane < 8 * ntl;  // lanes past the stage's valid K
+      for (int t = 0; t < M; ++t) {
+        float v[8];
+        if (act) {
+          fc2_activation(a, o, t, s2 * 256 + lane * 8, v);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = 0.f;
+        }
+        fz_build_row(v, ring + i * Cfg::kSlot, Cfg::kSFA, S.G[i][t], t, lane, act);
+      }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, 32 * kQuantWarps);  // FC2's terms and scales are staged
+    for (int i = n1; i < n_items; ++i) publish(i);
+    // this CTA has read its share of each of its items' h; the last reader
+    // of an item in the layer puts its two counters back to zero
+    for (int i = n1 + qw; lane == 0 && i < n_items; i += kQuantWarps) {
+      const size_t c = (size_t)item_o(i) * ns2 + item_s2(i);
+      if (atomicAdd(a.hused + c, 1u) == (uint32_t)(tiles2 - 1)) {
+        a.hflag[c] = 0u;
+        a.hused[c] = 0u;
+      }
+    }
+  } else {
+    // ---------------- accumulator drain; after FC1's last item the FC1
+    // reduction and h, after FC2's the FC2 partial rows.  Warps 7..10 own
+    // lanes 32*(warp%4) ...
+    const int qd = warp & 3;
+    const int row = 32 * qd + lane;
+    const uint32_t tq = S.tmem + ((uint32_t)(32 * qd) << 16);
+    cluster_wait();  // phase 1: every CTA of the cluster runs (before remote stores)
+    bool ok = true;
+    float vout[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) vout[t] = 0.f;
+    for (int i = 0; i < n_items; ++i) {
+      if (ok) {
+        // (ready: the builders' multipliers of the item are visible here)
+        ok = mbar_wait(&S.ready[i], 0, a.status, 4u) && mbar_wait(&S.done[i], 0, a.status, 4u);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (ok) {
+        tc_fence_after();
+        uint32_t r[16];
+        float acc[kN];
+        tmem_ld16(tq + kN * i, r);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) acc[c] = __uint_as_float(r[c]);
+        if (kN > 16) {
+          tmem_ld16(tq + kN * i + 16, r);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) acc[(16 + c) % kN] = __uint_as_float(r[c]);
+        }
+#pragma unroll
+        for (int t = 0; t < kN / kTerms; ++t)
+          if (t < M) {
+#pragma unroll
+            for (int u = 0; u < kTerms; ++u) vout[t] = fmaf(acc[t * kTerms + u], S.G[i][t][u], vout[t]);
+          }
+      }
+      if (i == n1 - 1) {
+        // ---- FC1 reduction: pair p of the unit is owned by rank
+        // sub*s1 + p % s1 of the sub-cluster; partial gate/up rows go there
+        // by asynchronous stores counted on its barrier and are summed in
+        // rank order; the owner writes h and publishes it
+        const int pr = row & 63, owner = sub * s1 + pr % s1, j = (row >> 6) * cpo + pr / s1;
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          if (t < M) st_async_peer_f32(&S.part1[(r1 * M + t) * rpo1 + j], &S.red1, (uint32_t)owner, vout[t]);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) vout[t] = 0.f;
+        const bool got = __all_sync(0xffffffffu, mbar_wait(&S.red1, 0, a.status, kErrFzRed));
+        if (got)
+          for (int idx = row; idx < M * cpo; idx += 128) {
+            const int t = idx / cpo, jj = idx % cpo, pair = r1 + s1 * jj;
+            if (pair >= 64) continue;
+            float gate = 0.f, up = 0.f;
+            for (int src = 0; src < s1; ++src) {
+              gate += S.part1[(src * M + t) * rpo1 + jj];
+              up += S.part1[(src * M + t) * rpo1 + cpo + jj];
+            }
+            const float hv =
+                (S.routed >> t) & 1u ? gated_act(gate * S.g3[0], up * S.g3[1], a.act) * (S.wtok[t] * S.g3[2]) : 0.f;
+            a.h[((size_t)o1 * M + t) * I + tile1 * 64 + pair] = hv;
+          }
+        named_bar_sync(2, 128);  // every h store of this CTA is made
+        if (row == 0 && got) {
+          fence_acq_rel_gpu();  // (cumulative: the drain warps' stores, ordered by the barrier)
+          red_release_gpu_add(a.hflag + (size_t)o1 * ns2 + tile1 / 4, 1u);
+        }
+      }
+    }
+    if (valid2) {
+      // ---- FC2 reduction: row r of the tile is owned by rank r % C
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+        if (t < M)
+          st_async_peer_f32(&S.part2[(rank * M + t) * rpo2 + row / C], &S.red2, (uint32_t)(row % C), vout[t]);
+    }
+  }
+
+  tc_fence_before();
+  __syncwarp();
+  __syncthreads();  // tensor memory is no longer read or written
+  if (warp == kMmaWarp0) tmem_dealloc(S.tmem, 512);
+  if (!is_epi) cluster_wait();  // (the drain warps completed phase 1 already)
+  if (is_epi && valid2 && __all_sync(0xffffffffu, mbar_wait(&S.red2, 0, a.status, kErrFzRed))) {
+    const int row = 32 * (warp & 3) + lane;
+    for (int idx = row; idx < M * rpo2; idx += 128) {
+      const int t = idx / rpo2, j = idx % rpo2, orow = rank + C * j;
+      if (orow >= 128) continue;
+      float v = 0.f;
+      for (int src = 0; src < C; ++src) v += S.part2[(src * M + t) * rpo2 + j];
+      a.out[(size_t)t * H + t2 * 128 + orow] = __float2bfloat16_rn(v);
+    }
+  }
+}
+
 // K ranges per w13 tile: about 1.5 CTAs per SM in total (measured best on
 // GB300 for 1..8 tokens: more ranges shorten each CTA's weight stream, fewer
 // leave room for FC2's CTAs beside them), at most 8.
@@ -861,10 +1316,18 @@ cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, co
     err = cudaFuncSetAttribute(decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     if (err == cudaSuccess)
       err = cudaFuncSetAttribute(decode_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    // all of the unified L1/shared array as shared memory: two CTAs per SM
+    // (FC2's beside FC1's)
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(decode_tc_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(decode_tc_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
     if (err != cudaSuccess) return err;
     attr_done[dev] = true;
   }
-  TcArgs a;
+  TcArgs a = {};
   a.x = static_cast<const __nv_bfloat16*>(x);
   a.ids = ids;
   a.ids64 = ids64;
@@ -953,6 +1416,148 @@ cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, co
   c2.attrs = at2;
   c2.numAttrs = 2;
   return cudaLaunchKernelEx(&c2, decode_tc_kernel<true>, m2, a);
+}
+
+
+// ---------------------------------------------------------------- single launch, host side
+
+// Words of the single-launch kernel's synchronisation area: an h-ready
+// counter and a reader count per (owner, K stage of h), for up to
+// MOE_FP4_DECODE_MAX_M tokens (so that its place in the workspace does not
+// depend on the batch).  Zero between calls.
+size_t decode_sync_bytes(int H, int I, int top_k) {
+  (void)H;
+  const size_t slots = (size_t)MOE_FP4_DECODE_MAX_M * top_k;
+  const size_t words = 2 * slots * ((I + 255) / 256);
+  return (words * 4 + 255) & ~(size_t)255;
+}
+
+namespace {
+// Clusters of `C` single-launch CTAs for kN activation rows that can be
+// resident at once on the current device (cached per device, cluster size
+// and kN); 0 if the query fails.
+template <int kN>
+int fused_max_clusters(int C) {
+  static int cache[64][9] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || C < 1 || C > 8) return 0;
+  if (cache[dev][C] != 0) return cache[dev][C] > 0 ? cache[dev][C] : 0;
+  int n = 0;
+  cudaError_t e =
+      cudaFuncSetAttribute(decode_fused_kernel<kN>, cudaFuncAttributeMaxDynamicSharedMemorySize, fz_smem<kN>());
+  if (e == cudaSuccess) {
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)C;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t c = {};
+    c.gridDim = dim3((unsigned)(C * 16));
+    c.blockDim = dim3(kTcThreads);
+    c.dynamicSmemBytes = fz_smem<kN>();
+    c.attrs = at;
+    c.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(&n, decode_fused_kernel<kN>, &c);
+  }
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  cache[dev][C] = n > 0 ? n : -1;
+  return n;
+}
+}  // namespace
+
+// The single-launch geometry for a shape, or false if none fits: clusters of
+// C = 8 CTAs, else 4 (the w2 tile's items dealt over C), FC1 K ranges s1 per
+// w13 tile (C, C/2, ... 1, at most H/256; the largest that fits), as many
+// clusters Q as the larger of the (slot, w13 tile) units / (C / s1) and the
+// w2 tiles; all Q clusters resident at once on the current device (the CTAs
+// wait for each other's h), and every CTA's items (its FC1 K stages and its
+// share of the w2 tile's (slot, K stage) items) within the ring, so that all
+// weight tiles are in flight from the start.  Up to 8 tokens (4 with the
+// larger ring).  *cap_out (if non-null) receives the resident-cluster limit
+// of the chosen C.
+bool decode_fused_plan(int M, int H, int I, int top_k, int* C_out, int* s1_out, int* Q_out, int* cap_out) {
+  if (M < 1 || M > 8) return false;
+  const int n_slots = M * top_k;
+  const int units = n_slots * (I / 64), tiles2 = H / 128, nk = H / 256, ns2 = (I + 255) / 256;
+  const int ring = M <= 4 ? FzCfg<16>::kRing : FzCfg<32>::kRing;
+  for (int C = 8; C >= 4; C /= 2) {
+    const int cap = M <= 4 ? fused_max_clusters<16>(C) : fused_max_clusters<32>(C);
+    if (cap <= 0) continue;
+    for (int s1 = C; s1 >= 1; s1 /= 2) {
+      if (s1 > nk) continue;
+      const int per = C / s1;
+      int Q = (units + per - 1) / per;
+      if (Q < tiles2) Q = tiles2;
+      const int items = (nk + s1 - 1) / s1 + (n_slots * ns2 + C - 1) / C;
+      if (Q <= cap && items <= ring) {
+        *C_out = C;
+        *s1_out = s1;
+        *Q_out = Q;
+        if (cap_out) *cap_out = cap;
+        return true;
+      }
+    }
+  }
+  return false;
+}
+
+cudaError_t launch_decode_fused(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
+                                const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
+                                int top_k, const ActParams& act, float* scratch, uint32_t* sync, uint32_t* status,
+                                cudaStream_t st, int* cu_err) {
+  int C = 0, s1 = 0, Q = 0;
+  if (!decode_fused_plan(M, H, I, top_k, &C, &s1, &Q, nullptr)) return cudaErrorInvalidConfiguration;
+  CUtensorMap m13, m2;
+  CUresult r = make_fp4_map(&m13, w13, (uint64_t)H / 2, (uint64_t)E * 2 * I, 128);
+  if (r == CUDA_SUCCESS) r = make_fp4_map(&m2, w2, (uint64_t)I / 2, (uint64_t)E * H, 128);
+  if (r != CUDA_SUCCESS) {
+    *cu_err = (int)r;
+    return cudaErrorInvalidValue;
+  }
+  TcArgs a = {};
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.ids = ids;
+  a.ids64 = ids64;
+  a.tw = tw;
+  a.s13 = static_cast<const uint8_t*>(s13);
+  a.s2 = static_cast<const uint8_t*>(s2);
+  a.h = scratch;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.status = status;
+  a.M = M;
+  a.E = E;
+  a.H = H;
+  a.I = I;
+  a.top_k = top_k;
+  a.n_slots = M * top_k;
+  a.N = (kTerms * M + 15) / 16 * 16;
+  a.act = act;
+  a.split = C;
+  a.s1 = s1;
+  a.hflag = sync;
+  a.hused = sync + (size_t)MOE_FP4_DECODE_MAX_M * top_k * ((I + 255) / 256);
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)C;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t c = {};
+  c.gridDim = dim3((unsigned)(Q * C));
+  c.blockDim = dim3(kTcThreads);
+  c.stream = st;
+  c.attrs = at;
+  c.numAttrs = 2;
+  if (M <= 4) {
+    c.dynamicSmemBytes = fz_smem<16>();
+    return cudaLaunchKernelEx(&c, decode_fused_kernel<16>, m13, m2, a);
+  }
+  c.dynamicSmemBytes = fz_smem<32>();
+  return cudaLaunchKernelEx(&c, decode_fused_kernel<32>, m13, m2, a);
 }
 
 }  // namespace moe_fp4

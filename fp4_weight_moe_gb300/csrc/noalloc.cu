@@ -16,6 +16,12 @@
 // host-side stand-in), so the first call on each device looks up the array's
 // device address with cudaGetSymbolAddress while that device is current and
 // caches it; make that first call before any stream capture.
+//
+// The array is laid out as the decode band's workspace: the 256-byte status
+// block, the single-launch kernel's synchronisation words, then the
+// intermediate.  The synchronisation words must be zero when a call starts:
+// the array is zero when the library's device code is loaded, and every call
+// that completes leaves them at zero again.
 #include <mutex>
 
 #include "common.cuh"
@@ -25,13 +31,14 @@ size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int fmt, int n
 cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                           const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
                           int top_k, int fmt, const ActParams& act, void* ws, int num_sms, cudaStream_t st);
+int check_layer_shape(int E, int H, int I, int top_k, int fmt);
 }  // namespace moe_fp4
 
 namespace {
 
 // Scratch of moe_fp4_forward_noalloc, shared by all its calls on a device:
-// the intermediate (MOE_FP4_NOALLOC_SCRATCH_BYTES) and the decode kernels'
-// 256-byte status block after it.
+// the decode band's 256-byte status block and synchronisation words, and the
+// intermediate (MOE_FP4_NOALLOC_SCRATCH_BYTES in all with the 256 bytes).
 constexpr size_t kNoallocStatusBytes = 256;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_FP4_NOALLOC_SCRATCH_BYTES + kNoallocStatusBytes];
 
@@ -72,9 +79,9 @@ extern "C" int moe_fp4_forward_noalloc(const void* x_bf16, const void* w13, cons
                                        void* out_bf16, int M, int E, int H, int I, int top_k, int fmt,
                                        void* stream) {
   using namespace moe_fp4;
-  if (fmt != MOE_FP4_MXFP4 && fmt != MOE_FP4_NVFP4) return MOE_FP4_EINVAL;
-  if (E <= 0 || H <= 0 || I <= 0 || top_k <= 0 || M < 0) return MOE_FP4_EINVAL;
-  if (E > 65536 || top_k > 16 || H % 256 != 0 || I % 64 != 0) return MOE_FP4_EUNSUPPORTED;
+  const int shape = check_layer_shape(E, H, I, top_k, fmt);
+  if (shape != MOE_FP4_OK) return shape;
+  if (M < 0) return MOE_FP4_EINVAL;
   if (M == 0) return MOE_FP4_OK;
   if (M > MOE_FP4_DECODE_MAX_M) return MOE_FP4_EUNSUPPORTED;  // decode band only
   if (!x_bf16 || !w13 || !s13 || !w2 || !s2 || !topk_ids || !topk_weights || !out_bf16) return MOE_FP4_EINVAL;
@@ -86,10 +93,27 @@ extern "C" int moe_fp4_forward_noalloc(const void* x_bf16, const void* w13, cons
   if (st != MOE_FP4_OK) return st;
   if (decode_workspace_bytes(M, H, I, top_k, fmt, sms) > (size_t)MOE_FP4_NOALLOC_SCRATCH_BYTES + kNoallocStatusBytes)
     return MOE_FP4_EWORKSPACE;
-  // Nothing in the scratch needs to start at zero: FC1 writes every
-  // intermediate element that FC2 reads in the same call.
+  // The intermediate needs no clearing (each call writes every element it
+  // reads); the synchronisation words are zero between calls (see above).
   const ActParams silu_act = {MOE_FP4_ACT_SILU, 0.f, 0.f, 0.f};
   cudaError_t e = launch_decode(x_bf16, w13, s13, w2, s2, topk_ids, 0, topk_weights, out_bf16, M, E, H, I, top_k, fmt,
                                 silu_act, scratch, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_FP4_OK : MOE_FP4_ECUDA;
+}
+
+extern "C" int moe_fp4_noalloc_status(uint32_t* flags, int clear, void* stream) {
+  if (!flags) return MOE_FP4_EINVAL;
+  void* scratch = nullptr;
+  int sms = 0;
+  int st = scratch_for_current_device(&scratch, &sms);
+  if (st != MOE_FP4_OK) return st;
+  uint32_t v = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&v, scratch, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess && clear) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return MOE_FP4_ECUDA;
+  *flags = v;
+  return MOE_FP4_OK;
 }

@@ -187,6 +187,8 @@ cudaError_t launch_debug_gemm(const void* a_q, const void* a_sf, const void* b_q
 // MMA tile never straddles two experts.
 // ============================================================================
 
+size_t decode_sync_bytes(int H, int I, int top_k);
+
 namespace {
 
 constexpr int kRouteBlock = 256;  // routing entries per count/scatter block
@@ -656,7 +658,7 @@ __device__ __forceinline__ void quant_row_mxfp8(int K, const Load32& load32, con
 #pragma unroll
     for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
     const int e = mxfp8_scale_exponent(amax);
-    const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, exact (e <= 119 for finite FP32)
+    const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, exact (e <= 120 for finite FP32)
     uint32_t w[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {  // (the second source lands in the low byte)
@@ -725,6 +727,10 @@ PrefillCarve prefill_carve(int M, int E, int H, int I, int top_k) {
     return at;
   };
   c.status = take(256);
+  // the decode band's synchronisation words of the same shape sit right
+  // after the status block in every workspace: this band leaves them alone
+  // (they must stay zero for a decode call sharing the workspace)
+  (void)take(decode_sync_bytes(H, I, top_k));
   c.counts = take(sizeof(int) * c.n_route_blocks * E);
   c.block_base = take(sizeof(int) * c.n_route_blocks * E);
   c.expert_off = take(sizeof(int) * (E + 1));

@@ -38,13 +38,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity; on timeout set *err (if any) and
-// return false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t code) {
-  for (uint32_t i = 0; i < kWaitPollLimit; ++i)
+// Wait for the phase with the given parity, polling at most `limit` times;
+// on timeout set the bits `code` in *err (if any) and return false.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t code,
+                                              uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   if (err) atomicOr(err, code);
   return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t code) {
+  return mbar_wait_for(bar, parity, err, code, kWaitPollLimit);
 }
 
 // 2-D TMA tile load into shared memory, completing on an mbarrier.

@@ -35,7 +35,8 @@
  *     CUDA launch or API call failed; moe_fp4_last_cuda_error() gives the
  *     cudaError_t value.
  *   - Shape limits: H % 256 == 0, I % 64 == 0, 1 <= top_k <= 16,
- *     1 <= E <= 65536; violating shapes return MOE_FP4_EUNSUPPORTED.
+ *     1 <= E <= 65536, 2I * H <= 2^31; violating shapes return
+ *     MOE_FP4_EUNSUPPORTED.
  */
 #ifndef MOE_FP4_H
 #define MOE_FP4_H
@@ -170,11 +171,17 @@ MOE_FP4_API int moe_fp4_forward(const void *x_bf16, const void *w13, const void 
 /*
  * Same as moe_fp4_forward with an explicit caller-owned workspace of at
  * least moe_fp4_workspace_bytes(M, E, H, I, top_k, fmt) bytes (256-byte
- * aligned).  Before its first use a workspace must be zero-filled
- * (cudaMemset); every call leaves its synchronisation counters at zero
- * again, so later calls need no re-zeroing.  Calls sharing one workspace must
- * be ordered (same stream or explicit dependencies).
+ * aligned).  Before its first use the first
+ * moe_fp4_workspace_zero_bytes(E, H, I, top_k, fmt) bytes of a workspace
+ * (the status word and the synchronisation words) must be zero (cudaMemset;
+ * the rest is scratch that needs no initialisation, and zero-filling the
+ * whole workspace is fine too); every call leaves its synchronisation words
+ * at zero again, so later calls need no re-zeroing.  Calls sharing one
+ * workspace must be ordered (same stream or explicit dependencies).  One
+ * workspace serves every batch size up to the M it was sized for, in both
+ * bands, for one (E, H, I, top_k, fmt).
  */
+MOE_FP4_API size_t moe_fp4_workspace_zero_bytes(int E, int H, int I, int top_k, int fmt);
 MOE_FP4_API int moe_fp4_forward_ws(const void *x_bf16, const void *w13, const void *s13, const void *w2, const void *s2,
                        const int32_t *topk_ids, const float *topk_weights, void *out_bf16, int M, int E, int H,
                        int I, int top_k, int fmt, void *workspace, size_t workspace_bytes, void *stream);
@@ -218,6 +225,43 @@ MOE_FP4_API int moe_fp4_forward_host(const void *x_bf16, const void *w13, const 
                                      const void *s2, const int32_t *topk_ids, const float *topk_weights,
                                      void *out_bf16, int M, int E, int H, int I, int top_k, int fmt, void *workspace,
                                      size_t workspace_bytes, void *stream);
+
+/*
+ * Device status of a workspace.  Every wait inside the kernels is bounded:
+ * a wait that has not completed after its poll limit (about a second) gives
+ * up, the kernel sets one of the bits below in the status word of the
+ * workspace it ran on (the first 4 bytes; 0 when the workspace is fresh) and
+ * goes on without waiting, so the GPU is never hung; the outputs of such a
+ * call are not valid.  The bits are sticky: they stay set for every later
+ * call until cleared.  A wait can give up only when the launch's CTAs cannot
+ * make progress together: the single-launch decode kernel needs its whole
+ * grid resident at once, which concurrent work on the same GPU (other
+ * streams, other processes) can prevent (flashinfer PR #4285, "sync SM12x
+ * NVFP4 fused-MoE kernels": a cooperative kernel deadlocks when concurrent
+ * work keeps part of its grid off the GPU).
+ *
+ * moe_fp4_workspace_status copies the status word of `workspace` (device
+ * memory passed to moe_fp4_forward_ws, _ex, _ex_i64 or _host; NULL: the
+ * library workspace of moe_fp4_reserve_workspace on the current device) into
+ * *flags (host), after everything enqueued on `stream` before it, and if
+ * `clear` is nonzero sets it back to 0.  It synchronises `stream` (call it
+ * outside stream capture).  MOE_FP4_EWORKSPACE if workspace is NULL and none
+ * is reserved, or not 256-byte aligned.  moe_fp4_noalloc_status does the same
+ * for the scratch array of moe_fp4_forward_noalloc on the current device.
+ */
+#define MOE_FP4_STATUS_OK 0u
+#define MOE_FP4_STATUS_TEST_WAIT 8192u /* set only by moe_fp4_debug_wait_timeout */
+MOE_FP4_API int moe_fp4_workspace_status(const void *workspace, uint32_t *flags, int clear, void *stream);
+MOE_FP4_API int moe_fp4_noalloc_status(uint32_t *flags, int clear, void *stream);
+/*
+ * Test support: one GPU thread waits on a barrier that nothing completes,
+ * with a poll limit of `polls` (1 .. 2^20) instead of the kernels' own, so
+ * that the bounded wait gives up and sets MOE_FP4_STATUS_TEST_WAIT in the
+ * 32-bit word at `status_word` (device, 4-byte aligned; e.g. a workspace's
+ * first word).  Nothing else is touched.  MOE_FP4_EINVAL for a null or
+ * misaligned pointer or a limit out of range.
+ */
+MOE_FP4_API int moe_fp4_debug_wait_timeout(void *status_word, unsigned polls, void *stream);
 
 /*
  * Gated activations of FC1's (gate, up) pair.  MOE_FP4_ACT_SILU,
@@ -279,18 +323,22 @@ MOE_FP4_API int moe_fp4_forward_ex_i64(const void *x_bf16, const void *w13, cons
  *
  * Arguments, layouts and results are those of moe_fp4_forward (same
  * kernels, bitwise the same output).  Instead of a workspace it uses one
- * fixed scratch array in the library's device image (an intermediate of
- * MOE_FP4_NOALLOC_SCRATCH_BYTES plus a 256-byte status block), which every
- * GPU that loads the library's device code keeps until the process exits.
- * Shapes whose scratch need (moe_fp4_workspace_bytes(M, ...)) exceeds
- * MOE_FP4_NOALLOC_SCRATCH_BYTES + 256 return
- * MOE_FP4_EWORKSPACE; M > MOE_FP4_DECODE_MAX_M returns MOE_FP4_EUNSUPPORTED.
- * The first call on each device looks up the array's device address while
- * that device is current; make that first call outside any stream capture.
- * All calls on a device share the one array: calls that may overlap on the
- * GPU (different streams without ordering between them) race and corrupt
- * each other's results, so order them.  Nothing in the array needs to start
- * at zero.
+ * fixed scratch array in the library's device image (laid out as a decode
+ * workspace: the 256-byte status block, the single-launch kernel's
+ * synchronisation words, the intermediate; MOE_FP4_NOALLOC_SCRATCH_BYTES +
+ * 256 bytes in all), which every GPU that loads the library's device code
+ * keeps until the process exits.  Shapes whose scratch need
+ * (moe_fp4_workspace_bytes(M, ...)) exceeds MOE_FP4_NOALLOC_SCRATCH_BYTES +
+ * 256 return MOE_FP4_EWORKSPACE; M > MOE_FP4_DECODE_MAX_M returns
+ * MOE_FP4_EUNSUPPORTED; other shape limits as moe_fp4_forward.  The first
+ * call on each device looks up the array's device address while that device
+ * is current; make that first call outside any stream capture.  All calls on
+ * a device share the one array: calls that may overlap on the GPU (different
+ * streams without ordering between them) race and corrupt each other's
+ * results, so order them.  The synchronisation words must be zero when a
+ * call starts: the array is zero when the device code is loaded and every
+ * completed call leaves them at zero; the intermediate needs no clearing.
+ * moe_fp4_noalloc_status reads the array's status word.
  */
 #define MOE_FP4_NOALLOC_SCRATCH_BYTES (16u << 20)
 MOE_FP4_API int moe_fp4_forward_noalloc(const void *x_bf16, const void *w13, const void *s13, const void *w2,
@@ -301,11 +349,16 @@ MOE_FP4_API int moe_fp4_forward_noalloc(const void *x_bf16, const void *w13, con
  * Test support: choose the kernel family of the decode band (M <=
  * MOE_FP4_DECODE_MAX_M) for every later call in the process.
  *   family 0  by shape (default): the streaming GEMV kernels for one token
- *             with at most 4 MB of routed weights, else the tcgen05 kernels
+ *             with at most 4 MB of routed weights, else the tcgen05 launch
+ *             chain
  *   family 1  the streaming GEMV kernels where the shape fits them
- *   family 2  the tcgen05 kernels
- * Both families compute the same layer; the GEMV family sums in a different
- * order, so results agree within the parity bound, not bitwise.  *previous
+ *   family 2  the tcgen05 launch chain (x pre-pass, FC1, h pre-pass from
+ *             M = 2, FC2)
+ *   family 3  the tcgen05 single launch where it fits (the whole grid
+ *             resident at once on this device), else the chain
+ * All compute the same layer and agree within the parity bound; they are not
+ * bitwise equal in general (the GEMV family sums in a different order, and
+ * the two tcgen05 plans may split FC1's K range differently).  *previous
  * (if non-null) receives the old setting.  MOE_FP4_EINVAL for other values.
  * moe_fp4_debug_decode_gemv_fits returns 1 if the GEMV kernels take the
  * shape (their shared memory holds all tokens' activations and every routed
@@ -327,14 +380,22 @@ MOE_FP4_API int moe_fp4_debug_set_decode_family(int family, int *previous);
  */
 MOE_FP4_API int moe_fp4_debug_set_mid_band(int mode, int *previous);
 MOE_FP4_API int moe_fp4_debug_decode_gemv_fits(int M, int E, int H, int I, int top_k);
-/* The family the current setting picks for a decode-band shape (1 streaming
- * GEMV, 2 tcgen05); 0 for M outside 1..MOE_FP4_DECODE_MAX_M or invalid
- * arguments. */
+/* The plan the current setting picks for a decode-band shape on the current
+ * device (1 streaming GEMV, 2 tcgen05 launch chain, 3 tcgen05 single
+ * launch); 0 for M outside 1..MOE_FP4_DECODE_MAX_M or invalid arguments. */
 MOE_FP4_API int moe_fp4_debug_decode_family_of(int M, int E, int H, int I, int top_k);
+/* The single-launch plan's geometry for a decode-band shape on the current
+ * device, into plan[4] (host): cluster size C, FC1 K ranges per w13 tile,
+ * clusters launched, and the clusters of that size the device can hold
+ * resident at once; all zero if the shape has no single-launch plan there
+ * (it then runs as the launch chain).  MOE_FP4_EINVAL for M outside
+ * 1..MOE_FP4_DECODE_MAX_M or a null plan. */
+MOE_FP4_API int moe_fp4_debug_decode_plan(int M, int E, int H, int I, int top_k, int *plan);
 /* Kernel launches one decode-band layer of this shape makes under the
- * current family and mid-band settings (2 streaming GEMV; 3, or 4 from
- * M = 2, tcgen05; the sum over the chunks of a chunked batch); 0 for shapes
- * that take the prefill band or invalid arguments. */
+ * current family and mid-band settings (2 streaming GEMV; 1 tcgen05 single
+ * launch; 3, or 4 from M = 2, tcgen05 chain; the sum over the chunks of a
+ * chunked batch); 0 for shapes that take the prefill band or invalid
+ * arguments. */
 MOE_FP4_API int moe_fp4_debug_decode_launches(int M, int E, int H, int I, int top_k);
 
 /*

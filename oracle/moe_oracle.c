@@ -140,64 +140,67 @@ static double gated_other(double gate, double up, const oracle_act *a)
     return (u + a->beta) * g / (1.0 + exp(-a->alpha * g));
 }
 
-/* h[n] = act(x . W13[e][n], x . W13[e][I+n]) for n < I (SiLU(gate) * up by
- * default). */
-static void expert_fc1(const double *x, const uint8_t *w13, const uint8_t *s13, const float *g13, int e, int H,
-                       int I, int fmt, const oracle_act *act, double *h)
+/* h_n = act(x . W13[e][n], x . W13[e][I+n]) for one intermediate index n < I
+ * (SiLU(gate) * up by default). */
+static double expert_fc1_row(const double *x, const uint8_t *w13, const uint8_t *s13, const float *g13, int e,
+                             int H, int I, int fmt, const oracle_act *act, int n)
 {
     int B = block_of(fmt);
     const uint8_t *nib = w13 + (size_t)e * 2 * I * (H / 2);
     const uint8_t *sc = s13 + (size_t)e * 2 * I * (H / B);
     double gg = fmt == ORACLE_NVFP4 ? (double)g13[2 * e + 0] : 1.0;
     double gu = fmt == ORACLE_NVFP4 ? (double)g13[2 * e + 1] : 1.0;
-    for (int n = 0; n < I; ++n) {
-        double gate = 0.0, up = 0.0;
-        for (int k = 0; k < H; ++k) {
-            gate += x[k] * weight_at(nib, sc, H, fmt, gg, n, k);
-            up += x[k] * weight_at(nib, sc, H, fmt, gu, I + n, k);
-        }
-        if (act->kind == ORACLE_ACT_SILU)
-            h[n] = silu(gate) * up;
-        else
-            h[n] = gated_other(gate, up, act);
+    double gate = 0.0, up = 0.0;
+    for (int k = 0; k < H; ++k) {
+        gate += x[k] * weight_at(nib, sc, H, fmt, gg, n, k);
+        up += x[k] * weight_at(nib, sc, H, fmt, gu, I + n, k);
     }
+    if (act->kind == ORACLE_ACT_SILU) return silu(gate) * up;
+    return gated_other(gate, up, act);
 }
 
-/* y[m] = W2[e][m] . h for m < H. */
-static void expert_fc2(const double *h, const uint8_t *w2, const uint8_t *s2, const float *g2, int e, int H, int I,
-                       int fmt, double *y)
+/* h[n] for every n < I. */
+static void expert_fc1(const double *x, const uint8_t *w13, const uint8_t *s13, const float *g13, int e, int H,
+                       int I, int fmt, const oracle_act *act, double *h)
+{
+    for (int n = 0; n < I; ++n) h[n] = expert_fc1_row(x, w13, s13, g13, e, H, I, fmt, act, n);
+}
+
+/* y_m = W2[e][m] . h for one output row m < H. */
+static double expert_fc2_row(const double *h, const uint8_t *w2, const uint8_t *s2, const float *g2, int e, int H,
+                             int I, int fmt, int m)
 {
     int B = block_of(fmt);
     const uint8_t *nib = w2 + (size_t)e * H * (I / 2);
     const uint8_t *sc = s2 + (size_t)e * H * (I / B);
     double gd = fmt == ORACLE_NVFP4 ? (double)g2[e] : 1.0;
-    for (int m = 0; m < H; ++m) {
-        double acc = 0.0;
-        for (int n = 0; n < I; ++n) acc += weight_at(nib, sc, I, fmt, gd, m, n) * h[n];
-        y[m] = acc;
-    }
+    double acc = 0.0;
+    for (int n = 0; n < I; ++n) acc += weight_at(nib, sc, I, fmt, gd, m, n) * h[n];
+    return acc;
 }
 
-/* One token: out[m] = sum over valid slots j of w[j] * FC2(SiLU(FC1 gate) * FC1 up). */
-static void token_forward(const double *x, const uint8_t *w13, const uint8_t *s13, const float *g13,
-                          const uint8_t *w2, const uint8_t *s2, const float *g2, const int32_t *ids,
-                          const float *tw, int E, int H, int I, int top_k, int fmt, const oracle_act *act,
-                          double *out, double *h, double *y)
+/* y[m] for every m < H. */
+static void expert_fc2(const double *h, const uint8_t *w2, const uint8_t *s2, const float *g2, int e, int H, int I,
+                       int fmt, double *y)
 {
-    for (int m = 0; m < H; ++m) out[m] = 0.0;
-    for (int j = 0; j < top_k; ++j) {
-        int e = ids[j];
-        if (e < 0 || e >= E) continue; /* invalid route: exact-zero contribution */
-        expert_fc1(x, w13, s13, g13, e, H, I, fmt, act, h);
-        expert_fc2(h, w2, s2, g2, e, H, I, fmt, y);
-        double w = (double)tw[j];
-        for (int m = 0; m < H; ++m) out[m] += w * y[m];
-    }
+    for (int m = 0; m < H; ++m) y[m] = expert_fc2_row(h, w2, s2, g2, e, H, I, fmt, m);
 }
+
+/* A routing id names an expert only inside [0, E); any other id is an
+ * invalid route with an exact-zero contribution (never dereferenced). */
+static int valid_route(int e, int E) { return e >= 0 && e < E; }
 
 /* Full layer for the tokens listed in `tokens` (n_tok entries; NULL = all M
  * tokens in order), activation `act_kind` with parameters alpha, beta, limit
- * (SwiGLU-OAI only).  out is [n_tok][H] FP64.  Returns 0 on success. */
+ * (SwiGLU-OAI only).  out is [n_tok][H] FP64.  Returns 0 on success.
+ *
+ *   out[t][m] = sum over valid slots j of w[t][j] * (W2[e] . h_tj)[m],
+ *   h_tj[n]   = act(x_t . W13[e][n], x_t . W13[e][I+n]),  e = ids[t][j].
+ *
+ * With OpenMP the work is spread over (token, slot, intermediate row) for
+ * FC1 and over (token, output row) for FC2; each sum runs in the same order
+ * as with one thread (K index, then intermediate index, then slot), so the
+ * result does not depend on the thread count. */
 int moe_oracle_forward_act(const uint16_t *x_bf16, const uint8_t *w13, const uint8_t *s13, const float *g13,
                            const uint8_t *w2, const uint8_t *s2, const float *g2, const int32_t *topk_ids,
                            const float *topk_w, int M, int E, int H, int I, int top_k, int fmt, const int32_t *tokens,
@@ -210,27 +213,54 @@ int moe_oracle_forward_act(const uint16_t *x_bf16, const uint8_t *w13, const uin
     if (fmt != ORACLE_MXFP4 && fmt != ORACLE_NVFP4) return 1;
     if (H % block_of(fmt) || I % block_of(fmt)) return 1;
     if (!tokens) n_tok = M;
-#ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
-#pragma omp parallel
-#endif
-    {
-        double *x = (double *)malloc(sizeof(double) * (size_t)H);
-        double *h = (double *)malloc(sizeof(double) * (size_t)I);
-        double *y = (double *)malloc(sizeof(double) * (size_t)H);
-#ifdef _OPENMP
-#pragma omp for schedule(dynamic, 1)
-#endif
-        for (int i = 0; i < n_tok; ++i) {
-            int t = tokens ? tokens[i] : i;
-            for (int k = 0; k < H; ++k) x[k] = bf16_to_double(x_bf16[(size_t)t * H + k]);
-            token_forward(x, w13, s13, g13, w2, s2, g2, topk_ids + (size_t)t * top_k, topk_w + (size_t)t * top_k,
-                          E, H, I, top_k, fmt, &act, out + (size_t)i * H, h, y);
-        }
+    double *x = (double *)malloc(sizeof(double) * ((size_t)n_tok * H + 1));
+    double *h = (double *)malloc(sizeof(double) * ((size_t)n_tok * top_k * I + 1));
+    if (!x || !h) {
         free(x);
         free(h);
-        free(y);
+        return 2;
     }
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+    /* the activations, exactly, as FP64 */
+    for (int i = 0; i < n_tok; ++i) {
+        int t = tokens ? tokens[i] : i;
+        for (int k = 0; k < H; ++k) x[(size_t)i * H + k] = bf16_to_double(x_bf16[(size_t)t * H + k]);
+    }
+    /* FC1 and the activation for every valid (token, slot) */
+    long n1 = (long)n_tok * top_k * I;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 8)
+#endif
+    for (long u = 0; u < n1; ++u) {
+        int i = (int)(u / ((long)top_k * I)), j = (int)(u / I % top_k), n = (int)(u % I);
+        int t = tokens ? tokens[i] : i;
+        int e = topk_ids[(size_t)t * top_k + j];
+        if (!valid_route(e, E)) continue;
+        h[u] = expert_fc1_row(x + (size_t)i * H, w13, s13, g13, e, H, I, fmt, &act, n);
+    }
+    /* FC2 and the router-weighted sum over the slots, per output element */
+    long n2 = (long)n_tok * H;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (long v = 0; v < n2; ++v) {
+        int i = (int)(v / H), m = (int)(v % H);
+        int t = tokens ? tokens[i] : i;
+        const int32_t *ids = topk_ids + (size_t)t * top_k;
+        const float *tw = topk_w + (size_t)t * top_k;
+        double o = 0.0; /* overwrite: out = the sum over valid slots */
+        for (int j = 0; j < top_k; ++j) {
+            int e = ids[j];
+            if (!valid_route(e, E)) continue; /* invalid route: exact-zero contribution */
+            double w = (double)tw[j];
+            o += w * expert_fc2_row(h + ((size_t)i * top_k + j) * I, w2, s2, g2, e, H, I, fmt, m);
+        }
+        out[v] = o;
+    }
+    free(x);
+    free(h);
     (void)nthreads;
     return 0;
 }

@@ -18,7 +18,7 @@ from workload import gen
 
 pytestmark = pytest.mark.gpu
 
-GEMV, TC = 1, 2
+GEMV, TC, SINGLE = 1, 2, 3  # decode plans: streaming GEMV, tcgen05 chain, tcgen05 single launch
 ACTS = [("gelu_tanh", (oracle.ACT_GELU_TANH, 0.0, 0.0, 0.0)),
         ("swigluoai", (oracle.ACT_SWIGLUOAI, 1.702, 1.0, 0.25))]
 
@@ -52,7 +52,7 @@ def _oracle_decode(wl, act):
     return oracle.forward(wl.x, w, ids_c, wl.topk_weights, E_c, wl.H, wl.I, wl.top_k, wl.fmt, act=act)
 
 
-@pytest.mark.parametrize("family", [GEMV, TC], ids=["gemv", "tc"])
+@pytest.mark.parametrize("family", [GEMV, TC, SINGLE], ids=["gemv", "chain", "single"])
 @pytest.mark.parametrize("name,ov", [("tiny_decode", dict(M=3, E=12, top_k=3)),
                                      ("decode_e512", dict(E=24)),
                                      ("decode_e288_m4", dict(E=24))])

@@ -135,10 +135,25 @@ def test_band_policy_by_shape(lib):
     tiny = (8, 256, 128, 2)
     assert c.moe_fp4_debug_decode_family_of(1, *tiny) == 1
     assert c.moe_fp4_debug_decode_launches(1, *tiny) == 2
+    # tcgen05 beyond that (the launch chain by default; the single launch
+    # only where its grid is resident at once on the current GPU, never
+    # without one)
+    prev_family = c.moe_fp4_debug_set_decode_family(3)
+    try:
+        single = c.moe_fp4_debug_decode_family_of(1, *e512) == 3
+        assert c.moe_fp4_debug_decode_family_of(1, *e512) in (2, 3)
+        assert c.moe_fp4_debug_decode_launches(1, *e512) == (1 if single else 3)
+    finally:
+        c.moe_fp4_debug_set_decode_family(prev_family)
     assert c.moe_fp4_debug_decode_family_of(1, *e512) == 2
-    assert [c.moe_fp4_debug_decode_launches(M, *e512) for M in (1, 2, 8)] == [3, 4, 4]
-    assert [c.moe_fp4_debug_decode_launches(M, *e512) for M in (9, 12, 16, 17, 24)] == [8, 8, 8, 0, 0]
-    assert [c.moe_fp4_debug_decode_launches(M, *e256) for M in (8, 9, 16)] == [4, 0, 0]
+    prev_family = c.moe_fp4_debug_set_decode_family(2)  # the chain: 3 launches, 4 from two tokens
+    try:
+        assert c.moe_fp4_debug_decode_family_of(1, *e512) == 2
+        assert [c.moe_fp4_debug_decode_launches(M, *e512) for M in (1, 2, 8)] == [3, 4, 4]
+        assert [c.moe_fp4_debug_decode_launches(M, *e512) for M in (9, 12, 16, 17, 24)] == [8, 8, 8, 0, 0]
+        assert [c.moe_fp4_debug_decode_launches(M, *e256) for M in (8, 9, 16)] == [4, 0, 0]
+    finally:
+        c.moe_fp4_debug_set_decode_family(prev_family)
     assert c.moe_fp4_debug_decode_family_of(9, *e512) == 0
     prev = c.moe_fp4_debug_set_mid_band(2)
     try:
@@ -149,6 +164,47 @@ def test_band_policy_by_shape(lib):
         c.moe_fp4_debug_set_mid_band(prev)
     with pytest.raises(c.MoeFp4Error):
         c.moe_fp4_debug_set_mid_band(3)
+    with pytest.raises(c.MoeFp4Error):
+        c.moe_fp4_debug_set_decode_family(4)
+
+
+def test_status_query_argument_errors(lib):
+    """The status queries and the wait-timeout test entry reject bad
+    arguments on the host: a null flags pointer, a workspace that is not
+    256-byte aligned, no reserved library workspace, a null or misaligned
+    status word, a poll limit out of range."""
+    import ctypes
+    v = ctypes.c_uint32(7)
+    assert lib.moe_fp4_workspace_status(ctypes.c_void_p(0x1000), None, 0, None) == _capi.MOE_FP4_EINVAL
+    assert lib.moe_fp4_workspace_status(ctypes.c_void_p(0x1010), ctypes.byref(v), 0, None) == \
+        _capi.MOE_FP4_EWORKSPACE
+    assert lib.moe_fp4_noalloc_status(None, 0, None) == _capi.MOE_FP4_EINVAL
+    assert lib.moe_fp4_debug_wait_timeout(None, 16, None) == _capi.MOE_FP4_EINVAL
+    assert lib.moe_fp4_debug_wait_timeout(ctypes.c_void_p(0x1002), 16, None) == _capi.MOE_FP4_EINVAL
+    assert lib.moe_fp4_debug_wait_timeout(ctypes.c_void_p(0x1000), 0, None) == _capi.MOE_FP4_EINVAL
+    assert lib.moe_fp4_debug_wait_timeout(ctypes.c_void_p(0x1000), (1 << 20) + 1, None) == _capi.MOE_FP4_EINVAL
+    assert v.value == 7
+
+
+def test_noalloc_shape_limits(lib):
+    """moe_fp4_forward_noalloc applies the same shape limits as the other
+    forward calls, including one projection's 2I x H elements within 2^31
+    (I = 2^19 at H = 4096 would fit the scratch array at one token)."""
+    import ctypes
+    p = ctypes.c_void_p(0x1000)
+
+    def st(E=8, H=256, I=128, top_k=2, M=1, fmt=1):
+        return lib.moe_fp4_forward_noalloc(p, p, p, p, p, p, p, p, M, E, H, I, top_k, fmt, None)
+
+    assert st(H=4096, I=1 << 19, top_k=1) == _capi.MOE_FP4_EUNSUPPORTED
+    assert st(H=384) == _capi.MOE_FP4_EUNSUPPORTED
+    assert st(I=96) == _capi.MOE_FP4_EUNSUPPORTED
+    assert st(top_k=17) == _capi.MOE_FP4_EUNSUPPORTED
+    assert st(E=65537) == _capi.MOE_FP4_EUNSUPPORTED
+    assert st(fmt=2) == _capi.MOE_FP4_EINVAL
+    assert st(M=-1) == _capi.MOE_FP4_EINVAL
+    assert st(M=0) == _capi.MOE_FP4_OK
+    assert st(M=9) == _capi.MOE_FP4_EUNSUPPORTED
 
 
 def test_header_is_plain_c_and_links(lib, tmp_path):

@@ -113,7 +113,8 @@ DECODE_CASES = [
 ]
 
 
-GEMV, TC = 1, 2  # decode kernel families (streaming GEMV, tcgen05)
+GEMV, TC, FUSED = 1, 2, 3  # decode plans (streaming GEMV, tcgen05 launch chain, tcgen05 single launch)
+FAMILY_IDS = {GEMV: "gemv", TC: "chain", FUSED: "single"}
 
 
 class decode_family:
@@ -136,12 +137,24 @@ def _fits_gemv(wl):
     return _capi.moe_fp4_debug_decode_gemv_fits(wl.M, wl.E, wl.H, wl.I, wl.top_k)
 
 
-@pytest.mark.parametrize("family", [GEMV, TC], ids=["gemv", "tc"])
+def _fits_single(wl):
+    from fp4_weight_moe_gb300 import _capi
+    with decode_family(FUSED):
+        return _capi.moe_fp4_debug_decode_family_of(wl.M, wl.E, wl.H, wl.I, wl.top_k) == FUSED
+
+
+def _skip_unless_fits(wl, family):
+    if family == GEMV and not _fits_gemv(wl):
+        pytest.skip("shape outside the streaming GEMV kernels' shared memory (served by tcgen05)")
+    if family == FUSED and not _fits_single(wl):
+        pytest.skip("grid of the single-launch plan not resident at once on this GPU (served by the chain)")
+
+
+@pytest.mark.parametrize("family", [GEMV, TC, FUSED], ids=lambda f: FAMILY_IDS[f])
 @pytest.mark.parametrize("name,ov", DECODE_CASES, ids=[f"{n}-{i}" for i, (n, _) in enumerate(DECODE_CASES)])
 def test_decode_parity(name, ov, family):
     wl = gen.make_workload(name, device="cuda", **ov)
-    if family == GEMV and not _fits_gemv(wl):
-        pytest.skip("shape outside the streaming GEMV kernels' shared memory (served by tcgen05)")
+    _skip_unless_fits(wl, family)
     out = torch.full((wl.M, wl.H), float("nan"), dtype=torch.bfloat16, device="cuda")
     with decode_family(family):
         got = _run(wl, out=out)
@@ -233,20 +246,44 @@ def test_workspace_too_small_is_rejected():
 FULL = [
     ("decode_e512", {}),
     ("decode_e288_m4", {}),
-    ("decode_e256", dict(M=1)),
-    ("decode_e256", dict(M=8, fmt=gen.NVFP4)),
 ]
 
 
-@pytest.mark.parametrize("family", [GEMV, TC], ids=["gemv", "tc"])
+@pytest.mark.parametrize("family", [GEMV, TC, FUSED], ids=lambda f: FAMILY_IDS[f])
 @pytest.mark.parametrize("name,ov", FULL, ids=[f"{n}-{i}" for i, (n, _) in enumerate(FULL)])
 def test_decode_full_size(name, ov, family):
     wl = gen.make_workload(name, device="cuda", **ov)
-    if family == GEMV and not _fits_gemv(wl):
-        pytest.skip("shape outside the streaming GEMV kernels' shared memory (served by tcgen05)")
+    _skip_unless_fits(wl, family)
     with decode_family(family):
         got = _run(wl)
         torch.cuda.synchronize()
     assert_layer_close(got, oracle_layer(wl), f"{name} {ov} family {family}")
     del wl
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("fmt", [gen.MXFP4, gen.NVFP4], ids=["mxfp4", "nvfp4"])
+def test_decode_e256_full_size_every_batch(fmt):
+    """The full E=256, H=7168, I=2048, top_k=8 layer (Zipf routing) at every
+    batch of the sweep, M = 1, 2, 4, 8, in both weight formats, on the plan
+    each batch takes by shape; the weights are drawn once per format."""
+    m = fm()
+    c = gen.CONFIGS["decode_e256"]
+    E, H, I, k = c["E"], c["H"], c["I"], c["top_k"]
+    seed = gen.CONFIG_SEED["decode_e256"]
+    weights = gen.make_expert_weights(E, H, I, fmt, seed, device="cuda")
+    pw = m.prepare_weights(weights, E, H, I, fmt)
+    ws = m.alloc_workspace(8, E, H, I, k, fmt)
+    for M in (1, 2, 4, 8):
+        wl = gen.Workload(name="decode_e256", E=E, H=H, I=I, top_k=k, M=M, fmt=fmt, seed=seed, weights=weights,
+                          x=gen.draw_activations(M, H, seed + 17 + M, device="cuda"),
+                          topk_ids=None, topk_weights=None)
+        ids, tw = gen.draw_routing(M, E, k, seed + 29 + M, mode="zipf")
+        wl.topk_ids, wl.topk_weights = ids.cuda(), tw.cuda()
+        got = m.forward(wl.x, pw, wl.topk_ids, wl.topk_weights, workspace=ws)
+        torch.cuda.synchronize()
+        assert m.workspace_status(ws) == 0
+        assert_layer_close(got, oracle_layer(wl), f"decode_e256 M={M} fmt={fmt}")
+    del weights, pw, ws
+    torch.cuda.empty_cache()
+

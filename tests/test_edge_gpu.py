@@ -14,7 +14,7 @@ from workload import gen
 
 pytestmark = pytest.mark.gpu
 
-GEMV, TC = 1, 2
+GEMV, TC, SINGLE = 1, 2, 3  # decode plans: streaming GEMV, tcgen05 chain, tcgen05 single launch
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -44,7 +44,7 @@ def _with_ids(wl, ids, seed=0):
     return wl
 
 
-@pytest.mark.parametrize("family", [0, GEMV, TC], ids=["auto", "gemv", "tc"])
+@pytest.mark.parametrize("family", [0, GEMV, TC, SINGLE], ids=["auto", "gemv", "chain", "single"])
 @pytest.mark.parametrize("case", ["max_batch_topk16", "one_expert_all_routes", "min_shape", "same_expert_slots"])
 def test_decode_edges(case, family):
     if case == "max_batch_topk16":

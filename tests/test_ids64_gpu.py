@@ -18,7 +18,7 @@ from workload import gen
 
 pytestmark = pytest.mark.gpu
 
-GEMV, TC = 1, 2
+GEMV, TC, SINGLE = 1, 2, 3  # decode plans: streaming GEMV, tcgen05 chain, tcgen05 single launch
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -60,7 +60,7 @@ def _run(wl, ids, family=0):
     return out
 
 
-@pytest.mark.parametrize("family", [GEMV, TC], ids=["gemv", "tc"])
+@pytest.mark.parametrize("family", [GEMV, TC, SINGLE], ids=["gemv", "chain", "single"])
 @pytest.mark.parametrize("name,ov", [("tiny_decode", dict(M=3, E=12, top_k=3)),
                                      ("decode_e512", dict(E=40, M=2)),
                                      ("decode_e288_m4", dict(E=24))])
@@ -72,7 +72,7 @@ def test_decode_int64_ids(name, ov, family):
     assert_layer_close(got, oracle_layer(wl), f"{name} {ov} int64 ids family {family}")
 
 
-@pytest.mark.parametrize("family", [GEMV, TC], ids=["gemv", "tc"])
+@pytest.mark.parametrize("family", [GEMV, TC, SINGLE], ids=["gemv", "chain", "single"])
 def test_decode_int64_matches_int32_bitwise(family):
     wl = gen.make_workload("decode_e512", device="cuda", E=32, M=4, top_k=6)
     ids32 = wl.topk_ids.clone()

@@ -29,18 +29,18 @@ MUTATIONS = {
     "e4m3_bias": ("else v = ldexp(1.0 + (double)m / 8.0, e - 7);", "else v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
     "e4m3_subnormal": ("if (e == 0) v = ldexp((double)m / 8.0, -6);", "if (e == 0) v = ldexp((double)m / 8.0, -7);"),
     "silu_sign": ("return v / (1.0 + exp(-v));", "return v / (1.0 + exp(v));"),
-    "dropped_up": ("h[n] = silu(gate) * up;", "h[n] = silu(gate);"),
-    "gate_up_swapped": ("h[n] = silu(gate) * up;", "h[n] = silu(up) * gate;"),
+    "dropped_up": ("return silu(gate) * up;", "return silu(gate);"),
+    "gate_up_swapped": ("return silu(gate) * up;", "return silu(up) * gate;"),
     "up_rows_offset": ("up += x[k] * weight_at(nib, sc, H, fmt, gu, I + n, k);",
                        "up += x[k] * weight_at(nib, sc, H, fmt, gu, n, k);"),
-    "nv_global_swapped": ("double gg = fmt == ORACLE_NVFP4 ? (double)g13[2 * e + 0] : 1.0;\n    double gu = fmt == ORACLE_NVFP4 ? (double)g13[2 * e + 1] : 1.0;\n    for (int n = 0; n < I; ++n) {\n        double gate = 0.0",
-                          "double gg = fmt == ORACLE_NVFP4 ? (double)g13[2 * e + 1] : 1.0;\n    double gu = fmt == ORACLE_NVFP4 ? (double)g13[2 * e + 0] : 1.0;\n    for (int n = 0; n < I; ++n) {\n        double gate = 0.0"),
-    "down_global_dropped": ("double gd = fmt == ORACLE_NVFP4 ? (double)g2[e] : 1.0;\n    for (int m = 0; m < H; ++m) {",
-                            "double gd = 1.0;\n    for (int m = 0; m < H; ++m) {"),
+    "nv_global_swapped": ("double gg = fmt == ORACLE_NVFP4 ? (double)g13[2 * e + 0] : 1.0;\n    double gu = fmt == ORACLE_NVFP4 ? (double)g13[2 * e + 1] : 1.0;\n    double gate = 0.0",
+                          "double gg = fmt == ORACLE_NVFP4 ? (double)g13[2 * e + 1] : 1.0;\n    double gu = fmt == ORACLE_NVFP4 ? (double)g13[2 * e + 0] : 1.0;\n    double gate = 0.0"),
+    "down_global_dropped": ("double gd = fmt == ORACLE_NVFP4 ? (double)g2[e] : 1.0;\n    double acc = 0.0;",
+                            "double gd = 1.0;\n    double acc = 0.0;"),
     "router_weight_ignored": ("double w = (double)tw[j];", "double w = 1.0;"),
     "router_weight_wrong_slot": ("double w = (double)tw[j];", "double w = (double)tw[0];"),
-    "invalid_upper_bound": ("if (e < 0 || e >= E) continue; /* invalid route", "if (e < 0 || e > E) continue; /* invalid route"),
-    "accumulate_instead_of_overwrite": ("for (int m = 0; m < H; ++m) out[m] = 0.0;", ";"),
+    "invalid_upper_bound": ("return e >= 0 && e < E;", "return e >= 0 && e <= E;"),
+    "accumulate_instead_of_overwrite": ("double o = 0.0; /* overwrite", "double o = out[v]; /* overwrite"),
     "fc2_index_transposed": ("for (int n = 0; n < I; ++n) acc += weight_at(nib, sc, I, fmt, gd, m, n) * h[n];",
                              "for (int n = 0; n < I; ++n) acc += weight_at(nib, sc, I, fmt, gd, m, (n + 1) % I) * h[n];"),
     "quant_global_rule": ("volatile float six448 = 6.0f * 448.0f;", "volatile float six448 = 6.0f * 256.0f;"),

@@ -160,7 +160,16 @@ def test_prefill_full_size_sampled():
     ws = m.alloc_workspace(wl.M, wl.E, wl.H, wl.I, wl.top_k, wl.fmt)
     got = m.forward(wl.x, pw, wl.topk_ids, wl.topk_weights, workspace=ws)
     torch.cuda.synchronize()
-    tokens = list(range(0, wl.M, wl.M // 24))
+    # every expert's first and last routed row (its lowest and highest
+    # token: the first row of its first 128-row tile and the last valid row
+    # of its last tile), plus every 170th token
+    ids = wl.topk_ids.cpu().numpy()
+    tokens = set(range(0, wl.M, wl.M // 24))
+    for e in range(wl.E):
+        rows = np.nonzero((ids == e).any(axis=1))[0]
+        if rows.size:
+            tokens.update((int(rows[0]), int(rows[-1])))
+    tokens = sorted(tokens)
     sub_ids = wl.topk_ids[tokens]
     sub, ids_c, Ec = compact_for_oracle(wl.weights, sub_ids, wl.E, wl.fmt)
     want, _, _, _ = oracle.forward_prefill(wl.x[tokens], sub, ids_c, wl.topk_weights[tokens].cpu(), Ec, wl.H, wl.I,

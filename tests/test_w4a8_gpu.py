@@ -3,8 +3,9 @@
 Bit-exact: E4M3 element bytes and UE8M0 scale bytes of every 32-block, on
 rows with a wide spread of magnitudes, all-zero and negative-zero blocks,
 blocks whose maximum sits exactly on 448 * 2^j and one unit in the last
-place above it, values on every E4M3 rounding midpoint after scaling, and
-values below the normal FP32 range.
+place above it, values on every E4M3 rounding midpoint after scaling,
+values below the normal FP32 range, and blocks in the top FP32 binade
+(FLT_MAX, 448 * 2^119 and one unit above it).
 """
 import numpy as np
 import pytest
@@ -42,6 +43,17 @@ def _rows():
         a[6, 32 * b] = 448.0
         a[6, 32 * b + 1:32 * b + 1 + len(chunk)] = chunk
     a[7] = np.float32(1e-40) * rng.standard_normal(K).astype(np.float32)  # below the normal range
+    # the top FP32 binade: a block holding FLT_MAX (largest scale exponent),
+    # one whose maximum is 448 * 2^119 exactly and one a unit above it
+    fmax = np.finfo(np.float32).max
+    a[8, :32] = rng.standard_normal(32).astype(np.float32) * np.float32(1e37)
+    a[8, 5] = fmax
+    a[8, 6] = -fmax
+    top = np.float32(448.0 * 2.0 ** 119)
+    a[8, 32:64] = np.linspace(-1, 1, 32, dtype=np.float32) * top
+    a[8, 63] = top
+    a[8, 64:96] = a[8, 32:64]
+    a[8, 95] = np.nextafter(top, np.float32(np.inf))
     return a
 
 
