@@ -10,9 +10,20 @@ from workload import gen
 
 # Acceptance bound of the layer output against the FP64 oracle: cosine
 # similarity over the flattened [M, H] output >= 0.99995 and the largest
-# absolute error <= 2e-2 * RMS(oracle output).
+# absolute error <= 2e-2 * RMS(oracle output), the error counted beyond the
+# output's own BF16 rounding: |got - want| <= 2e-2 * RMS + ulp_bf16(want) / 2
+# (a correctly rounded BF16 output already misses an FP64 value by up to
+# half a BF16 unit in the last place, which exceeds 2e-2 * RMS wherever |want|
+# is above about ten times the RMS).
 COS_MIN = 0.99995
 MAXABS_REL_RMS = 2e-2
+
+
+def bf16_half_ulp(w: np.ndarray) -> np.ndarray:
+    """Half a BF16 unit in the last place at each |w| (8 significant bits)."""
+    a = np.abs(np.asarray(w, np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.ldexp(1.0, (e - 8).astype(np.int64)), 0.0)
 
 _built = False
 
@@ -44,7 +55,9 @@ def assert_layer_close(got: torch.Tensor, want: np.ndarray, what: str = ""):
         return
     cos, maxabs, rms = layer_metrics(got, want)
     assert cos >= COS_MIN, f"{what}: cosine {cos:.7f} < {COS_MIN}"
-    assert maxabs <= MAXABS_REL_RMS * rms, f"{what}: max abs err {maxabs:.3e} > {MAXABS_REL_RMS} * rms {rms:.3e}"
+    excess = float(np.max(np.abs(g.astype(np.float64) - w.reshape(g.shape)) - bf16_half_ulp(w.reshape(g.shape))))
+    assert excess <= MAXABS_REL_RMS * rms, \
+        f"{what}: max abs err beyond the BF16 rounding {excess:.3e} > {MAXABS_REL_RMS} * rms {rms:.3e} (raw {maxabs:.3e})"
     # zero rows of the oracle (tokens without a valid route) must be exact zeros
     zero_rows = ~np.any(w.reshape(g.shape) != 0, axis=-1)
     assert not np.any(g[zero_rows]), f"{what}: tokens without valid routes are not exactly zero"

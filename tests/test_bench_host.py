@@ -63,3 +63,22 @@ def test_stored_traffic_file_shape():
     # ten distinct routed experts plus x, out, ids and router weights of one token
     assert np.isclose(d["configs"]["decode_e512/M=1/nvfp4"]["algorithmic_bytes_per_layer"],
                       10 * gen.expert_bytes(2560, 320, gen.NVFP4) + 2560 * 2 * 2 + 10 * 8)
+
+
+def test_bf16_half_ulp_bounds_the_bf16_rounding():
+    """The parity tests' allowance for the BF16 output's own rounding: half a
+    BF16 unit in the last place bounds |bf16(w) - w| (torch's
+    round-to-nearest-even conversion), and the bound is reached at midpoints."""
+    import numpy as np
+    import torch
+    from tests.gpu_util import bf16_half_ulp
+    rng = np.random.default_rng(3)
+    # FP32 values (what the kernels round to BF16); torch converts FP64 via
+    # FP32, which would round twice
+    w = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32).astype(np.float64)
+    r = torch.tensor(w, dtype=torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.all(np.abs(r - w) <= bf16_half_ulp(w))
+    mid = np.array([1.0 + 2.0 ** -8, 0.75 + 2.0 ** -9, -(3.0 + 2.0 ** -7)])  # halfway between BF16 neighbours
+    rm = torch.tensor(mid, dtype=torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.allclose(np.abs(rm - mid), bf16_half_ulp(mid), rtol=0, atol=0)
+    assert bf16_half_ulp(np.array([0.0]))[0] == 0.0

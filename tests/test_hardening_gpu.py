@@ -1,0 +1,225 @@
+"""Parity where real inputs differ from the N(0, 1) draws of the workloads.
+
+* Outlier-heavy activations: per 256-wide K stage a few channels at 2^8 ..
+  2^12 times the RMS and whole 16-element blocks near 2^-20 times it, on
+  every decode plan and on the prefill band (against its mirrored oracle).
+  These exercise the tcgen05 kernels' four-term activation expansion and the
+  streaming GEMV's power-of-two FP16 rescaling per stage.
+* MXFP4 block scales spanning more than 2^17 inside one projection, with an
+  outlier activation channel on the smallest blocks: the resident layout
+  stores blocks more than 2^17 below the projection's largest as zero, so the
+  GPU must match the oracle on the weights with exactly those blocks zeroed;
+  the effect of that limit is measured against the unmodified oracle.
+* Workspaces filled with NaN bytes beyond the prefix that must start at zero.
+* Invalid routing slots (ids -1, E, 2^31 - 1) carrying NaN and infinite
+  router weights: they still contribute exactly zero.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.gpu_util import assert_layer_close, compact_for_oracle, ensure_built, layer_metrics, oracle_layer
+from workload import gen
+
+pytestmark = pytest.mark.gpu
+
+PLANS = {"gemv": 1, "chain": 2, "single": 3}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    ensure_built()
+
+
+def fm():
+    import fp4_weight_moe_gb300 as m
+    return m
+
+
+class plan:
+    def __init__(self, family):
+        self.family = family
+
+    def __enter__(self):
+        self.prev = fm()._capi.moe_fp4_debug_set_decode_family(self.family)
+
+    def __exit__(self, *exc):
+        fm()._capi.moe_fp4_debug_set_decode_family(self.prev)
+
+
+def outlier_activations(M, H, seed):
+    """N(0, 1) activations with, in every 256-wide K stage of every token, two
+    channels at 2^8 .. 2^12 (random sign) and one 16-element block scaled to
+    about 2^-20; returned as BF16."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((M, H)).astype(np.float32)
+    for t in range(M):
+        for st in range(0, H, 256):
+            ch = rng.choice(256, size=2, replace=False) + st
+            x[t, ch] = np.float32(2.0) ** rng.integers(8, 13, size=2) * rng.choice([-1.0, 1.0], size=2)
+            blk = st + 16 * int(rng.integers(0, 16))
+            if not np.any(np.isin(np.arange(blk, blk + 16), ch)):
+                x[t, blk:blk + 16] *= np.float32(2.0 ** -20)
+    return torch.from_numpy(x).to(torch.bfloat16)
+
+
+def _run(wl, ws=None, out=None):
+    m = fm()
+    pw = m.prepare_weights(wl.weights, wl.E, wl.H, wl.I, wl.fmt)
+    if ws is None:
+        ws = m.alloc_workspace(wl.M, wl.E, wl.H, wl.I, wl.top_k, wl.fmt)
+    if out is None:
+        out = torch.full((wl.M, wl.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    got = m.forward(wl.x, pw, wl.topk_ids, wl.topk_weights, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    assert m.workspace_status(ws) == 0
+    return got
+
+
+DECODE = [("decode_e512", dict(E=24)), ("decode_e512", dict(E=32, M=4, fmt=gen.MXFP4)),
+          ("decode_e288_m4", dict(E=24)), ("tiny_decode", dict(M=2, E=8))]
+
+
+@pytest.mark.parametrize("pname", list(PLANS))
+@pytest.mark.parametrize("name,ov", DECODE, ids=[f"{n}-{i}" for i, (n, _) in enumerate(DECODE)])
+def test_outlier_activations_decode(name, ov, pname):
+    wl = gen.make_workload(name, device="cuda", **ov)
+    wl.x = outlier_activations(wl.M, wl.H, seed=wl.M * 7 + wl.E).cuda()
+    with plan(PLANS[pname]):
+        got = _run(wl)
+    assert_layer_close(got, oracle_layer(wl), f"{name} {ov} outliers, plan {pname}")
+
+
+def test_outlier_activations_prefill():
+    wl = gen.make_workload("decode_e512", device="cuda", E=12, M=40, fmt=gen.NVFP4)
+    wl.x = outlier_activations(wl.M, wl.H, seed=3).cuda()
+    got = _run(wl)
+    want = oracle.forward_prefill(wl.x, wl.weights, wl.topk_ids, wl.topk_weights, wl.E, wl.H, wl.I, wl.top_k,
+                                  fmt=wl.fmt)[0]
+    assert_layer_close(got, want, "prefill band, outlier activations")
+
+
+def _mx_weights_with_wide_scales(E, H, I, seed):
+    """MXFP4 weights whose block exponents span 30 binades inside every
+    projection (UE8M0 bytes 140 down to 111: 2^13 .. 2^-16)."""
+    w = gen.make_expert_weights(E, H, I, gen.MXFP4, seed, device="cpu")
+    for key, rows, kb in (("s13", 2 * I, H // 32), ("s2", H, I // 32)):
+        exps = 140 - (torch.arange(rows * kb) % 30)
+        w[key] = exps.reshape(1, rows, kb).repeat(E, 1, 1).to(torch.uint8)
+    return w
+
+
+def _flush_small_blocks(w, H, I):
+    """The documented resident-layout limit: a block scale more than 2^17
+    below its projection's largest (gate, up and down separately) reads as
+    zero."""
+    out = {k: v.clone() for k, v in w.items()}
+    for key, wkey, sl in (("s13", "w13", slice(0, I)), ("s13", "w13", slice(I, 2 * I)), ("s2", "w2", slice(None))):
+        s = out[key][:, sl]
+        top = s.reshape(s.shape[0], -1).max(dim=1).values.to(torch.int32)
+        small = s.to(torch.int32) < (top - 17).reshape(-1, 1, 1)
+        nib = out[wkey][:, sl]
+        K2 = nib.shape[-1]
+        mask = small.repeat_interleave(16, dim=-1)[..., :K2]  # 32 elements = 16 bytes per block
+        nib[mask] = 0
+        out[wkey][:, sl] = nib
+    return out
+
+
+def test_mx_scale_span_limit_is_exactly_the_documented_flush():
+    E, H, I, M, k = 4, 512, 128, 2, 2
+    w = _mx_weights_with_wide_scales(E, H, I, seed=31)
+    ids = torch.tensor([[0, 1], [2, 3]], dtype=torch.int32)
+    tw = torch.tensor([[0.6, 0.4], [0.5, 0.5]], dtype=torch.float32)
+    # activations: N(0, 1), with an outlier channel at K = 0, whose block
+    # exponent cycles through all 30 binades over the rows (so it falls on
+    # flushed blocks in a third of them)
+    x = torch.randn((M, H), generator=torch.Generator().manual_seed(32))
+    assert int((w["s13"][0, :, 0].to(torch.int32) < 140 - 17).sum()) > 0
+    x[:, 0] = 4096.0
+    x = x.to(torch.bfloat16)
+    m = fm()
+    dw = {kk: v.cuda() for kk, v in w.items()}
+    pw = m.prepare_weights(dw, E, H, I, gen.MXFP4)
+    ws = m.alloc_workspace(M, E, H, I, k, gen.MXFP4)
+    out = m.forward(x.cuda(), pw, ids.cuda(), tw.cuda(), workspace=ws)
+    torch.cuda.synchronize()
+    flushed = oracle.forward(x, _flush_small_blocks(w, H, I), ids, tw, E, H, I, k, gen.MXFP4)
+    exact = oracle.forward(x, w, ids, tw, E, H, I, k, gen.MXFP4)
+    assert_layer_close(out, flushed, "MXFP4 wide scale span vs the flushed-block oracle")
+    # the limit's measured effect on this adversarial layer (recorded, not bounded)
+    cos, maxabs, rms = layer_metrics(out, exact)
+    print(f"MXFP4 scale span > 2^17 with an outlier on the smallest blocks: cosine {cos:.8f}, "
+          f"max abs / rms {maxabs / rms:.3e} against the unflushed oracle")
+    assert np.isfinite(cos)
+
+
+def _poisoned_workspace(M, E, H, I, k, fmt):
+    m = fm()
+    n = m.workspace_bytes(M, E, H, I, k, fmt)
+    z = m._capi.moe_fp4_workspace_zero_bytes(E, H, I, k, fmt)
+    ws = torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda")  # NaN in every FP32 / BF16 / E4M3 slot
+    ws[:z] = 0
+    return ws
+
+
+@pytest.mark.parametrize("pname", list(PLANS))
+@pytest.mark.parametrize("name,ov", [("decode_e512", dict(E=24)), ("decode_e288_m4", dict(E=24, M=3)),
+                                     ("tiny_decode", dict(M=2, E=8)), ("decode_e512", dict(E=24, M=12))])
+def test_nan_poisoned_workspace(name, ov, pname):
+    wl = gen.make_workload(name, device="cuda", **ov)
+    ws = _poisoned_workspace(wl.M, wl.E, wl.H, wl.I, wl.top_k, wl.fmt)
+    with plan(PLANS[pname]):
+        got = _run(wl, ws=ws)
+    assert_layer_close(got, oracle_layer(wl), f"{name} {ov} poisoned workspace, plan {pname}")
+
+
+def test_nan_poisoned_workspace_prefill():
+    wl = gen.make_workload("decode_e512", device="cuda", E=12, M=40)
+    ws = _poisoned_workspace(wl.M, wl.E, wl.H, wl.I, wl.top_k, wl.fmt)
+    got = _run(wl, ws=ws)
+    want = oracle.forward_prefill(wl.x, wl.weights, wl.topk_ids, wl.topk_weights, wl.E, wl.H, wl.I, wl.top_k,
+                                  fmt=wl.fmt)[0]
+    assert_layer_close(got, want, "prefill band, poisoned workspace")
+
+
+def _invalid_with_bad_weights(wl, seed):
+    """Every token gets invalid slots (-1, E, 2^31 - 1 in turn) whose router
+    weights are NaN, +inf or -inf; returns the oracle's ids (the invalid
+    slots removed, their weights zero)."""
+    rng = np.random.default_rng(seed)
+    ids = wl.topk_ids.cpu().numpy().copy()
+    tw = wl.topk_weights.cpu().numpy().copy()
+    bad_ids = [-1, wl.E, 2 ** 31 - 1]
+    bad_w = [np.nan, np.inf, -np.inf]
+    for t in range(wl.M):
+        for i, j in enumerate(rng.choice(wl.top_k, size=min(2, wl.top_k - 1), replace=False)):
+            ids[t, j] = bad_ids[(t + i) % 3]
+            tw[t, j] = bad_w[(t + 2 * i) % 3]
+    wl.topk_ids = torch.from_numpy(ids).cuda()
+    wl.topk_weights = torch.from_numpy(tw).cuda()
+    tw_clean = np.where((ids >= 0) & (ids < wl.E), tw, 0.0).astype(np.float32)
+    return tw_clean
+
+
+@pytest.mark.parametrize("pname", list(PLANS))
+@pytest.mark.parametrize("name,ov", [("decode_e512", dict(E=24)), ("decode_e288_m4", dict(E=24)),
+                                     ("tiny_decode", dict(M=3, E=8, top_k=3))])
+def test_invalid_slots_with_nan_and_inf_weights(name, ov, pname):
+    wl = gen.make_workload(name, device="cuda", **ov)
+    tw_clean = _invalid_with_bad_weights(wl, seed=wl.E)
+    with plan(PLANS[pname]):
+        got = _run(wl)
+    sub, ids_c, Ec = compact_for_oracle(wl.weights, wl.topk_ids, wl.E, wl.fmt)
+    want = oracle.forward(wl.x, sub, ids_c, tw_clean, Ec, wl.H, wl.I, wl.top_k, wl.fmt)
+    assert_layer_close(got, want, f"{name} {ov} NaN/inf weights on invalid slots, plan {pname}")
+
+
+def test_invalid_slots_with_nan_and_inf_weights_prefill():
+    wl = gen.make_workload("decode_e512", device="cuda", E=12, M=40)
+    tw_clean = _invalid_with_bad_weights(wl, seed=5)
+    got = _run(wl)
+    want = oracle.forward_prefill(wl.x, wl.weights, wl.topk_ids.cpu(), tw_clean, wl.E, wl.H, wl.I, wl.top_k,
+                                  fmt=wl.fmt)[0]
+    assert_layer_close(got, want, "prefill band, NaN/inf weights on invalid slots")
