@@ -111,6 +111,45 @@ def unprepare_weights(pw: PreparedWeights, stream=None) -> dict:
     return out
 
 
+def prepare_weights_relu2(weights: dict, E: int, H: int, I: int, fmt: int, stream=None) -> PreparedWeights:
+    """Repack a non-gated (squared-ReLU) expert checkpoint: dict with w1
+    [E][I][H/2], s1, w2, s2 and, for NVFP4, g1, g2 (CUDA tensors).  The
+    result's w13/s13 fields hold the resident w1/s1; run it with
+    ``forward_act(..., kind=ACT_RELU2)``."""
+    w1_l, s1_l, w2_l, s2_l = (weights[k].contiguous() for k in ("w1", "s1", "w2", "s2"))
+    g1 = weights.get("g1") if fmt == NVFP4 else None
+    g2 = weights.get("g2") if fmt == NVFP4 else None
+    if g1 is not None:
+        g1 = g1.contiguous().float()
+        g2 = g2.contiguous().float()
+    _require_cuda(w1_l, s1_l, w2_l, s2_l, g1, g2)
+    dev = w1_l.device
+    sizes = _capi.moe_fp4_prepared_sizes_relu2(E, H, I, fmt)
+    out = [torch.empty(n, dtype=torch.uint8, device=dev) for n in sizes]
+    _capi.moe_fp4_prepare_weights_relu2(_ptr(w1_l), _ptr(s1_l), _ptr(g1), _ptr(w2_l), _ptr(s2_l), _ptr(g2), E, H,
+                                        I, fmt, *[_ptr(t) for t in out], _stream(stream))
+    return PreparedWeights(*out, E=E, H=H, I=I, fmt=fmt)
+
+
+def unprepare_weights_relu2(pw: PreparedWeights, stream=None) -> dict:
+    """Resident -> logical tensors of a non-gated checkpoint (test support)."""
+    E, H, I, fmt = pw.E, pw.H, pw.I, pw.fmt
+    B = 32 if fmt == MXFP4 else 16
+    dev = pw.w13.device
+    w1 = torch.empty((E, I, H // 2), dtype=torch.uint8, device=dev)
+    s1 = torch.empty((E, I, H // B), dtype=torch.uint8, device=dev)
+    w2 = torch.empty((E, H, I // 2), dtype=torch.uint8, device=dev)
+    s2 = torch.empty((E, H, I // B), dtype=torch.uint8, device=dev)
+    g1 = torch.empty((E,), dtype=torch.float32, device=dev) if fmt == NVFP4 else None
+    g2 = torch.empty((E,), dtype=torch.float32, device=dev) if fmt == NVFP4 else None
+    _capi.moe_fp4_unprepare_weights_relu2(*pw.ptrs(), E, H, I, fmt, _ptr(w1), _ptr(s1), _ptr(g1), _ptr(w2), _ptr(s2),
+                                          _ptr(g2), _stream(stream))
+    out = dict(w1=w1, s1=s1, w2=w2, s2=s2)
+    if fmt == NVFP4:
+        out.update(g1=g1, g2=g2)
+    return out
+
+
 def workspace_bytes(M_max: int, E: int, H: int, I: int, top_k: int, fmt: int) -> int:
     return _capi.moe_fp4_workspace_bytes(M_max, E, H, I, top_k, fmt)
 
@@ -159,15 +198,16 @@ def forward(x: torch.Tensor, pw: PreparedWeights, topk_ids: torch.Tensor, topk_w
     return out
 
 
-ACT_SILU, ACT_GELU_TANH, ACT_SWIGLUOAI = (_capi.MOE_FP4_ACT_SILU, _capi.MOE_FP4_ACT_GELU_TANH,
-                                        _capi.MOE_FP4_ACT_SWIGLUOAI)
+ACT_SILU, ACT_GELU_TANH, ACT_SWIGLUOAI, ACT_RELU2 = (_capi.MOE_FP4_ACT_SILU, _capi.MOE_FP4_ACT_GELU_TANH,
+                                                   _capi.MOE_FP4_ACT_SWIGLUOAI, _capi.MOE_FP4_ACT_RELU2)
 
 
 def forward_act(x: torch.Tensor, pw: PreparedWeights, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
                 workspace: torch.Tensor, kind: int = ACT_SILU, alpha: float = 0.0, beta: float = 1.0,
                 limit: float = 0.0, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """The layer with a chosen gated activation (ACT_SILU, ACT_GELU_TANH, or
-    ACT_SWIGLUOAI with alpha, beta, limit), on a caller-owned workspace."""
+    """The layer with a chosen activation (ACT_SILU, ACT_GELU_TANH, or
+    ACT_SWIGLUOAI with alpha, beta, limit; ACT_RELU2 with weights from
+    prepare_weights_relu2), on a caller-owned workspace."""
     _check_dtypes(x, topk_ids, topk_weights)
     _require_cuda(x, topk_ids, topk_weights, out, workspace)
     M, H = x.shape
@@ -213,9 +253,10 @@ def forward_host(x: torch.Tensor, pw: PreparedWeights, topk_ids: torch.Tensor, t
 
 
 def debug_dequant(pw: PreparedWeights, which: int, expert: int, stream=None) -> torch.Tensor:
-    rows, K = (2 * pw.I, pw.H) if which == 0 else (pw.H, pw.I)
+    """which: 0 w13, 1 w2, 2 the w1 of non-gated (squared-ReLU) weights."""
+    rows, K = {0: (2 * pw.I, pw.H), 1: (pw.H, pw.I), 2: (pw.I, pw.H)}[which]
     out = torch.empty((rows, K), dtype=torch.float32, device=pw.w13.device)
-    w, s = (pw.w13, pw.s13) if which == 0 else (pw.w2, pw.s2)
+    w, s = (pw.w2, pw.s2) if which == 1 else (pw.w13, pw.s13)
     _capi.moe_fp4_debug_dequant(_ptr(w), _ptr(s), which, expert, pw.E, pw.H, pw.I, pw.fmt, _ptr(out),
                                 _stream(stream))
     return out

@@ -27,6 +27,7 @@ MOE_FP4_NOALLOC_SCRATCH_BYTES = 16 << 20
 MOE_FP4_ACT_SILU = 0
 MOE_FP4_ACT_GELU_TANH = 1
 MOE_FP4_ACT_SWIGLUOAI = 2
+MOE_FP4_ACT_RELU2 = 3
 MOE_FP4_STATUS_OK = 0
 MOE_FP4_STATUS_TEST_WAIT = 8192
 
@@ -48,6 +49,9 @@ SIGNATURES = {
     "moe_fp4_version": (_I, []),
     "moe_fp4_prepared_sizes": (_I, [_I, _I, _I, _I, _PZ, _PZ, _PZ, _PZ]),
     "moe_fp4_prepare_weights": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "moe_fp4_prepared_sizes_relu2": (_I, [_I, _I, _I, _I, _PZ, _PZ, _PZ, _PZ]),
+    "moe_fp4_prepare_weights_relu2": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "moe_fp4_unprepare_weights_relu2": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "moe_fp4_unprepare_weights": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "moe_fp4_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
     "moe_fp4_workspace_zero_bytes": (_Z, [_I, _I, _I, _I, _I]),
@@ -144,6 +148,23 @@ def moe_fp4_unprepare_weights(w13, s13, w2, s2, E, H, I, fmt, w13_l, s13_l, g13,
     return _check("moe_fp4_unprepare_weights",
                   _load().moe_fp4_unprepare_weights(w13, s13, w2, s2, E, H, I, fmt, w13_l, s13_l, g13, w2_l, s2_l,
                                                     g2, stream))
+
+
+def moe_fp4_prepared_sizes_relu2(E, H, I, fmt):
+    out = [ctypes.c_size_t(0) for _ in range(4)]
+    _check("moe_fp4_prepared_sizes_relu2",
+           lib().moe_fp4_prepared_sizes_relu2(E, H, I, fmt, *[ctypes.byref(o) for o in out]))
+    return tuple(o.value for o in out)
+
+
+def moe_fp4_prepare_weights_relu2(w1_l, s1_l, g1, w2_l, s2_l, g2, E, H, I, fmt, w1, s1, w2, s2, stream):
+    _check("moe_fp4_prepare_weights_relu2",
+           lib().moe_fp4_prepare_weights_relu2(w1_l, s1_l, g1, w2_l, s2_l, g2, E, H, I, fmt, w1, s1, w2, s2, stream))
+
+
+def moe_fp4_unprepare_weights_relu2(w1, s1, w2, s2, E, H, I, fmt, w1_l, s1_l, g1, w2_l, s2_l, g2, stream):
+    _check("moe_fp4_unprepare_weights_relu2",
+           lib().moe_fp4_unprepare_weights_relu2(w1, s1, w2, s2, E, H, I, fmt, w1_l, s1_l, g1, w2_l, s2_l, g2, stream))
 
 
 def moe_fp4_workspace_bytes(M_max, E, H, I, top_k, fmt) -> int:

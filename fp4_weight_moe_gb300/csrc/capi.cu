@@ -14,6 +14,9 @@ cudaError_t launch_prepare(const void* w13_l, const void* s13_l, const float* g1
                            void* w2, void* s2, cudaStream_t st, bool inverse);
 cudaError_t launch_debug_dequant(const void* w, const void* s, int which, int e, int E, int H, int I, int fmt,
                                  float* out, cudaStream_t st);
+cudaError_t launch_prepare_relu2(const void* w1_l, const void* s1_l, const float* g1, const void* w2_l,
+                                 const void* s2_l, const float* g2, int E, int H, int I, int fmt, void* w1, void* s1,
+                                 void* w2, void* s2, cudaStream_t st, bool inverse);
 size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int fmt, int num_sms);
 size_t decode_sync_bytes(int H, int I, int top_k);
 cudaError_t launch_debug_gemm(const void* a_q, const void* a_sf, const void* b_q, const void* b_sf, float* d,
@@ -212,6 +215,45 @@ int moe_fp4_prepared_sizes(int E, int H, int I, int fmt, size_t* w13_bytes, size
   return MOE_FP4_OK;
 }
 
+int moe_fp4_prepared_sizes_relu2(int E, int H, int I, int fmt, size_t* w1_bytes, size_t* s1_bytes, size_t* w2_bytes,
+                                 size_t* s2_bytes) {
+  int st = check_shape(E, H, I, 1, fmt);
+  if (st != MOE_FP4_OK) return st;
+  auto pad16 = [](size_t v) { return (v + 15) & ~(size_t)15; };
+  const int rows1 = (I + kRowTile - 1) / kRowTile * kRowTile;
+  if (w1_bytes) *w1_bytes = (size_t)E * I * (H / 2);
+  if (s1_bytes) *s1_bytes = pad16((size_t)E * scale_chunk_bytes(rows1, H) + sizeof(float) * (size_t)E);
+  if (w2_bytes) *w2_bytes = (size_t)E * H * (I / 2);
+  if (s2_bytes) *s2_bytes = pad16((size_t)E * scale_chunk_bytes(H, I) + sizeof(float) * (size_t)E);
+  return MOE_FP4_OK;
+}
+
+int moe_fp4_prepare_weights_relu2(const void* w1_logical, const void* s1_logical, const float* g1,
+                                  const void* w2_logical, const void* s2_logical, const float* g2, int E, int H, int I,
+                                  int fmt, void* w1, void* s1, void* w2, void* s2, void* stream) {
+  int st = check_shape(E, H, I, 1, fmt);
+  if (st != MOE_FP4_OK) return st;
+  if (!w1_logical || !s1_logical || !w2_logical || !s2_logical || !w1 || !s1 || !w2 || !s2) return MOE_FP4_EINVAL;
+  if (fmt == MOE_FP4_NVFP4 && (!g1 || !g2)) return MOE_FP4_EINVAL;
+  if (!aligned16(w1) || !aligned16(s1) || !aligned16(w2) || !aligned16(s2)) return MOE_FP4_EINVAL;
+  cudaError_t e = launch_prepare_relu2(w1_logical, s1_logical, g1, w2_logical, s2_logical, g2, E, H, I, fmt, w1, s1,
+                                       w2, s2, static_cast<cudaStream_t>(stream), false);
+  return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
+}
+
+int moe_fp4_unprepare_weights_relu2(const void* w1, const void* s1, const void* w2, const void* s2, int E, int H,
+                                    int I, int fmt, void* w1_logical, void* s1_logical, float* g1, void* w2_logical,
+                                    void* s2_logical, float* g2, void* stream) {
+  int st = check_shape(E, H, I, 1, fmt);
+  if (st != MOE_FP4_OK) return st;
+  if (!w1_logical || !s1_logical || !w2_logical || !s2_logical || !w1 || !s1 || !w2 || !s2) return MOE_FP4_EINVAL;
+  if (fmt == MOE_FP4_NVFP4 && (!g1 || !g2)) return MOE_FP4_EINVAL;
+  cudaError_t e = launch_prepare_relu2(w1_logical, s1_logical, g1, w2_logical, s2_logical, g2, E, H, I, fmt,
+                                       const_cast<void*>(w1), const_cast<void*>(s1), const_cast<void*>(w2),
+                                       const_cast<void*>(s2), static_cast<cudaStream_t>(stream), true);
+  return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
+}
+
 int moe_fp4_prepare_weights(const void* w13_logical, const void* s13_logical, const float* g13,
                             const void* w2_logical, const void* s2_logical, const float* g2, int E, int H, int I,
                             int fmt, void* w13, void* s13, void* w2, void* s2, void* stream) {
@@ -335,7 +377,8 @@ int forward_any_ids(const void* x_bf16, const void* w13, const void* s13, const 
   const int32_t* ids = static_cast<const int32_t*>(topk_ids);
   ActParams ap = {MOE_FP4_ACT_SILU, 0.f, 0.f, 0.f};
   if (act) {
-    if (act->kind != MOE_FP4_ACT_SILU && act->kind != MOE_FP4_ACT_GELU_TANH && act->kind != MOE_FP4_ACT_SWIGLUOAI)
+    if (act->kind != MOE_FP4_ACT_SILU && act->kind != MOE_FP4_ACT_GELU_TANH && act->kind != MOE_FP4_ACT_SWIGLUOAI &&
+        act->kind != MOE_FP4_ACT_RELU2)
       return MOE_FP4_EINVAL;
     if (act->kind == MOE_FP4_ACT_SWIGLUOAI &&
         (!std::isfinite(act->alpha) || !std::isfinite(act->beta) || !(act->limit > 0.f)))
@@ -590,7 +633,7 @@ int moe_fp4_debug_dequant(const void* w, const void* s, int which, int expert, i
                           float* out_f32, void* stream) {
   int st = check_shape(E, H, I, 1, fmt);
   if (st != MOE_FP4_OK) return st;
-  if (!w || !s || !out_f32 || (which != 0 && which != 1) || expert < 0 || expert >= E) return MOE_FP4_EINVAL;
+  if (!w || !s || !out_f32 || which < 0 || which > 2 || expert < 0 || expert >= E) return MOE_FP4_EINVAL;
   cudaError_t e = launch_debug_dequant(w, s, which, expert, E, H, I, fmt, out_f32, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
 }

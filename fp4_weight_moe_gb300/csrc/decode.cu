@@ -97,7 +97,9 @@ cudaError_t launch_decode(const void* x, const void* w13, const void* s13, const
   uint32_t* status = reinterpret_cast<uint32_t*>(base);
   uint32_t* sync = reinterpret_cast<uint32_t*>(base + kStatusBytes);
   float* scratch = reinterpret_cast<float*>(base + kStatusBytes + decode_sync_bytes(H, I, top_k));
-  switch (decode_family_of(M, E, H, I, top_k)) {
+  // non-gated experts (squared ReLU) run on the tcgen05 launch chain only
+  const int plan = act.kind == MOE_FP4_ACT_RELU2 ? 2 : decode_family_of(M, E, H, I, top_k);
+  switch (plan) {
     case 1:
       return launch_decode_gemv(x, w13, s13, w2, s2, ids, ids64, tw, out, M, E, H, I, top_k, act, scratch, status, st,
                                 &cu);

@@ -368,7 +368,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   // `split` CTAs per w2 row tile
   const uint32_t rank = cluster_rank();
   const int unit = blockIdx.x / split;  // FC1: slot * tiles1 + tile; FC2: w2 row tile
-  const int tiles1 = I / 64, ns2 = (I + 255) / 256;
+  // FC1 of non-gated experts (squared ReLU): w1 tiles of 128 rows (h values),
+  // the last one padded (its scale rows past I are zero)
+  const bool relu2 = !kFc2 && a.act.kind == MOE_FP4_ACT_RELU2;
+  const int tiles1 = relu2 ? (I + 127) / 128 : I / 64, ns2 = (I + 255) / 256;
   const bool is_quant = warp >= kQuantWarp0 && warp < kQuantWarp0 + kQuantWarps;
   // activation terms from a pre-pass image (FC1 always, FC2 for larger M)
   // or built in this CTA (FC2 for small M)
@@ -403,7 +406,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     // FC1 the gate and up rows of pairs p = rank mod split, FC2 the rows
     // r = rank mod split
     mbar_init(&S.red, 1);
-    const int own = kFc2 ? (128 - (int)rank + split - 1) / split : 2 * ((64 - (int)rank + split - 1) / split);
+    const int own = kFc2 || relu2 ? (128 - (int)rank + split - 1) / split : 2 * ((64 - (int)rank + split - 1) / split);
     mbar_arrive_expect_tx(&S.red, (uint32_t)(split * own * M * 4));
     fence_mbar_init();
     tma_prefetch_desc(&map_w);
@@ -434,7 +437,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     int row0;
     const uint8_t* sfa;
     if (!kFc2) {
-      row0 = e * 2 * I + tile * 128;
+      row0 = (relu2 ? e * I : e * 2 * I) + tile * 128;
       sfa = a.s13 + (((uint64_t)e * tiles1 + tile) * KG + 4 * (uint64_t)st) * kChunkBytes;
     } else {
       row0 = e * H + unit * 128;
@@ -520,7 +523,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     if (warp == kQuantWarp0 && lane < 3) {  // (FC1's builder warps are free)
       const float* gl13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * tiles1 * (H / 64) * kChunkBytes);
       const float* gl2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * (H / 128) * (I / 64) * kChunkBytes);
-      S.g3[lane] = ld_nc_f32(lane < 2 ? gl13 + 2 * e1 + lane : gl2 + e1);
+      // gated: gate, up, down multipliers; non-gated: w1's ([E]) twice, down
+      S.g3[lane] = ld_nc_f32(lane < 2 ? (relu2 ? gl13 + e1 : gl13 + 2 * e1 + lane) : gl2 + e1);
     }
   } else {
     // owners: the first slot naming each valid expert, in slot order
@@ -750,13 +754,13 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   __syncwarp();
   cluster_wait();  // phase 1: every CTA of the cluster runs
   // FC1: pair p is owned by rank p % split (cpo pairs each, gate and up rows);
-  // FC2: row r by rank r % split
+  // FC2 and non-gated FC1: row r by rank r % split
   const int cpo = (64 + split - 1) / split;
-  const int rpo = kFc2 ? (128 + split - 1) / split : 2 * cpo;
+  const int rpo = kFc2 || relu2 ? (128 + split - 1) / split : 2 * cpo;
   if (is_epi) {
     const int row = 32 * (warp & 3) + lane;
     int owner, j;
-    if (!kFc2) {
+    if (!kFc2 && !relu2) {
       const int pr = row & 63;
       owner = pr % split;
       j = (row >> 6) * cpo + pr / split;
@@ -772,7 +776,19 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
   __syncthreads();  // tensor memory is no longer read
   if (warp == kMmaWarp0) tmem_dealloc(S.tmem, kTmemColsTc);
   if (!__all_sync(0xffffffffu, mbar_wait(&S.red, 0, a.status, 128u))) return;
-  if (!kFc2) {
+  if (relu2) {
+    // h_n = max(u_n, 0)^2 x (router weight) x (down multiplier), rows of the
+    // tile below I
+    for (int idx = threadIdx.x; idx < M * rpo; idx += kTcThreads) {
+      const int token = idx / rpo, j = idx % rpo, row = (int)rank + split * j;
+      if (row >= 128 || tile * 128 + row >= I) continue;
+      float u = 0.f;
+      for (int src = 0; src < split; ++src) u += S.part[(src * M + token) * rpo + j];
+      const float r = fmaxf(u * S.g3[0], 0.f);
+      const float hv = (S.routed >> token) & 1u ? r * r * (S.wtok[token] * S.g3[2]) : 0.f;
+      a.h[((size_t)slot1 * M + token) * I + tile * 128 + row] = hv;
+    }
+  } else if (!kFc2) {
     for (int idx = threadIdx.x; idx < M * cpo; idx += kTcThreads) {
       const int token = idx / cpo, jj = idx % cpo, pair = (int)rank + split * jj;
       if (pair >= 64) continue;
@@ -1249,8 +1265,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // K ranges per w13 tile: about 1.5 CTAs per SM in total (measured best on
 // GB300 for 1..8 tokens: more ranges shorten each CTA's weight stream, fewer
 // leave room for FC2's CTAs beside them), at most 8.
-int fc1_split(int n_slots, int H, int I, int sms) {
-  const int units = n_slots * (I / 64), nk = H / 256;
+int fc1_split(int units, int H, int sms) {
+  const int nk = H / 256;
   int s = 3 * sms / (2 * units);
   s = s > 8 ? 8 : s;
   s = s > nk ? nk : s;
@@ -1302,7 +1318,9 @@ cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, co
                              int top_k, const ActParams& act, float* scratch, uint32_t* status, int num_sms, cudaStream_t st,
                              int* cu_err) {
   CUtensorMap m13, m2;
-  CUresult r = make_fp4_map(&m13, w13, (uint64_t)H / 2, (uint64_t)E * 2 * I, 128);
+  // (w13: 2I rows per expert; the w1 of non-gated experts: I)
+  const uint64_t rows13 = (uint64_t)E * (act.kind == MOE_FP4_ACT_RELU2 ? I : 2 * I);
+  CUresult r = make_fp4_map(&m13, w13, (uint64_t)H / 2, rows13, 128);
   if (r == CUDA_SUCCESS) r = make_fp4_map(&m2, w2, (uint64_t)I / 2, (uint64_t)E * H, 128);
   if (r != CUDA_SUCCESS) {
     *cu_err = (int)r;
@@ -1365,8 +1383,9 @@ cudaError_t launch_decode_tc(const void* x, const void* w13, const void* s13, co
 
   // FC1: K ranges per w13 tile (independent CTAs); programmatic dependent
   // launch so that its prologue overlaps the pre-pass
-  const int units1 = a.n_slots * (I / 64);
-  const int s1 = fc1_split(a.n_slots, H, I, sms);
+  const int tiles1 = act.kind == MOE_FP4_ACT_RELU2 ? (I + 127) / 128 : I / 64;
+  const int units1 = a.n_slots * tiles1;
+  const int s1 = fc1_split(units1, H, sms);
   a.split = s1;
   cudaLaunchAttribute at1[2];
   at1[0].id = cudaLaunchAttributeClusterDimension;

@@ -503,9 +503,12 @@ template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     fc1_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                     PrefillArgs a) {
-  const int NT = 2 * a.I / BN;
+  // non-gated experts (squared ReLU): N tiles of 128 w1 rows, the expert's
+  // last one padded (its scale rows past I are zero); gated: 2I rows
+  const bool relu2 = a.act.kind == MOE_FP4_ACT_RELU2;
+  const int NT = relu2 ? (a.I + 127) / 128 : 2 * a.I / BN;
   const int KG = a.H / 64;
-  const size_t scb = scale_chunk_bytes(2 * a.I, a.H);
+  const size_t scb = scale_chunk_bytes(relu2 ? NT * 128 : 2 * a.I, a.H);
   const float* g13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * scb);
   const int n_mt = *a.num_tiles;
   auto tile_of = [&](int idx) {
@@ -517,7 +520,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (!t.valid) return t;
     const int e = a.tile_expert[mt];
     t.a_row0 = kGemmBM * mt;
-    t.b_row0 = e * 2 * a.I + BN * nt;
+    t.b_row0 = (relu2 ? e * a.I : e * 2 * a.I) + BN * nt;
     t.a_sf = a.xsf + (size_t)mt * KG * kChunkBytes;
     t.b_sf0 = a.s13 + (size_t)e * scb + (size_t)(BN / 128) * nt * KG * kChunkBytes;
     t.b_sf1 = t.b_sf0 + (size_t)KG * kChunkBytes;
@@ -528,6 +531,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int e = a.tile_expert[t.m_tile];
     const bool live = a.row_src[r] >= 0;
     const float xg = live ? a.xG[r] : 0.f;
+    if (relu2) {
+      // h = max(u, 0)^2 in BF16 for the tile's rows of w1 below I (BN = 128)
+      const float s1 = xg * g13[e];
+      __nv_bfloat16* hrow = a.hbuf + (size_t)r * a.I;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {  // 32-column chunks (I % 64 == 0: whole chunks)
+        uint32_t u[32];
+        tmem_ld32(tmem_row + 32 * c, u);
+        const int n0 = 128 * t.n_tile + 32 * c;
+        if (!live || n0 >= a.I) continue;
+        uint32_t packed[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float r0 = fmaxf(__uint_as_float(u[2 * j]) * s1, 0.f);
+          const float r1 = fmaxf(__uint_as_float(u[2 * j + 1]) * s1, 0.f);
+          const __nv_bfloat162 hv = __floats2bfloat162_rn(r0 * r0, r1 * r1);
+          packed[j] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(hrow + n0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+      }
+      return;
+    }
     const float sgate = xg * g13[2 * e], sup = xg * g13[2 * e + 1];
     __nv_bfloat16* hrow = a.hbuf + (size_t)r * a.I;
 #pragma unroll 1
@@ -824,7 +852,9 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
   // with 256-wide tiles (one accumulator: tensor memory also holds the ring's
   // scale factors).
   constexpr int bn1 = 128;
-  if (r == CUDA_SUCCESS) r = make_fp4_map(&mw13, w13, (uint64_t)H / 2, (uint64_t)E * 2 * I, (uint32_t)bn1);
+  const bool relu2 = act.kind == MOE_FP4_ACT_RELU2;  // non-gated experts: w1 of I rows
+  if (r == CUDA_SUCCESS)
+    r = make_fp4_map(&mw13, w13, (uint64_t)H / 2, (uint64_t)E * (relu2 ? I : 2 * I), (uint32_t)bn1);
   if (r == CUDA_SUCCESS) r = make_fp4_map(&mh, a.hq, (uint64_t)I / 2, rows, kGemmBM);
   if (r == CUDA_SUCCESS) r = make_fp4_map(&mw2, w2, (uint64_t)I / 2, (uint64_t)E * H, kFc2BN);
   if (r != CUDA_SUCCESS) {
@@ -848,7 +878,7 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
   cudaError_t es = gemm_sms(&sms);
   if (es != cudaSuccess) return es;
   // persistent: one CTA per SM (the valid tile count is known on the device)
-  const int g1 = c.max_tiles * (2 * I / bn1), g2 = c.max_tiles * (H / kFc2BN);
+  const int g1 = c.max_tiles * (relu2 ? (I + 127) / 128 : 2 * I / bn1), g2 = c.max_tiles * (H / kFc2BN);
   fc1_gemm_kernel<bn1><<<g1 < sms ? g1 : sms, kGemmThreads, GemmCfg<bn1>::kSmem, st>>>(mx, mw13, a);
   quant_h_kernel<<<(int)((rows + 7) / 8), 256, 0, st>>>(a);
   fc2_gemm_kernel<<<g2 < sms ? g2 : sms, kGemmThreads, GemmCfg<kFc2BN>::kSmem, st>>>(mh, mw2, a);

@@ -58,11 +58,14 @@ __device__ __forceinline__ int e4m3_pow2_exp(uint32_t b) {
   return b == 4u ? -7 : (b == 2u ? -8 : -9);
 }
 
-// Scales: logical [E][rows][K/B] <-> resident chunks of E4M3 bytes per 16.
-// g [E][nproj]: the projection multipliers (MXFP4: 2^b, written before this
-// kernel runs); nproj = 2 for w13 (rows < I gate, >= I up), 1 for w2.
+// Scales: logical [E][lrows][K/B] <-> resident chunks of E4M3 bytes per 16,
+// `rows` (lrows rounded up to a multiple of 128) per expert; the resident
+// bytes of rows past lrows are zero.  g [E][nproj]: the projection
+// multipliers (MXFP4: 2^b, written before this kernel runs); nproj = 2 for
+// w13 (rows < I gate, >= I up), 1 for w2 and w1.
 __global__ void repack_scales_kernel(const uint8_t* __restrict__ in, uint8_t* __restrict__ out, int E, int rows,
-                                     int K, int fmt, int I_for_w13, const float* __restrict__ g, bool inverse) {
+                                     int lrows, int K, int fmt, int I_for_w13, const float* __restrict__ g,
+                                     bool inverse) {
   const int KB = K / block_size(fmt);    // logical blocks per row
   const int KBr = K / kResBlock;         // resident blocks per row
   const int KG = k_groups(K);
@@ -80,8 +83,8 @@ __global__ void repack_scales_kernel(const uint8_t* __restrict__ in, uint8_t* __
     const int lrow = I_for_w13 > 0 ? w13_logical_row(row, I_for_w13) : row;
     const int proj = I_for_w13 > 0 && lrow >= I_for_w13 ? 1 : 0;
     const int lkb = mx ? kb / 2 : kb;  // logical block
-    const size_t li = ((size_t)e * rows + lrow) * KB + lkb;
-    if (kb >= KBr) {
+    const size_t li = ((size_t)e * lrows + lrow) * KB + lkb;
+    if (kb >= KBr || row >= lrows) {
       if (!inverse) out[idx] = 0;
       continue;
     }
@@ -133,15 +136,17 @@ __global__ void mx_multiplier_kernel(const uint8_t* __restrict__ s_logical, int 
 }
 
 // Dequantise one expert's projection (logical row order) for tests:
-// e2m1 * scale * g, as the kernels use them.
+// e2m1 * scale * g, as the kernels use them.  which: 0 w13, 1 w2, 2 w1
+// (non-gated experts: I rows, scale rows padded to a multiple of 128).
 __global__ void debug_dequant_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ s, int which, int e,
                                      int E, int H, int I, float* __restrict__ out) {
-  const int rows = which == 0 ? 2 * I : H;
-  const int K = which == 0 ? H : I;
+  const int rows = which == 0 ? 2 * I : (which == 1 ? H : I);
+  const int K = which == 1 ? I : H;
+  const int srows = which == 2 ? (I + kRowTile - 1) / kRowTile * kRowTile : rows;
   const int KG = k_groups(K);
   const uint8_t* wexp = w + (size_t)e * rows * (K / 2);
-  const uint8_t* sexp = s + (size_t)e * scale_chunk_bytes(rows, K);
-  const float* gl = reinterpret_cast<const float*>(s + (size_t)E * scale_chunk_bytes(rows, K));
+  const uint8_t* sexp = s + (size_t)e * scale_chunk_bytes(srows, K);
+  const float* gl = reinterpret_cast<const float*>(s + (size_t)E * scale_chunk_bytes(srows, K));
   const size_t total = (size_t)rows * K;
   for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
     int L = (int)(idx / K), k = (int)(idx % K);
@@ -164,6 +169,32 @@ static int grid_for(size_t n, int threads) {
   return (int)b;
 }
 
+// w2 and its scales (shared by the gated and the non-gated layouts): the
+// multipliers first (the MXFP4 scale conversion reads them), then the scale
+// chunks and the nibbles (the logical layout).
+static cudaError_t prepare_w2(const void* w2_l, const void* s2_l, const float* g2, int E, int H, int I, int fmt,
+                              void* w2, void* s2, cudaStream_t st, bool inverse) {
+  const size_t s2_bytes = (size_t)E * scale_chunk_bytes(H, I);
+  float* s2g = reinterpret_cast<float*>(static_cast<uint8_t*>(s2) + s2_bytes);
+  cudaError_t err = cudaSuccess;
+  if (fmt == MOE_FP4_MXFP4 && !inverse) {
+    mx_multiplier_kernel<<<E, 256, 0, st>>>(static_cast<const uint8_t*>(s2_l), H, I / 32, 1, s2g);
+    err = cudaGetLastError();
+  }
+  if (fmt == MOE_FP4_NVFP4)
+    err = inverse ? cudaMemcpyAsync(const_cast<float*>(g2), s2g, sizeof(float) * E, cudaMemcpyDeviceToDevice, st)
+                  : cudaMemcpyAsync(s2g, g2, sizeof(float) * E, cudaMemcpyDeviceToDevice, st);
+  if (err != cudaSuccess) return err;
+  repack_scales_kernel<<<grid_for(s2_bytes, 256), 256, 0, st>>>(
+      static_cast<const uint8_t*>(inverse ? s2 : s2_l), static_cast<uint8_t*>(inverse ? const_cast<void*>(s2_l) : s2),
+      E, H, H, I, fmt, 0, s2g, inverse);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const size_t w2_bytes = (size_t)E * H * (I / 2);
+  return inverse ? cudaMemcpyAsync(const_cast<void*>(w2_l), w2, w2_bytes, cudaMemcpyDeviceToDevice, st)
+                 : cudaMemcpyAsync(w2, w2_l, w2_bytes, cudaMemcpyDeviceToDevice, st);
+}
+
 cudaError_t launch_prepare(const void* w13_l, const void* s13_l, const float* g13, const void* w2_l,
                            const void* s2_l, const float* g2, int E, int H, int I, int fmt, void* w13, void* s13,
                            void* w2, void* s2, cudaStream_t st, bool inverse) {
@@ -172,47 +203,58 @@ cudaError_t launch_prepare(const void* w13_l, const void* s13_l, const float* g1
       static_cast<const uint4*>(inverse ? w13 : w13_l), static_cast<uint4*>(inverse ? const_cast<void*>(w13_l) : w13),
       E, I, H, inverse);
   const size_t s13_bytes = (size_t)E * scale_chunk_bytes(2 * I, H);
-  const size_t s2_bytes = (size_t)E * scale_chunk_bytes(H, I);
   float* s13g = reinterpret_cast<float*>(static_cast<uint8_t*>(s13) + s13_bytes);
-  float* s2g = reinterpret_cast<float*>(static_cast<uint8_t*>(s2) + s2_bytes);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   // the multipliers first: the MXFP4 scale conversion reads them
   if (fmt == MOE_FP4_MXFP4 && !inverse) {
     mx_multiplier_kernel<<<E * 2, 256, 0, st>>>(static_cast<const uint8_t*>(s13_l), I, H / 32, 2, s13g);
-    mx_multiplier_kernel<<<E, 256, 0, st>>>(static_cast<const uint8_t*>(s2_l), H, I / 32, 1, s2g);
     err = cudaGetLastError();
   }
-  if (fmt == MOE_FP4_NVFP4) {
-    if (!inverse) {
-      err = cudaMemcpyAsync(s13g, g13, sizeof(float) * 2 * E, cudaMemcpyDeviceToDevice, st);
-      if (err == cudaSuccess) err = cudaMemcpyAsync(s2g, g2, sizeof(float) * E, cudaMemcpyDeviceToDevice, st);
-    } else {
-      err = cudaMemcpyAsync(const_cast<float*>(g13), s13g, sizeof(float) * 2 * E, cudaMemcpyDeviceToDevice, st);
-      if (err == cudaSuccess)
-        err = cudaMemcpyAsync(const_cast<float*>(g2), s2g, sizeof(float) * E, cudaMemcpyDeviceToDevice, st);
-    }
-  }
+  if (fmt == MOE_FP4_NVFP4)
+    err = inverse ? cudaMemcpyAsync(const_cast<float*>(g13), s13g, sizeof(float) * 2 * E, cudaMemcpyDeviceToDevice, st)
+                  : cudaMemcpyAsync(s13g, g13, sizeof(float) * 2 * E, cudaMemcpyDeviceToDevice, st);
   if (err != cudaSuccess) return err;
   repack_scales_kernel<<<grid_for(s13_bytes, 256), 256, 0, st>>>(
       static_cast<const uint8_t*>(inverse ? s13 : s13_l),
-      static_cast<uint8_t*>(inverse ? const_cast<void*>(s13_l) : s13), E, 2 * I, H, fmt, I, s13g, inverse);
-  repack_scales_kernel<<<grid_for(s2_bytes, 256), 256, 0, st>>>(
-      static_cast<const uint8_t*>(inverse ? s2 : s2_l), static_cast<uint8_t*>(inverse ? const_cast<void*>(s2_l) : s2),
-      E, H, I, fmt, 0, s2g, inverse);
+      static_cast<uint8_t*>(inverse ? const_cast<void*>(s13_l) : s13), E, 2 * I, 2 * I, H, fmt, I, s13g, inverse);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const size_t w2_bytes = (size_t)E * H * (I / 2);
-  if (!inverse)
-    err = cudaMemcpyAsync(w2, w2_l, w2_bytes, cudaMemcpyDeviceToDevice, st);
-  else
-    err = cudaMemcpyAsync(const_cast<void*>(w2_l), w2, w2_bytes, cudaMemcpyDeviceToDevice, st);
-  return err;
+  return prepare_w2(w2_l, s2_l, g2, E, H, I, fmt, w2, s2, st, inverse);
+}
+
+// Non-gated experts (squared ReLU): w1 [E][I][H/2] kept in logical row order,
+// its scales in chunks with each expert's rows padded to a multiple of 128,
+// then the multipliers [E]; w2 as for the gated layout.
+cudaError_t launch_prepare_relu2(const void* w1_l, const void* s1_l, const float* g1, const void* w2_l,
+                                 const void* s2_l, const float* g2, int E, int H, int I, int fmt, void* w1, void* s1,
+                                 void* w2, void* s2, cudaStream_t st, bool inverse) {
+  const int rows = (I + kRowTile - 1) / kRowTile * kRowTile;
+  const size_t s1_bytes = (size_t)E * scale_chunk_bytes(rows, H);
+  float* s1g = reinterpret_cast<float*>(static_cast<uint8_t*>(s1) + s1_bytes);
+  const size_t w1_bytes = (size_t)E * I * (H / 2);
+  cudaError_t err = inverse ? cudaMemcpyAsync(const_cast<void*>(w1_l), w1, w1_bytes, cudaMemcpyDeviceToDevice, st)
+                            : cudaMemcpyAsync(w1, w1_l, w1_bytes, cudaMemcpyDeviceToDevice, st);
+  if (err != cudaSuccess) return err;
+  if (fmt == MOE_FP4_MXFP4 && !inverse) {
+    mx_multiplier_kernel<<<E, 256, 0, st>>>(static_cast<const uint8_t*>(s1_l), I, H / 32, 1, s1g);
+    err = cudaGetLastError();
+  }
+  if (fmt == MOE_FP4_NVFP4)
+    err = inverse ? cudaMemcpyAsync(const_cast<float*>(g1), s1g, sizeof(float) * E, cudaMemcpyDeviceToDevice, st)
+                  : cudaMemcpyAsync(s1g, g1, sizeof(float) * E, cudaMemcpyDeviceToDevice, st);
+  if (err != cudaSuccess) return err;
+  repack_scales_kernel<<<grid_for(s1_bytes, 256), 256, 0, st>>>(
+      static_cast<const uint8_t*>(inverse ? s1 : s1_l), static_cast<uint8_t*>(inverse ? const_cast<void*>(s1_l) : s1),
+      E, rows, I, H, fmt, 0, s1g, inverse);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  return prepare_w2(w2_l, s2_l, g2, E, H, I, fmt, w2, s2, st, inverse);
 }
 
 cudaError_t launch_debug_dequant(const void* w, const void* s, int which, int e, int E, int H, int I, int fmt,
                                  float* out, cudaStream_t st) {
-  const size_t n = (size_t)(which == 0 ? 2 * I : H) * (which == 0 ? H : I);
+  const size_t n = (size_t)(which == 0 ? 2 * I : (which == 1 ? H : I)) * (which == 1 ? I : H);
   (void)fmt;
   debug_dequant_kernel<<<grid_for(n, 256), 256, 0, st>>>(static_cast<const uint8_t*>(w),
                                                           static_cast<const uint8_t*>(s), which, e, E, H, I, out);

@@ -277,6 +277,7 @@ MOE_FP4_API int moe_fp4_debug_wait_timeout(void *status_word, unsigned polls, vo
 #define MOE_FP4_ACT_SILU 0
 #define MOE_FP4_ACT_GELU_TANH 1
 #define MOE_FP4_ACT_SWIGLUOAI 2
+#define MOE_FP4_ACT_RELU2 3 /* non-gated experts: see moe_fp4_prepare_weights_relu2 */
 typedef struct moe_fp4_activation {
   int kind;
   float alpha, beta, limit;
@@ -286,12 +287,44 @@ typedef struct moe_fp4_activation {
  * moe_fp4_forward_ws with a chosen activation (act == NULL: SiLU).  Same
  * arguments, workspace, results and errors otherwise; MOE_FP4_EINVAL for an
  * unknown kind, or for SwiGLU-OAI with a non-finite alpha or beta or a
- * limit that is not a positive number.
+ * limit that is not a positive number.  With MOE_FP4_ACT_RELU2 the experts
+ * are non-gated and w13, s13 are the w1, s1 of moe_fp4_prepare_weights_relu2.
  */
 MOE_FP4_API int moe_fp4_forward_ex(const void *x_bf16, const void *w13, const void *s13, const void *w2,
                                    const void *s2, const int32_t *topk_ids, const float *topk_weights, void *out_bf16,
                                    int M, int E, int H, int I, int top_k, int fmt, const moe_fp4_activation *act,
                                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Non-gated experts with the squared ReLU: "relu2" of flashinfer PR #4285
+ * ("sync SM12x NVFP4 fused-MoE kernels"), which names it among the
+ * activations and keeps the exact activation quantiser for it (its outputs
+ * are squares, not a gated product).  FC1 has I rows:
+ *     h_n = max(x_t . W1[e][n], 0)^2
+ * then FC2 and the router-weighted sum as for the gated layer.  Logical
+ * inputs (device): w1 [E][I][H/2] u8 (low nibble = even K), s1 [E][I][H/B]
+ * u8, g1 [E] f32 (NVFP4 only, else NULL), and w2, s2, g2 as for
+ * moe_fp4_prepare_weights.  Resident layout: w1 rows in logical order; s1
+ * scale chunks as for w13 (moe_fp4_prepared_sizes) with each expert's rows
+ * padded to a multiple of 128 (padding rows' scales are zero), then the FP32
+ * multipliers [E] (NVFP4: g1; MXFP4: the power of two of the re-expressed
+ * block scales, as for w13); w2, s2 as for the gated layer.  Run the layer
+ * with moe_fp4_forward_ex or moe_fp4_forward_ex_i64 and act kind
+ * MOE_FP4_ACT_RELU2, w1 and s1 in place of w13 and s13 (the same shape
+ * limits and workspace sizes; the decode band runs the tcgen05 launch chain,
+ * the prefill band quantises h = max(u, 0)^2 after BF16 staging with the
+ * same exact row quantiser).
+ */
+MOE_FP4_API int moe_fp4_prepared_sizes_relu2(int E, int H, int I, int fmt, size_t *w1_bytes, size_t *s1_bytes,
+                                             size_t *w2_bytes, size_t *s2_bytes);
+MOE_FP4_API int moe_fp4_prepare_weights_relu2(const void *w1_logical, const void *s1_logical, const float *g1,
+                                              const void *w2_logical, const void *s2_logical, const float *g2, int E,
+                                              int H, int I, int fmt, void *w1, void *s1, void *w2, void *s2,
+                                              void *stream);
+/* Inverse of moe_fp4_prepare_weights_relu2 (test support). */
+MOE_FP4_API int moe_fp4_unprepare_weights_relu2(const void *w1, const void *s1, const void *w2, const void *s2, int E,
+                                                int H, int I, int fmt, void *w1_logical, void *s1_logical, float *g1,
+                                                void *w2_logical, void *s2_logical, float *g2, void *stream);
 
 /*
  * moe_fp4_forward_ex with int64 routing ids (topk_ids int64 [M][top_k],
@@ -403,7 +436,8 @@ MOE_FP4_API int moe_fp4_debug_decode_launches(int M, int E, int H, int I, int to
  * into out_f32 [rows][K] in LOGICAL row order, each element computed as the
  * kernels use it: RN_fp32((e2m1 * e4m3) * g) (one rounding; exact for MXFP4,
  * whose e4m3 and g are powers of two).  which = 0: w13 (rows 2I, K = H, gate
- * rows first), which = 1: w2 (rows H, K = I).
+ * rows first), which = 1: w2 (rows H, K = I), which = 2: the w1 of
+ * moe_fp4_prepare_weights_relu2 (rows I, K = H).
  */
 MOE_FP4_API int moe_fp4_debug_dequant(const void *w, const void *s, int which, int expert, int E, int H, int I, int fmt,
                           float *out_f32, void *stream);

@@ -107,6 +107,8 @@ def _bind(lib):
     lib.moe_oracle_forward_w4a8_act.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, P, i, P, i, i, d, d, d]
     lib.moe_oracle_forward_relu2.restype = i
     lib.moe_oracle_forward_relu2.argtypes = [P, P, P, P, P, P, P, P, P, i, i, i, i, i, i, P, i, P, i]
+    lib.moe_oracle_forward_prefill_relu2.restype = i
+    lib.moe_oracle_forward_prefill_relu2.argtypes = [P, P, P, P, P, P, P, P, P, i, i, i, i, i, i, P, i, P, i]
     lib.moe_oracle_route.restype = i
     lib.moe_oracle_route.argtypes = [P, i, i, i, P, P]
     lib.moe_oracle_num_threads.restype = i
@@ -302,6 +304,30 @@ def forward_relu2(x_bf16, weights: dict, topk_ids, topk_weights, E: int, H: int,
     rc = _load().moe_oracle_forward_relu2(_ptr(x), _ptr(w1), _ptr(s1), _ptr(g1), _ptr(w2), _ptr(s2), _ptr(g2),
                                           _ptr(ids), _ptr(tw), M, E, H, I, top_k, fmt, _ptr(tok), n_tok, _ptr(out),
                                           nthreads)
+    if rc != 0:
+        raise ValueError("oracle rejected the shapes")
+    return out
+
+
+def forward_prefill_relu2(x_bf16, weights: dict, topk_ids, topk_weights, E: int, H: int, I: int, top_k: int,
+                          fmt: int, tokens: Optional[Sequence[int]] = None, nthreads: int = 0) -> np.ndarray:
+    """Prefill-band definition for non-gated experts (NVFP4 activations,
+    mirrored; h = max(u, 0)^2 staged in BF16): ``weights`` as for
+    ``forward_relu2``.  Returns ``[n_tok][H]`` FP64."""
+    x = _np(x_bf16, np.uint16)
+    M = x.shape[0]
+    w1, s1 = _np(weights["w1"], np.uint8), _np(weights["s1"], np.uint8)
+    g1 = _np(weights.get("g1"), np.float32) if fmt == NVFP4 else None
+    w2, s2 = _np(weights["w2"], np.uint8), _np(weights["s2"], np.uint8)
+    g2 = _np(weights.get("g2"), np.float32) if fmt == NVFP4 else None
+    ids = _np(topk_ids, np.int32)
+    tw = _np(topk_weights, np.float32)
+    tok = None if tokens is None else np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    n_tok = M if tok is None else len(tok)
+    out = np.full((n_tok, H), np.nan, dtype=np.float64)  # poisoned: the oracle must overwrite
+    rc = _load().moe_oracle_forward_prefill_relu2(_ptr(x), _ptr(w1), _ptr(s1), _ptr(g1), _ptr(w2), _ptr(s2),
+                                                  _ptr(g2), _ptr(ids), _ptr(tw), M, E, H, I, top_k, fmt, _ptr(tok),
+                                                  n_tok, _ptr(out), nthreads)
     if rc != 0:
         raise ValueError("oracle rejected the shapes")
     return out

@@ -659,6 +659,73 @@ int moe_oracle_forward_w4a8_act(const uint16_t *x_bf16, const uint8_t *w13, cons
     return 0;
 }
 
+/* The prefill band's mirror for non-gated experts (squared ReLU): x
+ * quantised per token to NVFP4 and dequantised, u = x . W1[e][n] in FP64,
+ * h = max(u, 0)^2 rounded to FP32 then BF16 (the same staging as the gated
+ * mirror), h quantised per routed row with the same row quantiser and
+ * dequantised, then FC2 and the router-weighted sum in FP64.  w1, s1, g1 as
+ * for moe_oracle_forward_relu2. */
+int moe_oracle_forward_prefill_relu2(const uint16_t *x_bf16, const uint8_t *w1, const uint8_t *s1, const float *g1,
+                                     const uint8_t *w2, const uint8_t *s2, const float *g2,
+                                     const int32_t *topk_ids, const float *topk_w, int M, int E, int H, int I,
+                                     int top_k, int fmt, const int32_t *tokens, int n_tok, double *out,
+                                     int nthreads)
+{
+    if (fmt != ORACLE_NVFP4 && fmt != ORACLE_MXFP4) return 1;
+    int B = block_of(fmt);
+    if (H % B || I % B || H % 16 || I % 16) return 1;
+    if (!tokens) n_tok = M;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel
+#endif
+    {
+        float *xf = (float *)malloc(sizeof(float) * (size_t)H);
+        uint8_t *xq = (uint8_t *)malloc((size_t)H / 2);
+        uint8_t *xs = (uint8_t *)malloc((size_t)H / 16);
+        double *xd = (double *)malloc(sizeof(double) * (size_t)H);
+        float *hf = (float *)malloc(sizeof(float) * (size_t)I);
+        uint8_t *hq = (uint8_t *)malloc((size_t)I / 2);
+        uint8_t *hs = (uint8_t *)malloc((size_t)I / 16);
+        double *hd = (double *)malloc(sizeof(double) * (size_t)I);
+        double *y = (double *)malloc(sizeof(double) * (size_t)H);
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int i = 0; i < n_tok; ++i) {
+            int t = tokens ? tokens[i] : i;
+            for (int k = 0; k < H; ++k) xf[k] = (float)bf16_to_double(x_bf16[(size_t)t * H + k]);
+            float xG;
+            moe_oracle_quant_nvfp4_row(xf, H, xq, xs, &xG);
+            dequant_nvfp4_row(xq, xs, xG, H, xd);
+            double *o = out + (size_t)i * H;
+            for (int m = 0; m < H; ++m) o[m] = 0.0;
+            for (int j = 0; j < top_k; ++j) {
+                int e = topk_ids[(size_t)t * top_k + j];
+                if (e < 0 || e >= E) continue;
+                const uint8_t *nib = w1 + (size_t)e * I * (H / 2);
+                const uint8_t *sc = s1 + (size_t)e * I * (H / B);
+                double g = fmt == ORACLE_NVFP4 ? (double)g1[e] : 1.0;
+                for (int n = 0; n < I; ++n) {
+                    double u = 0.0;
+                    for (int k = 0; k < H; ++k) u += xd[k] * weight_at(nib, sc, H, fmt, g, n, k);
+                    double r = u > 0.0 ? u : 0.0;
+                    hf[n] = bf16_round((float)(r * r));
+                }
+                float hG;
+                moe_oracle_quant_nvfp4_row(hf, I, hq, hs, &hG);
+                dequant_nvfp4_row(hq, hs, hG, I, hd);
+                expert_fc2(hd, w2, s2, g2, e, H, I, fmt, y);
+                double w = (double)topk_w[(size_t)t * top_k + j];
+                for (int m = 0; m < H; ++m) o[m] += w * y[m];
+            }
+        }
+        free(xf); free(xq); free(xs); free(xd); free(hf); free(hq); free(hs); free(hd); free(y);
+    }
+    (void)nthreads;
+    return 0;
+}
+
 /* ------------------------------------------------- routing / compaction */
 
 /* Stable grouping of routed rows by expert: rows (t, j) with a valid id are

@@ -86,8 +86,18 @@ def test_prepare_argument_errors(lib):
     st = _capi.raw_status("moe_fp4_prepare_weights", 0x1000, 0x1000, None, 0x1000, 0x1000, None, 4, 200, 128, 0,
                           0x1000, 0x1000, 0x1000, 0x1000, None)
     assert st == _capi.MOE_FP4_EUNSUPPORTED
-    st = _capi.raw_status("moe_fp4_debug_dequant", 0x1000, 0x1000, 2, 0, 4, 256, 128, 0, 0x1000, None)
-    assert st == _capi.MOE_FP4_EINVAL
+    st = _capi.raw_status("moe_fp4_debug_dequant", 0x1000, 0x1000, 3, 0, 4, 256, 128, 0, 0x1000, None)
+    assert st == _capi.MOE_FP4_EINVAL  # which: 0 w13, 1 w2, 2 w1 (non-gated)
+    # non-gated (squared-ReLU) weights: the same checks
+    st = _capi.raw_status("moe_fp4_prepare_weights_relu2", 0x1000, 0x1000, None, 0x1000, 0x1000, None, 4, 256, 128,
+                          1, 0x1000, 0x1000, 0x1000, 0x1000, None)
+    assert st == _capi.MOE_FP4_EINVAL  # NVFP4 needs the FP32 multipliers
+    st = _capi.raw_status("moe_fp4_prepare_weights_relu2", 0x1000, 0x1000, None, 0x1000, 0x1000, None, 4, 200, 128,
+                          0, 0x1000, 0x1000, 0x1000, 0x1000, None)
+    assert st == _capi.MOE_FP4_EUNSUPPORTED
+    st = _capi.raw_status("moe_fp4_prepare_weights_relu2", 0x1000, 0x1000, None, 0x1000, 0x1000, None, 4, 256, 128,
+                          0, 0x1008, 0x1000, 0x1000, 0x1000, None)
+    assert st == _capi.MOE_FP4_EINVAL  # resident buffers 16-byte aligned
     st = _capi.raw_status("moe_fp4_debug_dequant", 0x1000, 0x1000, 0, 4, 4, 256, 128, 0, 0x1000, None)
     assert st == _capi.MOE_FP4_EINVAL  # expert out of range
 
@@ -237,3 +247,17 @@ int main(void) {
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
     assert subprocess.run([str(exe)]).returncode == 0
+
+
+def test_relu2_prepared_sizes(lib):
+    """Non-gated layout sizes: w1 [E][I][H/2]; its scale chunks cover each
+    expert's rows padded to a multiple of 128, then the FP32 multipliers [E];
+    w2 and s2 as for the gated layout."""
+    E, H, I = 5, 512, 320
+    w1, s1, w2, s2 = _capi.moe_fp4_prepared_sizes_relu2(E, H, I, 1)
+    assert w1 == E * I * H // 2
+    chunks = E * ((I + 127) // 128) * (H // 64) * 512
+    assert s1 == (chunks + 4 * E + 15) // 16 * 16
+    g13 = _capi.moe_fp4_prepared_sizes(E, H, I, 1)
+    assert (w2, s2) == (g13[2], g13[3])
+

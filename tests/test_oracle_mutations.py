@@ -64,18 +64,23 @@ MUTATIONS = {
     "mxfp8_h_unquantised": ("moe_oracle_quant_mxfp8_row(hf, I, hq, hs);\n                dequant_mxfp8_row(hq, hs, I, hd);",
                             "moe_oracle_quant_mxfp8_row(hf, I, hq, hs);\n                for (int n = 0; n < I; ++n) hd[n] = h[n];"),
     "relu2_square_dropped": ("h[n] = r * r;", "h[n] = r;"),
-    "relu2_relu_dropped": ("double r = u > 0.0 ? u : 0.0;", "double r = u;"),
+    "relu2_relu_dropped": ("double r = u > 0.0 ? u : 0.0;\n                    h[n] = r * r;", "double r = u;\n                    h[n] = r * r;"),
+    "prefill_relu2_relu_dropped": ("double r = u > 0.0 ? u : 0.0;\n                    hf[n]", "double r = u;\n                    hf[n]"),
     "relu2_rows_shifted": ("for (int k = 0; k < H; ++k) u += x[k] * weight_at(nib, sc, H, fmt, g, n, k);",
                            "for (int k = 0; k < H; ++k) u += x[k] * weight_at(nib, sc, H, fmt, g, (n + 1) % I, k);"),
     "prefill_bf16_staging_dropped": ("hf[n] = bf16_round((float)h[n]);\n                float hG;",
                                      "hf[n] = (float)h[n];\n                float hG;"),
-    "prefill_h_takes_x_multiplier": ("moe_oracle_quant_nvfp4_row(hf, I, hq, hs, &hG);\n                dequant_nvfp4_row(hq, hs, hG, I, hd);",
-                                     "moe_oracle_quant_nvfp4_row(hf, I, hq, hs, &hG);\n                dequant_nvfp4_row(hq, hs, xG, I, hd);"),
-    "prefill_h_dequant_skipped": ("dequant_nvfp4_row(hq, hs, hG, I, hd);\n                expert_fc2(hd,",
-                                  "dequant_nvfp4_row(hq, hs, hG, I, hd);\n                expert_fc2(h,"),
-    "prefill_x_multiplier_dropped": ("dequant_nvfp4_row(xq, xs, xG, H, xd);", "dequant_nvfp4_row(xq, xs, 1.0f, H, xd);"),
-    "prefill_h_multiplier_per_token": ("float hG;\n                moe_oracle_quant_nvfp4_row(hf, I, hq, hs, &hG);",
-                                       "float hG;\n                static float shared_hG;\n                moe_oracle_quant_nvfp4_row(hf, I, hq, hs, &hG);\n                if (j > 0) hG = shared_hG; else shared_hG = hG;"),
+    "prefill_h_takes_x_multiplier": ("hf[n] = bf16_round((float)h[n]);\n                float hG;\n                moe_oracle_quant_nvfp4_row(hf, I, hq, hs, &hG);\n                dequant_nvfp4_row(hq, hs, hG, I, hd);",
+                                     "hf[n] = bf16_round((float)h[n]);\n                float hG;\n                moe_oracle_quant_nvfp4_row(hf, I, hq, hs, &hG);\n                dequant_nvfp4_row(hq, hs, xG, I, hd);"),
+    "prefill_h_dequant_skipped": ("hf[n] = bf16_round((float)h[n]);\n                float hG;\n                moe_oracle_quant_nvfp4_row(hf, I, hq, hs, &hG);\n                dequant_nvfp4_row(hq, hs, hG, I, hd);\n                expert_fc2(hd,",
+                                  "hf[n] = bf16_round((float)h[n]);\n                float hG;\n                moe_oracle_quant_nvfp4_row(hf, I, hq, hs, &hG);\n                dequant_nvfp4_row(hq, hs, hG, I, hd);\n                expert_fc2(h,"),
+    "prefill_x_multiplier_dropped": ("if (xg_out) xg_out[i] = xG;\n            dequant_nvfp4_row(xq, xs, xG, H, xd);",
+                                     "if (xg_out) xg_out[i] = xG;\n            dequant_nvfp4_row(xq, xs, 1.0f, H, xd);"),
+    "prefill_h_multiplier_per_token": ("hf[n] = bf16_round((float)h[n]);\n                float hG;\n                moe_oracle_quant_nvfp4_row(hf, I, hq, hs, &hG);",
+                                       "hf[n] = bf16_round((float)h[n]);\n                float hG;\n                static float shared_hG;\n                moe_oracle_quant_nvfp4_row(hf, I, hq, hs, &hG);\n                if (j > 0) hG = shared_hG; else shared_hG = hG;"),
+    "prefill_relu2_square_dropped": ("hf[n] = bf16_round((float)(r * r));", "hf[n] = bf16_round((float)r);"),
+    "prefill_relu2_h_unquantised": ("dequant_nvfp4_row(hq, hs, hG, I, hd);\n                expert_fc2(hd, w2, s2, g2, e, H, I, fmt, y);\n                double w = (double)topk_w[(size_t)t * top_k + j];\n                for (int m = 0; m < H; ++m) o[m] += w * y[m];\n            }\n        }\n        free(xf); free(xq); free(xs); free(xd); free(hf);",
+                                    "dequant_nvfp4_row(hq, hs, hG, I, hd);\n                for (int n = 0; n < I; ++n) hd[n] = hf[n];\n                expert_fc2(hd, w2, s2, g2, e, H, I, fmt, y);\n                double w = (double)topk_w[(size_t)t * top_k + j];\n                for (int m = 0; m < H; ++m) o[m] += w * y[m];\n            }\n        }\n        free(xf); free(xq); free(xs); free(xd); free(hf);"),
     "route_order": ("for (int t = 0; t < M; ++t)\n            for (int j = 0; j < top_k; ++j)\n                if (topk_ids[(size_t)t * top_k + j] == e) perm[r++] = t * top_k + j;",
                     "for (int j = 0; j < top_k; ++j)\n            for (int t = 0; t < M; ++t)\n                if (topk_ids[(size_t)t * top_k + j] == e) perm[r++] = t * top_k + j;"),
 }
@@ -113,6 +118,8 @@ def _run_pins():
         ("prefill_brute_nv", lambda: pins.test_prefill_mirror_brute_force(1)),
         ("prefill_brute_mx", lambda: pins.test_prefill_mirror_brute_force(0)),
         ("prefill_per_row_h", pins.test_prefill_mirror_quantises_h_per_routed_row),
+        ("prefill_relu2_nv", lambda: pins.test_prefill_relu2_mirror_brute_force(1)),
+        ("prefill_relu2_mx", lambda: pins.test_prefill_relu2_mirror_brute_force(0)),
     ]
     for case in pins._golden_cases():
         checks.append(("golden_" + case["name"], lambda c=case: pins.test_hand_worked_layers(c)))

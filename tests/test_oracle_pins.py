@@ -763,3 +763,31 @@ def test_prefill_mirror_quantises_h_per_routed_row():
                                E, H, I, 2)[0]
     assert np.abs(b).max() > 0
     np.testing.assert_allclose(both, a + b, rtol=1e-12, atol=1e-14 * np.abs(both).max())
+
+
+@pytest.mark.parametrize("fmt", [gen.NVFP4, gen.MXFP4])
+def test_prefill_relu2_mirror_brute_force(fmt):
+    """The prefill band's mirror for non-gated experts rebuilt from the same
+    independent pieces: x and h through the NumPy float32 NVFP4 round trip,
+    h = max(u, 0)^2 staged FP64 -> FP32 -> BF16 by torch, NumPy float64
+    matrix products on independently dequantised weights."""
+    E, H, I, M, k = 3, 64, 64, 3, 2
+    w = _relu2_weights(E, H, I, fmt, seed=81)
+    x = gen.draw_activations(M, H, seed=82)
+    ids = np.array([[0, 2], [1, -1], [2, 1]], np.int32)
+    tw = np.array([[0.6, 0.4], [0.8, 0.2], [0.3, 0.7]], np.float32)
+    got = oracle.forward_prefill_relu2(x, w, ids, tw, E, H, I, k, fmt)
+    xf = x.to(torch.float32).numpy()
+    want = np.zeros((M, H))
+    for t in range(M):
+        xq = _np_nvfp4_row(xf[t])
+        for j in range(k):
+            e = int(ids[t, j])
+            if not 0 <= e < E:
+                continue
+            W1 = _np_dequant(w["w1"][e], w["s1"][e], H, fmt, float(w["g1"][e]))
+            Wd = _np_dequant(w["w2"][e], w["s2"][e], I, fmt, float(w["g2"][e]))
+            r = np.maximum(W1 @ xq, 0.0)
+            hb = torch.tensor(r * r).to(torch.float32).to(torch.bfloat16).to(torch.float32).numpy()
+            want[t] += float(tw[t, j]) * (Wd @ _np_nvfp4_row(hb))
+    np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-12 * np.abs(want).max())

@@ -178,6 +178,43 @@ def make_expert_weights(E: int, H: int, I: int, fmt: int, seed: int, device="cpu
     return out
 
 
+def make_relu2_weights(E: int, H: int, I: int, fmt: int, seed: int, device="cpu", std: float = 0.02,
+                       experts=None):
+    """Non-gated (squared-ReLU) experts: w1 [E][I][H/2], s1 [E][I][H/B] from
+    N(0, std) floats of their own counter-seeded stream per expert, and w2, s2
+    drawn like the gated experts' down projection; NVFP4 adds g1 [E], g2 [E]."""
+    B = BLOCK[fmt]
+    expert_ids = list(range(E)) if experts is None else list(experts)
+    E = len(expert_ids)
+    w1 = torch.empty((E, I, H // 2), dtype=torch.uint8, device=device)
+    s1 = torch.empty((E, I, H // B), dtype=torch.uint8, device=device)
+    w2 = torch.empty((E, H, I // 2), dtype=torch.uint8, device=device)
+    s2 = torch.empty((E, H, I // B), dtype=torch.uint8, device=device)
+    g1 = torch.ones((E,), dtype=torch.float32, device=device) if fmt == NVFP4 else None
+    g2 = torch.ones((E,), dtype=torch.float32, device=device) if fmt == NVFP4 else None
+    for e, eid in enumerate(expert_ids):
+        for proj, rows, K in ((3, I, H), (2, H, I)):
+            gen = _expert_generator(seed, eid, proj, device)
+            wf = torch.randn((rows, K), generator=gen, device=device, dtype=torch.float32) * std
+            if fmt == MXFP4:
+                nib, sc = encode_mxfp4(wf)
+                g = None
+            else:
+                nib, sc, g = encode_nvfp4(wf)
+            if proj == 3:
+                w1[e], s1[e] = nib, sc
+                if g1 is not None:
+                    g1[e] = g
+            else:
+                w2[e], s2[e] = nib, sc
+                if g2 is not None:
+                    g2[e] = g
+    out = dict(w1=w1, s1=s1, w2=w2, s2=s2)
+    if fmt == NVFP4:
+        out.update(g1=g1, g2=g2)
+    return out
+
+
 # --------------------------------------------------------------------------
 # activations and routing
 # --------------------------------------------------------------------------
@@ -313,6 +350,6 @@ def ceil_div(a: int, b: int) -> int:
 
 __all__ = [
     "MXFP4", "NVFP4", "FMT_NAMES", "BLOCK", "CONFIGS", "CONFIG_SEED", "Workload", "make_workload",
-    "make_expert_weights", "encode_mxfp4", "encode_nvfp4", "draw_activations", "draw_routing",
+    "make_expert_weights", "make_relu2_weights", "encode_mxfp4", "encode_nvfp4", "draw_activations", "draw_routing",
     "draw_routing_pool", "routed_unique_experts", "expert_bytes", "ceil_div", "math",
 ]
