@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--M", type=int, default=None, help="override the token count")
     ap.add_argument("--E", type=int, default=None, help="override the expert count (profiling on smaller memory)")
     ap.add_argument("--fmt", choices=["mxfp4", "nvfp4"], default=None)
+    ap.add_argument("--prefill-mode", choices=["nvfp4", "bf16"], default="nvfp4",
+                    help="prefill-band activation precision of the headline (bf16: the exact band)")
     ap.add_argument("--decode-plan", choices=list(DECODE_PLANS), default="auto",
                     help="decode-band kernel plan (auto: by shape)")
     return ap.parse_args()
@@ -284,7 +286,7 @@ SWEEP = [("C0", "tiny_decode", {}),
          ("C2", "decode_e288_m4", {})] + \
     [(f"C3/M={M}/{f}", "decode_e256", dict(M=M, fmt=fmt)) for fmt, f in ((0, "mxfp4"), (1, "nvfp4"))
      for M in (1, 2, 4, 8)] + \
-    [("C4", "prefill_e128", {})]
+    [("C4", "prefill_e128", {}), ("C4/bf16-exact", "prefill_e128", dict(prefill_mode=1))]
 
 
 def affinity_cores():
@@ -318,10 +320,11 @@ def parity_metrics(got, want):
             "zero_rows_exact": zero_ok, "ok": ok}
 
 
-def oracle_check(m, gen, weights, c, x, ids, tw, got, prefill, threads):
+def oracle_check(m, gen, weights, c, x, ids, tw, got, prefill, threads, exact=False):
     """The layer of one routing draw on the FP64 oracle (routed experts only;
     the prefill band on a spread of 16 tokens, its activation quantisation
-    mirrored) against the GPU output of the same draw."""
+    mirrored unless the band ran with exact BF16 numerics, which has the
+    plain definition) against the GPU output of the same draw."""
     import numpy as np
     import oracle
     import torch
@@ -338,9 +341,13 @@ def oracle_check(m, gen, weights, c, x, ids, tw, got, prefill, threads):
     idx = torch.tensor(used if used else [0], dtype=torch.long, device=weights["w13"].device)
     sub = {kk: v.index_select(0, idx).cpu() for kk, v in weights.items() if v is not None}
     t0 = time.perf_counter()
-    if prefill:
+    if prefill and not exact:
         want = oracle.forward_prefill(x.cpu(), sub, ids_c, tw.cpu(), max(1, len(used)), H, I, k, tokens=tokens,
                                       nthreads=threads, fmt=fmt)[0]
+        got_rows = got.float().cpu().double().numpy()[tokens]
+    elif prefill:
+        want = oracle.forward(x.cpu()[tokens], sub, ids_c[tokens], tw.cpu()[tokens], max(1, len(used)), H, I, k, fmt,
+                              nthreads=threads)
         got_rows = got.float().cpu().double().numpy()[tokens]
     else:
         want = oracle.forward(x.cpu(), sub, ids_c, tw.cpu(), max(1, len(used)), H, I, k, fmt, nthreads=threads)
@@ -348,7 +355,8 @@ def oracle_check(m, gen, weights, c, x, ids, tw, got, prefill, threads):
     secs = time.perf_counter() - t0
     r = parity_metrics(got_rows, want)
     r["oracle_s"] = secs
-    r["checked"] = f"{len(tokens)} sampled tokens (mirrored activation quantisation)" if prefill else \
+    r["checked"] = (f"{len(tokens)} sampled tokens (plain definition)" if exact else
+                    f"{len(tokens)} sampled tokens (mirrored activation quantisation)") if prefill else \
         f"all {M} tokens"
     return r
 
@@ -364,6 +372,7 @@ def measure(m, name, ov, K, W, dev, rank, ws_world, min_timed_s, threads, do_e2e
     c = dict(gen.CONFIGS[name])
     c.update({kk: v for kk, v in ov.items() if v is not None})
     E, H, I, k, M, fmt = c["E"], c["H"], c["I"], c["top_k"], c["M"], c["fmt"]
+    mode = int(c.get("prefill_mode", 0))  # 1: the exact BF16 prefill band
     seed = gen.CONFIG_SEED[name]
     window = max(1, min(WINDOW, E // (k * M)))
     weights = gen.make_expert_weights(E, H, I, fmt, seed, device=dev)
@@ -372,15 +381,25 @@ def measure(m, name, ov, K, W, dev, rank, ws_world, min_timed_s, threads, do_e2e
     ids_pool, w_pool = gen.draw_routing_pool(max(K, window), M, E, k, seed + 29 + 1000 * rank, window)
     ids_d = [t.to(dev) for t in ids_pool]
     w_d = [t.to(dev) for t in w_pool]
-    ws = m.alloc_workspace(M, E, H, I, k, fmt, device=dev)
+    ws = m.alloc_workspace_mode(M, E, H, I, k, fmt, mode, device=dev)
     out = torch.full((M, H), float("nan"), dtype=torch.bfloat16, device=dev)
-    decode = M <= m.MOE_FP4_DECODE_MAX_M or m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) > 0
+    decode = M <= m.MOE_FP4_DECODE_MAX_M or (mode == 0 and m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) > 0)
     prefill = not decode
+    exact = prefill and mode == 1
+
+    def layer(i):
+        if mode:
+            m.forward_mode(x, pw, ids_d[i], w_d[i], ws, mode, out=out)
+        else:
+            m.forward(x, pw, ids_d[i], w_d[i], out=out, workspace=ws)
+
     res = {"workload": name, "E": E, "H": H, "I": I, "top_k": k, "M": M, "fmt": gen.FMT_NAMES[fmt]}
+    if exact:
+        res["prefill_mode"] = "bf16-exact"
     # correctness first: one layer against the oracle, and a clean status word
-    m.forward(x, pw, ids_d[0], w_d[0], out=out, workspace=ws)
+    layer(0)
     torch.cuda.synchronize()
-    res["parity"] = oracle_check(m, gen, weights, c, x, ids_pool[0], w_pool[0], out, prefill, threads)
+    res["parity"] = oracle_check(m, gen, weights, c, x, ids_pool[0], w_pool[0], out, prefill, threads, exact)
     res["parity"]["status_word"] = m.workspace_status(ws)
     del weights
     if not res["parity"]["ok"] or res["parity"]["status_word"] != 0:
@@ -389,14 +408,14 @@ def measure(m, name, ov, K, W, dev, rank, ws_world, min_timed_s, threads, do_e2e
     per_layer_bytes = [layer_bytes(ids_pool[i], E, H, I, M, k, fmt)[0] for i in range(K)]
     step_flops = sum(layer_flops(ids_pool[i], E, H, I) for i in range(K))
     for i in range(W):
-        m.forward(x, pw, ids_d[i % K], w_d[i % K], out=out, workspace=ws)
+        layer(i % K)
     torch.cuda.synchronize()
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         for i in range(K):
-            m.forward(x, pw, ids_d[i], w_d[i], out=out, workspace=ws)
+            layer(i)
     torch.cuda.synchronize()
     g.replay()
     torch.cuda.synchronize()
@@ -432,11 +451,14 @@ def measure(m, name, ov, K, W, dev, rank, ws_world, min_timed_s, threads, do_e2e
                 "us_per_layer": ms_max * 1e3 / K, "us_per_layer_min": min(times) * 1e3 / K,
                 "us_per_layer_max": max(times) * 1e3 / K, "routed_bytes_per_layer": sum(per_layer_bytes) / K,
                 "flops_per_layer": step_flops / K, "job_units": job_units, "ms_per_replay": ms_max,
-                "launches_per_layer": m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) if decode else 8,
+                "launches_per_layer": m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) if decode else
+                (7 if exact else 8),
                 "plan": decode_kernel_label(m, M, E, H, I, k) if decode else
-                "prefill layer: route, x quantiser, FC1 GEMM, h quantiser, FC2 GEMM, cast (8 launches)",
+                ("exact prefill layer: route, x copy per routed row, FC1 and FC2 BF16 GEMMs on FP4 weights decoded "
+                 "in shared memory, cast (7 launches)" if exact else
+                 "prefill layer: route, x quantiser, FC1 GEMM, h quantiser, FC2 GEMM, cast (8 launches)"),
                 "window": window, "prefill": prefill})
-    if do_e2e:
+    if do_e2e and not exact:
         # end to end through the host-buffer entry point, one eager call per
         # layer: H2D of x, ids and router weights, the layer, D2H of the output
         xh = x.cpu().pin_memory()
@@ -480,7 +502,8 @@ def roofline_of(res, peak, peak_kind, traffic):
                 "peak_source": f"hbm_gbs of {peak_kind}", "traffic": traffic, "kernel": res["plan"]}
     from workload import gen
     bf16, bf16_kind = load_bf16_peak()
-    fp4_peak = 6.0 * bf16
+    exact = res.get("prefill_mode") == "bf16-exact"  # BF16 tensor cores
+    fp4_peak = bf16 if exact else 6.0 * bf16
     c = res["_state"][0]
     E, H, I, M, fmt = c["E"], c["H"], c["I"], c["M"], c["fmt"]
     ids_pool = res["_state"][2]
@@ -495,12 +518,13 @@ def roofline_of(res, peak, peak_kind, traffic):
             "peak": peak if bound == "hbm" else fp4_peak, "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
             "frac": ach_gbs / peak if bound == "hbm" else ach_tf / fp4_peak,
             "peak_source": f"hbm_gbs of {peak_kind}" if bound == "hbm"
-            else f"bf16_tflops of {bf16_kind} x 6 (nominal fp4/bf16)",
+            else (f"bf16_tflops of {bf16_kind}" if exact else f"bf16_tflops of {bf16_kind} x 6 (nominal fp4/bf16)"),
             "traffic": traffic, "kernel": res["plan"], "algorithmic_bytes_per_layer": alg_bytes,
             "arithmetic_intensity_flop_per_byte": ai, "ceiling_tflops": min(fp4_peak, ai * peak * 1e9 / 1e12),
             "tflops": ach_tf,
             "tensor_view": {"achieved": ach_tf, "peak": fp4_peak, "unit": "TFLOP/s", "frac": ach_tf / fp4_peak,
-                            "peak_source": f"bf16_tflops of {bf16_kind} x 6 (nominal fp4/bf16)"}}
+                            "peak_source": f"bf16_tflops of {bf16_kind}" if exact else
+                            f"bf16_tflops of {bf16_kind} x 6 (nominal fp4/bf16)"}}
 
 
 def stored_traffic(args_workload, M, fmt_name, E_override):
@@ -536,7 +560,8 @@ def run_ours(args):
     threads = affinity_cores()
     K, W = args.steps, args.warmup
     sampler = ClockSampler(local)
-    ov = {"M": args.M, "E": args.E, "fmt": None if args.fmt is None else (0 if args.fmt == "mxfp4" else 1)}
+    ov = {"M": args.M, "E": args.E, "fmt": None if args.fmt is None else (0 if args.fmt == "mxfp4" else 1),
+          "prefill_mode": 1 if args.prefill_mode == "bf16" else None}
     head = measure(m, args.workload, ov, K, W, dev, rank, ws, args.min_timed_s, threads, not args.no_e2e, sampler)
     c, seed, ids_pool, w_pool, x = head.pop("_state")
     E, H, I, k, M, fmt = c["E"], c["H"], c["I"], c["top_k"], c["M"], c["fmt"]
@@ -567,7 +592,8 @@ def run_ours(args):
                      "e2e": head.get("e2e"),
                      "gpu_launches": head["launches_per_layer"] * K * head["replays"]})
         if prefill:
-            line["dtype"] = "e2m1 x e2m1 (nvfp4 activations), fp32 accumulate"
+            line["dtype"] = "bf16 x (e2m1 decoded to bf16), fp32 accumulate" if head.get("prefill_mode") else \
+                "e2m1 x e2m1 (nvfp4 activations), fp32 accumulate"
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and head["timed"] and not head["prefill"]:
         done, secs, nbytes, used_threads = oracle_layers(c, seed, ids_pool, w_pool, x.cpu(), args.cpu_seconds, K,
                                                          threads)
@@ -582,7 +608,7 @@ def run_ours(args):
         sweep = []
         for label, name, sov in SWEEP:
             if name == args.workload and all(sov.get(kk, c[kk]) == c[kk] for kk in ("M", "fmt")) \
-                    and args.E is None:
+                    and not sov.get("prefill_mode") and args.E is None:
                 continue  # the headline itself
             try:
                 r = measure(m, name, sov, K, W, dev, rank, ws, args.min_timed_s / 4, threads, not args.no_e2e,

@@ -220,6 +220,36 @@ def forward_act(x: torch.Tensor, pw: PreparedWeights, topk_ids: torch.Tensor, to
     return out
 
 
+PREFILL_NVFP4, PREFILL_BF16 = _capi.MOE_FP4_PREFILL_NVFP4, _capi.MOE_FP4_PREFILL_BF16
+
+
+def alloc_workspace_mode(M_max: int, E: int, H: int, I: int, top_k: int, fmt: int, prefill_mode: int,
+                         device=None) -> torch.Tensor:
+    """A zero-filled workspace for ``forward_mode`` with this prefill precision."""
+    n = _capi.moe_fp4_workspace_bytes_mode(M_max, E, H, I, top_k, fmt, prefill_mode)
+    if n == 0:
+        raise MoeFp4Error("moe_fp4_workspace_bytes_mode", _capi.MOE_FP4_EUNSUPPORTED)
+    return torch.zeros(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+
+
+def forward_mode(x: torch.Tensor, pw: PreparedWeights, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                 workspace: torch.Tensor, prefill_mode: int = PREFILL_BF16, kind: int = ACT_SILU, alpha: float = 0.0,
+                 beta: float = 1.0, limit: float = 0.0, out: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    """The layer with a chosen prefill precision (PREFILL_NVFP4 or the exact
+    PREFILL_BF16) and activation, on a workspace from alloc_workspace_mode."""
+    _check_dtypes(x, topk_ids, topk_weights)
+    _require_cuda(x, topk_ids, topk_weights, out, workspace)
+    M, H = x.shape
+    if out is None:
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    act = _capi.MoeFp4Activation(kind, alpha, beta, limit)
+    _capi.moe_fp4_forward_mode(_ptr(x), *pw.ptrs(), _ptr(topk_ids), 1 if topk_ids.dtype == torch.int64 else 0,
+                               _ptr(topk_weights), _ptr(out), M, pw.E, pw.H, pw.I, topk_ids.shape[1], pw.fmt, act,
+                               prefill_mode, _ptr(workspace), workspace.nbytes, _stream(stream, x.device))
+    return out
+
+
 def host_workspace_bytes(M_max: int, E: int, H: int, I: int, top_k: int, fmt: int) -> int:
     return _capi.moe_fp4_host_workspace_bytes(M_max, E, H, I, top_k, fmt)
 

@@ -28,6 +28,8 @@ MOE_FP4_ACT_SILU = 0
 MOE_FP4_ACT_GELU_TANH = 1
 MOE_FP4_ACT_SWIGLUOAI = 2
 MOE_FP4_ACT_RELU2 = 3
+MOE_FP4_PREFILL_NVFP4 = 0
+MOE_FP4_PREFILL_BF16 = 1
 MOE_FP4_STATUS_OK = 0
 MOE_FP4_STATUS_TEST_WAIT = 8192
 
@@ -55,6 +57,9 @@ SIGNATURES = {
     "moe_fp4_unprepare_weights": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "moe_fp4_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
     "moe_fp4_workspace_zero_bytes": (_Z, [_I, _I, _I, _I, _I]),
+    "moe_fp4_workspace_bytes_mode": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
+    "moe_fp4_forward_mode": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I,
+                                  ctypes.POINTER(MoeFp4Activation), _I, _P, _Z, _P]),
     "moe_fp4_reserve_workspace": (_I, [_I, _I, _I, _I, _I, _I, _P]),
     "moe_fp4_release_workspace": (_I, []),
     "moe_fp4_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
@@ -169,6 +174,16 @@ def moe_fp4_unprepare_weights_relu2(w1, s1, w2, s2, E, H, I, fmt, w1_l, s1_l, g1
 
 def moe_fp4_workspace_bytes(M_max, E, H, I, top_k, fmt) -> int:
     return int(_load().moe_fp4_workspace_bytes(M_max, E, H, I, top_k, fmt))
+
+
+def moe_fp4_workspace_bytes_mode(M_max, E, H, I, top_k, fmt, prefill_mode) -> int:
+    return int(lib().moe_fp4_workspace_bytes_mode(M_max, E, H, I, top_k, fmt, prefill_mode))
+
+
+def moe_fp4_forward_mode(x, w13, s13, w2, s2, ids, ids64, tw, out, M, E, H, I, top_k, fmt, act, prefill_mode, ws,
+                         ws_bytes, stream):
+    _check("moe_fp4_forward_mode", lib().moe_fp4_forward_mode(x, w13, s13, w2, s2, ids, ids64, tw, out, M, E, H, I,
+                                                               top_k, fmt, act, prefill_mode, ws, ws_bytes, stream))
 
 
 def moe_fp4_workspace_zero_bytes(E, H, I, top_k, fmt) -> int:

@@ -21,11 +21,11 @@ size_t decode_workspace_bytes(int M_max, int H, int I, int top_k, int fmt, int n
 size_t decode_sync_bytes(int H, int I, int top_k);
 cudaError_t launch_debug_gemm(const void* a_q, const void* a_sf, const void* b_q, const void* b_sf, float* d,
                               int M_rows, int N_rows, int K, uint32_t* status, cudaStream_t st, int* cu_err);
-size_t prefill_workspace_bytes(int M, int E, int H, int I, int top_k);
+size_t prefill_workspace_bytes(int M, int E, int H, int I, int top_k, bool exact);
 size_t debug_route_workspace_bytes(int M, int E, int top_k);
 cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                            const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
-                           int top_k, const ActParams& act, void* ws, cudaStream_t st, int* cu_err);
+                           int top_k, const ActParams& act, bool exact, void* ws, cudaStream_t st, int* cu_err);
 cudaError_t launch_debug_route(const int32_t* ids, int M, int E, int top_k, int32_t* perm, int32_t* expert_offset,
                                void* ws, cudaStream_t st);
 cudaError_t launch_debug_quant(const float* in, int rows, int K, uint8_t* q, uint8_t* s, float* G, cudaStream_t st);
@@ -126,14 +126,14 @@ int check_prefill(int M, int E, int I, int top_k, int fmt) {
 
 // Scratch for every batch size up to M (a workspace reserved for M_max serves
 // all smaller batches).
-size_t workspace_need(int M, int E, int H, int I, int top_k, int fmt, int sms) {
+size_t workspace_need(int M, int E, int H, int I, int top_k, int fmt, int sms, bool exact = false) {
   size_t d = 0;
   for (int m = 1; m <= M && m <= MOE_FP4_DECODE_MAX_M; ++m) {
     const size_t b = decode_workspace_bytes(m, H, I, top_k, fmt, sms);
     if (b > d) d = b;
   }
   if (M > MOE_FP4_DECODE_MAX_M) {
-    const size_t p = prefill_workspace_bytes(M, E, H, I, top_k);
+    const size_t p = prefill_workspace_bytes(M, E, H, I, top_k, exact);
     if (p > d) d = p;
   }
   return d;
@@ -373,7 +373,9 @@ bool mid_band_chunks(int M, int H, int I) {
 int forward_any_ids(const void* x_bf16, const void* w13, const void* s13, const void* w2, const void* s2,
                     const void* topk_ids, int ids64, const float* topk_weights, void* out_bf16, int M, int E, int H,
                     int I, int top_k, int fmt, const moe_fp4_activation* act, void* workspace, size_t workspace_bytes,
-                    void* stream) {
+                    void* stream, int prefill_mode = MOE_FP4_PREFILL_NVFP4) {
+  if (prefill_mode != MOE_FP4_PREFILL_NVFP4 && prefill_mode != MOE_FP4_PREFILL_BF16) return MOE_FP4_EINVAL;
+  const bool exact = prefill_mode == MOE_FP4_PREFILL_BF16;
   const int32_t* ids = static_cast<const int32_t*>(topk_ids);
   ActParams ap = {MOE_FP4_ACT_SILU, 0.f, 0.f, 0.f};
   if (act) {
@@ -400,7 +402,7 @@ int forward_any_ids(const void* x_bf16, const void* w13, const void* s13, const 
   int sms = 0;
   st = device_sms(&sms);
   if (st != MOE_FP4_OK) return st;
-  if (M > MOE_FP4_DECODE_MAX_M && mid_band_chunks(M, H, I)) {
+  if (M > MOE_FP4_DECODE_MAX_M && !exact && mid_band_chunks(M, H, I)) {
     // balanced chunks of at most MOE_FP4_DECODE_MAX_M tokens, one after
     // another on the stream (each overwrites only its own rows of out; a
     // chunk's first kernel waits for the previous chunk before it touches
@@ -435,11 +437,11 @@ int forward_any_ids(const void* x_bf16, const void* w13, const void* s13, const 
                                   fmt, ap, workspace, sms, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
   }
-  const size_t need = prefill_workspace_bytes(M, E, H, I, top_k);
+  const size_t need = prefill_workspace_bytes(M, E, H, I, top_k, exact);
   if (need >= kMaxWorkspace || workspace_bytes < need) return MOE_FP4_EWORKSPACE;
   int cu = 0;
   cudaError_t e = launch_prefill(x_bf16, w13, s13, w2, s2, ids, ids64, topk_weights, out_bf16, M, E, H, I, top_k,
-                                 ap, workspace, static_cast<cudaStream_t>(stream), &cu);
+                                 ap, exact, workspace, static_cast<cudaStream_t>(stream), &cu);
   return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
 }
 }  // namespace
@@ -459,6 +461,25 @@ int moe_fp4_forward_ex_i64(const void* x_bf16, const void* w13, const void* s13,
   if (((uintptr_t)topk_ids & 7u) != 0) return MOE_FP4_EINVAL;
   return forward_any_ids(x_bf16, w13, s13, w2, s2, topk_ids, 1, topk_weights, out_bf16, M, E, H, I, top_k, fmt, act,
                          workspace, workspace_bytes, stream);
+}
+
+int moe_fp4_forward_mode(const void* x_bf16, const void* w13, const void* s13, const void* w2, const void* s2,
+                         const void* topk_ids, int ids_int64, const float* topk_weights, void* out_bf16, int M, int E,
+                         int H, int I, int top_k, int fmt, const moe_fp4_activation* act, int prefill_mode,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (ids_int64 != 0 && ids_int64 != 1) return MOE_FP4_EINVAL;
+  if (ids_int64 && ((uintptr_t)topk_ids & 7u) != 0) return MOE_FP4_EINVAL;
+  return forward_any_ids(x_bf16, w13, s13, w2, s2, topk_ids, ids_int64, topk_weights, out_bf16, M, E, H, I, top_k,
+                         fmt, act, workspace, workspace_bytes, stream, prefill_mode);
+}
+
+size_t moe_fp4_workspace_bytes_mode(int M_max, int E, int H, int I, int top_k, int fmt, int prefill_mode) {
+  if (prefill_mode != MOE_FP4_PREFILL_NVFP4 && prefill_mode != MOE_FP4_PREFILL_BF16) return 0;
+  if (M_max < 0 || check_shape(E, H, I, top_k, fmt) != MOE_FP4_OK) return 0;
+  if (M_max > MOE_FP4_DECODE_MAX_M && check_prefill(M_max, E, I, top_k, fmt) != MOE_FP4_OK) return 0;
+  int sms = 0;
+  if (device_sms(&sms) != MOE_FP4_OK) return 0;
+  return workspace_need(M_max < 1 ? 1 : M_max, E, H, I, top_k, fmt, sms, prefill_mode == MOE_FP4_PREFILL_BF16);
 }
 
 int moe_fp4_forward_ws(const void* x_bf16, const void* w13, const void* s13, const void* w2, const void* s2,

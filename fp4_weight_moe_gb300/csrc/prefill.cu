@@ -2,6 +2,7 @@
 // test-support entry point.
 #include <mutex>
 
+#include "gemm_bf16w4.cuh"
 #include "gemm_fp4.cuh"
 
 namespace moe_fp4 {
@@ -216,6 +217,7 @@ struct PrefillArgs {
   uint8_t* xsf;     // chunks [rows/128][H/64][512]
   float* xG;        // [rows]
   __nv_bfloat16* hbuf;  // [rows][I]
+  __nv_bfloat16* xb;    // exact-numerics band: x copied to every routed row [rows][H]
   uint8_t* hq;      // [rows][I/2]
   uint8_t* hsf;     // chunks [rows/128][I/64][512]
   float* hG;        // [rows]
@@ -635,6 +637,167 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   gemm_fp4_persistent<kFc2BN>(&map_h, &map_w, a.I, a.status, n_mt * NT, tile_of, epi);
 }
 
+// ---------------------------------------------------------------- exact numerics
+// The prefill band without activation quantisation: x in BF16 against the
+// FP4 weights decoded to BF16 (exact), FP32 sums on the BF16 tensor cores;
+// h = act(gate, up) staged in BF16 for FC2 (the BF16 tensor cores take BF16
+// operands), FC2 into the same FP32 token accumulator, one cast.
+
+// One warp per token: x's BF16 row into every routed row of the token (the
+// GEMM's A tiles are rows of routed rows); also zeroes the token's FP32
+// accumulator row.
+__global__ void copy_x_kernel(PrefillArgs a) {
+  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (t >= a.M) return;
+  const int lane = threadIdx.x & 31;
+  const int H = a.H, k = a.top_k;
+  const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * H);
+  const int* prow = a.pos + (size_t)t * k;
+  for (int v = lane; v < H / 8; v += 32) {
+    const uint4 u = __ldg(xr + v);
+    for (int j = 0; j < k; ++j) {
+      const int r = prow[j];
+      if (r >= 0) reinterpret_cast<uint4*>(a.xb + (size_t)r * H)[v] = u;
+    }
+  }
+  float4* accr = reinterpret_cast<float4*>(a.acc + (size_t)t * H);
+  for (int v = lane; v < H / 4; v += 32) accr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// FC1, exact, on 128-wide N tiles (one resident 128-row tile: 64 gate/up
+// pairs, or 128 rows of a non-gated expert's w1), so that every I % 64 fits.
+template <int BN>
+__global__ void __launch_bounds__(kBwThreads, 1)
+    fc1_exact_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                     PrefillArgs a) {
+  const bool relu2 = a.act.kind == MOE_FP4_ACT_RELU2;
+  const int NT = relu2 ? (a.I + 127) / 128 : 2 * a.I / BN;
+  const int KG = a.H / 64;
+  const size_t scb = scale_chunk_bytes(relu2 ? (a.I + 127) / 128 * 128 : 2 * a.I, a.H);
+  const float* g13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * scb);
+  const int n_mt = *a.num_tiles;
+  auto tile_of = [&](int idx) {
+    BwTile t;
+    const int mt = idx / NT, nt = idx % NT;
+    t.m_tile = mt;
+    t.n_tile = nt;
+    t.valid = mt < n_mt;
+    if (!t.valid) return t;
+    const int e = a.tile_expert[mt];
+    t.a_row0 = kBwBM * mt;
+    t.b_row0 = (relu2 ? e * a.I : e * 2 * a.I) + BN * nt;
+    t.b_sf0 = a.s13 + (size_t)e * scb + (size_t)(BN / 128) * nt * KG * kChunkBytes;
+    t.b_sf1 = t.b_sf0 + (size_t)KG * kChunkBytes;
+    return t;
+  };
+  auto epi = [&](uint32_t tmem_row, int row, const BwTile& t) {
+    const int r = t.a_row0 + row;
+    const int e = a.tile_expert[t.m_tile];
+    const bool live = a.row_src[r] >= 0;
+    __nv_bfloat16* hrow = a.hbuf + (size_t)r * a.I;
+    if (relu2) {
+      const float g1 = g13[e];
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tmem_row + 32 * c, u);
+        const int n0 = 128 * t.n_tile + 32 * c;
+        if (!live || n0 >= a.I) continue;
+        uint32_t packed[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float r0 = fmaxf(__uint_as_float(u[2 * j]) * g1, 0.f);
+          const float r1 = fmaxf(__uint_as_float(u[2 * j + 1]) * g1, 0.f);
+          const __nv_bfloat162 hv = __floats2bfloat162_rn(r0 * r0, r1 * r1);
+          packed[j] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(hrow + n0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+      }
+      return;
+    }
+    const float sgate = g13[2 * e], sup = g13[2 * e + 1];
+#pragma unroll 1
+    for (int q = 0; q < BN / 128; ++q) {  // the 128-row resident tiles of this N tile
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {  // 32-pair chunks of the tile's 64 pairs
+        uint32_t g[32], u[32];
+        tmem_ld32(tmem_row + 128 * q + 32 * c, g);
+        tmem_ld32(tmem_row + 128 * q + 64 + 32 * c, u);
+        if (live) {
+          const int n0 = 64 * ((BN / 128) * t.n_tile + q) + 32 * c;
+          uint32_t packed[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float h0 = gated_act(__uint_as_float(g[2 * j]) * sgate, __uint_as_float(u[2 * j]) * sup, a.act);
+            const float h1 =
+                gated_act(__uint_as_float(g[2 * j + 1]) * sgate, __uint_as_float(u[2 * j + 1]) * sup, a.act);
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
+            packed[j] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(hrow + n0);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+        }
+      }
+    }
+  };
+  gemm_bf16w4_persistent<BN>(&map_x, &map_w, a.H, a.status, n_mt * NT, tile_of, epi);
+}
+
+// FC2, exact: h (BF16) against w2 decoded to BF16, router-weighted FP32
+// reductions into the token accumulator.
+__global__ void __launch_bounds__(kBwThreads, 1)
+    fc2_exact_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
+                     PrefillArgs a) {
+  constexpr int BN = 256;
+  const int NT = a.H / BN;
+  const int KG = a.I / 64;
+  const size_t scb = scale_chunk_bytes(a.H, a.I);
+  const float* g2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * scb);
+  const int n_mt = *a.num_tiles;
+  auto tile_of = [&](int idx) {
+    BwTile t;
+    const int mt = idx / NT, nt = idx % NT;
+    t.m_tile = mt;
+    t.n_tile = nt;
+    t.valid = mt < n_mt;
+    if (!t.valid) return t;
+    const int e = a.tile_expert[mt];
+    t.a_row0 = kBwBM * mt;
+    t.b_row0 = e * a.H + BN * nt;
+    t.b_sf0 = a.s2 + (size_t)e * scb + (size_t)(BN / 128) * nt * KG * kChunkBytes;
+    t.b_sf1 = t.b_sf0 + (size_t)KG * kChunkBytes;
+    return t;
+  };
+  auto epi = [&](uint32_t tmem_row, int row, const BwTile& t) {
+    const int r = t.a_row0 + row;
+    const int e = a.tile_expert[t.m_tile];
+    const int src = a.row_src[r];
+    const float f = src >= 0 ? g2[e] * a.tw[src] : 0.f;
+    float* dst = a.acc + (size_t)(src >= 0 ? src / a.top_k : 0) * a.H + BN * t.n_tile;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld32(tmem_row + 32 * c, v);
+      if (src >= 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float* p = dst + 32 * c + 4 * i;
+          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p),
+                       "f"(__uint_as_float(v[4 * i]) * f), "f"(__uint_as_float(v[4 * i + 1]) * f),
+                       "f"(__uint_as_float(v[4 * i + 2]) * f), "f"(__uint_as_float(v[4 * i + 3]) * f)
+                       : "memory");
+        }
+      }
+    }
+  };
+  gemm_bf16w4_persistent<BN>(&map_h, &map_w, a.I, a.status, n_mt * NT, tile_of, epi);
+}
+
 __global__ void cast_out_kernel(PrefillArgs a) {
   const size_t n8 = (size_t)a.M * a.H / 8;
   for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n8; v += (size_t)gridDim.x * blockDim.x) {
@@ -738,11 +901,13 @@ size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct PrefillCarve {
   size_t counts, block_base, expert_off, expert_poff, tile_expert, num_tiles, pos, row_src, xq, xsf, xG, hbuf, hq,
-      hsf, hG, acc, status, total;
+      hsf, hG, acc, xb, status, total;
   int n_route_blocks, max_tiles;
 };
 
-PrefillCarve prefill_carve(int M, int E, int H, int I, int top_k) {
+// Workspace carve of the band; the exact-numerics band appends x's BF16 copy
+// per routed row after the common part (a workspace sized for it serves both).
+PrefillCarve prefill_carve(int M, int E, int H, int I, int top_k, bool exact = false) {
   PrefillCarve c;
   const size_t n = (size_t)M * top_k;
   c.n_route_blocks = (int)((n + kRouteBlock - 1) / kRouteBlock);
@@ -775,6 +940,7 @@ PrefillCarve prefill_carve(int M, int E, int H, int I, int top_k) {
   c.hsf = take(rows * I / 16);
   c.hG = take(sizeof(float) * rows);
   c.acc = take(sizeof(float) * M * H);
+  c.xb = exact ? take(rows * H * 2) : 0;
   c.total = o;
   return c;
 }
@@ -813,6 +979,7 @@ PrefillArgs prefill_args(const PrefillCarve& c, void* ws, int M, int E, int H, i
   a.hsf = reinterpret_cast<uint8_t*>(b + c.hsf);
   a.hG = reinterpret_cast<float*>(b + c.hG);
   a.acc = reinterpret_cast<float*>(b + c.acc);
+  a.xb = c.xb ? reinterpret_cast<__nv_bfloat16*>(b + c.xb) : nullptr;
   return a;
 }
 
@@ -826,14 +993,59 @@ cudaError_t launch_route(PrefillArgs& a, cudaStream_t st) {
 }  // namespace
 
 // ---------------------------------------------------------------- host side
-size_t prefill_workspace_bytes(int M, int E, int H, int I, int top_k) {
-  return prefill_carve(M, E, H, I, top_k).total;
+size_t prefill_workspace_bytes(int M, int E, int H, int I, int top_k, bool exact) {
+  return prefill_carve(M, E, H, I, top_k, exact).total;
+}
+
+// The exact-numerics band: route, x copied per routed row, FC1 and FC2 on the
+// BF16 tensor cores with the weights decoded to BF16, the cast.
+static cudaError_t launch_prefill_exact(PrefillArgs& a, const PrefillCarve& c, const void* w13, const void* w2,
+                                        cudaStream_t st, int* cu_err) {
+  const int E = a.E, H = a.H, I = a.I;
+  const bool relu2 = a.act.kind == MOE_FP4_ACT_RELU2;
+  const size_t rows = (size_t)128 * c.max_tiles;
+  CUtensorMap mx, mw13, mh, mw2;
+  auto raw_map = [](CUtensorMap* m, const void* base, uint64_t inner, uint64_t nrows, uint32_t box_rows) {
+    const uint64_t d[2] = {inner, nrows};
+    const uint64_t stride[1] = {inner};
+    const uint32_t box[2] = {32, box_rows};  // 64 E2M1 elements per row and stage
+    return make_u8_map(m, base, 2, d, stride, box, false);
+  };
+  const int bn1 = 128;
+  CUresult r = make_fp4_map(&mx, a.xb, (uint64_t)H * 2, rows, kBwBM);
+  if (r == CUDA_SUCCESS) r = raw_map(&mw13, w13, (uint64_t)H / 2, (uint64_t)E * (relu2 ? I : 2 * I), (uint32_t)bn1);
+  if (r == CUDA_SUCCESS) r = make_fp4_map(&mh, a.hbuf, (uint64_t)I * 2, rows, kBwBM);
+  if (r == CUDA_SUCCESS) r = raw_map(&mw2, w2, (uint64_t)I / 2, (uint64_t)E * H, 256);
+  if (r != CUDA_SUCCESS) {
+    *cu_err = (int)r;
+    return cudaErrorInvalidValue;
+  }
+  static bool attrs = false;
+  if (!attrs) {
+    cudaError_t e = cudaFuncSetAttribute(fc1_exact_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         BwCfg<128>::kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fc2_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BwCfg<256>::kSmem);
+    if (e != cudaSuccess) return e;
+    attrs = true;
+  }
+  cudaError_t e = launch_route(a, st);
+  if (e != cudaSuccess) return e;
+  copy_x_kernel<<<(a.M + 7) / 8, 256, 0, st>>>(a);
+  int sms = 0;
+  e = gemm_sms(&sms);
+  if (e != cudaSuccess) return e;
+  const int g1 = c.max_tiles * (relu2 ? (I + 127) / 128 : 2 * I / 128), g2 = c.max_tiles * (H / 256);
+  fc1_exact_kernel<128><<<g1 < sms ? g1 : sms, kBwThreads, BwCfg<128>::kSmem, st>>>(mx, mw13, a);
+  fc2_exact_kernel<<<g2 < sms ? g2 : sms, kBwThreads, BwCfg<256>::kSmem, st>>>(mh, mw2, a);
+  cast_out_kernel<<<4 * 152, 256, 0, st>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                            const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
-                           int top_k, const ActParams& act, void* ws, cudaStream_t st, int* cu_err) {
-  const PrefillCarve c = prefill_carve(M, E, H, I, top_k);
+                           int top_k, const ActParams& act, bool exact, void* ws, cudaStream_t st, int* cu_err) {
+  const PrefillCarve c = prefill_carve(M, E, H, I, top_k, exact);
   PrefillArgs a = prefill_args(c, ws, M, E, H, I, top_k);
   a.act = act;
   a.x = static_cast<const __nv_bfloat16*>(x);
@@ -843,6 +1055,7 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
   a.s13 = static_cast<const uint8_t*>(s13);
   a.s2 = static_cast<const uint8_t*>(s2);
   a.out = static_cast<__nv_bfloat16*>(out);
+  if (exact) return launch_prefill_exact(a, c, w13, w2, st, cu_err);
   const size_t rows = (size_t)128 * c.max_tiles;
   CUtensorMap mx, mw13, mh, mw2;
   CUresult r = make_fp4_map(&mx, a.xq, (uint64_t)H / 2, rows, kGemmBM);

@@ -296,6 +296,41 @@ MOE_FP4_API int moe_fp4_forward_ex(const void *x_bf16, const void *w13, const vo
                                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * The prefill band's activation precision (M > MOE_FP4_DECODE_MAX_M, except
+ * the chunked decode batches):
+ *   MOE_FP4_PREFILL_NVFP4  (default of every other entry point) x per token
+ *                          and h per routed row quantised to NVFP4, both
+ *                          GEMMs on the FP4 tensor cores (kind::mxf4nvf4)
+ *   MOE_FP4_PREFILL_BF16   exact numerics: x in BF16 against the weights
+ *                          decoded to BF16 (exact: an E2M1 value times its
+ *                          E4M3 block scale has at most six significant
+ *                          bits), FP32 sums on the BF16 tensor cores
+ *                          (kind::f16), h staged in BF16 for FC2; the layer
+ *                          of the plain definition up to FP32/BF16 rounding,
+ *                          at the BF16 tensor-core rate.  Batches past the
+ *                          decode band always take the prefill band here
+ *                          (no decode-kernel chunks).
+ * The pages' decode keeps BF16 activations for accuracy (b12x PR #22, "rp-
+ * native tiny-decode kernel for w4a8_mx (M=1)", section Measured: cosine
+ * 0.999980 with BF16 activations against 0.9990 with MXFP8 ones).
+ *
+ * moe_fp4_forward_mode: moe_fp4_forward_ex (ids_int64 = 0) or _ex_i64
+ * (ids_int64 = 1, ids 8-byte aligned) with a prefill precision; the
+ * workspace must hold moe_fp4_workspace_bytes_mode(M, ..., prefill_mode)
+ * bytes (the BF16 band adds x's BF16 copy per routed row; a workspace sized
+ * for it serves both).  MOE_FP4_EINVAL for an unknown mode.
+ */
+#define MOE_FP4_PREFILL_NVFP4 0
+#define MOE_FP4_PREFILL_BF16 1
+MOE_FP4_API size_t moe_fp4_workspace_bytes_mode(int M_max, int E, int H, int I, int top_k, int fmt,
+                                                int prefill_mode);
+MOE_FP4_API int moe_fp4_forward_mode(const void *x_bf16, const void *w13, const void *s13, const void *w2,
+                                     const void *s2, const void *topk_ids, int ids_int64, const float *topk_weights,
+                                     void *out_bf16, int M, int E, int H, int I, int top_k, int fmt,
+                                     const moe_fp4_activation *act, int prefill_mode, void *workspace,
+                                     size_t workspace_bytes, void *stream);
+
+/*
  * Non-gated experts with the squared ReLU: "relu2" of flashinfer PR #4285
  * ("sync SM12x NVFP4 fused-MoE kernels"), which names it among the
  * activations and keeps the exact activation quantiser for it (its outputs

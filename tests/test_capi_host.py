@@ -261,3 +261,24 @@ def test_relu2_prepared_sizes(lib):
     g13 = _capi.moe_fp4_prepared_sizes(E, H, I, 1)
     assert (w2, s2) == (g13[2], g13[3])
 
+
+
+def test_prefill_mode_argument_errors(lib):
+    """An unknown prefill precision is rejected before anything touches the
+    device, by both the forward call and the workspace query."""
+    import ctypes
+    p = ctypes.c_void_p(0x1000)
+    for mode in (-1, 2, 7):
+        st = lib.moe_fp4_forward_mode(p, p, p, p, p, p, 0, p, p, 16, 8, 256, 128, 2, 1, None, mode, p, 1 << 20, None)
+        assert st == _capi.MOE_FP4_EINVAL
+        assert lib.moe_fp4_workspace_bytes_mode(16, 8, 256, 128, 2, 1, mode) == 0
+    # the shape checks of every entry point apply
+    st = lib.moe_fp4_forward_mode(p, p, p, p, p, p, 0, p, p, 16, 8, 384, 128, 2, 1, None, _capi.MOE_FP4_PREFILL_BF16,
+                                  p, 1 << 20, None)
+    assert st == _capi.MOE_FP4_EUNSUPPORTED
+    st = lib.moe_fp4_forward_mode(p, p, p, p, p, p, 2, p, p, 16, 8, 256, 128, 2, 1, None, _capi.MOE_FP4_PREFILL_BF16,
+                                  p, 1 << 20, None)
+    assert st == _capi.MOE_FP4_EINVAL  # ids_int64 is 0 or 1
+    st = lib.moe_fp4_forward_mode(p, p, p, p, p, p, 0, p, p, 0, 8, 256, 128, 2, 1, None, _capi.MOE_FP4_PREFILL_BF16,
+                                  p, 1 << 20, None)
+    assert st == _capi.MOE_FP4_OK  # empty batch
