@@ -54,8 +54,9 @@ def parse():
     ap.add_argument("--M", type=int, default=None, help="override the token count")
     ap.add_argument("--E", type=int, default=None, help="override the expert count (profiling on smaller memory)")
     ap.add_argument("--fmt", choices=["mxfp4", "nvfp4"], default=None)
-    ap.add_argument("--prefill-mode", choices=["nvfp4", "bf16"], default="nvfp4",
-                    help="prefill-band activation precision of the headline (bf16: the exact band)")
+    ap.add_argument("--prefill-mode", choices=["nvfp4", "bf16", "w4a8"], default="nvfp4",
+                    help="prefill-band activation precision of the headline (bf16: the exact band; w4a8: MXFP8 "
+                         "activations, MXFP4 weights)")
     ap.add_argument("--decode-plan", choices=list(DECODE_PLANS), default="auto",
                     help="decode-band kernel plan (auto: by shape)")
     return ap.parse_args()
@@ -286,7 +287,8 @@ SWEEP = [("C0", "tiny_decode", {}),
          ("C2", "decode_e288_m4", {})] + \
     [(f"C3/M={M}/{f}", "decode_e256", dict(M=M, fmt=fmt)) for fmt, f in ((0, "mxfp4"), (1, "nvfp4"))
      for M in (1, 2, 4, 8)] + \
-    [("C4", "prefill_e128", {}), ("C4/bf16-exact", "prefill_e128", dict(prefill_mode=1))]
+    [("C4", "prefill_e128", {}), ("C4/bf16-exact", "prefill_e128", dict(prefill_mode=1)),
+     ("C4/w4a8-mx", "prefill_e128", dict(prefill_mode=2, fmt=0))]
 
 
 def affinity_cores():
@@ -320,11 +322,13 @@ def parity_metrics(got, want):
             "zero_rows_exact": zero_ok, "ok": ok}
 
 
-def oracle_check(m, gen, weights, c, x, ids, tw, got, prefill, threads, exact=False):
+def oracle_check(m, gen, weights, c, x, ids, tw, got, prefill, threads, mode=0):
     """The layer of one routing draw on the FP64 oracle (routed experts only;
-    the prefill band on a spread of 16 tokens, its activation quantisation
-    mirrored unless the band ran with exact BF16 numerics, which has the
-    plain definition) against the GPU output of the same draw."""
+    the prefill band on a spread of 16 tokens: against the definition of its
+    activation precision, the NVFP4 mirror (mode 0), the plain layer (mode 1,
+    exact BF16) or the W4A8-MX mirror (mode 2)) against the GPU output of the
+    same draw."""
+    exact = mode != 0
     import numpy as np
     import oracle
     import torch
@@ -345,6 +349,10 @@ def oracle_check(m, gen, weights, c, x, ids, tw, got, prefill, threads, exact=Fa
         want = oracle.forward_prefill(x.cpu(), sub, ids_c, tw.cpu(), max(1, len(used)), H, I, k, tokens=tokens,
                                       nthreads=threads, fmt=fmt)[0]
         got_rows = got.float().cpu().double().numpy()[tokens]
+    elif prefill and mode == 2:
+        want = oracle.forward_w4a8(x.cpu()[tokens], sub, ids_c[tokens], tw.cpu()[tokens], max(1, len(used)), H, I, k,
+                                   nthreads=threads)
+        got_rows = got.float().cpu().double().numpy()[tokens]
     elif prefill:
         want = oracle.forward(x.cpu()[tokens], sub, ids_c[tokens], tw.cpu()[tokens], max(1, len(used)), H, I, k, fmt,
                               nthreads=threads)
@@ -355,7 +363,8 @@ def oracle_check(m, gen, weights, c, x, ids, tw, got, prefill, threads, exact=Fa
     secs = time.perf_counter() - t0
     r = parity_metrics(got_rows, want)
     r["oracle_s"] = secs
-    r["checked"] = (f"{len(tokens)} sampled tokens (plain definition)" if exact else
+    r["checked"] = (f"{len(tokens)} sampled tokens ({'W4A8-MX mirror' if mode == 2 else 'plain definition'})"
+                    if exact else
                     f"{len(tokens)} sampled tokens (mirrored activation quantisation)") if prefill else \
         f"all {M} tokens"
     return r
@@ -385,7 +394,7 @@ def measure(m, name, ov, K, W, dev, rank, ws_world, min_timed_s, threads, do_e2e
     out = torch.full((M, H), float("nan"), dtype=torch.bfloat16, device=dev)
     decode = M <= m.MOE_FP4_DECODE_MAX_M or (mode == 0 and m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) > 0)
     prefill = not decode
-    exact = prefill and mode == 1
+    exact = prefill and mode in (1, 2)  # the 16-bit bands (exact BF16, W4A8-MX)
 
     def layer(i):
         if mode:
@@ -395,15 +404,17 @@ def measure(m, name, ov, K, W, dev, rank, ws_world, min_timed_s, threads, do_e2e
 
     res = {"workload": name, "E": E, "H": H, "I": I, "top_k": k, "M": M, "fmt": gen.FMT_NAMES[fmt]}
     if exact:
-        res["prefill_mode"] = "bf16-exact"
+        res["prefill_mode"] = "bf16-exact" if mode == 1 else "w4a8-mx"
     # correctness first: one layer against the oracle, and a clean status word
     layer(0)
     torch.cuda.synchronize()
-    res["parity"] = oracle_check(m, gen, weights, c, x, ids_pool[0], w_pool[0], out, prefill, threads, exact)
+    res["parity"] = oracle_check(m, gen, weights, c, x, ids_pool[0], w_pool[0], out, prefill, threads,
+                                 mode if exact else 0)
     res["parity"]["status_word"] = m.workspace_status(ws)
     del weights
     if not res["parity"]["ok"] or res["parity"]["status_word"] != 0:
         res["timed"] = False
+        res["_state"] = (c, seed, ids_pool, w_pool, x)
         return res
     per_layer_bytes = [layer_bytes(ids_pool[i], E, H, I, M, k, fmt)[0] for i in range(K)]
     step_flops = sum(layer_flops(ids_pool[i], E, H, I) for i in range(K))
@@ -452,10 +463,11 @@ def measure(m, name, ov, K, W, dev, rank, ws_world, min_timed_s, threads, do_e2e
                 "us_per_layer_max": max(times) * 1e3 / K, "routed_bytes_per_layer": sum(per_layer_bytes) / K,
                 "flops_per_layer": step_flops / K, "job_units": job_units, "ms_per_replay": ms_max,
                 "launches_per_layer": m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) if decode else
-                (7 if exact else 8),
+                8,
                 "plan": decode_kernel_label(m, M, E, H, I, k) if decode else
-                ("exact prefill layer: route, x copy per routed row, FC1 and FC2 BF16 GEMMs on FP4 weights decoded "
-                 "in shared memory, cast (7 launches)" if exact else
+                ("16-bit prefill layer: route, x staged in row-scaled FP16 per routed row, FC1 GEMM, h rescaled to "
+                 "FP16, FC2 GEMM (FP16 tensor cores, FP4 weights decoded to FP16 in shared memory), cast (8 launches)"
+                 if exact else
                  "prefill layer: route, x quantiser, FC1 GEMM, h quantiser, FC2 GEMM, cast (8 launches)"),
                 "window": window, "prefill": prefill})
     if do_e2e and not exact:
@@ -502,7 +514,7 @@ def roofline_of(res, peak, peak_kind, traffic):
                 "peak_source": f"hbm_gbs of {peak_kind}", "traffic": traffic, "kernel": res["plan"]}
     from workload import gen
     bf16, bf16_kind = load_bf16_peak()
-    exact = res.get("prefill_mode") == "bf16-exact"  # BF16 tensor cores
+    exact = res.get("prefill_mode") in ("bf16-exact", "w4a8-mx")  # 16-bit tensor cores
     fp4_peak = bf16 if exact else 6.0 * bf16
     c = res["_state"][0]
     E, H, I, M, fmt = c["E"], c["H"], c["I"], c["M"], c["fmt"]
@@ -561,7 +573,7 @@ def run_ours(args):
     K, W = args.steps, args.warmup
     sampler = ClockSampler(local)
     ov = {"M": args.M, "E": args.E, "fmt": None if args.fmt is None else (0 if args.fmt == "mxfp4" else 1),
-          "prefill_mode": 1 if args.prefill_mode == "bf16" else None}
+          "prefill_mode": {"bf16": 1, "w4a8": 2}.get(args.prefill_mode)}
     head = measure(m, args.workload, ov, K, W, dev, rank, ws, args.min_timed_s, threads, not args.no_e2e, sampler)
     c, seed, ids_pool, w_pool, x = head.pop("_state")
     E, H, I, k, M, fmt = c["E"], c["H"], c["I"], c["top_k"], c["M"], c["fmt"]
@@ -592,8 +604,11 @@ def run_ours(args):
                      "e2e": head.get("e2e"),
                      "gpu_launches": head["launches_per_layer"] * K * head["replays"]})
         if prefill:
-            line["dtype"] = "bf16 x (e2m1 decoded to bf16), fp32 accumulate" if head.get("prefill_mode") else \
-                "e2m1 x e2m1 (nvfp4 activations), fp32 accumulate"
+            line["dtype"] = {"bf16-exact": "bf16 activations as row-scaled fp16 x (e2m1 decoded to fp16), fp32 "
+                                           "accumulate",
+                             "w4a8-mx": "mxfp8 activations as row-scaled fp16 x (e2m1 decoded to fp16), fp32 "
+                                        "accumulate"}.get(head.get("prefill_mode"),
+                                                          "e2m1 x e2m1 (nvfp4 activations), fp32 accumulate")
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and head["timed"] and not head["prefill"]:
         done, secs, nbytes, used_threads = oracle_layers(c, seed, ids_pool, w_pool, x.cpu(), args.cpu_seconds, K,
                                                          threads)

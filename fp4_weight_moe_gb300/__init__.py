@@ -220,7 +220,8 @@ def forward_act(x: torch.Tensor, pw: PreparedWeights, topk_ids: torch.Tensor, to
     return out
 
 
-PREFILL_NVFP4, PREFILL_BF16 = _capi.MOE_FP4_PREFILL_NVFP4, _capi.MOE_FP4_PREFILL_BF16
+PREFILL_NVFP4, PREFILL_BF16, PREFILL_W4A8_MX = (_capi.MOE_FP4_PREFILL_NVFP4, _capi.MOE_FP4_PREFILL_BF16,
+                                                _capi.MOE_FP4_PREFILL_W4A8_MX)
 
 
 def alloc_workspace_mode(M_max: int, E: int, H: int, I: int, top_k: int, fmt: int, prefill_mode: int,
@@ -236,8 +237,9 @@ def forward_mode(x: torch.Tensor, pw: PreparedWeights, topk_ids: torch.Tensor, t
                  workspace: torch.Tensor, prefill_mode: int = PREFILL_BF16, kind: int = ACT_SILU, alpha: float = 0.0,
                  beta: float = 1.0, limit: float = 0.0, out: Optional[torch.Tensor] = None,
                  stream=None) -> torch.Tensor:
-    """The layer with a chosen prefill precision (PREFILL_NVFP4 or the exact
-    PREFILL_BF16) and activation, on a workspace from alloc_workspace_mode."""
+    """The layer with a chosen prefill precision (PREFILL_NVFP4, the exact
+    PREFILL_BF16, or PREFILL_W4A8_MX with MXFP8 activations and MXFP4
+    weights) and activation, on a workspace from alloc_workspace_mode."""
     _check_dtypes(x, topk_ids, topk_weights)
     _require_cuda(x, topk_ids, topk_weights, out, workspace)
     M, H = x.shape

@@ -30,6 +30,7 @@ MOE_FP4_ACT_SWIGLUOAI = 2
 MOE_FP4_ACT_RELU2 = 3
 MOE_FP4_PREFILL_NVFP4 = 0
 MOE_FP4_PREFILL_BF16 = 1
+MOE_FP4_PREFILL_W4A8_MX = 2
 MOE_FP4_STATUS_OK = 0
 MOE_FP4_STATUS_TEST_WAIT = 8192
 

@@ -25,7 +25,7 @@ size_t prefill_workspace_bytes(int M, int E, int H, int I, int top_k, bool exact
 size_t debug_route_workspace_bytes(int M, int E, int top_k);
 cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                            const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
-                           int top_k, const ActParams& act, bool exact, void* ws, cudaStream_t st, int* cu_err);
+                           int top_k, const ActParams& act, int band, void* ws, cudaStream_t st, int* cu_err);
 cudaError_t launch_debug_route(const int32_t* ids, int M, int E, int top_k, int32_t* perm, int32_t* expert_offset,
                                void* ws, cudaStream_t st);
 cudaError_t launch_debug_quant(const float* in, int rows, int K, uint8_t* q, uint8_t* s, float* G, cudaStream_t st);
@@ -374,8 +374,10 @@ int forward_any_ids(const void* x_bf16, const void* w13, const void* s13, const 
                     const void* topk_ids, int ids64, const float* topk_weights, void* out_bf16, int M, int E, int H,
                     int I, int top_k, int fmt, const moe_fp4_activation* act, void* workspace, size_t workspace_bytes,
                     void* stream, int prefill_mode = MOE_FP4_PREFILL_NVFP4) {
-  if (prefill_mode != MOE_FP4_PREFILL_NVFP4 && prefill_mode != MOE_FP4_PREFILL_BF16) return MOE_FP4_EINVAL;
-  const bool exact = prefill_mode == MOE_FP4_PREFILL_BF16;
+  if (prefill_mode != MOE_FP4_PREFILL_NVFP4 && prefill_mode != MOE_FP4_PREFILL_BF16 &&
+      prefill_mode != MOE_FP4_PREFILL_W4A8_MX)
+    return MOE_FP4_EINVAL;
+  const bool exact = prefill_mode != MOE_FP4_PREFILL_NVFP4;  // the BF16-engine bands
   const int32_t* ids = static_cast<const int32_t*>(topk_ids);
   ActParams ap = {MOE_FP4_ACT_SILU, 0.f, 0.f, 0.f};
   if (act) {
@@ -389,6 +391,9 @@ int forward_any_ids(const void* x_bf16, const void* w13, const void* s13, const 
   }
   int st = check_shape(E, H, I, top_k, fmt);
   if (st != MOE_FP4_OK) return st;
+  // W4A8-MX: MXFP4 weights, gated activations (the mirror the band follows)
+  if (prefill_mode == MOE_FP4_PREFILL_W4A8_MX && (fmt != MOE_FP4_MXFP4 || ap.kind == MOE_FP4_ACT_RELU2))
+    return MOE_FP4_EUNSUPPORTED;
   if (M < 0) return MOE_FP4_EINVAL;
   if (M == 0) return MOE_FP4_OK;
   if (!x_bf16 || !w13 || !s13 || !w2 || !s2 || !topk_ids || !topk_weights || !out_bf16) return MOE_FP4_EINVAL;
@@ -441,7 +446,7 @@ int forward_any_ids(const void* x_bf16, const void* w13, const void* s13, const 
   if (need >= kMaxWorkspace || workspace_bytes < need) return MOE_FP4_EWORKSPACE;
   int cu = 0;
   cudaError_t e = launch_prefill(x_bf16, w13, s13, w2, s2, ids, ids64, topk_weights, out_bf16, M, E, H, I, top_k,
-                                 ap, exact, workspace, static_cast<cudaStream_t>(stream), &cu);
+                                 ap, prefill_mode, workspace, static_cast<cudaStream_t>(stream), &cu);
   return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
 }
 }  // namespace
@@ -474,12 +479,15 @@ int moe_fp4_forward_mode(const void* x_bf16, const void* w13, const void* s13, c
 }
 
 size_t moe_fp4_workspace_bytes_mode(int M_max, int E, int H, int I, int top_k, int fmt, int prefill_mode) {
-  if (prefill_mode != MOE_FP4_PREFILL_NVFP4 && prefill_mode != MOE_FP4_PREFILL_BF16) return 0;
+  if (prefill_mode != MOE_FP4_PREFILL_NVFP4 && prefill_mode != MOE_FP4_PREFILL_BF16 &&
+      prefill_mode != MOE_FP4_PREFILL_W4A8_MX)
+    return 0;
   if (M_max < 0 || check_shape(E, H, I, top_k, fmt) != MOE_FP4_OK) return 0;
+  if (prefill_mode == MOE_FP4_PREFILL_W4A8_MX && fmt != MOE_FP4_MXFP4) return 0;
   if (M_max > MOE_FP4_DECODE_MAX_M && check_prefill(M_max, E, I, top_k, fmt) != MOE_FP4_OK) return 0;
   int sms = 0;
   if (device_sms(&sms) != MOE_FP4_OK) return 0;
-  return workspace_need(M_max < 1 ? 1 : M_max, E, H, I, top_k, fmt, sms, prefill_mode == MOE_FP4_PREFILL_BF16);
+  return workspace_need(M_max < 1 ? 1 : M_max, E, H, I, top_k, fmt, sms, prefill_mode != MOE_FP4_PREFILL_NVFP4);
 }
 
 int moe_fp4_forward_ws(const void* x_bf16, const void* w13, const void* s13, const void* w2, const void* s2,

@@ -2,7 +2,7 @@
 // test-support entry point.
 #include <mutex>
 
-#include "gemm_bf16w4.cuh"
+#include "gemm_f16w4.cuh"
 #include "gemm_fp4.cuh"
 
 namespace moe_fp4 {
@@ -217,7 +217,8 @@ struct PrefillArgs {
   uint8_t* xsf;     // chunks [rows/128][H/64][512]
   float* xG;        // [rows]
   __nv_bfloat16* hbuf;  // [rows][I]
-  __nv_bfloat16* xb;    // exact-numerics band: x copied to every routed row [rows][H]
+  __half* xb;           // 16-bit bands: x (or its MXFP8 image) in FP16, row-scaled, per routed row [rows][H]
+  int amode;            // 16-bit bands: 0 exact BF16 activations, 1 MXFP8 (W4A8-MX)
   uint8_t* hq;      // [rows][I/2]
   uint8_t* hsf;     // chunks [rows/128][I/64][512]
   float* hG;        // [rows]
@@ -637,190 +638,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   gemm_fp4_persistent<kFc2BN>(&map_h, &map_w, a.I, a.status, n_mt * NT, tile_of, epi);
 }
 
-// ---------------------------------------------------------------- exact numerics
-// The prefill band without activation quantisation: x in BF16 against the
-// FP4 weights decoded to BF16 (exact), FP32 sums on the BF16 tensor cores;
-// h = act(gate, up) staged in BF16 for FC2 (the BF16 tensor cores take BF16
-// operands), FC2 into the same FP32 token accumulator, one cast.
-
-// One warp per token: x's BF16 row into every routed row of the token (the
-// GEMM's A tiles are rows of routed rows); also zeroes the token's FP32
-// accumulator row.
-__global__ void copy_x_kernel(PrefillArgs a) {
-  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-  if (t >= a.M) return;
-  const int lane = threadIdx.x & 31;
-  const int H = a.H, k = a.top_k;
-  const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * H);
-  const int* prow = a.pos + (size_t)t * k;
-  for (int v = lane; v < H / 8; v += 32) {
-    const uint4 u = __ldg(xr + v);
-    for (int j = 0; j < k; ++j) {
-      const int r = prow[j];
-      if (r >= 0) reinterpret_cast<uint4*>(a.xb + (size_t)r * H)[v] = u;
-    }
-  }
-  float4* accr = reinterpret_cast<float4*>(a.acc + (size_t)t * H);
-  for (int v = lane; v < H / 4; v += 32) accr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-}
-
-// FC1, exact, on 128-wide N tiles (one resident 128-row tile: 64 gate/up
-// pairs, or 128 rows of a non-gated expert's w1), so that every I % 64 fits.
-template <int BN>
-__global__ void __launch_bounds__(kBwThreads, 1)
-    fc1_exact_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
-                     PrefillArgs a) {
-  const bool relu2 = a.act.kind == MOE_FP4_ACT_RELU2;
-  const int NT = relu2 ? (a.I + 127) / 128 : 2 * a.I / BN;
-  const int KG = a.H / 64;
-  const size_t scb = scale_chunk_bytes(relu2 ? (a.I + 127) / 128 * 128 : 2 * a.I, a.H);
-  const float* g13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * scb);
-  const int n_mt = *a.num_tiles;
-  auto tile_of = [&](int idx) {
-    BwTile t;
-    const int mt = idx / NT, nt = idx % NT;
-    t.m_tile = mt;
-    t.n_tile = nt;
-    t.valid = mt < n_mt;
-    if (!t.valid) return t;
-    const int e = a.tile_expert[mt];
-    t.a_row0 = kBwBM * mt;
-    t.b_row0 = (relu2 ? e * a.I : e * 2 * a.I) + BN * nt;
-    t.b_sf0 = a.s13 + (size_t)e * scb + (size_t)(BN / 128) * nt * KG * kChunkBytes;
-    t.b_sf1 = t.b_sf0 + (size_t)KG * kChunkBytes;
-    return t;
-  };
-  auto epi = [&](uint32_t tmem_row, int row, const BwTile& t) {
-    const int r = t.a_row0 + row;
-    const int e = a.tile_expert[t.m_tile];
-    const bool live = a.row_src[r] >= 0;
-    __nv_bfloat16* hrow = a.hbuf + (size_t)r * a.I;
-    if (relu2) {
-      const float g1 = g13[e];
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tmem_row + 32 * c, u);
-        const int n0 = 128 * t.n_tile + 32 * c;
-        if (!live || n0 >= a.I) continue;
-        uint32_t packed[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float r0 = fmaxf(__uint_as_float(u[2 * j]) * g1, 0.f);
-          const float r1 = fmaxf(__uint_as_float(u[2 * j + 1]) * g1, 0.f);
-          const __nv_bfloat162 hv = __floats2bfloat162_rn(r0 * r0, r1 * r1);
-          packed[j] = *reinterpret_cast<const uint32_t*>(&hv);
-        }
-        uint4* dst = reinterpret_cast<uint4*>(hrow + n0);
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-          dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-      }
-      return;
-    }
-    const float sgate = g13[2 * e], sup = g13[2 * e + 1];
-#pragma unroll 1
-    for (int q = 0; q < BN / 128; ++q) {  // the 128-row resident tiles of this N tile
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {  // 32-pair chunks of the tile's 64 pairs
-        uint32_t g[32], u[32];
-        tmem_ld32(tmem_row + 128 * q + 32 * c, g);
-        tmem_ld32(tmem_row + 128 * q + 64 + 32 * c, u);
-        if (live) {
-          const int n0 = 64 * ((BN / 128) * t.n_tile + q) + 32 * c;
-          uint32_t packed[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float h0 = gated_act(__uint_as_float(g[2 * j]) * sgate, __uint_as_float(u[2 * j]) * sup, a.act);
-            const float h1 =
-                gated_act(__uint_as_float(g[2 * j + 1]) * sgate, __uint_as_float(u[2 * j + 1]) * sup, a.act);
-            const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
-            packed[j] = *reinterpret_cast<const uint32_t*>(&hv);
-          }
-          uint4* dst = reinterpret_cast<uint4*>(hrow + n0);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-        }
-      }
-    }
-  };
-  gemm_bf16w4_persistent<BN>(&map_x, &map_w, a.H, a.status, n_mt * NT, tile_of, epi);
-}
-
-// FC2, exact: h (BF16) against w2 decoded to BF16, router-weighted FP32
-// reductions into the token accumulator.
-__global__ void __launch_bounds__(kBwThreads, 1)
-    fc2_exact_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
-                     PrefillArgs a) {
-  constexpr int BN = 256;
-  const int NT = a.H / BN;
-  const int KG = a.I / 64;
-  const size_t scb = scale_chunk_bytes(a.H, a.I);
-  const float* g2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * scb);
-  const int n_mt = *a.num_tiles;
-  auto tile_of = [&](int idx) {
-    BwTile t;
-    const int mt = idx / NT, nt = idx % NT;
-    t.m_tile = mt;
-    t.n_tile = nt;
-    t.valid = mt < n_mt;
-    if (!t.valid) return t;
-    const int e = a.tile_expert[mt];
-    t.a_row0 = kBwBM * mt;
-    t.b_row0 = e * a.H + BN * nt;
-    t.b_sf0 = a.s2 + (size_t)e * scb + (size_t)(BN / 128) * nt * KG * kChunkBytes;
-    t.b_sf1 = t.b_sf0 + (size_t)KG * kChunkBytes;
-    return t;
-  };
-  auto epi = [&](uint32_t tmem_row, int row, const BwTile& t) {
-    const int r = t.a_row0 + row;
-    const int e = a.tile_expert[t.m_tile];
-    const int src = a.row_src[r];
-    const float f = src >= 0 ? g2[e] * a.tw[src] : 0.f;
-    float* dst = a.acc + (size_t)(src >= 0 ? src / a.top_k : 0) * a.H + BN * t.n_tile;
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      uint32_t v[32];
-      tmem_ld32(tmem_row + 32 * c, v);
-      if (src >= 0) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float* p = dst + 32 * c + 4 * i;
-          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p),
-                       "f"(__uint_as_float(v[4 * i]) * f), "f"(__uint_as_float(v[4 * i + 1]) * f),
-                       "f"(__uint_as_float(v[4 * i + 2]) * f), "f"(__uint_as_float(v[4 * i + 3]) * f)
-                       : "memory");
-        }
-      }
-    }
-  };
-  gemm_bf16w4_persistent<BN>(&map_h, &map_w, a.I, a.status, n_mt * NT, tile_of, epi);
-}
-
-__global__ void cast_out_kernel(PrefillArgs a) {
-  const size_t n8 = (size_t)a.M * a.H / 8;
-  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n8; v += (size_t)gridDim.x * blockDim.x) {
-    const float4 p = reinterpret_cast<const float4*>(a.acc)[2 * v];
-    const float4 q = reinterpret_cast<const float4*>(a.acc)[2 * v + 1];
-    const __nv_bfloat162 b0 = __floats2bfloat162_rn(p.x, p.y), b1 = __floats2bfloat162_rn(p.z, p.w);
-    const __nv_bfloat162 b2 = __floats2bfloat162_rn(q.x, q.y), b3 = __floats2bfloat162_rn(q.z, q.w);
-    reinterpret_cast<uint4*>(a.out)[v] =
-        make_uint4(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1),
-                   *reinterpret_cast<const uint32_t*>(&b2), *reinterpret_cast<const uint32_t*>(&b3));
-  }
-}
-
-// Grouped routed rows -> unpadded permutation (test support).
-__global__ void route_perm_kernel(PrefillArgs a, int32_t* perm) {
-  const int e = blockIdx.x;
-  const int n = a.expert_off[e + 1] - a.expert_off[e];
-  for (int i = threadIdx.x; i < n; i += blockDim.x) perm[a.expert_off[e] + i] = a.row_src[a.expert_poff[e] + i];
-}
-__global__ void fill_i32_kernel(int32_t* p, int n, int v) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = v;
-}
-
 // MXFP8 (W4A8-MX activations): E4M3 elements with one UE8M0 scale per 32
 // K-elements; block scale 2^e with e = ceil(log2(amax_blk / 448)) (0 for an
 // all-zero block), clamped to [-127, 127]; elements e4m3_rn(a / 2^e), never
@@ -860,6 +677,307 @@ __device__ __forceinline__ void quant_row_mxfp8(int K, const Load32& load32, con
     }
     emit(b, (uint32_t)(e + 127), w);
   }
+}
+
+// One MXFP8 block of 32 values quantised and dequantised in place: the
+// scale exponent and E4M3 rounding of quant_row_mxfp8, then each code times
+// 2^e, exact in FP32 (at most four significant bits, magnitudes >= 2^-136).
+__device__ __forceinline__ void mxfp8_qdq32(float (&v)[32]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int e = mxfp8_scale_exponent(amax);
+  const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e (e <= 120 for finite FP32)
+  const float sc = e > -127 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);  // 2^e
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {  // (the second source lands in the low byte, which widens to the low half)
+    uint16_t c;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(v[2 * j + 1] * inv), "f"(v[2 * j] * inv));
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+    const float2 f = half2_bits_to_float2(h2);
+    v[2 * j] = f.x * sc;
+    v[2 * j + 1] = f.y * sc;
+  }
+}
+
+// ---------------------------------------------------------------- exact numerics
+// The prefill band without NVFP4 activations, on the FP16 tensor cores: x in
+// BF16 (or its MXFP8 image, W4A8-MX) against the FP4 weights decoded to FP16
+// (exact), FP32 sums; h = act(gate, up) staged in BF16 (then, W4A8-MX,
+// through MXFP8), FC2 into the same FP32 token accumulator, one cast.  Every
+// 16-bit operand row is scaled by a power of two so that its largest
+// magnitude lies in [2^14, 2^15): BF16 and MXFP8 values are then exact in
+// FP16 unless they lie more than 2^31 below their row's largest, and the
+// epilogues multiply the power back out (exact).
+
+// FP16 row scale: 2^s with max |v| 2^s in [2^14, 2^15), s in [-126, 126];
+// 0 for a zero or non-finite maximum.
+__device__ __forceinline__ int f16_row_shift(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  if (b == 0u || b >= 0x7F800000u) return 0;
+  const int E = b >= 0x00800000u ? (int)(b >> 23) - 127 : -127;  // floor(log2 amax) (subnormals: below -126)
+  const int sft = 14 - E;
+  return sft < -126 ? -126 : (sft > 126 ? 126 : sft);
+}
+__device__ __forceinline__ float pow2f(int e) {  // e in [-126, 127]
+  return __uint_as_float((uint32_t)(e + 127) << 23);
+}
+__device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// One warp per token: x's BF16 row (amode 0), or its MXFP8 image (amode 1:
+// quantised per 32-element block, then dequantised), scaled by the row's
+// power of two and stored in FP16 into every routed row of the token (the
+// GEMM's A tiles are rows of routed rows), with 2^-s in xG; also zeroes the
+// token's FP32 accumulator row.  The MXFP8 image never exceeds max |x| by
+// more than 2^-4 of it (E4M3 rounds to nearest), so the FP16 range holds.
+__global__ void stage_x_f16_kernel(PrefillArgs a) {
+  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (t >= a.M) return;
+  const int lane = threadIdx.x & 31;
+  const int H = a.H, k = a.top_k;
+  const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * H);
+  const int* prow = a.pos + (size_t)t * k;
+  float amax = 0.f;
+  for (int v = lane; v < H / 8; v += 32) {
+    const uint4 u = __ldg(xr + v);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const int sft = f16_row_shift(amax);
+  const float up = pow2f(sft);
+  if (lane < k) {
+    const int r = prow[lane];
+    if (r >= 0) a.xG[r] = pow2f(-sft);
+  }
+  for (int b = lane; b < H / 32; b += 32) {  // one 32-element block per lane
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = __ldg(xr + 4 * b + q);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
+        v[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    }
+    if (a.amode) mxfp8_qdq32(v);
+    uint4 o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      o[q] = make_uint4(f16x2_of(v[8 * q] * up, v[8 * q + 1] * up), f16x2_of(v[8 * q + 2] * up, v[8 * q + 3] * up),
+                        f16x2_of(v[8 * q + 4] * up, v[8 * q + 5] * up), f16x2_of(v[8 * q + 6] * up, v[8 * q + 7] * up));
+    for (int j = 0; j < k; ++j) {
+      const int r = prow[j];
+      if (r < 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(a.xb + (size_t)r * H) + 4 * b;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = o[q];
+    }
+  }
+  float4* accr = reinterpret_cast<float4*>(a.acc + (size_t)t * H);
+  for (int v = lane; v < H / 4; v += 32) accr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// One warp per live routed row: h (BF16, written by FC1) rescaled by the
+// row's power of two and converted to FP16 in place, 2^-s in hG.
+__global__ void stage_h_f16_kernel(PrefillArgs a) {
+  const int r = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (r >= 128 * *a.num_tiles || a.row_src[r] < 0) return;
+  const int lane = threadIdx.x & 31;
+  uint4* hr = reinterpret_cast<uint4*>(a.hbuf + (size_t)r * a.I);
+  float amax = 0.f;
+  for (int v = lane; v < a.I / 8; v += 32) {
+    const uint4 u = hr[v];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const int sft = f16_row_shift(amax);
+  const float up = pow2f(sft);
+  if (lane == 0) a.hG[r] = pow2f(-sft);
+  for (int v = lane; v < a.I / 8; v += 32) {
+    const uint4 u = hr[v];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o[i] = f16x2_of(__uint_as_float(w[i] << 16) * up, __uint_as_float(w[i] & 0xFFFF0000u) * up);
+    hr[v] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// FC1, exact, on BN-wide N tiles: BN / 128 resident 128-row tiles of 64
+// gate/up pairs each, or (BN = 128) 128 rows of a non-gated expert's w1.
+template <int BN>
+__global__ void __launch_bounds__(kHwThreads, 1)
+    fc1_exact_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                     PrefillArgs a) {
+  const bool relu2 = a.act.kind == MOE_FP4_ACT_RELU2;
+  const int NT = relu2 ? (a.I + 127) / 128 : 2 * a.I / BN;
+  const int KG = a.H / 64;
+  const size_t scb = scale_chunk_bytes(relu2 ? (a.I + 127) / 128 * 128 : 2 * a.I, a.H);
+  const float* g13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * scb);
+  const int n_mt = *a.num_tiles;
+  auto tile_of = [&](int idx) {
+    HwTile t;
+    const int mt = idx / NT, nt = idx % NT;
+    t.m_tile = mt;
+    t.n_tile = nt;
+    t.valid = mt < n_mt;
+    if (!t.valid) return t;
+    const int e = a.tile_expert[mt];
+    t.a_row0 = kHwBM * mt;
+    t.b_row0 = (relu2 ? e * a.I : e * 2 * a.I) + BN * nt;
+    t.b_sf0 = a.s13 + (size_t)e * scb + (size_t)(BN / 128) * nt * KG * kChunkBytes;
+    t.b_sf1 = t.b_sf0 + (size_t)KG * kChunkBytes;
+    return t;
+  };
+  auto epi = [&](uint32_t tmem_row, int row, const HwTile& t) {
+    const int r = t.a_row0 + row;
+    const int e = a.tile_expert[t.m_tile];
+    const bool live = a.row_src[r] >= 0;
+    const float xs = live ? a.xG[r] : 0.f;  // the row's 2^-s
+    __nv_bfloat16* hrow = a.hbuf + (size_t)r * a.I;
+    if (relu2) {
+      const float g1 = g13[e] * xs;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tmem_row + 32 * c, u);
+        const int n0 = 128 * t.n_tile + 32 * c;
+        if (!live || n0 >= a.I) continue;
+        uint32_t packed[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float r0 = fmaxf(__uint_as_float(u[2 * j]) * g1, 0.f);
+          const float r1 = fmaxf(__uint_as_float(u[2 * j + 1]) * g1, 0.f);
+          const __nv_bfloat162 hv = __floats2bfloat162_rn(r0 * r0, r1 * r1);
+          packed[j] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(hrow + n0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+      }
+      return;
+    }
+    const float sgate = g13[2 * e] * xs, sup = g13[2 * e + 1] * xs;
+#pragma unroll 1
+    for (int q = 0; q < BN / 128; ++q) {  // the 128-row resident tiles of this N tile
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {  // 32-pair chunks of the tile's 64 pairs
+        uint32_t g[32], u[32];
+        tmem_ld32(tmem_row + 128 * q + 32 * c, g);
+        tmem_ld32(tmem_row + 128 * q + 64 + 32 * c, u);
+        if (live) {
+          const int n0 = 64 * ((BN / 128) * t.n_tile + q) + 32 * c;
+          float hf[32];  // h staged in BF16 (one 32-element block of the row)
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            hf[j] = __bfloat162float(__float2bfloat16_rn(
+                gated_act(__uint_as_float(g[j]) * sgate, __uint_as_float(u[j]) * sup, a.act)));
+          if (a.amode) mxfp8_qdq32(hf);  // W4A8-MX: h quantised per routed row, block of 32
+          uint32_t packed[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(hf[2 * j], hf[2 * j + 1]);  // exact
+            packed[j] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(hrow + n0);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+        }
+      }
+    }
+  };
+  gemm_f16w4_persistent<BN>(&map_x, &map_w, a.H, a.status, n_mt * NT, tile_of, epi);
+}
+
+// FC2, exact: h (BF16) against w2 decoded to BF16, router-weighted FP32
+// reductions into the token accumulator.
+__global__ void __launch_bounds__(kHwThreads, 1)
+    fc2_exact_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
+                     PrefillArgs a) {
+  constexpr int BN = 256;
+  const int NT = a.H / BN;
+  const int KG = a.I / 64;
+  const size_t scb = scale_chunk_bytes(a.H, a.I);
+  const float* g2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * scb);
+  const int n_mt = *a.num_tiles;
+  auto tile_of = [&](int idx) {
+    HwTile t;
+    const int mt = idx / NT, nt = idx % NT;
+    t.m_tile = mt;
+    t.n_tile = nt;
+    t.valid = mt < n_mt;
+    if (!t.valid) return t;
+    const int e = a.tile_expert[mt];
+    t.a_row0 = kHwBM * mt;
+    t.b_row0 = e * a.H + BN * nt;
+    t.b_sf0 = a.s2 + (size_t)e * scb + (size_t)(BN / 128) * nt * KG * kChunkBytes;
+    t.b_sf1 = t.b_sf0 + (size_t)KG * kChunkBytes;
+    return t;
+  };
+  auto epi = [&](uint32_t tmem_row, int row, const HwTile& t) {
+    const int r = t.a_row0 + row;
+    const int e = a.tile_expert[t.m_tile];
+    const int src = a.row_src[r];
+    const float f = src >= 0 ? g2[e] * a.tw[src] * a.hG[r] : 0.f;
+    float* dst = a.acc + (size_t)(src >= 0 ? src / a.top_k : 0) * a.H + BN * t.n_tile;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld32(tmem_row + 32 * c, v);
+      if (src >= 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float* p = dst + 32 * c + 4 * i;
+          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p),
+                       "f"(__uint_as_float(v[4 * i]) * f), "f"(__uint_as_float(v[4 * i + 1]) * f),
+                       "f"(__uint_as_float(v[4 * i + 2]) * f), "f"(__uint_as_float(v[4 * i + 3]) * f)
+                       : "memory");
+        }
+      }
+    }
+  };
+  gemm_f16w4_persistent<BN>(&map_h, &map_w, a.I, a.status, n_mt * NT, tile_of, epi);
+}
+
+__global__ void cast_out_kernel(PrefillArgs a) {
+  const size_t n8 = (size_t)a.M * a.H / 8;
+  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n8; v += (size_t)gridDim.x * blockDim.x) {
+    const float4 p = reinterpret_cast<const float4*>(a.acc)[2 * v];
+    const float4 q = reinterpret_cast<const float4*>(a.acc)[2 * v + 1];
+    const __nv_bfloat162 b0 = __floats2bfloat162_rn(p.x, p.y), b1 = __floats2bfloat162_rn(p.z, p.w);
+    const __nv_bfloat162 b2 = __floats2bfloat162_rn(q.x, q.y), b3 = __floats2bfloat162_rn(q.z, q.w);
+    reinterpret_cast<uint4*>(a.out)[v] =
+        make_uint4(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1),
+                   *reinterpret_cast<const uint32_t*>(&b2), *reinterpret_cast<const uint32_t*>(&b3));
+  }
+}
+
+// Grouped routed rows -> unpadded permutation (test support).
+__global__ void route_perm_kernel(PrefillArgs a, int32_t* perm) {
+  const int e = blockIdx.x;
+  const int n = a.expert_off[e + 1] - a.expert_off[e];
+  for (int i = threadIdx.x; i < n; i += blockDim.x) perm[a.expert_off[e] + i] = a.row_src[a.expert_poff[e] + i];
+}
+__global__ void fill_i32_kernel(int32_t* p, int n, int v) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = v;
 }
 
 // One warp per row: the MXFP8 quantiser alone (test support).
@@ -954,6 +1072,7 @@ PrefillArgs prefill_args(const PrefillCarve& c, void* ws, int M, int E, int H, i
   a.tw = nullptr;
   a.s13 = a.s2 = nullptr;
   a.out = nullptr;
+  a.amode = 0;
   a.M = M;
   a.E = E;
   a.H = H;
@@ -979,7 +1098,7 @@ PrefillArgs prefill_args(const PrefillCarve& c, void* ws, int M, int E, int H, i
   a.hsf = reinterpret_cast<uint8_t*>(b + c.hsf);
   a.hG = reinterpret_cast<float*>(b + c.hG);
   a.acc = reinterpret_cast<float*>(b + c.acc);
-  a.xb = c.xb ? reinterpret_cast<__nv_bfloat16*>(b + c.xb) : nullptr;
+  a.xb = c.xb ? reinterpret_cast<__half*>(b + c.xb) : nullptr;
   return a;
 }
 
@@ -1011,10 +1130,16 @@ static cudaError_t launch_prefill_exact(PrefillArgs& a, const PrefillCarve& c, c
     const uint32_t box[2] = {32, box_rows};  // 64 E2M1 elements per row and stage
     return make_u8_map(m, base, 2, d, stride, box, false);
   };
-  const int bn1 = 128;
-  CUresult r = make_fp4_map(&mx, a.xb, (uint64_t)H * 2, rows, kBwBM);
+  // FC1 tile width: 256 (two resident 128-row tiles of gate/up pairs) for
+  // gated experts when I % 128 == 0, else 128.  Measured on GB300 at E=128
+  // H=4096 I=1536 M=4096 (exact BF16): 1791 us per layer against 2087 with
+  // 128-wide tiles (A, the activations, staged half as often per FLOP).
+  constexpr int kFc1Wide = 256;
+  const int bn1 = (!relu2 && kFc1Wide == 256 && I % 128 == 0) ? 256 : 128;
+  const int nt1 = relu2 ? (I + 127) / 128 : 2 * I / bn1, nt2 = H / 256;
+  CUresult r = make_fp4_map(&mx, a.xb, (uint64_t)H * 2, rows, kHwBM);
   if (r == CUDA_SUCCESS) r = raw_map(&mw13, w13, (uint64_t)H / 2, (uint64_t)E * (relu2 ? I : 2 * I), (uint32_t)bn1);
-  if (r == CUDA_SUCCESS) r = make_fp4_map(&mh, a.hbuf, (uint64_t)I * 2, rows, kBwBM);
+  if (r == CUDA_SUCCESS) r = make_fp4_map(&mh, a.hbuf, (uint64_t)I * 2, rows, kHwBM);
   if (r == CUDA_SUCCESS) r = raw_map(&mw2, w2, (uint64_t)I / 2, (uint64_t)E * H, 256);
   if (r != CUDA_SUCCESS) {
     *cu_err = (int)r;
@@ -1022,29 +1147,38 @@ static cudaError_t launch_prefill_exact(PrefillArgs& a, const PrefillCarve& c, c
   }
   static bool attrs = false;
   if (!attrs) {
-    cudaError_t e = cudaFuncSetAttribute(fc1_exact_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         BwCfg<128>::kSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(fc2_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BwCfg<256>::kSmem);
+    cudaError_t e = cudaSuccess;
+    auto smem_attr = [&](const void* f, uint32_t bytes) {
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    };
+    smem_attr((const void*)fc1_exact_kernel<128>, HwCfg<128>::kSmem);
+    smem_attr((const void*)fc1_exact_kernel<256>, HwCfg<256>::kSmem);
+    smem_attr((const void*)fc2_exact_kernel, HwCfg<256>::kSmem);
     if (e != cudaSuccess) return e;
     attrs = true;
   }
   cudaError_t e = launch_route(a, st);
   if (e != cudaSuccess) return e;
-  copy_x_kernel<<<(a.M + 7) / 8, 256, 0, st>>>(a);
+  stage_x_f16_kernel<<<(a.M + 7) / 8, 256, 0, st>>>(a);
   int sms = 0;
   e = gemm_sms(&sms);
   if (e != cudaSuccess) return e;
-  const int g1 = c.max_tiles * (relu2 ? (I + 127) / 128 : 2 * I / 128), g2 = c.max_tiles * (H / 256);
-  fc1_exact_kernel<128><<<g1 < sms ? g1 : sms, kBwThreads, BwCfg<128>::kSmem, st>>>(mx, mw13, a);
-  fc2_exact_kernel<<<g2 < sms ? g2 : sms, kBwThreads, BwCfg<256>::kSmem, st>>>(mh, mw2, a);
+  const int g1 = c.max_tiles * nt1, g2 = c.max_tiles * nt2;
+  const int p1 = g1 < sms ? g1 : sms, p2 = g2 < sms ? g2 : sms;
+  if (bn1 == 256)
+    fc1_exact_kernel<256><<<p1, kHwThreads, HwCfg<256>::kSmem, st>>>(mx, mw13, a);
+  else
+    fc1_exact_kernel<128><<<p1, kHwThreads, HwCfg<128>::kSmem, st>>>(mx, mw13, a);
+  stage_h_f16_kernel<<<(unsigned)(rows / 8), 256, 0, st>>>(a);
+  fc2_exact_kernel<<<p2, kHwThreads, HwCfg<256>::kSmem, st>>>(mh, mw2, a);
   cast_out_kernel<<<4 * 152, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                            const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
-                           int top_k, const ActParams& act, bool exact, void* ws, cudaStream_t st, int* cu_err) {
+                           int top_k, const ActParams& act, int band, void* ws, cudaStream_t st, int* cu_err) {
+  const bool exact = band != MOE_FP4_PREFILL_NVFP4;  // the BF16-engine bands
   const PrefillCarve c = prefill_carve(M, E, H, I, top_k, exact);
   PrefillArgs a = prefill_args(c, ws, M, E, H, I, top_k);
   a.act = act;
@@ -1055,7 +1189,10 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
   a.s13 = static_cast<const uint8_t*>(s13);
   a.s2 = static_cast<const uint8_t*>(s2);
   a.out = static_cast<__nv_bfloat16*>(out);
-  if (exact) return launch_prefill_exact(a, c, w13, w2, st, cu_err);
+  if (exact) {
+    a.amode = band == MOE_FP4_PREFILL_W4A8_MX ? 1 : 0;
+    return launch_prefill_exact(a, c, w13, w2, st, cu_err);
+  }
   const size_t rows = (size_t)128 * c.max_tiles;
   CUtensorMap mx, mw13, mh, mw2;
   CUresult r = make_fp4_map(&mx, a.xq, (uint64_t)H / 2, rows, kGemmBM);

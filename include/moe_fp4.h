@@ -307,9 +307,23 @@ MOE_FP4_API int moe_fp4_forward_ex(const void *x_bf16, const void *w13, const vo
  *                          bits), FP32 sums on the BF16 tensor cores
  *                          (kind::f16), h staged in BF16 for FC2; the layer
  *                          of the plain definition up to FP32/BF16 rounding,
- *                          at the BF16 tensor-core rate.  Batches past the
- *                          decode band always take the prefill band here
- *                          (no decode-kernel chunks).
+ *                          at the BF16 tensor-core rate.
+ *   MOE_FP4_PREFILL_W4A8_MX  MXFP8 activations (b12x PR #22, section What:
+ *                          the w4a8_mx variant; flashinfer PR #4285,
+ *                          Description: scale_format_e8m0_k32): x quantised
+ *                          per token and h (staged in BF16) per routed row,
+ *                          E4M3 elements with one UE8M0 scale per 32, block
+ *                          exponent ceil(log2(amax / 448)); MXFP4 weights and
+ *                          gated activations only (MOE_FP4_EUNSUPPORTED
+ *                          otherwise).  Computed on the BF16 engine of the
+ *                          previous mode: every MXFP8 value is exact in BF16
+ *                          (except magnitudes below 2^-133, rounded to BF16
+ *                          subnormals), so the FP32 sums are those of the
+ *                          MXFP8 x MXFP4 products.
+ * Batches past the decode band always take the prefill band in the BF16 and
+ * W4A8-MX modes (no decode-kernel chunks); batches of at most
+ * MOE_FP4_DECODE_MAX_M tokens run the decode band in every mode (BF16
+ * activations, as the pages' w4a8_mx tiny-decode kernel keeps them).
  * The pages' decode keeps BF16 activations for accuracy (b12x PR #22, "rp-
  * native tiny-decode kernel for w4a8_mx (M=1)", section Measured: cosine
  * 0.999980 with BF16 activations against 0.9990 with MXFP8 ones).
@@ -317,11 +331,14 @@ MOE_FP4_API int moe_fp4_forward_ex(const void *x_bf16, const void *w13, const vo
  * moe_fp4_forward_mode: moe_fp4_forward_ex (ids_int64 = 0) or _ex_i64
  * (ids_int64 = 1, ids 8-byte aligned) with a prefill precision; the
  * workspace must hold moe_fp4_workspace_bytes_mode(M, ..., prefill_mode)
- * bytes (the BF16 band adds x's BF16 copy per routed row; a workspace sized
- * for it serves both).  MOE_FP4_EINVAL for an unknown mode.
+ * bytes (the BF16 and W4A8-MX bands add x's BF16 image per routed row; a
+ * workspace sized for either serves every mode; moe_fp4_workspace_bytes_mode
+ * returns 0 for an unknown mode or a mode the format does not support).
+ * MOE_FP4_EINVAL for an unknown mode.
  */
 #define MOE_FP4_PREFILL_NVFP4 0
 #define MOE_FP4_PREFILL_BF16 1
+#define MOE_FP4_PREFILL_W4A8_MX 2
 MOE_FP4_API size_t moe_fp4_workspace_bytes_mode(int M_max, int E, int H, int I, int top_k, int fmt,
                                                 int prefill_mode);
 MOE_FP4_API int moe_fp4_forward_mode(const void *x_bf16, const void *w13, const void *s13, const void *w2,

@@ -268,7 +268,7 @@ def test_prefill_mode_argument_errors(lib):
     device, by both the forward call and the workspace query."""
     import ctypes
     p = ctypes.c_void_p(0x1000)
-    for mode in (-1, 2, 7):
+    for mode in (-1, 3, 7):
         st = lib.moe_fp4_forward_mode(p, p, p, p, p, p, 0, p, p, 16, 8, 256, 128, 2, 1, None, mode, p, 1 << 20, None)
         assert st == _capi.MOE_FP4_EINVAL
         assert lib.moe_fp4_workspace_bytes_mode(16, 8, 256, 128, 2, 1, mode) == 0
@@ -282,3 +282,19 @@ def test_prefill_mode_argument_errors(lib):
     st = lib.moe_fp4_forward_mode(p, p, p, p, p, p, 0, p, p, 0, 8, 256, 128, 2, 1, None, _capi.MOE_FP4_PREFILL_BF16,
                                   p, 1 << 20, None)
     assert st == _capi.MOE_FP4_OK  # empty batch
+
+
+def test_w4a8_mode_limits_on_host(lib):
+    """The W4A8-MX prefill mode takes MXFP4 weights and gated activations
+    only; both limits are checked before anything touches the device."""
+    import ctypes
+    p = ctypes.c_void_p(0x1000)
+    mode = _capi.MOE_FP4_PREFILL_W4A8_MX
+    st = lib.moe_fp4_forward_mode(p, p, p, p, p, p, 0, p, p, 16, 8, 256, 128, 2, _capi.MOE_FP4_NVFP4, None, mode, p,
+                                  1 << 20, None)
+    assert st == _capi.MOE_FP4_EUNSUPPORTED
+    relu2 = _capi.MoeFp4Activation(_capi.MOE_FP4_ACT_RELU2, 0.0, 0.0, 0.0)
+    st = lib.moe_fp4_forward_mode(p, p, p, p, p, p, 0, p, p, 16, 8, 256, 128, 2, _capi.MOE_FP4_MXFP4,
+                                  ctypes.byref(relu2), mode, p, 1 << 20, None)
+    assert st == _capi.MOE_FP4_EUNSUPPORTED
+    assert lib.moe_fp4_workspace_bytes_mode(16, 8, 256, 128, 2, _capi.MOE_FP4_NVFP4, mode) == 0
