@@ -59,6 +59,7 @@ SIGNATURES = {
     "moe_fp4_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
     "moe_fp4_workspace_zero_bytes": (_Z, [_I, _I, _I, _I, _I]),
     "moe_fp4_workspace_bytes_mode": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
+    "moe_fp4_debug_set_w4a8_engine": (_I, [_I]),
     "moe_fp4_forward_mode": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I,
                                   ctypes.POINTER(MoeFp4Activation), _I, _P, _Z, _P]),
     "moe_fp4_reserve_workspace": (_I, [_I, _I, _I, _I, _I, _I, _P]),
@@ -175,6 +176,10 @@ def moe_fp4_unprepare_weights_relu2(w1, s1, w2, s2, E, H, I, fmt, w1_l, s1_l, g1
 
 def moe_fp4_workspace_bytes(M_max, E, H, I, top_k, fmt) -> int:
     return int(_load().moe_fp4_workspace_bytes(M_max, E, H, I, top_k, fmt))
+
+
+def moe_fp4_debug_set_w4a8_engine(fp8: int) -> int:
+    return int(lib().moe_fp4_debug_set_w4a8_engine(fp8))
 
 
 def moe_fp4_workspace_bytes_mode(M_max, E, H, I, top_k, fmt, prefill_mode) -> int:

@@ -22,6 +22,7 @@ size_t decode_sync_bytes(int H, int I, int top_k);
 cudaError_t launch_debug_gemm(const void* a_q, const void* a_sf, const void* b_q, const void* b_sf, float* d,
                               int M_rows, int N_rows, int K, uint32_t* status, cudaStream_t st, int* cu_err);
 size_t prefill_workspace_bytes(int M, int E, int H, int I, int top_k, bool exact);
+int set_w4a8_fp8_engine(int on);
 size_t debug_route_workspace_bytes(int M, int E, int top_k);
 cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                            const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
@@ -477,6 +478,8 @@ int moe_fp4_forward_mode(const void* x_bf16, const void* w13, const void* s13, c
   return forward_any_ids(x_bf16, w13, s13, w2, s2, topk_ids, ids_int64, topk_weights, out_bf16, M, E, H, I, top_k,
                          fmt, act, workspace, workspace_bytes, stream, prefill_mode);
 }
+
+int moe_fp4_debug_set_w4a8_engine(int fp8) { return moe_fp4::set_w4a8_fp8_engine(fp8); }
 
 size_t moe_fp4_workspace_bytes_mode(int M_max, int E, int H, int I, int top_k, int fmt, int prefill_mode) {
   if (prefill_mode != MOE_FP4_PREFILL_NVFP4 && prefill_mode != MOE_FP4_PREFILL_BF16 &&

@@ -4,6 +4,7 @@
 
 #include "gemm_f16w4.cuh"
 #include "gemm_fp4.cuh"
+#include "gemm_mxf8.cuh"
 
 namespace moe_fp4 {
 
@@ -30,10 +31,30 @@ static EncodeTiledFn encode_tiled() {
 // boxes of box[0..rank) bytes x rows, optional 128-byte swizzle.  Encoded
 // maps are kept in a small cache keyed by every argument (a map depends on
 // nothing else), so repeated layer calls skip the encoding.
+static CUresult make_typed_map(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, int rank, const uint64_t* d,
+                               const uint64_t* stride, const uint32_t* box, bool swizzle128);
 CUresult make_u8_map(CUtensorMap* m, const void* base, int rank, const uint64_t* d, const uint64_t* stride,
                      const uint32_t* box, bool swizzle128) {
+  return make_typed_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, rank, d, stride, box, swizzle128);
+}
+
+// 2-D tensor map over packed E2M1 rows [rows][K / 2 bytes] that unpacks them
+// into shared memory as 16-byte groups (8 bytes of 16 packed values, then 8
+// bytes of gap: the layout tcgen05.mma kind::mxf8f6f4 reads 4-bit operands
+// in), box of box_rows x 128 elements (128 bytes in shared memory), 128-byte
+// swizzle.  K % 128 == 0, base 32-byte aligned (the driver checks both).
+CUresult make_e2m1_unpacked_map(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows) {
+  const uint64_t d[2] = {K, rows};
+  const uint64_t stride[1] = {K / 2};
+  const uint32_t box[2] = {128, box_rows};
+  return make_typed_map(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, base, 2, d, stride, box, true);
+}
+
+static CUresult make_typed_map(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, int rank, const uint64_t* d,
+                               const uint64_t* stride, const uint32_t* box, bool swizzle128) {
   struct Entry {
     const void* base;
+    CUtensorMapDataType dtype;
     int rank;
     uint64_t d[3], stride[2];
     uint32_t box[3];
@@ -45,7 +66,7 @@ CUresult make_u8_map(CUtensorMap* m, const void* base, int rank, const uint64_t*
   static std::mutex mu;
   if (rank < 1 || rank > 3) return CUDA_ERROR_INVALID_VALUE;
   auto same = [&](const Entry& e) {
-    if (e.base != base || e.rank != rank || e.sw != swizzle128) return false;
+    if (e.base != base || e.dtype != dtype || e.rank != rank || e.sw != swizzle128) return false;
     for (int i = 0; i < rank; ++i)
       if (e.d[i] != d[i] || e.box[i] != box[i] || (i + 1 < rank && e.stride[i] != stride[i])) return false;
     return true;
@@ -67,7 +88,7 @@ CUresult make_u8_map(CUtensorMap* m, const void* base, int rank, const uint64_t*
     bx[i] = box[i];
     if (i + 1 < rank) strides[i] = stride[i];
   }
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), dims, strides,
+  const CUresult r = enc(m, dtype, (cuuint32_t)rank, const_cast<void*>(base), dims, strides,
                          bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -76,6 +97,7 @@ CUresult make_u8_map(CUtensorMap* m, const void* base, int rank, const uint64_t*
     Entry& e = cache[next];
     e = Entry{};
     e.base = base;
+    e.dtype = dtype;
     e.rank = rank;
     e.sw = swizzle128;
     for (int i = 0; i < rank; ++i) {
@@ -193,6 +215,9 @@ size_t decode_sync_bytes(int H, int I, int top_k);
 namespace {
 
 constexpr int kRouteBlock = 256;  // routing entries per count/scatter block
+// W4A8-MX engine choice (test support): 1 = FP8 tensor cores where the shape
+// allows, 0 = always the 16-bit engine
+int g_w4a8_fp8 = 1;
 constexpr int kMaxPrefillE = 4096;
 
 struct PrefillArgs {
@@ -223,6 +248,11 @@ struct PrefillArgs {
   uint8_t* hsf;     // chunks [rows/128][I/64][512]
   float* hG;        // [rows]
   float* acc;       // [M][H]
+  // W4A8-MX band on the FP8 tensor cores (inside the 16-bit bands' x and h areas)
+  uint8_t* xq8;     // [rows][H] E4M3
+  uint8_t* xsf8;    // UE8M0 chunks [rows/128][H/128][512]
+  uint8_t* hq8;     // [rows][I] E4M3
+  uint8_t* hsf8;    // UE8M0 chunks [rows/128][I/128][512]
   uint32_t* status;
 };
 
@@ -957,6 +987,183 @@ __global__ void __launch_bounds__(kHwThreads, 1)
   gemm_f16w4_persistent<BN>(&map_h, &map_w, a.I, a.status, n_mt * NT, tile_of, epi);
 }
 
+// ---------------------------------------------------------------- W4A8-MX, FP8 tensor cores
+// MXFP8 x (per token) and h (per routed row) against the MXFP4 weights on
+// tcgen05.mma kind::mxf8f6f4 (gemm_mxf8.cuh): the products are those of the
+// W4A8-MX definition exactly, summed in FP32.  Needs I % 128 == 0 (the
+// unpacking tensor map's row length); gated activations.
+
+// Byte offset of (row, 32-element block b) in a UE8M0 chunk array of K =
+// 128 * nst: chunk (row / 128, b / 4), byte (row % 32) * 16 + (row / 32 % 4) * 4
+// + b % 4.
+__device__ __forceinline__ size_t mx_sf_offset(int row, int b, int nst) {
+  return ((size_t)(row >> 7) * nst + (b >> 2)) * kChunkBytes + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (b & 3);
+}
+
+// One warp per token: x quantised to MXFP8 (one 32-block per lane and
+// round) into every routed row of the token; zeroes the token's accumulator.
+__global__ void quant_x_mx_kernel(PrefillArgs a) {
+  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (t >= a.M) return;
+  const int lane = threadIdx.x & 31;
+  const int H = a.H, k = a.top_k, nst = H / 128;
+  const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * H);
+  const int* prow = a.pos + (size_t)t * k;
+  quant_row_mxfp8(
+      H,
+      [&](int b, float (&v)[32]) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 u = __ldg(xr + 4 * b + q);
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            v[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
+            v[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+          }
+        }
+      },
+      [&](int b, uint32_t sb, const uint32_t (&w)[8]) {
+        for (int j = 0; j < k; ++j) {
+          const int r = prow[j];
+          if (r < 0) continue;
+          uint4* dst = reinterpret_cast<uint4*>(a.xq8 + (size_t)r * H + 32 * b);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          a.xsf8[mx_sf_offset(r, b, nst)] = (uint8_t)sb;
+        }
+      });
+  float4* accr = reinterpret_cast<float4*>(a.acc + (size_t)t * H);
+  for (int v = lane; v < H / 4; v += 32) accr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// One MXFP8 block of 32 values (this thread's): E4M3 codes as 8 words
+// (element 4j + i in byte i of word j) and the UE8M0 scale byte, by the rule
+// of quant_row_mxfp8.
+__device__ __forceinline__ uint32_t mxfp8_block32(const float (&v)[32], uint32_t (&w)[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int e = mxfp8_scale_exponent(amax);
+  const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e (e <= 120 for finite FP32)
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {  // (the second source lands in the low byte)
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(v[4 * j + 1] * inv), "f"(v[4 * j] * inv));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(v[4 * j + 3] * inv), "f"(v[4 * j + 2] * inv));
+    w[j] = (uint32_t)lo | ((uint32_t)hi << 16);
+  }
+  return (uint32_t)(e + 127);
+}
+
+// FC1, W4A8-MX: 128-wide N tiles (64 gate/up pairs), two accumulators; the
+// epilogue applies the activation, stages h in BF16 and quantises it per
+// 32-block of the routed row (the thread owns the row) for FC2.
+__global__ void __launch_bounds__(kMxThreads, 1)
+    fc1_mx_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                  PrefillArgs a) {
+  constexpr int BN = 128;
+  const int NT = 2 * a.I / BN;
+  const int KG = a.H / 64, nst = a.H / 128, nsth = a.I / 128;
+  const size_t scb = scale_chunk_bytes(2 * a.I, a.H);
+  const float* g13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * scb);
+  const int n_mt = *a.num_tiles;
+  auto tile_of = [&](int idx) {
+    MxTile t;
+    const int mt = idx / NT, nt = idx % NT;
+    t.m_tile = mt;
+    t.n_tile = nt;
+    t.valid = mt < n_mt;
+    if (!t.valid) return t;
+    const int e = a.tile_expert[mt];
+    t.a_row0 = kMxBM * mt;
+    t.a_sf = a.xsf8 + (size_t)mt * nst * kChunkBytes;
+    t.b_row0 = e * 2 * a.I + BN * nt;
+    t.b_sf0 = a.s13 + (size_t)e * scb + (size_t)nt * KG * kChunkBytes;
+    t.b_sf1 = t.b_sf0;
+    return t;
+  };
+  auto epi = [&](uint32_t tmem_row, int row, const MxTile& t) {
+    const int r = t.a_row0 + row;
+    const int e = a.tile_expert[t.m_tile];
+    const bool live = a.row_src[r] >= 0;
+    const float sgate = g13[2 * e], sup = g13[2 * e + 1];
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {  // 32-pair chunks of the tile's 64 pairs
+      uint32_t g[32], u[32];
+      tmem_ld32(tmem_row + 32 * c, g);
+      tmem_ld32(tmem_row + 64 + 32 * c, u);
+      const int n0 = 64 * t.n_tile + 32 * c;
+      uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      uint32_t sb = 0u;
+      if (live) {
+        float hf[32];  // h staged in BF16
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          hf[j] = __bfloat162float(__float2bfloat16_rn(
+              gated_act(__uint_as_float(g[j]) * sgate, __uint_as_float(u[j]) * sup, a.act)));
+        sb = mxfp8_block32(hf, w);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(a.hq8 + (size_t)r * a.I + n0);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      a.hsf8[mx_sf_offset(r, n0 / 32, nsth)] = (uint8_t)sb;
+    }
+  };
+  gemm_mxf8_persistent<BN>(&map_x, &map_w, a.H, a.status, n_mt * NT, tile_of, epi);
+}
+
+// FC2, W4A8-MX: MXFP8 h against w2, router-weighted FP32 reductions into the
+// token accumulator.
+__global__ void __launch_bounds__(kMxThreads, 1)
+    fc2_mx_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
+                  PrefillArgs a) {
+  constexpr int BN = 256;
+  const int NT = a.H / BN;
+  const int KG = a.I / 64, nst = a.I / 128;
+  const size_t scb = scale_chunk_bytes(a.H, a.I);
+  const float* g2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * scb);
+  const int n_mt = *a.num_tiles;
+  auto tile_of = [&](int idx) {
+    MxTile t;
+    const int mt = idx / NT, nt = idx % NT;
+    t.m_tile = mt;
+    t.n_tile = nt;
+    t.valid = mt < n_mt;
+    if (!t.valid) return t;
+    const int e = a.tile_expert[mt];
+    t.a_row0 = kMxBM * mt;
+    t.a_sf = a.hsf8 + (size_t)mt * nst * kChunkBytes;
+    t.b_row0 = e * a.H + BN * nt;
+    t.b_sf0 = a.s2 + (size_t)e * scb + (size_t)(BN / 128) * nt * KG * kChunkBytes;
+    t.b_sf1 = t.b_sf0 + (size_t)KG * kChunkBytes;
+    return t;
+  };
+  auto epi = [&](uint32_t tmem_row, int row, const MxTile& t) {
+    const int r = t.a_row0 + row;
+    const int e = a.tile_expert[t.m_tile];
+    const int src = a.row_src[r];
+    const float f = src >= 0 ? g2[e] * a.tw[src] : 0.f;
+    float* dst = a.acc + (size_t)(src >= 0 ? src / a.top_k : 0) * a.H + BN * t.n_tile;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld32(tmem_row + 32 * c, v);
+      if (src >= 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float* p = dst + 32 * c + 4 * i;
+          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p),
+                       "f"(__uint_as_float(v[4 * i]) * f), "f"(__uint_as_float(v[4 * i + 1]) * f),
+                       "f"(__uint_as_float(v[4 * i + 2]) * f), "f"(__uint_as_float(v[4 * i + 3]) * f)
+                       : "memory");
+        }
+      }
+    }
+  };
+  gemm_mxf8_persistent<BN>(&map_h, &map_w, a.I, a.status, n_mt * NT, tile_of, epi);
+}
+
 __global__ void cast_out_kernel(PrefillArgs a) {
   const size_t n8 = (size_t)a.M * a.H / 8;
   for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n8; v += (size_t)gridDim.x * blockDim.x) {
@@ -1073,6 +1280,7 @@ PrefillArgs prefill_args(const PrefillCarve& c, void* ws, int M, int E, int H, i
   a.s13 = a.s2 = nullptr;
   a.out = nullptr;
   a.amode = 0;
+  a.xq8 = a.xsf8 = a.hq8 = a.hsf8 = nullptr;
   a.M = M;
   a.E = E;
   a.H = H;
@@ -1112,6 +1320,14 @@ cudaError_t launch_route(PrefillArgs& a, cudaStream_t st) {
 }  // namespace
 
 // ---------------------------------------------------------------- host side
+// Test support: the W4A8-MX engine (1 FP8 tensor cores where the shape
+// allows, 0 the 16-bit engine); returns the previous choice.
+int set_w4a8_fp8_engine(int on) {
+  const int prev = g_w4a8_fp8;
+  g_w4a8_fp8 = on ? 1 : 0;
+  return prev;
+}
+
 size_t prefill_workspace_bytes(int M, int E, int H, int I, int top_k, bool exact) {
   return prefill_carve(M, E, H, I, top_k, exact).total;
 }
@@ -1175,6 +1391,47 @@ static cudaError_t launch_prefill_exact(PrefillArgs& a, const PrefillCarve& c, c
   return cudaGetLastError();
 }
 
+// The W4A8-MX band on the FP8 tensor cores: route, x to MXFP8 per routed row,
+// FC1 (h quantised to MXFP8 in its epilogue), FC2, the cast.  The MXFP8 x and
+// h with their scale chunks live in the 16-bit bands' x and h areas.
+static cudaError_t launch_prefill_mx(PrefillArgs& a, const PrefillCarve& c, const void* w13, const void* w2,
+                                     cudaStream_t st, int* cu_err) {
+  const int E = a.E, H = a.H, I = a.I;
+  const size_t rows = (size_t)128 * c.max_tiles;
+  a.xq8 = reinterpret_cast<uint8_t*>(a.xb);
+  a.xsf8 = a.xq8 + rows * H;
+  a.hq8 = reinterpret_cast<uint8_t*>(a.hbuf);
+  a.hsf8 = a.hq8 + rows * I;
+  CUtensorMap mx, mw13, mh, mw2;
+  CUresult r = make_fp4_map(&mx, a.xq8, (uint64_t)H, rows, kMxBM);
+  if (r == CUDA_SUCCESS) r = make_e2m1_unpacked_map(&mw13, w13, (uint64_t)H, (uint64_t)E * 2 * I, 128);
+  if (r == CUDA_SUCCESS) r = make_fp4_map(&mh, a.hq8, (uint64_t)I, rows, kMxBM);
+  if (r == CUDA_SUCCESS) r = make_e2m1_unpacked_map(&mw2, w2, (uint64_t)I, (uint64_t)E * H, 256);
+  if (r != CUDA_SUCCESS) {
+    *cu_err = (int)r;
+    return cudaErrorInvalidValue;
+  }
+  static bool attrs = false;
+  if (!attrs) {
+    cudaError_t e = cudaFuncSetAttribute(fc1_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MxCfg<128>::kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fc2_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MxCfg<256>::kSmem);
+    if (e != cudaSuccess) return e;
+    attrs = true;
+  }
+  cudaError_t e = launch_route(a, st);
+  if (e != cudaSuccess) return e;
+  quant_x_mx_kernel<<<(a.M + 7) / 8, 256, 0, st>>>(a);
+  int sms = 0;
+  e = gemm_sms(&sms);
+  if (e != cudaSuccess) return e;
+  const int g1 = c.max_tiles * (2 * I / 128), g2 = c.max_tiles * (H / 256);
+  fc1_mx_kernel<<<g1 < sms ? g1 : sms, kMxThreads, MxCfg<128>::kSmem, st>>>(mx, mw13, a);
+  fc2_mx_kernel<<<g2 < sms ? g2 : sms, kMxThreads, MxCfg<256>::kSmem, st>>>(mh, mw2, a);
+  cast_out_kernel<<<4 * 152, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                            const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
                            int top_k, const ActParams& act, int band, void* ws, cudaStream_t st, int* cu_err) {
@@ -1190,6 +1447,9 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
   a.s2 = static_cast<const uint8_t*>(s2);
   a.out = static_cast<__nv_bfloat16*>(out);
   if (exact) {
+    // W4A8-MX on the FP8 tensor cores where w2's rows suit the unpacking
+    // tensor map (I % 128 == 0), else on the 16-bit engine (same products)
+    if (band == MOE_FP4_PREFILL_W4A8_MX && I % 128 == 0 && g_w4a8_fp8) return launch_prefill_mx(a, c, w13, w2, st, cu_err);
     a.amode = band == MOE_FP4_PREFILL_W4A8_MX ? 1 : 0;
     return launch_prefill_exact(a, c, w13, w2, st, cu_err);
   }

@@ -315,11 +315,14 @@ MOE_FP4_API int moe_fp4_forward_ex(const void *x_bf16, const void *w13, const vo
  *                          E4M3 elements with one UE8M0 scale per 32, block
  *                          exponent ceil(log2(amax / 448)); MXFP4 weights and
  *                          gated activations only (MOE_FP4_EUNSUPPORTED
- *                          otherwise).  Computed on the BF16 engine of the
- *                          previous mode: every MXFP8 value is exact in BF16
- *                          (except magnitudes below 2^-133, rounded to BF16
- *                          subnormals), so the FP32 sums are those of the
- *                          MXFP8 x MXFP4 products.
+ *                          otherwise).  Where I % 128 == 0 on the FP8 tensor
+ *                          cores (tcgen05.mma kind::mxf8f6f4: E4M3 x E2M1
+ *                          with UE8M0 scales per 32, the weights' MXFP4
+ *                          scales taken exactly); otherwise on the 16-bit
+ *                          engine of the previous mode (every MXFP8 value is
+ *                          exact in row-scaled FP16 within 2^31 of its row's
+ *                          largest).  Either way the FP32 sums are those of
+ *                          the MXFP8 x MXFP4 products.
  * Batches past the decode band always take the prefill band in the BF16 and
  * W4A8-MX modes (no decode-kernel chunks); batches of at most
  * MOE_FP4_DECODE_MAX_M tokens run the decode band in every mode (BF16
@@ -336,6 +339,12 @@ MOE_FP4_API int moe_fp4_forward_ex(const void *x_bf16, const void *w13, const vo
  * returns 0 for an unknown mode or a mode the format does not support).
  * MOE_FP4_EINVAL for an unknown mode.
  */
+/* Test support: the W4A8-MX engine, 1 (default) = the FP8 tensor cores
+ * (tcgen05.mma kind::mxf8f6f4 on the MXFP8 activations and the MXFP4 weights
+ * as stored) wherever I % 128 == 0, 0 = always the 16-bit engine (the same
+ * products).  Process-wide; returns the previous setting. */
+MOE_FP4_API int moe_fp4_debug_set_w4a8_engine(int fp8);
+
 #define MOE_FP4_PREFILL_NVFP4 0
 #define MOE_FP4_PREFILL_BF16 1
 #define MOE_FP4_PREFILL_W4A8_MX 2

@@ -298,3 +298,11 @@ def test_w4a8_mode_limits_on_host(lib):
                                   ctypes.byref(relu2), mode, p, 1 << 20, None)
     assert st == _capi.MOE_FP4_EUNSUPPORTED
     assert lib.moe_fp4_workspace_bytes_mode(16, 8, 256, 128, 2, _capi.MOE_FP4_NVFP4, mode) == 0
+
+
+def test_w4a8_engine_switch(lib):
+    """The W4A8-MX engine switch returns the previous setting and is restored."""
+    prev = _capi.moe_fp4_debug_set_w4a8_engine(0)
+    assert prev in (0, 1)
+    assert _capi.moe_fp4_debug_set_w4a8_engine(1) == 0
+    assert _capi.moe_fp4_debug_set_w4a8_engine(prev) == 1

@@ -1,11 +1,12 @@
 """The W4A8-MX prefill band (MOE_FP4_PREFILL_W4A8_MX: MXFP4 weights, MXFP8
 activations) on the GPU against the oracle's W4A8-MX definition, through the
-C ABI.
+C ABI, on both of its engines.
 
 The band quantises x per token and h (staged in BF16) per routed row to MXFP8
-(E4M3 elements, one UE8M0 scale per 32) and runs both GEMMs on the BF16
-tensor cores with the MXFP8 values dequantised (exact in BF16) and the
-weights decoded to BF16 (exact); ``oracle.forward_w4a8`` is the same
+(E4M3 elements, one UE8M0 scale per 32).  Where I % 128 == 0 both GEMMs run
+on the FP8 tensor cores (tcgen05.mma kind::mxf8f6f4, the MXFP4 weights as
+stored); otherwise, or with the engine switch at 0, on the 16-bit engine with
+the MXFP8 values carried exactly; ``oracle.forward_w4a8`` is the same
 definition in FP64.  Cases: several tiles per expert, I % 128 != 0, empty
 experts, invalid and int64 ids, the three gated activations, outlier-heavy
 activations (wide block exponents), a full-size E=128 / H=4096 / I=1536 /
@@ -26,6 +27,16 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(scope="module", autouse=True)
 def _build():
     ensure_built()
+
+
+@pytest.fixture(params=[1, 0], ids=["fp8", "16bit"])
+def engine(request):
+    """The W4A8-MX engine: 1 the FP8 tensor cores where I % 128 == 0, 0 the
+    16-bit engine."""
+    c = fm()._capi
+    prev = c.moe_fp4_debug_set_w4a8_engine(request.param)
+    yield request.param
+    c.moe_fp4_debug_set_w4a8_engine(prev)
 
 
 def fm():
@@ -64,7 +75,7 @@ CASES = [  # M, E, H, I, top_k, invalid slots
 
 
 @pytest.mark.parametrize("M,E,H,I,k,invalid", CASES)
-def test_w4a8_prefill_parity(M, E, H, I, k, invalid):
+def test_w4a8_prefill_parity(M, E, H, I, k, invalid, engine):
     m = fm()
     wl = gen.make_workload("decode_e512", device="cuda", M=M, E=E, H=H, I=I, top_k=k, fmt=gen.MXFP4)
     if invalid:
@@ -80,25 +91,25 @@ def test_w4a8_prefill_parity(M, E, H, I, k, invalid):
 
 
 @pytest.mark.parametrize("kind,alpha,beta,limit", [(1, 0.0, 1.0, 0.0), (2, 1.702, 1.0, 7.0)])
-def test_w4a8_prefill_activations(kind, alpha, beta, limit):
+def test_w4a8_prefill_activations(kind, alpha, beta, limit, engine):
     m = fm()
     wl = gen.make_workload("decode_e512", device="cuda", M=96, E=10, H=1024, I=384, top_k=4, fmt=gen.MXFP4)
     got, _ = _run(wl, m.PREFILL_W4A8_MX, kind=kind, alpha=alpha, beta=beta, limit=limit)
     assert_layer_close(got, _want(wl, act=(kind, alpha, beta, limit)), f"W4A8-MX prefill, activation {kind}")
 
 
-def test_w4a8_prefill_outlier_activations():
+def test_w4a8_prefill_outlier_activations(engine):
     """Per 256-wide K stage two channels at 2^8 .. 2^12 and one block near
     2^-20 of the RMS: block exponents spread over the row."""
     from tests.test_hardening_gpu import outlier_activations
     m = fm()
-    wl = gen.make_workload("decode_e512", device="cuda", M=48, E=12, H=2560, I=320, top_k=4, fmt=gen.MXFP4)
+    wl = gen.make_workload("decode_e512", device="cuda", M=48, E=12, H=2560, I=384, top_k=4, fmt=gen.MXFP4)
     wl.x = outlier_activations(wl.M, wl.H, seed=9).cuda()
     got, _ = _run(wl, m.PREFILL_W4A8_MX)
     assert_layer_close(got, _want(wl), "W4A8-MX prefill, outlier activations")
 
 
-def test_w4a8_prefill_full_size_sampled():
+def test_w4a8_prefill_full_size_sampled(engine):
     m = fm()
     wl = gen.make_workload("prefill_e128", device="cuda", fmt=gen.MXFP4)
     got, _ = _run(wl, m.PREFILL_W4A8_MX)
