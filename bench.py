@@ -405,6 +405,8 @@ def measure(m, name, ov, K, W, dev, rank, ws_world, min_timed_s, threads, do_e2e
     res = {"workload": name, "E": E, "H": H, "I": I, "top_k": k, "M": M, "fmt": gen.FMT_NAMES[fmt]}
     if exact:
         res["prefill_mode"] = "bf16-exact" if mode == 1 else "w4a8-mx"
+        # W4A8-MX runs on the FP8 tensor cores where I % 128 == 0
+        res["engine"] = "fp8" if mode == 2 and I % 128 == 0 else "16-bit"
     # correctness first: one layer against the oracle, and a clean status word
     layer(0)
     torch.cuda.synchronize()
@@ -463,9 +465,12 @@ def measure(m, name, ov, K, W, dev, rank, ws_world, min_timed_s, threads, do_e2e
                 "us_per_layer_max": max(times) * 1e3 / K, "routed_bytes_per_layer": sum(per_layer_bytes) / K,
                 "flops_per_layer": step_flops / K, "job_units": job_units, "ms_per_replay": ms_max,
                 "launches_per_layer": m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) if decode else
-                8,
+                (7 if res.get("engine") == "fp8" else 8),
                 "plan": decode_kernel_label(m, M, E, H, I, k) if decode else
-                ("16-bit prefill layer: route, x staged in row-scaled FP16 per routed row, FC1 GEMM, h rescaled to "
+                ("W4A8-MX prefill layer: route, x to MXFP8 per routed row, FC1 and FC2 on tcgen05 kind::mxf8f6f4 "
+                 "(E4M3 x E2M1 as stored, h to MXFP8 in FC1's epilogue), cast (7 launches)"
+                 if res.get("engine") == "fp8" else
+                 "16-bit prefill layer: route, x staged in row-scaled FP16 per routed row, FC1 GEMM, h rescaled to "
                  "FP16, FC2 GEMM (FP16 tensor cores, FP4 weights decoded to FP16 in shared memory), cast (8 launches)"
                  if exact else
                  "prefill layer: route, x quantiser, FC1 GEMM, h quantiser, FC2 GEMM, cast (8 launches)"),
@@ -514,8 +519,9 @@ def roofline_of(res, peak, peak_kind, traffic):
                 "peak_source": f"hbm_gbs of {peak_kind}", "traffic": traffic, "kernel": res["plan"]}
     from workload import gen
     bf16, bf16_kind = load_bf16_peak()
-    exact = res.get("prefill_mode") in ("bf16-exact", "w4a8-mx")  # 16-bit tensor cores
-    fp4_peak = bf16 if exact else 6.0 * bf16
+    exact = res.get("prefill_mode") in ("bf16-exact", "w4a8-mx")  # 16-bit or FP8 tensor cores
+    fp8 = res.get("engine") == "fp8"
+    fp4_peak = (2.0 * bf16 if fp8 else bf16) if exact else 6.0 * bf16
     c = res["_state"][0]
     E, H, I, M, fmt = c["E"], c["H"], c["I"], c["M"], c["fmt"]
     ids_pool = res["_state"][2]
@@ -530,12 +536,14 @@ def roofline_of(res, peak, peak_kind, traffic):
             "peak": peak if bound == "hbm" else fp4_peak, "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
             "frac": ach_gbs / peak if bound == "hbm" else ach_tf / fp4_peak,
             "peak_source": f"hbm_gbs of {peak_kind}" if bound == "hbm"
-            else (f"bf16_tflops of {bf16_kind}" if exact else f"bf16_tflops of {bf16_kind} x 6 (nominal fp4/bf16)"),
+            else (f"bf16_tflops of {bf16_kind} x 2 (nominal fp8/bf16)" if fp8 else f"bf16_tflops of {bf16_kind}"
+                  if exact else f"bf16_tflops of {bf16_kind} x 6 (nominal fp4/bf16)"),
             "traffic": traffic, "kernel": res["plan"], "algorithmic_bytes_per_layer": alg_bytes,
             "arithmetic_intensity_flop_per_byte": ai, "ceiling_tflops": min(fp4_peak, ai * peak * 1e9 / 1e12),
             "tflops": ach_tf,
             "tensor_view": {"achieved": ach_tf, "peak": fp4_peak, "unit": "TFLOP/s", "frac": ach_tf / fp4_peak,
-                            "peak_source": f"bf16_tflops of {bf16_kind}" if exact else
+                            "peak_source": f"bf16_tflops of {bf16_kind} x 2 (nominal fp8/bf16)" if fp8 else
+                            f"bf16_tflops of {bf16_kind}" if exact else
                             f"bf16_tflops of {bf16_kind} x 6 (nominal fp4/bf16)"}}
 
 
@@ -606,9 +614,11 @@ def run_ours(args):
         if prefill:
             line["dtype"] = {"bf16-exact": "bf16 activations as row-scaled fp16 x (e2m1 decoded to fp16), fp32 "
                                            "accumulate",
-                             "w4a8-mx": "mxfp8 activations as row-scaled fp16 x (e2m1 decoded to fp16), fp32 "
-                                        "accumulate"}.get(head.get("prefill_mode"),
-                                                          "e2m1 x e2m1 (nvfp4 activations), fp32 accumulate")
+                             "w4a8-mx": "e4m3 x e2m1 with ue8m0 scales (mxfp8 activations), fp32 accumulate"
+                             if head.get("engine") == "fp8" else
+                             "mxfp8 activations as row-scaled fp16 x (e2m1 decoded to fp16), fp32 "
+                             "accumulate"}.get(head.get("prefill_mode"),
+                                               "e2m1 x e2m1 (nvfp4 activations), fp32 accumulate")
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and head["timed"] and not head["prefill"]:
         done, secs, nbytes, used_threads = oracle_layers(c, seed, ids_pool, w_pool, x.cpu(), args.cpu_seconds, K,
                                                          threads)

@@ -87,19 +87,22 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
                : "memory");
 }
 
-// UE8M0 byte of an E4M3 power of two (0 -> 0: a flushed block, read as 2^-127,
-// which leaves its products below the FP32 sums' resolution).  Normal
-// 2^(E - 7) -> E + 120; subnormal 2^-9, 2^-8, 2^-7 -> 118, 119, 120.
-__device__ __forceinline__ uint32_t ue8m0_of_e4m3_pow2(uint32_t v) {
-  const uint32_t E = (v >> 3) & 15u;
-  if (E) return E + 120u;
-  return v == 0u ? 0u : (v == 1u ? 118u : (v == 2u ? 119u : 120u));
+// UE8M0 bytes of four E4M3 powers of two (one per byte; 0 -> 0: a flushed
+// block, read as 2^-127, which leaves its products below the FP32 sums'
+// resolution), without branches: a normal 2^(E - 7) (byte E << 3) gives E +
+// 120; a subnormal 2^-9, 2^-8, 2^-7 (bytes 1, 2, 4) gives 118, 119, 120 by a
+// byte lookup on its low three bits.
+__device__ __forceinline__ uint32_t ue8m0_x4(uint32_t w) {
+  const uint32_t hi = (w >> 3) & 0x1F1F1F1Fu;                                 // E per byte
+  const uint32_t normal = (((hi + 0x7F7F7F7Fu) & 0x80808080u) >> 7) * 0xFFu;  // 0xFF where E > 0
+  const uint32_t sub = w & 0x07070707u;                                       // subnormal code (0 if normal)
+  const uint32_t sel = (sub & 0xFu) | ((sub >> 4) & 0xF0u) | ((sub >> 8) & 0xF00u) | ((sub >> 12) & 0xF000u);
+  return ((hi + 0x78787878u) & normal) | __byte_perm(0x00777600u, 0x00000078u, sel);
 }
 // Four UE8M0 scales of one 128-K stage from the E4M3 words of its two 64-K
 // chunks (bytes = 16-element blocks; each 32-block takes its first half's).
 __device__ __forceinline__ uint32_t ue8m0_word(uint32_t c0, uint32_t c1) {
-  return ue8m0_of_e4m3_pow2(c0 & 0xFFu) | (ue8m0_of_e4m3_pow2((c0 >> 16) & 0xFFu) << 8) |
-         (ue8m0_of_e4m3_pow2(c1 & 0xFFu) << 16) | (ue8m0_of_e4m3_pow2((c1 >> 16) & 0xFFu) << 24);
+  return ue8m0_x4(__byte_perm(c0, c1, 0x6420));
 }
 
 struct MxTile {

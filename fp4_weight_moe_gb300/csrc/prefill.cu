@@ -218,6 +218,11 @@ constexpr int kRouteBlock = 256;  // routing entries per count/scatter block
 // W4A8-MX engine choice (test support): 1 = FP8 tensor cores where the shape
 // allows, 0 = always the 16-bit engine
 int g_w4a8_fp8 = 1;
+// W4A8-MX FC1 tile width (I % 128 == 0 makes either fit).  Measured on GB300
+// at E=128 H=4096 I=1536 M=4096: 1022 us per layer with 128-wide tiles (two
+// accumulators, the epilogue beside the next tile's MMAs) against 1046 with
+// 256-wide ones (one accumulator).
+constexpr int kMxFc1BN = 128;
 constexpr int kMaxPrefillE = 4096;
 
 struct PrefillArgs {
@@ -1056,13 +1061,14 @@ __device__ __forceinline__ uint32_t mxfp8_block32(const float (&v)[32], uint32_t
   return (uint32_t)(e + 127);
 }
 
-// FC1, W4A8-MX: 128-wide N tiles (64 gate/up pairs), two accumulators; the
-// epilogue applies the activation, stages h in BF16 and quantises it per
-// 32-block of the routed row (the thread owns the row) for FC2.
+// FC1, W4A8-MX: BN-wide N tiles (BN / 128 resident 128-row tiles of 64
+// gate/up pairs; two accumulators at BN = 128, one at 256); the epilogue
+// applies the activation, stages h in BF16 and quantises it per 32-block of
+// the routed row (the thread owns the row) for FC2.
+template <int BN>
 __global__ void __launch_bounds__(kMxThreads, 1)
     fc1_mx_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                   PrefillArgs a) {
-  constexpr int BN = 128;
   const int NT = 2 * a.I / BN;
   const int KG = a.H / 64, nst = a.H / 128, nsth = a.I / 128;
   const size_t scb = scale_chunk_bytes(2 * a.I, a.H);
@@ -1079,8 +1085,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     t.a_row0 = kMxBM * mt;
     t.a_sf = a.xsf8 + (size_t)mt * nst * kChunkBytes;
     t.b_row0 = e * 2 * a.I + BN * nt;
-    t.b_sf0 = a.s13 + (size_t)e * scb + (size_t)nt * KG * kChunkBytes;
-    t.b_sf1 = t.b_sf0;
+    t.b_sf0 = a.s13 + (size_t)e * scb + (size_t)(BN / 128) * nt * KG * kChunkBytes;
+    t.b_sf1 = t.b_sf0 + (size_t)KG * kChunkBytes;
     return t;
   };
   auto epi = [&](uint32_t tmem_row, int row, const MxTile& t) {
@@ -1089,25 +1095,28 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const bool live = a.row_src[r] >= 0;
     const float sgate = g13[2 * e], sup = g13[2 * e + 1];
 #pragma unroll 1
-    for (int c = 0; c < 2; ++c) {  // 32-pair chunks of the tile's 64 pairs
-      uint32_t g[32], u[32];
-      tmem_ld32(tmem_row + 32 * c, g);
-      tmem_ld32(tmem_row + 64 + 32 * c, u);
-      const int n0 = 64 * t.n_tile + 32 * c;
-      uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-      uint32_t sb = 0u;
-      if (live) {
-        float hf[32];  // h staged in BF16
+    for (int q = 0; q < BN / 128; ++q) {  // the 128-row resident tiles of this N tile
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {  // 32-pair chunks of the tile's 64 pairs
+        uint32_t g[32], u[32];
+        tmem_ld32(tmem_row + 128 * q + 32 * c, g);
+        tmem_ld32(tmem_row + 128 * q + 64 + 32 * c, u);
+        const int n0 = 64 * ((BN / 128) * t.n_tile + q) + 32 * c;
+        uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        uint32_t sb = 0u;
+        if (live) {
+          float hf[32];  // h staged in BF16
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          hf[j] = __bfloat162float(__float2bfloat16_rn(
-              gated_act(__uint_as_float(g[j]) * sgate, __uint_as_float(u[j]) * sup, a.act)));
-        sb = mxfp8_block32(hf, w);
+          for (int j = 0; j < 32; ++j)
+            hf[j] = __bfloat162float(__float2bfloat16_rn(
+                gated_act(__uint_as_float(g[j]) * sgate, __uint_as_float(u[j]) * sup, a.act)));
+          sb = mxfp8_block32(hf, w);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(a.hq8 + (size_t)r * a.I + n0);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        a.hsf8[mx_sf_offset(r, n0 / 32, nsth)] = (uint8_t)sb;
       }
-      uint4* dst = reinterpret_cast<uint4*>(a.hq8 + (size_t)r * a.I + n0);
-      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      a.hsf8[mx_sf_offset(r, n0 / 32, nsth)] = (uint8_t)sb;
     }
   };
   gemm_mxf8_persistent<BN>(&map_x, &map_w, a.H, a.status, n_mt * NT, tile_of, epi);
@@ -1402,9 +1411,12 @@ static cudaError_t launch_prefill_mx(PrefillArgs& a, const PrefillCarve& c, cons
   a.xsf8 = a.xq8 + rows * H;
   a.hq8 = reinterpret_cast<uint8_t*>(a.hbuf);
   a.hsf8 = a.hq8 + rows * I;
+  // FC1 tile width (128: two accumulators, the epilogue beside the next
+  // tile's MMAs; 256: A staged half as often per FLOP, one accumulator)
+  constexpr int bn1 = kMxFc1BN;
   CUtensorMap mx, mw13, mh, mw2;
   CUresult r = make_fp4_map(&mx, a.xq8, (uint64_t)H, rows, kMxBM);
-  if (r == CUDA_SUCCESS) r = make_e2m1_unpacked_map(&mw13, w13, (uint64_t)H, (uint64_t)E * 2 * I, 128);
+  if (r == CUDA_SUCCESS) r = make_e2m1_unpacked_map(&mw13, w13, (uint64_t)H, (uint64_t)E * 2 * I, bn1);
   if (r == CUDA_SUCCESS) r = make_fp4_map(&mh, a.hq8, (uint64_t)I, rows, kMxBM);
   if (r == CUDA_SUCCESS) r = make_e2m1_unpacked_map(&mw2, w2, (uint64_t)I, (uint64_t)E * H, 256);
   if (r != CUDA_SUCCESS) {
@@ -1413,7 +1425,8 @@ static cudaError_t launch_prefill_mx(PrefillArgs& a, const PrefillCarve& c, cons
   }
   static bool attrs = false;
   if (!attrs) {
-    cudaError_t e = cudaFuncSetAttribute(fc1_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MxCfg<128>::kSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(fc1_mx_kernel<bn1>, cudaFuncAttributeMaxDynamicSharedMemorySize, MxCfg<bn1>::kSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(fc2_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MxCfg<256>::kSmem);
     if (e != cudaSuccess) return e;
@@ -1425,8 +1438,8 @@ static cudaError_t launch_prefill_mx(PrefillArgs& a, const PrefillCarve& c, cons
   int sms = 0;
   e = gemm_sms(&sms);
   if (e != cudaSuccess) return e;
-  const int g1 = c.max_tiles * (2 * I / 128), g2 = c.max_tiles * (H / 256);
-  fc1_mx_kernel<<<g1 < sms ? g1 : sms, kMxThreads, MxCfg<128>::kSmem, st>>>(mx, mw13, a);
+  const int g1 = c.max_tiles * (2 * I / bn1), g2 = c.max_tiles * (H / 256);
+  fc1_mx_kernel<bn1><<<g1 < sms ? g1 : sms, kMxThreads, MxCfg<bn1>::kSmem, st>>>(mx, mw13, a);
   fc2_mx_kernel<<<g2 < sms ? g2 : sms, kMxThreads, MxCfg<256>::kSmem, st>>>(mh, mw2, a);
   cast_out_kernel<<<4 * 152, 256, 0, st>>>(a);
   return cudaGetLastError();

@@ -1,9 +1,10 @@
 """The exact-numerics prefill band (MOE_FP4_PREFILL_BF16) on the GPU against
 the plain FP64 definition of the layer, through the C ABI.
 
-This band quantises no activation: x stays BF16, the FP4 weights are decoded
-to BF16 exactly, both GEMMs sum in FP32 on the BF16 tensor cores and only h
-(staged in BF16 for FC2) and the output are rounded.  So it is compared with
+This band quantises no activation: x keeps its BF16 values (carried in FP16
+rows scaled by a power of two), the FP4 weights are decoded to FP16 exactly,
+both GEMMs sum in FP32 on the FP16 tensor cores and only h (staged in BF16
+for FC2) and the output are rounded.  So it is compared with
 ``oracle.forward`` / ``oracle.forward_relu2`` (the decode band's reference:
 no activation quantisation anywhere), not with the mirrored-quantisation
 prefill definition.  Cases: several tiles per expert, I % 128 != 0 (a
