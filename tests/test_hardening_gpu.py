@@ -13,6 +13,10 @@
 * Workspaces filled with NaN bytes beyond the prefix that must start at zero.
 * Invalid routing slots (ids -1, E, 2^31 - 1) carrying NaN and infinite
   router weights: they still contribute exactly zero.
+* The exact BF16 and W4A8-MX prefill modes (both W4A8 engines) under the
+  same poisoned workspaces and invalid slots, and the exact mode under
+  outlier activations (rows spanning 2^-20 .. 2^12 of the RMS: the FP16 row
+  scaling keeps them exact).
 """
 import numpy as np
 import pytest
@@ -223,3 +227,57 @@ def test_invalid_slots_with_nan_and_inf_weights_prefill():
     want = oracle.forward_prefill(wl.x, wl.weights, wl.topk_ids.cpu(), tw_clean, wl.E, wl.H, wl.I, wl.top_k,
                                   fmt=wl.fmt)[0]
     assert_layer_close(got, want, "prefill band, NaN/inf weights on invalid slots")
+
+
+# ---------------------------------------------------------------- the 16-bit and FP8 prefill modes
+def _run_mode(wl, mode, ws=None):
+    m = fm()
+    pw = m.prepare_weights(wl.weights, wl.E, wl.H, wl.I, wl.fmt)
+    if ws is None:
+        ws = m.alloc_workspace_mode(wl.M, wl.E, wl.H, wl.I, wl.top_k, wl.fmt, mode)
+    out = torch.full((wl.M, wl.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    got = m.forward_mode(wl.x, pw, wl.topk_ids, wl.topk_weights, ws, mode, out=out)
+    torch.cuda.synchronize()
+    assert m.workspace_status(ws) == 0
+    return got
+
+
+def _mode_want(wl, mode, tw=None):
+    m = fm()
+    sub, ids_c, Ec = compact_for_oracle(wl.weights, wl.topk_ids, wl.E, wl.fmt)
+    tw = wl.topk_weights.cpu() if tw is None else tw
+    if mode == m.PREFILL_W4A8_MX:
+        return oracle.forward_w4a8(wl.x, sub, ids_c, tw, Ec, wl.H, wl.I, wl.top_k)
+    return oracle.forward(wl.x, sub, ids_c, tw, Ec, wl.H, wl.I, wl.top_k, wl.fmt)
+
+
+MODES = [("bf16", 1, gen.NVFP4, 320), ("w4a8-fp8", 2, gen.MXFP4, 384), ("w4a8-16bit", 2, gen.MXFP4, 320)]
+
+
+@pytest.mark.parametrize("label,mode,fmt,I", MODES, ids=[x[0] for x in MODES])
+def test_modes_nan_poisoned_workspace(label, mode, fmt, I):
+    m = fm()
+    wl = gen.make_workload("decode_e512", device="cuda", E=12, M=40, I=I, fmt=fmt)
+    n = m._capi.moe_fp4_workspace_bytes_mode(wl.M, wl.E, wl.H, wl.I, wl.top_k, wl.fmt, mode)
+    z = m._capi.moe_fp4_workspace_zero_bytes(wl.E, wl.H, wl.I, wl.top_k, wl.fmt)
+    ws = torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda")  # NaN in every FP32 / BF16 / E4M3 slot
+    ws[:z] = 0
+    got = _run_mode(wl, mode, ws=ws)
+    assert_layer_close(got, _mode_want(wl, mode), f"{label} band, poisoned workspace")
+
+
+@pytest.mark.parametrize("label,mode,fmt,I", MODES, ids=[x[0] for x in MODES])
+def test_modes_invalid_slots_with_nan_and_inf_weights(label, mode, fmt, I):
+    wl = gen.make_workload("decode_e512", device="cuda", E=12, M=40, I=I, fmt=fmt)
+    tw_clean = _invalid_with_bad_weights(wl, seed=7)
+    got = _run_mode(wl, mode)
+    want = _mode_want(wl, mode, tw=tw_clean)
+    assert_layer_close(got, want, f"{label} band, NaN/inf weights on invalid slots")
+
+
+def test_exact_band_outlier_activations():
+    m = fm()
+    wl = gen.make_workload("decode_e512", device="cuda", E=12, M=40, fmt=gen.NVFP4)
+    wl.x = outlier_activations(wl.M, wl.H, seed=4).cuda()
+    got = _run_mode(wl, m.PREFILL_BF16)
+    assert_layer_close(got, _mode_want(wl, m.PREFILL_BF16), "exact band, outlier activations")
