@@ -123,6 +123,25 @@ CUresult make_fp4_map(CUtensorMap* m, const void* base, uint64_t inner_bytes, ui
 
 // SM count of the current device (cached): the persistent GEMMs launch one
 // CTA per SM.
+// Launch with programmatic dependent launch: the kernel may become resident
+// while its predecessor on the stream finishes; every prefill kernel waits
+// for the predecessor's completion (griddepcontrol.wait) before it touches
+// global memory, so only the launch latency overlaps.
+template <class Kern, class... Args>
+static cudaError_t launch_pdl(Kern kern, unsigned grid, unsigned threads, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t c = {};
+  c.gridDim = dim3(grid);
+  c.blockDim = dim3(threads);
+  c.dynamicSmemBytes = smem;
+  c.stream = st;
+  c.attrs = at;
+  c.numAttrs = 1;
+  return cudaLaunchKernelEx(&c, kern, args...);
+}
+
 static cudaError_t gemm_sms(int* sms) {
   static int cache[64] = {0};
   int dev = 0;
@@ -335,6 +354,8 @@ __device__ __forceinline__ void bf16x16_to_f32(const __nv_bfloat16* p, float (&v
 
 // ---------------------------------------------------------------- routing
 __global__ void route_count_kernel(PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
   extern __shared__ int s_hist[];
   for (int e = threadIdx.x; e < a.E; e += blockDim.x) s_hist[e] = 0;
   __syncthreads();
@@ -350,6 +371,8 @@ __global__ void route_count_kernel(PrefillArgs a) {
 // One CTA: per-expert totals, unpadded and 128-padded exclusive offsets, the
 // per-block bases of the stable scatter, the tile list and the padding rows.
 __global__ void route_scan_kernel(PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
   __shared__ int s_tot[kMaxPrefillE];
   __shared__ int s_part[2][1024];
   __shared__ int s_poff[kMaxPrefillE];
@@ -363,8 +386,11 @@ __global__ void route_scan_kernel(PrefillArgs a) {
   for (int base = 0; base < E * tpe; base += blockDim.x) {
     const int v = base + threadIdx.x, e = v / tpe, part = v % tpe;
     int t = 0;
-    if (e < E)
-      for (int b = part * seg; b < min(nb, part * seg + seg); ++b) t += a.counts[(size_t)b * E + e];
+    if (e < E) {
+      const int b1 = min(nb, part * seg + seg);
+#pragma unroll 8  // independent loads in flight together (the sum is the only chain)
+      for (int b = part * seg; b < b1; ++b) t += __ldg(a.counts + (size_t)b * E + e);
+    }
     for (int d = 1; d < tpe; d <<= 1) t += __shfl_xor_sync(0xffffffffu, t, d);
     if (e < E && part == 0) s_tot[e] = t;
   }
@@ -433,7 +459,8 @@ __global__ void route_scan_kernel(PrefillArgs a) {
     const int v = base + threadIdx.x, e = v / tpe, part = v % tpe;
     const int b0 = part * seg, b1 = e < E ? min(nb, b0 + seg) : b0;
     int t = 0;
-    for (int b = b0; b < b1; ++b) t += a.counts[(size_t)b * E + e];
+#pragma unroll 8
+    for (int b = b0; b < b1; ++b) t += __ldg(a.counts + (size_t)b * E + e);
     int incl = t;  // inclusive scan over the parts of this expert
     for (int d = 1; d < tpe; d <<= 1) {
       const int o = __shfl_up_sync(0xffffffffu, incl, d);
@@ -441,9 +468,11 @@ __global__ void route_scan_kernel(PrefillArgs a) {
     }
     if (e < E) {
       int run = s_poff[e] + incl - t;
+#pragma unroll 8
       for (int b = b0; b < b1; ++b) {
+        const int cnt = __ldg(a.counts + (size_t)b * E + e);
         a.block_base[(size_t)b * E + e] = run;
-        run += a.counts[(size_t)b * E + e];
+        run += cnt;
       }
     }
   }
@@ -451,6 +480,8 @@ __global__ void route_scan_kernel(PrefillArgs a) {
 
 // One warp per block of entries: stable ranks by expert in index order.
 __global__ void route_scatter_kernel(PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
   extern __shared__ int s_base[];
   const int lane = threadIdx.x;
   for (int e = lane; e < a.E; e += 32) s_base[e] = a.block_base[(size_t)blockIdx.x * a.E + e];
@@ -479,6 +510,8 @@ __global__ void route_scatter_kernel(PrefillArgs a) {
 // One warp per token: NVFP4 row of x into every routed row of the token;
 // also zeroes the token's FP32 accumulator row.
 __global__ void quant_x_kernel(PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
   const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (t >= a.M) return;
   const int lane = threadIdx.x & 31;
@@ -505,6 +538,8 @@ __global__ void quant_x_kernel(PrefillArgs a) {
 // One warp per routed row: NVFP4 row of h (BF16) for FC2; padding rows get
 // zero codes, zero scales and G = 0.
 __global__ void quant_h_kernel(PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
   const int r = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (r >= 128 * *a.num_tiles) return;
   const int lane = threadIdx.x & 31;
@@ -541,6 +576,8 @@ template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     fc1_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                     PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
   // non-gated experts (squared ReLU): N tiles of 128 w1 rows, the expert's
   // last one padded (its scale rows past I are zero); gated: 2I rows
   const bool relu2 = a.act.kind == MOE_FP4_ACT_RELU2;
@@ -628,6 +665,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 __global__ void __launch_bounds__(kGemmThreads, 1)
     fc2_gemm_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
                     PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
   const int NT = a.H / kFc2BN;
   const int KG = a.I / 64;
   const size_t scb = scale_chunk_bytes(a.H, a.I);
@@ -771,6 +810,8 @@ __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
 // token's FP32 accumulator row.  The MXFP8 image never exceeds max |x| by
 // more than 2^-4 of it (E4M3 rounds to nearest), so the FP16 range holds.
 __global__ void stage_x_f16_kernel(PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
   const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (t >= a.M) return;
   const int lane = threadIdx.x & 31;
@@ -826,6 +867,8 @@ __global__ void stage_x_f16_kernel(PrefillArgs a) {
 // One warp per live routed row: h (BF16, written by FC1) rescaled by the
 // row's power of two and converted to FP16 in place, 2^-s in hG.
 __global__ void stage_h_f16_kernel(PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
   const int r = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (r >= 128 * *a.num_tiles || a.row_src[r] < 0) return;
   const int lane = threadIdx.x & 31;
@@ -860,6 +903,8 @@ template <int BN>
 __global__ void __launch_bounds__(kHwThreads, 1)
     fc1_exact_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                      PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
   const bool relu2 = a.act.kind == MOE_FP4_ACT_RELU2;
   const int NT = relu2 ? (a.I + 127) / 128 : 2 * a.I / BN;
   const int KG = a.H / 64;
@@ -947,6 +992,8 @@ __global__ void __launch_bounds__(kHwThreads, 1)
 __global__ void __launch_bounds__(kHwThreads, 1)
     fc2_exact_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
                      PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
   constexpr int BN = 256;
   const int NT = a.H / BN;
   const int KG = a.I / 64;
@@ -1008,6 +1055,8 @@ __device__ __forceinline__ size_t mx_sf_offset(int row, int b, int nst) {
 // One warp per token: x quantised to MXFP8 (one 32-block per lane and
 // round) into every routed row of the token; zeroes the token's accumulator.
 __global__ void quant_x_mx_kernel(PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
   const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (t >= a.M) return;
   const int lane = threadIdx.x & 31;
@@ -1069,6 +1118,8 @@ template <int BN>
 __global__ void __launch_bounds__(kMxThreads, 1)
     fc1_mx_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                   PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
   const int NT = 2 * a.I / BN;
   const int KG = a.H / 64, nst = a.H / 128, nsth = a.I / 128;
   const size_t scb = scale_chunk_bytes(2 * a.I, a.H);
@@ -1127,6 +1178,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 __global__ void __launch_bounds__(kMxThreads, 1)
     fc2_mx_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
                   PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
   constexpr int BN = 256;
   const int NT = a.H / BN;
   const int KG = a.I / 64, nst = a.I / 128;
@@ -1174,6 +1227,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 }
 
 __global__ void cast_out_kernel(PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
   const size_t n8 = (size_t)a.M * a.H / 8;
   for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n8; v += (size_t)gridDim.x * blockDim.x) {
     const float4 p = reinterpret_cast<const float4*>(a.acc)[2 * v];
@@ -1320,10 +1375,10 @@ PrefillArgs prefill_args(const PrefillCarve& c, void* ws, int M, int E, int H, i
 }
 
 cudaError_t launch_route(PrefillArgs& a, cudaStream_t st) {
-  route_count_kernel<<<a.n_route_blocks, kRouteBlock, sizeof(int) * a.E, st>>>(a);
-  route_scan_kernel<<<1, 1024, 0, st>>>(a);
-  route_scatter_kernel<<<a.n_route_blocks, 32, sizeof(int) * a.E, st>>>(a);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(route_count_kernel, (unsigned)a.n_route_blocks, kRouteBlock, sizeof(int) * a.E, st, a);
+  if (e == cudaSuccess) e = launch_pdl(route_scan_kernel, 1u, 1024u, 0, st, a);
+  if (e == cudaSuccess) e = launch_pdl(route_scatter_kernel, (unsigned)a.n_route_blocks, 32u, sizeof(int) * a.E, st, a);
+  return e;
 }
 
 }  // namespace
@@ -1384,20 +1439,21 @@ static cudaError_t launch_prefill_exact(PrefillArgs& a, const PrefillCarve& c, c
   }
   cudaError_t e = launch_route(a, st);
   if (e != cudaSuccess) return e;
-  stage_x_f16_kernel<<<(a.M + 7) / 8, 256, 0, st>>>(a);
+  e = launch_pdl(stage_x_f16_kernel, (unsigned)((a.M + 7) / 8), 256u, 0, st, a);
+  if (e != cudaSuccess) return e;
   int sms = 0;
   e = gemm_sms(&sms);
   if (e != cudaSuccess) return e;
   const int g1 = c.max_tiles * nt1, g2 = c.max_tiles * nt2;
   const int p1 = g1 < sms ? g1 : sms, p2 = g2 < sms ? g2 : sms;
   if (bn1 == 256)
-    fc1_exact_kernel<256><<<p1, kHwThreads, HwCfg<256>::kSmem, st>>>(mx, mw13, a);
+    e = launch_pdl(fc1_exact_kernel<256>, (unsigned)p1, kHwThreads, HwCfg<256>::kSmem, st, mx, mw13, a);
   else
-    fc1_exact_kernel<128><<<p1, kHwThreads, HwCfg<128>::kSmem, st>>>(mx, mw13, a);
-  stage_h_f16_kernel<<<(unsigned)(rows / 8), 256, 0, st>>>(a);
-  fc2_exact_kernel<<<p2, kHwThreads, HwCfg<256>::kSmem, st>>>(mh, mw2, a);
-  cast_out_kernel<<<4 * 152, 256, 0, st>>>(a);
-  return cudaGetLastError();
+    e = launch_pdl(fc1_exact_kernel<128>, (unsigned)p1, kHwThreads, HwCfg<128>::kSmem, st, mx, mw13, a);
+  if (e == cudaSuccess) e = launch_pdl(stage_h_f16_kernel, (unsigned)(rows / 8), 256u, 0, st, a);
+  if (e == cudaSuccess) e = launch_pdl(fc2_exact_kernel, (unsigned)p2, kHwThreads, HwCfg<256>::kSmem, st, mh, mw2, a);
+  if (e == cudaSuccess) e = launch_pdl(cast_out_kernel, 4u * 152u, 256u, 0, st, a);
+  return e;
 }
 
 // The W4A8-MX band on the FP8 tensor cores: route, x to MXFP8 per routed row,
@@ -1434,15 +1490,17 @@ static cudaError_t launch_prefill_mx(PrefillArgs& a, const PrefillCarve& c, cons
   }
   cudaError_t e = launch_route(a, st);
   if (e != cudaSuccess) return e;
-  quant_x_mx_kernel<<<(a.M + 7) / 8, 256, 0, st>>>(a);
+  e = launch_pdl(quant_x_mx_kernel, (unsigned)((a.M + 7) / 8), 256u, 0, st, a);
+  if (e != cudaSuccess) return e;
   int sms = 0;
   e = gemm_sms(&sms);
   if (e != cudaSuccess) return e;
   const int g1 = c.max_tiles * (2 * I / bn1), g2 = c.max_tiles * (H / 256);
-  fc1_mx_kernel<bn1><<<g1 < sms ? g1 : sms, kMxThreads, MxCfg<bn1>::kSmem, st>>>(mx, mw13, a);
-  fc2_mx_kernel<<<g2 < sms ? g2 : sms, kMxThreads, MxCfg<256>::kSmem, st>>>(mh, mw2, a);
-  cast_out_kernel<<<4 * 152, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  e = launch_pdl(fc1_mx_kernel<bn1>, (unsigned)(g1 < sms ? g1 : sms), kMxThreads, MxCfg<bn1>::kSmem, st, mx, mw13, a);
+  if (e == cudaSuccess)
+    e = launch_pdl(fc2_mx_kernel, (unsigned)(g2 < sms ? g2 : sms), kMxThreads, MxCfg<256>::kSmem, st, mh, mw2, a);
+  if (e == cudaSuccess) e = launch_pdl(cast_out_kernel, 4u * 152u, 256u, 0, st, a);
+  return e;
 }
 
 cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
@@ -1496,17 +1554,21 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
   }
   cudaError_t e = launch_route(a, st);
   if (e != cudaSuccess) return e;
-  quant_x_kernel<<<(M + 7) / 8, 256, 0, st>>>(a);
+  e = launch_pdl(quant_x_kernel, (unsigned)((M + 7) / 8), 256u, 0, st, a);
+  if (e != cudaSuccess) return e;
   int sms = 0;
   cudaError_t es = gemm_sms(&sms);
   if (es != cudaSuccess) return es;
   // persistent: one CTA per SM (the valid tile count is known on the device)
   const int g1 = c.max_tiles * (relu2 ? (I + 127) / 128 : 2 * I / bn1), g2 = c.max_tiles * (H / kFc2BN);
-  fc1_gemm_kernel<bn1><<<g1 < sms ? g1 : sms, kGemmThreads, GemmCfg<bn1>::kSmem, st>>>(mx, mw13, a);
-  quant_h_kernel<<<(int)((rows + 7) / 8), 256, 0, st>>>(a);
-  fc2_gemm_kernel<<<g2 < sms ? g2 : sms, kGemmThreads, GemmCfg<kFc2BN>::kSmem, st>>>(mh, mw2, a);
-  cast_out_kernel<<<4 * 152, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  e = launch_pdl(fc1_gemm_kernel<bn1>, (unsigned)(g1 < sms ? g1 : sms), kGemmThreads, GemmCfg<bn1>::kSmem, st, mx,
+                 mw13, a);
+  if (e == cudaSuccess) e = launch_pdl(quant_h_kernel, (unsigned)((rows + 7) / 8), 256u, 0, st, a);
+  if (e == cudaSuccess)
+    e = launch_pdl(fc2_gemm_kernel, (unsigned)(g2 < sms ? g2 : sms), kGemmThreads, GemmCfg<kFc2BN>::kSmem, st, mh,
+                   mw2, a);
+  if (e == cudaSuccess) e = launch_pdl(cast_out_kernel, 4u * 152u, 256u, 0, st, a);
+  return e;
 }
 
 size_t debug_route_workspace_bytes(int M, int E, int top_k) { return prefill_carve(M, E, 256, 256, top_k).total; }
