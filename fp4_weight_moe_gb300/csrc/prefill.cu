@@ -605,6 +605,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int r = t.a_row0 + row;
     const int e = a.tile_expert[t.m_tile];
     const bool live = a.row_src[r] >= 0;
+    if (!__any_sync(0xffffffffu, live)) return;  // no live row among this warp's 32: nothing to read out
     const float xg = live ? a.xG[r] : 0.f;
     if (relu2) {
       // h = max(u, 0)^2 in BF16 for the tile's rows of w1 below I (BN = 128)
@@ -691,6 +692,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int r = t.a_row0 + row;
     const int e = a.tile_expert[t.m_tile];
     const int src = a.row_src[r];
+    if (!__any_sync(0xffffffffu, src >= 0)) return;  // no live row among this warp's 32: nothing to add
     const float f = src >= 0 ? a.hG[r] * g2[e] * a.tw[src] : 0.f;
     float* dst = a.acc + (size_t)(src >= 0 ? src / a.top_k : 0) * a.H + kFc2BN * t.n_tile;
 #pragma unroll 1
@@ -929,6 +931,7 @@ __global__ void __launch_bounds__(kHwThreads, 1)
     const int r = t.a_row0 + row;
     const int e = a.tile_expert[t.m_tile];
     const bool live = a.row_src[r] >= 0;
+    if (!__any_sync(0xffffffffu, live)) return;  // no live row among this warp's 32: nothing to read out
     const float xs = live ? a.xG[r] : 0.f;  // the row's 2^-s
     __nv_bfloat16* hrow = a.hbuf + (size_t)r * a.I;
     if (relu2) {
@@ -1018,6 +1021,7 @@ __global__ void __launch_bounds__(kHwThreads, 1)
     const int r = t.a_row0 + row;
     const int e = a.tile_expert[t.m_tile];
     const int src = a.row_src[r];
+    if (!__any_sync(0xffffffffu, src >= 0)) return;  // no live row among this warp's 32: nothing to add
     const float f = src >= 0 ? g2[e] * a.tw[src] * a.hG[r] : 0.f;
     float* dst = a.acc + (size_t)(src >= 0 ? src / a.top_k : 0) * a.H + BN * t.n_tile;
 #pragma unroll 1
@@ -1144,6 +1148,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const int r = t.a_row0 + row;
     const int e = a.tile_expert[t.m_tile];
     const bool live = a.row_src[r] >= 0;
+    if (!__any_sync(0xffffffffu, live)) return;  // no live row among this warp's 32: nothing to read out
     const float sgate = g13[2 * e], sup = g13[2 * e + 1];
 #pragma unroll 1
     for (int q = 0; q < BN / 128; ++q) {  // the 128-row resident tiles of this N tile
@@ -1205,6 +1210,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const int r = t.a_row0 + row;
     const int e = a.tile_expert[t.m_tile];
     const int src = a.row_src[r];
+    if (!__any_sync(0xffffffffu, src >= 0)) return;  // no live row among this warp's 32: nothing to add
     const float f = src >= 0 ? g2[e] * a.tw[src] : 0.f;
     float* dst = a.acc + (size_t)(src >= 0 ? src / a.top_k : 0) * a.H + BN * t.n_tile;
 #pragma unroll 1
