@@ -82,3 +82,31 @@ def test_bf16_half_ulp_bounds_the_bf16_rounding():
     rm = torch.tensor(mid, dtype=torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
     assert np.allclose(np.abs(rm - mid), bf16_half_ulp(mid), rtol=0, atol=0)
     assert bf16_half_ulp(np.array([0.0]))[0] == 0.0
+
+
+def _prefill_res(mode=None, engine=None, us=1000.0):
+    c = dict(gen.CONFIGS["prefill_e128"])
+    ids = [torch.tensor([[0, 1], [2, 3]], dtype=torch.int32)]
+    res = {"us_per_layer": us, "prefill": True, "plan": "p", "layers_per_replay": 1,
+           "flops_per_layer": 1e12, "_state": (c, 0, ids, None, None)}
+    if mode:
+        res["prefill_mode"] = mode
+    if engine:
+        res["engine"] = engine
+    return res
+
+
+def test_prefill_roofline_peaks_follow_the_tensor_core_kind(monkeypatch):
+    """The NVFP4 band is judged against the FP4 peak (measured BF16 x 6), the
+    exact mode against the BF16 peak, the W4A8-MX FP8 engine against the FP8
+    peak (measured BF16 x 2); each above its ridge reports TFLOP/s."""
+    monkeypatch.setattr(bench, "load_bf16_peak", lambda: (1000.0, "measured"))
+    hbm = 1e9  # so high that every case sits above the ridge: the tensor bound
+    r = bench.roofline_of(_prefill_res(), hbm, "measured", None)
+    assert r["bound"] == "tensor" and r["peak"] == 6000.0 and abs(r["achieved"] - 1000.0) < 1e-6
+    r = bench.roofline_of(_prefill_res("bf16-exact", "16-bit"), hbm, "measured", None)
+    assert r["peak"] == 1000.0 and abs(r["frac"] - 1.0) < 1e-9
+    r = bench.roofline_of(_prefill_res("w4a8-mx", "fp8"), hbm, "measured", None)
+    assert r["peak"] == 2000.0 and "x 2" in r["peak_source"]
+    r = bench.roofline_of(_prefill_res("w4a8-mx", "16-bit"), hbm, "measured", None)
+    assert r["peak"] == 1000.0
