@@ -251,18 +251,22 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ GPU arm
-def decode_src_sha256():
-    """Hash of the decode kernels' code: a stored ncu traffic figure is used
-    only while the kernels it was measured on are unchanged.  Line comments
-    and blank lines are left out (they do not change the kernels)."""
+def _src_sha256(files):
     import hashlib
     import re
     h = hashlib.sha256()
-    for f in ("common.cuh", "tcgen05.cuh", "decode_tc.cu", "decode.cu"):
+    for f in files:
         text = open(os.path.join(ROOT, "fp4_weight_moe_gb300", "csrc", f)).read()
         code = [re.sub(r"\s*//.*$", "", ln).rstrip() for ln in text.splitlines()]
         h.update("\n".join(ln for ln in code if ln).encode())
     return h.hexdigest()
+
+
+def decode_src_sha256():
+    """Hash of the decode kernels' code: a stored ncu traffic figure is used
+    only while the kernels it was measured on are unchanged.  Line comments
+    and blank lines are left out (they do not change the kernels)."""
+    return _src_sha256(("common.cuh", "tcgen05.cuh", "decode_tc.cu", "decode.cu"))
 
 
 def decode_kernel_label(m, M, E, H, I, k):
@@ -547,15 +551,26 @@ def roofline_of(res, peak, peak_kind, traffic):
                             f"bf16_tflops of {bf16_kind} x 6 (nominal fp4/bf16)"}}
 
 
-def stored_traffic(args_workload, M, fmt_name, E_override):
-    prof = os.path.join(ROOT, "profiles", "decode_e512_traffic.json")
+def prefill_src_sha256():
+    """Hash of the prefill kernels' code (line comments and blank lines left
+    out), the key of the stored prefill traffic figures."""
+    return _src_sha256(("common.cuh", "tcgen05.cuh", "gemm_fp4.cuh", "gemm_f16w4.cuh", "gemm_mxf8.cuh", "prefill.cu"))
+
+
+def stored_traffic(args_workload, M, fmt_name, E_override, prefill_mode=None):
+    """Per-layer DRAM bytes from a stored ncu capture of this workload, or None
+    when there is none or the kernels changed since (decode and prefill keep
+    separate files keyed on their sources' code)."""
+    name, key_src = (("prefill_e128_traffic.json", prefill_src_sha256) if prefill_mode is not None else
+                     ("decode_e512_traffic.json", decode_src_sha256))
+    prof = os.path.join(ROOT, "profiles", name)
     if E_override is not None or not os.path.exists(prof):
         return None
     try:
         with open(prof) as f:
             pd = json.load(f)
-        key = f"{args_workload}/M={M}/{fmt_name}"
-        if pd.get("decode_src_sha256") == decode_src_sha256() and key in pd.get("configs", {}):
+        key = f"{args_workload}/M={M}/{fmt_name}" + (f"/{prefill_mode}" if prefill_mode is not None else "")
+        if pd.get("src_sha256", pd.get("decode_src_sha256")) == key_src() and key in pd.get("configs", {}):
             return pd["configs"][key]["dram_bytes_per_layer"]
     except Exception:
         return None
@@ -601,7 +616,8 @@ def run_ours(args):
     else:
         prefill = head["prefill"]
         head["_state"] = (c, seed, ids_pool, w_pool, x)
-        traffic = None if prefill else stored_traffic(args.workload, M, gen.FMT_NAMES[fmt], args.E)
+        traffic = stored_traffic(args.workload, M, gen.FMT_NAMES[fmt], args.E,
+                                 head.get("prefill_mode", "nvfp4") if prefill else None)
         rl = roofline_of(head, peak, peak_kind, traffic)
         head.pop("_state")
         line.update({"value": head["job_units"] / (head["ms_per_replay"] * 1e-3) / (1e12 if prefill else 1e9),
@@ -644,7 +660,8 @@ def run_ours(args):
                 continue
             ent = {"config": label}
             if r["timed"]:
-                r["roofline"] = roofline_of(r, peak, peak_kind, None)
+                tr = stored_traffic(name, r["M"], r["fmt"], None, r.get("prefill_mode", "nvfp4") if r["prefill"] else None)
+                r["roofline"] = roofline_of(r, peak, peak_kind, tr)
             r.pop("_state", None)
             r.pop("job_units", None)
             ent.update(r)

@@ -110,3 +110,23 @@ def test_prefill_roofline_peaks_follow_the_tensor_core_kind(monkeypatch):
     assert r["peak"] == 2000.0 and "x 2" in r["peak_source"]
     r = bench.roofline_of(_prefill_res("w4a8-mx", "16-bit"), hbm, "measured", None)
     assert r["peak"] == 1000.0
+
+
+def test_stored_prefill_traffic_file_shape_and_lookup():
+    with open(os.path.join(ROOT, "profiles", "prefill_e128_traffic.json")) as f:
+        d = json.load(f)
+    assert len(d["src_sha256"]) == 64
+    for key, c in d["configs"].items():
+        workload, m, fmt, mode = key.split("/")
+        assert workload in gen.CONFIGS and m.startswith("M=") and fmt in gen.FMT_NAMES.values()
+        assert mode in ("nvfp4", "bf16-exact", "w4a8-mx")
+        assert c["dram_bytes_per_layer"] == sum(c["kernels_per_layer"].values())
+        assert c["algorithmic_bytes_per_layer"] > 0 and "ncu" in c["command"]
+        assert "--clock-control none" in c["command"]
+    # the bench finds a figure exactly while the prefill sources hash to the stored key
+    got = bench.stored_traffic("prefill_e128", 4096, "nvfp4", None, "nvfp4")
+    if d["src_sha256"] == bench.prefill_src_sha256():
+        assert got == d["configs"]["prefill_e128/M=4096/nvfp4/nvfp4"]["dram_bytes_per_layer"]
+    else:
+        assert got is None
+    assert bench.stored_traffic("prefill_e128", 4096, "nvfp4", 32, "nvfp4") is None  # another E: no figure
