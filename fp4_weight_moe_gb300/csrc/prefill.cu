@@ -507,6 +507,24 @@ __global__ void route_scatter_kernel(PrefillArgs a) {
 }
 
 // ---------------------------------------------------------------- quantisers
+// Largest magnitude over the 128 threads of a block (every thread gets it).
+__device__ __forceinline__ float block128_max(float v, float* red4) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) red4[threadIdx.x >> 5] = v;
+  __syncthreads();
+  return fmaxf(fmaxf(red4[0], red4[1]), fmaxf(red4[2], red4[3]));
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&v)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
 // One warp per token: NVFP4 row of x into every routed row of the token;
 // also zeroes the token's FP32 accumulator row.
 __global__ void quant_x_kernel(PrefillArgs a) {
@@ -605,7 +623,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int r = t.a_row0 + row;
     const int e = a.tile_expert[t.m_tile];
     const bool live = a.row_src[r] >= 0;
-    if (!__any_sync(0xffffffffu, live)) return;  // no live row among this warp's 32: nothing to read out
     const float xg = live ? a.xG[r] : 0.f;
     if (relu2) {
       // h = max(u, 0)^2 in BF16 for the tile's rows of w1 below I (BN = 128)
@@ -692,7 +709,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int r = t.a_row0 + row;
     const int e = a.tile_expert[t.m_tile];
     const int src = a.row_src[r];
-    if (!__any_sync(0xffffffffu, src >= 0)) return;  // no live row among this warp's 32: nothing to add
     const float f = src >= 0 ? a.hG[r] * g2[e] * a.tw[src] : 0.f;
     float* dst = a.acc + (size_t)(src >= 0 ? src / a.top_k : 0) * a.H + kFc2BN * t.n_tile;
 #pragma unroll 1
@@ -777,6 +793,25 @@ __device__ __forceinline__ void mxfp8_qdq32(float (&v)[32]) {
   }
 }
 
+// Eight values of an MXFP8 block whose largest magnitude is amax, quantised
+// and dequantised in place (the same exponent and per-element rounding as
+// mxfp8_qdq32, for a block spread over four threads).
+__device__ __forceinline__ void mxfp8_qdq8(float (&v)[8], float amax) {
+  const int e = mxfp8_scale_exponent(amax);
+  const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
+  const float sc = e > -127 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint16_t c;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(v[2 * j + 1] * inv), "f"(v[2 * j] * inv));
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+    const float2 f = half2_bits_to_float2(h2);
+    v[2 * j] = f.x * sc;
+    v[2 * j + 1] = f.y * sc;
+  }
+}
+
 // ---------------------------------------------------------------- exact numerics
 // The prefill band without NVFP4 activations, on the FP16 tensor cores: x in
 // BF16 (or its MXFP8 image, W4A8-MX) against the FP4 weights decoded to FP16
@@ -805,65 +840,58 @@ __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
   return r;
 }
 
-// One warp per token: x's BF16 row (amode 0), or its MXFP8 image (amode 1:
-// quantised per 32-element block, then dequantised), scaled by the row's
-// power of two and stored in FP16 into every routed row of the token (the
-// GEMM's A tiles are rows of routed rows), with 2^-s in xG; also zeroes the
-// token's FP32 accumulator row.  The MXFP8 image never exceeds max |x| by
-// more than 2^-4 of it (E4M3 rounds to nearest), so the FP16 range holds.
-__global__ void stage_x_f16_kernel(PrefillArgs a) {
+// One block of 128 threads per token: x's BF16 row (amode 0), or its MXFP8
+// image (amode 1: quantised per 32-element block, then dequantised), scaled
+// by the row's power of two and stored in FP16 into every routed row of the
+// token (the GEMM's A tiles are rows of routed rows), with 2^-s in xG; also
+// zeroes the token's FP32 accumulator row.  Thread t takes the 8-element
+// chunks t, t + 128, ...; the four threads of a 32-element block are
+// neighbouring lanes.  The MXFP8 image never exceeds max |x| by more than
+// 2^-4 of it (E4M3 rounds to nearest), so the FP16 range holds.
+__global__ void __launch_bounds__(128) stage_x_f16_kernel(PrefillArgs a) {
   pdl_wait();               // the previous kernel on the stream is complete and visible
   pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
-  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-  if (t >= a.M) return;
-  const int lane = threadIdx.x & 31;
-  const int H = a.H, k = a.top_k;
+  __shared__ float red4[4];
+  const int t = blockIdx.x;
+  const int H = a.H, k = a.top_k, nc = H / 8;
   const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * H);
   const int* prow = a.pos + (size_t)t * k;
   float amax = 0.f;
-  for (int v = lane; v < H / 8; v += 32) {
-    const uint4 u = __ldg(xr + v);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  for (int c = threadIdx.x; c < nc; c += 128) {
+    float v[8];
+    bf16x8_to_f32(__ldg(xr + c), v);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  amax = block128_max(amax, red4);
   const int sft = f16_row_shift(amax);
   const float up = pow2f(sft);
-  if (lane < k) {
-    const int r = prow[lane];
+  if (threadIdx.x < k) {
+    const int r = prow[threadIdx.x];
     if (r >= 0) a.xG[r] = pow2f(-sft);
   }
-  for (int b = lane; b < H / 32; b += 32) {  // one 32-element block per lane
-    float v[32];
+  int rows[16];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 u = __ldg(xr + 4 * b + q);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  for (int j = 0; j < 16; ++j) rows[j] = j < k ? prow[j] : -1;
+  for (int c = threadIdx.x; c < nc; c += 128) {  // (nc % 32 == 0: a warp's lanes stay converged)
+    float v[8];
+    bf16x8_to_f32(__ldg(xr + c), v);
+    if (a.amode) {
+      float bm = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
-        v[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-      }
+      for (int i = 0; i < 8; ++i) bm = fmaxf(bm, fabsf(v[i]));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+      mxfp8_qdq8(v, bm);
     }
-    if (a.amode) mxfp8_qdq32(v);
-    uint4 o[4];
+    const uint4 o = make_uint4(f16x2_of(v[0] * up, v[1] * up), f16x2_of(v[2] * up, v[3] * up),
+                               f16x2_of(v[4] * up, v[5] * up), f16x2_of(v[6] * up, v[7] * up));
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      o[q] = make_uint4(f16x2_of(v[8 * q] * up, v[8 * q + 1] * up), f16x2_of(v[8 * q + 2] * up, v[8 * q + 3] * up),
-                        f16x2_of(v[8 * q + 4] * up, v[8 * q + 5] * up), f16x2_of(v[8 * q + 6] * up, v[8 * q + 7] * up));
-    for (int j = 0; j < k; ++j) {
-      const int r = prow[j];
-      if (r < 0) continue;
-      uint4* dst = reinterpret_cast<uint4*>(a.xb + (size_t)r * H) + 4 * b;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) dst[q] = o[q];
-    }
+    for (int j = 0; j < 16; ++j)
+      if (rows[j] >= 0) reinterpret_cast<uint4*>(a.xb + (size_t)rows[j] * H)[c] = o;
   }
   float4* accr = reinterpret_cast<float4*>(a.acc + (size_t)t * H);
-  for (int v = lane; v < H / 4; v += 32) accr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int v = threadIdx.x; v < H / 4; v += 128) accr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // One warp per live routed row: h (BF16, written by FC1) rescaled by the
@@ -931,7 +959,6 @@ __global__ void __launch_bounds__(kHwThreads, 1)
     const int r = t.a_row0 + row;
     const int e = a.tile_expert[t.m_tile];
     const bool live = a.row_src[r] >= 0;
-    if (!__any_sync(0xffffffffu, live)) return;  // no live row among this warp's 32: nothing to read out
     const float xs = live ? a.xG[r] : 0.f;  // the row's 2^-s
     __nv_bfloat16* hrow = a.hbuf + (size_t)r * a.I;
     if (relu2) {
@@ -1021,7 +1048,6 @@ __global__ void __launch_bounds__(kHwThreads, 1)
     const int r = t.a_row0 + row;
     const int e = a.tile_expert[t.m_tile];
     const int src = a.row_src[r];
-    if (!__any_sync(0xffffffffu, src >= 0)) return;  // no live row among this warp's 32: nothing to add
     const float f = src >= 0 ? g2[e] * a.tw[src] * a.hG[r] : 0.f;
     float* dst = a.acc + (size_t)(src >= 0 ? src / a.top_k : 0) * a.H + BN * t.n_tile;
 #pragma unroll 1
@@ -1056,43 +1082,49 @@ __device__ __forceinline__ size_t mx_sf_offset(int row, int b, int nst) {
   return ((size_t)(row >> 7) * nst + (b >> 2)) * kChunkBytes + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (b & 3);
 }
 
-// One warp per token: x quantised to MXFP8 (one 32-block per lane and
-// round) into every routed row of the token; zeroes the token's accumulator.
-__global__ void quant_x_mx_kernel(PrefillArgs a) {
+// One block of 128 threads per token: x quantised to MXFP8 into every
+// routed row of the token, thread t taking the 8-element chunks t, t + 128,
+// ... (the four threads of a 32-element block are neighbouring lanes and
+// share its largest magnitude by shuffles; the first writes the scale byte);
+// zeroes the token's accumulator.  The rule is quant_row_mxfp8's.
+__global__ void __launch_bounds__(128) quant_x_mx_kernel(PrefillArgs a) {
   pdl_wait();               // the previous kernel on the stream is complete and visible
   pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
-  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-  if (t >= a.M) return;
-  const int lane = threadIdx.x & 31;
-  const int H = a.H, k = a.top_k, nst = H / 128;
+  const int t = blockIdx.x;
+  const int H = a.H, k = a.top_k, nst = H / 128, nc = H / 8;
   const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * H);
   const int* prow = a.pos + (size_t)t * k;
-  quant_row_mxfp8(
-      H,
-      [&](int b, float (&v)[32]) {
+  int rows[16];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 u = __ldg(xr + 4 * b + q);
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  for (int j = 0; j < 16; ++j) rows[j] = j < k ? prow[j] : -1;
+  for (int c = threadIdx.x; c < nc; c += 128) {  // (nc % 32 == 0: a warp's lanes stay converged)
+    float v[8];
+    bf16x8_to_f32(__ldg(xr + c), v);
+    float bm = 0.f;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            v[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
-            v[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-          }
-        }
-      },
-      [&](int b, uint32_t sb, const uint32_t (&w)[8]) {
-        for (int j = 0; j < k; ++j) {
-          const int r = prow[j];
-          if (r < 0) continue;
-          uint4* dst = reinterpret_cast<uint4*>(a.xq8 + (size_t)r * H + 32 * b);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          a.xsf8[mx_sf_offset(r, b, nst)] = (uint8_t)sb;
-        }
-      });
+    for (int i = 0; i < 8; ++i) bm = fmaxf(bm, fabsf(v[i]));
+    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+    const int e = mxfp8_scale_exponent(bm);
+    const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e (e <= 120 for finite FP32)
+    uint32_t w[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {  // (the second source lands in the low byte)
+      uint16_t lo, hi;
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(v[4 * j + 1] * inv), "f"(v[4 * j] * inv));
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(v[4 * j + 3] * inv), "f"(v[4 * j + 2] * inv));
+      w[j] = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int r = rows[j];
+      if (r < 0) continue;
+      reinterpret_cast<uint2*>(a.xq8 + (size_t)r * H)[c] = make_uint2(w[0], w[1]);
+      if ((c & 3) == 0) a.xsf8[mx_sf_offset(r, c >> 2, nst)] = (uint8_t)(e + 127);
+    }
+  }
   float4* accr = reinterpret_cast<float4*>(a.acc + (size_t)t * H);
-  for (int v = lane; v < H / 4; v += 32) accr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int v = threadIdx.x; v < H / 4; v += 128) accr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // One MXFP8 block of 32 values (this thread's): E4M3 codes as 8 words
@@ -1148,7 +1180,6 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const int r = t.a_row0 + row;
     const int e = a.tile_expert[t.m_tile];
     const bool live = a.row_src[r] >= 0;
-    if (!__any_sync(0xffffffffu, live)) return;  // no live row among this warp's 32: nothing to read out
     const float sgate = g13[2 * e], sup = g13[2 * e + 1];
 #pragma unroll 1
     for (int q = 0; q < BN / 128; ++q) {  // the 128-row resident tiles of this N tile
@@ -1210,7 +1241,6 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const int r = t.a_row0 + row;
     const int e = a.tile_expert[t.m_tile];
     const int src = a.row_src[r];
-    if (!__any_sync(0xffffffffu, src >= 0)) return;  // no live row among this warp's 32: nothing to add
     const float f = src >= 0 ? g2[e] * a.tw[src] : 0.f;
     float* dst = a.acc + (size_t)(src >= 0 ? src / a.top_k : 0) * a.H + BN * t.n_tile;
 #pragma unroll 1
@@ -1445,7 +1475,7 @@ static cudaError_t launch_prefill_exact(PrefillArgs& a, const PrefillCarve& c, c
   }
   cudaError_t e = launch_route(a, st);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(stage_x_f16_kernel, (unsigned)((a.M + 7) / 8), 256u, 0, st, a);
+  e = launch_pdl(stage_x_f16_kernel, (unsigned)a.M, 128u, 0, st, a);
   if (e != cudaSuccess) return e;
   int sms = 0;
   e = gemm_sms(&sms);
@@ -1496,7 +1526,7 @@ static cudaError_t launch_prefill_mx(PrefillArgs& a, const PrefillCarve& c, cons
   }
   cudaError_t e = launch_route(a, st);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(quant_x_mx_kernel, (unsigned)((a.M + 7) / 8), 256u, 0, st, a);
+  e = launch_pdl(quant_x_mx_kernel, (unsigned)a.M, 128u, 0, st, a);
   if (e != cudaSuccess) return e;
   int sms = 0;
   e = gemm_sms(&sms);
