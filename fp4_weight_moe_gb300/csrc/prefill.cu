@@ -1,5 +1,16 @@
-// Prefill band building blocks: the tcgen05 block-scaled FP4 GEMM and its
-// test-support entry point.
+// The prefill bands (batches past the decode band): routing compaction
+// (count, scan, stable scatter into 128-row tiles per expert), then one of
+// three launch chains over the same routed rows and FP32 token accumulator:
+//   NVFP4 activations  x and h quantised to NVFP4, both GEMMs on the FP4
+//                      tensor cores (gemm_fp4.cuh, kind::mxf4nvf4);
+//   exact BF16         x and h carried exactly in row-scaled FP16, the FP4
+//                      weights decoded to FP16 in shared memory (gemm_f16w4.cuh);
+//   W4A8-MX            x and h quantised to MXFP8, both GEMMs on the FP8 tensor
+//                      cores with the MXFP4 weights as stored (gemm_mxf8.cuh,
+//                      kind::mxf8f6f4) where I % 128 == 0, else the 16-bit chain;
+// and the test-support entry points (GEMM, routing, quantisers).  Every
+// kernel of a chain is launched with programmatic dependent launch and waits
+// for its predecessor before it touches global memory.
 #include <mutex>
 
 #include "gemm_f16w4.cuh"
