@@ -36,6 +36,7 @@ WORKLOAD = "decode_e512"
 WINDOW = 20
 # decode-band kernel plans of moe_fp4_debug_set_decode_family
 DECODE_PLANS = {"auto": 0, "gemv": 1, "chain": 2, "single": 3}
+MID_BANDS = {"auto": 0, "prefill": 1, "chunks": 2, "mid": 3}
 
 
 def parse():
@@ -59,6 +60,9 @@ def parse():
                          "activations, MXFP4 weights)")
     ap.add_argument("--decode-plan", choices=list(DECODE_PLANS), default="auto",
                     help="decode-band kernel plan (auto: by shape)")
+    ap.add_argument("--mid-band", choices=list(MID_BANDS), default="auto",
+                    help="kernels of batches past 8 tokens (auto: by shape; prefill: the prefill band's GEMMs; "
+                         "chunks: decode kernels on chunks of 8; mid: the mid band's swapped GEMMs)")
     return ap.parse_args()
 
 
@@ -592,6 +596,7 @@ def run_ours(args):
     from workload import gen
     b.build()
     m._capi.moe_fp4_debug_set_decode_family(DECODE_PLANS[args.decode_plan])
+    m._capi.moe_fp4_debug_set_mid_band(MID_BANDS[args.mid_band])
     threads = affinity_cores()
     K, W = args.steps, args.warmup
     sampler = ClockSampler(local)

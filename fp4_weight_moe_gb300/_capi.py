@@ -77,6 +77,7 @@ SIGNATURES = {
     "moe_fp4_debug_set_mid_band": (_I, [_I, ctypes.POINTER(ctypes.c_int)]),
     "moe_fp4_debug_decode_gemv_fits": (_I, [_I, _I, _I, _I, _I]),
     "moe_fp4_debug_decode_launches": (_I, [_I, _I, _I, _I, _I]),
+    "moe_fp4_debug_mid_band_of": (_I, [_I, _I, _I, _I, _I]),
     "moe_fp4_debug_decode_family_of": (_I, [_I, _I, _I, _I, _I]),
     "moe_fp4_debug_dequant": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "moe_fp4_debug_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
@@ -266,6 +267,12 @@ def moe_fp4_debug_decode_family_of(M, E, H, I, top_k) -> int:
 
 def moe_fp4_debug_decode_launches(M, E, H, I, top_k) -> int:
     return int(_load().moe_fp4_debug_decode_launches(M, E, H, I, top_k))
+
+
+def moe_fp4_debug_mid_band_of(M, E, H, I, top_k) -> int:
+    """1 the prefill band's GEMMs, 2 decode-band chunks, 3 the mid band's
+    GEMMs, 0 for the decode band or invalid shapes."""
+    return int(_load().moe_fp4_debug_mid_band_of(M, E, H, I, top_k))
 
 
 def moe_fp4_debug_dequant(w, s, which, expert, E, H, I, fmt, out, stream):

@@ -26,7 +26,8 @@ int set_w4a8_fp8_engine(int on);
 size_t debug_route_workspace_bytes(int M, int E, int top_k);
 cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                            const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
-                           int top_k, const ActParams& act, int band, void* ws, cudaStream_t st, int* cu_err);
+                           int top_k, const ActParams& act, int band, bool mid, void* ws, cudaStream_t st,
+                           int* cu_err);
 cudaError_t launch_debug_route(const int32_t* ids, int M, int E, int top_k, int32_t* perm, int32_t* expert_offset,
                                void* ws, cudaStream_t st);
 cudaError_t launch_debug_quant(const float* in, int rows, int K, uint8_t* q, uint8_t* s, float* G, cudaStream_t st);
@@ -347,8 +348,9 @@ int moe_fp4_release_workspace(void) {
 }
 
 namespace {
-// Batches past the decode band: 0 by shape, 1 the prefill band, 2 the decode
-// kernels in chunks (test support: moe_fp4_debug_set_mid_band).
+// Batches past the decode band: 0 by shape, 1 the prefill band's GEMMs, 2 the
+// decode kernels in chunks, 3 the mid band's swapped GEMMs (test support:
+// moe_fp4_debug_set_mid_band).
 std::atomic<int> g_mid_band{0};
 constexpr int kMidBandMaxM = 3 * MOE_FP4_DECODE_MAX_M;
 
@@ -367,6 +369,21 @@ bool mid_band_chunks(int M, int H, int I) {
   if (M > kMidBandMaxM) return false;
   if (mode != 0) return mode == 2;
   return M <= 2 * MOE_FP4_DECODE_MAX_M && 3 * (size_t)I * H / 2 <= ((size_t)8 << 20);
+}
+
+// Does a batch past the decode band (and not in chunks) run on the mid band's
+// swapped GEMMs rather than the prefill band's?  By shape: while the experts
+// average at most kMidBandMaxRows routed rows, where the prefill tiles would
+// stage mostly padding rows of activations.  Measured on GB300 (us per layer,
+// prefill / mid band): E=512 H=2560 I=320 k=10: M=24 112.7 / 98.0, 64 183.0
+// / 159.4, 256 236.4 / 213.5; E=288 H=4096 I=512 k=10: M=64 234.4 / 211.4;
+// E=128 H=4096 I=1536 k=8: M=64 270.5 / 268.0, 256 284.1 / 286.7 (16 rows
+// per expert: even), 1024 342.2 / 550.3.
+constexpr int kMidBandMaxRows = 16;
+bool mid_band_swap(int M, int E, int top_k) {
+  const int mode = g_mid_band.load(std::memory_order_relaxed);
+  if (mode == 1 || mode == 3) return mode == 3;
+  return (int64_t)M * top_k <= (int64_t)kMidBandMaxRows * E;  // (mode 2: past the chunks' reach)
 }
 
 // moe_fp4_forward_ex and moe_fp4_forward_ex_i64: topk_ids int32 (ids64 = 0)
@@ -447,7 +464,8 @@ int forward_any_ids(const void* x_bf16, const void* w13, const void* s13, const 
   if (need >= kMaxWorkspace || workspace_bytes < need) return MOE_FP4_EWORKSPACE;
   int cu = 0;
   cudaError_t e = launch_prefill(x_bf16, w13, s13, w2, s2, ids, ids64, topk_weights, out_bf16, M, E, H, I, top_k,
-                                 ap, prefill_mode, workspace, static_cast<cudaStream_t>(stream), &cu);
+                                 ap, prefill_mode, !exact && mid_band_swap(M, E, top_k), workspace,
+                                 static_cast<cudaStream_t>(stream), &cu);
   return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
 }
 }  // namespace
@@ -616,7 +634,7 @@ int moe_fp4_debug_set_decode_family(int family, int* previous) {
 }
 
 int moe_fp4_debug_set_mid_band(int mode, int* previous) {
-  if (mode < 0 || mode > 2) return MOE_FP4_EINVAL;
+  if (mode < 0 || mode > 3) return MOE_FP4_EINVAL;
   const int old = g_mid_band.exchange(mode);
   if (previous) *previous = old;
   return MOE_FP4_OK;
@@ -659,6 +677,12 @@ int moe_fp4_debug_decode_launches(int M, int E, int H, int I, int top_k) {
     m0 += mc;
   }
   return total;
+}
+
+int moe_fp4_debug_mid_band_of(int M, int E, int H, int I, int top_k) {
+  if (M <= MOE_FP4_DECODE_MAX_M || check_shape(E, H, I, top_k, MOE_FP4_NVFP4) != MOE_FP4_OK) return 0;
+  if (mid_band_chunks(M, H, I)) return 2;
+  return mid_band_swap(M, E, top_k) ? 3 : 1;
 }
 
 int moe_fp4_debug_dequant(const void* w, const void* s, int which, int expert, int E, int H, int I, int fmt,

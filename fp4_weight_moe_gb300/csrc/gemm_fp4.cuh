@@ -139,9 +139,13 @@ __device__ __forceinline__ void gemm_fp4_persistent(const CUtensorMap* map_a, co
     if (lane == 0) {
       int g = 0;
       bool ok = true;
+      GemmTile t = tile_of(blockIdx.x);
       for (int idx = blockIdx.x; ok && idx < n_tiles; idx += gridDim.x) {
-        const GemmTile t = tile_of(idx);
         if (!t.valid) break;
+        // the next tile's parameters load while this tile's stages issue
+        GemmTile tn;
+        tn.valid = false;
+        if (idx + (int)gridDim.x < n_tiles) tn = tile_of(idx + (int)gridDim.x);
         for (int s = 0; s < nk; ++s, ++g) {
           const int slot = g % S, round = g / S;
           if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, err, 1u)) {
@@ -157,6 +161,7 @@ __device__ __forceinline__ void gemm_fp4_persistent(const CUtensorMap* map_a, co
           if (BN == 256)
             bulk_load(stage_sfb(slot) + 4 * kChunkBytes, t.b_sf1 + (size_t)(4 * s) * kChunkBytes, sfb, &full[slot]);
         }
+        t = tn;
       }
     }
   } else if (warp == 1) {

@@ -15,6 +15,7 @@
 
 #include "gemm_f16w4.cuh"
 #include "gemm_fp4.cuh"
+#include "gemm_fp4_swap.cuh"
 #include "gemm_mxf8.cuh"
 
 namespace moe_fp4 {
@@ -270,6 +271,7 @@ struct PrefillArgs {
   int* expert_off;  // [E+1]
   int* expert_poff; // [E+1]
   int* tile_expert; // [max_tiles]
+  int* tile_rows;   // [max_tiles] routed rows of each 128-row routing tile (1..128)
   int* num_tiles;   // [1]
   int* pos;         // [n_entries]
   int* row_src;     // [128 * max_tiles]
@@ -379,8 +381,10 @@ __global__ void route_count_kernel(PrefillArgs a) {
   for (int e = threadIdx.x; e < a.E; e += blockDim.x) a.counts[(size_t)blockIdx.x * a.E + e] = s_hist[e];
 }
 
-// One CTA: per-expert totals, unpadded and 128-padded exclusive offsets, the
-// per-block bases of the stable scatter, the tile list and the padding rows.
+// One CTA: per-expert totals, unpadded and P-padded exclusive offsets, the
+// per-block bases of the stable scatter, the list of P-row routing tiles and
+// the padding rows (P = 128: the prefill band; 32: the mid band).
+template <int P>
 __global__ void route_scan_kernel(PrefillArgs a) {
   pdl_wait();               // the previous kernel on the stream is complete and visible
   pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
@@ -412,7 +416,7 @@ __global__ void route_scan_kernel(PrefillArgs a) {
   int su = 0, sp = 0;
   for (int e = e0; e < e1; ++e) {
     su += s_tot[e];
-    sp += (s_tot[e] + 127) & ~127;
+    sp += (s_tot[e] + P - 1) & ~(P - 1);
   }
   // exclusive block scan of (su, sp): within warps by shuffles, then over
   // the warp totals
@@ -447,23 +451,30 @@ __global__ void route_scan_kernel(PrefillArgs a) {
     if (lane == nw - 1) {
       a.expert_off[E] = wu;
       a.expert_poff[E] = wp;
-      *a.num_tiles = wp / 128;
+      *a.num_tiles = wp / P;
     }
   }
   __syncthreads();
   int ru = iu - su + (warp > 0 ? s_part[0][32 + warp - 1] : 0);
   int rp = ip - sp + (warp > 0 ? s_part[1][32 + warp - 1] : 0);
   for (int e = e0; e < e1; ++e) {
-    const int tot = s_tot[e], padded = (tot + 127) & ~127;
+    const int tot = s_tot[e], padded = (tot + P - 1) & ~(P - 1);
     a.expert_off[e] = ru;
     a.expert_poff[e] = rp;
     s_poff[e] = rp;
-    for (int t = 0; t < padded / 128; ++t) a.tile_expert[rp / 128 + t] = e;
-    for (int r = rp + tot; r < rp + padded; ++r) a.row_src[r] = -1;
+    for (int t = 0; t < padded / P; ++t) {
+      a.tile_expert[rp / P + t] = e;
+      a.tile_rows[rp / P + t] = min(P, tot - P * t);
+    }
     ru += tot;
     rp += padded;
   }
   __syncthreads();
+  // padding rows (past the routed rows of each expert's last tile) -> -1,
+  // all threads over all tiles, coalesced
+  const int n_rows = s_part[1][32 + nw - 1];
+  for (int v = threadIdx.x; v < n_rows; v += blockDim.x)
+    if (v % P >= a.tile_rows[v / P]) a.row_src[v] = -1;
   // per-block bases of the stable scatter: the expert's padded offset plus
   // the counts of the earlier blocks (segment sums, then a scan in order)
   for (int base = 0; base < E * tpe; base += blockDim.x) {
@@ -564,6 +575,48 @@ __global__ void quant_x_kernel(PrefillArgs a) {
   for (int v = lane; v < H / 4; v += 32) accr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// Small batches: one warp per routing entry quantises its token's row into
+// the entry's routed row (the same codes as quant_x_kernel, k times the
+// arithmetic for k times the warps); the token's first entry zeroes its FP32
+// accumulator row.
+__global__ void quant_x_entry_kernel(PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
+  const int i = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (i >= a.n_entries) return;
+  const int lane = threadIdx.x & 31;
+  const int H = a.H, KG = H / 64, t = i / a.top_k;
+  const int r = a.pos[i];
+  if (r >= 0) {
+    const __nv_bfloat16* xr = a.x + (size_t)t * H;
+    const float G = quant_row_nvfp4(
+        H, [&](int b, float (&v)[16]) { bf16x16_to_f32(xr + 16 * b, v); },
+        [&](int b, uint32_t sb, uint32_t w0, uint32_t w1) {
+          *reinterpret_cast<uint2*>(a.xq + (size_t)r * (H / 2) + 8 * b) = make_uint2(w0, w1);
+          a.xsf[sf_chunk_offset(r, b, KG)] = (uint8_t)sb;
+        });
+    if (lane == 0) a.xG[r] = G;
+  }
+  if (i % a.top_k == 0) {
+    float4* accr = reinterpret_cast<float4*>(a.acc + (size_t)t * H);
+    for (int v = lane; v < H / 4; v += 32) accr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+// Batches up to this many tokens quantise x per routing entry.
+constexpr int kQuantXEntryMaxM = 256;
+
+// NVFP4 row r of h (BF16) for FC2, by one warp; returns the row's G.
+__device__ __forceinline__ float quant_h_row(const PrefillArgs& a, int r) {
+  const int I = a.I, KG = I / 64;
+  const __nv_bfloat16* hr = a.hbuf + (size_t)r * I;
+  return quant_row_nvfp4(
+      I, [&](int b, float (&v)[16]) { bf16x16_to_f32(hr + 16 * b, v); },
+      [&](int b, uint32_t sb, uint32_t w0, uint32_t w1) {
+        *reinterpret_cast<uint2*>(a.hq + (size_t)r * (I / 2) + 8 * b) = make_uint2(w0, w1);
+        a.hsf[sf_chunk_offset(r, b, KG)] = (uint8_t)sb;
+      });
+}
+
 // One warp per routed row: NVFP4 row of h (BF16) for FC2; padding rows get
 // zero codes, zero scales and G = 0.
 __global__ void quant_h_kernel(PrefillArgs a) {
@@ -581,14 +634,27 @@ __global__ void quant_h_kernel(PrefillArgs a) {
     if (lane == 0) a.hG[r] = 0.f;
     return;
   }
-  const __nv_bfloat16* hr = a.hbuf + (size_t)r * I;
-  const float G = quant_row_nvfp4(
-      I, [&](int b, float (&v)[16]) { bf16x16_to_f32(hr + 16 * b, v); },
-      [&](int b, uint32_t sb, uint32_t w0, uint32_t w1) {
-        *reinterpret_cast<uint2*>(a.hq + (size_t)r * (I / 2) + 8 * b) = make_uint2(w0, w1);
-        a.hsf[sf_chunk_offset(r, b, KG)] = (uint8_t)sb;
-      });
+  const float G = quant_h_row(a, r);
   if (lane == 0) a.hG[r] = G;
+}
+
+// Mid band: one warp per routing entry, the routed rows only (the swapped
+// GEMMs never use a padding row's products, so its bytes stay as they are).
+// The row's FC2 factor G * (down multiplier) * (router weight) -- the
+// product the prefill band's FC2 epilogue forms, in the same order -- takes
+// G's place.
+__global__ void quant_h_routed_kernel(PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
+  const int i = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (i >= a.n_entries) return;
+  const int r = a.pos[i];
+  if (r < 0) return;
+  const float G = quant_h_row(a, r);
+  if ((threadIdx.x & 31) == 0) {
+    const float* g2 = reinterpret_cast<const float*>(a.s2 + (size_t)a.E * scale_chunk_bytes(a.H, a.I));
+    a.hG[r] = G * g2[route_id(a.ids, i, a.ids64, a.E)] * a.tw[i];
+  }
 }
 
 // ---------------------------------------------------------------- GEMMs
@@ -739,6 +805,218 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   };
   gemm_fp4_persistent<kFc2BN>(&map_h, &map_w, a.I, a.status, n_mt * NT, tile_of, epi);
+}
+
+// ---------------------------------------------------------------- mid band
+// Batches with few routed rows per expert: the same layer (same activation
+// quantisation, same products) with the GEMM operands swapped
+// (gemm_fp4_swap.cuh): the weights fill the MMA's 128-row side, and the
+// routed rows of a 32-row routing tile (each expert's rows padded to a
+// multiple of 32) are its N side, 16 or 32 of them.  A tile is (routing
+// tile, group of up to four 128-row weight tiles), the group fastest.
+struct BMaps {
+  CUtensorMap m[2];  // B boxes of 16 and 32 rows
+};
+constexpr int kMidPad = 32;  // the mid band's routing-tile height
+constexpr int kFc1SwapSubs = 2;  // FC1's weight tiles per item at most (the gate/up exchange area)
+static_assert(kFc1SwapSubs * 32 * 64 * 4 + 16 <= SwapCfg::kExtra && 4 * (32 * 33 + 32) * 4 <= SwapCfg::kExtra,
+              "epilogue exchange area");
+
+// Per-routing-tile values of the epilogues, fetched by each epilogue thread
+// for its next tile while it finishes the current one (lane j: column j).
+struct MidCols {
+  int mt = -1, nv = 0, e = 0, src = 0;
+  float v = 0.f;
+};
+
+// FC1: D[w13 row][routed row].  A 128-row w13 tile holds 64 gate rows then
+// the 64 matching up rows, so the up lanes hand their values to the gate
+// lanes through shared memory (mbarriers: up values written / read).
+__global__ void __launch_bounds__(kSwapThreads, 1)
+    fc1_swap_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ BMaps maps_x, PrefillArgs a,
+                    int subs) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
+  const bool relu2 = a.act.kind == MOE_FP4_ACT_RELU2;
+  const int NT = relu2 ? (a.I + 127) / 128 : 2 * a.I / 128;  // weight tiles per expert
+  const int NG = (NT + subs - 1) / subs;  // weight-tile groups per routing tile
+  const int KG = a.H / 64;
+  const size_t scb = scale_chunk_bytes(relu2 ? NT * 128 : 2 * a.I, a.H);
+  const float* g13 = reinterpret_cast<const float*>(a.s13 + (size_t)a.E * scb);
+  const int n_mt = *a.num_tiles;
+  const int lane = threadIdx.x & 31;
+  // [weight tile][column][64] up values of at most kFc1SwapSubs weight tiles
+  float* xch = reinterpret_cast<float*>(swap_extra_smem());
+  uint64_t* xbar = reinterpret_cast<uint64_t*>(xch + kFc1SwapSubs * 32 * 64);  // [0] written, [1] read
+  if (threadIdx.x == 0) {
+    mbar_init(&xbar[0], 64);
+    mbar_init(&xbar[1], 64);
+  }
+  auto tile_of = [&](int idx) {
+    SwapTile t;
+    const int mt = idx / NG, g = idx % NG;
+    t.m_tile = mt;
+    t.group = g;
+    t.valid = mt < n_mt;
+    if (!t.valid) return t;
+    const int e = a.tile_expert[mt];
+    t.subs = NT - subs * g < subs ? NT - subs * g : subs;
+    t.n_rows = a.tile_rows[mt] <= 16 ? 16 : 32;
+    t.a_row0 = (relu2 ? e * a.I : e * 2 * a.I) + 128 * subs * g;
+    t.b_row0 = kMidPad * mt;
+    t.b_word = mt & 3;
+    t.a_sf = a.s13 + (size_t)e * scb + (size_t)subs * g * KG * kChunkBytes;
+    t.a_sf_step = (size_t)KG * kChunkBytes;
+    t.b_sf = a.xsf + (size_t)(mt >> 2) * KG * kChunkBytes;
+    return t;
+  };
+  MidCols cur, pf;
+  auto fetch = [&](int mt) {
+    MidCols c;
+    c.mt = mt;
+    c.e = a.tile_expert[mt];
+    c.nv = a.tile_rows[mt];
+    c.v = a.xG[kMidPad * mt + lane];
+    return c;
+  };
+  int xi = 0;  // tiles this epilogue thread has finished
+  auto epi = [&](uint32_t tmem_row, int row, const SwapTile& t) {
+    cur = pf.mt == t.m_tile ? pf : fetch(t.m_tile);
+    const int next = t.m_tile * NG + t.group + (int)gridDim.x;
+    if (next < n_mt * NG && next / NG != t.m_tile) pf = fetch(next / NG);
+    const int nv = cur.nv, N = t.n_rows;
+    const float xg = cur.v;  // lane c: column c's x multiplier
+    if (relu2) {
+      // h = max(u, 0)^2 for w1 rows below I
+      const float m0 = g13[cur.e];
+#pragma unroll 1
+      for (int j = 0; j < t.subs; ++j) {
+        const int n = 128 * (subs * t.group + j) + row;
+        uint32_t v[32];
+        tmem_ld32(tmem_row + j * N, v);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          if (c < nv) {  // (warp-uniform)
+            const float xc = __shfl_sync(0xffffffffu, xg, c);
+            if (n < a.I) {
+              const float u = fmaxf(__uint_as_float(v[c]) * (xc * m0), 0.f);
+              a.hbuf[(size_t)(t.b_row0 + c) * a.I + n] = __float2bfloat16_rn(u * u);
+            }
+          }
+        }
+      }
+      return;
+    }
+    const int l = row & 63;
+    if (row >= 64) {
+      // up lanes: this tile's up values into the exchange area once the gate
+      // lanes have read the previous tile's
+      if (xi > 0) mbar_wait(&xbar[1], (xi - 1) & 1, a.status, 16u);
+#pragma unroll 1
+      for (int j = 0; j < t.subs; ++j) {
+        uint32_t v[32];
+        tmem_ld32(tmem_row + j * N, v);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) xch[(j * 32 + c) * 64 + l] = __uint_as_float(v[c]);
+      }
+      mbar_arrive(&xbar[0]);
+    } else {
+      const float mg = g13[2 * cur.e], mu = g13[2 * cur.e + 1];
+      mbar_wait(&xbar[0], xi & 1, a.status, 16u);
+#pragma unroll 1
+      for (int j = 0; j < t.subs; ++j) {
+        const int n = 64 * (subs * t.group + j) + l;
+        uint32_t v[32];
+        tmem_ld32(tmem_row + j * N, v);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          if (c < nv) {  // (warp-uniform)
+            const float xc = __shfl_sync(0xffffffffu, xg, c);
+            const float h =
+                gated_act(__uint_as_float(v[c]) * (xc * mg), xch[(j * 32 + c) * 64 + l] * (xc * mu), a.act);
+            a.hbuf[(size_t)(t.b_row0 + c) * a.I + n] = __float2bfloat16_rn(h);
+          }
+        }
+      }
+      mbar_arrive(&xbar[1]);
+    }
+    ++xi;
+  };
+  gemm_fp4_swap_persistent(&map_w, &maps_x.m[0], a.H, a.status, n_mt * NG, tile_of, epi);
+}
+
+// FC2: D[w2 row][routed row]; each lane owns an output column and reduces its
+// routed rows' products, times the rows' factors (hG, with the down
+// multiplier and router weight folded in), into the FP32 token accumulator;
+// the values go through shared memory so that a lane reduces four
+// consecutive outputs of one token at a time (red.v4).
+__global__ void __launch_bounds__(kSwapThreads, 1)
+    fc2_swap_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ BMaps maps_h, PrefillArgs a,
+                    int subs) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
+  const int NT = a.H / 128;
+  const int NG = (NT + subs - 1) / subs;  // weight-tile groups per routing tile
+  const int KG = a.I / 64;
+  const size_t scb = scale_chunk_bytes(a.H, a.I);
+  const int n_mt = *a.num_tiles;
+  const int lane = threadIdx.x & 31;
+  auto tile_of = [&](int idx) {
+    SwapTile t;
+    const int mt = idx / NG, g = idx % NG;
+    t.m_tile = mt;
+    t.group = g;
+    t.valid = mt < n_mt;
+    if (!t.valid) return t;
+    const int e = a.tile_expert[mt];
+    t.subs = NT - subs * g < subs ? NT - subs * g : subs;
+    t.n_rows = a.tile_rows[mt] <= 16 ? 16 : 32;
+    t.a_row0 = e * a.H + 128 * subs * g;
+    t.b_row0 = kMidPad * mt;
+    t.b_word = mt & 3;
+    t.a_sf = a.s2 + (size_t)e * scb + (size_t)subs * g * KG * kChunkBytes;
+    t.a_sf_step = (size_t)KG * kChunkBytes;
+    t.b_sf = a.hsf + (size_t)(mt >> 2) * KG * kChunkBytes;
+    return t;
+  };
+  MidCols cur, pf;
+  auto fetch = [&](int mt) {
+    MidCols c;
+    c.mt = mt;
+    c.nv = a.tile_rows[mt];
+    c.src = a.row_src[kMidPad * mt + lane];  // (-1 on padding rows, never used)
+    c.v = a.hG[kMidPad * mt + lane];
+    return c;
+  };
+  // per epilogue warp: 32 routed rows x its 32 output columns
+  float* stg = reinterpret_cast<float*>(swap_extra_smem()) + (threadIdx.x / 32 % 4) * (32 * 33 + 32);
+  int* stg_tok = reinterpret_cast<int*>(stg + 32 * 33);
+  auto epi = [&](uint32_t tmem_row, int row, const SwapTile& t) {
+    cur = pf.mt == t.m_tile ? pf : fetch(t.m_tile);
+    const int next = t.m_tile * NG + t.group + (int)gridDim.x;
+    if (next < n_mt * NG && next / NG != t.m_tile) pf = fetch(next / NG);
+    const int nv = cur.nv, N = t.n_rows;
+    if (lane < nv) stg_tok[lane] = cur.src / a.top_k;
+#pragma unroll 1
+    for (int j = 0; j < t.subs; ++j) {
+      uint32_t v[32];
+      tmem_ld32(tmem_row + j * N, v);
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c < nv) stg[c * 33 + lane] = __uint_as_float(v[c]) * __shfl_sync(0xffffffffu, cur.v, c);
+      __syncwarp();
+      float* out0 = a.acc + 128 * (subs * t.group + j) + (row & ~31);
+      for (int p = lane; p < nv * 8; p += 32) {
+        const int c = p >> 3, q = p & 7;
+        const float* sv = stg + c * 33 + 4 * q;
+        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(out0 + (size_t)stg_tok[c] * a.H + 4 * q),
+                     "f"(sv[0]), "f"(sv[1]), "f"(sv[2]), "f"(sv[3])
+                     : "memory");
+      }
+      __syncwarp();
+    }
+  };
+  gemm_fp4_swap_persistent(&map_w, &maps_h.m[0], a.I, a.status, n_mt * NG, tile_of, epi);
 }
 
 // MXFP8 (W4A8-MX activations): E4M3 elements with one UE8M0 scale per 32
@@ -1336,7 +1614,8 @@ __global__ void debug_quant_kernel(const float* in, int rows, int K, uint8_t* q,
 size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct PrefillCarve {
-  size_t counts, block_base, expert_off, expert_poff, tile_expert, num_tiles, pos, row_src, xq, xsf, xG, hbuf, hq,
+  size_t counts, block_base, expert_off, expert_poff, tile_expert, tile_rows, num_tiles, pos, row_src, xq, xsf, xG,
+      hbuf, hq,
       hsf, hG, acc, xb, status, total;
   int n_route_blocks, max_tiles;
 };
@@ -1348,6 +1627,7 @@ PrefillCarve prefill_carve(int M, int E, int H, int I, int top_k, bool exact = f
   const size_t n = (size_t)M * top_k;
   c.n_route_blocks = (int)((n + kRouteBlock - 1) / kRouteBlock);
   c.max_tiles = (int)((n + 127) / 128) + E;
+  const int max_tiles_mid = (int)((n + kMidPad - 1) / kMidPad) + E;  // the mid band's 32-row tiles
   const size_t rows = (size_t)128 * c.max_tiles;
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -1364,7 +1644,8 @@ PrefillCarve prefill_carve(int M, int E, int H, int I, int top_k, bool exact = f
   c.block_base = take(sizeof(int) * c.n_route_blocks * E);
   c.expert_off = take(sizeof(int) * (E + 1));
   c.expert_poff = take(sizeof(int) * (E + 1));
-  c.tile_expert = take(sizeof(int) * c.max_tiles);
+  c.tile_expert = take(sizeof(int) * max_tiles_mid);
+  c.tile_rows = take(sizeof(int) * max_tiles_mid);
   c.num_tiles = take(sizeof(int));
   c.pos = take(sizeof(int) * n);
   c.row_src = take(sizeof(int) * rows);
@@ -1406,6 +1687,7 @@ PrefillArgs prefill_args(const PrefillCarve& c, void* ws, int M, int E, int H, i
   a.expert_off = reinterpret_cast<int*>(b + c.expert_off);
   a.expert_poff = reinterpret_cast<int*>(b + c.expert_poff);
   a.tile_expert = reinterpret_cast<int*>(b + c.tile_expert);
+  a.tile_rows = reinterpret_cast<int*>(b + c.tile_rows);
   a.num_tiles = reinterpret_cast<int*>(b + c.num_tiles);
   a.pos = reinterpret_cast<int*>(b + c.pos);
   a.row_src = reinterpret_cast<int*>(b + c.row_src);
@@ -1421,9 +1703,11 @@ PrefillArgs prefill_args(const PrefillCarve& c, void* ws, int M, int E, int H, i
   return a;
 }
 
-cudaError_t launch_route(PrefillArgs& a, cudaStream_t st) {
+cudaError_t launch_route(PrefillArgs& a, cudaStream_t st, int pad = 128) {
   cudaError_t e = launch_pdl(route_count_kernel, (unsigned)a.n_route_blocks, kRouteBlock, sizeof(int) * a.E, st, a);
-  if (e == cudaSuccess) e = launch_pdl(route_scan_kernel, 1u, 1024u, 0, st, a);
+  if (e == cudaSuccess)
+    e = pad == 128 ? launch_pdl(route_scan_kernel<128>, 1u, 1024u, 0, st, a)
+                   : launch_pdl(route_scan_kernel<kMidPad>, 1u, 1024u, 0, st, a);
   if (e == cudaSuccess) e = launch_pdl(route_scatter_kernel, (unsigned)a.n_route_blocks, 32u, sizeof(int) * a.E, st, a);
   return e;
 }
@@ -1550,9 +1834,69 @@ static cudaError_t launch_prefill_mx(PrefillArgs& a, const PrefillCarve& c, cons
   return e;
 }
 
+// The mid band: route, x quantised per routed row, the swapped FC1, h
+// quantised per routed row, the swapped FC2, the cast (same numerics as the
+// prefill band).
+static cudaError_t launch_prefill_mid(PrefillArgs& a, const PrefillCarve& c, const void* w13, const void* w2,
+                                      cudaStream_t st, int* cu_err) {
+  const int E = a.E, H = a.H, I = a.I;
+  const bool relu2 = a.act.kind == MOE_FP4_ACT_RELU2;
+  const size_t rows = (size_t)128 * c.max_tiles;
+  CUtensorMap mw13, mw2;
+  BMaps mx, mh;
+  CUresult r = make_fp4_map(&mw13, w13, (uint64_t)H / 2, (uint64_t)E * (relu2 ? I : 2 * I), 128u);
+  if (r == CUDA_SUCCESS) r = make_fp4_map(&mw2, w2, (uint64_t)I / 2, (uint64_t)E * H, 128u);
+  for (int i = 0; i < 2 && r == CUDA_SUCCESS; ++i) {
+    r = make_fp4_map(&mx.m[i], a.xq, (uint64_t)H / 2, rows, 16u << i);
+    if (r == CUDA_SUCCESS) r = make_fp4_map(&mh.m[i], a.hq, (uint64_t)I / 2, rows, 16u << i);
+  }
+  if (r != CUDA_SUCCESS) {
+    *cu_err = (int)r;
+    return cudaErrorInvalidValue;
+  }
+  static bool attrs = false;
+  if (!attrs) {
+    cudaError_t e = cudaFuncSetAttribute(fc1_swap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SwapCfg::kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fc2_swap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SwapCfg::kSmem);
+    if (e != cudaSuccess) return e;
+    attrs = true;
+  }
+  cudaError_t e = launch_route(a, st, kMidPad);
+  if (e == cudaSuccess)
+    e = a.M <= kQuantXEntryMaxM ? launch_pdl(quant_x_entry_kernel, (unsigned)((a.n_entries + 7) / 8), 256u, 0, st, a)
+                                : launch_pdl(quant_x_kernel, (unsigned)((a.M + 7) / 8), 256u, 0, st, a);
+  if (e != cudaSuccess) return e;
+  int sms = 0;
+  e = gemm_sms(&sms);
+  if (e != cudaSuccess) return e;
+  // persistent, one CTA per SM; tiles: (32-row routing tile, group of up to
+  // four weight tiles)
+  // weight tiles per item: enough for about eight K stages between
+  // accumulator hand-offs (FC2's K = I is often one or two stages)
+  auto subs_for = [](int K) {
+    const int nk = (K + 255) / 256, sb = (8 + nk - 1) / nk;
+    return sb < kSwapSubs ? sb : kSwapSubs;
+  };
+  const int s1 = subs_for(H) < kFc1SwapSubs ? subs_for(H) : kFc1SwapSubs, s2 = subs_for(I);
+  const int n = a.n_entries, max_mid = (n + kMidPad - 1) / kMidPad + E;
+  const int nt1 = relu2 ? (I + 127) / 128 : 2 * I / 128, nt2 = H / 128;
+  const int g1 = max_mid * ((nt1 + s1 - 1) / s1), g2 = max_mid * ((nt2 + s2 - 1) / s2);
+  e = launch_pdl(fc1_swap_kernel, (unsigned)(g1 < sms ? g1 : sms), kSwapThreads, SwapCfg::kSmem, st, mw13, mx, a,
+                 s1);
+  if (e == cudaSuccess)
+    e = launch_pdl(quant_h_routed_kernel, (unsigned)((a.n_entries + 7) / 8), 256u, 0, st, a);
+  if (e == cudaSuccess)
+    e = launch_pdl(fc2_swap_kernel, (unsigned)(g2 < sms ? g2 : sms), kSwapThreads, SwapCfg::kSmem, st, mw2, mh, a,
+                   s2);
+  if (e == cudaSuccess) e = launch_pdl(cast_out_kernel, 4u * 152u, 256u, 0, st, a);
+  return e;
+}
+
 cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, const void* w2, const void* s2,
                            const int32_t* ids, int ids64, const float* tw, void* out, int M, int E, int H, int I,
-                           int top_k, const ActParams& act, int band, void* ws, cudaStream_t st, int* cu_err) {
+                           int top_k, const ActParams& act, int band, bool mid, void* ws, cudaStream_t st,
+                           int* cu_err) {
   const bool exact = band != MOE_FP4_PREFILL_NVFP4;  // the BF16-engine bands
   const PrefillCarve c = prefill_carve(M, E, H, I, top_k, exact);
   PrefillArgs a = prefill_args(c, ws, M, E, H, I, top_k);
@@ -1589,6 +1933,7 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
     *cu_err = (int)r;
     return cudaErrorInvalidValue;
   }
+  if (mid) return launch_prefill_mid(a, c, w13, w2, st, cu_err);
   static bool attrs = false;
   if (!attrs) {
     cudaError_t e =
@@ -1601,7 +1946,8 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
   }
   cudaError_t e = launch_route(a, st);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(quant_x_kernel, (unsigned)((M + 7) / 8), 256u, 0, st, a);
+  e = M <= kQuantXEntryMaxM ? launch_pdl(quant_x_entry_kernel, (unsigned)((a.n_entries + 7) / 8), 256u, 0, st, a)
+                            : launch_pdl(quant_x_kernel, (unsigned)((M + 7) / 8), 256u, 0, st, a);
   if (e != cudaSuccess) return e;
   int sms = 0;
   cudaError_t es = gemm_sms(&sms);

@@ -460,17 +460,24 @@ MOE_FP4_API int moe_fp4_forward_noalloc(const void *x_bf16, const void *w13, con
  */
 MOE_FP4_API int moe_fp4_debug_set_decode_family(int family, int *previous);
 /*
- * Test support: the kernels of batches just past the decode band
- * (MOE_FP4_DECODE_MAX_M < M <= 3 * MOE_FP4_DECODE_MAX_M) for every later
+ * Test support: the kernels of batches past the decode band
+ * (M > MOE_FP4_DECODE_MAX_M) under MOE_FP4_PREFILL_NVFP4 for every later
  * call in the process.
- *   mode 0  by shape (default): the chunks up to 2 * MOE_FP4_DECODE_MAX_M
- *           tokens when one expert's weights (3IH/2 nibble bytes) are at
- *           most 8 MiB, else the prefill band
- *   mode 1  the prefill band
+ *   mode 0  by shape (default): up to 2 * MOE_FP4_DECODE_MAX_M tokens the
+ *           chunks when one expert's weights (3IH/2 nibble bytes) are at
+ *           most 8 MiB; otherwise the mid band's GEMMs while the experts
+ *           average at most 16 routed rows (M * top_k <= 16 E), else the
+ *           prefill band's
+ *   mode 1  the prefill band's GEMMs (routed rows on the MMA's 128-row
+ *           side)
  *   mode 2  the decode-band kernels on balanced chunks of at most
- *           MOE_FP4_DECODE_MAX_M tokens, one chunk after another
- * Larger batches always take the prefill band.  *previous (if non-null)
- * receives the old setting.  MOE_FP4_EINVAL for other values.
+ *           MOE_FP4_DECODE_MAX_M tokens, one chunk after another (up to
+ *           3 * MOE_FP4_DECODE_MAX_M tokens; larger batches as mode 0)
+ *   mode 3  the mid band's GEMMs (weights on the MMA's 128-row side, an
+ *           expert's routed rows on its N side), any batch size
+ * The prefill and mid bands compute the same layer (NVFP4 activations).
+ * *previous (if non-null) receives the old setting.  MOE_FP4_EINVAL for
+ * other values.
  */
 MOE_FP4_API int moe_fp4_debug_set_mid_band(int mode, int *previous);
 MOE_FP4_API int moe_fp4_debug_decode_gemv_fits(int M, int E, int H, int I, int top_k);
@@ -491,6 +498,11 @@ MOE_FP4_API int moe_fp4_debug_decode_plan(int M, int E, int H, int I, int top_k,
  * chunked batch); 0 for shapes that take the prefill band or invalid
  * arguments. */
 MOE_FP4_API int moe_fp4_debug_decode_launches(int M, int E, int H, int I, int top_k);
+/* The kernels the current moe_fp4_debug_set_mid_band setting picks for a
+ * batch past the decode band under MOE_FP4_PREFILL_NVFP4 (1 the prefill
+ * band's GEMMs, 2 decode-band chunks, 3 the mid band's GEMMs); 0 for
+ * M <= MOE_FP4_DECODE_MAX_M or invalid shape arguments. */
+MOE_FP4_API int moe_fp4_debug_mid_band_of(int M, int E, int H, int I, int top_k);
 
 /*
  * Test support: dequantise one expert's projection from the resident layout

@@ -1,11 +1,13 @@
-"""Batches just past the decode band (MOE_FP4_DECODE_MAX_M < M <= 3x that).
+"""Batches past the decode band (M > MOE_FP4_DECODE_MAX_M).
 
-They run either on the prefill band or on the decode-band kernels over
-balanced chunks of at most MOE_FP4_DECODE_MAX_M tokens.  The chunked path
-keeps the decode band's numerics (BF16 activations, no activation
-quantisation), so it is held to the unquantised FP64 oracle, and it must be
-bitwise the concatenation of the chunks run as separate decode calls.  The
-prefill path is held to the oracle that mirrors its activation quantisation.
+They run on the prefill band's GEMMs, on the mid band's swapped GEMMs
+(weights on the MMA's 128-row side, an expert's routed rows on N), or, just
+past the band, on the decode-band kernels over balanced chunks of at most
+MOE_FP4_DECODE_MAX_M tokens.  The chunked path keeps the decode band's
+numerics (BF16 activations, no activation quantisation), so it is held to
+the unquantised FP64 oracle, and it must be bitwise the concatenation of the
+chunks run as separate decode calls.  The prefill and mid bands quantise the
+activations to NVFP4 and are held to the oracle that mirrors it.
 """
 import pytest
 import torch
@@ -16,7 +18,7 @@ from workload import gen
 
 pytestmark = pytest.mark.gpu
 
-PREFILL, CHUNKS = 1, 2
+PREFILL, CHUNKS, MID = 1, 2, 3
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -74,3 +76,31 @@ def test_int64_ids_through_chunks():
     a = _run(wl, CHUNKS)
     b = _run(wl, CHUNKS, ids=wl.topk_ids.long())
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# The mid band on the decode workloads' expert shapes: routed rows per expert
+# from about one (N = 16) to past a 128-row routing tile, invalid slots,
+# MXFP4 and NVFP4 weights.
+@pytest.mark.parametrize("name,ov", [("decode_e512", dict(M=64)), ("decode_e512", dict(E=64, M=200)),
+                                     ("decode_e288_m4", dict(E=96, M=40)),
+                                     ("decode_e256", dict(E=16, H=2048, I=1024, M=24)),
+                                     ("tiny_decode", dict(M=700, E=8, top_k=2))])
+def test_mid_band_swapped_gemms_parity(name, ov):
+    wl = gen.make_workload(name, device="cuda", **ov)
+    got = _run(wl, MID)
+    want, _, _, _ = oracle.forward_prefill(wl.x, wl.weights, wl.topk_ids, wl.topk_weights, wl.E, wl.H, wl.I,
+                                           wl.top_k, fmt=wl.fmt)
+    assert_layer_close(got, want, f"{name} {ov} mid band")
+    got64 = _run(wl, MID, ids=wl.topk_ids.long())
+    assert_layer_close(got64, want, f"{name} {ov} mid band, int64 ids")
+
+
+def test_mid_band_by_shape_matches_its_plan():
+    """decode_e512 at 32 tokens runs the mid band's GEMMs by shape."""
+    from fp4_weight_moe_gb300 import _capi
+    wl = gen.make_workload("decode_e512", device="cuda", M=32)
+    assert _capi.moe_fp4_debug_mid_band_of(wl.M, wl.E, wl.H, wl.I, wl.top_k) == MID
+    got = _run(wl, 0)
+    want, _, _, _ = oracle.forward_prefill(wl.x, wl.weights, wl.topk_ids, wl.topk_weights, wl.E, wl.H, wl.I,
+                                           wl.top_k, fmt=wl.fmt)
+    assert_layer_close(got, want, "decode_e512 M=32 by shape")

@@ -21,13 +21,15 @@ from workload import gen
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", autouse=True)
-def _build():
-    """Build, and send every batch past the decode band to the prefill band
-    (small ones would otherwise run as chunks of the decode band)."""
+@pytest.fixture(scope="module", autouse=True, params=[1, 3], ids=["prefill", "mid"])
+def _build(request):
+    """Build, and send every batch past the decode band to one set of GEMMs:
+    the prefill band's (routed rows on the MMA's 128-row side) or the mid
+    band's (weights there, an expert's routed rows on N).  Both compute the
+    same layer, so every case here runs on both."""
     ensure_built()
     from fp4_weight_moe_gb300 import _capi as c
-    prev = c.moe_fp4_debug_set_mid_band(1)
+    prev = c.moe_fp4_debug_set_mid_band(request.param)
     yield
     c.moe_fp4_debug_set_mid_band(prev)
 

@@ -90,14 +90,16 @@ def test_relu2_decode_parity(E, H, I, k, M, fmt, invalid):
     assert torch.equal(got64.view(torch.int16), got.view(torch.int16))
 
 
+@pytest.mark.parametrize("band", [1, 3], ids=["prefill", "mid"])
 @pytest.mark.parametrize("M,E,H,I,k,fmt", [(40, 12, 512, 320, 4, gen.NVFP4), (64, 8, 1024, 256, 2, gen.MXFP4),
-                                           (24, 6, 256, 128, 3, gen.NVFP4)])
-def test_relu2_prefill_parity(M, E, H, I, k, fmt):
+                                           (24, 6, 256, 128, 3, gen.NVFP4), (300, 4, 512, 192, 2, gen.NVFP4)])
+def test_relu2_prefill_parity(M, E, H, I, k, fmt, band):
     m = fm()
     w, x, ids, tw = _case(E, H, I, k, M, fmt, seed=M + E)
     pw = m.prepare_weights_relu2(w, E, H, I, fmt)
     ws = m.alloc_workspace(M, E, H, I, k, fmt)
-    prev = m._capi.moe_fp4_debug_set_mid_band(1)  # batches past 8 tokens: the prefill band
+    # batches past 8 tokens: the prefill band's GEMMs, or the mid band's
+    prev = m._capi.moe_fp4_debug_set_mid_band(band)
     try:
         got = m.forward_act(x, pw, ids, tw, ws, kind=m.ACT_RELU2)
         torch.cuda.synchronize()
