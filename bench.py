@@ -426,6 +426,9 @@ def measure(m, name, ov, K, W, dev, rank, ws_world, min_timed_s, threads, do_e2e
         res["timed"] = False
         res["_state"] = (c, seed, ids_pool, w_pool, x)
         return res
+    # batches of at most 8192 routing entries route in one kernel, larger in three
+    route_launches = 1 if M * k <= 8192 else 3
+    mid = prefill and not exact and m._capi.moe_fp4_debug_mid_band_of(M, E, H, I, k) == 3
     per_layer_bytes = [layer_bytes(ids_pool[i], E, H, I, M, k, fmt)[0] for i in range(K)]
     step_flops = sum(layer_flops(ids_pool[i], E, H, I) for i in range(K))
     for i in range(W):
@@ -473,15 +476,19 @@ def measure(m, name, ov, K, W, dev, rank, ws_world, min_timed_s, threads, do_e2e
                 "us_per_layer_max": max(times) * 1e3 / K, "routed_bytes_per_layer": sum(per_layer_bytes) / K,
                 "flops_per_layer": step_flops / K, "job_units": job_units, "ms_per_replay": ms_max,
                 "launches_per_layer": m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) if decode else
-                (7 if res.get("engine") == "fp8" else 8),
+                route_launches + (4 if res.get("engine") == "fp8" else 5),
                 "plan": decode_kernel_label(m, M, E, H, I, k) if decode else
                 ("W4A8-MX prefill layer: route, x to MXFP8 per routed row, FC1 and FC2 on tcgen05 kind::mxf8f6f4 "
-                 "(E4M3 x E2M1 as stored, h to MXFP8 in FC1's epilogue), cast (7 launches)"
+                 "(E4M3 x E2M1 as stored, h to MXFP8 in FC1's epilogue), cast"
                  if res.get("engine") == "fp8" else
                  "16-bit prefill layer: route, x staged in row-scaled FP16 per routed row, FC1 GEMM, h rescaled to "
-                 "FP16, FC2 GEMM (FP16 tensor cores, FP4 weights decoded to FP16 in shared memory), cast (8 launches)"
+                 "FP16, FC2 GEMM (FP16 tensor cores, FP4 weights decoded to FP16 in shared memory), cast"
                  if exact else
-                 "prefill layer: route, x quantiser, FC1 GEMM, h quantiser, FC2 GEMM, cast (8 launches)"),
+                 "mid-band layer: route (32-row routing tiles), x quantiser, FC1 and FC2 GEMMs with the weights on "
+                 "the MMA's 128-row side and the routed rows on N, h quantiser, cast"
+                 if mid else
+                 "prefill layer: route, x quantiser, FC1 GEMM, h quantiser, FC2 GEMM, cast")
+                + f" ({route_launches} routing launch{'es' if route_launches > 1 else ''})",
                 "window": window, "prefill": prefill})
     if do_e2e and not exact:
         # end to end through the host-buffer entry point, one eager call per

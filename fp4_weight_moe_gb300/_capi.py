@@ -82,6 +82,7 @@ SIGNATURES = {
     "moe_fp4_debug_dequant": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "moe_fp4_debug_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_fp4_debug_route": (_I, [_P, _I, _I, _I, _P, _P, _P, _Z, _P]),
+"moe_fp4_debug_route_small": (_I, [_P, _I, _I, _I, _P, _P, _P, _Z, _P]),
     "moe_fp4_debug_route_workspace_bytes": (_Z, [_I, _I, _I]),
     "moe_fp4_debug_quant_mxfp8_rows": (_I, [_P, _I, _I, _P, _P, _P]),
     "moe_fp4_debug_quant_rows": (_I, [_P, _I, _I, _P, _P, _P, _P]),
@@ -288,6 +289,11 @@ def moe_fp4_debug_gemm(a_q, a_sf, b_q, b_sf, d, M_rows, N_rows, K, fmt, status, 
 def moe_fp4_debug_route(ids, M, E, top_k, perm, offset, ws, ws_bytes, stream):
     return _check("moe_fp4_debug_route", _load().moe_fp4_debug_route(ids, M, E, top_k, perm, offset, ws, ws_bytes,
                                                                        stream))
+
+
+def moe_fp4_debug_route_small(ids, M, E, top_k, perm, offset, ws, ws_bytes, stream):
+    return _check("moe_fp4_debug_route_small",
+                  _load().moe_fp4_debug_route_small(ids, M, E, top_k, perm, offset, ws, ws_bytes, stream))
 
 
 def moe_fp4_debug_route_workspace_bytes(M, E, top_k) -> int:

@@ -29,7 +29,7 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
                            int top_k, const ActParams& act, int band, bool mid, void* ws, cudaStream_t st,
                            int* cu_err);
 cudaError_t launch_debug_route(const int32_t* ids, int M, int E, int top_k, int32_t* perm, int32_t* expert_offset,
-                               void* ws, cudaStream_t st);
+                               void* ws, cudaStream_t st, bool small);
 cudaError_t launch_debug_quant(const float* in, int rows, int K, uint8_t* q, uint8_t* s, float* G, cudaStream_t st);
 cudaError_t launch_debug_quant_mxfp8(const float* in, int rows, int K, uint8_t* q, uint8_t* s, cudaStream_t st);
 extern std::atomic<int> g_decode_family;
@@ -355,30 +355,30 @@ std::atomic<int> g_mid_band{0};
 constexpr int kMidBandMaxM = 3 * MOE_FP4_DECODE_MAX_M;
 
 // Does a batch of M > MOE_FP4_DECODE_MAX_M tokens run as decode-band chunks?
-// By shape: up to 2 * MOE_FP4_DECODE_MAX_M tokens when one expert's weights
-// (3IH/2 nibble bytes) are at most 8 MiB.  Chunks stream an expert once per
-// chunk that routes to it instead of once per layer, but skip the prefill
-// band's routing, quantisation and cast launches; with small experts the
-// launches cost more.  Measured on GB300 (us per layer, prefill / chunks):
-// E=512 H=2560 I=320 k=10: M=9 78.8 / 49.0, 12 89.8 / 58.1, 16 103.6 / 82.8,
-// 24 124.2 / 124.1; E=288 H=4096 I=512 k=10: M=9 106.6 / 80.9, 16 150.0 /
-// 120.9, 24 181.4 / 181.0; E=256 H=7168 I=2048 k=8 (21 MiB experts, Zipf
-// routing): M=9 285.0 / 298.2, 16 412.5 / 482.6.
+// By shape: up to 3 * MOE_FP4_DECODE_MAX_M / 2 tokens when one expert's
+// weights (3IH/2 nibble bytes) are at most 8 MiB.  Chunks stream an expert
+// once per chunk that routes to it instead of once per layer, but skip the
+// routing, quantisation and cast launches; with small experts the launches
+// cost more.  Measured on GB300 (us per layer, chunks / mid band): E=512
+// H=2560 I=320 k=10: M=9 49.0 / -, 12 56.5 / 67.0, 16 81.1 / 77.0; E=288
+// H=4096 I=512 k=10: M=9 80.9 / -, 16 122.2 / 120.2; E=256 H=7168 I=2048 k=8
+// (21 MiB experts, Zipf routing): M=9 298.2 chunks against 285.0 on the
+// prefill band.
 bool mid_band_chunks(int M, int H, int I) {
   const int mode = g_mid_band.load(std::memory_order_relaxed);
   if (M > kMidBandMaxM) return false;
   if (mode != 0) return mode == 2;
-  return M <= 2 * MOE_FP4_DECODE_MAX_M && 3 * (size_t)I * H / 2 <= ((size_t)8 << 20);
+  return M <= 3 * MOE_FP4_DECODE_MAX_M / 2 && 3 * (size_t)I * H / 2 <= ((size_t)8 << 20);
 }
 
 // Does a batch past the decode band (and not in chunks) run on the mid band's
 // swapped GEMMs rather than the prefill band's?  By shape: while the experts
 // average at most kMidBandMaxRows routed rows, where the prefill tiles would
 // stage mostly padding rows of activations.  Measured on GB300 (us per layer,
-// prefill / mid band): E=512 H=2560 I=320 k=10: M=24 112.7 / 98.0, 64 183.0
-// / 159.4, 256 236.4 / 213.5; E=288 H=4096 I=512 k=10: M=64 234.4 / 211.4;
-// E=128 H=4096 I=1536 k=8: M=64 270.5 / 268.0, 256 284.1 / 286.7 (16 rows
-// per expert: even), 1024 342.2 / 550.3.
+// prefill / mid band): E=512 H=2560 I=320 k=10: M=24 106.1 / 93.1, 64 177.2
+// / 154.3, 256 232.3 / 207.6, 512 247.3 / 227.8; E=288 H=4096 I=512 k=10:
+// M=64 227.8 / 206.5; E=128 H=4096 I=1536 k=8: M=64 263.2 / 263.0, 256
+// 279.5 / 280.5 (16 rows per expert: even), 512 306.6 / 388.7.
 constexpr int kMidBandMaxRows = 16;
 bool mid_band_swap(int M, int E, int top_k) {
   const int mode = g_mid_band.load(std::memory_order_relaxed);
@@ -716,7 +716,18 @@ int moe_fp4_debug_route(const int32_t* topk_ids, int M, int E, int top_k, int32_
   if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < debug_route_workspace_bytes(M, E, top_k))
     return MOE_FP4_EWORKSPACE;
   cudaError_t e = launch_debug_route(topk_ids, M, E, top_k, perm, expert_offset, workspace,
-                                     static_cast<cudaStream_t>(stream));
+                                     static_cast<cudaStream_t>(stream), false);
+  return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
+}
+
+int moe_fp4_debug_route_small(const int32_t* topk_ids, int M, int E, int top_k, int32_t* perm,
+                              int32_t* expert_offset, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!topk_ids || !perm || !expert_offset || M <= 0 || E <= 0 || top_k <= 0) return MOE_FP4_EINVAL;
+  if (E > 4096 || top_k > 16 || (int64_t)M * top_k > 8192) return MOE_FP4_EUNSUPPORTED;
+  if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < debug_route_workspace_bytes(M, E, top_k))
+    return MOE_FP4_EWORKSPACE;
+  cudaError_t e = launch_debug_route(topk_ids, M, E, top_k, perm, expert_offset, workspace,
+                                     static_cast<cudaStream_t>(stream), true);
   return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
 }
 

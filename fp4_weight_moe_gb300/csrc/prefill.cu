@@ -500,6 +500,108 @@ __global__ void route_scan_kernel(PrefillArgs a) {
   }
 }
 
+// Small batches (n_entries <= kRouteSmallMax): the whole routing in one CTA
+// of 1024 threads -- per-expert counts and each entry's rank among its
+// expert's entries by shared-memory atomics, the exclusive scans (unpadded
+// and P-padded), the tile list, the rows, the padding rows.  The rank order
+// within an expert is the atomics' order, not the entries' (every routed
+// row computes the same products wherever it sits).
+constexpr int kRouteSmallMax = 8192;
+template <int P>
+__global__ void __launch_bounds__(1024, 1) route_small_kernel(PrefillArgs a) {
+  pdl_wait();               // the previous kernel on the stream is complete and visible
+  pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
+  __shared__ int s_cnt[kMaxPrefillE];
+  __shared__ int s_off[kMaxPrefillE];
+  __shared__ int s_wsum[2][32];
+  const int E = a.E, n = a.n_entries;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += 1024) s_cnt[e] = 0;
+  __syncthreads();
+  constexpr int R = kRouteSmallMax / 1024;
+  int ex[R], rk[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int i = tid + 1024 * r;
+    ex[r] = i < n ? route_id(a.ids, i, a.ids64, E) : -1;
+    rk[r] = ex[r] >= 0 && ex[r] < E ? atomicAdd(&s_cnt[ex[r]], 1) : -1;
+  }
+  __syncthreads();
+  // exclusive scans over experts (counts, P-padded counts): each thread a
+  // contiguous run of experts, then the runs' totals across the block
+  const int per = (E + 1023) / 1024;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int su = 0, sp = 0;
+  for (int e = e0; e < e1; ++e) {
+    su += s_cnt[e];
+    sp += (s_cnt[e] + P - 1) & ~(P - 1);
+  }
+  int iu = su, ip = sp;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int ou = __shfl_up_sync(0xffffffffu, iu, d), op = __shfl_up_sync(0xffffffffu, ip, d);
+    if (lane >= d) {
+      iu += ou;
+      ip += op;
+    }
+  }
+  if (lane == 31) {
+    s_wsum[0][warp] = iu;
+    s_wsum[1][warp] = ip;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int wu = s_wsum[0][lane], wp = s_wsum[1][lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int ou = __shfl_up_sync(0xffffffffu, wu, d), op = __shfl_up_sync(0xffffffffu, wp, d);
+      if (lane >= d) {
+        wu += ou;
+        wp += op;
+      }
+    }
+    s_wsum[0][lane] = wu;  // inclusive over warps
+    s_wsum[1][lane] = wp;
+    if (lane == 31) {
+      a.expert_off[E] = wu;
+      a.expert_poff[E] = wp;
+      *a.num_tiles = wp / P;
+    }
+  }
+  __syncthreads();
+  int ru = iu - su + (warp > 0 ? s_wsum[0][warp - 1] : 0);
+  int rp = ip - sp + (warp > 0 ? s_wsum[1][warp - 1] : 0);
+  for (int e = e0; e < e1; ++e) {
+    const int tot = s_cnt[e], padded = (tot + P - 1) & ~(P - 1);
+    a.expert_off[e] = ru;
+    a.expert_poff[e] = rp;
+    s_off[e] = rp;
+    for (int t = 0; t < padded / P; ++t) {
+      a.tile_expert[rp / P + t] = e;
+      a.tile_rows[rp / P + t] = min(P, tot - P * t);
+    }
+    ru += tot;
+    rp += padded;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int i = tid + 1024 * r;
+    if (i >= n) break;
+    if (rk[r] >= 0) {
+      const int row = s_off[ex[r]] + rk[r];
+      a.pos[i] = row;
+      a.row_src[row] = i;
+    } else {
+      a.pos[i] = -1;
+    }
+  }
+  // padding rows (past the routed rows of each expert's last tile) -> -1
+  const int n_rows = s_wsum[1][31];
+  for (int v = tid; v < n_rows; v += 1024)
+    if (v % P >= a.tile_rows[v / P]) a.row_src[v] = -1;
+}
+
 // One warp per block of entries: stable ranks by expert in index order.
 __global__ void route_scatter_kernel(PrefillArgs a) {
   pdl_wait();               // the previous kernel on the stream is complete and visible
@@ -825,8 +927,8 @@ static_assert(kFc1SwapSubs * 32 * 64 * 4 + 16 <= SwapCfg::kExtra && 4 * (32 * 33
 // Per-routing-tile values of the epilogues, fetched by each epilogue thread
 // for its next tile while it finishes the current one (lane j: column j).
 struct MidCols {
-  int mt = -1, nv = 0, e = 0, src = 0;
-  float v = 0.f;
+  int mt = -1, nv = 0, src = 0;
+  float v = 0.f, m0 = 0.f, m1 = 0.f;
 };
 
 // FC1: D[w13 row][routed row].  A 128-row w13 tile holds 64 gate rows then
@@ -870,15 +972,19 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
     t.b_sf = a.xsf + (size_t)(mt >> 2) * KG * kChunkBytes;
     return t;
   };
-  MidCols cur, pf;
   auto fetch = [&](int mt) {
     MidCols c;
     c.mt = mt;
-    c.e = a.tile_expert[mt];
+    const int e = a.tile_expert[mt];
     c.nv = a.tile_rows[mt];
     c.v = a.xG[kMidPad * mt + lane];
+    c.m0 = relu2 ? g13[e] : g13[2 * e];  // gate (w1) multiplier
+    c.m1 = relu2 ? 0.f : g13[2 * e + 1];  // up multiplier
     return c;
   };
+  // the epilogue warps fetch their first tile's values while its stages stream
+  MidCols cur, pf;
+  if (threadIdx.x >= 192 && (int)blockIdx.x < n_mt * NG) pf = fetch((int)blockIdx.x / NG);
   int xi = 0;  // tiles this epilogue thread has finished
   auto epi = [&](uint32_t tmem_row, int row, const SwapTile& t) {
     cur = pf.mt == t.m_tile ? pf : fetch(t.m_tile);
@@ -888,7 +994,7 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
     const float xg = cur.v;  // lane c: column c's x multiplier
     if (relu2) {
       // h = max(u, 0)^2 for w1 rows below I
-      const float m0 = g13[cur.e];
+      const float m0 = cur.m0;
 #pragma unroll 1
       for (int j = 0; j < t.subs; ++j) {
         const int n = 128 * (subs * t.group + j) + row;
@@ -921,7 +1027,7 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
       }
       mbar_arrive(&xbar[0]);
     } else {
-      const float mg = g13[2 * cur.e], mu = g13[2 * cur.e + 1];
+      const float mg = cur.m0, mu = cur.m1;
       mbar_wait(&xbar[0], xi & 1, a.status, 16u);
 #pragma unroll 1
       for (int j = 0; j < t.subs; ++j) {
@@ -979,7 +1085,6 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
     t.b_sf = a.hsf + (size_t)(mt >> 2) * KG * kChunkBytes;
     return t;
   };
-  MidCols cur, pf;
   auto fetch = [&](int mt) {
     MidCols c;
     c.mt = mt;
@@ -988,6 +1093,9 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
     c.v = a.hG[kMidPad * mt + lane];
     return c;
   };
+  // the epilogue warps fetch their first tile's values while its stages stream
+  MidCols cur, pf;
+  if (threadIdx.x >= 192 && (int)blockIdx.x < n_mt * NG) pf = fetch((int)blockIdx.x / NG);
   // per epilogue warp: 32 routed rows x its 32 output columns
   float* stg = reinterpret_cast<float*>(swap_extra_smem()) + (threadIdx.x / 32 % 4) * (32 * 33 + 32);
   int* stg_tok = reinterpret_cast<int*>(stg + 32 * 33);
@@ -1703,7 +1811,10 @@ PrefillArgs prefill_args(const PrefillCarve& c, void* ws, int M, int E, int H, i
   return a;
 }
 
-cudaError_t launch_route(PrefillArgs& a, cudaStream_t st, int pad = 128) {
+cudaError_t launch_route(PrefillArgs& a, cudaStream_t st, int pad = 128, bool stable = false) {
+  if (!stable && a.n_entries <= kRouteSmallMax)
+    return pad == 128 ? launch_pdl(route_small_kernel<128>, 1u, 1024u, 0, st, a)
+                      : launch_pdl(route_small_kernel<kMidPad>, 1u, 1024u, 0, st, a);
   cudaError_t e = launch_pdl(route_count_kernel, (unsigned)a.n_route_blocks, kRouteBlock, sizeof(int) * a.E, st, a);
   if (e == cudaSuccess)
     e = pad == 128 ? launch_pdl(route_scan_kernel<128>, 1u, 1024u, 0, st, a)
@@ -1967,11 +2078,12 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
 size_t debug_route_workspace_bytes(int M, int E, int top_k) { return prefill_carve(M, E, 256, 256, top_k).total; }
 
 cudaError_t launch_debug_route(const int32_t* ids, int M, int E, int top_k, int32_t* perm, int32_t* expert_offset,
-                               void* ws, cudaStream_t st) {
+                               void* ws, cudaStream_t st, bool small) {
   const PrefillCarve c = prefill_carve(M, E, 256, 256, top_k);
   PrefillArgs a = prefill_args(c, ws, M, E, 256, 256, top_k);
   a.ids = ids;
-  cudaError_t e = launch_route(a, st);
+  if (small && a.n_entries > kRouteSmallMax) return cudaErrorInvalidValue;
+  cudaError_t e = launch_route(a, st, 128, !small);
   if (e != cudaSuccess) return e;
   fill_i32_kernel<<<64, 256, 0, st>>>(perm, M * top_k, -1);
   route_perm_kernel<<<E, 256, 0, st>>>(a, perm);

@@ -463,8 +463,8 @@ MOE_FP4_API int moe_fp4_debug_set_decode_family(int family, int *previous);
  * Test support: the kernels of batches past the decode band
  * (M > MOE_FP4_DECODE_MAX_M) under MOE_FP4_PREFILL_NVFP4 for every later
  * call in the process.
- *   mode 0  by shape (default): up to 2 * MOE_FP4_DECODE_MAX_M tokens the
- *           chunks when one expert's weights (3IH/2 nibble bytes) are at
+ *   mode 0  by shape (default): up to 3 * MOE_FP4_DECODE_MAX_M / 2 tokens
+ *           the chunks when one expert's weights (3IH/2 nibble bytes) are at
  *           most 8 MiB; otherwise the mid band's GEMMs while the experts
  *           average at most 16 routed rows (M * top_k <= 16 E), else the
  *           prefill band's
@@ -540,6 +540,17 @@ MOE_FP4_API int moe_fp4_debug_gemm(const void *a_q, const void *a_sf, const void
 MOE_FP4_API int moe_fp4_debug_route(const int32_t *topk_ids, int M, int E, int top_k, int32_t *perm,
                                     int32_t *expert_offset, void *workspace, size_t workspace_bytes, void *stream);
 MOE_FP4_API size_t moe_fp4_debug_route_workspace_bytes(int M, int E, int top_k);
+/*
+ * Test support: the same compaction as the layers of at most 8192 routing
+ * entries compute it (one CTA; each expert's rows in the order its entries
+ * won a shared-memory counter, not necessarily token order).  Same arguments
+ * and outputs as moe_fp4_debug_route; expert_offset is the same, and perm
+ * holds the same entries per expert.  MOE_FP4_EUNSUPPORTED for
+ * M * top_k > 8192.
+ */
+MOE_FP4_API int moe_fp4_debug_route_small(const int32_t *topk_ids, int M, int E, int top_k, int32_t *perm,
+                                          int32_t *expert_offset, void *workspace, size_t workspace_bytes,
+                                          void *stream);
 
 /*
  * Test support: the prefill band's NVFP4 activation quantiser on FP32 rows

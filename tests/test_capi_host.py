@@ -160,7 +160,7 @@ def test_band_policy_by_shape(lib):
     try:
         assert c.moe_fp4_debug_decode_family_of(1, *e512) == 2
         assert [c.moe_fp4_debug_decode_launches(M, *e512) for M in (1, 2, 8)] == [3, 4, 4]
-        assert [c.moe_fp4_debug_decode_launches(M, *e512) for M in (9, 12, 16, 17, 24)] == [8, 8, 8, 0, 0]
+        assert [c.moe_fp4_debug_decode_launches(M, *e512) for M in (9, 12, 13, 16, 24)] == [8, 8, 0, 0, 0]
         assert [c.moe_fp4_debug_decode_launches(M, *e256) for M in (8, 9, 16)] == [4, 0, 0]
     finally:
         c.moe_fp4_debug_set_decode_family(prev_family)
@@ -179,12 +179,12 @@ def test_band_policy_by_shape(lib):
 
 
 def test_mid_band_plan_by_shape(lib):
-    """Past the decode band: chunks for up to 16 tokens of small experts, the
+    """Past the decode band: chunks for up to 12 tokens of small experts, the
     mid band's GEMMs while the experts average at most 16 routed rows, the
     prefill band's beyond; the switch overrides the rule."""
     c = _capi
     e512, e288, e256, e128 = (512, 2560, 320, 10), (288, 4096, 512, 10), (256, 7168, 2048, 8), (128, 4096, 1536, 8)
-    assert [c.moe_fp4_debug_mid_band_of(M, *e512) for M in (1, 8, 9, 16, 17, 819, 820)] == [0, 0, 2, 2, 3, 3, 1]
+    assert [c.moe_fp4_debug_mid_band_of(M, *e512) for M in (1, 8, 9, 12, 13, 819, 820)] == [0, 0, 2, 2, 3, 3, 1]
     assert [c.moe_fp4_debug_mid_band_of(M, *e256) for M in (9, 512, 513)] == [3, 3, 1]
     assert [c.moe_fp4_debug_mid_band_of(M, *e128) for M in (9, 256, 257, 4096)] == [3, 3, 1, 1]
     assert c.moe_fp4_debug_mid_band_of(12, *e288) == 2

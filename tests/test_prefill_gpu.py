@@ -44,7 +44,7 @@ def _capi():
     return c
 
 
-@pytest.mark.parametrize("M,E,k", [(16, 8, 2), (300, 16, 4), (1000, 64, 8), (4096, 128, 8)])
+@pytest.mark.parametrize("M,E,k", [(16, 8, 2), (300, 16, 4), (1000, 64, 8), (600, 512, 10), (4096, 128, 8)])
 def test_route_bit_exact(M, E, k):
     rng = np.random.default_rng(M + E)
     ids = rng.integers(0, E, (M, k)).astype(np.int32)
@@ -67,6 +67,21 @@ def test_route_bit_exact(M, E, k):
     n = int(want_off[-1])
     got = perm.cpu().numpy()
     assert np.array_equal(got[:n], want_perm)
+    assert np.all(got[n:] == -1)
+    if M * k > 8192:
+        return
+    # the single-CTA routing of small batches: the same offsets, and per
+    # expert the same entries (in the order they won the expert's counter)
+    perm.fill_(-7)
+    off.fill_(-7)
+    c.moe_fp4_debug_route_small(tids.data_ptr(), M, E, k, perm.data_ptr(), off.data_ptr(), ws.data_ptr(), nws,
+                                torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert np.array_equal(off.cpu().numpy(), want_off)
+    got = perm.cpu().numpy()
+    for e in range(E):
+        a, b = int(want_off[e]), int(want_off[e + 1])
+        assert np.array_equal(np.sort(got[a:b]), np.sort(want_perm[a:b])), e
     assert np.all(got[n:] == -1)
 
 
