@@ -200,8 +200,10 @@ __device__ __forceinline__ void gemm_f16w4_persistent(const CUtensorMap* map_a, 
       const uint32_t acc = tmem + (uint32_t)(ab * BN);
       for (int s = 0; s < nk; ++s, ++g) {
         const int slot = g % S, round = g / S, bs = g % SB, bround = g / SB;
-        bool w = mbar_wait(&full[slot], round & 1, err, 2u);
-        w = w && mbar_wait(&bready[bs], bround & 1, err, 2u);
+        // the decode warps arrive on bready only after they saw the stage's
+        // TMA complete (full), so bready alone orders the MMAs after both
+        (void)round;
+        const bool w = mbar_wait(&bready[bs], bround & 1, err, 2u);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;

@@ -35,6 +35,25 @@
 
 namespace moe_fp4 {
 
+// The four K = 64 MMAs of a full 256-K stage from one elected lane of a
+// converged warp: A and B descriptors advance by 2 units (32 bytes), the
+// scale columns by 4 (A) and sfb_step (B); the first accumulates iff
+// `accumulate` (the others always).
+__device__ __forceinline__ void mma_nvf4_warp_x4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t sfa, uint32_t sfb, uint32_t sfb_step, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q, e;\n\tsetp.ne.u32 p, %16, 0;\n\tsetp.eq.u32 q, %16, %16;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %5, %9, [%10], [%13], p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %2, %6, %9, [%11], [%14], q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %3, %7, %9, [%12], [%15], q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %4, %8, %9, [%17], [%18], q;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(a_desc + 2), "l"(a_desc + 4), "l"(a_desc + 6), "l"(b_desc), "l"(b_desc + 2),
+        "l"(b_desc + 4), "l"(b_desc + 6), "r"(idesc), "r"(sfa), "r"(sfa + 4), "r"(sfa + 8), "r"(sfb),
+        "r"(sfb + sfb_step), "r"(sfb + 2 * sfb_step), "r"(accumulate ? 1u : 0u), "r"(sfa + 12), "r"(sfb + 3 * sfb_step)
+      : "memory");
+}
+
 constexpr int kGemmBM = 128;
 constexpr int kGemmBN = 256;  // the default tile width (FC1, test GEMM)
 constexpr int kGemmBK = 256;  // K elements per stage (128 bytes per row)
@@ -191,9 +210,13 @@ __device__ __forceinline__ void gemm_fp4_persistent(const CUtensorMap* map_a, co
         const uint64_t da = smem_desc(smem_u32(stage_a(slot)), 16, 1024, kLayoutSW128);
         const uint64_t db = smem_desc(smem_u32(stage_b(slot)), 16, 1024, kLayoutSW128);
         const int ng = groups(s);
-        for (int k = 0; k < ng; ++k)  // K step of 64 = 32 bytes = 2 descriptor units
-          mma_nvf4_warp(acc, da + 2 * k, db + 2 * k, idesc, sf_a + 4 * k, sf_b + 4 * (BN / 128) * k,
-                        s > 0 || k > 0);
+        if (ng == 4) {
+          mma_nvf4_warp_x4(acc, da, db, idesc, sf_a, sf_b, 4 * (BN / 128), s > 0);
+        } else {
+          for (int k = 0; k < ng; ++k)  // K step of 64 = 32 bytes = 2 descriptor units
+            mma_nvf4_warp(acc, da + 2 * k, db + 2 * k, idesc, sf_a + 4 * k, sf_b + 4 * (BN / 128) * k,
+                          s > 0 || k > 0);
+        }
         mma_commit_warp(&empty[slot]);
       }
       if (ok) mma_commit_warp(&done[ab]);

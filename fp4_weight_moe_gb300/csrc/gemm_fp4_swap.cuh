@@ -31,6 +31,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "gemm_fp4.cuh"
 #include "tcgen05.cuh"
 
 namespace moe_fp4 {
@@ -197,8 +198,12 @@ __device__ __forceinline__ void gemm_fp4_swap_persistent(const CUtensorMap* map_
           const uint64_t da = smem_desc(smem_u32(stage_a(slot)), 16, 1024, kLayoutSW128);
           const uint64_t db = smem_desc(smem_u32(stage_b(slot)), 16, 1024, kLayoutSW128);
           const int ng = groups(s);
-          for (int k = 0; k < ng; ++k)  // K step of 64 = 32 bytes = 2 descriptor units
-            mma_nvf4_warp(acc, da + 2 * k, db + 2 * k, idesc, sf_a + 4 * k, sf_a + 16 + 4 * k, s > 0 || k > 0);
+          if (ng == 4) {
+            mma_nvf4_warp_x4(acc, da, db, idesc, sf_a, sf_a + 16, 4, s > 0);
+          } else {
+            for (int k = 0; k < ng; ++k)  // K step of 64 = 32 bytes = 2 descriptor units
+              mma_nvf4_warp(acc, da + 2 * k, db + 2 * k, idesc, sf_a + 4 * k, sf_a + 16 + 4 * k, s > 0 || k > 0);
+          }
           mma_commit_warp(&empty[slot]);
         }
       }

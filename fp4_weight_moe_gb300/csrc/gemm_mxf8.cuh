@@ -203,8 +203,9 @@ __device__ __forceinline__ void gemm_mxf8_persistent(const CUtensorMap* map_a, c
       const uint32_t acc = tmem + (uint32_t)(ab * BN);
       for (int s = 0; s < nk; ++s, ++g) {
         const int slot = g % S, round = g / S;
-        bool w = mbar_wait(&full[slot], round & 1, err, 2u);
-        w = w && mbar_wait(&sfready[slot], round & 1, err, 2u);
+        // the scale warps arrive on sfready only after they saw the stage's
+        // TMA complete (full), so sfready alone orders the MMAs after both
+        const bool w = mbar_wait(&sfready[slot], round & 1, err, 2u);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
