@@ -292,6 +292,8 @@ COS_MIN, MAXABS_REL_RMS = 0.99995, 2e-2  # the parity bound of the layer output 
 # against the oracle before it is timed.  (label, workload, overrides)
 SWEEP = [("C0", "tiny_decode", {}),
          ("C1/M=8", "decode_e512", dict(M=8)),
+         # the C1 expert shape past the decode band: the mid band's GEMMs
+         ("C1/M=64", "decode_e512", dict(M=64)),
          ("C2", "decode_e288_m4", {})] + \
     [(f"C3/M={M}/{f}", "decode_e256", dict(M=M, fmt=fmt)) for fmt, f in ((0, "mxfp4"), (1, "nvfp4"))
      for M in (1, 2, 4, 8)] + \
