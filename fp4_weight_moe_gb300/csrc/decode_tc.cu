@@ -626,9 +626,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
     const uint32_t idesc = idesc_mxf4nvf4(128, N, false);
     for (int i = mw; i < n_items; i += kMmaWarps) {
       const int sl = i % kRing, round = i / kRing;
-      bool ok = mbar_wait(&S.fullA[sl], round & 1, a.status, 2u);
-      ok = ok && mbar_wait(&S.sfa[sl], round & 1, a.status, 2u);
-      ok = ok && mbar_wait(&S.fullB[sl], round & 1, a.status, 2u);
+      // the scale writers arrive on sfa only after they saw the item's
+      // weight tile (and, from a pre-pass image, its activation terms) land
+      bool ok = mbar_wait(&S.sfa[sl], round & 1, a.status, 2u);
+      if (!use_img) ok = ok && mbar_wait(&S.fullB[sl], round & 1, a.status, 2u);
       ok = ok && (round == 0 || mbar_wait(&S.acce[sl], (round - 1) & 1, a.status, 2u));
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
