@@ -40,14 +40,20 @@ constexpr int kSwapMaxN = 32;                    // B rows per tile at most
 constexpr int kSwapSubs = 128 / kSwapMaxN;       // weight tiles per tile at most
 constexpr int kSwapThreads = 320;
 
+// A stage is 512 K: two 128-byte-wide boxes per operand (each 256 K, 128-byte
+// swizzle) and eight 64-K scale groups, so that the MMA warp's per-stage cost
+// (barrier wait, fence, commit) is paid once per eight MMAs.
 struct SwapCfg {
-  static constexpr uint32_t kStageA = 128 * 128;                     // 16 KB
-  static constexpr uint32_t kStageB = kSwapMaxN * 128;               // 4 KB
-  static constexpr uint32_t kStageSF = 4 * kChunkBytes;              // 2 KB (A), 2 KB (B)
+  static constexpr int kStageK = 512;
+  static constexpr uint32_t kBoxA = 128 * 128;                       // 16 KB: 128 rows x 256 K
+  static constexpr uint32_t kBoxB = kSwapMaxN * 128;                 // 4 KB: up to 32 rows x 256 K
+  static constexpr uint32_t kStageA = 2 * kBoxA;
+  static constexpr uint32_t kStageB = 2 * kBoxB;
+  static constexpr uint32_t kStageSF = 8 * kChunkBytes;              // 4 KB (A), 4 KB (B)
   static constexpr uint32_t kStageBytes = kStageA + kStageB + 2 * kStageSF;
-  static constexpr int kStages = 8;
+  static constexpr int kStages = 4;
   static constexpr uint32_t kTmemSF = 2 * 128;                       // after two accumulators
-  static constexpr uint32_t kSFPerSlot = 32;                         // 16 A + 16 B columns
+  static constexpr uint32_t kSFPerSlot = 64;                         // 32 A + 32 B columns
   static constexpr uint32_t kExtra = 18 * 1024;                      // epilogue exchange area
   static constexpr uint32_t kSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/ + kExtra;
   static_assert(kStageBytes % 1024 == 0, "swizzled stages stay 1024-byte aligned");
@@ -102,8 +108,8 @@ __device__ __forceinline__ void gemm_fp4_swap_persistent(const CUtensorMap* map_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if ((int)blockIdx.x >= n_tiles || !tile_of((int)blockIdx.x).valid) return;
-  const int nk = (K + 255) / 256;
-  auto groups = [&](int s) { return s + 1 < nk ? 4 : K / 64 - 4 * (nk - 1); };
+  const int nk = (K + Cfg::kStageK - 1) / Cfg::kStageK;
+  auto groups = [&](int s) { return s + 1 < nk ? 8 : K / 64 - 8 * (nk - 1); };  // 64-K groups of stage s
   // the tile after idx for this CTA (invalid past the end); its loads are in
   // flight while the current tile is processed
   auto next_of = [&](int idx) {
@@ -157,12 +163,16 @@ __device__ __forceinline__ void gemm_fp4_swap_persistent(const CUtensorMap* map_
               ok = false;
               break;
             }
-            const uint32_t sfb = (uint32_t)groups(s) * kChunkBytes;
-            mbar_arrive_expect_tx(&full[slot], Cfg::kStageA + (uint32_t)t.n_rows * 128 + 2 * sfb);
-            tma_load_2d(stage_a(slot), map_a, s * 128, t.a_row0 + 128 * j, &full[slot]);
-            tma_load_2d(stage_b(slot), mb, s * 128, t.b_row0, &full[slot]);
-            bulk_load(stage_sfa(slot), t.a_sf + j * t.a_sf_step + (size_t)(4 * s) * kChunkBytes, sfb, &full[slot]);
-            bulk_load(stage_sfb(slot), t.b_sf + (size_t)(4 * s) * kChunkBytes, sfb, &full[slot]);
+            const int ng = groups(s);
+            const uint32_t sfb = (uint32_t)ng * kChunkBytes, boxes = ng > 4 ? 2u : 1u;
+            mbar_arrive_expect_tx(&full[slot], boxes * (Cfg::kBoxA + (uint32_t)t.n_rows * 128) + 2 * sfb);
+            for (uint32_t h = 0; h < boxes; ++h) {
+              tma_load_2d(stage_a(slot) + h * Cfg::kBoxA, map_a, s * 256 + (int)h * 128, t.a_row0 + 128 * j,
+                          &full[slot]);
+              tma_load_2d(stage_b(slot) + h * Cfg::kBoxB, mb, s * 256 + (int)h * 128, t.b_row0, &full[slot]);
+            }
+            bulk_load(stage_sfa(slot), t.a_sf + j * t.a_sf_step + (size_t)(8 * s) * kChunkBytes, sfb, &full[slot]);
+            bulk_load(stage_sfb(slot), t.b_sf + (size_t)(8 * s) * kChunkBytes, sfb, &full[slot]);
           }
         }
         t = tn;
@@ -194,15 +204,24 @@ __device__ __forceinline__ void gemm_fp4_swap_persistent(const CUtensorMap* map_
             break;
           }
           tc_fence_after();
-          const uint32_t sf_a = tmem + Cfg::kTmemSF + slot * Cfg::kSFPerSlot;
-          const uint64_t da = smem_desc(smem_u32(stage_a(slot)), 16, 1024, kLayoutSW128);
-          const uint64_t db = smem_desc(smem_u32(stage_b(slot)), 16, 1024, kLayoutSW128);
+          // scale columns: A's group k at 4k, B's at 32 + 4k; boxes h = 0, 1
+          // hold groups 0-3 and 4-7 (K step of 64 = 32 bytes = 2 descriptor
+          // units within a box)
+          const uint32_t sf_a = tmem + Cfg::kTmemSF + slot * Cfg::kSFPerSlot, sf_b = sf_a + 32;
           const int ng = groups(s);
-          if (ng == 4) {
-            mma_nvf4_warp_x4(acc, da, db, idesc, sf_a, sf_a + 16, 4, s > 0);
-          } else {
-            for (int k = 0; k < ng; ++k)  // K step of 64 = 32 bytes = 2 descriptor units
-              mma_nvf4_warp(acc, da + 2 * k, db + 2 * k, idesc, sf_a + 4 * k, sf_a + 16 + 4 * k, s > 0 || k > 0);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int k0 = 4 * h;
+            if (ng <= k0) break;
+            const uint64_t da = smem_desc(smem_u32(stage_a(slot) + h * Cfg::kBoxA), 16, 1024, kLayoutSW128);
+            const uint64_t db = smem_desc(smem_u32(stage_b(slot) + h * Cfg::kBoxB), 16, 1024, kLayoutSW128);
+            if (ng >= k0 + 4) {
+              mma_nvf4_warp_x4(acc, da, db, idesc, sf_a + 4 * k0, sf_b + 4 * k0, 4, s > 0 || h > 0);
+            } else {
+              for (int k = k0; k < ng; ++k)
+                mma_nvf4_warp(acc, da + 2 * (k - k0), db + 2 * (k - k0), idesc, sf_a + 4 * k, sf_b + 4 * k,
+                              s > 0 || k > 0);
+            }
           }
           mma_commit_warp(&empty[slot]);
         }
@@ -226,24 +245,29 @@ __device__ __forceinline__ void gemm_fp4_swap_persistent(const CUtensorMap* map_
           ok = false;
           break;
         }
-        uint32_t r[16], rb[16];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint4 u = *reinterpret_cast<const uint4*>(stage_sfa(slot) + k * kChunkBytes + lane * 16);
-          r[4 * k] = u.x;
-          r[4 * k + 1] = u.y;
-          r[4 * k + 2] = u.z;
-          r[4 * k + 3] = u.w;
-          // B row l of the tile is row 32 b_word + l of the chunk: lane l's
-          // word b_word, into the first column of the K group
-          rb[4 * k] = *reinterpret_cast<const uint32_t*>(stage_sfb(slot) + k * kChunkBytes + lane * 16 + 4 * t.b_word);
-          rb[4 * k + 1] = 0u;
-          rb[4 * k + 2] = 0u;
-          rb[4 * k + 3] = 0u;
-        }
         const uint32_t col = tmem + lane_base + Cfg::kTmemSF + slot * Cfg::kSFPerSlot;
-        tmem_st16(col, r);
-        tmem_st16(col + 16, rb);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // K groups 4h .. 4h + 3
+          uint32_t r[16], rb[16];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint8_t* ca = stage_sfa(slot) + (4 * h + k) * kChunkBytes;
+            const uint4 u = *reinterpret_cast<const uint4*>(ca + lane * 16);
+            r[4 * k] = u.x;
+            r[4 * k + 1] = u.y;
+            r[4 * k + 2] = u.z;
+            r[4 * k + 3] = u.w;
+            // B row l of the tile is row 32 b_word + l of the chunk: lane l's
+            // word b_word, into the first column of the K group
+            const uint8_t* cb = stage_sfb(slot) + (4 * h + k) * kChunkBytes;
+            rb[4 * k] = *reinterpret_cast<const uint32_t*>(cb + lane * 16 + 4 * t.b_word);
+            rb[4 * k + 1] = 0u;
+            rb[4 * k + 2] = 0u;
+            rb[4 * k + 3] = 0u;
+          }
+          tmem_st16(col + 16 * h, r);
+          tmem_st16(col + 32 + 16 * h, rb);
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();

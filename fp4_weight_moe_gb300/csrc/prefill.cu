@@ -1983,10 +1983,10 @@ static cudaError_t launch_prefill_mid(PrefillArgs& a, const PrefillCarve& c, con
   if (e != cudaSuccess) return e;
   // persistent, one CTA per SM; tiles: (32-row routing tile, group of up to
   // four weight tiles)
-  // weight tiles per item: enough for about eight K stages between
-  // accumulator hand-offs (FC2's K = I is often one or two stages)
+  // weight tiles per item: enough for about four 512-K stages between
+  // accumulator hand-offs (FC2's K = I is often one stage)
   auto subs_for = [](int K) {
-    const int nk = (K + 255) / 256, sb = (8 + nk - 1) / nk;
+    const int nk = (K + SwapCfg::kStageK - 1) / SwapCfg::kStageK, sb = (4 + nk - 1) / nk;
     return sb < kSwapSubs ? sb : kSwapSubs;
   };
   const int s1 = subs_for(H) < kFc1SwapSubs ? subs_for(H) : kFc1SwapSubs, s2 = subs_for(I);
