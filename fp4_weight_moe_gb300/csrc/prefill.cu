@@ -921,8 +921,7 @@ struct BMaps {
 };
 constexpr int kMidPad = 32;  // the mid band's routing-tile height
 constexpr int kFc1SwapSubs = 2;  // FC1's weight tiles per item at most (the gate/up exchange area)
-static_assert(kFc1SwapSubs * 32 * 64 * 4 + 16 <= SwapCfg::kExtra && 4 * (32 * 33 + 32) * 4 <= SwapCfg::kExtra,
-              "epilogue exchange area");
+static_assert(kFc1SwapSubs * 32 * 64 * 4 + 16 <= SwapCfg::kExtra, "epilogue exchange area");
 
 // Per-routing-tile values of the epilogues, fetched by each epilogue thread
 // for its next tile while it finishes the current one (lane j: column j).
@@ -1053,9 +1052,7 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
 
 // FC2: D[w2 row][routed row]; each lane owns an output column and reduces its
 // routed rows' products, times the rows' factors (hG, with the down
-// multiplier and router weight folded in), into the FP32 token accumulator;
-// the values go through shared memory so that a lane reduces four
-// consecutive outputs of one token at a time (red.v4).
+// multiplier and router weight folded in), into the FP32 token accumulator.
 __global__ void __launch_bounds__(kSwapThreads, 1)
     fc2_swap_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ BMaps maps_h, PrefillArgs a,
                     int subs) {
@@ -1096,32 +1093,47 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
   // the epilogue warps fetch their first tile's values while its stages stream
   MidCols cur, pf;
   if (threadIdx.x >= 192 && (int)blockIdx.x < n_mt * NG) pf = fetch((int)blockIdx.x / NG);
-  // per epilogue warp: 32 routed rows x its 32 output columns
-  float* stg = reinterpret_cast<float*>(swap_extra_smem()) + (threadIdx.x / 32 % 4) * (32 * 33 + 32);
-  int* stg_tok = reinterpret_cast<int*>(stg + 32 * 33);
+  // one red.add per (output row, routed row): a warp's 32 lanes reduce 32
+  // consecutive outputs of one token; the tile's accumulator columns come
+  // out of tensor memory 64 at a time under one wait
   auto epi = [&](uint32_t tmem_row, int row, const SwapTile& t) {
     cur = pf.mt == t.m_tile ? pf : fetch(t.m_tile);
     const int next = t.m_tile * NG + t.group + (int)gridDim.x;
     if (next < n_mt * NG && next / NG != t.m_tile) pf = fetch(next / NG);
-    const int nv = cur.nv, N = t.n_rows;
-    if (lane < nv) stg_tok[lane] = cur.src / a.top_k;
+    const int nv = cur.nv, N = t.n_rows, tok = cur.src / a.top_k;
+    float* out0 = a.acc + 128 * (subs * t.group) + row;
+    // sub-tile j's column c: value v, token and factor of routed row c
+    auto put = [&](int j, int c, uint32_t v) {
+      const int tc = __shfl_sync(0xffffffffu, tok, c);
+      const float fc = __shfl_sync(0xffffffffu, cur.v, c);
+      asm volatile("red.global.add.f32 [%0], %1;" ::"l"(out0 + (size_t)tc * a.H + 128 * j), "f"(__uint_as_float(v) * fc)
+                   : "memory");
+    };
 #pragma unroll 1
-    for (int j = 0; j < t.subs; ++j) {
-      uint32_t v[32];
-      tmem_ld32(tmem_row + j * N, v);
+    for (int j0 = 0; j0 < t.subs; j0 += 64 / N) {  // 64 accumulator columns per round
+      uint32_t v0[32], v1[32];
+      swap_tmem_ld32(tmem_row + j0 * N, v0);
+      swap_tmem_ld32(tmem_row + j0 * N + 32, v1);
+      swap_tmem_ld_wait();
+      if (N == 16) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        if (c < nv) stg[c * 33 + lane] = __uint_as_float(v[c]) * __shfl_sync(0xffffffffu, cur.v, c);
-      __syncwarp();
-      float* out0 = a.acc + 128 * (subs * t.group + j) + (row & ~31);
-      for (int p = lane; p < nv * 8; p += 32) {
-        const int c = p >> 3, q = p & 7;
-        const float* sv = stg + c * 33 + 4 * q;
-        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(out0 + (size_t)stg_tok[c] * a.H + 4 * q),
-                     "f"(sv[0]), "f"(sv[1]), "f"(sv[2]), "f"(sv[3])
-                     : "memory");
+        for (int c = 0; c < 16; ++c) {
+          if (c < nv) {  // (warp-uniform)
+            put(j0, c, v0[c]);
+            if (j0 + 1 < t.subs) put(j0 + 1, c, v0[16 + c]);
+            if (j0 + 2 < t.subs) put(j0 + 2, c, v1[c]);
+            if (j0 + 3 < t.subs) put(j0 + 3, c, v1[16 + c]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          if (c < nv) {  // (warp-uniform)
+            put(j0, c, v0[c]);
+            if (j0 + 1 < t.subs) put(j0 + 1, c, v1[c]);
+          }
+        }
       }
-      __syncwarp();
     }
   };
   gemm_fp4_swap_persistent(&map_w, &maps_h.m[0], a.I, a.status, n_mt * NG, tile_of, epi);
