@@ -760,6 +760,21 @@ __global__ void quant_h_routed_kernel(PrefillArgs a) {
 }
 
 // ---------------------------------------------------------------- GEMMs
+// 16 lanes x 256 bits of tensor memory, eight times along the columns (64
+// FP32 columns): thread t holds, per 8-column block q, columns 2 (t % 4) and
+// 2 (t % 4) + 1 of lanes t / 4 (registers 4q, 4q + 1) and t / 4 + 8 (4q + 2,
+// 4q + 3) of the 16 lanes at the address's lane field.
+__device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
 // FC2's tile width.  128 (two accumulators, the reduction epilogue beside
 // the next tile's MMAs) measured slower on GB300 than 256 (FC2 327 vs 300 us
 // on prefill_e128): the narrower tiles stage a third more bytes per FLOP.
@@ -884,24 +899,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     t.b_sf1 = t.b_sf0 + (size_t)KG * kChunkBytes;
     return t;
   };
+  // The accumulator leaves tensor memory in the 16-lane x 256-bit shape: a
+  // thread holds two consecutive columns of rows g and g + 8 of a 16-row half
+  // (g = lane / 4, the columns 2 (lane % 4) + {0, 1} of each 8-column block),
+  // so that a warp's reductions cover 8 rows x 32 contiguous bytes (whole
+  // sectors) instead of 32 rows x 16 bytes.
+  const int lane = threadIdx.x & 31;
   auto epi = [&](uint32_t tmem_row, int row, const GemmTile& t) {
     const int r = t.a_row0 + row;
     const int e = a.tile_expert[t.m_tile];
     const int src = a.row_src[r];
     const float f = src >= 0 ? a.hG[r] * g2[e] * a.tw[src] : 0.f;
-    float* dst = a.acc + (size_t)(src >= 0 ? src / a.top_k : 0) * a.H + kFc2BN * t.n_tile;
+    const int tok = src >= 0 ? src / a.top_k : -1;
+    float* out = a.acc + kFc2BN * t.n_tile + 2 * (lane & 3);
+    const uint32_t tbase = tmem_row;  // (its lane field: this warp's 32 lanes)
 #pragma unroll 1
-    for (int c = 0; c < kFc2BN / 32; ++c) {
-      uint32_t v[32];
-      tmem_ld32(tmem_row + 32 * c, v);
-      if (src >= 0) {
+    for (int hf = 0; hf < 2; ++hf) {  // 16-lane halves of the warp's 32 rows
+      const int ra = 16 * hf + (lane >> 2), rb = ra + 8;  // this thread's two rows (within the 32)
+      const int ta = __shfl_sync(0xffffffffu, tok, ra), tb = __shfl_sync(0xffffffffu, tok, rb);
+      const float fa = __shfl_sync(0xffffffffu, f, ra), fb = __shfl_sync(0xffffffffu, f, rb);
+#pragma unroll 1
+      for (int c = 0; c < kFc2BN / 64; ++c) {  // 64 columns per load
+        uint32_t v[32];
+        tmem_ld_16x256b_x8(tbase + ((uint32_t)(16 * hf) << 16) + 64 * c, v);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float* p = dst + 32 * c + 4 * i;
-          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p),
-                       "f"(__uint_as_float(v[4 * i]) * f), "f"(__uint_as_float(v[4 * i + 1]) * f),
-                       "f"(__uint_as_float(v[4 * i + 2]) * f), "f"(__uint_as_float(v[4 * i + 3]) * f)
-                       : "memory");
+        for (int q = 0; q < 8; ++q) {
+          const int col = 64 * c + 8 * q;
+          if (ta >= 0)
+            asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(out + (size_t)ta * a.H + col),
+                         "f"(__uint_as_float(v[4 * q]) * fa), "f"(__uint_as_float(v[4 * q + 1]) * fa)
+                         : "memory");
+          if (tb >= 0)
+            asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(out + (size_t)tb * a.H + col),
+                         "f"(__uint_as_float(v[4 * q + 2]) * fb), "f"(__uint_as_float(v[4 * q + 3]) * fb)
+                         : "memory");
         }
       }
     }
@@ -2081,7 +2112,8 @@ cudaError_t launch_prefill(const void* x, const void* w13, const void* s13, cons
                  mw13, a);
   if (e == cudaSuccess) e = launch_pdl(quant_h_kernel, (unsigned)((rows + 7) / 8), 256u, 0, st, a);
   if (e == cudaSuccess)
-    e = launch_pdl(fc2_gemm_kernel, (unsigned)(g2 < sms ? g2 : sms), kGemmThreads, GemmCfg<kFc2BN>::kSmem, st, mh,
+    e = launch_pdl(fc2_gemm_kernel, (unsigned)(g2 < sms ? g2 : sms), kGemmThreads, GemmCfg<kFc2BN>::kSmem,
+                   st, mh,
                    mw2, a);
   if (e == cudaSuccess) e = launch_pdl(cast_out_kernel, 4u * 152u, 256u, 0, st, a);
   return e;
