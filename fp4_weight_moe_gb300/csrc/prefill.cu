@@ -793,6 +793,7 @@ __device__ __forceinline__ void reduce_rows_to_tokens(uint32_t tmem_row, float f
     const int ra = 16 * hf + (lane >> 2), rb = ra + 8;  // this thread's two rows
     const int ta = __shfl_sync(0xffffffffu, tok, ra), tb = __shfl_sync(0xffffffffu, tok, rb);
     const float fa = __shfl_sync(0xffffffffu, f, ra), fb = __shfl_sync(0xffffffffu, f, rb);
+    if (!__any_sync(0xffffffffu, ta >= 0 || tb >= 0)) continue;  // a half of padding rows (small batches)
 #pragma unroll 1
     for (int c = 0; c < BN / 64; ++c) {  // 64 columns per load
       uint32_t v[32];
