@@ -84,7 +84,13 @@ def test_int64_ids_through_chunks():
 @pytest.mark.parametrize("name,ov", [("decode_e512", dict(M=64)), ("decode_e512", dict(E=64, M=200)),
                                      ("decode_e288_m4", dict(E=96, M=40)),
                                      ("decode_e256", dict(E=16, H=2048, I=1024, M=24)),
-                                     ("tiny_decode", dict(M=700, E=8, top_k=2))])
+                                     ("tiny_decode", dict(M=700, E=8, top_k=2)),
+                                     # the smallest K of both GEMMs (H = 256: one stage without its second
+                                     # box; I = 64: one scale group)
+                                     ("tiny_decode", dict(M=40, E=3, H=256, I=64, top_k=2)),
+                                     # every expert on every token, past the one-kernel routing's 8192
+                                     # entries (the three-kernel routing with 32-row tiles)
+                                     ("tiny_decode", dict(M=600, E=16, H=512, I=192, top_k=16))])
 def test_mid_band_swapped_gemms_parity(name, ov):
     wl = gen.make_workload(name, device="cuda", **ov)
     got = _run(wl, MID)
