@@ -6,21 +6,24 @@
 // Batches of 9 to a few hundred tokens route a handful of rows to each
 // expert.  With the routed rows on the 128-row side (the prefill engine,
 // gemm_fp4.cuh) every weight stage travels beside 16 KB of mostly padding
-// activation rows; here a stage is one 16 KB weight tile slice plus 2 or 4 KB
-// of activations.  Short expert dimensions (FC2's K = I = 320 is two stages)
-// would leave a work item with too little to stream per accumulator
-// hand-off, so a work item ("tile") multiplies one B tile (the <= 32 routed
-// rows of a 32-row routing tile) with `subs` (<= kSwapSubs) consecutive
-// 128-row weight tiles: weight tile j accumulates into columns [j N, j N + N)
-// of one 128-column accumulator, and the epilogue runs once for all of them.
+// activation rows; here a 256-K slice of a weight tile (16 KB) travels with 2
+// or 4 KB of activations.  Short expert dimensions (FC2's K = I = 320 is one
+// 512-K stage) would leave a work item with too little to stream per
+// accumulator hand-off, so a work item ("tile") multiplies one B tile (the
+// <= 32 routed rows of a 32-row routing tile) with `subs` (<= kSwapSubs)
+// consecutive 128-row weight tiles: weight tile j accumulates into columns
+// [j N, j N + N) of one 128-column accumulator, and the epilogue runs once for
+// all of them.
 //
 // Persistent CTA (one per SM), ten warps as in the prefill engine:
-//   warp 0 lane 0  TMA producer: per (weight tile j, K stage) a 128 x 128 B
-//                  weight box, the N x 128 B activation box (SWIZZLE_128B),
-//                  and the two 512 B-per-K-group scale chunk sets, into an
-//                  8-slot ring;
-//   warp 1         tensor-memory allocation and, converged, the MMAs (four
-//                  K = 64 per full stage) and the commits;
+//   warp 0 lane 0  TMA producer: per (weight tile j, 512-K stage) two
+//                  128 x 128 B weight boxes, two N x 128 B activation boxes
+//                  (SWIZZLE_128B; the second pair only where the stage
+//                  reaches past 256 K) and the two operands' scale chunks
+//                  (512 B per 64-K group), into a 4-slot ring;
+//   warp 1         tensor-memory allocation and, converged, the MMAs (eight
+//                  K = 64 per full stage, four from one elected lane at a
+//                  time) and the commits;
 //   warps 2-5      scale chunks -> tensor memory (tcgen05.st, each warp its
 //                  lane quarter); B's 32 rows sit in one 4-byte word of each
 //                  lane's 16 bytes of a 128-row chunk (word b_word), which
