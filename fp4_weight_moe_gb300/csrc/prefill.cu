@@ -1,8 +1,13 @@
 // The prefill bands (batches past the decode band): routing compaction
-// (count, scan, stable scatter into 128-row tiles per expert), then one of
-// three launch chains over the same routed rows and FP32 token accumulator:
+// (count, scan, stable scatter into routing tiles per expert; one kernel for
+// up to 8192 routing entries), then one of four launch chains over the same
+// routed rows and FP32 token accumulator:
 //   NVFP4 activations  x and h quantised to NVFP4, both GEMMs on the FP4
-//                      tensor cores (gemm_fp4.cuh, kind::mxf4nvf4);
+//                      tensor cores (gemm_fp4.cuh, kind::mxf4nvf4), routed
+//                      rows on the MMA's 128-row side;
+//   mid band           the same layer with the operands swapped for experts
+//                      with few routed rows (gemm_fp4_swap.cuh: weights on the
+//                      128-row side, 32-row routing tiles on N);
 //   exact BF16         x and h carried exactly in row-scaled FP16, the FP4
 //                      weights decoded to FP16 in shared memory (gemm_f16w4.cuh);
 //   W4A8-MX            x and h quantised to MXFP8, both GEMMs on the FP8 tensor
@@ -237,8 +242,9 @@ cudaError_t launch_debug_gemm(const void* a_q, const void* a_sf, const void* b_q
 //   G = amax/(6*448) (1 if the row is zero), s = e4m3_rn_satfinite(bmax/(6G)),
 //   q = e2m1_rn_satfinite(a/(s*G)) (0 where s*G == 0),
 // every step an IEEE FP32 operation; h is staged in BF16 between FC1 and its
-// quantiser.  Each expert's routed rows are padded to a multiple of 128 so an
-// MMA tile never straddles two experts.
+// quantiser.  Each expert's routed rows are padded to a multiple of the
+// routing-tile height (128; 32 in the mid band) so a tile never straddles two
+// experts.
 // ============================================================================
 
 size_t decode_sync_bytes(int H, int I, int top_k);
