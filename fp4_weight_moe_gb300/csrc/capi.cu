@@ -376,10 +376,10 @@ bool mid_band_chunks(int M, int H, int I) {
 // average at most kMidBandMaxRows routed rows, where the prefill tiles would
 // stage mostly padding rows of activations.  Measured on GB300 (us per layer,
 // prefill / mid band): E=512 H=2560 I=320 k=10: M=64 196.9 / 127.4, 256
-// 255.5 / 164.8, 1024 310.9 / 227.2; E=288 H=4096 I=512 k=10: M=64 266.5 /
-// 178.5; E=128 H=4096 I=1536 k=8: M=256 281.2 / 256.9, 512 (32 rows per
-// expert) 308.2 / 294.4, 1024 331.8 / 434.2.
-constexpr int kMidBandMaxRows = 32;
+// 255.5 / 164.8, 1024 (20 rows per expert) 310.9 / 227.2; E=288 H=4096 I=512
+// k=10: M=64 266.5 / 178.5; E=128 H=4096 I=1536 k=8: M=256 281.2 / 256.9,
+// 512 (32 rows per expert) 286.2 / 292.2, 1024 306.6 / 434.2.
+constexpr int kMidBandMaxRows = 24;
 bool mid_band_swap(int M, int E, int top_k) {
   const int mode = g_mid_band.load(std::memory_order_relaxed);
   if (mode == 1 || mode == 3) return mode == 3;

@@ -819,10 +819,12 @@ __device__ __forceinline__ void reduce_rows_to_tokens(uint32_t tmem_row, float f
     }
   }
 }
-// FC2's tile width.  128 (two accumulators, the reduction epilogue beside
-// the next tile's MMAs) measured slower on GB300 than 256 (FC2 327 vs 300 us
-// on prefill_e128): the narrower tiles stage a third more bytes per FLOP.
-constexpr int kFc2BN = 256;
+// FC2's tile width: 128, two accumulators, so that a tile's reduction
+// epilogue runs beside the next tile's MMAs.  Measured on GB300 at
+// prefill_e128 (us per layer, 128 / 256): 672 / 685 with the reductions in
+// whole sectors; with the earlier row-wise reductions 256 was ahead (737 /
+// 756): the narrower tiles stage a third more bytes per FLOP.
+constexpr int kFc2BN = 128;
 // Tile (m, n) with n fastest, dealt round-robin to one persistent CTA per
 // SM: CTAs sharing an activation tile run together, and the M-tiles of one
 // expert (sharing weight tiles) follow each other.

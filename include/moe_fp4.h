@@ -466,7 +466,7 @@ MOE_FP4_API int moe_fp4_debug_set_decode_family(int family, int *previous);
  *   mode 0  by shape (default): up to 3 * MOE_FP4_DECODE_MAX_M / 2 tokens
  *           the chunks when one expert's weights (3IH/2 nibble bytes) are at
  *           most 8 MiB; otherwise the mid band's GEMMs while the experts
- *           average at most 32 routed rows (M * top_k <= 32 E), else the
+ *           average at most 24 routed rows (M * top_k <= 24 E), else the
  *           prefill band's
  *   mode 1  the prefill band's GEMMs (routed rows on the MMA's 128-row
  *           side)

@@ -180,13 +180,13 @@ def test_band_policy_by_shape(lib):
 
 def test_mid_band_plan_by_shape(lib):
     """Past the decode band: chunks for up to 12 tokens of small experts, the
-    mid band's GEMMs while the experts average at most 32 routed rows, the
+    mid band's GEMMs while the experts average at most 24 routed rows, the
     prefill band's beyond; the switch overrides the rule."""
     c = _capi
     e512, e288, e256, e128 = (512, 2560, 320, 10), (288, 4096, 512, 10), (256, 7168, 2048, 8), (128, 4096, 1536, 8)
-    assert [c.moe_fp4_debug_mid_band_of(M, *e512) for M in (1, 8, 9, 12, 13, 1638, 1639)] == [0, 0, 2, 2, 3, 3, 1]
-    assert [c.moe_fp4_debug_mid_band_of(M, *e256) for M in (9, 1024, 1025)] == [3, 3, 1]
-    assert [c.moe_fp4_debug_mid_band_of(M, *e128) for M in (9, 512, 513, 4096)] == [3, 3, 1, 1]
+    assert [c.moe_fp4_debug_mid_band_of(M, *e512) for M in (1, 8, 9, 12, 13, 1228, 1229)] == [0, 0, 2, 2, 3, 3, 1]
+    assert [c.moe_fp4_debug_mid_band_of(M, *e256) for M in (9, 768, 769)] == [3, 3, 1]
+    assert [c.moe_fp4_debug_mid_band_of(M, *e128) for M in (9, 384, 385, 4096)] == [3, 3, 1, 1]
     assert c.moe_fp4_debug_mid_band_of(12, *e288) == 2
     assert c.moe_fp4_debug_mid_band_of(9, 512, 2560, 320, 0) == 0  # invalid top_k
     prev = c.moe_fp4_debug_set_mid_band(1)
