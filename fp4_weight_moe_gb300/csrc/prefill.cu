@@ -260,6 +260,12 @@ int g_w4a8_fp8 = 1;
 // accumulators, the epilogue beside the next tile's MMAs) against 1046 with
 // 256-wide ones (one accumulator).
 constexpr int kMxFc1BN = 128;
+// FC2 tile widths of the 16-bit and FP8 bands.  Measured on GB300 at
+// prefill_e128 (us per layer, 256 / 128): exact 1699 / 1970 (the 16-bit
+// engine decodes the weights once per tile: twice as often per FLOP at 128);
+// W4A8-MX 997 / 983 (two accumulators, the reductions beside the MMAs).
+constexpr int kFc2ExactBN = 256;
+constexpr int kMxFc2BN = 128;
 constexpr int kMaxPrefillE = 4096;
 
 struct PrefillArgs {
@@ -1479,7 +1485,7 @@ __global__ void __launch_bounds__(kHwThreads, 1)
                      PrefillArgs a) {
   pdl_wait();               // the previous kernel on the stream is complete and visible
   pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
-  constexpr int BN = 256;
+  constexpr int BN = kFc2ExactBN;
   const int NT = a.H / BN;
   const int KG = a.I / 64;
   const size_t scb = scale_chunk_bytes(a.H, a.I);
@@ -1656,7 +1662,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                   PrefillArgs a) {
   pdl_wait();               // the previous kernel on the stream is complete and visible
   pdl_launch_dependents();  // the next may start its prologue (it waits the same way)
-  constexpr int BN = 256;
+  constexpr int BN = kMxFc2BN;
   const int NT = a.H / BN;
   const int KG = a.I / 64, nst = a.I / 128;
   const size_t scb = scale_chunk_bytes(a.H, a.I);
@@ -1886,11 +1892,11 @@ static cudaError_t launch_prefill_exact(PrefillArgs& a, const PrefillCarve& c, c
   // 128-wide tiles (A, the activations, staged half as often per FLOP).
   constexpr int kFc1Wide = 256;
   const int bn1 = (!relu2 && kFc1Wide == 256 && I % 128 == 0) ? 256 : 128;
-  const int nt1 = relu2 ? (I + 127) / 128 : 2 * I / bn1, nt2 = H / 256;
+  const int nt1 = relu2 ? (I + 127) / 128 : 2 * I / bn1, nt2 = H / kFc2ExactBN;
   CUresult r = make_fp4_map(&mx, a.xb, (uint64_t)H * 2, rows, kHwBM);
   if (r == CUDA_SUCCESS) r = raw_map(&mw13, w13, (uint64_t)H / 2, (uint64_t)E * (relu2 ? I : 2 * I), (uint32_t)bn1);
   if (r == CUDA_SUCCESS) r = make_fp4_map(&mh, a.hbuf, (uint64_t)I * 2, rows, kHwBM);
-  if (r == CUDA_SUCCESS) r = raw_map(&mw2, w2, (uint64_t)I / 2, (uint64_t)E * H, 256);
+  if (r == CUDA_SUCCESS) r = raw_map(&mw2, w2, (uint64_t)I / 2, (uint64_t)E * H, kFc2ExactBN);
   if (r != CUDA_SUCCESS) {
     *cu_err = (int)r;
     return cudaErrorInvalidValue;
@@ -1903,7 +1909,7 @@ static cudaError_t launch_prefill_exact(PrefillArgs& a, const PrefillCarve& c, c
     };
     smem_attr((const void*)fc1_exact_kernel<128>, HwCfg<128>::kSmem);
     smem_attr((const void*)fc1_exact_kernel<256>, HwCfg<256>::kSmem);
-    smem_attr((const void*)fc2_exact_kernel, HwCfg<256>::kSmem);
+    smem_attr((const void*)fc2_exact_kernel, HwCfg<kFc2ExactBN>::kSmem);
     if (e != cudaSuccess) return e;
     attrs = true;
   }
@@ -1921,7 +1927,8 @@ static cudaError_t launch_prefill_exact(PrefillArgs& a, const PrefillCarve& c, c
   else
     e = launch_pdl(fc1_exact_kernel<128>, (unsigned)p1, kHwThreads, HwCfg<128>::kSmem, st, mx, mw13, a);
   if (e == cudaSuccess) e = launch_pdl(stage_h_f16_kernel, (unsigned)(rows / 8), 256u, 0, st, a);
-  if (e == cudaSuccess) e = launch_pdl(fc2_exact_kernel, (unsigned)p2, kHwThreads, HwCfg<256>::kSmem, st, mh, mw2, a);
+  if (e == cudaSuccess)
+    e = launch_pdl(fc2_exact_kernel, (unsigned)p2, kHwThreads, HwCfg<kFc2ExactBN>::kSmem, st, mh, mw2, a);
   if (e == cudaSuccess) e = launch_pdl(cast_out_kernel, 4u * 152u, 256u, 0, st, a);
   return e;
 }
@@ -1944,7 +1951,7 @@ static cudaError_t launch_prefill_mx(PrefillArgs& a, const PrefillCarve& c, cons
   CUresult r = make_fp4_map(&mx, a.xq8, (uint64_t)H, rows, kMxBM);
   if (r == CUDA_SUCCESS) r = make_e2m1_unpacked_map(&mw13, w13, (uint64_t)H, (uint64_t)E * 2 * I, bn1);
   if (r == CUDA_SUCCESS) r = make_fp4_map(&mh, a.hq8, (uint64_t)I, rows, kMxBM);
-  if (r == CUDA_SUCCESS) r = make_e2m1_unpacked_map(&mw2, w2, (uint64_t)I, (uint64_t)E * H, 256);
+  if (r == CUDA_SUCCESS) r = make_e2m1_unpacked_map(&mw2, w2, (uint64_t)I, (uint64_t)E * H, kMxFc2BN);
   if (r != CUDA_SUCCESS) {
     *cu_err = (int)r;
     return cudaErrorInvalidValue;
@@ -1954,7 +1961,7 @@ static cudaError_t launch_prefill_mx(PrefillArgs& a, const PrefillCarve& c, cons
     cudaError_t e =
         cudaFuncSetAttribute(fc1_mx_kernel<bn1>, cudaFuncAttributeMaxDynamicSharedMemorySize, MxCfg<bn1>::kSmem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(fc2_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MxCfg<256>::kSmem);
+      e = cudaFuncSetAttribute(fc2_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MxCfg<kMxFc2BN>::kSmem);
     if (e != cudaSuccess) return e;
     attrs = true;
   }
@@ -1965,10 +1972,11 @@ static cudaError_t launch_prefill_mx(PrefillArgs& a, const PrefillCarve& c, cons
   int sms = 0;
   e = gemm_sms(&sms);
   if (e != cudaSuccess) return e;
-  const int g1 = c.max_tiles * (2 * I / bn1), g2 = c.max_tiles * (H / 256);
+  const int g1 = c.max_tiles * (2 * I / bn1), g2 = c.max_tiles * (H / kMxFc2BN);
   e = launch_pdl(fc1_mx_kernel<bn1>, (unsigned)(g1 < sms ? g1 : sms), kMxThreads, MxCfg<bn1>::kSmem, st, mx, mw13, a);
   if (e == cudaSuccess)
-    e = launch_pdl(fc2_mx_kernel, (unsigned)(g2 < sms ? g2 : sms), kMxThreads, MxCfg<256>::kSmem, st, mh, mw2, a);
+    e = launch_pdl(fc2_mx_kernel, (unsigned)(g2 < sms ? g2 : sms), kMxThreads, MxCfg<kMxFc2BN>::kSmem, st, mh, mw2,
+                   a);
   if (e == cudaSuccess) e = launch_pdl(cast_out_kernel, 4u * 152u, 256u, 0, st, a);
   return e;
 }
