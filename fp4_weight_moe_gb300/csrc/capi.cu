@@ -355,30 +355,27 @@ std::atomic<int> g_mid_band{0};
 constexpr int kMidBandMaxM = 3 * MOE_FP4_DECODE_MAX_M;
 
 // Does a batch of M > MOE_FP4_DECODE_MAX_M tokens run as decode-band chunks?
-// By shape: up to 3 * MOE_FP4_DECODE_MAX_M / 2 tokens when one expert's
-// weights (3IH/2 nibble bytes) are at most 8 MiB.  Chunks stream an expert
-// once per chunk that routes to it instead of once per layer, but skip the
-// routing, quantisation and cast launches; with small experts the launches
-// cost more.  Measured on GB300 (us per layer, chunks / mid band): E=512
-// H=2560 I=320 k=10: M=9 49.0 / -, 12 56.5 / 67.0, 16 81.1 / 77.0; E=288
-// H=4096 I=512 k=10: M=9 80.9 / -, 16 122.2 / 120.2; E=256 H=7168 I=2048 k=8
-// (21 MiB experts, Zipf routing): M=9 298.2 chunks against 285.0 on the
-// prefill band.
-bool mid_band_chunks(int M, int H, int I) {
-  const int mode = g_mid_band.load(std::memory_order_relaxed);
-  if (M > kMidBandMaxM) return false;
-  if (mode != 0) return mode == 2;
-  return M <= 3 * MOE_FP4_DECODE_MAX_M / 2 && 3 * (size_t)I * H / 2 <= ((size_t)8 << 20);
+// Only when forced (mode 2), for up to kMidBandMaxM tokens.  Chunks stream an
+// expert once per chunk that routes to it instead of once per layer, but skip
+// the routing, quantisation and cast launches, and keep the decode band's
+// BF16-activation numerics.  They led the mid band for up to 12 tokens with
+// small experts until the mid band's first-tile latency came down; measured
+// on GB300 since (us per layer, chunks / mid band): E=512 H=2560 I=320 k=10:
+// M=9 47.7 / 43.6, 12 55.3 / 50.8; E=288 H=4096 I=512 k=10: M=9 80.6 / 69.7,
+// 12 99.8 / 80.2; E=8 H=256 I=128 k=2: M=9 21.3 / 20.1, 12 22.5 / 20.3.
+bool mid_band_chunks(int M) {
+  return M <= kMidBandMaxM && g_mid_band.load(std::memory_order_relaxed) == 2;
 }
 
 // Does a batch past the decode band (and not in chunks) run on the mid band's
 // swapped GEMMs rather than the prefill band's?  By shape: while the experts
 // average at most kMidBandMaxRows routed rows, where the prefill tiles would
 // stage mostly padding rows of activations.  Measured on GB300 (us per layer,
-// prefill / mid band): E=512 H=2560 I=320 k=10: M=64 196.9 / 127.4, 256
-// 255.5 / 164.8, 1024 (20 rows per expert) 310.9 / 227.2; E=288 H=4096 I=512
-// k=10: M=64 266.5 / 178.5; E=128 H=4096 I=1536 k=8: M=256 281.2 / 256.9,
-// 512 (32 rows per expert) 286.2 / 292.2, 1024 306.6 / 434.2.
+// prefill / mid band): E=512 H=2560 I=320 k=10: M=64 196.9 / 116.9, 512
+// 290.9 / 172.5, 1024 (20 rows per expert) 334.1 / 220.4; E=256 H=7168
+// I=2048 k=8: M=9 255.1 / 239.3, 64 871.4 / 816.5; E=128 H=4096 I=1536 k=8:
+// M=256 263.0 / 248.3, 512 (32 rows per expert) 286.3 / 289.9, 1024 304.5 /
+// 433.6.
 constexpr int kMidBandMaxRows = 24;
 bool mid_band_swap(int M, int E, int top_k) {
   const int mode = g_mid_band.load(std::memory_order_relaxed);
@@ -425,7 +422,7 @@ int forward_any_ids(const void* x_bf16, const void* w13, const void* s13, const 
   int sms = 0;
   st = device_sms(&sms);
   if (st != MOE_FP4_OK) return st;
-  if (M > MOE_FP4_DECODE_MAX_M && !exact && mid_band_chunks(M, H, I)) {
+  if (M > MOE_FP4_DECODE_MAX_M && !exact && mid_band_chunks(M)) {
     // balanced chunks of at most MOE_FP4_DECODE_MAX_M tokens, one after
     // another on the stream (each overwrites only its own rows of out; a
     // chunk's first kernel waits for the previous chunk before it touches
@@ -574,7 +571,7 @@ int moe_fp4_forward_host(const void* x_bf16, const void* w13, const void* s13, c
   // few KB each, where a copy's fixed cost would exceed the layer's.
   // Everything else, and the prefill band's large tensors, go through the
   // staging area.
-  const bool decode = M <= MOE_FP4_DECODE_MAX_M || mid_band_chunks(M, H, I);
+  const bool decode = M <= MOE_FP4_DECODE_MAX_M || mid_band_chunks(M);
   void* xd = decode ? device_view(x_bf16) : nullptr;
   void* idd = decode ? device_view(topk_ids) : nullptr;
   void* twd = decode ? device_view(topk_weights) : nullptr;
@@ -668,7 +665,7 @@ int moe_fp4_debug_decode_gemv_fits(int M, int E, int H, int I, int top_k) {
 int moe_fp4_debug_decode_launches(int M, int E, int H, int I, int top_k) {
   if (M < 1 || check_shape(E, H, I, top_k, MOE_FP4_NVFP4) != MOE_FP4_OK) return 0;
   if (M <= MOE_FP4_DECODE_MAX_M) return decode_launches(M, E, H, I, top_k);
-  if (!mid_band_chunks(M, H, I)) return 0;
+  if (!mid_band_chunks(M)) return 0;
   const int n = (M + MOE_FP4_DECODE_MAX_M - 1) / MOE_FP4_DECODE_MAX_M;
   int total = 0;
   for (int c = 0, m0 = 0; c < n; ++c) {
@@ -681,7 +678,7 @@ int moe_fp4_debug_decode_launches(int M, int E, int H, int I, int top_k) {
 
 int moe_fp4_debug_mid_band_of(int M, int E, int H, int I, int top_k) {
   if (M <= MOE_FP4_DECODE_MAX_M || check_shape(E, H, I, top_k, MOE_FP4_NVFP4) != MOE_FP4_OK) return 0;
-  if (mid_band_chunks(M, H, I)) return 2;
+  if (mid_band_chunks(M)) return 2;
   return mid_band_swap(M, E, top_k) ? 3 : 1;
 }
 

@@ -124,7 +124,10 @@ __device__ __forceinline__ void gemm_fp4_swap_persistent(const CUtensorMap* map_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accfree + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if ((int)blockIdx.x >= n_tiles || !tile_of((int)blockIdx.x).valid) return;
+  // the first tile's fields, read before the ring's TMA traffic starts: read
+  // behind it, they held the first MMA back by 1.5 us (stage timestamps)
+  const SwapTile t0 = tile_of((int)blockIdx.x);
+  if ((int)blockIdx.x >= n_tiles || !t0.valid) return;
   const int nk = (K + Cfg::kStageK - 1) / Cfg::kStageK;
   auto groups = [&](int s) { return s + 1 < nk ? 8 : K / 64 - 8 * (nk - 1); };  // 64-K groups of stage s
   // the tile after idx for this CTA (invalid past the end); its loads are in
@@ -168,7 +171,7 @@ __device__ __forceinline__ void gemm_fp4_swap_persistent(const CUtensorMap* map_
     if (lane == 0) {
       int g = 0;
       bool ok = true;
-      SwapTile t = tile_of(blockIdx.x);
+      SwapTile t = t0;
       for (int idx = blockIdx.x; ok && idx < n_tiles; idx += gridDim.x) {
         if (!t.valid) break;
         const SwapTile tn = next_of(idx);
@@ -199,7 +202,7 @@ __device__ __forceinline__ void gemm_fp4_swap_persistent(const CUtensorMap* map_
     // MMA issuer, converged
     int g = 0, it = 0;
     bool ok = true;
-    SwapTile t = tile_of(blockIdx.x);
+    SwapTile t = t0;
     for (int idx = blockIdx.x; ok && idx < n_tiles; idx += gridDim.x, ++it) {
       if (!t.valid) break;
       const SwapTile tn = next_of(idx);
@@ -251,7 +254,7 @@ __device__ __forceinline__ void gemm_fp4_swap_persistent(const CUtensorMap* map_
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     int g = 0;
     bool ok = true;
-    SwapTile t = tile_of(blockIdx.x);
+    SwapTile t = t0;
     for (int idx = blockIdx.x; ok && idx < n_tiles; idx += gridDim.x) {
       if (!t.valid) break;
       const SwapTile tn = next_of(idx);
@@ -298,7 +301,7 @@ __device__ __forceinline__ void gemm_fp4_swap_persistent(const CUtensorMap* map_
     const int row = (warp & 3) * 32 + lane;
     int it = 0;
     for (int idx = blockIdx.x; idx < n_tiles; idx += gridDim.x, ++it) {
-      const SwapTile t = tile_of(idx);
+      const SwapTile t = it == 0 ? t0 : tile_of(idx);
       if (!t.valid) break;
       const int ab = it & 1, use = it >> 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&done[ab], use & 1, err, 4u))) break;

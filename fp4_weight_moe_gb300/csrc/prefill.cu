@@ -1053,12 +1053,11 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
         tmem_ld32(tmem_row + j * N, v);
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          if (c < nv) {  // (warp-uniform)
-            const float xc = __shfl_sync(0xffffffffu, xg, c);
-            if (n < a.I) {
-              const float u = fmaxf(__uint_as_float(v[c]) * (xc * m0), 0.f);
-              a.hbuf[(size_t)(t.b_row0 + c) * a.I + n] = __float2bfloat16_rn(u * u);
-            }
+          if (c >= nv) break;  // (warp-uniform)
+          const float xc = __shfl_sync(0xffffffffu, xg, c);
+          if (n < a.I) {
+            const float u = fmaxf(__uint_as_float(v[c]) * (xc * m0), 0.f);
+            a.hbuf[(size_t)(t.b_row0 + c) * a.I + n] = __float2bfloat16_rn(u * u);
           }
         }
       }
@@ -1087,12 +1086,16 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
         tmem_ld32(tmem_row + j * N, v);
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          if (c < nv) {  // (warp-uniform)
-            const float xc = __shfl_sync(0xffffffffu, xg, c);
-            const float h =
-                gated_act(__uint_as_float(v[c]) * (xc * mg), xch[(j * 32 + c) * 64 + l] * (xc * mu), a.act);
-            a.hbuf[(size_t)(t.b_row0 + c) * a.I + n] = __float2bfloat16_rn(h);
-          }
+          // (warp-uniform) leaving at the first padding column keeps the
+          // unrolled loop's later iterations out of the instruction stream:
+          // skipping them one by one fetched each from memory, and the first
+          // tile's epilogue took 12 us against 2 (decode_e512 M=64 126 ->
+          // 118 us per layer)
+          if (c >= nv) break;
+          const float xc = __shfl_sync(0xffffffffu, xg, c);
+          const float h =
+              gated_act(__uint_as_float(v[c]) * (xc * mg), xch[(j * 32 + c) * 64 + l] * (xc * mu), a.act);
+          a.hbuf[(size_t)(t.b_row0 + c) * a.I + n] = __float2bfloat16_rn(h);
         }
       }
       mbar_arrive(&xbar[1]);
@@ -1170,20 +1173,18 @@ __global__ void __launch_bounds__(kSwapThreads, 1)
       if (N == 16) {
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          if (c < nv) {  // (warp-uniform)
-            put(j0, c, v0[c]);
-            if (j0 + 1 < t.subs) put(j0 + 1, c, v0[16 + c]);
-            if (j0 + 2 < t.subs) put(j0 + 2, c, v1[c]);
-            if (j0 + 3 < t.subs) put(j0 + 3, c, v1[16 + c]);
-          }
+          if (c >= nv) break;  // (warp-uniform)
+          put(j0, c, v0[c]);
+          if (j0 + 1 < t.subs) put(j0 + 1, c, v0[16 + c]);
+          if (j0 + 2 < t.subs) put(j0 + 2, c, v1[c]);
+          if (j0 + 3 < t.subs) put(j0 + 3, c, v1[16 + c]);
         }
       } else {
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          if (c < nv) {  // (warp-uniform)
-            put(j0, c, v0[c]);
-            if (j0 + 1 < t.subs) put(j0 + 1, c, v1[c]);
-          }
+          if (c >= nv) break;  // (warp-uniform)
+          put(j0, c, v0[c]);
+          if (j0 + 1 < t.subs) put(j0 + 1, c, v1[c]);
         }
       }
     }

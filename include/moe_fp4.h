@@ -65,9 +65,10 @@ typedef enum {
 } moe_fp4_status;
 
 /* Largest token count handled by one pass of the decode band (HBM-bound
- * weight-streaming kernels).  Batches of up to twice this run as balanced
- * chunks of the decode band when one expert's weights are at most 8 MiB;
- * other larger batches use the prefill band (grouped block-scaled GEMM). */
+ * weight-streaming kernels).  Larger batches run the mid band (the grouped
+ * block-scaled GEMMs with the weights on the MMA's 128-row side) while the
+ * experts average at most 24 routed rows, else the prefill band (the
+ * grouped block-scaled GEMMs with the routed rows on that side). */
 #define MOE_FP4_DECODE_MAX_M 8
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -154,15 +155,14 @@ MOE_FP4_API int moe_fp4_release_workspace(void);
  *   out_bf16     [M][H] bf16, fully overwritten (tokens with no valid slot
  *                get +0.0); must not overlap any input.
  * M = 0 is a no-op.  Inputs are never written.  Decode-band results (M <=
- * 8, and 9 <= M <= 16 with experts of at most 8 MiB of weights, which run
- * as chunks of at most 8 tokens on the decode kernels) are bitwise
- * deterministic; the prefill band sums routed rows into an FP32 token
- * accumulator with atomic adds, so its low-order bits may vary run to run.
+ * 8) are bitwise deterministic; the mid and prefill bands sum routed rows
+ * into an FP32 token accumulator with atomic adds, so their low-order bits
+ * may vary run to run.
  *
- * Prefill band (M > 8, except the chunked batches above): E <= 4096 (else
- * MOE_FP4_EUNSUPPORTED).  Activations are quantised to NVFP4 per row (x per
- * token, h = SiLU(gate)*up per routed row after BF16 staging) so both GEMMs
- * run on the FP4 tensor cores.
+ * Mid and prefill bands (M > 8): E <= 4096 (else MOE_FP4_EUNSUPPORTED).
+ * Activations are quantised to NVFP4 per row (x per token, h =
+ * SiLU(gate)*up per routed row after BF16 staging) so both GEMMs run on the
+ * FP4 tensor cores; the two bands compute the same products.
  */
 MOE_FP4_API int moe_fp4_forward(const void *x_bf16, const void *w13, const void *s13, const void *w2, const void *s2,
                     const int32_t *topk_ids, const float *topk_weights, void *out_bf16, int M, int E, int H, int I,
@@ -296,8 +296,8 @@ MOE_FP4_API int moe_fp4_forward_ex(const void *x_bf16, const void *w13, const vo
                                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * The prefill band's activation precision (M > MOE_FP4_DECODE_MAX_M, except
- * the chunked decode batches):
+ * The activation precision of batches past the decode band (M >
+ * MOE_FP4_DECODE_MAX_M):
  *   MOE_FP4_PREFILL_NVFP4  (default of every other entry point) x per token
  *                          and h per routed row quantised to NVFP4, both
  *                          GEMMs on the FP4 tensor cores (kind::mxf4nvf4)
@@ -324,9 +324,9 @@ MOE_FP4_API int moe_fp4_forward_ex(const void *x_bf16, const void *w13, const vo
  *                          largest).  Either way the FP32 sums are those of
  *                          the MXFP8 x MXFP4 products.
  * Batches past the decode band always take the prefill band in the BF16 and
- * W4A8-MX modes (no decode-kernel chunks); batches of at most
- * MOE_FP4_DECODE_MAX_M tokens run the decode band in every mode (BF16
- * activations, as the pages' w4a8_mx tiny-decode kernel keeps them).
+ * W4A8-MX modes (neither the mid band nor decode-kernel chunks); batches of
+ * at most MOE_FP4_DECODE_MAX_M tokens run the decode band in every mode
+ * (BF16 activations, as the pages' w4a8_mx tiny-decode kernel keeps them).
  * The pages' decode keeps BF16 activations for accuracy (b12x PR #22, "rp-
  * native tiny-decode kernel for w4a8_mx (M=1)", section Measured: cosine
  * 0.999980 with BF16 activations against 0.9990 with MXFP8 ones).
@@ -463,9 +463,7 @@ MOE_FP4_API int moe_fp4_debug_set_decode_family(int family, int *previous);
  * Test support: the kernels of batches past the decode band
  * (M > MOE_FP4_DECODE_MAX_M) under MOE_FP4_PREFILL_NVFP4 for every later
  * call in the process.
- *   mode 0  by shape (default): up to 3 * MOE_FP4_DECODE_MAX_M / 2 tokens
- *           the chunks when one expert's weights (3IH/2 nibble bytes) are at
- *           most 8 MiB; otherwise the mid band's GEMMs while the experts
+ *   mode 0  by shape (default): the mid band's GEMMs while the experts
  *           average at most 24 routed rows (M * top_k <= 24 E), else the
  *           prefill band's
  *   mode 1  the prefill band's GEMMs (routed rows on the MMA's 128-row
@@ -495,8 +493,8 @@ MOE_FP4_API int moe_fp4_debug_decode_plan(int M, int E, int H, int I, int top_k,
 /* Kernel launches one decode-band layer of this shape makes under the
  * current family and mid-band settings (2 streaming GEMV; 1 tcgen05 single
  * launch; 3, or 4 from M = 2, tcgen05 chain; the sum over the chunks of a
- * chunked batch); 0 for shapes that take the prefill band or invalid
- * arguments. */
+ * batch that mode 2 of moe_fp4_debug_set_mid_band runs in chunks); 0 for
+ * shapes that take the mid or prefill band, or invalid arguments. */
 MOE_FP4_API int moe_fp4_debug_decode_launches(int M, int E, int H, int I, int top_k);
 /* The kernels the current moe_fp4_debug_set_mid_band setting picks for a
  * batch past the decode band under MOE_FP4_PREFILL_NVFP4 (1 the prefill

@@ -136,9 +136,9 @@ def test_forward_ex_i64_argument_errors(lib):
 def test_band_policy_by_shape(lib):
     """Which kernels a batch takes (host logic only): the decode band up to 8
     tokens (streaming GEMV for one token with few routed bytes, else tcgen05
-    with 3 launches, 4 from two tokens), 9-16 tokens with experts of at most
-    8 MiB as balanced chunks of the decode kernels, everything else the
-    prefill band (0 decode launches); the test knobs force either path."""
+    with 3 launches, 4 from two tokens), everything else the mid or prefill
+    band (0 decode launches); the test knobs force the decode kernels in
+    balanced chunks of at most 8 tokens for up to 24 tokens, or the GEMV."""
     c = _capi
     e512 = (512, 2560, 320, 10)     # 1.38 MB experts
     e256 = (256, 7168, 2048, 8)     # 22 MB experts
@@ -160,8 +160,13 @@ def test_band_policy_by_shape(lib):
     try:
         assert c.moe_fp4_debug_decode_family_of(1, *e512) == 2
         assert [c.moe_fp4_debug_decode_launches(M, *e512) for M in (1, 2, 8)] == [3, 4, 4]
-        assert [c.moe_fp4_debug_decode_launches(M, *e512) for M in (9, 12, 13, 16, 24)] == [8, 8, 0, 0, 0]
+        assert [c.moe_fp4_debug_decode_launches(M, *e512) for M in (9, 12, 13, 16, 24)] == [0, 0, 0, 0, 0]
         assert [c.moe_fp4_debug_decode_launches(M, *e256) for M in (8, 9, 16)] == [4, 0, 0]
+        prev = c.moe_fp4_debug_set_mid_band(2)
+        try:
+            assert [c.moe_fp4_debug_decode_launches(M, *e512) for M in (9, 12, 13, 24, 25)] == [8, 8, 8, 12, 0]
+        finally:
+            c.moe_fp4_debug_set_mid_band(prev)
     finally:
         c.moe_fp4_debug_set_decode_family(prev_family)
     assert c.moe_fp4_debug_decode_family_of(9, *e512) == 0
@@ -179,15 +184,15 @@ def test_band_policy_by_shape(lib):
 
 
 def test_mid_band_plan_by_shape(lib):
-    """Past the decode band: chunks for up to 12 tokens of small experts, the
-    mid band's GEMMs while the experts average at most 24 routed rows, the
-    prefill band's beyond; the switch overrides the rule."""
+    """Past the decode band: the mid band's GEMMs while the experts average
+    at most 24 routed rows, the prefill band's beyond; the switch overrides
+    the rule (decode-kernel chunks only when forced)."""
     c = _capi
     e512, e288, e256, e128 = (512, 2560, 320, 10), (288, 4096, 512, 10), (256, 7168, 2048, 8), (128, 4096, 1536, 8)
-    assert [c.moe_fp4_debug_mid_band_of(M, *e512) for M in (1, 8, 9, 12, 13, 1228, 1229)] == [0, 0, 2, 2, 3, 3, 1]
+    assert [c.moe_fp4_debug_mid_band_of(M, *e512) for M in (1, 8, 9, 12, 13, 1228, 1229)] == [0, 0, 3, 3, 3, 3, 1]
     assert [c.moe_fp4_debug_mid_band_of(M, *e256) for M in (9, 768, 769)] == [3, 3, 1]
     assert [c.moe_fp4_debug_mid_band_of(M, *e128) for M in (9, 384, 385, 4096)] == [3, 3, 1, 1]
-    assert c.moe_fp4_debug_mid_band_of(12, *e288) == 2
+    assert [c.moe_fp4_debug_mid_band_of(M, *e288) for M in (9, 12)] == [3, 3]
     assert c.moe_fp4_debug_mid_band_of(9, 512, 2560, 320, 0) == 0  # invalid top_k
     prev = c.moe_fp4_debug_set_mid_band(1)
     try:

@@ -2,9 +2,9 @@
 
 The largest decode batch with the largest top_k, one expert taking every
 route (all of a layer's tokens in one expert: the GEMV family's 8-token path),
-the smallest H and I the boundary accepts, the band boundaries (M = 8, the
-chunked M = 9 and 16, the first prefill batch M = 17), and routings whose
-slots all repeat one expert.  Each decode case runs on both kernel families.
+the smallest H and I the boundary accepts, the band boundary (M = 8, and
+the first batches past it on the mid band), and routings whose slots all
+repeat one expert.  Each decode case runs on both kernel families.
 """
 import pytest
 import torch
@@ -63,12 +63,13 @@ def test_decode_edges(case, family):
 
 @pytest.mark.parametrize("M", [8, 9, 12, 13, 17])
 def test_band_boundary(M):
-    """The last decode batch, the chunked batches past it (9..12 tokens: this
-    geometry's experts are small) and the first batches on the mid band's
-    GEMMs (13 on)."""
+    """The last decode batch and the first batches past it, on the mid band's
+    GEMMs (9 on)."""
+    from fp4_weight_moe_gb300 import _capi
     wl = gen.make_workload("decode_e512", device="cuda", E=32, M=M)
+    assert _capi.moe_fp4_debug_mid_band_of(wl.M, wl.E, wl.H, wl.I, wl.top_k) == (0 if M <= 8 else 3)
     got = _run(wl)
-    if M <= 12:
+    if M <= 8:
         want = oracle_layer(wl)
     else:  # the mid band quantises the activations; the oracle mirrors it
         import oracle

@@ -2,7 +2,8 @@
 
 * Outlier-heavy activations: per 256-wide K stage a few channels at 2^8 ..
   2^12 times the RMS and whole 16-element blocks near 2^-20 times it, on
-  every decode plan and on the prefill band (against its mirrored oracle).
+  every decode plan and on the prefill and mid bands (against their mirrored
+  oracle).
   These exercise the tcgen05 kernels' four-term activation expansion and the
   streaming GEMV's power-of-two FP16 rescaling per stage.
 * MXFP4 block scales spanning more than 2^17 inside one projection, with an
@@ -42,14 +43,22 @@ def fm():
 
 
 class plan:
-    def __init__(self, family):
+    """A decode family, and optionally a past-decode mode (2: the decode
+    kernels in chunks), for the calls inside."""
+
+    def __init__(self, family, past=None):
         self.family = family
+        self.past = past
 
     def __enter__(self):
         self.prev = fm()._capi.moe_fp4_debug_set_decode_family(self.family)
+        if self.past is not None:
+            self.prev_past = fm()._capi.moe_fp4_debug_set_mid_band(self.past)
 
     def __exit__(self, *exc):
         fm()._capi.moe_fp4_debug_set_decode_family(self.prev)
+        if self.past is not None:
+            fm()._capi.moe_fp4_debug_set_mid_band(self.prev_past)
 
 
 def outlier_activations(M, H, seed):
@@ -95,13 +104,15 @@ def test_outlier_activations_decode(name, ov, pname):
     assert_layer_close(got, oracle_layer(wl), f"{name} {ov} outliers, plan {pname}")
 
 
-def test_outlier_activations_prefill():
+@pytest.mark.parametrize("band", [1, 3])  # the prefill band's GEMMs, the mid band's
+def test_outlier_activations_prefill(band):
     wl = gen.make_workload("decode_e512", device="cuda", E=12, M=40, fmt=gen.NVFP4)
     wl.x = outlier_activations(wl.M, wl.H, seed=3).cuda()
-    got = _run(wl)
+    with plan(0, band):
+        got = _run(wl)
     want = oracle.forward_prefill(wl.x, wl.weights, wl.topk_ids, wl.topk_weights, wl.E, wl.H, wl.I, wl.top_k,
                                   fmt=wl.fmt)[0]
-    assert_layer_close(got, want, "prefill band, outlier activations")
+    assert_layer_close(got, want, f"band {band}, outlier activations")
 
 
 def _mx_weights_with_wide_scales(E, H, I, seed):
@@ -174,18 +185,20 @@ def _poisoned_workspace(M, E, H, I, k, fmt):
 def test_nan_poisoned_workspace(name, ov, pname):
     wl = gen.make_workload(name, device="cuda", **ov)
     ws = _poisoned_workspace(wl.M, wl.E, wl.H, wl.I, wl.top_k, wl.fmt)
-    with plan(PLANS[pname]):
+    with plan(PLANS[pname], 2 if wl.M > 8 else None):  # past 8 tokens: the decode kernels in chunks
         got = _run(wl, ws=ws)
     assert_layer_close(got, oracle_layer(wl), f"{name} {ov} poisoned workspace, plan {pname}")
 
 
-def test_nan_poisoned_workspace_prefill():
+@pytest.mark.parametrize("band", [1, 3])  # the prefill band's GEMMs, the mid band's
+def test_nan_poisoned_workspace_prefill(band):
     wl = gen.make_workload("decode_e512", device="cuda", E=12, M=40)
     ws = _poisoned_workspace(wl.M, wl.E, wl.H, wl.I, wl.top_k, wl.fmt)
-    got = _run(wl, ws=ws)
+    with plan(0, band):
+        got = _run(wl, ws=ws)
     want = oracle.forward_prefill(wl.x, wl.weights, wl.topk_ids, wl.topk_weights, wl.E, wl.H, wl.I, wl.top_k,
                                   fmt=wl.fmt)[0]
-    assert_layer_close(got, want, "prefill band, poisoned workspace")
+    assert_layer_close(got, want, f"band {band}, poisoned workspace")
 
 
 def _invalid_with_bad_weights(wl, seed):
@@ -220,13 +233,15 @@ def test_invalid_slots_with_nan_and_inf_weights(name, ov, pname):
     assert_layer_close(got, want, f"{name} {ov} NaN/inf weights on invalid slots, plan {pname}")
 
 
-def test_invalid_slots_with_nan_and_inf_weights_prefill():
+@pytest.mark.parametrize("band", [1, 3])  # the prefill band's GEMMs, the mid band's
+def test_invalid_slots_with_nan_and_inf_weights_prefill(band):
     wl = gen.make_workload("decode_e512", device="cuda", E=12, M=40)
     tw_clean = _invalid_with_bad_weights(wl, seed=5)
-    got = _run(wl)
+    with plan(0, band):
+        got = _run(wl)
     want = oracle.forward_prefill(wl.x, wl.weights, wl.topk_ids.cpu(), tw_clean, wl.E, wl.H, wl.I, wl.top_k,
                                   fmt=wl.fmt)[0]
-    assert_layer_close(got, want, "prefill band, NaN/inf weights on invalid slots")
+    assert_layer_close(got, want, f"band {band}, NaN/inf weights on invalid slots")
 
 
 # ---------------------------------------------------------------- the 16-bit and FP8 prefill modes

@@ -66,7 +66,7 @@ def test_host_entry_shared_workspace_across_batches():
         outh = torch.empty((M, H), dtype=torch.bfloat16).pin_memory()
         m.forward_host(_host(x, True), pw, _host(ids, True), _host(tw, True), outh, hws)
         torch.cuda.current_stream().synchronize()
-        if m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) > 0:  # decode kernels (M = 12: in chunks)
+        if m._capi.moe_fp4_debug_decode_launches(M, E, H, I, k) > 0:  # decode kernels
             assert torch.equal(outh.view(torch.int16), ref.cpu().view(torch.int16)), M
         else:
             assert_layer_close(outh, ref.float().cpu().double().numpy(), f"prefill M={M} host vs device")

@@ -1,9 +1,9 @@
 """Batches past the decode band (M > MOE_FP4_DECODE_MAX_M).
 
-They run on the prefill band's GEMMs, on the mid band's swapped GEMMs
-(weights on the MMA's 128-row side, an expert's routed rows on N), or, just
-past the band, on the decode-band kernels over balanced chunks of at most
-MOE_FP4_DECODE_MAX_M tokens.  The chunked path keeps the decode band's
+They run on the prefill band's GEMMs or on the mid band's swapped GEMMs
+(weights on the MMA's 128-row side, an expert's routed rows on N), and on
+request (a test switch) on the decode-band kernels over balanced chunks of
+at most MOE_FP4_DECODE_MAX_M tokens.  The chunked path keeps the decode band's
 numerics (BF16 activations, no activation quantisation), so it is held to
 the unquantised FP64 oracle, and it must be bitwise the concatenation of the
 chunks run as separate decode calls.  The prefill and mid bands quantise the
@@ -101,12 +101,13 @@ def test_mid_band_swapped_gemms_parity(name, ov):
     assert_layer_close(got64, want, f"{name} {ov} mid band, int64 ids")
 
 
-def test_mid_band_by_shape_matches_its_plan():
-    """decode_e512 at 32 tokens runs the mid band's GEMMs by shape."""
+@pytest.mark.parametrize("M", [9, 32])
+def test_mid_band_by_shape_matches_its_plan(M):
+    """decode_e512 past 8 tokens runs the mid band's GEMMs by shape."""
     from fp4_weight_moe_gb300 import _capi
-    wl = gen.make_workload("decode_e512", device="cuda", M=32)
+    wl = gen.make_workload("decode_e512", device="cuda", M=M)
     assert _capi.moe_fp4_debug_mid_band_of(wl.M, wl.E, wl.H, wl.I, wl.top_k) == MID
     got = _run(wl, 0)
     want, _, _, _ = oracle.forward_prefill(wl.x, wl.weights, wl.topk_ids, wl.topk_weights, wl.E, wl.H, wl.I,
                                            wl.top_k, fmt=wl.fmt)
-    assert_layer_close(got, want, "decode_e512 M=32 by shape")
+    assert_layer_close(got, want, f"decode_e512 M={M} by shape")
