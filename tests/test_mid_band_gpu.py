@@ -88,6 +88,11 @@ def test_int64_ids_through_chunks():
                                      # the smallest K of both GEMMs (H = 256: one stage without its second
                                      # box; I = 64: one scale group)
                                      ("tiny_decode", dict(M=40, E=3, H=256, I=64, top_k=2)),
+                                     # FC2's K of 256 + 128 and 256 + 64 (one stage, its second box ragged),
+                                     # and 512 + 64 (a second stage of one scale group)
+                                     ("tiny_decode", dict(M=90, E=6, H=512, I=384, top_k=3)),
+                                     ("decode_e288_m4", dict(E=20, H=768, I=320, M=50, fmt=gen.MXFP4)),
+                                     ("tiny_decode", dict(M=70, E=5, H=256, I=576, top_k=2)),
                                      # every expert on every token, past the one-kernel routing's 8192
                                      # entries (the three-kernel routing with 32-row tiles)
                                      ("tiny_decode", dict(M=600, E=16, H=512, I=192, top_k=16))])
