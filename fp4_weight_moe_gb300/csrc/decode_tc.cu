@@ -443,8 +443,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const __grid_c
       row0 = e * H + unit * 128;
       sfa = a.s2 + (((uint64_t)e * (H / 128) + unit) * KG + 4 * (uint64_t)st) * kChunkBytes;
     }
-    tma_load_2d(slotp, &map_w, st * 128, row0, &S.fullA[sl]);
-    bulk_load(slotp + kSlotA + kSlotB, sfa, (uint32_t)ng * kChunkBytes, &S.fullA[sl]);
+    // the weights stream through L2 once per layer: evict-first
+    const uint64_t wpol = l2_evict_first_policy();
+    tma_load_2d_hint(slotp, &map_w, st * 128, row0, &S.fullA[sl], wpol);
+    bulk_load_hint(slotp + kSlotA + kSlotB, sfa, (uint32_t)ng * kChunkBytes, &S.fullA[sl], wpol);
   };
   // FC1: bulk copy of item i's activation terms (B tile, scales, G) from the
   // pre-pass's image into the ring slot
@@ -1013,7 +1015,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   };
   const uint64_t KG1 = (uint64_t)(H / 64), KG2 = (uint64_t)(I / 64);
   if (threadIdx.x == 0) {
-    // every weight tile of the CTA, FC1's first
+    // every weight tile of the CTA, FC1's first (streaming once per layer:
+    // evict-first in L2)
+    const uint64_t wpol = l2_evict_first_policy();
     for (int i = 0; i < n_items; ++i) {
       uint8_t* slotp = ring + i * Cfg::kSlot;
       const int ng = item_groups(i);
@@ -1021,13 +1025,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (i < n1) {
         const int st = k0 + i;
         const uint8_t* sfa = a.s13 + (((uint64_t)e1 * tiles1 + tile1) * KG1 + 4 * (uint64_t)st) * kChunkBytes;
-        tma_load_2d(slotp, &map13, st * 128, e1 * 2 * I + tile1 * 128, &S.fullA[i]);
-        bulk_load(slotp + Cfg::kSFA, sfa, (uint32_t)ng * kChunkBytes, &S.fullA[i]);
+        tma_load_2d_hint(slotp, &map13, st * 128, e1 * 2 * I + tile1 * 128, &S.fullA[i], wpol);
+        bulk_load_hint(slotp + Cfg::kSFA, sfa, (uint32_t)ng * kChunkBytes, &S.fullA[i], wpol);
       } else {
         const int st = item_s2(i), e = S.ids[S.own[item_o(i)]];
         const uint8_t* sfa = a.s2 + (((uint64_t)e * tiles2 + t2) * KG2 + 4 * (uint64_t)st) * kChunkBytes;
-        tma_load_2d(slotp, &map2, st * 128, e * H + t2 * 128, &S.fullA[i]);
-        bulk_load(slotp + Cfg::kSFA, sfa, (uint32_t)ng * kChunkBytes, &S.fullA[i]);
+        tma_load_2d_hint(slotp, &map2, st * 128, e * H + t2 * 128, &S.fullA[i], wpol);
+        bulk_load_hint(slotp + Cfg::kSFA, sfa, (uint32_t)ng * kChunkBytes, &S.fullA[i], wpol);
       }
     }
     // the partial rows this CTA reduces: FC1 from the s1 CTAs of its

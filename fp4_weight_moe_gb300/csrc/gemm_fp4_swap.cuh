@@ -169,6 +169,8 @@ __device__ __forceinline__ void gemm_fp4_swap_persistent(const CUtensorMap* map_
   if (warp == 0) {
     // producer
     if (lane == 0) {
+      // the weights stream through L2 once per routing tile
+      const uint64_t wpol = l2_evict_first_policy();
       int g = 0;
       bool ok = true;
       SwapTile t = t0;
@@ -187,11 +189,12 @@ __device__ __forceinline__ void gemm_fp4_swap_persistent(const CUtensorMap* map_
             const uint32_t sfb = (uint32_t)ng * kChunkBytes, boxes = ng > 4 ? 2u : 1u;
             mbar_arrive_expect_tx(&full[slot], boxes * (Cfg::kBoxA + (uint32_t)t.n_rows * 128) + 2 * sfb);
             for (uint32_t h = 0; h < boxes; ++h) {
-              tma_load_2d(stage_a(slot) + h * Cfg::kBoxA, map_a, s * 256 + (int)h * 128, t.a_row0 + 128 * j,
-                          &full[slot]);
+              tma_load_2d_hint(stage_a(slot) + h * Cfg::kBoxA, map_a, s * 256 + (int)h * 128, t.a_row0 + 128 * j,
+                               &full[slot], wpol);
               tma_load_2d(stage_b(slot) + h * Cfg::kBoxB, mb, s * 256 + (int)h * 128, t.b_row0, &full[slot]);
             }
-            bulk_load(stage_sfa(slot), t.a_sf + j * t.a_sf_step + (size_t)(8 * s) * kChunkBytes, sfb, &full[slot]);
+            bulk_load_hint(stage_sfa(slot), t.a_sf + j * t.a_sf_step + (size_t)(8 * s) * kChunkBytes, sfb, &full[slot],
+                           wpol);
             bulk_load(stage_sfb(slot), t.b_sf + (size_t)(8 * s) * kChunkBytes, sfb, &full[slot]);
           }
         }
