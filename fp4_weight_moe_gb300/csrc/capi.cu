@@ -371,12 +371,13 @@ bool mid_band_chunks(int M) {
 // swapped GEMMs rather than the prefill band's?  By shape: while the experts
 // average at most kMidBandMaxRows routed rows, where the prefill tiles would
 // stage mostly padding rows of activations.  Measured on GB300 (us per layer,
-// prefill / mid band): E=512 H=2560 I=320 k=10: M=64 196.9 / 116.9, 512
-// 290.9 / 172.5, 1024 (20 rows per expert) 334.1 / 220.4; E=256 H=7168
-// I=2048 k=8: M=9 255.1 / 239.3, 64 871.4 / 816.5; E=128 H=4096 I=1536 k=8:
-// M=256 263.0 / 248.3, 512 (32 rows per expert) 286.3 / 289.9, 1024 304.5 /
-// 433.6.
-constexpr int kMidBandMaxRows = 24;
+// prefill / mid band, routed rows per expert in brackets): E=512 H=2560 I=320
+// k=10: M=64 (1.25) 196.9 / 107.7, 1024 (20) 334.1 / 210.8, 1536 (30) 352.9 /
+// 290.3, 1792 (35) 351.8 / 338.9, 2048 (40) 357.0 / 377.5; E=288 H=4096 I=512
+// k=10: M=768 (26.7) 344.8 / 264.0, 1024 (35.6) 347.3 / 357.0; E=256 H=7168
+// I=2048 k=8: M=832 (26) 1091.1 / 1065.7, 1024 (32) 1108.9 / 1241.5; E=128
+// H=4096 I=1536 k=8: M=416 (26) 283.1 / 261.5, 512 (32) 287.1 / 301.2.
+constexpr int kMidBandMaxRows = 28;
 bool mid_band_swap(int M, int E, int top_k) {
   const int mode = g_mid_band.load(std::memory_order_relaxed);
   if (mode == 1 || mode == 3) return mode == 3;
