@@ -377,11 +377,16 @@ bool mid_band_chunks(int M) {
 // k=10: M=768 (26.7) 344.8 / 264.0, 1024 (35.6) 347.3 / 357.0; E=256 H=7168
 // I=2048 k=8: M=832 (26) 1091.1 / 1065.7, 1024 (32) 1108.9 / 1241.5; E=128
 // H=4096 I=1536 k=8: M=416 (26) 283.1 / 261.5, 512 (32) 287.1 / 301.2.
+// With I <= 384 the prefill band's FC2 has one or two K stages per tile and
+// the mid band stays ahead further (the E=512 rows above): up to
+// kMidBandMaxRowsShortI rows there.
 constexpr int kMidBandMaxRows = 28;
-bool mid_band_swap(int M, int E, int top_k) {
+constexpr int kMidBandMaxRowsShortI = 36;
+bool mid_band_swap(int M, int E, int I, int top_k) {
   const int mode = g_mid_band.load(std::memory_order_relaxed);
   if (mode == 1 || mode == 3) return mode == 3;
-  return (int64_t)M * top_k <= (int64_t)kMidBandMaxRows * E;  // (mode 2: past the chunks' reach)
+  const int rows = I <= 384 ? kMidBandMaxRowsShortI : kMidBandMaxRows;
+  return (int64_t)M * top_k <= (int64_t)rows * E;  // (mode 2: past the chunks' reach)
 }
 
 // moe_fp4_forward_ex and moe_fp4_forward_ex_i64: topk_ids int32 (ids64 = 0)
@@ -462,7 +467,7 @@ int forward_any_ids(const void* x_bf16, const void* w13, const void* s13, const 
   if (need >= kMaxWorkspace || workspace_bytes < need) return MOE_FP4_EWORKSPACE;
   int cu = 0;
   cudaError_t e = launch_prefill(x_bf16, w13, s13, w2, s2, ids, ids64, topk_weights, out_bf16, M, E, H, I, top_k,
-                                 ap, prefill_mode, !exact && mid_band_swap(M, E, top_k), workspace,
+                                 ap, prefill_mode, !exact && mid_band_swap(M, E, I, top_k), workspace,
                                  static_cast<cudaStream_t>(stream), &cu);
   return e == cudaSuccess ? MOE_FP4_OK : fail_cuda(e);
 }
@@ -680,7 +685,7 @@ int moe_fp4_debug_decode_launches(int M, int E, int H, int I, int top_k) {
 int moe_fp4_debug_mid_band_of(int M, int E, int H, int I, int top_k) {
   if (M <= MOE_FP4_DECODE_MAX_M || check_shape(E, H, I, top_k, MOE_FP4_NVFP4) != MOE_FP4_OK) return 0;
   if (mid_band_chunks(M)) return 2;
-  return mid_band_swap(M, E, top_k) ? 3 : 1;
+  return mid_band_swap(M, E, I, top_k) ? 3 : 1;
 }
 
 int moe_fp4_debug_dequant(const void* w, const void* s, int which, int expert, int E, int H, int I, int fmt,

@@ -67,8 +67,9 @@ typedef enum {
 /* Largest token count handled by one pass of the decode band (HBM-bound
  * weight-streaming kernels).  Larger batches run the mid band (the grouped
  * block-scaled GEMMs with the weights on the MMA's 128-row side) while the
- * experts average at most 28 routed rows, else the prefill band (the
- * grouped block-scaled GEMMs with the routed rows on that side). */
+ * experts average at most 28 routed rows (36 with I <= 384), else the
+ * prefill band (the grouped block-scaled GEMMs with the routed rows on that
+ * side). */
 #define MOE_FP4_DECODE_MAX_M 8
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -464,7 +465,8 @@ MOE_FP4_API int moe_fp4_debug_set_decode_family(int family, int *previous);
  * (M > MOE_FP4_DECODE_MAX_M) under MOE_FP4_PREFILL_NVFP4 for every later
  * call in the process.
  *   mode 0  by shape (default): the mid band's GEMMs while the experts
- *           average at most 28 routed rows (M * top_k <= 28 E), else the
+ *           average at most 28 routed rows (M * top_k <= 28 E; 36 rows with
+ *           I <= 384, where the prefill band's FC2 has little K), else the
  *           prefill band's
  *   mode 1  the prefill band's GEMMs (routed rows on the MMA's 128-row
  *           side)

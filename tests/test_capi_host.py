@@ -185,11 +185,12 @@ def test_band_policy_by_shape(lib):
 
 def test_mid_band_plan_by_shape(lib):
     """Past the decode band: the mid band's GEMMs while the experts average
-    at most 28 routed rows, the prefill band's beyond; the switch overrides
+    at most 28 routed rows (36 with I <= 384), the prefill band's beyond; the switch overrides
     the rule (decode-kernel chunks only when forced)."""
     c = _capi
     e512, e288, e256, e128 = (512, 2560, 320, 10), (288, 4096, 512, 10), (256, 7168, 2048, 8), (128, 4096, 1536, 8)
-    assert [c.moe_fp4_debug_mid_band_of(M, *e512) for M in (1, 8, 9, 12, 13, 1433, 1434)] == [0, 0, 3, 3, 3, 3, 1]
+    assert [c.moe_fp4_debug_mid_band_of(M, *e512) for M in (1, 8, 9, 12, 13, 1843, 1844)] == [0, 0, 3, 3, 3, 3, 1]
+    assert [c.moe_fp4_debug_mid_band_of(M, *e288) for M in (806, 807)] == [3, 1]  # I = 512: 28 rows
     assert [c.moe_fp4_debug_mid_band_of(M, *e256) for M in (9, 896, 897)] == [3, 3, 1]
     assert [c.moe_fp4_debug_mid_band_of(M, *e128) for M in (9, 448, 449, 4096)] == [3, 3, 1, 1]
     assert [c.moe_fp4_debug_mid_band_of(M, *e288) for M in (9, 12)] == [3, 3]
